@@ -1,0 +1,226 @@
+"""Whole-plan statements built on ``rules`` (TEST INFRASTRUCTURE ONLY).
+
+* ``llama_step_plan`` -- the tile expansion of one decode step of a dense
+  Llama-style decoder into per-op grids and tensor edges, run through the MPK
+  gcd/lcm event rule, then queued.  The op set is the lecture's seven fused
+  instruction types ("CMU 15-779 Lecture 7 notes", section 5.1): RMSNorm+QKV,
+  attention (+ reduction), O-projection+residual, RMSNorm+gate/up+SiLU,
+  down+residual with its intermediate split into K chunks that each have a
+  counter, RMSNorm+LM head.  An embedding-gather task starts the step.
+* ``megartp_glm_plan`` -- the MegaRTP article's GLM pre-attention plan
+  (section 4, TaskGraph and KernelPlan): fixed per-op tile counts and the
+  publications / waits the article lists.
+
+The tile-expansion reading (which tensor dimension each grid axis cuts, the
+cost model used to balance queues) is this project's; both this file and the
+C++ planner state it independently and must agree bit for bit.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Dict, List, Optional, Sequence, Tuple
+
+from . import rules
+from .rules import Edge, Op
+
+
+@dataclass
+class LlamaShape:
+    L: int
+    H: int
+    Hq: int
+    Hkv: int
+    D: int
+    F: int
+    V: int
+
+
+@dataclass
+class Knobs:
+    rows_qkv: int
+    rows_o: int
+    rows_up: int      # gate rows (= up rows) per MLP-up tile
+    rows_down: int
+    kchunk_down: int  # K extent of one down-projection tile
+    rows_lm: int
+    attn_split: int   # cache positions per attention task
+
+
+def _ceil(a, b):
+    return -(-a // b)
+
+
+@dataclass
+class PlannedTask:
+    op: str
+    kind: str
+    layer: int
+    bid: Tuple[int, int, int]
+    cost: int
+    waits: List[Tuple[int, int, int]]   # (event, threshold, epoch offset)
+    signals: List[Tuple[int, int]]      # (event, increment)
+
+
+@dataclass
+class Plan:
+    tasks: List[PlannedTask]
+    thresholds: List[int]
+    queues: List[List[int]]   # task ids, -1 = NoOp
+    lmax: int
+    graph: rules.TaskGraph
+
+
+def llama_step_ops(shape: LlamaShape, k: Knobs, B: int, seq0: Sequence[int], max_steps: int):
+    G = shape.Hq // shape.Hkv
+    rows_group = (G + 2) * shape.D
+    assert rows_group % k.rows_qkv == 0 and shape.F % k.rows_up == 0 and shape.F % k.kchunk_down == 0
+    nsplit = [_ceil(seq0[b] + max_steps, k.attn_split) for b in range(B)]
+    ns_max = max(nsplit)
+
+    def attn_rows(bid):
+        g, b, s = bid
+        last_pos = seq0[b] + max_steps - 1          # cached rows at the last step
+        return max(0, min(k.attn_split, last_pos - s * k.attn_split))
+
+    def rows_cost(n_rows, rows, kdim, mult=1):
+        def f(bid):
+            r0 = bid[0] * rows
+            return mult * min(rows, n_rows - r0) * kdim * 2
+        return f
+
+    ops: List[Op] = [Op("embed", (1, 1, 1), cost=lambda bid: B * shape.H * 2)]
+    kinds = {"embed": ("embed", -1)}
+    edges: List[Edge] = []
+    prev = "embed"
+    for l in range(shape.L):
+        qkv, attn, o, up, down = (f"{n}{l}" for n in ("qkv", "attn", "o", "up", "down"))
+        ops.append(Op(qkv, (shape.Hkv, rows_group // k.rows_qkv, 1),
+                      cost=lambda bid: k.rows_qkv * shape.H * 2))
+        ops.append(Op(attn, (shape.Hkv, B, ns_max), exists=lambda bid: bid[2] < nsplit[bid[1]],
+                      cost=lambda bid: 2 * shape.D * 2 * attn_rows(bid)))
+        ops.append(Op(o, (_ceil(shape.H, k.rows_o), 1, 1), cost=rows_cost(shape.H, k.rows_o, shape.Hq * shape.D)))
+        ops.append(Op(up, (shape.F // k.rows_up, 1, 1), cost=lambda bid: 2 * k.rows_up * shape.H * 2))
+        ops.append(Op(down, (_ceil(shape.H, k.rows_down), shape.F // k.kchunk_down, 1),
+                      cost=rows_cost(shape.H, k.rows_down, k.kchunk_down)))
+        for n, kind in ((qkv, "qkv"), (attn, "attn"), (o, "o"), (up, "up"), (down, "down")):
+            kinds[n] = (kind, l)
+        # h [B, H] -> qkv reads all of it
+        edges.append(Edge(prev, qkv, (1, -1, -1), (-1, -1, -1)))
+        # qkv [B, Hkv, rows_group]: producer cuts group and rows, consumer cuts batch and group
+        edges.append(Edge(qkv, attn, (1, 2, -1), (1, 0, -1)))
+        # attn_out [B, Hkv, G*D]: O reads all of it; the split axis is a reduction
+        edges.append(Edge(attn, o, (1, 0, -1), (-1, -1, -1)))
+        # h after O -> MLP-up reads all of it
+        edges.append(Edge(o, up, (1, -1, -1), (-1, -1, -1)))
+        # act [B, F]: up cuts F by tiles, down cuts F by K chunks
+        edges.append(Edge(up, down, (1, -1, -1), (-1, 1, -1)))
+        prev = down
+    ops.append(Op("lm", (_ceil(shape.V, k.rows_lm), 1, 1), cost=rows_cost(shape.V, k.rows_lm, shape.H)))
+    kinds["lm"] = ("lm", -1)
+    edges.append(Edge(prev, "lm", (1, -1, -1), (-1, -1, -1)))
+    # the embed op writes all of h with one task: its out_map cuts nothing
+    edges[0] = Edge("embed", "qkv0", (-1, -1, -1), (-1, -1, -1))
+    return ops, edges, kinds
+
+
+def _queue(tasks: List[PlannedTask], graph: rules.TaskGraph, n_workers: int) -> Tuple[List[List[int]], int]:
+    q = rules.greedy_balance(range(len(tasks)), [t.cost for t in tasks], n_workers)
+    return rules.pad_queues(q)
+
+
+def llama_step_plan(shape: LlamaShape, k: Knobs, B: int, seq0: Sequence[int], max_steps: int,
+                    n_workers: int) -> Plan:
+    """Plan one decode step; the same plan serves ``max_steps`` consecutive steps.
+
+    Tasks inside each event's successor range are placed longest-first (only
+    attention tasks differ in size), then dealt to workers greedily by bytes in
+    that order.  The step ends with an extra event that every LM-head task
+    triggers; the next step's embedding task waits on it one epoch back.
+    """
+    ops, edges, kinds = llama_step_ops(shape, k, B, seq0, max_steps)
+    g = rules.build_task_graph(ops, edges)
+    opmap = {o.name: o for o in ops}
+    cost = [opmap[t.op].cost(t.bid) for t in g.tasks]
+    # longest-first inside every successor range (stable), then renumber
+    ranges = [(0, len(g.first_tasks))] + [(e.first_task_id, e.last_task_id) for e in g.events]
+    order = rules.longest_first_within(sorted(ranges), cost)
+    new_id = {old: new for new, old in enumerate(order)}
+    step_done = len(g.events)
+    thresholds = [e.num_triggers for e in g.events] + [0]
+    tasks: List[PlannedTask] = []
+    for old in order:
+        t = g.tasks[old]
+        kind, layer = kinds[t.op]
+        waits, signals = [], []
+        if t.dependent_event is not None:
+            waits.append((t.dependent_event, g.events[t.dependent_event].num_triggers, 0))
+        if t.trigger_event is not None:
+            signals.append((t.trigger_event, 1))
+        if kind == "lm":
+            signals.append((step_done, 1))
+            thresholds[step_done] += 1
+        tasks.append(PlannedTask(t.op, kind, layer, t.bid, cost[old], waits, signals))
+    # the embedding task waits for the previous step's LM head (epoch offset -1)
+    for t in tasks:
+        if t.kind == "embed":
+            t.waits.append((step_done, thresholds[step_done], -1))
+    # remap event first/last ids are unchanged by a within-range permutation
+    assert sorted(new_id.values()) == list(range(len(order)))
+    queues, lmax = _queue(tasks, g, n_workers)
+    return Plan(tasks, thresholds, queues, lmax, g)
+
+
+# ---------------------------------------------------------------------------
+# MegaRTP GLM pre-attention plan (M=16, KV=8192)
+# ---------------------------------------------------------------------------
+
+GLM_TILE_COUNTS = {"A0": 16, "B0": 84, "C0": 48, "B1": 8, "D1": 128, "D0": 128, "D2": 256, "E1": 64}
+
+
+def megartp_glm_plan(n_workers: int = 148):
+    """The article's plan: tiles A0 16, B0 1*21*4, C0 1*12*4, B1 8, D1 1*32*4,
+    D0 1*64*2, D2 1*64*4, E1 4*16 (732), listed in that order.  Publications:
+    event0 (A0's 16 hidden/scale rows, whole) feeds B0 and B1; event1 (A0's 16
+    norm rows, whole) feeds C0; event2 (16 final B0 Q/scale tiles) feeds D0
+    and D1; event3 (48 C0 partials, tile_reduce) feeds D1; events 4-67 (D0's
+    128 tiles, tile_cover in pairs, one per head) feed D2; event68 (32 D1
+    Indexer-Q tiles) and event69 (B1's cache write, threshold 1) feed E1.
+
+    Which 16 of B0's and 32 of D1's tiles publish is not stated; the last ones
+    are taken (parity unpinned for that mapping).
+    """
+    order = list(GLM_TILE_COUNTS)
+    base, n = {}, 0
+    for op in order:
+        base[op] = n
+        n += GLM_TILE_COUNTS[op]
+    thresholds: List[int] = []
+    waits: Dict[int, List[Tuple[int, int]]] = {i: [] for i in range(n)}
+    signals: Dict[int, List[Tuple[int, int]]] = {i: [] for i in range(n)}
+
+    def publish(op, publishers, strategy, k, consumers):
+        ths = rules.pairing(strategy, len(publishers), k)
+        first = len(thresholds)
+        thresholds.extend(ths)
+        per = len(publishers) // len(ths)
+        for j, t in enumerate(publishers):
+            signals[base[op] + t].append((first + j // per, 1))
+        for cop in consumers:
+            nc = GLM_TILE_COUNTS[cop]
+            cper = nc // len(ths)
+            for c in range(nc):
+                ev = first + c // cper
+                waits[base[cop] + c].append((ev, thresholds[ev]))
+
+    a0 = list(range(16))
+    publish("A0", a0, rules.WHOLE, 16, ["B0", "B1"])                       # event 0
+    publish("A0", a0, rules.WHOLE, 16, ["C0"])                             # event 1
+    publish("B0", list(range(84 - 16, 84)), rules.WHOLE, 16, ["D0", "D1"])  # event 2
+    publish("C0", list(range(48)), rules.TILE_REDUCE, 48, ["D1"])          # event 3
+    publish("D0", list(range(128)), rules.TILE_COVER, 2, ["D2"])           # events 4..67
+    publish("D1", list(range(128 - 32, 128)), rules.WHOLE, 32, ["E1"])     # event 68
+    publish("B1", [7], rules.WHOLE, 1, ["E1"])                             # event 69
+    queues = rules.round_robin(n, n_workers)
+    padded, lmax = rules.pad_queues(queues)
+    return {"n_tasks": n, "thresholds": thresholds, "waits": waits, "signals": signals,
+            "queues": padded, "lmax": lmax, "base": base}

@@ -1,0 +1,133 @@
+"""Model shapes and seeded synthetic inputs.
+
+This module holds no arithmetic of the decode method: it only names the
+workloads (shapes, step counts, cache lengths) and draws their random
+weights, caches, tokens and lengths from seeded generators.  It serves both
+the CUDA path and the CPU checks, which receive the same tensors.
+
+Recipe: weights bf16 N(0, 0.02) (norm weights 1), KV caches bf16 N(0, 1),
+tokens uniform over the vocabulary, batch-8 cache lengths uniform in
+[512, 4096]; seeds 1234 + workload index for weights, +100 for caches,
++200 for tokens and lengths.  There are no trained weights and no dataset.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Dict, List, Optional
+
+import torch
+
+
+@dataclass(frozen=True)
+class ModelShape:
+    L: int
+    H: int
+    Hq: int
+    Hkv: int
+    D: int
+    F: int
+    V: int
+    eps: float
+    theta: float
+    qk_norm: bool = False
+    tied: bool = True
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int
+    shape: ModelShape
+    batch: int
+    seq_len: int              # cached tokens per sequence before the first step
+    steps: int
+    len_range: Optional[tuple] = None   # (lo, hi) inclusive: per-sequence lengths drawn from a seed
+
+    @property
+    def weight_seed(self):
+        return 1234 + self.index
+
+    @property
+    def cache_seed(self):
+        return 1234 + self.index + 100
+
+    @property
+    def token_seed(self):
+        return 1234 + self.index + 200
+
+
+TINY = ModelShape(L=2, H=256, Hq=4, Hkv=2, D=64, F=688, V=1024, eps=1e-5, theta=1e4)
+LLAMA_1B = ModelShape(L=16, H=2048, Hq=32, Hkv=8, D=64, F=8192, V=128256, eps=1e-5, theta=5e5)
+QWEN3_8B = ModelShape(L=36, H=4096, Hq=32, Hkv=8, D=128, F=12288, V=151936, eps=1e-6, theta=1e6,
+                      qk_norm=True, tied=False)
+
+WORKLOADS: Dict[str, Workload] = {
+    "tiny": Workload("tiny", 0, TINY, 1, 64, 8),
+    "llama1b_b1": Workload("llama1b_b1", 1, LLAMA_1B, 1, 1024, 128),
+    "llama1b_b8": Workload("llama1b_b8", 2, LLAMA_1B, 8, 4096, 64, len_range=(512, 4096)),
+    "qwen3_8b_b1": Workload("qwen3_8b_b1", 4, QWEN3_8B, 1, 2048, 32),
+    "qwen3_8b_b16": Workload("qwen3_8b_b16", 4, QWEN3_8B, 16, 2048, 32),
+}
+
+
+def seq_lengths(w: Workload) -> List[int]:
+    """Cached tokens per sequence before the first step."""
+    if w.len_range is None:
+        return [w.seq_len] * w.batch
+    g = torch.Generator().manual_seed(w.token_seed)
+    lo, hi = w.len_range
+    return torch.randint(lo, hi + 1, (w.batch,), generator=g).tolist()
+
+
+def first_tokens(w: Workload) -> List[int]:
+    g = torch.Generator().manual_seed(w.token_seed + 1)
+    return torch.randint(0, w.shape.V, (w.batch,), generator=g).tolist()
+
+
+def _randn(shape, g, device, std=1.0):
+    t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(torch.bfloat16)
+
+
+def make_weights(shape: ModelShape, seed: int, device="cpu", std: float = 0.02) -> Dict[str, object]:
+    """Weights in the usual [out_features, in_features] row-major layout.
+    Per-layer tensors are lists indexed by layer.  With tied embeddings
+    ``lm_head`` is the same tensor as ``embed``."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    s = shape
+    w: Dict[str, object] = {"embed": _randn((s.V, s.H), g, device, std)}
+    per = {k: [] for k in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "norm_attn", "norm_mlp")}
+    if s.qk_norm:
+        per["qnorm"], per["knorm"] = [], []
+    ones_h = torch.ones(s.H, dtype=torch.bfloat16, device=device)
+    for _ in range(s.L):
+        per["wq"].append(_randn((s.Hq * s.D, s.H), g, device, std))
+        per["wk"].append(_randn((s.Hkv * s.D, s.H), g, device, std))
+        per["wv"].append(_randn((s.Hkv * s.D, s.H), g, device, std))
+        per["wo"].append(_randn((s.H, s.Hq * s.D), g, device, std))
+        per["wg"].append(_randn((s.F, s.H), g, device, std))
+        per["wu"].append(_randn((s.F, s.H), g, device, std))
+        per["wd"].append(_randn((s.H, s.F), g, device, std))
+        per["norm_attn"].append(ones_h.clone())
+        per["norm_mlp"].append(ones_h.clone())
+        if s.qk_norm:
+            per["qnorm"].append(torch.ones(s.D, dtype=torch.bfloat16, device=device))
+            per["knorm"].append(torch.ones(s.D, dtype=torch.bfloat16, device=device))
+    w.update(per)
+    w["norm_final"] = ones_h.clone()
+    w["lm_head"] = w["embed"] if s.tied else _randn((s.V, s.H), g, device, std)
+    return w
+
+
+def make_cache(shape: ModelShape, batch: int, smax: int, seed: int, device="cpu"):
+    """K and V caches, [L, B, Hkv, smax, D] bf16, every slot N(0, 1)."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    dims = (shape.L, batch, shape.Hkv, smax, shape.D)
+    return _randn(dims, g, device), _randn(dims, g, device)
+
+
+def to_host_u16(t: torch.Tensor):
+    """bf16 tensor -> numpy uint16 bit patterns (for the CPU checks)."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")
