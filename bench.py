@@ -1,0 +1,297 @@
+"""Decode-step benchmark of the persistent megakernel (one JSON line on rank 0).
+
+Default workload: Llama-3.2-1B shape, batch 1, KV cache pre-filled to 1024
+tokens, random bf16 weights (synthetic; no trained weights, no dataset).  A
+step is one decode step of the whole model: embedding, 16 layers, LM head and
+argmax, run as one persistent kernel launch.  Weights (2.5 GB) exceed the
+129 MB L2, so no flush is needed between steps.
+
+Arms:
+  --impl mk (default)   the CUDA path through the C ABI (libmk)
+  --impl reference      the plain CPU oracle (fp32 twin) on the host cores
+Multi-GPU: independent replicas, one per rank, no collective on the data path
+(weak scaling); value = tokens of all ranks / slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode step µs & tokens/s at 1 GB300; achieved HBM GB/s as % of roofline"
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("interp.cu", "mk_internal.h", "planner.cpp"):
+        with open(os.path.join(ROOT, "persistent_megakernel_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"mk_interp_{workload}.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("kernel_source_hash") == kernel_source_hash():
+            return d.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n):
+    if n <= 1 or "RANK" not in os.environ:
+        return 0, 1, None
+    import torch
+    import torch.distributed as dist
+    dist.init_process_group("nccl")
+    rank = dist.get_rank()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+    return rank, dist.get_world_size(), dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def cpu_oracle_rate(w, steps, warmup=0, device_for_inputs=None):
+    """Time the oracle's fp32 twin on the host cores over `steps` decode steps."""
+    import torch
+    from oracle import forward as orc
+    from persistent_megakernel_decode_gb300 import synth
+    s = w.shape
+    seq0 = synth.seq_lengths(w)
+    dev = device_for_inputs or "cpu"
+    wt = synth.make_weights(s, w.weight_seed, device=dev)
+    hw = {k: ([synth.to_host_u16(t) for t in v] if isinstance(v, list) else synth.to_host_u16(v)) for k, v in wt.items()}
+    del wt
+    smax = max(seq0) + warmup + steps + 1
+    dims = (s.L, w.batch, s.Hkv, smax, s.D)
+    rng = np.random.default_rng(w.cache_seed)
+    kc = rng.integers(0x3000, 0x3F80, size=dims, dtype=np.uint16)   # finite bf16 bit patterns
+    vc = rng.integers(0x3000, 0x3F80, size=dims, dtype=np.uint16)
+    shape = orc.Shape(s.L, s.H, s.Hq, s.Hkv, s.D, s.F, s.V, s.qk_norm, s.eps, s.theta)
+    cores = os.cpu_count() or 1
+    toks = synth.first_tokens(w)
+    times = []
+    for i in range(warmup + steps):
+        t0 = time.perf_counter()
+        _, _, am = orc.decode_step(shape, hw, kc, vc, [x + i for x in seq0], toks, precision=32, nthreads=cores,
+                                   want_hidden=False)
+        dt = time.perf_counter() - t0
+        toks = [int(x) for x in am]
+        if i >= warmup:
+            times.append(dt)
+    return float(np.sum(times)), cores
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    total, cores = cpu_oracle_rate(w, args.steps, args.warmup)
+    tps = w.batch * args.steps / total
+    sample = f"{args.steps} timed decode steps of {w.name} (fp32 oracle, all layers), after {args.warmup} warm-up"
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seq_len, "layers": w.shape.L},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_mk(args, w, rank, world, dist):
+    import torch
+    from persistent_megakernel_decode_gb300 import build, runtime as rt, synth
+    build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    s = w.shape
+    seq0 = synth.seq_lengths(w)
+    steps_total = args.warmup + args.steps
+    max_steps = max(w.steps, steps_total)
+    weights = synth.make_weights(s, w.weight_seed, device=dev)
+    smax = max(seq0) + max_steps + 1
+    kc, vc = synth.make_cache(s, w.batch, smax, w.cache_seed, device=dev)
+    stream = torch.cuda.Stream(dev)
+    target = {"mode": rt.MODE_PER_OP} if args.mode == "per_op" else {}
+    sess = rt.Session(s, weights, kc, vc, seq0, max_steps, stream=stream, **target)
+    info = sess.plan.info()
+    sess.tokens[0] = torch.tensor(synth.first_tokens(w), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    # warm-up
+    with torch.cuda.stream(stream):
+        for st in range(args.warmup):
+            sess.run(st, 1)
+    sess.sync()
+    # timed: one launch per step, events on the launching stream
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for i in range(args.steps):
+                sess.run(args.warmup + i, 1)
+                ev[i + 1].record(stream)
+        stream.synchronize()
+    rec = sess.sync()
+    barrier(dist)
+    step_ms = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)])
+    total_ms = float(ev[0].elapsed_time(ev[-1]))
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens_all = w.batch * args.steps * world
+    value = tokens_all / (total_ms / 1e3)
+    # end to end through the public API with host buffers: token in, argmax out
+    e2e_steps = min(args.steps, 32)
+    pinned_tok = torch.tensor(synth.first_tokens(w), dtype=torch.int32).pin_memory()
+    pinned_key = torch.zeros(w.batch, dtype=torch.int64).pin_memory()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            sess.tokens[i].copy_(pinned_tok, non_blocking=True)
+            sess.run(i, 1, host_tokens=True)
+            pinned_key.copy_(sess.argmax[i], non_blocking=True)
+            stream.synchronize()
+            pinned_tok.copy_(torch.from_numpy(rt.argmax_index(pinned_key.numpy().view(np.uint64)).astype(np.int32)))
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": w.batch * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * w.batch,
+           "d2h_bytes_per_step": 8 * w.batch, "steps": e2e_steps}
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    alg = info["algorithmic_bytes_step"]
+    avg_launch_s = float(np.mean(step_ms)) / 1e3
+    achieved = alg / avg_launch_s / 1e9
+    traffic = profiled_traffic(w.name)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": alg,
+                "kernel": "mk_interp", "nominal_8tbs_frac": achieved / 8000.0}
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu_steps = 2
+        total, cores = cpu_oracle_rate(w, cpu_steps, 0, device_for_inputs=dev)
+        cpu = {"value": w.batch * cpu_steps / total, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{cpu_steps} decode steps of {w.name} (fp32 oracle, all layers, batch {w.batch})"}
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seq_len, "layers": s.L, "hidden": s.H,
+                   "vocab": s.V, "mode": args.mode, "l2": "weights (2.5 GB) exceed L2 (129 MB); no flush",
+                   "parallelism": f"replicas{world}"},
+        "step_us": {"median": float(np.median(step_ms)) * 1e3, "p10": float(np.percentile(step_ms, 10)) * 1e3,
+                    "p90": float(np.percentile(step_ms, 90)) * 1e3},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": args.steps * info["num_launches"],
+        "plan": {k: info[k] for k in ("num_workers", "lmax", "num_tasks", "num_events", "num_pages", "smem_bytes")},
+        "device_error": int(rec.code),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
+    ap.add_argument("--workload", default="llama1b_b1")
+    ap.add_argument("--mode", default="megakernel", choices=["megakernel", "per_op"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from persistent_megakernel_decode_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, w, rank)
+        return
+    rank, world, dist = dist_setup(args.gpus)
+    run_mk(args, w, rank, world, dist)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,259 @@
+/*
+ * mk.h -- C ABI of libmk: planner and persistent decode megakernel for GB300
+ * (sm_103a).  Plain C types only; device buffers are passed as 64-bit device
+ * addresses (uint64_t) or void*, the CUDA stream as void* (a cudaStream_t).
+ *
+ * A decode step of a dense Llama-style decoder runs as ONE resident kernel
+ * (one worker CTA per SM).  Each worker interprets its slice of a host-built
+ * static queue of tile instructions, int32 [num_workers, lmax, 32], padded
+ * with NoOp ("MegaRTP megakernel article", sections 3 and 4, KernelPlan).
+ * Instructions synchronise through global event counters: a producer adds to
+ * a counter after its write-back, a consumer waits for counter >= target
+ * right before it reads the activation ("CMU 15-779 Lecture 7 notes",
+ * section 4.1; MegaRTP section 3).  Events are derived from producer /
+ * consumer grid cuts with MPK's gcd rule and fork/join lcm normalisation
+ * ("MPK code walkthrough", fine-grained pipeline).  Counters are never reset
+ * between steps: the target at step s is threshold x (s + 1) (monotone
+ * epochs, "GEMM + AllToAll fusion post", section 2).
+ *
+ * Ownership: a plan owns host memory only.  Every device buffer -- weights,
+ * KV caches, outputs and the workspace -- belongs to the caller.  No entry
+ * point allocates or frees device memory.
+ *
+ * Errors: every int-returning call returns MK_OK (0) or an MK_ERR_* code;
+ * mk_last_error() then describes it (thread-local).  Device-side failures
+ * (a wait that timed out, an instruction that failed its checks) are recorded
+ * in the workspace and reported by mk_sync_status(); the kernel never traps.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define MK_OK               0
+#define MK_ERR_INVALID      1   /* malformed descriptor or argument */
+#define MK_ERR_UNSUPPORTED  2   /* shape the kernels do not handle (divisibility, sizes) */
+#define MK_ERR_DEADLOCK     3   /* the planner's own queue simulation did not finish */
+#define MK_ERR_CUDA         4   /* a CUDA runtime call failed */
+#define MK_ERR_RESIDENCY    5   /* the worker grid cannot be co-resident on the GPU */
+#define MK_ERR_TIMEOUT      6   /* a device wait ran past its time budget */
+#define MK_ERR_DEVICE_CHECK 7   /* an instruction failed its device-side checks */
+#define MK_ERR_UNBOUND      8   /* a required binding was not set */
+
+/* ---- opcodes (word 0 of an instruction) ---- */
+#define MK_OP_NOOP     0   /* queue padding */
+#define MK_OP_COUNTER  1   /* waits and signals only (explicit-graph plans) */
+#define MK_OP_EMBED    2   /* h = E[token] */
+#define MK_OP_QKV      3   /* RMSNorm + rows of Wq/Wk/Wv */
+#define MK_OP_ATTN     4   /* q/k norm, RoPE, KV append, split-KV attention, last split merges */
+#define MK_OP_O        5   /* rows of Wo + residual */
+#define MK_OP_UP       6   /* RMSNorm + gate/up rows + SiLU(g) * u */
+#define MK_OP_DOWN     7   /* K chunk of Wd rows, added into the residual */
+#define MK_OP_LM       8   /* final RMSNorm + LM-head rows + argmax */
+#define MK_NUM_OPCODES 9
+
+/* ---- plan modes ---- */
+#define MK_MODE_MEGAKERNEL 0   /* one persistent launch per step */
+#define MK_MODE_PER_OP     1   /* baseline: one launch per op, same device code */
+
+/* ---- mk_run flags ---- */
+#define MK_RUN_HOST_TOKENS 1u  /* every step reads tokens[s] (teacher forcing) */
+#define MK_RUN_TRACE       2u  /* record per-instruction globaltimer stamps */
+
+typedef struct mk_plan_s *mk_plan_t;
+
+/* Dense Llama-style decoder.  Weights use the usual [out, in] row-major bf16
+ * layout; norm weights are bf16 vectors. */
+typedef struct {
+    int layers, hidden, q_heads, kv_heads, head_dim, ffn, vocab;
+    int qk_norm;        /* per-head RMSNorm of q and k before RoPE (Qwen3-style) */
+    float eps;          /* RMSNorm epsilon */
+    float rope_theta;   /* RoPE base, rotate-half pairing (i, i + head_dim/2) */
+} mk_model_desc;
+
+typedef struct {
+    int batch;             /* sequences decoded together, 1..8 */
+    const int *seq_len0;   /* host [batch]: cached tokens per sequence before step 0 */
+    int max_steps;         /* the plan serves steps 0 .. max_steps-1 */
+    int cache_slots;       /* S_max of the KV cache tensors; >= seq_len0[b] + max_steps */
+    int capture_hidden;    /* 1: write the residual stream after every layer (tests) */
+} mk_step_desc;
+
+typedef struct {
+    int num_sms;           /* workers; 0 = all SMs of the current device */
+    int smem_per_cta;      /* dynamic shared memory per CTA; 0 = device opt-in maximum */
+    int mode;              /* MK_MODE_* */
+    /* tile knobs, 0 = default */
+    int rows_qkv, rows_o, rows_up, rows_down, kchunk_down, rows_lm, attn_split;
+    int page_bytes;        /* shared-memory page size; 0 = 16384 */
+} mk_target_desc;
+
+typedef struct {
+    int num_workers, lmax, num_tasks, num_events, num_ops, num_launches;
+    int num_pages, page_bytes, smem_bytes, act_bytes;
+    int rows_qkv, rows_o, rows_up, rows_down, kchunk_down, rows_lm, attn_split;
+    int total_slots;                 /* instruction slots over all launches of a step */
+    uint64_t workspace_bytes;        /* device bytes mk_run needs */
+    uint64_t scratch_offset;         /* workspace offset from which every byte is rewritten
+                                        within a step before it is read (activations, partials) */
+    uint64_t algorithmic_bytes_step; /* weights once + KV read + KV append, at step 0 */
+} mk_plan_info;
+
+/* ---- bindings: caller-owned device buffers ---- */
+#define MK_BIND_EMBED       0   /* bf16 [V, H] */
+#define MK_BIND_LM_HEAD     1   /* bf16 [V, H] (may be the embedding) */
+#define MK_BIND_NORM_FINAL  2   /* bf16 [H] */
+#define MK_BIND_WQ          3   /* per layer, bf16 [Hq*D, H] */
+#define MK_BIND_WK          4   /* per layer, bf16 [Hkv*D, H] */
+#define MK_BIND_WV          5   /* per layer, bf16 [Hkv*D, H] */
+#define MK_BIND_WO          6   /* per layer, bf16 [H, Hq*D] */
+#define MK_BIND_WG          7   /* per layer, bf16 [F, H] */
+#define MK_BIND_WU          8   /* per layer, bf16 [F, H] */
+#define MK_BIND_WD          9   /* per layer, bf16 [H, F] */
+#define MK_BIND_NORM_ATTN  10   /* per layer, bf16 [H] */
+#define MK_BIND_NORM_MLP   11   /* per layer, bf16 [H] */
+#define MK_BIND_QNORM      12   /* per layer, bf16 [D] (qk_norm only) */
+#define MK_BIND_KNORM      13   /* per layer, bf16 [D] (qk_norm only) */
+#define MK_BIND_KCACHE     14   /* bf16 [L, B, Hkv, S_max, D]; layer argument ignored */
+#define MK_BIND_VCACHE     15   /* bf16 [L, B, Hkv, S_max, D]; layer argument ignored */
+#define MK_BIND_TOKENS     16   /* int32 [max_steps + 1, B]: tokens[s] feeds step s */
+#define MK_BIND_LOGITS     17   /* fp32 [B, V]: logits of the last step run */
+#define MK_BIND_ARGMAX     18   /* uint64 [max_steps, B]: packed argmax of each step */
+#define MK_BIND_HIDDEN     19   /* fp32 [L, B, H]: residual after each layer (capture_hidden) */
+#define MK_BIND_COUNT      20
+
+/* Packed argmax key: (order-preserving bits of the fp32 logit << 32) |
+ * (0xFFFFFFFF - index); the largest key is the largest logit, lowest index on
+ * ties.  mk_argmax_index() recovers the index. */
+int32_t mk_argmax_index(uint64_t key);
+
+/* Device-side failure record, read back by mk_sync_status(). */
+typedef struct {
+    int32_t code;        /* MK_OK or MK_ERR_TIMEOUT / MK_ERR_DEVICE_CHECK */
+    int32_t worker;      /* CTA that recorded it */
+    int32_t slot;        /* queue slot of the instruction */
+    int32_t event;       /* event waited on (-1 if none) */
+    uint32_t observed;   /* counter value seen last */
+    uint32_t needed;     /* target it waited for */
+    int32_t opcode;
+    int32_t role;        /* 0 loader, 1 activation loader, 2 consumers */
+} mk_error_record;
+
+/* ---- planning (host only, no CUDA calls unless num_sms/smem are 0) ---- */
+
+/* Plan one decode step of a Llama-style decoder.  The op DAG (per layer:
+ * qkv -> attention -> o -> mlp-up -> mlp-down; then the LM head; an
+ * embedding task first) is expanded into tile tasks, events are derived with
+ * the gcd/lcm rule, tasks are linearised so each event's successors are
+ * contiguous ("MPK code walkthrough", building the SM-level DAG), placed
+ * longest-first within each successor range and dealt to workers by bytes.
+ * The plan is checked by simulating its queues.  *out receives a plan the
+ * caller frees with mk_free().  Returns MK_ERR_INVALID / MK_ERR_UNSUPPORTED
+ * / MK_ERR_DEADLOCK on failure (nothing allocated). */
+int mk_plan(const mk_model_desc *model, const mk_step_desc *step, const mk_target_desc *target,
+            mk_plan_t *out);
+
+/* Explicit task graphs (tests of the event rules and of the device protocol):
+ * ops of MK_OP_COUNTER tasks, either with MPK-style edges (gcd/lcm rule) or
+ * with MegaRTP-style publications (whole / tile / tile_cover / tile_reduce,
+ * "MegaRTP megakernel article", section 4, TaskGraph). */
+typedef struct {
+    int grid[3];
+    int cost;            /* bytes, for queue balancing */
+} mk_graph_op;
+
+typedef struct {
+    int prod, cons;      /* op indices */
+    int out_map[3];      /* tensor dim cut by each producer grid axis, -1 = none */
+    int in_map[3];       /* tensor dim cut by each consumer grid axis, -1 = none */
+} mk_graph_edge;
+
+#define MK_PAIR_WHOLE       0
+#define MK_PAIR_TILE        1
+#define MK_PAIR_TILE_COVER  2
+#define MK_PAIR_TILE_REDUCE 3
+
+typedef struct {
+    int prod;            /* producing op */
+    int first_pub;       /* first publishing task of that op (op-local index) */
+    int num_pub;         /* publishing tasks: first_pub .. first_pub+num_pub-1 */
+    int strategy;        /* MK_PAIR_* */
+    int k;               /* producer tasks per event for cover / reduce */
+    int num_cons;
+    int cons[4];         /* consumer ops; their tasks are spread evenly over the events */
+} mk_graph_pub;
+
+typedef struct {
+    int num_ops;
+    const mk_graph_op *ops;
+    int num_edges;                 /* MPK-style edges, or 0 */
+    const mk_graph_edge *edges;
+    int num_pubs;                  /* MegaRTP-style publications, or 0 */
+    const mk_graph_pub *pubs;
+    int round_robin;               /* 1: task i -> worker i mod W, in op order */
+} mk_graph_desc;
+
+int mk_plan_graph(const mk_graph_desc *graph, const mk_target_desc *target, mk_plan_t *out);
+
+int mk_plan_info_get(mk_plan_t plan, mk_plan_info *info);
+
+/* Copies of the plan for inspection and bit-exact tests (caller-owned host
+ * buffers, sized from mk_plan_info):
+ *  queue      int32 [total_slots, 32]   raw instruction words; the megakernel
+ *             plan's single launch is [num_workers, lmax, 32]; per-op plans
+ *             concatenate one [workers_k, lmax_k, 32] block per launch
+ *  task_ids   int32 [total_slots]       task id per slot, -1 = NoOp
+ *  thresholds int32 [num_events]              per-step increments of each event
+ *  tasks      int32 [num_tasks, MK_TASK_FIELDS]
+ * Any pointer may be NULL. */
+#define MK_TASK_FIELDS 24
+/* tasks row: kind(opcode), layer, bx, by, bz, cost, n_waits, 3 x (event,
+ * threshold, epoch_offset), n_signals, 2 x (event, increment), 4 reserved */
+int mk_plan_export(mk_plan_t plan, int32_t *queue, int32_t *task_ids, int32_t *thresholds, int32_t *tasks);
+
+/* Bind a caller-owned device buffer (MK_BIND_*).  `layer` selects the layer
+ * of per-layer bindings and is ignored otherwise.  Host-only; the table is
+ * uploaded by the next mk_run.  Pointers must be 16-byte aligned. */
+int mk_bind(mk_plan_t plan, int binding, int layer, uint64_t device_ptr);
+
+/* Run steps first_step .. first_step+num_steps-1 asynchronously on `stream`.
+ * `workspace` is caller-allocated device memory of at least
+ * info.workspace_bytes (16-byte aligned); it holds the queue, operand table,
+ * event counters, activations and the error record.  When first_step == 0
+ * the counters, the error record and the ARGMAX binding are cleared.
+ * One cooperative launch per step (MK_MODE_MEGAKERNEL) or per op
+ * (MK_MODE_PER_OP).  Returns MK_ERR_UNBOUND if a required binding is
+ * missing, MK_ERR_RESIDENCY if the grid cannot be co-resident, MK_ERR_CUDA on
+ * a launch failure.  timeout_ns bounds every device wait (0 = 200 ms). */
+int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_step, int num_steps,
+           uint32_t flags, uint64_t timeout_ns, void *stream);
+
+/* Synchronise `stream`, read the device error record into *rec (may be
+ * NULL) and return its code (MK_OK, MK_ERR_TIMEOUT, MK_ERR_DEVICE_CHECK) or
+ * MK_ERR_CUDA. */
+int mk_sync_status(mk_plan_t plan, void *workspace, void *stream, mk_error_record *rec);
+
+/* Copy the event counters (uint32 [num_events]) from the workspace to host. */
+int mk_read_counters(mk_plan_t plan, void *workspace, uint32_t *out);
+
+/* Copy the per-instruction trace (uint64 [num_workers, lmax, 4]: opcode,
+ * start, activation-ready, done, in globaltimer ns) to host.  Only filled by
+ * runs with MK_RUN_TRACE. */
+int mk_read_trace(mk_plan_t plan, void *workspace, uint64_t *out);
+
+/* Free the plan's host memory.  NULL-safe.  Never touches device memory. */
+void mk_free(mk_plan_t plan);
+
+/* Thread-local description of the last non-zero status. */
+const char *mk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

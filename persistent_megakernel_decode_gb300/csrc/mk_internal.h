@@ -1,0 +1,102 @@
+// Internal definitions shared by the planner (planner.cpp), the host launch
+// code and the interpreter kernel (interp.cu).  Not part of the C ABI.
+#pragma once
+#include <stdint.h>
+
+#include "../../include/mk.h"
+
+namespace mk {
+
+// ---- instruction word layout: 32 x int32 = 128 bytes ---------------------
+// (opcode, operand row, wait/signal counts, waits (event, threshold),
+//  signals (event, increment), payload with tile coordinates; no absolute
+//  addresses -- "MegaRTP megakernel article", section 4, KernelPlan)
+enum : int {
+    W_OPC = 0,      // opcode
+    W_ROW = 1,      // operand-table row
+    W_CNT = 2,      // n_waits | n_signals << 8
+    W_TASK = 3,     // task id (traces, error records)
+    W_WAIT = 4,     // 3 x {event | 0x80000000 if waiting one epoch back, threshold}
+    W_SIG = 10,     // 2 x {event, increment}
+    W_P = 14,       // payload, 18 words
+    W_WORDS = 32,
+};
+constexpr int MAX_WAITS = 3;
+constexpr int MAX_SIGS = 2;
+constexpr uint32_t WAIT_PREV_EPOCH = 0x80000000u;
+
+// GEMV payload (QKV, O, UP, DOWN, LM)
+enum : int {
+    P_ROW0 = W_P + 0,   // first row in the source matrix
+    P_NROWS = W_P + 1,  // rows in the tile (UP: gate rows; the tile also holds as many up rows)
+    P_K0 = W_P + 2,     // first column of the K chunk
+    P_KC = W_P + 3,     // K chunk length
+    P_OUT0 = W_P + 4,   // first output index (QKV: row of the group-major qkv buffer)
+    P_MAT = W_P + 5,    // QKV: 0 = Wq, 1 = Wk, 2 = Wv
+    P_SNAP = W_P + 6,   // 1 + layer whose residual the activation loader snapshots, or 0
+    P_KTOT = W_P + 7,   // row length (elements) of the source matrix
+};
+// ATTN payload
+enum : int {
+    P_G = W_P + 0, P_B = W_P + 1, P_SPLIT = W_P + 2, P_T0 = W_P + 3, P_T = W_P + 4,
+    P_NSPLIT = W_P + 5, P_LAYER = W_P + 6,
+};
+
+// ---- operand table slots (16 x uint64 per op row) ------------------------
+enum : int {
+    // EMBED
+    S_EMB_W = 0, S_EMB_H = 1, S_EMB_TOK = 2, S_EMB_KEYS = 3,
+    // QKV
+    S_QKV_WQ = 0, S_QKV_WK = 1, S_QKV_WV = 2, S_QKV_NORM = 3, S_QKV_H = 4, S_QKV_OUT = 5, S_QKV_HIST = 6,
+    // ATTN
+    S_AT_K = 0, S_AT_V = 1, S_AT_QKV = 2, S_AT_QN = 3, S_AT_KN = 4, S_AT_PART = 5, S_AT_OUT = 6,
+    S_AT_ARRIVE = 7, S_AT_SEQ0 = 8,
+    // O
+    S_O_W = 0, S_O_IN = 1, S_O_HRES = 2, S_O_HMID = 3,
+    // UP
+    S_UP_WG = 0, S_UP_WU = 1, S_UP_NORM = 2, S_UP_H = 3, S_UP_OUT = 4,
+    // DOWN
+    S_DN_W = 0, S_DN_IN = 1, S_DN_HRES = 2,
+    // LM
+    S_LM_W = 0, S_LM_NORM = 1, S_LM_H = 2, S_LM_LOGITS = 3, S_LM_KEYS = 4, S_LM_HIST = 5,
+    N_SLOTS = 16,
+};
+
+// ---- error record layout in the workspace (uint32 words) -----------------
+enum : int {
+    E_CODE = 0, E_WORKER = 1, E_SLOT = 2, E_EVENT = 3, E_OBSERVED = 4, E_NEEDED = 5,
+    E_OPCODE = 6, E_ROLE = 7, E_ABORT = 8, E_WORDS = 64,
+};
+
+// ---- kernel parameters ---------------------------------------------------
+struct KParams {
+    const int32_t *queue;   // this launch's [num_workers, lmax, 32]
+    const uint64_t *optab;  // [num_ops, 16]
+    uint32_t *counters;     // [num_events]
+    uint32_t *err;          // error record
+    uint64_t *trace;        // [num_workers, lmax, 4] or null
+    uint64_t timeout_ns;
+    int lmax, num_workers, num_ops, num_events;
+    int step, flags;
+    int num_pages, page_bytes, act_bytes, aux_bytes, smem_bytes;
+    int B, H, Hq, Hkv, D, F, V, L, Smax, qk_norm, nsplit_max;
+    float eps, theta;
+};
+
+constexpr int CONSUMER_WARPS = 8;
+constexpr int CONSUMERS = CONSUMER_WARPS * 32;
+constexpr int THREADS = CONSUMERS + 64;   // + loader warp + activation-loader warp
+constexpr int MAX_TILE_ROWS = 16;
+
+}  // namespace mk
+
+namespace mk {
+// ---- shared-memory budget (bytes); the kernel lays memory out in this order:
+// two activation slots, the page pool, an op scratch area, mbarriers, flags.
+inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
+inline int red_bytes(int B) { return CONSUMER_WARPS * MAX_TILE_ROWS * B * 4; }
+inline int attn_aux_bytes(int G, int T, int D) { return (G * T + CONSUMER_WARPS * G * D + 8 * G) * 4; }
+constexpr int MBAR_BYTES = 512;    // up to 64 mbarriers
+constexpr int CTRL_BYTES = 128;
+constexpr int MAX_PAGES = 28;      // 2 * MAX_PAGES + 4 mbarriers must fit MBAR_BYTES
+}  // namespace mk

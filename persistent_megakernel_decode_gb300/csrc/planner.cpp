@@ -1,0 +1,752 @@
+// Host planner of libmk: op DAG -> tile tasks -> events -> static queues.
+//
+// Event rule: "MPK code walkthrough" (Mirage Persistent Kernel), fine-grained
+// pipeline section -- every tensor edge gets event_dim[d] = gcd(producer
+// cuts, consumer cuts); a producer feeding several consumers (fork) and a
+// consumer fed by several producers (join) have their group sizes lcm'd so
+// the edges share one event set.  Task creation walks the op linearisation
+// and, per event, creates the consumer tasks inside that event's box, so an
+// event's successors are contiguous (building-the-SM-level-DAG section).
+// Pairing strategies whole / tile / tile_cover / tile_reduce: "MegaRTP
+// megakernel article", section 4 (TaskGraph).  Queues: section 4
+// (KernelPlan) and "CMU 15-779 Lecture 7 notes", sections 6.3-6.4.
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <functional>
+#include <numeric>
+#include <queue>
+#include <string>
+#include <vector>
+
+#include "mk_internal.h"
+#include "planner.h"
+
+namespace mk {
+
+thread_local std::string g_last_error;
+
+int set_error(int code, const std::string &msg) {
+    g_last_error = msg;
+    return code;
+}
+
+namespace {
+
+constexpr int MAXD = 4;
+
+struct OpDef {
+    int opcode = MK_OP_COUNTER;
+    int layer = -1;
+    int grid[3] = {1, 1, 1};
+    std::function<bool(const int *)> exists;      // empty: every grid point exists
+    std::function<int64_t(const int *)> cost;     // bytes streamed by one task
+};
+
+struct EdgeDef {
+    int prod, cons;
+    int out_map[3], in_map[3];
+};
+
+struct EdgeEv {
+    int ev[MAXD], pp[MAXD], cp[MAXD];
+};
+
+struct RawTask {
+    int op;
+    int bid[3];
+    int trig = -1, dep = -1;
+};
+
+struct RawEvent {
+    int ntrig, first, last;
+};
+
+void cut_counts(const int grid[3], const int map[3], int out[MAXD]) {
+    for (int d = 0; d < MAXD; ++d) out[d] = 1;
+    for (int a = 0; a < 3; ++a)
+        if (map[a] >= 0) out[map[a]] *= grid[a];
+}
+
+int piece(const int bid[3], const int grid[3], const int map[3], int d) {
+    int idx = 0;
+    for (int a = 0; a < 3; ++a)
+        if (map[a] == d) idx = idx * grid[a] + bid[a];
+    return idx;
+}
+
+int64_t lcm64(int64_t a, int64_t b) { return a / std::gcd(a, b) * b; }
+
+// gcd per edge, then lcm normalisation of fork groups and of join groups; a
+// group whose producer (fork) or consumer (join) cuts differ, or whose lcm
+// does not divide the cut, falls back to one whole event.
+int derive_event_dims(const std::vector<OpDef> &ops, const std::vector<EdgeDef> &edges, std::vector<EdgeEv> &ee) {
+    ee.assign(edges.size(), EdgeEv{});
+    for (size_t i = 0; i < edges.size(); ++i) {
+        cut_counts(ops[edges[i].prod].grid, edges[i].out_map, ee[i].pp);
+        cut_counts(ops[edges[i].cons].grid, edges[i].in_map, ee[i].cp);
+        for (int d = 0; d < MAXD; ++d) ee[i].ev[d] = std::gcd(ee[i].pp[d], ee[i].cp[d]);
+    }
+    auto normalise = [&](const std::vector<int> &idx, bool prod_side) {
+        auto part = [&](int i) { return prod_side ? ee[i].pp : ee[i].cp; };
+        bool same = true;
+        for (int i : idx)
+            for (int d = 0; d < MAXD; ++d) same &= part(i)[d] == part(idx[0])[d];
+        int new_ev[MAXD];
+        bool ok = same;
+        for (int d = 0; ok && d < MAXD; ++d) {
+            int64_t l = 1;
+            for (int i : idx) l = lcm64(l, part(i)[d] / ee[i].ev[d]);
+            if (part(idx[0])[d] % l != 0) ok = false;
+            else new_ev[d] = (int)(part(idx[0])[d] / l);
+        }
+        for (int i : idx)
+            for (int d = 0; d < MAXD; ++d) ee[i].ev[d] = ok ? new_ev[d] : 1;
+    };
+    std::vector<char> in_fork(edges.size(), 0);
+    for (size_t o = 0; o < ops.size(); ++o) {
+        std::vector<int> out;
+        for (size_t i = 0; i < edges.size(); ++i)
+            if (edges[i].prod == (int)o) out.push_back((int)i);
+        if (out.size() > 1) {
+            normalise(out, true);
+            for (int i : out) in_fork[i] = 1;
+        }
+    }
+    for (size_t o = 0; o < ops.size(); ++o) {
+        std::vector<int> in;
+        for (size_t i = 0; i < edges.size(); ++i)
+            if (edges[i].cons == (int)o) in.push_back((int)i);
+        if (in.size() > 1) {
+            for (int i : in)
+                if (in_fork[i]) return set_error(MK_ERR_UNSUPPORTED, "an edge in both a fork and a join");
+            normalise(in, false);
+        }
+    }
+    return MK_OK;
+}
+
+bool in_box(const int bid[3], const int grid[3], const int map[3], const int part[MAXD], const int ev[MAXD],
+            const int coord[MAXD]) {
+    for (int d = 0; d < MAXD; ++d) {
+        int g = part[d] / ev[d];
+        if (piece(bid, grid, map, d) / g != coord[d]) return false;
+    }
+    return true;
+}
+
+void unravel(int k, const int radix[MAXD], int out[MAXD]) {
+    for (int d = MAXD - 1; d >= 0; --d) {
+        out[d] = k % radix[d];
+        k /= radix[d];
+    }
+}
+
+bool exists(const OpDef &op, const int bid[3]) { return !op.exists || op.exists(bid); }
+
+// MPK task creation (ops must be listed in a topological order).
+int build_tasks(const std::vector<OpDef> &ops, const std::vector<EdgeDef> &edges, std::vector<RawTask> &tasks,
+                std::vector<RawEvent> &events, int &n_first) {
+    std::vector<EdgeEv> ee;
+    int rc = derive_event_dims(ops, edges, ee);
+    if (rc) return rc;
+    std::vector<std::vector<int>> tid(ops.size());
+    for (size_t o = 0; o < ops.size(); ++o)
+        tid[o].assign((size_t)ops[o].grid[0] * ops[o].grid[1] * ops[o].grid[2], -1);
+    auto lin = [&](int o, const int b[3]) { return ((size_t)b[0] * ops[o].grid[1] + b[1]) * ops[o].grid[2] + b[2]; };
+    auto add = [&](int o, const int b[3], int dep) {
+        RawTask t;
+        t.op = o;
+        std::memcpy(t.bid, b, sizeof(t.bid));
+        t.dep = dep;
+        tid[o][lin(o, b)] = (int)tasks.size();
+        tasks.push_back(t);
+    };
+    auto for_bids = [&](int o, const std::function<void(const int *)> &f) {
+        int b[3];
+        for (b[0] = 0; b[0] < ops[o].grid[0]; ++b[0])
+            for (b[1] = 0; b[1] < ops[o].grid[1]; ++b[1])
+                for (b[2] = 0; b[2] < ops[o].grid[2]; ++b[2])
+                    if (exists(ops[o], b)) f(b);
+    };
+    std::vector<char> done(ops.size(), 0);
+    n_first = 0;
+    for (int o = 0; o < (int)ops.size(); ++o) {
+        if (done[o]) continue;
+        std::vector<int> in;
+        for (size_t i = 0; i < edges.size(); ++i)
+            if (edges[i].cons == o) in.push_back((int)i);
+        if (in.empty()) {
+            if (!tasks.empty() && n_first != (int)tasks.size())
+                return set_error(MK_ERR_UNSUPPORTED, "ops without inputs must come first");
+            for_bids(o, [&](const int *b) { add(o, b, -1); });
+            n_first = (int)tasks.size();
+            done[o] = 1;
+            continue;
+        }
+        if (in.size() > 1) {  // join consumer
+            const EdgeEv &e0 = ee[in[0]];
+            int nev = 1;
+            for (int d = 0; d < MAXD; ++d) nev *= e0.ev[d];
+            for (int k = 0; k < nev; ++k) {
+                int c[MAXD];
+                unravel(k, e0.ev, c);
+                int ev_id = (int)events.size();
+                RawEvent ev{0, (int)tasks.size(), 0};
+                for_bids(o, [&](const int *b) {
+                    if (in_box(b, ops[o].grid, edges[in[0]].in_map, e0.cp, e0.ev, c)) add(o, b, ev_id);
+                });
+                ev.last = (int)tasks.size();
+                for (int i : in) {
+                    int p = edges[i].prod;
+                    for_bids(p, [&](const int *b) {
+                        if (in_box(b, ops[p].grid, edges[i].out_map, ee[i].pp, e0.ev, c)) {
+                            tasks[tid[p][lin(p, b)]].trig = ev_id;
+                            ev.ntrig++;
+                        }
+                    });
+                }
+                events.push_back(ev);
+            }
+            done[o] = 1;
+            continue;
+        }
+        const EdgeDef &e0 = edges[in[0]];
+        int p = e0.prod;
+        std::vector<int> bundle;
+        for (size_t i = 0; i < edges.size(); ++i)
+            if (edges[i].prod == p) bundle.push_back((int)i);
+        for (int i : bundle) {
+            int n = 0;
+            for (auto &e : edges) n += e.cons == edges[i].cons;
+            if (n != 1) return set_error(MK_ERR_UNSUPPORTED, "fork consumer with several in-edges");
+        }
+        std::sort(bundle.begin(), bundle.end(), [&](int a, int b) { return edges[a].cons < edges[b].cons; });
+        const EdgeEv &eb = ee[bundle[0]];
+        int nev = 1;
+        for (int d = 0; d < MAXD; ++d) nev *= eb.ev[d];
+        for (int k = 0; k < nev; ++k) {
+            int c[MAXD];
+            unravel(k, eb.ev, c);
+            int ev_id = (int)events.size();
+            RawEvent ev{0, (int)tasks.size(), 0};
+            for (int i : bundle) {
+                int co = edges[i].cons;
+                for_bids(co, [&](const int *b) {
+                    if (in_box(b, ops[co].grid, edges[i].in_map, ee[i].cp, eb.ev, c)) add(co, b, ev_id);
+                });
+            }
+            ev.last = (int)tasks.size();
+            for_bids(p, [&](const int *b) {
+                if (in_box(b, ops[p].grid, e0.out_map, eb.pp, eb.ev, c)) {
+                    tasks[tid[p][lin(p, b)]].trig = ev_id;
+                    ev.ntrig++;
+                }
+            });
+            events.push_back(ev);
+        }
+        for (int i : bundle) done[edges[i].cons] = 1;
+    }
+    return MK_OK;
+}
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// in-order queues, counters with epochs, `steps` back-to-back passes
+bool simulate(const std::vector<std::vector<int>> &queues, const std::vector<TaskRec> &tasks, int n_events,
+              int steps, std::string &why) {
+    std::vector<int64_t> cnt(n_events, 0);
+    for (int s = 0; s < steps; ++s) {
+        std::vector<size_t> pos(queues.size(), 0);
+        size_t remaining = 0;
+        for (auto &q : queues) remaining += q.size();
+        bool progress = true;
+        while (remaining && progress) {
+            progress = false;
+            for (size_t w = 0; w < queues.size(); ++w) {
+                while (pos[w] < queues[w].size()) {
+                    const TaskRec &t = tasks[queues[w][pos[w]]];
+                    bool ready = true;
+                    for (int i = 0; i < t.nw && ready; ++i)
+                        ready = cnt[t.w_ev[i]] >= (int64_t)t.w_thr[i] * (s + 1 + t.w_off[i]);
+                    if (!ready) break;
+                    for (int i = 0; i < t.ns; ++i) cnt[t.s_ev[i]] += t.s_inc[i];
+                    pos[w]++;
+                    remaining--;
+                    progress = true;
+                }
+            }
+        }
+        if (remaining) {
+            for (size_t w = 0; w < queues.size(); ++w)
+                if (pos[w] < queues[w].size()) {
+                    char buf[160];
+                    std::snprintf(buf, sizeof buf, "queue simulation stuck at step %d: worker %zu task %d", s, w,
+                                  queues[w][pos[w]]);
+                    why = buf;
+                    break;
+                }
+            return false;
+        }
+    }
+    return true;
+}
+
+// Deal tasks in order to the least-loaded worker (ties: lowest index).
+std::vector<std::vector<int>> greedy(const std::vector<int> &order, const std::vector<TaskRec> &tasks, int workers) {
+    using Item = std::pair<int64_t, int>;
+    std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
+    for (int w = 0; w < workers; ++w) heap.push({0, w});
+    std::vector<std::vector<int>> q(workers);
+    for (int t : order) {
+        Item it = heap.top();
+        heap.pop();
+        q[it.second].push_back(t);
+        it.first += tasks[t].cost;
+        heap.push(it);
+    }
+    return q;
+}
+
+}  // namespace
+
+// ---- encode and finish a plan --------------------------------------------
+
+void encode_task(const TaskRec &t, int task_id, int32_t *w) {
+    std::memset(w, 0, W_WORDS * sizeof(int32_t));
+    w[W_OPC] = t.opcode;
+    w[W_ROW] = t.op_row;
+    w[W_CNT] = t.nw | (t.ns << 8);
+    w[W_TASK] = task_id;
+    for (int i = 0; i < t.nw; ++i) {
+        w[W_WAIT + 2 * i] = (int32_t)((uint32_t)t.w_ev[i] | (t.w_off[i] < 0 ? WAIT_PREV_EPOCH : 0u));
+        w[W_WAIT + 2 * i + 1] = t.w_thr[i];
+    }
+    for (int i = 0; i < t.ns; ++i) {
+        w[W_SIG + 2 * i] = t.s_ev[i];
+        w[W_SIG + 2 * i + 1] = t.s_inc[i];
+    }
+    for (int i = 0; i < W_WORDS - W_P; ++i) w[W_P + i] = t.payload[i];
+}
+
+// Build the launch segments (one for the megakernel, one per op otherwise),
+// simulate them and encode the instruction words.
+int finish_queues(Plan &p, bool round_robin) {
+    std::vector<Segment> segs;
+    std::vector<std::vector<int>> all_q;
+    int n = (int)p.tasks.size();
+    auto make = [&](const std::vector<int> &order, int workers) {
+        std::vector<std::vector<int>> q;
+        if (round_robin) {
+            q.assign(workers, {});
+            for (size_t i = 0; i < order.size(); ++i) q[i % workers].push_back(order[i]);
+        } else {
+            q = greedy(order, p.tasks, workers);
+        }
+        Segment s;
+        s.workers = workers;
+        s.lmax = 0;
+        for (auto &r : q) s.lmax = std::max<int>(s.lmax, (int)r.size());
+        s.word_offset = (int64_t)p.words.size();
+        s.slot_offset = (int64_t)p.slot_task.size();
+        p.words.resize(p.words.size() + (size_t)workers * s.lmax * W_WORDS, 0);
+        p.slot_task.resize(p.slot_task.size() + (size_t)workers * s.lmax, -1);
+        for (int w = 0; w < workers; ++w)
+            for (int i = 0; i < s.lmax; ++i) {
+                size_t slot = (size_t)w * s.lmax + i;
+                if (i < (int)q[w].size()) {
+                    int t = q[w][i];
+                    encode_task(p.tasks[t], t, &p.words[s.word_offset + slot * W_WORDS]);
+                    p.slot_task[s.slot_offset + slot] = t;
+                }  // else NoOp: all-zero words
+            }
+        segs.push_back(s);
+        return q;
+    };
+    p.words.clear();
+    p.slot_task.clear();
+    if (p.mode == MK_MODE_MEGAKERNEL) {
+        std::vector<int> order(n);
+        std::iota(order.begin(), order.end(), 0);
+        auto q = make(order, p.num_workers);
+        std::string why;
+        if (!simulate(q, p.tasks, (int)p.thresholds.size(), 2, why)) return set_error(MK_ERR_DEADLOCK, why);
+    } else {
+        // per-op launches, ops in plan order; each launch only depends on earlier ones
+        std::vector<std::vector<int>> by_op(p.num_ops);
+        for (int t = 0; t < n; ++t) by_op[p.tasks[t].op_row].push_back(t);
+        std::vector<int64_t> cnt(p.thresholds.size(), 0);
+        for (int o = 0; o < p.num_ops; ++o) {
+            if (by_op[o].empty()) continue;
+            int workers = std::min<int>(p.num_workers, (int)by_op[o].size());
+            auto q = make(by_op[o], workers);
+            for (int t : by_op[o])
+                for (int i = 0; i < p.tasks[t].nw; ++i)
+                    if (p.tasks[t].w_off[i] == 0 && cnt[p.tasks[t].w_ev[i]] < p.tasks[t].w_thr[i])
+                        return set_error(MK_ERR_DEADLOCK, "per-op launch waits on a later launch");
+            for (int t : by_op[o])
+                for (int i = 0; i < p.tasks[t].ns; ++i) cnt[p.tasks[t].s_ev[i]] += p.tasks[t].s_inc[i];
+        }
+    }
+    p.segments = segs;
+    p.lmax = segs.empty() ? 0 : segs[0].lmax;
+    return MK_OK;
+}
+
+// ---- explicit graphs ----------------------------------------------------
+
+int plan_graph(const mk_graph_desc *g, const mk_target_desc *tgt, int num_workers, Plan &p) {
+    if (!g || g->num_ops <= 0 || !g->ops) return set_error(MK_ERR_INVALID, "empty graph");
+    p = Plan{};
+    p.kind = PLAN_GRAPH;
+    p.mode = tgt && tgt->mode == MK_MODE_PER_OP ? MK_MODE_PER_OP : MK_MODE_MEGAKERNEL;
+    p.num_workers = num_workers;
+    p.num_ops = g->num_ops;
+    for (int o = 0; o < g->num_ops; ++o)
+        for (int a = 0; a < 3; ++a)
+            if (g->ops[o].grid[a] <= 0) return set_error(MK_ERR_INVALID, "grid extents must be positive");
+    if (g->num_pubs > 0) {
+        // MegaRTP publications: ops in the given order, tasks in index order
+        std::vector<int> base(g->num_ops + 1, 0);
+        for (int o = 0; o < g->num_ops; ++o)
+            base[o + 1] = base[o] + g->ops[o].grid[0] * g->ops[o].grid[1] * g->ops[o].grid[2];
+        p.tasks.assign(base[g->num_ops], TaskRec{});
+        for (int o = 0; o < g->num_ops; ++o)
+            for (int i = base[o]; i < base[o + 1]; ++i) {
+                TaskRec &t = p.tasks[i];
+                t.opcode = MK_OP_COUNTER;
+                t.op_row = o;
+                int li = i - base[o];
+                t.bid[0] = li;
+                t.cost = g->ops[o].cost;
+            }
+        for (int k = 0; k < g->num_pubs; ++k) {
+            const mk_graph_pub &pb = g->pubs[k];
+            if (pb.prod < 0 || pb.prod >= g->num_ops || pb.num_pub <= 0 || pb.num_cons < 0 || pb.num_cons > 4)
+                return set_error(MK_ERR_INVALID, "bad publication");
+            int n_ev, thr;
+            if (pb.strategy == MK_PAIR_WHOLE) { n_ev = 1; thr = pb.num_pub; }
+            else if (pb.strategy == MK_PAIR_TILE) { n_ev = pb.num_pub; thr = 1; }
+            else if (pb.strategy == MK_PAIR_TILE_COVER || pb.strategy == MK_PAIR_TILE_REDUCE) {
+                if (pb.k <= 0 || pb.num_pub % pb.k) return set_error(MK_ERR_INVALID, "k must divide num_pub");
+                n_ev = pb.num_pub / pb.k;
+                thr = pb.k;
+            } else return set_error(MK_ERR_INVALID, "unknown strategy");
+            int first = (int)p.thresholds.size();
+            for (int e = 0; e < n_ev; ++e) p.thresholds.push_back(thr);
+            int per = pb.num_pub / n_ev;
+            for (int j = 0; j < pb.num_pub; ++j) {
+                TaskRec &t = p.tasks[base[pb.prod] + pb.first_pub + j];
+                if (t.ns >= MAX_SIGS) return set_error(MK_ERR_UNSUPPORTED, "more than 2 signals on a task");
+                t.s_ev[t.ns] = first + j / per;
+                t.s_inc[t.ns++] = 1;
+            }
+            for (int c = 0; c < pb.num_cons; ++c) {
+                int co = pb.cons[c];
+                int nc = base[co + 1] - base[co];
+                if (nc % n_ev) return set_error(MK_ERR_INVALID, "consumer tasks not divisible by events");
+                for (int i = 0; i < nc; ++i) {
+                    TaskRec &t = p.tasks[base[co] + i];
+                    if (t.nw >= MAX_WAITS) return set_error(MK_ERR_UNSUPPORTED, "more than 3 waits on a task");
+                    int ev = first + i / (nc / n_ev);
+                    t.w_ev[t.nw] = ev;
+                    t.w_thr[t.nw] = thr;
+                    t.w_off[t.nw++] = 0;
+                }
+            }
+        }
+    } else {
+        std::vector<OpDef> ops(g->num_ops);
+        for (int o = 0; o < g->num_ops; ++o) {
+            std::memcpy(ops[o].grid, g->ops[o].grid, sizeof(ops[o].grid));
+            int c = g->ops[o].cost;
+            ops[o].cost = [c](const int *) { return (int64_t)c; };
+        }
+        std::vector<EdgeDef> edges(g->num_edges);
+        for (int i = 0; i < g->num_edges; ++i) {
+            const mk_graph_edge &e = g->edges[i];
+            if (e.prod < 0 || e.cons < 0 || e.prod >= g->num_ops || e.cons >= g->num_ops || e.prod >= e.cons)
+                return set_error(MK_ERR_INVALID, "edges must go from an earlier op to a later one");
+            edges[i] = EdgeDef{e.prod, e.cons, {e.out_map[0], e.out_map[1], e.out_map[2]},
+                               {e.in_map[0], e.in_map[1], e.in_map[2]}};
+            for (int a = 0; a < 3; ++a)
+                if (e.out_map[a] >= MAXD || e.in_map[a] >= MAXD) return set_error(MK_ERR_INVALID, "map beyond 4 dims");
+        }
+        std::vector<RawTask> raw;
+        std::vector<RawEvent> evs;
+        int n_first;
+        int rc = build_tasks(ops, edges, raw, evs, n_first);
+        if (rc) return rc;
+        for (auto &e : evs) p.thresholds.push_back(e.ntrig);
+        p.tasks.resize(raw.size());
+        for (size_t i = 0; i < raw.size(); ++i) {
+            TaskRec &t = p.tasks[i];
+            t.opcode = MK_OP_COUNTER;
+            t.op_row = raw[i].op;
+            std::memcpy(t.bid, raw[i].bid, sizeof(t.bid));
+            t.cost = g->ops[raw[i].op].cost;
+            if (raw[i].dep >= 0) {
+                t.w_ev[0] = raw[i].dep;
+                t.w_thr[0] = evs[raw[i].dep].ntrig;
+                t.nw = 1;
+            }
+            if (raw[i].trig >= 0) {
+                t.s_ev[0] = raw[i].trig;
+                t.s_inc[0] = 1;
+                t.ns = 1;
+            }
+        }
+        for (auto &e : evs) p.events.push_back({e.ntrig, e.first, e.last});
+    }
+    p.op_kind.assign(g->num_ops, MK_OP_COUNTER);
+    p.op_layer.assign(g->num_ops, -1);
+    return finish_queues(p, g->round_robin != 0);
+}
+
+// ---- Llama-style decode step --------------------------------------------
+
+int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_desc *tgt, int num_workers,
+               int smem_per_cta, Plan &p) {
+    if (!m || !s || !tgt) return set_error(MK_ERR_INVALID, "null descriptor");
+    p = Plan{};
+    p.kind = PLAN_LLAMA;
+    p.model = *m;
+    p.mode = tgt->mode == MK_MODE_PER_OP ? MK_MODE_PER_OP : MK_MODE_MEGAKERNEL;
+    p.num_workers = num_workers;
+    const int L = m->layers, H = m->hidden, Hq = m->q_heads, Hkv = m->kv_heads, D = m->head_dim, F = m->ffn,
+              V = m->vocab, B = s->batch;
+    if (L <= 0 || H <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || F <= 0 || V <= 0 || B <= 0 || s->max_steps <= 0 ||
+        !s->seq_len0 || num_workers <= 0)
+        return set_error(MK_ERR_INVALID, "non-positive model or step size");
+    if (Hq % Hkv) return set_error(MK_ERR_INVALID, "q_heads must be a multiple of kv_heads");
+    const int G = Hq / Hkv;
+    if (B > 8) return set_error(MK_ERR_UNSUPPORTED, "batch above 8");
+    if (D != 64 && D != 128) return set_error(MK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (G > 8) return set_error(MK_ERR_UNSUPPORTED, "more than 8 q heads per kv head");
+    if (H % 8 || F % 8) return set_error(MK_ERR_UNSUPPORTED, "hidden and ffn must be multiples of 8");
+    p.B = B;
+    p.max_steps = s->max_steps;
+    p.smax = s->cache_slots;
+    p.capture = s->capture_hidden != 0;
+    p.seq0.assign(s->seq_len0, s->seq_len0 + B);
+    for (int b = 0; b < B; ++b) {
+        if (p.seq0[b] < 0) return set_error(MK_ERR_INVALID, "negative sequence length");
+        if ((int64_t)p.seq0[b] + s->max_steps > s->cache_slots)
+            return set_error(MK_ERR_INVALID, "cache_slots smaller than seq_len0 + max_steps");
+    }
+    auto clampi = [](int v, int lo, int hi) { return std::max(lo, std::min(hi, v)); };
+    auto pow2_floor = [](int v) { int r = 1; while (r * 2 <= v) r *= 2; return r; };
+    const int tile = 65536;
+    p.page_bytes = tgt->page_bytes > 0 ? tgt->page_bytes : 16384;
+    if (p.page_bytes % 128) return set_error(MK_ERR_INVALID, "page_bytes must be a multiple of 128");
+    int kn_qkv = tgt->rows_qkv > 0 ? tgt->rows_qkv : pow2_floor(clampi(tile / (2 * H), 1, 16));
+    int kn_o = tgt->rows_o > 0 ? tgt->rows_o : pow2_floor(clampi(tile / (2 * Hq * D), 1, 16));
+    int kn_up = tgt->rows_up > 0 ? tgt->rows_up : pow2_floor(clampi(tile / (4 * H), 1, 8));
+    int kn_kc = tgt->kchunk_down;
+    if (kn_kc <= 0) {
+        kn_kc = 8;
+        for (int c = 8; c <= std::min(F, 2048); c += 8)
+            if (F % c == 0) kn_kc = c;
+    }
+    int kn_dn = tgt->rows_down > 0 ? tgt->rows_down : pow2_floor(clampi(tile / (2 * kn_kc), 1, 16));
+    int kn_lm = tgt->rows_lm > 0 ? tgt->rows_lm : pow2_floor(clampi(tile / (2 * H), 1, 16));
+    int kn_T = tgt->attn_split > 0 ? tgt->attn_split : clampi(16384 / (2 * D), 16, 256);
+    p.rows_qkv = kn_qkv; p.rows_o = kn_o; p.rows_up = kn_up; p.rows_down = kn_dn; p.kchunk_down = kn_kc;
+    p.rows_lm = kn_lm; p.attn_split = kn_T;
+    const int rows_group = (G + 2) * D;
+    if (kn_qkv > MAX_TILE_ROWS || kn_o > MAX_TILE_ROWS || kn_dn > MAX_TILE_ROWS || kn_lm > MAX_TILE_ROWS ||
+        2 * kn_up > MAX_TILE_ROWS)
+        return set_error(MK_ERR_UNSUPPORTED, "tile rows above 16 (mlp-up: 8)");
+    if (D % kn_qkv) return set_error(MK_ERR_UNSUPPORTED, "rows_qkv must divide head_dim");
+    if (F % kn_up || F % kn_kc || kn_kc % 8) return set_error(MK_ERR_UNSUPPORTED, "rows_up / kchunk_down must divide ffn");
+    if (kn_T > 256 || kn_T < 1) return set_error(MK_ERR_UNSUPPORTED, "attn_split must be 1..256");
+    for (int K : {H, Hq * D, kn_kc}) {
+        if (2 * K > p.page_bytes) return set_error(MK_ERR_UNSUPPORTED, "a weight row does not fit one page");
+        if (B * ceil_div(K, 2048) > 8) return set_error(MK_ERR_UNSUPPORTED, "batch x K too large for register-held activations");
+    }
+    if (kn_T * D * 2 > p.page_bytes * 8) return set_error(MK_ERR_UNSUPPORTED, "attention split too long");
+    // shared memory budget
+    int kmax = std::max(std::max(H, Hq * D), kn_kc);
+    int attn_slot = (G * (D + 16) + 2 * D) * 4;
+    p.act_bytes = round_up(std::max(B * kmax * 4, attn_slot), 128);
+    const int maxb = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8;  // kernel batch template
+    int aux = round_up(std::max(red_bytes(maxb), attn_aux_bytes(G, kn_T, D)), 128);
+    int fixed = 2 * p.act_bytes + aux + MBAR_BYTES + CTRL_BYTES;
+    p.aux_bytes = aux;
+    p.num_pages = std::min(MAX_PAGES, (smem_per_cta - fixed) / p.page_bytes);
+    p.smem_bytes = fixed + p.num_pages * p.page_bytes;
+    // pages used by the largest instruction
+    auto pages_for = [&](int rows, int row_bytes) {
+        if (rows <= 0) return 0;
+        int rpp = p.page_bytes / row_bytes;
+        return ceil_div(rows, rpp);
+    };
+    int need = std::max({pages_for(kn_qkv, 2 * H), pages_for(kn_o, 2 * Hq * D), 2 * pages_for(kn_up, 2 * H),
+                         pages_for(kn_dn, 2 * kn_kc), pages_for(kn_lm, 2 * H), 2 * pages_for(kn_T, 2 * D)});
+    if (p.num_pages < std::max(2, need))
+        return set_error(MK_ERR_UNSUPPORTED, "shared memory too small for the page pool");
+
+    // ---- op list (topological): embed, per layer qkv attn o up down, lm
+    std::vector<int> nsplit(B);
+    for (int b = 0; b < B; ++b) nsplit[b] = ceil_div(p.seq0[b] + s->max_steps, kn_T);
+    int ns_max = *std::max_element(nsplit.begin(), nsplit.end());
+    p.nsplit_max = ns_max;
+    std::vector<int> seq0 = p.seq0;
+    const int max_steps = s->max_steps;
+    std::vector<OpDef> ops;
+    std::vector<EdgeDef> edges;
+    auto add_op = [&](int opcode, int layer, int gx, int gy, int gz) {
+        OpDef o;
+        o.opcode = opcode;
+        o.layer = layer;
+        o.grid[0] = gx; o.grid[1] = gy; o.grid[2] = gz;
+        ops.push_back(o);
+        return (int)ops.size() - 1;
+    };
+    auto rows_cost = [](int n_rows, int rows, int kdim) {
+        return [=](const int *b) { return (int64_t)std::min(rows, n_rows - b[0] * rows) * kdim * 2; };
+    };
+    int emb = add_op(MK_OP_EMBED, -1, 1, 1, 1);
+    ops[emb].cost = [=](const int *) { return (int64_t)B * H * 2; };
+    int prev = emb;
+    for (int l = 0; l < L; ++l) {
+        int q = add_op(MK_OP_QKV, l, Hkv, rows_group / kn_qkv, 1);
+        ops[q].cost = [=](const int *) { return (int64_t)kn_qkv * H * 2; };
+        int a = add_op(MK_OP_ATTN, l, Hkv, B, ns_max);
+        ops[a].exists = [nsplit](const int *b) { return b[2] < nsplit[b[1]]; };
+        ops[a].cost = [=](const int *b) {
+            int last = seq0[b[1]] + max_steps - 1;
+            int rows = std::max(0, std::min(kn_T, last - b[2] * kn_T));
+            return (int64_t)2 * D * 2 * rows;
+        };
+        int o = add_op(MK_OP_O, l, ceil_div(H, kn_o), 1, 1);
+        ops[o].cost = rows_cost(H, kn_o, Hq * D);
+        int u = add_op(MK_OP_UP, l, F / kn_up, 1, 1);
+        ops[u].cost = [=](const int *) { return (int64_t)2 * kn_up * H * 2; };
+        int d = add_op(MK_OP_DOWN, l, ceil_div(H, kn_dn), F / kn_kc, 1);
+        ops[d].cost = rows_cost(H, kn_dn, kn_kc);
+        if (prev == emb) edges.push_back({prev, q, {-1, -1, -1}, {-1, -1, -1}});
+        else edges.push_back({prev, q, {1, -1, -1}, {-1, -1, -1}});
+        edges.push_back({q, a, {1, 2, -1}, {1, 0, -1}});   // qkv [B, Hkv, rows]: group & row cuts vs batch & group
+        edges.push_back({a, o, {1, 0, -1}, {-1, -1, -1}});  // attn_out read whole; split axis reduces
+        edges.push_back({o, u, {1, -1, -1}, {-1, -1, -1}}); // h read whole
+        edges.push_back({u, d, {1, -1, -1}, {-1, 1, -1}});  // act [B, F]: tiles vs K chunks
+        prev = d;
+    }
+    int lm = add_op(MK_OP_LM, -1, ceil_div(V, kn_lm), 1, 1);
+    ops[lm].cost = rows_cost(V, kn_lm, H);
+    edges.push_back({prev, lm, {1, -1, -1}, {-1, -1, -1}});
+
+    std::vector<RawTask> raw;
+    std::vector<RawEvent> evs;
+    int n_first;
+    int rc = build_tasks(ops, edges, raw, evs, n_first);
+    if (rc) return rc;
+    // longest-first inside each successor range (stable), ranges in order
+    std::vector<int64_t> cost(raw.size());
+    for (size_t i = 0; i < raw.size(); ++i) cost[i] = ops[raw[i].op].cost(raw[i].bid);
+    std::vector<std::pair<int, int>> ranges{{0, n_first}};
+    for (auto &e : evs) ranges.push_back({e.first, e.last});
+    std::sort(ranges.begin(), ranges.end());
+    std::vector<int> order;
+    for (auto &r : ranges) {
+        std::vector<int> ids(r.second - r.first);
+        std::iota(ids.begin(), ids.end(), r.first);
+        std::stable_sort(ids.begin(), ids.end(), [&](int x, int y) { return cost[x] > cost[y]; });
+        order.insert(order.end(), ids.begin(), ids.end());
+    }
+    if ((int)order.size() != (int)raw.size()) return set_error(MK_ERR_INVALID, "task ranges do not cover the graph");
+    const int step_done = (int)evs.size();
+    for (auto &e : evs) p.thresholds.push_back(e.ntrig);
+    p.thresholds.push_back(0);
+    for (auto &e : evs) p.events.push_back({e.ntrig, e.first, e.last});
+    p.events.push_back({0, 0, n_first});
+    // operand rows = ops
+    p.num_ops = (int)ops.size();
+    for (auto &o : ops) {
+        p.op_kind.push_back(o.opcode);
+        p.op_layer.push_back(o.layer);
+    }
+    std::vector<int> first_task_of_op(ops.size(), -1);
+    p.tasks.reserve(order.size());
+    for (int old : order) {
+        const RawTask &r = raw[old];
+        const OpDef &op = ops[r.op];
+        TaskRec t;
+        t.opcode = op.opcode;
+        t.op_row = r.op;
+        t.layer = op.layer;
+        std::memcpy(t.bid, r.bid, sizeof(t.bid));
+        t.cost = cost[old];
+        if (r.dep >= 0) {
+            t.w_ev[t.nw] = r.dep; t.w_thr[t.nw] = evs[r.dep].ntrig; t.w_off[t.nw++] = 0;
+        }
+        if (r.trig >= 0) { t.s_ev[t.ns] = r.trig; t.s_inc[t.ns++] = 1; }
+        if (op.opcode == MK_OP_LM) {
+            t.s_ev[t.ns] = step_done; t.s_inc[t.ns++] = 1;
+            p.thresholds[step_done]++;
+        }
+        bool first_of_op = first_task_of_op[r.op] < 0;
+        if (first_of_op) first_task_of_op[r.op] = (int)p.tasks.size();
+        int32_t *pl = t.payload;
+        switch (op.opcode) {
+        case MK_OP_QKV: {
+            int g = r.bid[0], lr = r.bid[1] * kn_qkv;
+            pl[P_NROWS - W_P] = kn_qkv;
+            pl[P_K0 - W_P] = 0;
+            pl[P_KC - W_P] = H;
+            pl[P_KTOT - W_P] = H;
+            pl[P_OUT0 - W_P] = g * rows_group + lr;
+            if (lr < G * D) { pl[P_MAT - W_P] = 0; pl[P_ROW0 - W_P] = g * G * D + lr; }
+            else if (lr < (G + 1) * D) { pl[P_MAT - W_P] = 1; pl[P_ROW0 - W_P] = g * D + lr - G * D; }
+            else { pl[P_MAT - W_P] = 2; pl[P_ROW0 - W_P] = g * D + lr - (G + 1) * D; }
+            pl[P_SNAP - W_P] = (p.capture && op.layer > 0 && first_of_op) ? op.layer : 0;  // layer-1 residual
+            break;
+        }
+        case MK_OP_ATTN:
+            pl[P_G - W_P] = r.bid[0]; pl[P_B - W_P] = r.bid[1]; pl[P_SPLIT - W_P] = r.bid[2];
+            pl[P_T0 - W_P] = r.bid[2] * kn_T; pl[P_T - W_P] = kn_T; pl[P_NSPLIT - W_P] = nsplit[r.bid[1]];
+            pl[P_LAYER - W_P] = op.layer;
+            break;
+        case MK_OP_O:
+            pl[P_ROW0 - W_P] = r.bid[0] * kn_o; pl[P_NROWS - W_P] = std::min(kn_o, H - r.bid[0] * kn_o);
+            pl[P_K0 - W_P] = 0; pl[P_KC - W_P] = Hq * D; pl[P_KTOT - W_P] = Hq * D; pl[P_OUT0 - W_P] = r.bid[0] * kn_o;
+            break;
+        case MK_OP_UP:
+            pl[P_ROW0 - W_P] = r.bid[0] * kn_up; pl[P_NROWS - W_P] = kn_up;
+            pl[P_K0 - W_P] = 0; pl[P_KC - W_P] = H; pl[P_KTOT - W_P] = H; pl[P_OUT0 - W_P] = r.bid[0] * kn_up;
+            break;
+        case MK_OP_DOWN:
+            pl[P_ROW0 - W_P] = r.bid[0] * kn_dn; pl[P_NROWS - W_P] = std::min(kn_dn, H - r.bid[0] * kn_dn);
+            pl[P_K0 - W_P] = r.bid[1] * kn_kc; pl[P_KC - W_P] = kn_kc; pl[P_KTOT - W_P] = F;
+            pl[P_OUT0 - W_P] = r.bid[0] * kn_dn;
+            break;
+        case MK_OP_LM:
+            pl[P_ROW0 - W_P] = r.bid[0] * kn_lm; pl[P_NROWS - W_P] = std::min(kn_lm, V - r.bid[0] * kn_lm);
+            pl[P_K0 - W_P] = 0; pl[P_KC - W_P] = H; pl[P_KTOT - W_P] = H; pl[P_OUT0 - W_P] = r.bid[0] * kn_lm;
+            pl[P_SNAP - W_P] = (p.capture && first_of_op) ? L : 0;
+            break;
+        default:
+            break;
+        }
+        p.tasks.push_back(t);
+    }
+    for (auto &t : p.tasks)
+        if (t.opcode == MK_OP_EMBED) {
+            t.w_ev[t.nw] = step_done; t.w_thr[t.nw] = p.thresholds[step_done]; t.w_off[t.nw++] = -1;
+        }
+    // algorithmic bytes at step 0: weights once, KV read, KV append
+    int64_t weights = 0;
+    for (auto &t : p.tasks)
+        if (t.opcode != MK_OP_ATTN && t.opcode != MK_OP_EMBED) weights += t.cost;
+    weights += (int64_t)B * H * 2;  // embedding rows
+    int64_t kv_read = 0;
+    for (int b = 0; b < B; ++b) kv_read += (int64_t)2 * p.seq0[b] * Hkv * D * 2 * L;
+    int64_t kv_write = (int64_t)2 * B * Hkv * D * 2 * L;
+    int64_t norms = (int64_t)(2 * L + 1) * H * 2 + (m->qk_norm ? (int64_t)2 * L * D * 2 : 0);
+    p.alg_bytes = weights + kv_read + kv_write + norms;
+    return finish_queues(p, false);
+}
+
+}  // namespace mk

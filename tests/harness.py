@@ -1,0 +1,139 @@
+"""GPU-vs-oracle parity harness (test infrastructure; imports the oracle).
+
+Both sides receive the same seeded tensors: weights and caches are drawn on
+the GPU by ``synth`` and copied to the host for the oracle.  A checked step
+gives the oracle exactly the GPU's inputs for that step (token, KV cache
+contents before the step), then compares:
+
+* per-layer residual stream: err = max|h_gpu - h_ref| / max|h_ref|, bar 1e-2
+  (the normwise reading of "per-layer hidden-state max relative error");
+* logits (same normwise error) and the greedy argmax, taken by the oracle on
+  its logits rounded to fp32 (the GPU's precision), lowest index on ties;
+* the K/V entries the step appended, within one bf16 ulp.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+import torch
+
+from oracle import forward as orc
+from persistent_megakernel_decode_gb300 import runtime as rt
+from persistent_megakernel_decode_gb300 import synth
+
+HIDDEN_TOL = 1e-2
+
+
+def host_weights(w: Dict[str, object]) -> Dict[str, object]:
+    out = {}
+    for k, v in w.items():
+        out[k] = [synth.to_host_u16(t) for t in v] if isinstance(v, list) else synth.to_host_u16(v)
+    return out
+
+
+def oracle_shape(s: synth.ModelShape) -> orc.Shape:
+    return orc.Shape(s.L, s.H, s.Hq, s.Hkv, s.D, s.F, s.V, s.qk_norm, s.eps, s.theta)
+
+
+def normwise(a: np.ndarray, ref: np.ndarray) -> float:
+    return float(np.max(np.abs(a - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+@dataclass
+class StepReport:
+    step: int
+    hidden_err: List[float]
+    logits_err: float
+    argmax_gpu: List[int]
+    argmax_ref: List[int]
+    gaps: List[float]
+    kv_max_ulp: float
+
+
+@dataclass
+class ParityRun:
+    shape: synth.ModelShape
+    seq0: List[int]
+    steps: int
+    reports: List[StepReport] = field(default_factory=list)
+
+    def matches(self):
+        m = t = 0
+        for r in self.reports:
+            for a, b in zip(r.argmax_gpu, r.argmax_ref):
+                m += int(a == b)
+                t += 1
+        return m, t
+
+    def worst_hidden(self):
+        return max(max(r.hidden_err) for r in self.reports)
+
+
+def bf16_ulp_distance(a_u16: np.ndarray, b_u16: np.ndarray) -> float:
+    """Distance in bf16 ulps between two arrays of bf16 bit patterns."""
+    def ordered(u):
+        u = u.astype(np.int32)
+        return np.where(u & 0x8000, -(u & 0x7FFF), u)
+    return float(np.max(np.abs(ordered(a_u16) - ordered(b_u16)))) if a_u16.size else 0.0
+
+
+def run_parity(shape: synth.ModelShape, seq0: Sequence[int], steps: int, check_steps: Sequence[int],
+               seed: int = 0, teacher_forced: bool = True, nthreads: Optional[int] = None,
+               first_tokens: Optional[Sequence[int]] = None, **target) -> ParityRun:
+    """Run ``steps`` decode steps on the GPU; check the listed steps against the oracle.
+
+    teacher_forced: every step's token is the oracle's argmax of the previous
+    step (host-provided tokens); otherwise the GPU feeds its own argmax and the
+    oracle is given that token."""
+    B = len(seq0)
+    smax = max(seq0) + steps + 1
+    dev = torch.device("cuda:0")
+    w = synth.make_weights(shape, seed, device=dev)
+    kc, vc = synth.make_cache(shape, B, smax, seed + 100, device=dev)
+    hw = host_weights(w)
+    oshape = oracle_shape(shape)
+    sess = rt.Session(shape, w, kc, vc, seq0, steps, capture_hidden=True, **target)
+    g = torch.Generator().manual_seed(seed + 200)
+    toks = list(first_tokens) if first_tokens is not None else torch.randint(0, shape.V, (B,), generator=g).tolist()
+    sess.tokens[0] = torch.tensor(toks, dtype=torch.int32, device=dev)
+    run = ParityRun(shape, list(seq0), steps)
+    check = set(check_steps)
+    for s in range(steps):
+        pos = [seq0[b] + s for b in range(B)]
+        if s in check:
+            torch.cuda.synchronize()
+            k_before = synth.to_host_u16(kc).copy()
+            v_before = synth.to_host_u16(vc).copy()
+            if not teacher_forced and s > 0:
+                prev = sess.step_tokens(s - 1)
+                toks = [int(t) for t in prev]
+        if teacher_forced:
+            sess.tokens[s] = torch.tensor(toks, dtype=torch.int32, device=dev)
+        sess.run(s, 1, host_tokens=teacher_forced)
+        sess.sync()
+        if s in check:
+            logits_ref, hidden_ref, am_ref = orc.decode_step(oshape, hw, k_before, v_before, pos, toks,
+                                                             nthreads=nthreads)
+            hid = sess.hidden.cpu().numpy().astype(np.float64)
+            lg = sess.logits.cpu().numpy().astype(np.float64)
+            am = [int(x) for x in sess.step_tokens(s)]
+            herr = [normwise(hid[l], hidden_ref[l]) for l in range(shape.L)]
+            lerr = normwise(lg, logits_ref)
+            gaps = []
+            for b in range(B):
+                srt = np.sort(logits_ref[b].astype(np.float32))
+                gaps.append(float(srt[-1] - srt[-2]))
+            kg, vg = synth.to_host_u16(kc), synth.to_host_u16(vc)
+            ulp = 0.0
+            for b in range(B):
+                ulp = max(ulp, bf16_ulp_distance(kg[:, b, :, pos[b]], k_before[:, b, :, pos[b]]),
+                          bf16_ulp_distance(vg[:, b, :, pos[b]], v_before[:, b, :, pos[b]]))
+            run.reports.append(StepReport(s, herr, lerr, am, [int(x) for x in am_ref], gaps, ulp))
+            if teacher_forced:
+                toks = [int(x) for x in am_ref]
+        elif teacher_forced:
+            # unchecked step under teacher forcing: follow the GPU's own argmax
+            toks = [int(x) for x in sess.step_tokens(s)]
+    return run

@@ -1,0 +1,143 @@
+"""The CUDA path through the C ABI on a GPU: protocol checks and parity with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import plans
+from persistent_megakernel_decode_gb300 import runtime as rt
+from persistent_megakernel_decode_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from persistent_megakernel_decode_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def _fabg():
+    x = (0, -1, -1)
+    ops = [dict(grid=(4, 1, 1)), dict(grid=(4, 1, 1)), dict(grid=(2, 1, 1)), dict(grid=(4, 1, 1))]
+    edges = [dict(prod=0, cons=1, out_map=x, in_map=x), dict(prod=0, cons=2, out_map=x, in_map=x),
+             dict(prod=1, cons=3, out_map=x, in_map=x), dict(prod=2, cons=3, out_map=x, in_map=x)]
+    return ops, edges
+
+
+@pytest.mark.parametrize("workers", [1, 3, 8])
+def test_counter_graph_final_counters_bit_exact(workers):
+    ops, edges = _fabg()
+    p = rt.Plan.graph(ops, edges, num_sms=workers, smem_per_cta=0)
+    s = rt.GraphSession(p)
+    th = p.export()[2]
+    s.run(0, 5)
+    rec = s.sync()
+    assert rec.code == 0
+    assert s.counters().tolist() == [5 * int(t) for t in th]
+    s.run(5, 2)      # counters carry on across launches (epochs)
+    assert s.sync().code == 0
+    assert s.counters().tolist() == [7 * int(t) for t in th]
+
+
+def test_counter_graph_megartp_plan_on_device():
+    counts = plans.GLM_TILE_COUNTS
+    names = list(counts)
+    ix = {n: i for i, n in enumerate(names)}
+    pubs = [dict(prod=ix["A0"], num_pub=16, strategy=rt.PAIR_WHOLE, cons=[ix["B0"], ix["B1"]]),
+            dict(prod=ix["A0"], num_pub=16, strategy=rt.PAIR_WHOLE, cons=[ix["C0"]]),
+            dict(prod=ix["B0"], first_pub=68, num_pub=16, strategy=rt.PAIR_WHOLE, cons=[ix["D0"], ix["D1"]]),
+            dict(prod=ix["C0"], num_pub=48, strategy=rt.PAIR_TILE_REDUCE, k=48, cons=[ix["D1"]]),
+            dict(prod=ix["D0"], num_pub=128, strategy=rt.PAIR_TILE_COVER, k=2, cons=[ix["D2"]]),
+            dict(prod=ix["D1"], first_pub=96, num_pub=32, strategy=rt.PAIR_WHOLE, cons=[ix["E1"]]),
+            dict(prod=ix["B1"], first_pub=7, num_pub=1, strategy=rt.PAIR_WHOLE, cons=[ix["E1"]])]
+    p = rt.Plan.graph([dict(grid=(counts[n], 1, 1)) for n in names], pubs=pubs, round_robin=True)
+    s = rt.GraphSession(p)
+    s.run(0, 3)
+    assert s.sync().code == 0
+    assert s.counters().tolist() == [3 * int(t) for t in p.export()[2]]
+
+
+def test_wait_that_never_completes_returns_timeout():
+    """Running step 1 on fresh counters: its consumers wait for 2x thresholds that
+    only 1x ever arrives.  The kernel must give up within its budget, record the
+    wait and return; the context stays usable for a normal run afterwards."""
+    ops, edges = _fabg()
+    p = rt.Plan.graph(ops, edges, num_sms=4, smem_per_cta=0)
+    s = rt.GraphSession(p)
+    s.run(1, 1, timeout_ns=20_000_000)
+    rec = s.sync()
+    assert rec.code == rt.MK_ERR_TIMEOUT
+    assert rec.role == 1 and rec.event >= 0 and rec.observed < rec.needed
+    s.run(0, 2)
+    assert s.sync().code == 0
+    assert s.counters().tolist() == [2 * int(t) for t in p.export()[2]]
+
+
+def _check_run(run, hidden_tol=1e-2):
+    for r in run.reports:
+        assert max(r.hidden_err) <= hidden_tol, (r.step, r.hidden_err)
+        assert r.logits_err <= hidden_tol, (r.step, r.logits_err)
+        assert r.kv_max_ulp <= 1, (r.step, r.kv_max_ulp)
+
+
+def test_tiny_parity_teacher_forced_all_steps():
+    from harness import run_parity
+    w = synth.WORKLOADS["tiny"]
+    run = run_parity(w.shape, [w.seq_len] * w.batch, w.steps, range(w.steps))
+    _check_run(run)
+    m, t = run.matches()
+    assert m == t, [(r.argmax_gpu, r.argmax_ref, r.gaps) for r in run.reports]
+
+
+def test_tiny_parity_ragged_batch_small_tiles_few_workers():
+    """Several tiles per op, ragged last tiles, splits that start empty and fill
+    as the sequences grow, 5 workers."""
+    from harness import run_parity
+    shape = synth.TINY
+    run = run_parity(shape, [0, 31, 64, 100], 6, range(6), num_sms=5, rows_qkv=8, rows_o=12, rows_lm=12,
+                     rows_down=12, attn_split=32)
+    _check_run(run)
+    m, t = run.matches()
+    assert m >= 0.99 * t
+
+
+def test_tiny_parity_per_op_baseline_mode():
+    from harness import run_parity
+    run = run_parity(synth.TINY, [64], 3, range(3), mode=rt.MODE_PER_OP)
+    _check_run(run)
+
+
+def test_tiny_gpu_fed_argmax_chain():
+    """Tokens fed back on the device (no host round trip) across 8 steps."""
+    from harness import run_parity
+    run = run_parity(synth.TINY, [64, 10], 8, [0, 3, 7], teacher_forced=False)
+    _check_run(run)
+    m, t = run.matches()
+    assert m == t
+
+
+def test_poisoned_activation_buffers_are_overwritten_before_use():
+    """Fill the workspace activations with NaN before every step: every value an
+    instruction reads must have been written in this step, after its wait."""
+    from harness import host_weights, normwise, oracle_shape
+    from oracle import forward as orc
+    shape = synth.TINY
+    dev = torch.device("cuda:0")
+    w = synth.make_weights(shape, 5, device=dev)
+    kc, vc = synth.make_cache(shape, 1, 80, 105, device=dev)
+    hw = host_weights(w)
+    kh, vh = synth.to_host_u16(kc).copy(), synth.to_host_u16(vc).copy()
+    sess = rt.Session(shape, w, kc, vc, [64], 4, capture_hidden=True)
+    info = sess.plan.info()
+    for s in range(4):
+        sess.tokens[s] = 17 + s
+        ws = sess.workspace
+        # poison everything after the operand table (activations, partials)
+        lo = sess.ws_ptr - ws.data_ptr() + info["scratch_offset"]
+        n = (ws.numel() - lo) // 4
+        ws[lo:lo + 4 * n] = torch.full((n,), float("nan"), device=dev).view(torch.uint8)
+        sess.run(s, 1, host_tokens=True)
+        sess.sync()
+        lref, href, _ = orc.decode_step(oracle_shape(shape), hw, kh, vh, [64 + s], [17 + s])
+        assert normwise(sess.logits.cpu().numpy().astype(np.float64), lref) < 1e-2

@@ -1,0 +1,177 @@
+"""libmk host side on CPU: exported symbols, and the C++ planner against the
+oracle's independent statement of the same rules -- bit for bit."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+from oracle import plans, rules, sim
+from persistent_megakernel_decode_gb300 import runtime as rt
+from persistent_megakernel_decode_gb300 import synth
+
+GB300 = dict(num_sms=152, smem_per_cta=232448)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from persistent_megakernel_decode_gb300 import build
+    build.build()
+
+
+def test_library_exports_every_declared_function():
+    hdr = open(os.path.join(ROOT, "include", "mk.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    names = set(re.findall(r"\b(mk_[a-z_]+)\s*\(", hdr))
+    assert names == set(rt.EXPORTED)
+    lib = rt.load()
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _oracle_knobs(info):
+    return plans.Knobs(rows_qkv=info["rows_qkv"], rows_o=info["rows_o"], rows_up=info["rows_up"],
+                       rows_down=info["rows_down"], kchunk_down=info["kchunk_down"], rows_lm=info["rows_lm"],
+                       attn_split=info["attn_split"])
+
+
+def _compare(shape, B, seq0, steps, workers=152, **kn):
+    p = rt.Plan.llama(shape, B, seq0, steps, max(seq0) + steps + 3, num_sms=workers, smem_per_cta=232448, **kn)
+    info = p.info()
+    q, ids, th, tasks = p.export()
+    osh = plans.LlamaShape(shape.L, shape.H, shape.Hq, shape.Hkv, shape.D, shape.F, shape.V)
+    op = plans.llama_step_plan(osh, _oracle_knobs(info), B, seq0, steps, workers)
+    assert info["num_tasks"] == len(op.tasks)
+    assert list(th) == op.thresholds
+    for i, t in enumerate(op.tasks):
+        r = tasks[i]
+        assert rt.OP_NAMES[r[0]] == t.kind, i
+        assert (r[1], r[2], r[3], r[4], r[5]) == (t.layer, *t.bid, t.cost), i
+        assert [(r[7 + 3 * k], r[8 + 3 * k], r[9 + 3 * k]) for k in range(r[6])] == list(t.waits), i
+        assert [(r[17 + 2 * k], r[18 + 2 * k]) for k in range(r[16])] == list(t.signals), i
+    assert info["lmax"] == op.lmax
+    assert ids.tolist() == op.queues
+    # instruction words carry the same waits/signals as the task table
+    for w in range(ids.shape[0]):
+        for s in range(ids.shape[1]):
+            t = ids[w, s]
+            if t < 0:
+                assert not q[w, s].any()
+            else:
+                assert q[w, s, 0] == tasks[t][0] and q[w, s, 3] == t
+    return p, op
+
+
+def test_planner_matches_oracle_tiny():
+    _compare(synth.TINY, 1, [64], 8)
+
+
+def test_planner_matches_oracle_tiny_ragged_batch():
+    _compare(synth.TINY, 3, [5, 64, 130], 4, workers=7, attn_split=32, rows_qkv=8, rows_o=4, rows_lm=8)
+
+
+def test_planner_matches_oracle_llama1b_b1():
+    p, op = _compare(synth.LLAMA_1B, 1, [1024], 128)
+    assert p.info()["num_events"] == 16 * 15 + 2
+
+
+def test_planner_matches_oracle_llama1b_b8_variable_lengths():
+    w = synth.WORKLOADS["llama1b_b8"]
+    _compare(synth.LLAMA_1B, 8, synth.seq_lengths(w), 64)
+
+
+def test_planner_matches_oracle_qwen3_8b_b1():
+    _compare(synth.QWEN3_8B, 1, [2048], 32, workers=148)
+
+
+def test_planner_queue_simulates_over_steps():
+    p = rt.Plan.llama(synth.TINY, 2, [3, 70], 5, 80, **GB300)
+    q, ids, th, tasks = p.export()
+    waits = {i: [(r[7 + 3 * k], r[8 + 3 * k], r[9 + 3 * k]) for k in range(r[6])] for i, r in enumerate(tasks)}
+    sigs = {i: [(r[17 + 2 * k], r[18 + 2 * k]) for k in range(r[16])] for i, r in enumerate(tasks)}
+    res = sim.deadlock_check(ids.tolist(), waits, sigs, len(th), steps=5)
+    assert res.ok and res.counters == rules.expected_counters(th.tolist(), 5)
+
+
+def test_graph_plan_fork_join_example():
+    ops = [dict(grid=(4, 1, 1)), dict(grid=(4, 1, 1)), dict(grid=(2, 1, 1)), dict(grid=(4, 1, 1))]
+    x = (0, -1, -1)
+    edges = [dict(prod=0, cons=1, out_map=x, in_map=x), dict(prod=0, cons=2, out_map=x, in_map=x),
+             dict(prod=1, cons=3, out_map=x, in_map=x), dict(prod=2, cons=3, out_map=x, in_map=x)]
+    p = rt.Plan.graph(ops, edges, num_sms=3, smem_per_cta=65536)
+    _, ids, th, tasks = p.export()
+    g = rules.build_task_graph([rules.Op(n, tuple(o["grid"])) for n, o in zip("FABG", ops)],
+                               [rules.Edge("FABG"[e["prod"]], "FABG"[e["cons"]], x, x) for e in edges])
+    assert th.tolist() == [e.num_triggers for e in g.events] == [2, 2, 3, 3]
+    for i, t in enumerate(g.tasks):
+        r = tasks[i]
+        assert "FABG"[r[21]] == t.op and r[2] == t.bid[0]
+        assert (r[7] if r[6] else None) == t.dependent_event
+        assert (r[17] if r[16] else None) == t.trigger_event
+
+
+def test_graph_plan_gcd_examples():
+    for cons, events in ((128, 128), (64, 64), (1, 1), (127, 1)):
+        p = rt.Plan.graph([dict(grid=(128, 1, 1)), dict(grid=(cons, 1, 1))],
+                          [dict(prod=0, cons=1, out_map=(0, -1, -1), in_map=(0, -1, -1))], num_sms=16,
+                          smem_per_cta=65536)
+        assert p.info()["num_events"] == events
+
+
+def test_graph_plan_megartp_glm():
+    """MegaRTP article: 732 tile tasks, 70 events, [148, 5, 32] queue, 8-op table of 1024 B."""
+    counts = plans.GLM_TILE_COUNTS
+    names = list(counts)
+    ops = [dict(grid=(counts[n], 1, 1)) for n in names]
+    ix = {n: i for i, n in enumerate(names)}
+    pubs = [dict(prod=ix["A0"], num_pub=16, strategy=rt.PAIR_WHOLE, cons=[ix["B0"], ix["B1"]]),
+            dict(prod=ix["A0"], num_pub=16, strategy=rt.PAIR_WHOLE, cons=[ix["C0"]]),
+            dict(prod=ix["B0"], first_pub=68, num_pub=16, strategy=rt.PAIR_WHOLE, cons=[ix["D0"], ix["D1"]]),
+            dict(prod=ix["C0"], num_pub=48, strategy=rt.PAIR_TILE_REDUCE, k=48, cons=[ix["D1"]]),
+            dict(prod=ix["D0"], num_pub=128, strategy=rt.PAIR_TILE_COVER, k=2, cons=[ix["D2"]]),
+            dict(prod=ix["D1"], first_pub=96, num_pub=32, strategy=rt.PAIR_WHOLE, cons=[ix["E1"]]),
+            dict(prod=ix["B1"], first_pub=7, num_pub=1, strategy=rt.PAIR_WHOLE, cons=[ix["E1"]])]
+    p = rt.Plan.graph(ops, pubs=pubs, round_robin=True, num_sms=148, smem_per_cta=232448)
+    info = p.info()
+    q, ids, th, tasks = p.export()
+    ref = plans.megartp_glm_plan(148)
+    assert info["num_tasks"] == 732 and info["num_events"] == 70
+    assert list(q.shape) == [148, 5, 32]
+    assert th.tolist() == ref["thresholds"]
+    assert ids.tolist() == ref["queues"]
+    assert info["num_ops"] * 16 * 8 == 1024
+    for i in range(732):
+        r = tasks[i]
+        assert [(r[7 + 3 * k], r[8 + 3 * k]) for k in range(r[6])] == ref["waits"][i]
+        assert [(r[17 + 2 * k], r[18 + 2 * k]) for k in range(r[16])] == ref["signals"][i]
+
+
+def test_per_op_mode_segments():
+    p = rt.Plan.llama(synth.TINY, 1, [64], 2, 80, mode=rt.MODE_PER_OP, **GB300)
+    info = p.info()
+    assert info["num_launches"] == info["num_ops"] == 2 + 5 * synth.TINY.L
+    _, ids, th, tasks = p.export()
+    got = sorted(int(t) for t in ids if t >= 0)
+    assert got == list(range(info["num_tasks"]))
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(batch=9), rt.MK_ERR_UNSUPPORTED),
+    (dict(cache_slots=10), rt.MK_ERR_INVALID),
+    (dict(rows_qkv=24), rt.MK_ERR_UNSUPPORTED),
+    (dict(smem_per_cta=40000), rt.MK_ERR_UNSUPPORTED),
+])
+def test_planner_rejects(bad, code):
+    B = bad.pop("batch", 1)
+    cs = bad.pop("cache_slots", 80)
+    tgt = dict(GB300)
+    tgt.update(bad)
+    with pytest.raises(rt.MkError) as e:
+        rt.Plan.llama(synth.TINY, B, [64] * B, 8, cs, **tgt)
+    assert e.value.code == code
+
+
+def test_argmax_key_decoding():
+    assert rt.load().mk_argmax_index(0xFFFFFFFF) == 0
+    assert rt.load().mk_argmax_index((123 << 32) | (0xFFFFFFFF - 77)) == 77
