@@ -9,7 +9,9 @@ contents before the step), then compares:
   (the normwise reading of "per-layer hidden-state max relative error");
 * logits (same normwise error) and the greedy argmax, taken by the oracle on
   its logits rounded to fp32 (the GPU's precision), lowest index on ties;
-* the K/V entries the step appended, within one bf16 ulp.
+* the K/V entries the step appended: normwise error per (layer, sequence)
+  over the decoded bf16 values (the same 1e-2 bar; single elements can sit
+  several bf16 ulps apart where RoPE's a*cos - b*sin cancels).
 """
 from __future__ import annotations
 
@@ -49,7 +51,7 @@ class StepReport:
     argmax_gpu: List[int]
     argmax_ref: List[int]
     gaps: List[float]
-    kv_max_ulp: float
+    kv_err: float
 
 
 @dataclass
@@ -126,11 +128,13 @@ def run_parity(shape: synth.ModelShape, seq0: Sequence[int], steps: int, check_s
                 srt = np.sort(logits_ref[b].astype(np.float32))
                 gaps.append(float(srt[-1] - srt[-2]))
             kg, vg = synth.to_host_u16(kc), synth.to_host_u16(vc)
-            ulp = 0.0
+            kv = 0.0
             for b in range(B):
-                ulp = max(ulp, bf16_ulp_distance(kg[:, b, :, pos[b]], k_before[:, b, :, pos[b]]),
-                          bf16_ulp_distance(vg[:, b, :, pos[b]], v_before[:, b, :, pos[b]]))
-            run.reports.append(StepReport(s, herr, lerr, am, [int(x) for x in am_ref], gaps, ulp))
+                for l in range(shape.L):
+                    for got, ref in ((kg, k_before), (vg, v_before)):
+                        kv = max(kv, normwise(orc.bf16_to_f64(got[l, b, :, pos[b]]),
+                                              orc.bf16_to_f64(ref[l, b, :, pos[b]])))
+            run.reports.append(StepReport(s, herr, lerr, am, [int(x) for x in am_ref], gaps, kv))
             if teacher_forced:
                 toks = [int(x) for x in am_ref]
         elif teacher_forced:

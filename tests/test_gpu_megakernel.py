@@ -78,7 +78,7 @@ def _check_run(run, hidden_tol=1e-2):
     for r in run.reports:
         assert max(r.hidden_err) <= hidden_tol, (r.step, r.hidden_err)
         assert r.logits_err <= hidden_tol, (r.step, r.logits_err)
-        assert r.kv_max_ulp <= 1, (r.step, r.kv_max_ulp)
+        assert r.kv_err <= hidden_tol, (r.step, r.kv_err)
 
 
 def test_tiny_parity_teacher_forced_all_steps():
