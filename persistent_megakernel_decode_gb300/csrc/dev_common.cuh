@@ -1,0 +1,328 @@
+// Device-side building blocks of the interpreter: PTX wrappers (mbarrier,
+// bulk TMA copy, acquire/release counters), the shared-memory map, bounded
+// waits with the abort protocol, and warp-distributed instruction decoding.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+#define DEV __device__ __forceinline__
+constexpr unsigned FULL = 0xffffffffu;
+
+// ---------------------------------------------------------------- PTX helpers
+DEV uint32_t saddr(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+DEV uint64_t gtimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+DEV uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+DEV uint32_t ld_relaxed(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+DEV void red_release_add(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+DEV uint32_t atom_acqrel_add(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+DEV void mbar_init(uint64_t *b, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(n) : "memory");
+}
+DEV void mbar_arrive(uint64_t *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+DEV void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+DEV bool mbar_test(uint64_t *b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(saddr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Weight and cache rows are read once per step: evict-first keeps them from
+// displacing activations, counters and the queue in L2.
+DEV uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            saddr(dst)),
+        "l"(src), "r"(bytes), "r"(saddr(bar)), "l"(pol)
+        : "memory");
+}
+DEV void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p)); }
+
+DEV void bf16x8(uint4 w, float f[8]) {
+    f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xffff0000u);
+    f[2] = __uint_as_float(w.y << 16); f[3] = __uint_as_float(w.y & 0xffff0000u);
+    f[4] = __uint_as_float(w.z << 16); f[5] = __uint_as_float(w.z & 0xffff0000u);
+    f[6] = __uint_as_float(w.w << 16); f[7] = __uint_as_float(w.w & 0xffff0000u);
+}
+DEV float bf16_at(const uint16_t *p, size_t i) { return __uint_as_float((uint32_t)p[i] << 16); }
+DEV float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+DEV float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+    return v;
+}
+DEV float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+    return v;
+}
+DEV uint64_t argmax_key(float v, int idx) {
+    if (v == 0.0f) v = 0.0f;  // -0 and +0 compare equal
+    uint32_t u = __float_as_uint(v);
+    uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((uint64_t)ord << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)idx);
+}
+
+// Transposed butterfly: V partial sums per lane -> full warp sums.  After the
+// call, for V >= 32 lane l holds sums of indices l*(V/32) + j in v[j]; for
+// V < 32 it holds the sum of index l / (32/V) in v[0].  V - 1 + (5 - log2 V)
+// shuffles instead of 5 V.
+template <int N, int OFF>
+struct Bfly {
+    template <int V>
+    DEV static void run(float (&v)[V], int lane) {
+        if constexpr (OFF > 0) {
+            if constexpr (N >= 2) {
+                constexpr int H = N / 2;
+                const bool up = (lane & OFF) != 0;
+#pragma unroll
+                for (int i = 0; i < H; ++i) {
+                    const float send = up ? v[i] : v[i + H];
+                    const float keep = up ? v[i + H] : v[i];
+                    v[i] = keep + __shfl_xor_sync(FULL, send, OFF);
+                }
+                Bfly<H, OFF / 2>::run(v, lane);
+            } else {
+                v[0] += __shfl_xor_sync(FULL, v[0], OFF);
+                Bfly<1, OFF / 2>::run(v, lane);
+            }
+        }
+    }
+};
+
+// ---------------------------------------------------------------- shared state
+struct Smem {
+    uint8_t *act[2];
+    uint8_t *pages;
+    float *aux;
+    uint64_t *full, *empty, *act_full, *act_empty;
+    uint64_t *cbar;      // consumer-group barrier (8 warp arrivals per phase)
+    volatile int *ctrl;  // [0] abort, [1..2] slot flags, [3] attention: last split
+};
+
+constexpr int SLOT_FRESH = 1;
+
+DEV void raise_error(const KParams &P, const Smem &S, int code, int slot, int event, uint32_t obs, uint32_t need,
+                     int opc, int role) {
+    if (atomicCAS(&P.err[E_CODE], 0u, (uint32_t)code) == 0u) {
+        P.err[E_WORKER] = blockIdx.x;
+        P.err[E_SLOT] = (uint32_t)slot;
+        P.err[E_EVENT] = (uint32_t)event;
+        P.err[E_OBSERVED] = obs;
+        P.err[E_NEEDED] = need;
+        P.err[E_OPCODE] = (uint32_t)opc;
+        P.err[E_ROLE] = (uint32_t)role;
+    }
+    atomicExch(&P.err[E_ABORT], 1u);
+    S.ctrl[0] = 1;
+}
+
+DEV bool aborted(const KParams &P, const Smem &S) {
+    if (S.ctrl[0]) return true;
+    if (ld_relaxed(&P.err[E_ABORT])) {
+        S.ctrl[0] = 1;
+        return true;
+    }
+    return false;
+}
+
+// Whole-warp bounded wait on an mbarrier phase; uniform result, false = abort.
+DEV bool warp_wait_bar(const KParams &P, const Smem &S, uint64_t *bar, uint32_t parity, int role, int slot, int opc) {
+    const int lane = threadIdx.x & 31;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (__all_sync(FULL, mbar_test(bar, parity))) return true;
+        if ((it & 15) == 15) {
+            int stop = 0;
+            if (lane == 0) {
+                uint64_t now = gtimer();
+                if (t0 == 0) t0 = now;
+                if (aborted(P, S)) stop = 1;
+                else if (now - t0 > P.timeout_ns) {
+                    raise_error(P, S, MK_ERR_TIMEOUT, slot, -1, 0, parity, opc, role);
+                    stop = 1;
+                }
+            }
+            if (__shfl_sync(FULL, stop, 0)) return false;
+        }
+    }
+}
+
+// Whole-warp bounded wait for counter >= target (acquire on every poll).
+DEV bool warp_wait_counter(const KParams &P, const Smem &S, int ev, uint32_t target, int slot, int opc) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t *c = P.counters + ev;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t v = ld_acquire(c);
+        if (__all_sync(FULL, v >= target)) return true;
+        if ((it & 15) == 15) {
+            int stop = 0;
+            if (lane == 0) {
+                uint64_t now = gtimer();
+                if (t0 == 0) t0 = now;
+                if (aborted(P, S)) stop = 1;
+                else if (now - t0 > P.timeout_ns) {
+                    raise_error(P, S, MK_ERR_TIMEOUT, slot, ev, v, target, opc, 1);
+                    stop = 1;
+                }
+            }
+            if (__shfl_sync(FULL, stop, 0)) return false;
+        }
+    }
+}
+
+// Barrier of the 8 consumer warps on an mbarrier: each warp reconverges,
+// lane 0 arrives, the warp waits for the phase with the same bounded wait as
+// every other wait (a lost arrival becomes a recorded timeout, not a hang).
+// `phase` counts the barrier uses of this warp (uniform across the warp).
+DEV void consumer_sync(const KParams &P, const Smem &S, uint32_t &phase, bool &ab, int slot) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(S.cbar);
+    if (!ab) ab = !warp_wait_bar(P, S, S.cbar, phase & 1, 3, slot, -1);
+    ++phase;
+}
+
+DEV bool cta_aborting(const Smem &S) { return __shfl_sync(FULL, (int)S.ctrl[0], 0) != 0; }
+
+// ---------------------------------------------------------------- instruction decoding
+// A warp holds one instruction: lane k keeps word k; lanes 0..15 keep the 16
+// operand-table slots of its op row, cached while consecutive instructions
+// share the row.  Fields are read with shuffles (no repeated global loads).
+struct WIns {
+    int w = 0;
+    uint64_t orow = 0;
+    int row = -1;
+};
+
+DEV int F(const WIns &I, int k) { return __shfl_sync(FULL, I.w, k); }
+DEV uint64_t PTR(const WIns &I, int k) {
+    const uint32_t lo = __shfl_sync(FULL, (uint32_t)I.orow, k);
+    const uint32_t hi = __shfl_sync(FULL, (uint32_t)(I.orow >> 32), k);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+DEV void fetch(WIns &I, const KParams &P, const int32_t *ins) {
+    const int lane = threadIdx.x & 31;
+    I.w = __ldg(ins + lane);
+    const int opc = __shfl_sync(FULL, I.w, W_OPC);
+    const int row = __shfl_sync(FULL, I.w, W_ROW);
+    if (opc != MK_OP_NOOP && row != I.row && row >= 0 && row < P.num_ops) {
+        I.orow = lane < N_SLOTS ? __ldg(P.optab + (size_t)row * N_SLOTS + lane) : 0ull;
+        I.row = row;
+    }
+}
+
+// Warp-uniform sanity checks of one instruction against the launch.
+DEV bool ins_valid(const KParams &P, const WIns &I) {
+    const int opc = F(I, W_OPC);
+    if (opc < 0 || opc >= MK_NUM_OPCODES) return false;
+    if (opc == MK_OP_NOOP) return true;
+    const int row = F(I, W_ROW);
+    if (row < 0 || row >= P.num_ops) return false;
+    const int cnt = F(I, W_CNT);
+    const int nw = cnt & 0xff, ns = (cnt >> 8) & 0xff;
+    if (nw > MAX_WAITS || ns > MAX_SIGS) return false;
+    for (int i = 0; i < nw; ++i)
+        if ((int)((uint32_t)F(I, W_WAIT + 2 * i) & ~WAIT_PREV_EPOCH) >= P.num_events) return false;
+    for (int i = 0; i < ns; ++i)
+        if ((uint32_t)F(I, W_SIG + 2 * i) >= (uint32_t)P.num_events) return false;
+    if (opc >= MK_OP_QKV && opc != MK_OP_ATTN) {
+        const int nrows = F(I, P_NROWS), kc = F(I, P_KC);
+        const int rmax = P.B > 4 ? 8 : MAX_TILE_ROWS;
+        if (nrows <= 0 || (opc == MK_OP_UP ? 2 * nrows : nrows) > rmax) return false;
+        if (kc <= 0 || kc % 8 || 2 * kc > P.page_bytes || kc * P.B * 4 > P.act_bytes) return false;
+    }
+    if (opc == MK_OP_ATTN) {
+        const int T = F(I, P_T);
+        if (T <= 0 || T > 256 || F(I, P_B) >= P.B || F(I, P_G) >= P.Hkv || F(I, P_SPLIT) >= P.nsplit_max) return false;
+    }
+    return true;
+}
+
+struct Seg {
+    const uint8_t *src;
+    int rows;
+    int row_bytes;
+    long long stride;
+};
+
+DEV int attn_pos(const KParams &P, const WIns &I) {
+    const int32_t *seq0 = reinterpret_cast<const int32_t *>(PTR(I, S_AT_SEQ0));
+    return __ldg(seq0 + F(I, P_B)) + P.step;
+}
+DEV int attn_cached_rows(const WIns &I, int pos) { return max(0, min(F(I, P_T), pos - F(I, P_T0))); }
+
+// Weight / cache rows streamed by the loader for one instruction.  Loader and
+// consumers derive the same segments and walk the same page ring.
+DEV int describe(const KParams &P, const WIns &I, Seg &s0, Seg &s1) {
+    const int opc = F(I, W_OPC);
+    if (opc == MK_OP_QKV || opc == MK_OP_O || opc == MK_OP_DOWN || opc == MK_OP_LM || opc == MK_OP_UP) {
+        const long long ktot = F(I, P_KTOT);
+        const long long off = ((long long)F(I, P_ROW0) * ktot + F(I, P_K0)) * 2;
+        const int slot = opc == MK_OP_QKV ? S_QKV_WQ + F(I, P_MAT)
+                       : opc == MK_OP_O   ? S_O_W
+                       : opc == MK_OP_DOWN ? S_DN_W
+                       : opc == MK_OP_LM  ? S_LM_W
+                                          : S_UP_WG;
+        s0.src = reinterpret_cast<const uint8_t *>(PTR(I, slot)) + off;
+        s0.rows = F(I, P_NROWS);
+        s0.row_bytes = F(I, P_KC) * 2;
+        s0.stride = ktot * 2;
+        if (opc != MK_OP_UP) return 1;
+        s1 = s0;
+        s1.src = reinterpret_cast<const uint8_t *>(PTR(I, S_UP_WU)) + off;
+        return 2;
+    }
+    if (opc == MK_OP_ATTN) {
+        const int pos = attn_pos(P, I);
+        const int n = attn_cached_rows(I, pos);
+        const long long base =
+            (((long long)F(I, P_B) * P.Hkv + F(I, P_G)) * P.Smax + F(I, P_T0)) * (long long)P.D * 2;
+        s0.src = reinterpret_cast<const uint8_t *>(PTR(I, S_AT_K)) + base;
+        s0.rows = n;
+        s0.row_bytes = P.D * 2;
+        s0.stride = P.D * 2;
+        s1 = s0;
+        s1.src = reinterpret_cast<const uint8_t *>(PTR(I, S_AT_V)) + base;
+        return 2;
+    }
+    return 0;
+}
+
+}  // namespace mk

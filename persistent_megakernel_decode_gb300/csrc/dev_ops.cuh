@@ -1,0 +1,533 @@
+// Op bodies of the interpreter: what the activation loader stages for each
+// opcode and what the consumer warps compute from the page ring.
+//
+// GEMV tiles (QKV, O, MLP-up, MLP-down, LM head) follow "CMU 15-779 Lecture 7
+// notes", section 5.1 (fused RMSNorm+QKV, O-proj+residual, RMSNorm+up/gate+
+// SiLU, down+residual with a counter per K chunk, RMSNorm+LM head); the
+// attention task is split over KV positions and the last split of a
+// (sequence, kv head) merges the partials (the same section's attention and
+// attention-reduction instructions).  RoPE and the KV-cache append sit in the
+// attention task's activation stage instead of the QKV epilogue, because a
+// QKV tile holds 16 rows of a head and RoPE pairs dimension i with i + D/2.
+#pragma once
+#include "dev_common.cuh"
+
+namespace mk {
+
+// ================================================================ activation stage (one warp)
+
+// RMSNorm-fused ops stage x^ = h * rsqrt(mean(h^2) + eps) * w (fp32); O and
+// DOWN stage the attention output / their K chunk of the MLP activation.
+template <int MAXB>
+DEV void stage_gemv(const KParams &P, const WIns &I, float *slot, bool ab) {
+    const int lane = threadIdx.x & 31;
+    const int opc = F(I, W_OPC);
+    const int B = P.B;
+    if (opc == MK_OP_QKV || opc == MK_OP_UP || opc == MK_OP_LM) {
+        const int H = P.H;
+        const float *h = reinterpret_cast<const float *>(
+            PTR(I, opc == MK_OP_QKV ? S_QKV_H : opc == MK_OP_UP ? S_UP_H : S_LM_H));
+        const uint16_t *w = reinterpret_cast<const uint16_t *>(
+            PTR(I, opc == MK_OP_QKV ? S_QKV_NORM : opc == MK_OP_UP ? S_UP_NORM : S_LM_NORM));
+        const int snap = F(I, P_SNAP);
+        float *hist = nullptr;
+        if (snap > 0 && !ab) hist = reinterpret_cast<float *>(PTR(I, opc == MK_OP_QKV ? S_QKV_HIST : S_LM_HIST));
+        for (int b = 0; b < B; ++b) {
+            const float4 *src = reinterpret_cast<const float4 *>(h + (size_t)b * H);
+            float4 *dst = reinterpret_cast<float4 *>(slot + (size_t)b * H);
+            float4 *hs = hist ? reinterpret_cast<float4 *>(hist + ((size_t)(snap - 1) * B + b) * H) : nullptr;
+            float ss = 0.f;
+#pragma unroll 4
+            for (int k = lane; k < H / 4; k += 32) {
+                const float4 v = __ldcg(src + k);
+                dst[k] = v;
+                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                if (hs) hs[k] = v;
+            }
+            ss = warp_sum(ss);
+            const float scale = rsqrtf(ss / (float)H + P.eps);
+            __syncwarp();
+            const uint2 *w4 = reinterpret_cast<const uint2 *>(w);
+#pragma unroll 4
+            for (int k = lane; k < H / 4; k += 32) {
+                const uint2 ww = __ldg(w4 + k);
+                float4 v = dst[k];
+                v.x *= scale * __uint_as_float(ww.x << 16);
+                v.y *= scale * __uint_as_float(ww.x & 0xffff0000u);
+                v.z *= scale * __uint_as_float(ww.y << 16);
+                v.w *= scale * __uint_as_float(ww.y & 0xffff0000u);
+                dst[k] = v;
+            }
+        }
+    } else {
+        const int kc = F(I, P_KC);
+        const float *src;
+        size_t ld;
+        if (opc == MK_OP_O) {
+            src = reinterpret_cast<const float *>(PTR(I, S_O_IN));
+            ld = (size_t)P.Hq * P.D;
+        } else {
+            src = reinterpret_cast<const float *>(PTR(I, S_DN_IN)) + F(I, P_K0);
+            ld = (size_t)P.F;
+        }
+        for (int b = 0; b < B; ++b) {
+            const float4 *s4 = reinterpret_cast<const float4 *>(src + b * ld);
+            float4 *d4 = reinterpret_cast<float4 *>(slot + (size_t)b * kc);
+#pragma unroll 4
+            for (int k = lane; k < kc / 4; k += 32) d4[k] = __ldcg(s4 + k);
+        }
+    }
+}
+
+// q (pre-scaled by log2(e)/sqrt(D)), new k and v of one (sequence, kv group):
+// q/k RMSNorm (optional), RoPE at the new position (rotate-half pairs,
+// theta_i = theta^(-2i/D)), bf16 rounding of the new k/v, and the KV-cache
+// append by the split that owns the new position.  Slot layout: q as
+// [G][4 quarters][D/4 + 4] (padded against bank conflicts), then k, then v.
+template <int D>
+DEV void stage_attn(const KParams &P, const WIns &I, float *slot, bool ab) {
+    constexpr int PER = D / 32;
+    constexpr int QS = D / 4 + 4;
+    const int lane = threadIdx.x & 31;
+    const int G = P.Hq / P.Hkv, b = F(I, P_B), g = F(I, P_G);
+    const int pos = attn_pos(P, I);
+    const int t0 = F(I, P_T0), T = F(I, P_T);
+    const float *src = reinterpret_cast<const float *>(PTR(I, S_AT_QKV)) + ((size_t)b * P.Hkv + g) * (G + 2) * D;
+    const uint16_t *wq = reinterpret_cast<const uint16_t *>(PTR(I, S_AT_QN));
+    const uint16_t *wk = reinterpret_cast<const uint16_t *>(PTR(I, S_AT_KN));
+    float *qp = slot;
+    float *kn = slot + G * 4 * QS;
+    float *vn = kn + D;
+    const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
+    // angle of pair i in double, reduced mod 2 pi, then a float sincos
+    float cs[PER / 2], sn[PER / 2];
+#pragma unroll
+    for (int j = 0; j < PER / 2; ++j) {
+        const int i = lane + 32 * j;
+        const double inv_freq = exp2(-(2.0 * i / D) * log2((double)P.theta));
+        const double ang = (double)pos * inv_freq;
+        const double two_pi = 6.283185307179586476925286766559;
+        const double red = ang - rint(ang / two_pi) * two_pi;
+        sincosf((float)red, &sn[j], &cs[j]);
+    }
+    for (int h = 0; h < G + 2; ++h) {
+        float x[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) x[e] = __ldcg(src + (size_t)h * D + lane + 32 * e);
+        const bool is_q = h < G, is_k = h == G;
+        if (P.qk_norm && (is_q || is_k)) {
+            const uint16_t *w = is_q ? wq : wk;
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) ss += x[e] * x[e];
+            ss = warp_sum(ss);
+            const float sc = rsqrtf(ss / (float)D + P.eps);
+#pragma unroll
+            for (int e = 0; e < PER; ++e) x[e] = x[e] * sc * bf16_at(w, lane + 32 * e);
+        }
+        if (is_q || is_k) {
+#pragma unroll
+            for (int e = 0; e < PER / 2; ++e) {   // element lane+32e pairs with lane+32e+D/2
+                const float a = x[e], c = x[e + PER / 2];
+                x[e] = a * cs[e] - c * sn[e];
+                x[e + PER / 2] = a * sn[e] + c * cs[e];
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            const int d = lane + 32 * e;
+            if (is_q) qp[(h * 4 + d / (D / 4)) * QS + d % (D / 4)] = x[e] * qscale;
+            else if (is_k) kn[d] = round_bf16(x[e]);
+            else vn[d] = round_bf16(x[e]);
+        }
+    }
+    if (!ab && pos >= t0 && pos < t0 + T) {
+        __syncwarp();
+        const size_t c = (((size_t)b * P.Hkv + g) * P.Smax + pos) * D;
+        __nv_bfloat16 *kc = reinterpret_cast<__nv_bfloat16 *>(PTR(I, S_AT_K)) + c;
+        __nv_bfloat16 *vc = reinterpret_cast<__nv_bfloat16 *>(PTR(I, S_AT_V)) + c;
+        for (int d = lane; d < D; d += 32) {
+            kc[d] = __float2bfloat16_rn(kn[d]);
+            vc[d] = __float2bfloat16_rn(vn[d]);
+        }
+    }
+}
+
+// ================================================================ consumers (8 warps)
+
+template <int MAXB>
+struct XRegs {
+    static constexpr int NCH = MAXB >= 8 ? 1 : (MAXB >= 4 ? 2 : 4);
+    float v[NCH][MAXB][8];
+};
+
+template <int MAXB>
+__host__ __device__ constexpr int rows_max() { return MAXB > 4 ? 8 : MAX_TILE_ROWS; }
+
+// One GEMV tile: rows resident in the page ring times the activation chunk a
+// thread holds in registers; one butterfly reduction per tile; epilogue per op.
+template <int MAXB, int NCH>
+DEV void gemv_tile(const KParams &P, const Smem &S, const WIns &I, int i, const float *slot, bool fresh,
+                   XRegs<MAXB> &xr, uint32_t &ring, uint32_t &cph, bool &ab) {
+    constexpr int RMAX = rows_max<MAXB>();
+    constexpr int V = RMAX * MAXB;
+    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int opc = F(I, W_OPC);
+    const int B = P.B;
+    const int kc = F(I, P_KC), nchunk = kc / 8, row_bytes = kc * 2;
+    const int nrows = F(I, P_NROWS);
+    const int nseg = opc == MK_OP_UP ? 2 : 1;
+    const int total = nseg * nrows;
+    const int rpp = P.page_bytes / row_bytes;
+    if (fresh) {
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+            const int c = ct + CONSUMERS * j;
+#pragma unroll
+            for (int b = 0; b < MAXB; ++b) {
+                if (c < nchunk && b < B) {
+                    const float4 *s4 = reinterpret_cast<const float4 *>(slot + (size_t)b * kc + c * 8);
+                    const float4 a = s4[0], bb = s4[1];
+                    xr.v[j][b][0] = a.x; xr.v[j][b][1] = a.y; xr.v[j][b][2] = a.z; xr.v[j][b][3] = a.w;
+                    xr.v[j][b][4] = bb.x; xr.v[j][b][5] = bb.y; xr.v[j][b][6] = bb.z; xr.v[j][b][7] = bb.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xr.v[j][b][e] = 0.f;
+                }
+            }
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.act_empty[i & 1]);  // the slot is no longer needed
+
+    float acc[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) acc[k] = 0.f;
+    uint32_t p = 0;
+    int pr = 0;
+    const uint8_t *page = nullptr;
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+        if (r < total) {
+            if (r == 0 || pr == rpp || (nseg == 2 && r == nrows)) {
+                if (r > 0) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&S.empty[p]);
+                    ++ring;
+                }
+                p = ring % P.num_pages;
+                if (!ab) ab = !warp_wait_bar(P, S, &S.full[p], (ring / P.num_pages) & 1, 2, i, opc);
+                page = S.pages + (size_t)p * P.page_bytes;
+                pr = 0;
+            }
+            const uint8_t *wrow = page + (size_t)pr * row_bytes;
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+                const int c = ct + CONSUMERS * j;
+                if (c < nchunk) {
+                    float w8[8];
+                    bf16x8(*reinterpret_cast<const uint4 *>(wrow + c * 16), w8);
+#pragma unroll
+                    for (int b = 0; b < MAXB; ++b)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[r * MAXB + b] = fmaf(w8[e], xr.v[j][b][e], acc[r * MAXB + b]);
+                }
+            }
+            ++pr;
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[p]);
+    ++ring;
+
+    // warp reduction, then the 8 warps' partials through shared memory
+    Bfly<V, 16>::run(acc, lane);
+    float *red = S.aux;  // [warp][V]
+    if constexpr (V >= 32) {
+#pragma unroll
+        for (int j = 0; j < V / 32; ++j) red[warp * V + lane * (V / 32) + j] = acc[j];
+    } else {
+        if ((lane & (32 / V - 1)) == 0) red[warp * V + lane / (32 / V)] = acc[0];
+    }
+    consumer_sync(P, S, cph, ab, i);
+
+    // epilogue: thread ct -> (b = ct / RMAX, r = ct % RMAX)
+    const int eb = ct / RMAX, er = ct % RMAX;
+    const bool mine = eb < B && er < nrows && !ab;
+    auto total_of = [&](int r, int b) {
+        float y = 0.f;
+#pragma unroll
+        for (int w = 0; w < CONSUMER_WARPS; ++w) y += red[w * V + r * MAXB + b];
+        return y;
+    };
+    // operand pointers are decoded by the whole warp before any lane-divergent code
+    const int out0 = F(I, P_OUT0);
+    const uint64_t ptr_a = PTR(I, opc == MK_OP_QKV ? S_QKV_OUT : opc == MK_OP_O ? S_O_HRES
+                                : opc == MK_OP_UP ? S_UP_OUT : opc == MK_OP_DOWN ? S_DN_HRES : S_LM_LOGITS);
+    const uint64_t ptr_b = PTR(I, opc == MK_OP_O ? S_O_HMID : S_LM_KEYS);
+    if (opc == MK_OP_QKV) {
+        if (mine) {
+            float *out = reinterpret_cast<float *>(ptr_a);
+            const int G = P.Hq / P.Hkv;
+            out[(size_t)eb * P.Hkv * (G + 2) * P.D + out0 + er] = total_of(er, eb);
+            __threadfence();
+        }
+    } else if (opc == MK_OP_O) {
+        if (mine) {
+            float *hres = reinterpret_cast<float *>(ptr_a);
+            float *hmid = reinterpret_cast<float *>(ptr_b);
+            const size_t k = (size_t)eb * P.H + out0 + er;
+            const float v = __ldcg(hres + k) + total_of(er, eb);
+            hres[k] = v;
+            hmid[k] = v;
+            __threadfence();
+        }
+    } else if (opc == MK_OP_UP) {
+        if (mine) {
+            float *act = reinterpret_cast<float *>(ptr_a);
+            const float g = total_of(er, eb), u = total_of(nrows + er, eb);
+            act[(size_t)eb * P.F + out0 + er] = g / (1.0f + __expf(-g)) * u;
+            __threadfence();
+        }
+    } else if (opc == MK_OP_DOWN) {
+        if (mine) {
+            float *hres = reinterpret_cast<float *>(ptr_a);
+            atomicAdd(hres + (size_t)eb * P.H + out0 + er, total_of(er, eb));
+            __threadfence();
+        }
+    } else if (opc == MK_OP_LM) {
+        const float y = (eb < B && er < nrows) ? total_of(er, eb) : -INFINITY;
+        if (mine) reinterpret_cast<float *>(ptr_a)[(size_t)eb * P.V + out0 + er] = y;
+        // argmax over the RMAX lanes of one sequence (lowest index on ties)
+        float bv = y;
+        int bi = er;
+#pragma unroll
+        for (int o = RMAX / 2; o; o >>= 1) {
+            const float ov = __shfl_xor_sync(FULL, bv, o);
+            const int oi = __shfl_xor_sync(FULL, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (er == 0 && eb < B && !ab) {
+            unsigned long long *keys = reinterpret_cast<unsigned long long *>(ptr_b);
+            atomicMax(keys + (size_t)P.step * B + eb, (unsigned long long)argmax_key(bv, out0 + bi));
+        }
+        if (mine) __threadfence();
+    }
+}
+
+// Split-KV attention of one (sequence, kv group, split): scores from the
+// cached K rows in the page ring plus the new token, softmax partial in log2
+// units (max, sum), P.V, partial written out; the last split of the
+// (sequence, group) to arrive merges every split (log-sum-exp combine).
+template <int D>
+DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const float *slot, uint32_t &ring,
+                   uint32_t &cph, bool &ab) {
+    constexpr int PER = D / 32;
+    constexpr int QS = D / 4 + 4;
+    constexpr int DQ = D / 4;
+    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int G = P.Hq / P.Hkv, b = F(I, P_B), g = F(I, P_G);
+    const int split = F(I, P_SPLIT), nsplit = F(I, P_NSPLIT), layer = F(I, P_LAYER);
+    const int pos = attn_pos(P, I);
+    const int t0 = F(I, P_T0), T = F(I, P_T);
+    const int ncache = attn_cached_rows(I, pos);
+    const bool has_new = pos >= t0 && pos < t0 + T;
+    const int ntot = ncache + (has_new ? 1 : 0);
+    const float *qp = slot, *kn = slot + G * 4 * QS, *vn = kn + D;
+    float *sc = S.aux;                        // [G][T] scores, then probabilities
+    float *ow = sc + G * T;                   // [warp][G][D]
+    float *ml = ow + CONSUMER_WARPS * G * D;  // [G] max, [G] sum
+    const int rpp = P.page_bytes / (D * 2);
+    const int npg = (ncache + rpp - 1) / rpp;
+    const uint32_t kring = ring, vring = ring + npg;
+    for (int k = 0; k < npg; ++k) {
+        const uint32_t p = (kring + k) % P.num_pages;
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full[p], ((kring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
+    }
+    // scores: a warp takes 8 tokens at a time, 4 lanes per token, D/4 dims per lane
+    const int qtr = lane & 3;
+    for (int tb = warp * 8; tb < ntot; tb += CONSUMER_WARPS * 8) {
+        const int tk = tb + (lane >> 2);
+        float s[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) s[h] = 0.f;
+        if (tk < ntot) {
+            const uint8_t *row = nullptr;
+            if (tk < ncache)
+                row = S.pages + (size_t)((kring + tk / rpp) % P.num_pages) * P.page_bytes + (size_t)(tk % rpp) * D * 2;
+#pragma unroll
+            for (int dd = 0; dd < DQ; dd += 8) {
+                float k8[8];
+                if (row) {
+                    bf16x8(*reinterpret_cast<const uint4 *>(row + (qtr * DQ + dd) * 2), k8);
+                } else {
+                    const float4 a = *reinterpret_cast<const float4 *>(kn + qtr * DQ + dd);
+                    const float4 c = *reinterpret_cast<const float4 *>(kn + qtr * DQ + dd + 4);
+                    k8[0] = a.x; k8[1] = a.y; k8[2] = a.z; k8[3] = a.w; k8[4] = c.x; k8[5] = c.y; k8[6] = c.z; k8[7] = c.w;
+                }
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    if (h < G) {
+                        const float4 qa = *reinterpret_cast<const float4 *>(qp + (h * 4 + qtr) * QS + dd);
+                        const float4 qb = *reinterpret_cast<const float4 *>(qp + (h * 4 + qtr) * QS + dd + 4);
+                        s[h] = fmaf(qa.x, k8[0], s[h]); s[h] = fmaf(qa.y, k8[1], s[h]);
+                        s[h] = fmaf(qa.z, k8[2], s[h]); s[h] = fmaf(qa.w, k8[3], s[h]);
+                        s[h] = fmaf(qb.x, k8[4], s[h]); s[h] = fmaf(qb.y, k8[5], s[h]);
+                        s[h] = fmaf(qb.z, k8[6], s[h]); s[h] = fmaf(qb.w, k8[7], s[h]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            s[h] += __shfl_xor_sync(FULL, s[h], 1);
+            s[h] += __shfl_xor_sync(FULL, s[h], 2);
+        }
+        if (qtr == 0 && tk < ntot) {
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+                if (h < G) sc[h * T + tk] = s[h];
+        }
+    }
+    __syncwarp();
+    if (lane == 0)
+        for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty[(kring + k) % P.num_pages]);
+    consumer_sync(P, S, cph, ab, i);
+    // softmax statistics, one warp per head
+    if (warp < G) {
+        float m = -INFINITY;
+        for (int tk = lane; tk < ntot; tk += 32) m = fmaxf(m, sc[warp * T + tk]);
+        m = warp_max(m);
+        float l = 0.f;
+        for (int tk = lane; tk < ntot; tk += 32) {
+            const float e = exp2f(sc[warp * T + tk] - m);
+            sc[warp * T + tk] = e;
+            l += e;
+        }
+        l = warp_sum(l);
+        if (lane == 0) {
+            ml[warp] = m;
+            ml[G + warp] = l;
+        }
+    }
+    for (int k = 0; k < npg; ++k) {
+        const uint32_t p = (vring + k) % P.num_pages;
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full[p], ((vring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
+    }
+    ring = vring + npg;
+    consumer_sync(P, S, cph, ab, i);
+    // P.V: warp w takes tokens w, w+8, ...; lane holds D/32 consecutive dims
+    {
+        float acc[8][PER];
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[h][e] = 0.f;
+        for (int tk = warp; tk < ntot; tk += CONSUMER_WARPS) {
+            float v[PER];
+            if (tk < ncache) {
+                const uint8_t *row =
+                    S.pages + (size_t)((vring + tk / rpp) % P.num_pages) * P.page_bytes + (size_t)(tk % rpp) * D * 2;
+                if constexpr (PER == 2) {
+                    const uint32_t u = *reinterpret_cast<const uint32_t *>(row + lane * 4);
+                    v[0] = __uint_as_float(u << 16);
+                    v[1] = __uint_as_float(u & 0xffff0000u);
+                } else {
+                    const uint2 u = *reinterpret_cast<const uint2 *>(row + lane * 8);
+                    v[0] = __uint_as_float(u.x << 16);
+                    v[1] = __uint_as_float(u.x & 0xffff0000u);
+                    v[2] = __uint_as_float(u.y << 16);
+                    v[3] = __uint_as_float(u.y & 0xffff0000u);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < PER; ++e) v[e] = vn[lane * PER + e];
+            }
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+                if (h < G) {
+                    const float pr = sc[h * T + tk];
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) acc[h][e] = fmaf(pr, v[e], acc[h][e]);
+                }
+        }
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+            if (h < G)
+#pragma unroll
+                for (int e = 0; e < PER; ++e) ow[(warp * G + h) * D + lane * PER + e] = acc[h][e];
+    }
+    __syncwarp();
+    if (lane == 0) {
+        for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty[(vring + k) % P.num_pages]);
+        mbar_arrive(&S.act_empty[i & 1]);
+    }
+    consumer_sync(P, S, cph, ab, i);
+    float *part = reinterpret_cast<float *>(PTR(I, S_AT_PART));
+    auto part_at = [&](int h, int s) {
+        return part + (((size_t)b * P.Hq + g * G + h) * P.nsplit_max + s) * (D + 2);
+    };
+    for (int k = ct; k < G * D && !ab; k += CONSUMERS) {
+        const int h = k / D, d = k % D;
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < CONSUMER_WARPS; ++w) o += ow[(w * G + h) * D + d];
+        part_at(h, split)[d] = o;
+    }
+    if (ct < G && !ab) {
+        part_at(ct, split)[D] = ml[ct];
+        part_at(ct, split)[D + 1] = ml[G + ct];
+    }
+    __threadfence();
+    consumer_sync(P, S, cph, ab, i);
+    uint32_t *arrive = reinterpret_cast<uint32_t *>(PTR(I, S_AT_ARRIVE)) + ((size_t)layer * P.B + b) * P.Hkv + g;
+    if (ct == 0) {
+        int last = 0;
+        if (!ab) {
+            const uint32_t old = atom_acqrel_add(arrive, 1u);
+            last = old == (uint32_t)(P.step + 1) * (uint32_t)nsplit - 1u;
+        }
+        S.ctrl[3] = last;
+    }
+    consumer_sync(P, S, cph, ab, i);
+    if (S.ctrl[3] && !ab) {
+        float *out = reinterpret_cast<float *>(PTR(I, S_AT_OUT));
+        for (int k = ct; k < G * D; k += CONSUMERS) {
+            const int h = k / D, d = k % D;
+            float M = -INFINITY;
+            for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(part_at(h, s) + D));
+            float L = 0.f, o = 0.f;
+            for (int s = 0; s < nsplit; ++s) {
+                const float *ps = part_at(h, s);
+                const float f = exp2f(__ldcg(ps + D) - M);
+                L += f * __ldcg(ps + D + 1);
+                o += f * __ldcg(ps + d);
+            }
+            out[(size_t)b * P.Hq * D + (size_t)(g * G + h) * D + d] = o / L;
+        }
+        __threadfence();
+    }
+}
+
+DEV void embed_task(const KParams &P, const Smem &S, const WIns &I, int i, bool ab) {
+    const int ct = threadIdx.x - 64, lane = ct & 31;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.act_empty[i & 1]);
+    if (ab) return;
+    const uint16_t *E = reinterpret_cast<const uint16_t *>(PTR(I, S_EMB_W));
+    float *h = reinterpret_cast<float *>(PTR(I, S_EMB_H));
+    int32_t *tokens = reinterpret_cast<int32_t *>(PTR(I, S_EMB_TOK));
+    const unsigned long long *keys = reinterpret_cast<const unsigned long long *>(PTR(I, S_EMB_KEYS));
+    const bool host_tokens = (P.flags & MK_RUN_HOST_TOKENS) || P.step == 0;
+    for (int b = 0; b < P.B; ++b) {
+        int tok;
+        if (host_tokens) tok = __ldcg(tokens + (size_t)P.step * P.B + b);
+        else tok = (int)(0xFFFFFFFFu - (uint32_t)(__ldcg(keys + (size_t)(P.step - 1) * P.B + b) & 0xFFFFFFFFull));
+        if (tok < 0 || tok >= P.V) tok = 0;  // out-of-range ids read row 0 instead of faulting
+        if (!host_tokens && ct == 0) tokens[(size_t)P.step * P.B + b] = tok;
+        for (int k = ct; k < P.H; k += CONSUMERS) h[(size_t)b * P.H + k] = bf16_at(E, (size_t)tok * P.H + k);
+    }
+    __threadfence();
+}
+
+}  // namespace mk

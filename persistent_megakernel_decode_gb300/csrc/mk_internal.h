@@ -98,5 +98,5 @@ inline int red_bytes(int B) { return CONSUMER_WARPS * MAX_TILE_ROWS * B * 4; }
 inline int attn_aux_bytes(int G, int T, int D) { return (G * T + CONSUMER_WARPS * G * D + 8 * G) * 4; }
 constexpr int MBAR_BYTES = 512;    // up to 64 mbarriers
 constexpr int CTRL_BYTES = 128;
-constexpr int MAX_PAGES = 28;      // 2 * MAX_PAGES + 4 mbarriers must fit MBAR_BYTES
+constexpr int MAX_PAGES = 28;      // 2 * MAX_PAGES + 5 mbarriers must fit MBAR_BYTES
 }  // namespace mk

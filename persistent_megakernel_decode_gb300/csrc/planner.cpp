@@ -540,24 +540,25 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     const int tile = 65536;
     p.page_bytes = tgt->page_bytes > 0 ? tgt->page_bytes : 16384;
     if (p.page_bytes % 128) return set_error(MK_ERR_INVALID, "page_bytes must be a multiple of 128");
-    int kn_qkv = tgt->rows_qkv > 0 ? tgt->rows_qkv : pow2_floor(clampi(tile / (2 * H), 1, 16));
-    int kn_o = tgt->rows_o > 0 ? tgt->rows_o : pow2_floor(clampi(tile / (2 * Hq * D), 1, 16));
-    int kn_up = tgt->rows_up > 0 ? tgt->rows_up : pow2_floor(clampi(tile / (4 * H), 1, 8));
+    const int rcap = B > 4 ? 8 : 16;
+    int kn_qkv = tgt->rows_qkv > 0 ? tgt->rows_qkv : pow2_floor(clampi(tile / (2 * H), 1, rcap));
+    int kn_o = tgt->rows_o > 0 ? tgt->rows_o : pow2_floor(clampi(tile / (2 * Hq * D), 1, rcap));
+    int kn_up = tgt->rows_up > 0 ? tgt->rows_up : pow2_floor(clampi(tile / (4 * H), 1, rcap / 2));
     int kn_kc = tgt->kchunk_down;
     if (kn_kc <= 0) {
         kn_kc = 8;
         for (int c = 8; c <= std::min(F, 2048); c += 8)
             if (F % c == 0) kn_kc = c;
     }
-    int kn_dn = tgt->rows_down > 0 ? tgt->rows_down : pow2_floor(clampi(tile / (2 * kn_kc), 1, 16));
-    int kn_lm = tgt->rows_lm > 0 ? tgt->rows_lm : pow2_floor(clampi(tile / (2 * H), 1, 16));
+    int kn_dn = tgt->rows_down > 0 ? tgt->rows_down : pow2_floor(clampi(tile / (2 * kn_kc), 1, rcap));
+    int kn_lm = tgt->rows_lm > 0 ? tgt->rows_lm : pow2_floor(clampi(tile / (2 * H), 1, rcap));
     int kn_T = tgt->attn_split > 0 ? tgt->attn_split : clampi(16384 / (2 * D), 16, 256);
     p.rows_qkv = kn_qkv; p.rows_o = kn_o; p.rows_up = kn_up; p.rows_down = kn_dn; p.kchunk_down = kn_kc;
     p.rows_lm = kn_lm; p.attn_split = kn_T;
     const int rows_group = (G + 2) * D;
-    if (kn_qkv > MAX_TILE_ROWS || kn_o > MAX_TILE_ROWS || kn_dn > MAX_TILE_ROWS || kn_lm > MAX_TILE_ROWS ||
-        2 * kn_up > MAX_TILE_ROWS)
-        return set_error(MK_ERR_UNSUPPORTED, "tile rows above 16 (mlp-up: 8)");
+    const int rmax = B > 4 ? 8 : MAX_TILE_ROWS;  // the batch-8 kernel keeps 8 rows x 8 sequences in registers
+    if (kn_qkv > rmax || kn_o > rmax || kn_dn > rmax || kn_lm > rmax || 2 * kn_up > rmax)
+        return set_error(MK_ERR_UNSUPPORTED, "tile rows above 16 (8 for batch > 4; mlp-up: half of that)");
     if (D % kn_qkv) return set_error(MK_ERR_UNSUPPORTED, "rows_qkv must divide head_dim");
     if (F % kn_up || F % kn_kc || kn_kc % 8) return set_error(MK_ERR_UNSUPPORTED, "rows_up / kchunk_down must divide ffn");
     if (kn_T > 256 || kn_T < 1) return set_error(MK_ERR_UNSUPPORTED, "attn_split must be 1..256");

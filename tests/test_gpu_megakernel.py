@@ -7,7 +7,7 @@ from oracle import plans
 from persistent_megakernel_decode_gb300 import runtime as rt
 from persistent_megakernel_decode_gb300 import synth
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.timeout(180)]
 
 
 @pytest.fixture(scope="module", autouse=True)
