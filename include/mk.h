@@ -242,9 +242,12 @@ int mk_sync_status(mk_plan_t plan, void *workspace, void *stream, mk_error_recor
 /* Copy the event counters (uint32 [num_events]) from the workspace to host. */
 int mk_read_counters(mk_plan_t plan, void *workspace, uint32_t *out);
 
-/* Copy the per-instruction trace (uint64 [num_workers, lmax, 4]: opcode,
- * start, activation-ready, done, in globaltimer ns) to host.  Only filled by
- * runs with MK_RUN_TRACE. */
+/* Copy the per-instruction trace to host: uint64 [total_slots, 16] =
+ * (opcode | task << 32, consumer start, activation ready, consumer done,
+ * loader issue start, loader issue end, first page ready, last page ready,
+ * pages not ready on arrival, page loop end, reduction end, epilogue end,
+ * activation not ready on arrival, activation handed over, 2 reserved),
+ * globaltimer ns for times.  Only filled by runs with MK_RUN_TRACE. */
 int mk_read_trace(mk_plan_t plan, void *workspace, uint64_t *out);
 
 /* Free the plan's host memory.  NULL-safe.  Never touches device memory. */

@@ -40,7 +40,7 @@ void layout_workspace(Plan &p) {
     } else {
         p.ws.hres = p.ws.hmid = p.ws.qkv = p.ws.part = p.ws.attn_out = p.ws.act = 0;
     }
-    p.ws.trace = take(total_slots * 4 * 8);
+    p.ws.trace = take(total_slots * 16 * 8);
     p.ws.total = off;
 }
 
@@ -110,8 +110,10 @@ int mk_plan_graph(const mk_graph_desc *graph, const mk_target_desc *target, mk_p
     p.num_pages = 2;
     p.page_bytes = 16384;
     p.act_bytes = 128;
-    p.aux_bytes = 128;
-    p.smem_bytes = 2 * p.act_bytes + p.num_pages * p.page_bytes + p.aux_bytes + MBAR_BYTES + CTRL_BYTES;
+    p.abuf_bytes = 128;
+    p.red_bytes = 128;
+    p.aux_bytes = 256;
+    p.smem_bytes = p.abuf_bytes + 2 * p.act_bytes + p.num_pages * p.page_bytes + p.aux_bytes + MBAR_BYTES + CTRL_BYTES;
     return finish_new_plan(p, out);
 }
 

@@ -31,6 +31,21 @@ DEV uint32_t ld_relaxed(const uint32_t *p) {
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+DEV void red_max_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+DEV void red_relaxed_add(uint32_t *p, uint32_t v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+DEV void st_release_cta(volatile int *p, int v) {
+    asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(saddr((const void *)p)), "r"(v) : "memory");
+}
+DEV int ld_acquire_cta(volatile int *p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr((const void *)p)) : "memory");
+    return v;
+}
 DEV void red_release_add(uint32_t *p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -126,18 +141,40 @@ struct Bfly {
 };
 
 // ---------------------------------------------------------------- shared state
+// The dynamic shared memory of the interpreter, one array; everything below
+// addresses it through offsets so that every access compiles to a
+// shared-memory instruction (a generic pointer kept in a struct would not).
+extern __shared__ __align__(1024) uint8_t mk_smem[];
+
+// Offsets into the dynamic shared memory and accessors for its regions.
 struct Smem {
-    uint8_t *act[2];
-    uint8_t *pages;
-    float *aux;
-    uint64_t *full, *empty, *act_full, *act_empty;
-    uint64_t *cbar;      // consumer-group barrier (8 warp arrivals per phase)
-    volatile int *ctrl;  // [0] abort, [1..2] slot flags, [3] attention: last split
+    uint32_t o_abuf;      // GEMV activation [B][K] (RMSNorm-ed where the op fuses it)
+    uint32_t o_act0;      // slot 0; slot s at o_act0 + s * act_stride
+    uint32_t act_stride;
+    uint32_t o_pages;     // page ring
+    uint32_t o_aux;       // op scratch (attention scores, partial outputs)
+    uint32_t o_red0;      // cross-warp reduction buffers, alternating per instruction
+    uint32_t red_stride;  // bytes
+    uint32_t o_bars;      // full[NP], empty[NP], act_full[2], act_empty[2], consumer barrier
+    uint32_t o_ctrl;      // [0] abort, [1..2] slot flags, [3] attention: last split,
+                          // [8..15] consumer warp progress (instructions finished + 1)
+    int num_pages;
+    DEV float *abuf() const { return reinterpret_cast<float *>(mk_smem + o_abuf); }
+    DEV uint8_t *act(int s) const { return mk_smem + o_act0 + s * act_stride; }
+    DEV uint8_t *pages() const { return mk_smem + o_pages; }
+    DEV float *aux() const { return reinterpret_cast<float *>(mk_smem + o_aux); }
+    DEV float *red(int k) const { return reinterpret_cast<float *>(mk_smem + o_red0 + k * red_stride); }
+    DEV uint64_t *full() const { return reinterpret_cast<uint64_t *>(mk_smem + o_bars); }
+    DEV uint64_t *empty() const { return full() + num_pages; }
+    DEV uint64_t *act_full() const { return full() + 2 * num_pages; }
+    DEV uint64_t *act_empty() const { return full() + 2 * num_pages + 2; }
+    DEV uint64_t *cbar() const { return full() + 2 * num_pages + 4; }
+    DEV volatile int *ctrl() const { return reinterpret_cast<volatile int *>(mk_smem + o_ctrl); }
 };
 
 constexpr int SLOT_FRESH = 1;
 
-DEV void raise_error(const KParams &P, const Smem &S, int code, int slot, int event, uint32_t obs, uint32_t need,
+DEV void raise_error(const KParams &P, const Smem S, int code, int slot, int event, uint32_t obs, uint32_t need,
                      int opc, int role) {
     if (atomicCAS(&P.err[E_CODE], 0u, (uint32_t)code) == 0u) {
         P.err[E_WORKER] = blockIdx.x;
@@ -149,20 +186,20 @@ DEV void raise_error(const KParams &P, const Smem &S, int code, int slot, int ev
         P.err[E_ROLE] = (uint32_t)role;
     }
     atomicExch(&P.err[E_ABORT], 1u);
-    S.ctrl[0] = 1;
+    S.ctrl()[0] = 1;
 }
 
-DEV bool aborted(const KParams &P, const Smem &S) {
-    if (S.ctrl[0]) return true;
+DEV bool aborted(const KParams &P, const Smem S) {
+    if (S.ctrl()[0]) return true;
     if (ld_relaxed(&P.err[E_ABORT])) {
-        S.ctrl[0] = 1;
+        S.ctrl()[0] = 1;
         return true;
     }
     return false;
 }
 
 // Whole-warp bounded wait on an mbarrier phase; uniform result, false = abort.
-DEV bool warp_wait_bar(const KParams &P, const Smem &S, uint64_t *bar, uint32_t parity, int role, int slot, int opc) {
+DEV bool warp_wait_bar(const KParams &P, const Smem S, uint64_t *bar, uint32_t parity, int role, int slot, int opc) {
     const int lane = threadIdx.x & 31;
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
@@ -184,7 +221,7 @@ DEV bool warp_wait_bar(const KParams &P, const Smem &S, uint64_t *bar, uint32_t 
 }
 
 // Whole-warp bounded wait for counter >= target (acquire on every poll).
-DEV bool warp_wait_counter(const KParams &P, const Smem &S, int ev, uint32_t target, int slot, int opc) {
+DEV bool warp_wait_counter(const KParams &P, const Smem S, int ev, uint32_t target, int slot, int opc) {
     const int lane = threadIdx.x & 31;
     const uint32_t *c = P.counters + ev;
     uint64_t t0 = 0;
@@ -211,14 +248,14 @@ DEV bool warp_wait_counter(const KParams &P, const Smem &S, int ev, uint32_t tar
 // lane 0 arrives, the warp waits for the phase with the same bounded wait as
 // every other wait (a lost arrival becomes a recorded timeout, not a hang).
 // `phase` counts the barrier uses of this warp (uniform across the warp).
-DEV void consumer_sync(const KParams &P, const Smem &S, uint32_t &phase, bool &ab, int slot) {
+DEV void consumer_sync(const KParams &P, const Smem S, uint32_t &phase, bool &ab, int slot) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(S.cbar);
-    if (!ab) ab = !warp_wait_bar(P, S, S.cbar, phase & 1, 3, slot, -1);
+    if ((threadIdx.x & 31) == 0) mbar_arrive(S.cbar());
+    if (!ab) ab = !warp_wait_bar(P, S, S.cbar(), phase & 1, 3, slot, -1);
     ++phase;
 }
 
-DEV bool cta_aborting(const Smem &S) { return __shfl_sync(FULL, (int)S.ctrl[0], 0) != 0; }
+DEV bool cta_aborting(const Smem S) { return __shfl_sync(FULL, (int)S.ctrl()[0], 0) != 0; }
 
 // ---------------------------------------------------------------- instruction decoding
 // A warp holds one instruction: lane k keeps word k; lanes 0..15 keep the 16
@@ -266,7 +303,7 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
         const int nrows = F(I, P_NROWS), kc = F(I, P_KC);
         const int rmax = P.B > 4 ? 8 : MAX_TILE_ROWS;
         if (nrows <= 0 || (opc == MK_OP_UP ? 2 * nrows : nrows) > rmax) return false;
-        if (kc <= 0 || kc % 8 || 2 * kc > P.page_bytes || kc * P.B * 4 > P.act_bytes) return false;
+        if (kc <= 0 || kc % 8 || 2 * kc > P.page_bytes || kc * P.B * 4 > P.abuf_bytes) return false;
     }
     if (opc == MK_OP_ATTN) {
         const int T = F(I, P_T);

@@ -19,7 +19,7 @@ namespace mk {
 // RMSNorm-fused ops stage x^ = h * rsqrt(mean(h^2) + eps) * w (fp32); O and
 // DOWN stage the attention output / their K chunk of the MLP activation.
 template <int MAXB>
-DEV void stage_gemv(const KParams &P, const WIns &I, float *slot, bool ab) {
+DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab) {
     const int lane = threadIdx.x & 31;
     const int opc = F(I, W_OPC);
     const int B = P.B;
@@ -34,7 +34,7 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *slot, bool ab) {
         if (snap > 0 && !ab) hist = reinterpret_cast<float *>(PTR(I, opc == MK_OP_QKV ? S_QKV_HIST : S_LM_HIST));
         for (int b = 0; b < B; ++b) {
             const float4 *src = reinterpret_cast<const float4 *>(h + (size_t)b * H);
-            float4 *dst = reinterpret_cast<float4 *>(slot + (size_t)b * H);
+            float4 *dst = reinterpret_cast<float4 *>(abuf + (size_t)b * H);
             float4 *hs = hist ? reinterpret_cast<float4 *>(hist + ((size_t)(snap - 1) * B + b) * H) : nullptr;
             float ss = 0.f;
 #pragma unroll 4
@@ -72,10 +72,24 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *slot, bool ab) {
         }
         for (int b = 0; b < B; ++b) {
             const float4 *s4 = reinterpret_cast<const float4 *>(src + b * ld);
-            float4 *d4 = reinterpret_cast<float4 *>(slot + (size_t)b * kc);
+            float4 *d4 = reinterpret_cast<float4 *>(abuf + (size_t)b * kc);
 #pragma unroll 4
             for (int k = lane; k < kc / 4; k += 32) d4[k] = __ldcg(s4 + k);
         }
+    }
+}
+
+// O tiles add their rows of the residual stream; the activation loader stages
+// that slice into the slot's tail so the consumers' epilogue reads shared memory.
+DEV float *slot_resid(const KParams &P, float *slot) { return slot + (P.act_bytes / 4 - P.B * RESID_ROWS); }
+DEV void stage_resid(const KParams &P, const WIns &I, float *slot) {
+    const int lane = threadIdx.x & 31;
+    const float *hres = reinterpret_cast<const float *>(PTR(I, S_O_HRES));
+    const int out0 = F(I, P_OUT0), nrows = F(I, P_NROWS);
+    float *resid = slot_resid(P, slot);
+    for (int k = lane; k < P.B * RESID_ROWS; k += 32) {
+        const int b = k / RESID_ROWS, r = k % RESID_ROWS;
+        resid[k] = r < nrows ? __ldcg(hres + (size_t)b * P.H + out0 + r) : 0.f;
     }
 }
 
@@ -156,19 +170,15 @@ DEV void stage_attn(const KParams &P, const WIns &I, float *slot, bool ab) {
 // ================================================================ consumers (8 warps)
 
 template <int MAXB>
-struct XRegs {
-    static constexpr int NCH = MAXB >= 8 ? 1 : (MAXB >= 4 ? 2 : 4);
-    float v[NCH][MAXB][8];
-};
-
-template <int MAXB>
 __host__ __device__ constexpr int rows_max() { return MAXB > 4 ? 8 : MAX_TILE_ROWS; }
 
-// One GEMV tile: rows resident in the page ring times the activation chunk a
-// thread holds in registers; one butterfly reduction per tile; epilogue per op.
+// Batch > 1: one GEMV tile split over K -- a thread holds an 8-wide K chunk of
+// x for every sequence in registers (loaded from the activation buffer) and
+// accumulates every row of the tile; one butterfly reduction per tile and the
+// 8 warps' partials combined through shared memory.
 template <int MAXB, int NCH>
-DEV void gemv_tile(const KParams &P, const Smem &S, const WIns &I, int i, const float *slot, bool fresh,
-                   XRegs<MAXB> &xr, uint32_t &ring, uint32_t &cph, bool &ab) {
+DEV void gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+                   uint32_t &cph, bool &ab) {
     constexpr int RMAX = rows_max<MAXB>();
     constexpr int V = RMAX * MAXB;
     const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
@@ -179,26 +189,28 @@ DEV void gemv_tile(const KParams &P, const Smem &S, const WIns &I, int i, const 
     const int nseg = opc == MK_OP_UP ? 2 : 1;
     const int total = nseg * nrows;
     const int rpp = P.page_bytes / row_bytes;
-    if (fresh) {
+    float xv[NCH][MAXB][8];
 #pragma unroll
-        for (int j = 0; j < NCH; ++j) {
-            const int c = ct + CONSUMERS * j;
+    for (int j = 0; j < NCH; ++j) {
+        const int c = ct + CONSUMERS * j;
 #pragma unroll
-            for (int b = 0; b < MAXB; ++b) {
-                if (c < nchunk && b < B) {
-                    const float4 *s4 = reinterpret_cast<const float4 *>(slot + (size_t)b * kc + c * 8);
-                    const float4 a = s4[0], bb = s4[1];
-                    xr.v[j][b][0] = a.x; xr.v[j][b][1] = a.y; xr.v[j][b][2] = a.z; xr.v[j][b][3] = a.w;
-                    xr.v[j][b][4] = bb.x; xr.v[j][b][5] = bb.y; xr.v[j][b][6] = bb.z; xr.v[j][b][7] = bb.w;
-                } else {
+        for (int b = 0; b < MAXB; ++b) {
+            if (c < nchunk && b < B) {
+                const float4 *s4 = reinterpret_cast<const float4 *>(S.abuf() + (size_t)b * kc + c * 8);
+                const float4 a = s4[0], bb = s4[1];
+                xv[j][b][0] = a.x; xv[j][b][1] = a.y; xv[j][b][2] = a.z; xv[j][b][3] = a.w;
+                xv[j][b][4] = bb.x; xv[j][b][5] = bb.y; xv[j][b][6] = bb.z; xv[j][b][7] = bb.w;
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) xr.v[j][b][e] = 0.f;
-                }
+                for (int e = 0; e < 8; ++e) xv[j][b][e] = 0.f;
             }
         }
     }
+    // O tiles: this thread's residual value, read before the slot is released
+    float resid_v = 0.f;
+    if (opc == MK_OP_O && ct / RMAX < B) resid_v = slot_resid(P, const_cast<float *>(slot))[(ct / RMAX) * RESID_ROWS + ct % RMAX];
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.act_empty[i & 1]);  // the slot is no longer needed
+    if (lane == 0) mbar_arrive(&S.act_empty()[i & 1]);  // activation buffer and slot no longer needed
 
     float acc[V];
 #pragma unroll
@@ -212,12 +224,13 @@ DEV void gemv_tile(const KParams &P, const Smem &S, const WIns &I, int i, const 
             if (r == 0 || pr == rpp || (nseg == 2 && r == nrows)) {
                 if (r > 0) {
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&S.empty[p]);
+                    if (lane == 0) mbar_arrive(&S.empty()[p]);
                     ++ring;
                 }
                 p = ring % P.num_pages;
-                if (!ab) ab = !warp_wait_bar(P, S, &S.full[p], (ring / P.num_pages) & 1, 2, i, opc);
-                page = S.pages + (size_t)p * P.page_bytes;
+                if (!ab) ab = !warp_wait_bar(P, S, &S.full()[p], (ring / P.num_pages) & 1, 2, i, opc);
+                if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + (r == 0 ? 6 : 7)] = gtimer();
+                page = S.pages() + (size_t)p * P.page_bytes;
                 pr = 0;
             }
             const uint8_t *wrow = page + (size_t)pr * row_bytes;
@@ -230,19 +243,19 @@ DEV void gemv_tile(const KParams &P, const Smem &S, const WIns &I, int i, const 
 #pragma unroll
                     for (int b = 0; b < MAXB; ++b)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[r * MAXB + b] = fmaf(w8[e], xr.v[j][b][e], acc[r * MAXB + b]);
+                        for (int e = 0; e < 8; ++e) acc[r * MAXB + b] = fmaf(w8[e], xv[j][b][e], acc[r * MAXB + b]);
                 }
             }
             ++pr;
         }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[p]);
+    if (lane == 0) mbar_arrive(&S.empty()[p]);
     ++ring;
 
     // warp reduction, then the 8 warps' partials through shared memory
     Bfly<V, 16>::run(acc, lane);
-    float *red = S.aux;  // [warp][V]
+    float *red = S.red(i & 1);  // [warp][V]
     if constexpr (V >= 32) {
 #pragma unroll
         for (int j = 0; j < V / 32; ++j) red[warp * V + lane * (V / 32) + j] = acc[j];
@@ -270,30 +283,26 @@ DEV void gemv_tile(const KParams &P, const Smem &S, const WIns &I, int i, const 
             float *out = reinterpret_cast<float *>(ptr_a);
             const int G = P.Hq / P.Hkv;
             out[(size_t)eb * P.Hkv * (G + 2) * P.D + out0 + er] = total_of(er, eb);
-            __threadfence();
         }
     } else if (opc == MK_OP_O) {
         if (mine) {
             float *hres = reinterpret_cast<float *>(ptr_a);
             float *hmid = reinterpret_cast<float *>(ptr_b);
             const size_t k = (size_t)eb * P.H + out0 + er;
-            const float v = __ldcg(hres + k) + total_of(er, eb);
+            const float v = resid_v + total_of(er, eb);
             hres[k] = v;
             hmid[k] = v;
-            __threadfence();
         }
     } else if (opc == MK_OP_UP) {
         if (mine) {
             float *act = reinterpret_cast<float *>(ptr_a);
             const float g = total_of(er, eb), u = total_of(nrows + er, eb);
             act[(size_t)eb * P.F + out0 + er] = g / (1.0f + __expf(-g)) * u;
-            __threadfence();
         }
     } else if (opc == MK_OP_DOWN) {
         if (mine) {
             float *hres = reinterpret_cast<float *>(ptr_a);
             atomicAdd(hres + (size_t)eb * P.H + out0 + er, total_of(er, eb));
-            __threadfence();
         }
     } else if (opc == MK_OP_LM) {
         const float y = (eb < B && er < nrows) ? total_of(er, eb) : -INFINITY;
@@ -309,10 +318,145 @@ DEV void gemv_tile(const KParams &P, const Smem &S, const WIns &I, int i, const 
         }
         if (er == 0 && eb < B && !ab) {
             unsigned long long *keys = reinterpret_cast<unsigned long long *>(ptr_b);
-            atomicMax(keys + (size_t)P.step * B + eb, (unsigned long long)argmax_key(bv, out0 + bi));
+            red_max_u64(keys + (size_t)P.step * B + eb, (unsigned long long)argmax_key(bv, out0 + bi));
         }
-        if (mine) __threadfence();
     }
+}
+
+// Batch 1: whole rows per warp.  Warp w owns rows w*NRW .. w*NRW+NRW-1 of
+// every segment of the tile; lane l covers the 8-element groups l, l+32, ...
+// of a row (KG groups), with the matching x kept in registers for the tile,
+// so a row is finished with one warp reduction -- no cross-warp reduction and
+// no barrier between warps.  KG = 0 selects a variant that reads x from
+// shared memory (rows longer than 32 * 8 * 8 elements).  The LM head keeps a
+// per-warp running best (logit, index) and updates the global argmax only
+// when it improves.
+template <int NRW, int KG>
+DEV void gemv_rows(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+                   unsigned long long &lm_best, bool &ab) {
+    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int opc = F(I, W_OPC);
+    const int kc = F(I, P_KC), ngrp = kc / 8, row_bytes = kc * 2;
+    const int nrows = F(I, P_NROWS), out0 = F(I, P_OUT0);
+    const int nseg = opc == MK_OP_UP ? 2 : 1;
+    const int rpp = P.page_bytes / row_bytes;
+    const int npg = (nrows + rpp - 1) / rpp;
+    const int r0 = warp * NRW;
+    const uint64_t ptr_a = PTR(I, opc == MK_OP_QKV ? S_QKV_OUT : opc == MK_OP_O ? S_O_HRES
+                                : opc == MK_OP_UP ? S_UP_OUT : opc == MK_OP_DOWN ? S_DN_HRES : S_LM_LOGITS);
+    const uint64_t ptr_b = PTR(I, opc == MK_OP_O ? S_O_HMID : S_LM_KEYS);
+    const float *xs = S.abuf();
+    float x[KG > 0 ? KG : 1][8];
+    if constexpr (KG > 0) {
+#pragma unroll
+        for (int k = 0; k < KG; ++k) {
+            const int g = lane + 32 * k;
+            if (g < ngrp) {
+                const float4 a = *reinterpret_cast<const float4 *>(xs + g * 8);
+                const float4 b = *reinterpret_cast<const float4 *>(xs + g * 8 + 4);
+                x[k][0] = a.x; x[k][1] = a.y; x[k][2] = a.z; x[k][3] = a.w;
+                x[k][4] = b.x; x[k][5] = b.y; x[k][6] = b.z; x[k][7] = b.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[k][e] = 0.f;
+            }
+        }
+    }
+    float acc[2][NRW];
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int j = 0; j < NRW; ++j) acc[s][j] = 0.f;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        if (s < nseg) {
+            for (int pg = 0; pg < npg; ++pg) {
+                const uint32_t p = ring % P.num_pages;
+                if (P.trace && ct == 0 && !mbar_test(&S.full()[p], (ring / P.num_pages) & 1))
+                    P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 8] += 1;   // page not ready on arrival
+                if (!ab) ab = !warp_wait_bar(P, S, &S.full()[p], (ring / P.num_pages) & 1, 2, i, opc);
+                if (P.trace && ct == 0)
+                    P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + ((s == 0 && pg == 0) ? 6 : 7)] = gtimer();
+                const int prow0 = pg * rpp, pnr = min(rpp, nrows - prow0);
+                const uint8_t *page = S.pages() + (size_t)p * P.page_bytes;
+#pragma unroll
+                for (int j = 0; j < NRW; ++j) {
+                    const int r = r0 + j;
+                    if (r >= prow0 && r < prow0 + pnr) {  // warp-uniform
+                        const uint8_t *wr = page + (size_t)(r - prow0) * row_bytes;
+                        float a0 = 0.f, a1 = 0.f;
+                        if constexpr (KG > 0) {
+#pragma unroll
+                            for (int k = 0; k < KG; ++k) {
+                                const int g = lane + 32 * k;
+                                if (g < ngrp) {
+                                    float w8[8];
+                                    bf16x8(*reinterpret_cast<const uint4 *>(wr + g * 16), w8);
+                                    a0 = fmaf(w8[0], x[k][0], a0); a1 = fmaf(w8[1], x[k][1], a1);
+                                    a0 = fmaf(w8[2], x[k][2], a0); a1 = fmaf(w8[3], x[k][3], a1);
+                                    a0 = fmaf(w8[4], x[k][4], a0); a1 = fmaf(w8[5], x[k][5], a1);
+                                    a0 = fmaf(w8[6], x[k][6], a0); a1 = fmaf(w8[7], x[k][7], a1);
+                                }
+                            }
+                        } else {
+#pragma unroll 4
+                            for (int g = lane; g < ngrp; g += 32) {
+                                float w8[8];
+                                bf16x8(*reinterpret_cast<const uint4 *>(wr + g * 16), w8);
+                                const float4 xa = *reinterpret_cast<const float4 *>(xs + g * 8);
+                                const float4 xb = *reinterpret_cast<const float4 *>(xs + g * 8 + 4);
+                                a0 = fmaf(w8[0], xa.x, a0); a1 = fmaf(w8[1], xa.y, a1);
+                                a0 = fmaf(w8[2], xa.z, a0); a1 = fmaf(w8[3], xa.w, a1);
+                                a0 = fmaf(w8[4], xb.x, a0); a1 = fmaf(w8[5], xb.y, a1);
+                                a0 = fmaf(w8[6], xb.z, a0); a1 = fmaf(w8[7], xb.w, a1);
+                            }
+                        }
+                        acc[s][j] += a0 + a1;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty()[p]);
+                ++ring;
+            }
+        }
+    }
+    if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 9] = gtimer();
+    float y[2][NRW];
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int j = 0; j < NRW; ++j) y[s][j] = s < nseg ? warp_sum(acc[s][j]) : 0.f;
+    if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 10] = gtimer();
+    const float *resid = slot_resid(P, const_cast<float *>(slot));
+    if (lane == 0 && !ab) {
+#pragma unroll
+        for (int j = 0; j < NRW; ++j) {
+            const int r = r0 + j;
+            if (r >= nrows) continue;
+            if (opc == MK_OP_QKV) {
+                reinterpret_cast<float *>(ptr_a)[out0 + r] = y[0][j];
+            } else if (opc == MK_OP_O) {
+                const float v = resid[r] + y[0][j];
+                reinterpret_cast<float *>(ptr_a)[out0 + r] = v;
+                reinterpret_cast<float *>(ptr_b)[out0 + r] = v;
+            } else if (opc == MK_OP_UP) {
+                const float g = y[0][j], u = y[1][j];
+                reinterpret_cast<float *>(ptr_a)[out0 + r] = g / (1.0f + __expf(-g)) * u;
+            } else if (opc == MK_OP_DOWN) {
+                atomicAdd(reinterpret_cast<float *>(ptr_a) + out0 + r, y[0][j]);
+            } else if (opc == MK_OP_LM) {
+                reinterpret_cast<float *>(ptr_a)[out0 + r] = y[0][j];
+                const unsigned long long key = argmax_key(y[0][j], out0 + r);
+                if (key > lm_best) {
+                    lm_best = key;
+                    red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)P.step, key);
+                }
+            }
+        }
+    }
+    if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 11] = gtimer();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.act_empty()[i & 1]);  // activation buffer and slot no longer needed
 }
 
 // Split-KV attention of one (sequence, kv group, split): scores from the
@@ -320,7 +464,7 @@ DEV void gemv_tile(const KParams &P, const Smem &S, const WIns &I, int i, const 
 // units (max, sum), P.V, partial written out; the last split of the
 // (sequence, group) to arrive merges every split (log-sum-exp combine).
 template <int D>
-DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const float *slot, uint32_t &ring,
+DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
                    uint32_t &cph, bool &ab) {
     constexpr int PER = D / 32;
     constexpr int QS = D / 4 + 4;
@@ -334,7 +478,7 @@ DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const 
     const bool has_new = pos >= t0 && pos < t0 + T;
     const int ntot = ncache + (has_new ? 1 : 0);
     const float *qp = slot, *kn = slot + G * 4 * QS, *vn = kn + D;
-    float *sc = S.aux;                        // [G][T] scores, then probabilities
+    float *sc = S.aux();                        // [G][T] scores, then probabilities
     float *ow = sc + G * T;                   // [warp][G][D]
     float *ml = ow + CONSUMER_WARPS * G * D;  // [G] max, [G] sum
     const int rpp = P.page_bytes / (D * 2);
@@ -342,7 +486,7 @@ DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const 
     const uint32_t kring = ring, vring = ring + npg;
     for (int k = 0; k < npg; ++k) {
         const uint32_t p = (kring + k) % P.num_pages;
-        if (!ab) ab = !warp_wait_bar(P, S, &S.full[p], ((kring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[p], ((kring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
     }
     // scores: a warp takes 8 tokens at a time, 4 lanes per token, D/4 dims per lane
     const int qtr = lane & 3;
@@ -354,7 +498,7 @@ DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const 
         if (tk < ntot) {
             const uint8_t *row = nullptr;
             if (tk < ncache)
-                row = S.pages + (size_t)((kring + tk / rpp) % P.num_pages) * P.page_bytes + (size_t)(tk % rpp) * D * 2;
+                row = S.pages() + (size_t)((kring + tk / rpp) % P.num_pages) * P.page_bytes + (size_t)(tk % rpp) * D * 2;
 #pragma unroll
             for (int dd = 0; dd < DQ; dd += 8) {
                 float k8[8];
@@ -391,7 +535,7 @@ DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const 
     }
     __syncwarp();
     if (lane == 0)
-        for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty[(kring + k) % P.num_pages]);
+        for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(kring + k) % P.num_pages]);
     consumer_sync(P, S, cph, ab, i);
     // softmax statistics, one warp per head
     if (warp < G) {
@@ -412,7 +556,7 @@ DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const 
     }
     for (int k = 0; k < npg; ++k) {
         const uint32_t p = (vring + k) % P.num_pages;
-        if (!ab) ab = !warp_wait_bar(P, S, &S.full[p], ((vring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[p], ((vring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
     }
     ring = vring + npg;
     consumer_sync(P, S, cph, ab, i);
@@ -427,7 +571,7 @@ DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const 
             float v[PER];
             if (tk < ncache) {
                 const uint8_t *row =
-                    S.pages + (size_t)((vring + tk / rpp) % P.num_pages) * P.page_bytes + (size_t)(tk % rpp) * D * 2;
+                    S.pages() + (size_t)((vring + tk / rpp) % P.num_pages) * P.page_bytes + (size_t)(tk % rpp) * D * 2;
                 if constexpr (PER == 2) {
                     const uint32_t u = *reinterpret_cast<const uint32_t *>(row + lane * 4);
                     v[0] = __uint_as_float(u << 16);
@@ -459,8 +603,8 @@ DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const 
     }
     __syncwarp();
     if (lane == 0) {
-        for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty[(vring + k) % P.num_pages]);
-        mbar_arrive(&S.act_empty[i & 1]);
+        for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(vring + k) % P.num_pages]);
+        mbar_arrive(&S.act_empty()[i & 1]);
     }
     consumer_sync(P, S, cph, ab, i);
     float *part = reinterpret_cast<float *>(PTR(I, S_AT_PART));
@@ -478,7 +622,8 @@ DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const 
         part_at(ct, split)[D] = ml[ct];
         part_at(ct, split)[D + 1] = ml[G + ct];
     }
-    __threadfence();
+    // the acq_rel add below is cumulative over every partial this CTA wrote
+    // before the barrier, and acquires the other splits' partials
     consumer_sync(P, S, cph, ab, i);
     uint32_t *arrive = reinterpret_cast<uint32_t *>(PTR(I, S_AT_ARRIVE)) + ((size_t)layer * P.B + b) * P.Hkv + g;
     if (ct == 0) {
@@ -487,10 +632,10 @@ DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const 
             const uint32_t old = atom_acqrel_add(arrive, 1u);
             last = old == (uint32_t)(P.step + 1) * (uint32_t)nsplit - 1u;
         }
-        S.ctrl[3] = last;
+        S.ctrl()[3] = last;
     }
     consumer_sync(P, S, cph, ab, i);
-    if (S.ctrl[3] && !ab) {
+    if (S.ctrl()[3] && !ab) {
         float *out = reinterpret_cast<float *>(PTR(I, S_AT_OUT));
         for (int k = ct; k < G * D; k += CONSUMERS) {
             const int h = k / D, d = k % D;
@@ -505,14 +650,13 @@ DEV void attn_task(const KParams &P, const Smem &S, const WIns &I, int i, const 
             }
             out[(size_t)b * P.Hq * D + (size_t)(g * G + h) * D + d] = o / L;
         }
-        __threadfence();
     }
 }
 
-DEV void embed_task(const KParams &P, const Smem &S, const WIns &I, int i, bool ab) {
+DEV void embed_task(const KParams &P, const Smem S, const WIns &I, int i, bool ab) {
     const int ct = threadIdx.x - 64, lane = ct & 31;
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.act_empty[i & 1]);
+    if (lane == 0) mbar_arrive(&S.act_empty()[i & 1]);
     if (ab) return;
     const uint16_t *E = reinterpret_cast<const uint16_t *>(PTR(I, S_EMB_W));
     float *h = reinterpret_cast<float *>(PTR(I, S_EMB_H));
@@ -527,7 +671,6 @@ DEV void embed_task(const KParams &P, const Smem &S, const WIns &I, int i, bool 
         if (!host_tokens && ct == 0) tokens[(size_t)P.step * P.B + b] = tok;
         for (int k = ct; k < P.H; k += CONSUMERS) h[(size_t)b * P.H + k] = bf16_at(E, (size_t)tok * P.H + k);
     }
-    __threadfence();
 }
 
 }  // namespace mk

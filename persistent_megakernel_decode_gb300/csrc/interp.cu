@@ -28,7 +28,7 @@
 namespace mk {
 
 // ---------------------------------------------------------------- loader warp
-DEV void loader_role(const KParams &P, const Smem &S, const int32_t *myq) {
+DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int lane = threadIdx.x & 31;
     const uint64_t pol = evict_first_policy();
     uint32_t ring = 0;
@@ -44,42 +44,45 @@ DEV void loader_role(const KParams &P, const Smem &S, const int32_t *myq) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
             break;
         }
-        Seg seg[2];
-        const int nseg = describe(P, I, seg[0], seg[1]);
+        Seg s0, s1;
+        const int nseg = describe(P, I, s0, s1);
         bool stop = false;
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-            if (s >= nseg || stop) break;
-            const int rpp = seg[s].row_bytes > 0 ? PS / seg[s].row_bytes : 0;
+        if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 4] = gtimer();
+        // one segment: its rows packed into as few pages as the page size allows
+        auto issue = [&](const Seg &sg) {
+            const int rpp = sg.row_bytes > 0 ? PS / sg.row_bytes : 0;
             if (rpp < 1) {
                 if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
                 stop = true;
-                break;
+                return;
             }
-            for (int r = 0; r < seg[s].rows; r += rpp) {
-                const int nr = min(rpp, seg[s].rows - r);
+            for (int r = 0; r < sg.rows; r += rpp) {
+                const int nr = min(rpp, sg.rows - r);
                 const uint32_t p = ring % NP, use = ring / NP;
-                if (!warp_wait_bar(P, S, &S.empty[p], (use & 1) ^ 1, 0, i, opc)) {
+                if (!warp_wait_bar(P, S, &S.empty()[p], (use & 1) ^ 1, 0, i, opc)) {
                     stop = true;
-                    break;
+                    return;
                 }
                 if (lane == 0) {
-                    uint8_t *dst = S.pages + (size_t)p * PS;
-                    const uint32_t bytes = (uint32_t)nr * seg[s].row_bytes;
-                    mbar_expect_tx(&S.full[p], bytes);
-                    const uint8_t *src = seg[s].src + (long long)r * seg[s].stride;
-                    if (seg[s].stride == seg[s].row_bytes) {
-                        bulk_g2s(dst, src, bytes, &S.full[p], pol);
+                    uint8_t *dst = S.pages() + (size_t)p * PS;
+                    const uint32_t bytes = (uint32_t)nr * sg.row_bytes;
+                    mbar_expect_tx(&S.full()[p], bytes);
+                    const uint8_t *src = sg.src + (long long)r * sg.stride;
+                    if (sg.stride == sg.row_bytes) {
+                        bulk_g2s(dst, src, bytes, &S.full()[p], pol);
                     } else {
                         for (int j = 0; j < nr; ++j)
-                            bulk_g2s(dst + (size_t)j * seg[s].row_bytes, src + (long long)j * seg[s].stride,
-                                     seg[s].row_bytes, &S.full[p], pol);
+                            bulk_g2s(dst + (size_t)j * sg.row_bytes, src + (long long)j * sg.stride, sg.row_bytes,
+                                     &S.full()[p], pol);
                     }
                 }
                 __syncwarp();
                 ++ring;
             }
-        }
+        };
+        if (nseg > 0) issue(s0);
+        if (nseg > 1 && !stop) issue(s1);
+        if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 5] = gtimer();
         if (stop) break;
     }
     // no bulk copy may still target this CTA's shared memory when it exits
@@ -88,7 +91,7 @@ DEV void loader_role(const KParams &P, const Smem &S, const int32_t *myq) {
         const uint64_t t0 = gtimer();
         for (uint32_t k = first; k < ring; ++k) {
             const uint32_t p = k % NP, use = k / NP;
-            while (!mbar_test(&S.full[p], use & 1)) {
+            while (!mbar_test(&S.full()[p], use & 1)) {
                 if (gtimer() - t0 > 2 * P.timeout_ns) break;  // copies of valid memory land in microseconds
             }
         }
@@ -98,10 +101,12 @@ DEV void loader_role(const KParams &P, const Smem &S, const int32_t *myq) {
 
 // ---------------------------------------------------------------- activation-loader warp
 template <int MAXB>
-DEV void aloader_role(const KParams &P, const Smem &S, const int32_t *myq) {
+DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int lane = threadIdx.x & 31;
     long long prev_key = -1;
     bool ab = false;
+    int seen_ev = -1;           // last event seen satisfied, and the target it met
+    uint32_t seen_target = 0;
     WIns I;
     for (int i = 0; i < P.lmax; ++i) {
         const int32_t *ins = myq + (size_t)i * W_WORDS;
@@ -114,7 +119,7 @@ DEV void aloader_role(const KParams &P, const Smem &S, const int32_t *myq) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 1);
             ab = true;
         }
-        if (!ab) ab = !warp_wait_bar(P, S, &S.act_empty[sl], (use & 1) ^ 1, 1, i, opc);
+        if (!ab) ab = !warp_wait_bar(P, S, &S.act_empty()[sl], (use & 1) ^ 1, 1, i, opc);
         const int cnt = F(I, W_CNT);
         for (int w = 0; w < (cnt & 0xff) && !ab; ++w) {
             const uint32_t ew = (uint32_t)F(I, W_WAIT + 2 * w);
@@ -122,10 +127,15 @@ DEV void aloader_role(const KParams &P, const Smem &S, const int32_t *myq) {
             const int ev = (int)(ew & ~WAIT_PREV_EPOCH);
             const int epoch = P.step + 1 - ((ew & WAIT_PREV_EPOCH) ? 1 : 0);
             const uint32_t target = thr * (uint32_t)epoch;
-            if (target > 0) ab = !warp_wait_counter(P, S, ev, target, i, opc);
+            // counters only grow within a launch: a target already met needs no new round trip
+            if (target > 0 && !(ev == seen_ev && target <= seen_target)) {
+                ab = !warp_wait_counter(P, S, ev, target, i, opc);
+                seen_ev = ev;
+                seen_target = target;
+            }
         }
-        if (!ab && lane == 0 && P.trace) P.trace[((size_t)blockIdx.x * P.lmax + i) * 4 + 2] = gtimer();
-        float *slot = reinterpret_cast<float *>(S.act[sl]);
+        if (!ab && lane == 0 && P.trace) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 2] = gtimer();
+        float *slot = reinterpret_cast<float *>(S.act(sl));
         int flags = 0;
         if (opc == MK_OP_ATTN) {
             if (P.D == 64) stage_attn<64>(P, I, slot, ab);
@@ -135,38 +145,79 @@ DEV void aloader_role(const KParams &P, const Smem &S, const int32_t *myq) {
         } else if (opc >= MK_OP_QKV) {
             const long long key = ((long long)F(I, W_ROW) << 32) | (uint32_t)F(I, P_K0);
             if (key != prev_key || F(I, P_SNAP) > 0) {
-                stage_gemv<MAXB>(P, I, slot, ab);
+                // the previous instruction's consumers may still read the activation buffer
+                if (i > 0 && !ab)
+                    ab = !warp_wait_bar(P, S, &S.act_empty()[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1, 1, i, opc);
+                stage_gemv<MAXB>(P, I, S.abuf(), ab);
                 flags = SLOT_FRESH;
             }
+            if (opc == MK_OP_O) stage_resid(P, I, slot);
             prev_key = key;
         } else {
             prev_key = -1;
         }
         __syncwarp();
         if (lane == 0) {
-            S.ctrl[1 + sl] = flags;
-            mbar_arrive(&S.act_full[sl]);
+            S.ctrl()[1 + sl] = flags;
+            mbar_arrive(&S.act_full()[sl]);
         }
     }
 }
 
 // ---------------------------------------------------------------- consumer warps
-DEV void publish(const KParams &P, const Smem &S, const WIns &I, int i, int ct, uint32_t &cph, bool &ab) {
-    const int ns = (F(I, W_CNT) >> 8) & 0xff;
-    const int e0 = F(I, W_SIG), i0 = F(I, W_SIG + 1), e1 = F(I, W_SIG + 2), i1 = F(I, W_SIG + 3);
-    consumer_sync(P, S, cph, ab, i);
-    if (ct == 0 && !ab) {
-        if (ns > 0) red_release_add(P.counters + e0, (uint32_t)i0);
-        if (ns > 1) red_release_add(P.counters + e1, (uint32_t)i1);
+// Publisher warp.  Every consumer warp posts, with a CTA-scope release store,
+// how many queue slots it has finished.  The publisher takes the minimum over
+// the 8 warps: every instruction below it is fully written back.  One
+// GPU-scope fence then covers the whole batch (it is cumulative over what the
+// CTA-scope acquires observed) and the batch's signals are added to the event
+// counters -- so consumers never wait for a fence.
+DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
+    if ((threadIdx.x & 31) != 0) return;
+    int next = 0;  // first slot not yet published
+    uint64_t t0 = 0;
+    uint32_t it = 0;
+    while (next < P.lmax) {
+        if (__ldg(myq + (size_t)next * W_WORDS + W_OPC) == MK_OP_NOOP) break;  // NoOps only pad the tail
+        int done = P.lmax;
+#pragma unroll
+        for (int w = 0; w < CONSUMER_WARPS; ++w) done = min(done, ld_acquire_cta(&S.ctrl()[8 + w]));
+        if (done > next) {
+            const bool ab = S.ctrl()[0] != 0;
+            if (!ab) fence_acq_rel_gpu();
+            for (; next < done; ++next) {
+                const int32_t *ins = myq + (size_t)next * W_WORDS;
+                const int cnt = __ldg(ins + W_CNT), ns = (cnt >> 8) & 0xff;
+                if (ab) continue;
+                for (int k = 0; k < ns; ++k)
+                    red_relaxed_add(P.counters + __ldg(ins + W_SIG + 2 * k), (uint32_t)__ldg(ins + W_SIG + 2 * k + 1));
+            }
+            t0 = 0;
+            it = 0;
+        } else if ((++it & 63) == 0) {
+            const uint64_t now = gtimer();
+            if (t0 == 0) t0 = now;
+            if (aborted(P, S)) break;
+            if (now - t0 > P.timeout_ns) {
+                raise_error(P, S, MK_ERR_TIMEOUT, next, -1, (uint32_t)done, (uint32_t)next + 1, -1, 4);
+                break;
+            }
+        }
     }
 }
 
+// A consumer warp records that queue slot i is written back.
+DEV void handoff(const Smem S, int i) {
+    __syncwarp();
+    const int warp = (threadIdx.x >> 5) - 2;
+    if ((threadIdx.x & 31) == 0) st_release_cta(&S.ctrl()[8 + warp], i + 1);
+}
+
 template <int MAXB>
-DEV void consumer_role(const KParams &P, const Smem &S, const int32_t *myq) {
+DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int ct = threadIdx.x - 64, lane = ct & 31;
     uint32_t ring = 0, cph = 0;
     bool ab = false;
-    XRegs<MAXB> xr;
+    unsigned long long lm_best = 0;
     WIns I;
     for (int i = 0; i < P.lmax; ++i) {
         const int32_t *ins = myq + (size_t)i * W_WORDS;
@@ -176,29 +227,43 @@ DEV void consumer_role(const KParams &P, const Smem &S, const int32_t *myq) {
         uint64_t t_start = 0;
         if (ct == 0 && P.trace) t_start = gtimer();
         const int sl = i & 1;
-        if (!ab) ab = !warp_wait_bar(P, S, &S.act_full[sl], (uint32_t)(i >> 1) & 1, 2, i, opc);
-        const bool fresh = (S.ctrl[1 + sl] & SLOT_FRESH) != 0;
-        const float *slot = reinterpret_cast<const float *>(S.act[sl]);
+        if (P.trace && ct == 0 && !mbar_test(&S.act_full()[sl], (uint32_t)(i >> 1) & 1))
+            P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 12] = 1;   // activation not ready on arrival
+        if (!ab) ab = !warp_wait_bar(P, S, &S.act_full()[sl], (uint32_t)(i >> 1) & 1, 2, i, opc);
+        if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 13] = gtimer();
+        const float *slot = reinterpret_cast<const float *>(S.act(sl));
         if (opc == MK_OP_ATTN) {
             if (P.D == 64) attn_task<64>(P, S, I, i, slot, ring, cph, ab);
             else attn_task<128>(P, S, I, i, slot, ring, cph, ab);
         } else if (opc == MK_OP_EMBED) {
+            consumer_sync(P, S, cph, ab, i);
             embed_task(P, S, I, i, ab);
         } else if (opc >= MK_OP_QKV) {
-            const int nch = (F(I, P_KC) / 8 + CONSUMERS - 1) / CONSUMERS;
-            if (nch <= 1) gemv_tile<MAXB, 1>(P, S, I, i, slot, fresh, xr, ring, cph, ab);
-            else if constexpr (XRegs<MAXB>::NCH >= 2) {
-                if (nch <= 2) gemv_tile<MAXB, 2>(P, S, I, i, slot, fresh, xr, ring, cph, ab);
-                else if constexpr (XRegs<MAXB>::NCH >= 4) gemv_tile<MAXB, 4>(P, S, I, i, slot, fresh, xr, ring, cph, ab);
+            if constexpr (MAXB == 1) {
+                const int two = F(I, P_NROWS) > CONSUMER_WARPS;
+                const int kg = (F(I, P_KC) / 8 + 31) / 32;  // 8-element groups per lane
+                if (kg <= 1) two ? gemv_rows<2, 1>(P, S, I, i, slot, ring, lm_best, ab) : gemv_rows<1, 1>(P, S, I, i, slot, ring, lm_best, ab);
+                else if (kg <= 3) two ? gemv_rows<2, 3>(P, S, I, i, slot, ring, lm_best, ab) : gemv_rows<1, 3>(P, S, I, i, slot, ring, lm_best, ab);
+                else if (kg <= 8) two ? gemv_rows<2, 8>(P, S, I, i, slot, ring, lm_best, ab) : gemv_rows<1, 8>(P, S, I, i, slot, ring, lm_best, ab);
+                else two ? gemv_rows<2, 0>(P, S, I, i, slot, ring, lm_best, ab) : gemv_rows<1, 0>(P, S, I, i, slot, ring, lm_best, ab);
+            } else {
+                const int nch = (F(I, P_KC) / 8 + CONSUMERS - 1) / CONSUMERS;
+                constexpr int NCHMAX = MAXB >= 8 ? 1 : (MAXB >= 4 ? 2 : 4);
+                if (nch <= 1) gemv_tile<MAXB, 1>(P, S, I, i, slot, ring, cph, ab);
+                else if constexpr (NCHMAX >= 2) {
+                    if (nch <= 2) gemv_tile<MAXB, 2>(P, S, I, i, slot, ring, cph, ab);
+                    else if constexpr (NCHMAX >= 4) gemv_tile<MAXB, 4>(P, S, I, i, slot, ring, cph, ab);
+                }
             }
         } else {  // COUNTER: the slot handshake only
+            consumer_sync(P, S, cph, ab, i);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&S.act_empty[sl]);
+            if (lane == 0) mbar_arrive(&S.act_empty()[sl]);
         }
-        publish(P, S, I, i, ct, cph, ab);
+        handoff(S, i);
         const int task = F(I, W_TASK);
         if (ct == 0 && P.trace) {
-            uint64_t *tr = P.trace + ((size_t)blockIdx.x * P.lmax + i) * 4;
+            uint64_t *tr = P.trace + ((size_t)blockIdx.x * P.lmax + i) * 16;
             tr[0] = (uint64_t)opc | ((uint64_t)(uint32_t)task << 32);
             tr[1] = t_start;
             tr[3] = gtimer();
@@ -209,30 +274,28 @@ DEV void consumer_role(const KParams &P, const Smem &S, const int32_t *myq) {
 // ---------------------------------------------------------------- kernel
 template <int MAXB>
 __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
-    extern __shared__ __align__(1024) uint8_t smem[];
     Smem S;
-    S.act[0] = smem;
-    S.act[1] = smem + P.act_bytes;
-    S.pages = smem + 2 * P.act_bytes;
-    S.aux = reinterpret_cast<float *>(S.pages + (size_t)P.num_pages * P.page_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(S.aux) + P.aux_bytes);
-    S.full = bars;
-    S.empty = bars + P.num_pages;
-    S.act_full = bars + 2 * P.num_pages;
-    S.act_empty = bars + 2 * P.num_pages + 2;
-    S.cbar = bars + 2 * P.num_pages + 4;
-    S.ctrl = reinterpret_cast<volatile int *>(reinterpret_cast<uint8_t *>(bars) + MBAR_BYTES);
+    S.o_abuf = 0;
+    S.o_act0 = P.abuf_bytes;
+    S.act_stride = P.act_bytes;
+    S.o_pages = P.abuf_bytes + 2 * P.act_bytes;
+    S.o_aux = S.o_pages + P.num_pages * P.page_bytes;
+    S.o_red0 = S.o_aux + P.aux_bytes - 2 * P.red_bytes;
+    S.red_stride = P.red_bytes;
+    S.o_bars = S.o_aux + P.aux_bytes;
+    S.o_ctrl = S.o_bars + MBAR_BYTES;
+    S.num_pages = P.num_pages;
     if (threadIdx.x == 0) {
         for (int p = 0; p < P.num_pages; ++p) {
-            mbar_init(&S.full[p], 1);
-            mbar_init(&S.empty[p], CONSUMER_WARPS);
+            mbar_init(&S.full()[p], 1);
+            mbar_init(&S.empty()[p], CONSUMER_WARPS);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&S.act_full[s], 1);
-            mbar_init(&S.act_empty[s], CONSUMER_WARPS);
+            mbar_init(&S.act_full()[s], 1);
+            mbar_init(&S.act_empty()[s], CONSUMER_WARPS);
         }
-        mbar_init(S.cbar, CONSUMER_WARPS);
-        for (int k = 0; k < 4; ++k) S.ctrl[k] = 0;
+        mbar_init(S.cbar(), CONSUMER_WARPS);
+        for (int k = 0; k < 16; ++k) S.ctrl()[k] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -241,6 +304,7 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
     const int warp = threadIdx.x >> 5;
     if (warp == 0) loader_role(P, S, myq);
     else if (warp == 1) aloader_role<MAXB>(P, S, myq);
+    else if (warp == PUBLISHER_WARP) publisher_role(P, S, myq);
     else consumer_role<MAXB>(P, S, myq);
     __syncthreads();
 }
@@ -355,7 +419,9 @@ static KParams base_params(const Plan &p, uint8_t *ws) {
     k.num_pages = p.num_pages;
     k.page_bytes = p.page_bytes;
     k.act_bytes = p.act_bytes;
+    k.abuf_bytes = p.abuf_bytes;
     k.aux_bytes = p.aux_bytes;
+    k.red_bytes = p.red_bytes;
     k.smem_bytes = p.smem_bytes;
     const mk_model_desc &m = p.model;
     k.B = p.B;
@@ -485,7 +551,7 @@ int mk_read_trace(mk_plan_t plan, void *workspace, uint64_t *out) {
     if (!plan || !workspace || !out) return set_error(MK_ERR_INVALID, "null argument");
     size_t slots = 0;
     for (auto &s : plan->p.segments) slots += (size_t)s.workers * s.lmax;
-    cudaError_t e = cudaMemcpy(out, static_cast<uint8_t *>(workspace) + plan->p.ws.trace, slots * 32,
+    cudaError_t e = cudaMemcpy(out, static_cast<uint8_t *>(workspace) + plan->p.ws.trace, slots * 128,
                                cudaMemcpyDeviceToHost);
     return e == cudaSuccess ? MK_OK : cuda_fail(e, "read trace");
 }

@@ -78,14 +78,16 @@ struct KParams {
     uint64_t timeout_ns;
     int lmax, num_workers, num_ops, num_events;
     int step, flags;
-    int num_pages, page_bytes, act_bytes, aux_bytes, smem_bytes;
+    int num_pages, page_bytes, act_bytes, abuf_bytes, aux_bytes, red_bytes, smem_bytes;
     int B, H, Hq, Hkv, D, F, V, L, Smax, qk_norm, nsplit_max;
     float eps, theta;
 };
 
 constexpr int CONSUMER_WARPS = 8;
 constexpr int CONSUMERS = CONSUMER_WARPS * 32;
-constexpr int THREADS = CONSUMERS + 64;   // + loader warp + activation-loader warp
+constexpr int THREADS = CONSUMERS + 96;   // + loader, activation-loader and publisher warps
+constexpr int PUBLISHER_WARP = CONSUMER_WARPS + 2;
+constexpr int RESID_ROWS = 16;           // residual slice staged per slot for O tiles
 constexpr int MAX_TILE_ROWS = 16;
 
 }  // namespace mk
@@ -98,5 +100,5 @@ inline int red_bytes(int B) { return CONSUMER_WARPS * MAX_TILE_ROWS * B * 4; }
 inline int attn_aux_bytes(int G, int T, int D) { return (G * T + CONSUMER_WARPS * G * D + 8 * G) * 4; }
 constexpr int MBAR_BYTES = 512;    // up to 64 mbarriers
 constexpr int CTRL_BYTES = 128;
-constexpr int MAX_PAGES = 28;      // 2 * MAX_PAGES + 5 mbarriers must fit MBAR_BYTES
+constexpr int MAX_PAGES = 26;      // 2 * MAX_PAGES + 9 mbarriers must fit MBAR_BYTES
 }  // namespace mk

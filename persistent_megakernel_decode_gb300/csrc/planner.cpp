@@ -570,10 +570,15 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     // shared memory budget
     int kmax = std::max(std::max(H, Hq * D), kn_kc);
     int attn_slot = (G * (D + 16) + 2 * D) * 4;
-    p.act_bytes = round_up(std::max(B * kmax * 4, attn_slot), 128);
+    // GEMV activation buffer [B][K]; two small slots for per-instruction data
+    // (attention q / new k / new v, the residual slice of O tiles)
+    p.abuf_bytes = round_up(B * kmax * 4, 128);
+    p.act_bytes = round_up(attn_slot + B * RESID_ROWS * 4, 128);
     const int maxb = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8;  // kernel batch template
-    int aux = round_up(std::max(red_bytes(maxb), attn_aux_bytes(G, kn_T, D)), 128);
-    int fixed = 2 * p.act_bytes + aux + MBAR_BYTES + CTRL_BYTES;
+    // attention scratch, then two reduction buffers (double-buffered across tiles)
+    p.red_bytes = round_up(red_bytes(maxb), 128);
+    int aux = round_up(attn_aux_bytes(G, kn_T, D), 128) + 2 * p.red_bytes;
+    int fixed = p.abuf_bytes + 2 * p.act_bytes + aux + MBAR_BYTES + CTRL_BYTES;
     p.aux_bytes = aux;
     p.num_pages = std::min(MAX_PAGES, (smem_per_cta - fixed) / p.page_bytes);
     p.smem_bytes = fixed + p.num_pages * p.page_bytes;

@@ -281,7 +281,7 @@ class Session:
 
     def trace(self) -> np.ndarray:
         i = self.plan.info()
-        out = np.zeros((i["num_workers"], i["lmax"], 4), np.uint64)
+        out = np.zeros((i["num_workers"], i["lmax"], 16), np.uint64)
         _check(load().mk_read_trace(self.plan.h, C.c_void_p(self.ws_ptr), out.ctypes.data))
         return out
 
