@@ -250,6 +250,33 @@ int mk_read_counters(mk_plan_t plan, void *workspace, uint32_t *out);
  * globaltimer ns for times.  Only filled by runs with MK_RUN_TRACE. */
 int mk_read_trace(mk_plan_t plan, void *workspace, uint64_t *out);
 
+/* Allocation-free variant of mk_run (no counterpart on the source pages).
+ *
+ * For callers that must not allocate device memory themselves: code embedded
+ * in a host application whose own allocator owns the whole device (a direct
+ * cudaMalloc there would exceed or fragment that allocator's budget), or a
+ * latency-critical loop in which cudaMalloc could block or synchronise the
+ * device.  Such callers still pass every input and output through mk_bind();
+ * only the workspace (queue, operand table, event counters, activations,
+ * error record) moves into a fixed array inside this library.
+ *
+ * The array is a file-scope static device array of MK_STATIC_WORKSPACE_BYTES
+ * (64 MiB); every GPU that loads the library holds it until the process exits.
+ * Plans whose mk_plan_info.workspace_bytes exceed it are rejected with
+ * MK_ERR_INVALID.  The first call on each device (with that device current)
+ * looks up the array's device address; make that first call before any
+ * stream capture.  All calls share the one array and it keeps the previous
+ * call's contents: counters and the error record are cleared when first_step
+ * is 0, exactly as in mk_run, and a call made with a different plan than the
+ * previous one uploads its queue again.  Calls whose work overlaps on the GPU
+ * (other streams, other threads) race on the array -- serialise them.
+ * This entry point calls no cudaMalloc, cudaFree or allocating library
+ * routine.  *workspace_out (may be NULL) receives the array's device address,
+ * to pass to mk_sync_status(), mk_read_counters() and mk_read_trace(). */
+#define MK_STATIC_WORKSPACE_BYTES (64u << 20)
+int mk_run_static(mk_plan_t plan, int first_step, int num_steps, uint32_t flags, uint64_t timeout_ns, void *stream,
+                  uint64_t *workspace_out);
+
 /* Free the plan's host memory.  NULL-safe.  Never touches device memory. */
 void mk_free(mk_plan_t plan);
 

@@ -20,6 +20,7 @@
 // kernel always returns.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "dev_ops.cuh"
@@ -512,6 +513,50 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
         }
     }
     return MK_OK;
+}
+
+// ---------------------------------------------------------------- allocation-free entry point
+// The workspace of mk_run_static(): a fixed device array owned by this
+// library.  Host code only ever sees the array's host-side stand-in; the
+// device address comes from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) uint8_t g_static_workspace[MK_STATIC_WORKSPACE_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_addr[kMaxDevices] = {};      // device address of the array, per device
+const void *g_static_owner[kMaxDevices] = {};  // plan whose queue the array holds
+}  // namespace
+
+int mk_run_static(mk_plan_t plan, int first_step, int num_steps, uint32_t flags, uint64_t timeout_ns, void *stream,
+                  uint64_t *workspace_out) {
+    if (!plan) return set_error(MK_ERR_INVALID, "null plan");
+    if (plan->p.ws.total > MK_STATIC_WORKSPACE_BYTES) {
+        char buf[160];
+        std::snprintf(buf, sizeof buf, "plan needs %llu workspace bytes; the static workspace holds %u",
+                      (unsigned long long)plan->p.ws.total, (unsigned)MK_STATIC_WORKSPACE_BYTES);
+        return set_error(MK_ERR_INVALID, buf);
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return set_error(MK_ERR_INVALID, "device ordinal out of range");
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (!g_static_addr[dev]) {
+            void *addr = nullptr;
+            e = cudaGetSymbolAddress(&addr, g_static_workspace);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static workspace)");
+            g_static_addr[dev] = addr;
+        }
+        ws = g_static_addr[dev];
+        // another plan may have uploaded its queue into the shared array since
+        if (g_static_owner[dev] != plan) plan->p.uploaded_ws = nullptr;
+        g_static_owner[dev] = plan;
+    }
+    if (workspace_out) *workspace_out = (uint64_t)(uintptr_t)ws;
+    return mk_run(plan, ws, MK_STATIC_WORKSPACE_BYTES, first_step, num_steps, flags, timeout_ns, stream);
 }
 
 int mk_sync_status(mk_plan_t plan, void *workspace, void *stream, mk_error_record *rec) {

@@ -32,7 +32,9 @@ BIND = {n: i for i, n in enumerate([
 PER_LAYER = ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "norm_attn", "norm_mlp", "qnorm", "knorm")
 
 EXPORTED = ["mk_plan", "mk_plan_graph", "mk_plan_info_get", "mk_plan_export", "mk_bind", "mk_run",
-            "mk_sync_status", "mk_read_counters", "mk_read_trace", "mk_free", "mk_last_error", "mk_argmax_index"]
+            "mk_sync_status", "mk_read_counters", "mk_read_trace", "mk_free", "mk_last_error", "mk_argmax_index",
+            "mk_run_static"]
+STATIC_WORKSPACE_BYTES = 64 << 20
 
 
 class MkError(RuntimeError):
@@ -109,6 +111,7 @@ def load():
     lib.mk_plan_export.argtypes = [P, P, P, P, P]
     lib.mk_bind.argtypes = [P, C.c_int, C.c_int, C.c_uint64]
     lib.mk_run.argtypes = [P, P, C.c_size_t, C.c_int, C.c_int, C.c_uint32, C.c_uint64, P]
+    lib.mk_run_static.argtypes = [P, C.c_int, C.c_int, C.c_uint32, C.c_uint64, P, C.POINTER(C.c_uint64)]
     lib.mk_sync_status.argtypes = [P, P, P, C.POINTER(ErrorRecord)]
     lib.mk_read_counters.argtypes = [P, P, P]
     lib.mk_read_trace.argtypes = [P, P, P]
@@ -265,6 +268,22 @@ class Session:
         rec = ErrorRecord()
         rc = load().mk_sync_status(self.plan.h, C.c_void_p(self.ws_ptr), C.c_void_p(self.stream.cuda_stream),
                                    C.byref(rec))
+        if rc != MK_OK:
+            raise MkError(rc, load().mk_last_error().decode())
+        return rec
+
+    def run_static(self, first_step: int, num_steps: int = 1, host_tokens: bool = False, timeout_ns: int = 0) -> int:
+        """Run through mk_run_static (library-owned workspace, no device allocation).
+        Returns the device address of that workspace, for sync_static()."""
+        addr = C.c_uint64(0)
+        flags = RUN_HOST_TOKENS if host_tokens else 0
+        _check(load().mk_run_static(self.plan.h, first_step, num_steps, flags, timeout_ns,
+                                    C.c_void_p(self.stream.cuda_stream), C.byref(addr)))
+        return addr.value
+
+    def sync_static(self, addr: int) -> ErrorRecord:
+        rec = ErrorRecord()
+        rc = load().mk_sync_status(self.plan.h, C.c_void_p(addr), C.c_void_p(self.stream.cuda_stream), C.byref(rec))
         if rc != MK_OK:
             raise MkError(rc, load().mk_last_error().decode())
         return rec
