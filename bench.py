@@ -191,6 +191,9 @@ def run_mk(args, w, rank, world, dist):
     kc, vc = synth.make_cache(s, w.batch, smax, w.cache_seed, device=dev)
     stream = torch.cuda.Stream(dev)
     target = {"mode": rt.MODE_PER_OP} if args.mode == "per_op" else {}
+    for kv in args.knob:
+        k, v = kv.split("=")
+        target[k] = int(v)
     sess = rt.Session(s, weights, kc, vc, seq0, max_steps, stream=stream, **target)
     info = sess.plan.info()
     sess.tokens[0] = torch.tensor(synth.first_tokens(w), dtype=torch.int32, device=dev)
@@ -280,6 +283,7 @@ def main():
     ap.add_argument("--workload", default="llama1b_b1")
     ap.add_argument("--mode", default="megakernel", choices=["megakernel", "per_op"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--knob", action="append", default=[], help="planner knob, e.g. attn_split=512")
     args = ap.parse_args()
     from persistent_megakernel_decode_gb300 import synth
     w = synth.WORKLOADS[args.workload]

@@ -637,16 +637,40 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, const f
     consumer_sync(P, S, cph, ab, i);
     if (S.ctrl()[3] && !ab) {
         float *out = reinterpret_cast<float *>(PTR(I, S_AT_OUT));
+        // log-sum-exp combine; partials are loaded 8 splits at a time so their
+        // L2 round trips overlap instead of queueing one behind another
         for (int k = ct; k < G * D; k += CONSUMERS) {
             const int h = k / D, d = k % D;
-            float M = -INFINITY;
-            for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(part_at(h, s) + D));
-            float L = 0.f, o = 0.f;
-            for (int s = 0; s < nsplit; ++s) {
-                const float *ps = part_at(h, s);
-                const float f = exp2f(__ldcg(ps + D) - M);
-                L += f * __ldcg(ps + D + 1);
-                o += f * __ldcg(ps + d);
+            float M = -INFINITY, L = 0.f, o = 0.f;
+            for (int s0 = 0; s0 < nsplit; s0 += 8) {
+                float mv[8], lv[8], ov[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int s = s0 + u;
+                    if (s < nsplit) {
+                        const float *ps = part_at(h, s);
+                        mv[u] = __ldcg(ps + D);
+                        lv[u] = __ldcg(ps + D + 1);
+                        ov[u] = __ldcg(ps + d);
+                    } else {
+                        mv[u] = -INFINITY;
+                        lv[u] = 0.f;
+                        ov[u] = 0.f;
+                    }
+                }
+                float Mn = M;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) Mn = fmaxf(Mn, mv[u]);
+                const float r = exp2f(M - Mn);  // rescale what was accumulated so far
+                L *= r;
+                o *= r;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float f = exp2f(mv[u] - Mn);
+                    L += f * lv[u];
+                    o += f * ov[u];
+                }
+                M = Mn;
             }
             out[(size_t)b * P.Hq * D + (size_t)(g * G + h) * D + d] = o / L;
         }
