@@ -42,7 +42,7 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("interp.cu", "mk_internal.h", "planner.cpp"):
+    for f in ("interp.cu", "dev_common.cuh", "dev_ops.cuh", "mk_internal.h", "planner.cpp"):
         with open(os.path.join(ROOT, "persistent_megakernel_decode_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -262,7 +262,8 @@ def run_mk(args, w, rank, world, dist):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seq_len, "layers": s.L, "hidden": s.H,
-                   "vocab": s.V, "mode": args.mode, "l2": "weights (2.5 GB) exceed L2 (129 MB); no flush",
+                   "vocab": s.V, "mode": args.mode,
+                   "l2": f"weights ({alg / 1e9:.2f} GB) exceed L2 (129 MB); no flush",
                    "parallelism": f"replicas{world}"},
         "step_us": {"median": float(np.median(step_ms)) * 1e3, "p10": float(np.percentile(step_ms, 10)) * 1e3,
                     "p90": float(np.percentile(step_ms, 90)) * 1e3},
@@ -284,9 +285,14 @@ def main():
     ap.add_argument("--mode", default="megakernel", choices=["megakernel", "per_op"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--knob", action="append", default=[], help="planner knob, e.g. attn_split=512")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="keep only the first N decoder layers (a small case for profiling, not a bench line)")
     args = ap.parse_args()
+    from dataclasses import replace
     from persistent_megakernel_decode_gb300 import synth
     w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        w = replace(w, name=f"{w.name}_L{args.layers}", shape=replace(w.shape, L=args.layers))
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, w, rank)
