@@ -46,6 +46,16 @@ DEV int ld_acquire_cta(volatile int *p) {
     asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr((const void *)p)) : "memory");
     return v;
 }
+DEV int ld_relaxed_cta(volatile int *p) {
+    int v;
+    asm volatile("ld.relaxed.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr((const void *)p)) : "memory");
+    return v;
+}
+DEV int atom_add_acqrel_cta(volatile int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.cta.shared.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(saddr((const void *)p)), "r"(v) : "memory");
+    return old;
+}
 DEV void red_release_add(uint32_t *p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -72,6 +82,16 @@ DEV bool mbar_test(uint64_t *b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Like mbar_test, but the thread may sleep up to about `ns` nanoseconds for the phase.
+DEV bool mbar_wait_hint(uint64_t *b, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(saddr(b)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 // Weight and cache rows are read once per step: evict-first keeps them from
 // displacing activations, counters and the queue in L2.
 DEV uint64_t evict_first_policy() {
@@ -88,6 +108,13 @@ DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uin
 }
 DEV void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p)); }
 
+// Two fp32 fused multiply-adds in one instruction: acc.{lo,hi} += a.{lo,hi} * b.{lo,hi}, each rounded
+// to nearest like fmaf.
+DEV void fma2(uint64_t &acc, uint64_t a, uint64_t b) { asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b)); }
+DEV uint64_t pack2(float lo, float hi) { return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32); }
+DEV float sum2(uint64_t v) { return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32)); }
+// A 32-bit word of two bf16 weights as an fp32 pair (exact).
+DEV uint64_t bf16x2_pair(uint32_t w) { return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); }
 DEV void bf16x8(uint4 w, float f[8]) {
     f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xffff0000u);
     f[2] = __uint_as_float(w.y << 16); f[3] = __uint_as_float(w.y & 0xffff0000u);
@@ -148,18 +175,20 @@ extern __shared__ __align__(1024) uint8_t mk_smem[];
 
 // Offsets into the dynamic shared memory and accessors for its regions.
 struct Smem {
-    uint32_t o_abuf;      // GEMV activation [B][K] (RMSNorm-ed where the op fuses it)
+    uint32_t o_abuf;      // GEMV activation [B][K] (RMSNorm-ed where the op fuses it); one per
+    uint32_t abuf_stride; // slot when two fit (stride in bytes), else one shared buffer (stride 0)
     uint32_t o_act0;      // slot 0; slot s at o_act0 + s * act_stride
     uint32_t act_stride;
     uint32_t o_pages;     // page ring
     uint32_t o_aux;       // op scratch (attention scores, partial outputs)
     uint32_t o_red0;      // cross-warp reduction buffers, alternating per instruction
     uint32_t red_stride;  // bytes
-    uint32_t o_bars;      // full[NP], empty[NP], act_full[2], act_empty[2], consumer barrier
+    uint32_t o_bars;      // full[NP], empty[NP], act_full[2], act_empty[2], consumer barrier, doorbell
     uint32_t o_ctrl;      // [0] abort, [1..2] slot flags, [3] attention: last split,
-                          // [8..15] consumer warp progress (instructions finished + 1)
+                          // [8..15] consumer warp progress (instructions finished + 1),
+                          // [16..19] reduction buffer arrivals, [20..23] reduction buffer epilogues done
     int num_pages;
-    DEV float *abuf() const { return reinterpret_cast<float *>(mk_smem + o_abuf); }
+    DEV float *abuf(int s) const { return reinterpret_cast<float *>(mk_smem + o_abuf + s * abuf_stride); }
     DEV uint8_t *act(int s) const { return mk_smem + o_act0 + s * act_stride; }
     DEV uint8_t *pages() const { return mk_smem + o_pages; }
     DEV float *aux() const { return reinterpret_cast<float *>(mk_smem + o_aux); }
@@ -169,37 +198,52 @@ struct Smem {
     DEV uint64_t *act_full() const { return full() + 2 * num_pages; }
     DEV uint64_t *act_empty() const { return full() + 2 * num_pages + 2; }
     DEV uint64_t *cbar() const { return full() + 2 * num_pages + 4; }
+    DEV uint64_t *bell() const { return full() + 2 * num_pages + 5; }  // rung by every consumer hand-off
     DEV volatile int *ctrl() const { return reinterpret_cast<volatile int *>(mk_smem + o_ctrl); }
 };
 
 constexpr int SLOT_FRESH = 1;
+constexpr int C_RED_ARR = 16;   // ctrl words: arrivals per reduction buffer (monotone)
+constexpr int C_RED_FIN = 20;   // ctrl words: finished epilogues per reduction buffer (monotone)
+constexpr int CTRL_WORDS = 24;
 
-DEV void raise_error(const KParams &P, const Smem S, int code, int slot, int event, uint32_t obs, uint32_t need,
-                     int opc, int role) {
-    if (atomicCAS(&P.err[E_CODE], 0u, (uint32_t)code) == 0u) {
-        P.err[E_WORKER] = blockIdx.x;
-        P.err[E_SLOT] = (uint32_t)slot;
-        P.err[E_EVENT] = (uint32_t)event;
-        P.err[E_OBSERVED] = obs;
-        P.err[E_NEEDED] = need;
-        P.err[E_OPCODE] = (uint32_t)opc;
-        P.err[E_ROLE] = (uint32_t)role;
+// Error path, kept out of line so that the hot loops stay small.
+static __device__ __noinline__ void raise_error_at(uint32_t *err, Smem S, int code, int slot, int event, uint32_t obs,
+                                            uint32_t need, int opc, int role) {
+    if (atomicCAS(&err[E_CODE], 0u, (uint32_t)code) == 0u) {
+        err[E_WORKER] = blockIdx.x;
+        err[E_SLOT] = (uint32_t)slot;
+        err[E_EVENT] = (uint32_t)event;
+        err[E_OBSERVED] = obs;
+        err[E_NEEDED] = need;
+        err[E_OPCODE] = (uint32_t)opc;
+        err[E_ROLE] = (uint32_t)role;
     }
-    atomicExch(&P.err[E_ABORT], 1u);
+    atomicExch(&err[E_ABORT], 1u);
     S.ctrl()[0] = 1;
 }
+DEV void raise_error(const KParams &P, const Smem S, int code, int slot, int event, uint32_t obs, uint32_t need,
+                     int opc, int role) {
+    raise_error_at(P.err, S, code, slot, event, obs, need, opc, role);
+}
 
-DEV bool aborted(const KParams &P, const Smem S) {
+DEV bool aborted_at(uint32_t *err, const Smem S) {
     if (S.ctrl()[0]) return true;
-    if (ld_relaxed(&P.err[E_ABORT])) {
+    if (ld_relaxed(&err[E_ABORT])) {
         S.ctrl()[0] = 1;
         return true;
     }
     return false;
 }
+DEV bool aborted(const KParams &P, const Smem S) { return aborted_at(P.err, S); }
 
-// Whole-warp bounded wait on an mbarrier phase; uniform result, false = abort.
-DEV bool warp_wait_bar(const KParams &P, const Smem S, uint64_t *bar, uint32_t parity, int role, int slot, int opc) {
+// Bounded whole-warp waits.  Each has an inline fast path (the condition
+// already holds: one test) and an out-of-line polling loop that gives up
+// after the launch's timeout or on a grid-wide abort (uniform result,
+// false = abort).  Keeping the loops out of line keeps the code of the hot
+// paths small enough for the instruction cache.
+static __device__ __noinline__ bool wait_bar_slow(uint32_t *err, uint64_t timeout_ns, Smem S, uint64_t *bar,
+                                           uint32_t parity, int role, int slot, int opc) {
     const int lane = threadIdx.x & 31;
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
@@ -209,9 +253,9 @@ DEV bool warp_wait_bar(const KParams &P, const Smem S, uint64_t *bar, uint32_t p
             if (lane == 0) {
                 uint64_t now = gtimer();
                 if (t0 == 0) t0 = now;
-                if (aborted(P, S)) stop = 1;
-                else if (now - t0 > P.timeout_ns) {
-                    raise_error(P, S, MK_ERR_TIMEOUT, slot, -1, 0, parity, opc, role);
+                if (aborted_at(err, S)) stop = 1;
+                else if (now - t0 > timeout_ns) {
+                    raise_error_at(err, S, MK_ERR_TIMEOUT, slot, -1, 0, parity, opc, role);
                     stop = 1;
                 }
             }
@@ -219,29 +263,69 @@ DEV bool warp_wait_bar(const KParams &P, const Smem S, uint64_t *bar, uint32_t p
         }
     }
 }
+DEV bool warp_wait_bar(const KParams &P, const Smem S, uint64_t *bar, uint32_t parity, int role, int slot, int opc) {
+    if (__all_sync(FULL, mbar_test(bar, parity))) return true;
+    return wait_bar_slow(P.err, P.timeout_ns, S, bar, parity, role, slot, opc);
+}
 
-// Whole-warp bounded wait for counter >= target (acquire on every poll).
-DEV bool warp_wait_counter(const KParams &P, const Smem S, int ev, uint32_t target, int slot, int opc) {
+// Shared flag word >= target (acquire, CTA scope).
+static __device__ __noinline__ bool wait_smem_slow(uint32_t *err, uint64_t timeout_ns, Smem S, volatile int *flag,
+                                            uint32_t target, int slot, int opc) {
     const int lane = threadIdx.x & 31;
-    const uint32_t *c = P.counters + ev;
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
-        uint32_t v = ld_acquire(c);
-        if (__all_sync(FULL, v >= target)) return true;
+        if (__all_sync(FULL, (uint32_t)ld_acquire_cta(flag) >= target)) return true;
         if ((it & 15) == 15) {
             int stop = 0;
             if (lane == 0) {
                 uint64_t now = gtimer();
                 if (t0 == 0) t0 = now;
-                if (aborted(P, S)) stop = 1;
-                else if (now - t0 > P.timeout_ns) {
-                    raise_error(P, S, MK_ERR_TIMEOUT, slot, ev, v, target, opc, 1);
+                if (aborted_at(err, S)) stop = 1;
+                else if (now - t0 > timeout_ns) {
+                    raise_error_at(err, S, MK_ERR_TIMEOUT, slot, -1, 0, target, opc, 2);
                     stop = 1;
                 }
             }
             if (__shfl_sync(FULL, stop, 0)) return false;
         }
     }
+}
+DEV bool warp_wait_smem(const KParams &P, const Smem S, volatile int *flag, uint32_t target, int slot, int opc) {
+    if (__all_sync(FULL, (uint32_t)ld_acquire_cta(flag) >= target)) return true;
+    return wait_smem_slow(P.err, P.timeout_ns, S, flag, target, slot, opc);
+}
+
+// Event counter >= target.  Polls are relaxed loads (an acquire load per
+// poll would also drop the SM's L1 each time); once the target is seen, one
+// fence.acq_rel turns the last poll into the acquire.
+static __device__ __noinline__ bool wait_counter_slow(uint32_t *err, uint64_t timeout_ns, Smem S, const uint32_t *c,
+                                               int ev, uint32_t target, int slot, int opc) {
+    const int lane = threadIdx.x & 31;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t v = ld_relaxed(c);
+        if (__all_sync(FULL, v >= target)) return true;
+        if ((it & 15) == 15) {
+            int stop = 0;
+            if (lane == 0) {
+                uint64_t now = gtimer();
+                if (t0 == 0) t0 = now;
+                if (aborted_at(err, S)) stop = 1;
+                else if (now - t0 > timeout_ns) {
+                    raise_error_at(err, S, MK_ERR_TIMEOUT, slot, ev, v, target, opc, 1);
+                    stop = 1;
+                }
+            }
+            if (__shfl_sync(FULL, stop, 0)) return false;
+        }
+    }
+}
+DEV bool warp_wait_counter(const KParams &P, const Smem S, int ev, uint32_t target, int slot, int opc) {
+    const uint32_t *c = P.counters + ev;
+    bool ok = __all_sync(FULL, ld_relaxed(c) >= target);
+    if (!ok) ok = wait_counter_slow(P.err, P.timeout_ns, S, c, ev, target, slot, opc);
+    if (ok) fence_acq_rel_gpu();
+    return ok;
 }
 
 // Barrier of the 8 consumer warps on an mbarrier: each warp reconverges,
@@ -261,10 +345,16 @@ DEV bool cta_aborting(const Smem S) { return __shfl_sync(FULL, (int)S.ctrl()[0],
 // A warp holds one instruction: lane k keeps word k; lanes 0..15 keep the 16
 // operand-table slots of its op row, cached while consecutive instructions
 // share the row.  Fields are read with shuffles (no repeated global loads).
+// The queue is read ahead: while slot i runs, the words of slot i + 2 and the
+// operand row of slot i + 1 are in flight, so no role waits on a round trip to
+// L2 when it moves to its next instruction.
 struct WIns {
-    int w = 0;
-    uint64_t orow = 0;
+    int w = 0;              // words of the current slot
+    uint64_t orow = 0;      // operand row of the current slot
     int row = -1;
+    int w1 = 0, w2 = 0;     // words of the next two slots
+    uint64_t orow1 = 0;     // operand row of the next slot
+    int row1 = -1;
 };
 
 DEV int F(const WIns &I, int k) { return __shfl_sync(FULL, I.w, k); }
@@ -274,15 +364,37 @@ DEV uint64_t PTR(const WIns &I, int k) {
     return ((uint64_t)hi << 32) | lo;
 }
 
-DEV void fetch(WIns &I, const KParams &P, const int32_t *ins) {
+// Lane k's word of queue slot i (all zero, i.e. a NoOp, past the queue's end).
+DEV int queue_word(const KParams &P, const int32_t *q, int i) {
+    return i < P.lmax ? __ldg(q + (size_t)i * W_WORDS + (threadIdx.x & 31)) : 0;
+}
+
+// Starts loading the operand row of the instruction held in `w` unless `row`
+// already is that row.
+DEV void load_orow(const KParams &P, int w, int &row, uint64_t &orow) {
     const int lane = threadIdx.x & 31;
-    I.w = __ldg(ins + lane);
-    const int opc = __shfl_sync(FULL, I.w, W_OPC);
-    const int row = __shfl_sync(FULL, I.w, W_ROW);
-    if (opc != MK_OP_NOOP && row != I.row && row >= 0 && row < P.num_ops) {
-        I.orow = lane < N_SLOTS ? __ldg(P.optab + (size_t)row * N_SLOTS + lane) : 0ull;
-        I.row = row;
+    const int opc = __shfl_sync(FULL, w, W_OPC);
+    const int r = __shfl_sync(FULL, w, W_ROW);
+    if (opc != MK_OP_NOOP && r != row && r >= 0 && r < P.num_ops) {
+        orow = lane < N_SLOTS ? __ldg(P.optab + (size_t)r * N_SLOTS + lane) : 0ull;
+        row = r;
     }
+}
+
+DEV void fetch_init(WIns &I, const KParams &P, const int32_t *q) {
+    I.w1 = queue_word(P, q, 0);
+    load_orow(P, I.w1, I.row1, I.orow1);
+    I.w2 = queue_word(P, q, 1);
+}
+
+// Moves the warp to slot i; slots must be visited in order 0, 1, 2, ...
+DEV void fetch(WIns &I, const KParams &P, const int32_t *q, int i) {
+    I.w = I.w1;
+    I.orow = I.orow1;
+    I.row = I.row1;
+    I.w1 = I.w2;
+    I.w2 = queue_word(P, q, i + 2);
+    load_orow(P, I.w1, I.row1, I.orow1);
 }
 
 // Warp-uniform sanity checks of one instruction against the launch.
@@ -304,6 +416,11 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
         const int rmax = P.B > 4 ? 8 : MAX_TILE_ROWS;
         if (nrows <= 0 || (opc == MK_OP_UP ? 2 * nrows : nrows) > rmax) return false;
         if (kc <= 0 || kc % 8 || 2 * kc > P.page_bytes || kc * P.B * 4 > P.abuf_bytes) return false;
+        const int rpp = F(I, P_RPP);
+        if (rpp != P.page_bytes / (2 * kc) || F(I, P_NPG) != (nrows + rpp - 1) / rpp) return false;
+        // x chunks per consumer thread x batch template must fit the kernel's registers
+        const int maxb = P.B <= 1 ? 1 : P.B <= 2 ? 2 : P.B <= 4 ? 4 : 8;
+        if ((kc / 8 + CONSUMERS - 1) / CONSUMERS * maxb > 8) return false;
     }
     if (opc == MK_OP_ATTN) {
         const int T = F(I, P_T);
@@ -311,6 +428,21 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
     }
     return true;
 }
+
+// Position in the page ring: page index and the parity of its current use.
+struct RingPos {
+    uint32_t p = 0, ph = 0;
+    DEV void next(int num_pages) {
+        if (++p == (uint32_t)num_pages) {
+            p = 0;
+            ph ^= 1;
+        }
+    }
+    DEV void set(uint32_t ring, int num_pages) {
+        p = ring % num_pages;
+        ph = (ring / num_pages) & 1;
+    }
+};
 
 struct Seg {
     const uint8_t *src;

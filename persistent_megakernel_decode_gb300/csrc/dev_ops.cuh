@@ -10,6 +10,8 @@
 // attention task's activation stage instead of the QKV epilogue, because a
 // QKV tile holds 16 rows of a head and RoPE pairs dimension i with i + D/2.
 #pragma once
+#include <type_traits>
+
 #include "dev_common.cuh"
 
 namespace mk {
@@ -172,291 +174,248 @@ DEV void stage_attn(const KParams &P, const WIns &I, float *slot, bool ab) {
 template <int MAXB>
 __host__ __device__ constexpr int rows_max() { return MAXB > 4 ? 8 : MAX_TILE_ROWS; }
 
-// Batch > 1: one GEMV tile split over K -- a thread holds an 8-wide K chunk of
-// x for every sequence in registers (loaded from the activation buffer) and
-// accumulates every row of the tile; one butterfly reduction per tile and the
-// 8 warps' partials combined through shared memory.
+// x of one consumer thread: its 8-wide K chunks of every sequence.  Batch 1
+// keeps them as fp32 pairs for the packed multiply-add (two partial sums per
+// row, even and odd columns); larger batches keep plain floats (one sum per
+// row and sequence) to stay within the register budget.
 template <int MAXB, int NCH>
-DEV void gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
-                   uint32_t &cph, bool &ab) {
-    constexpr int RMAX = rows_max<MAXB>();
-    constexpr int V = RMAX * MAXB;
-    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
-    const int opc = F(I, W_OPC);
-    const int B = P.B;
-    const int kc = F(I, P_KC), nchunk = kc / 8, row_bytes = kc * 2;
-    const int nrows = F(I, P_NROWS);
-    const int nseg = opc == MK_OP_UP ? 2 : 1;
-    const int total = nseg * nrows;
-    const int rpp = P.page_bytes / row_bytes;
-    float xv[NCH][MAXB][8];
+struct XChunks {
+    static constexpr bool PAIRS = MAXB == 1;
+    using Acc = std::conditional_t<PAIRS, uint64_t, float>;
+    uint64_t v[PAIRS ? NCH : 1][4];
+    float f[PAIRS ? 1 : NCH][MAXB][8];
+    DEV void load(const float *xs, int ct, int nchunk, int kc, int B) {
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+            const int c = ct + CONSUMERS * j;
+#pragma unroll
+            for (int b = 0; b < MAXB; ++b) {
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f), bb = a;
+                if (c < nchunk && b < B) {
+                    const float4 *s4 = reinterpret_cast<const float4 *>(xs + (size_t)b * kc + c * 8);
+                    a = s4[0];
+                    bb = s4[1];
+                }
+                if constexpr (PAIRS) {
+                    v[j][0] = pack2(a.x, a.y); v[j][1] = pack2(a.z, a.w);
+                    v[j][2] = pack2(bb.x, bb.y); v[j][3] = pack2(bb.z, bb.w);
+                } else {
+                    f[j][b][0] = a.x; f[j][b][1] = a.y; f[j][b][2] = a.z; f[j][b][3] = a.w;
+                    f[j][b][4] = bb.x; f[j][b][5] = bb.y; f[j][b][6] = bb.z; f[j][b][7] = bb.w;
+                }
+            }
+        }
+    }
+    DEV static float value(Acc a) {
+        if constexpr (PAIRS) return sum2(a);
+        else return a;
+    }
+};
+
+// acc[b] += one weight row chunk . x (sequence b)
+template <int MAXB, int NCH>
+DEV void row_dot(const uint8_t *wrow, int ct, int nchunk, const XChunks<MAXB, NCH> &x,
+                 typename XChunks<MAXB, NCH>::Acc (&acc)[MAXB]) {
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
         const int c = ct + CONSUMERS * j;
-#pragma unroll
-        for (int b = 0; b < MAXB; ++b) {
-            if (c < nchunk && b < B) {
-                const float4 *s4 = reinterpret_cast<const float4 *>(S.abuf() + (size_t)b * kc + c * 8);
-                const float4 a = s4[0], bb = s4[1];
-                xv[j][b][0] = a.x; xv[j][b][1] = a.y; xv[j][b][2] = a.z; xv[j][b][3] = a.w;
-                xv[j][b][4] = bb.x; xv[j][b][5] = bb.y; xv[j][b][6] = bb.z; xv[j][b][7] = bb.w;
+        if (c < nchunk) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(wrow + c * 16);
+            if constexpr (XChunks<MAXB, NCH>::PAIRS) {
+                fma2(acc[0], bf16x2_pair(w.x), x.v[j][0]);
+                fma2(acc[0], bf16x2_pair(w.y), x.v[j][1]);
+                fma2(acc[0], bf16x2_pair(w.z), x.v[j][2]);
+                fma2(acc[0], bf16x2_pair(w.w), x.v[j][3]);
             } else {
+                float w8[8];
+                bf16x8(w, w8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) xv[j][b][e] = 0.f;
+                for (int b = 0; b < MAXB; ++b)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[b] = fmaf(w8[e], x.f[j][b][e], acc[b]);
             }
-        }
-    }
-    // O tiles: this thread's residual value, read before the slot is released
-    float resid_v = 0.f;
-    if (opc == MK_OP_O && ct / RMAX < B) resid_v = slot_resid(P, const_cast<float *>(slot))[(ct / RMAX) * RESID_ROWS + ct % RMAX];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.act_empty()[i & 1]);  // activation buffer and slot no longer needed
-
-    float acc[V];
-#pragma unroll
-    for (int k = 0; k < V; ++k) acc[k] = 0.f;
-    uint32_t p = 0;
-    int pr = 0;
-    const uint8_t *page = nullptr;
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) {
-        if (r < total) {
-            if (r == 0 || pr == rpp || (nseg == 2 && r == nrows)) {
-                if (r > 0) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&S.empty()[p]);
-                    ++ring;
-                }
-                p = ring % P.num_pages;
-                if (!ab) ab = !warp_wait_bar(P, S, &S.full()[p], (ring / P.num_pages) & 1, 2, i, opc);
-                if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + (r == 0 ? 6 : 7)] = gtimer();
-                page = S.pages() + (size_t)p * P.page_bytes;
-                pr = 0;
-            }
-            const uint8_t *wrow = page + (size_t)pr * row_bytes;
-#pragma unroll
-            for (int j = 0; j < NCH; ++j) {
-                const int c = ct + CONSUMERS * j;
-                if (c < nchunk) {
-                    float w8[8];
-                    bf16x8(*reinterpret_cast<const uint4 *>(wrow + c * 16), w8);
-#pragma unroll
-                    for (int b = 0; b < MAXB; ++b)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[r * MAXB + b] = fmaf(w8[e], xv[j][b][e], acc[r * MAXB + b]);
-                }
-            }
-            ++pr;
-        }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty()[p]);
-    ++ring;
-
-    // warp reduction, then the 8 warps' partials through shared memory
-    Bfly<V, 16>::run(acc, lane);
-    float *red = S.red(i & 1);  // [warp][V]
-    if constexpr (V >= 32) {
-#pragma unroll
-        for (int j = 0; j < V / 32; ++j) red[warp * V + lane * (V / 32) + j] = acc[j];
-    } else {
-        if ((lane & (32 / V - 1)) == 0) red[warp * V + lane / (32 / V)] = acc[0];
-    }
-    consumer_sync(P, S, cph, ab, i);
-
-    // epilogue: thread ct -> (b = ct / RMAX, r = ct % RMAX)
-    const int eb = ct / RMAX, er = ct % RMAX;
-    const bool mine = eb < B && er < nrows && !ab;
-    auto total_of = [&](int r, int b) {
-        float y = 0.f;
-#pragma unroll
-        for (int w = 0; w < CONSUMER_WARPS; ++w) y += red[w * V + r * MAXB + b];
-        return y;
-    };
-    // operand pointers are decoded by the whole warp before any lane-divergent code
-    const int out0 = F(I, P_OUT0);
-    const uint64_t ptr_a = PTR(I, opc == MK_OP_QKV ? S_QKV_OUT : opc == MK_OP_O ? S_O_HRES
-                                : opc == MK_OP_UP ? S_UP_OUT : opc == MK_OP_DOWN ? S_DN_HRES : S_LM_LOGITS);
-    const uint64_t ptr_b = PTR(I, opc == MK_OP_O ? S_O_HMID : S_LM_KEYS);
-    if (opc == MK_OP_QKV) {
-        if (mine) {
-            float *out = reinterpret_cast<float *>(ptr_a);
-            const int G = P.Hq / P.Hkv;
-            out[(size_t)eb * P.Hkv * (G + 2) * P.D + out0 + er] = total_of(er, eb);
-        }
-    } else if (opc == MK_OP_O) {
-        if (mine) {
-            float *hres = reinterpret_cast<float *>(ptr_a);
-            float *hmid = reinterpret_cast<float *>(ptr_b);
-            const size_t k = (size_t)eb * P.H + out0 + er;
-            const float v = resid_v + total_of(er, eb);
-            hres[k] = v;
-            hmid[k] = v;
-        }
-    } else if (opc == MK_OP_UP) {
-        if (mine) {
-            float *act = reinterpret_cast<float *>(ptr_a);
-            const float g = total_of(er, eb), u = total_of(nrows + er, eb);
-            act[(size_t)eb * P.F + out0 + er] = g / (1.0f + __expf(-g)) * u;
-        }
-    } else if (opc == MK_OP_DOWN) {
-        if (mine) {
-            float *hres = reinterpret_cast<float *>(ptr_a);
-            atomicAdd(hres + (size_t)eb * P.H + out0 + er, total_of(er, eb));
-        }
-    } else if (opc == MK_OP_LM) {
-        const float y = (eb < B && er < nrows) ? total_of(er, eb) : -INFINITY;
-        if (mine) reinterpret_cast<float *>(ptr_a)[(size_t)eb * P.V + out0 + er] = y;
-        // argmax over the RMAX lanes of one sequence (lowest index on ties)
-        float bv = y;
-        int bi = er;
-#pragma unroll
-        for (int o = RMAX / 2; o; o >>= 1) {
-            const float ov = __shfl_xor_sync(FULL, bv, o);
-            const int oi = __shfl_xor_sync(FULL, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if (er == 0 && eb < B && !ab) {
-            unsigned long long *keys = reinterpret_cast<unsigned long long *>(ptr_b);
-            red_max_u64(keys + (size_t)P.step * B + eb, (unsigned long long)argmax_key(bv, out0 + bi));
         }
     }
 }
 
-// Batch 1: whole rows per warp.  Warp w owns rows w*NRW .. w*NRW+NRW-1 of
-// every segment of the tile; lane l covers the 8-element groups l, l+32, ...
-// of a row (KG groups), with the matching x kept in registers for the tile,
-// so a row is finished with one warp reduction -- no cross-warp reduction and
-// no barrier between warps.  KG = 0 selects a variant that reads x from
-// shared memory (rows longer than 32 * 8 * 8 elements).  The LM head keeps a
-// per-warp running best (logit, index) and updates the global argmax only
-// when it improves.
-template <int NRW, int KG>
-DEV void gemv_rows(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
-                   unsigned long long &lm_best, bool &ab) {
+// One GEMV tile (QKV, O, MLP-up, MLP-down, LM head) split over K: consumer
+// thread t holds the 8-wide K chunks t, t + 256, ... of x for every sequence
+// in registers (x is read once per tile, 4 bytes per weight column), so each
+// warp reads a contiguous 512-byte slice of every weight row.  Each warp's
+// partial sums are reduced across its lanes with a transposed butterfly and
+// parked in one of NRED shared buffers; the warp that arrives last sums the
+// 8 warps' partials in warp order and runs the epilogue -- no warp waits for
+// another.  EXACT: every page holds RPP rows of the tile (the page loop is
+// unrolled and one butterfly covers the tile); otherwise pages hold up to RPP
+// rows and each page is reduced on its own.
+template <int MAXB, int NCH, int RPP, bool EXACT>
+DEV void gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+                   RingPos &rq, uint32_t &ured, unsigned long long &lm_best, bool &ab) {
+    constexpr int RMAX = rows_max<MAXB>();
+    constexpr int VT = RMAX * MAXB;            // partials per warp in a reduction buffer: row * MAXB + b
+    constexpr int VL = VT >= 32 ? VT / 32 : 1; // epilogue values per lane: v = lane + 32 j
     const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
     const int opc = F(I, W_OPC);
-    const int kc = F(I, P_KC), ngrp = kc / 8, row_bytes = kc * 2;
-    const int nrows = F(I, P_NROWS), out0 = F(I, P_OUT0);
-    const int nseg = opc == MK_OP_UP ? 2 : 1;
-    const int rpp = P.page_bytes / row_bytes;
-    const int npg = (nrows + rpp - 1) / rpp;
-    const int r0 = warp * NRW;
+    const int kc = F(I, P_KC), nrows = F(I, P_NROWS), npg0 = F(I, P_NPG);
+    const int rpp = EXACT ? RPP : min(F(I, P_RPP), RPP);
+    const int npg = (opc == MK_OP_UP ? 2 : 1) * npg0;
+    const int nchunk = kc >> 3, row_bytes = kc * 2;
+    const int B = P.B;
+    using X = XChunks<MAXB, NCH>;
+    X x;
+    x.load(S.abuf(i & 1), ct, nchunk, kc, B);
+    // O tiles: the residual values this lane would need in the epilogue, read
+    // before the slot is released (any warp may turn out to run the epilogue)
+    float resid_v[VL];
+#pragma unroll
+    for (int j = 0; j < VL; ++j) resid_v[j] = 0.f;
+    if (opc == MK_OP_O) {
+        const float *rs = slot_resid(P, const_cast<float *>(slot));
+#pragma unroll
+        for (int j = 0; j < VL; ++j) {
+            const int v = lane + 32 * j, r = v / MAXB, b = v % MAXB;
+            if (v < VT && b < B && r < nrows) resid_v[j] = rs[b * RESID_ROWS + r];
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.act_empty()[i & 1]);  // activation buffer and slot no longer needed
+
+    // the reduction buffer this tile uses; its previous tile's epilogue must have read it
+    const int rb = (int)(ured % NRED);
+    const uint32_t use = ured / NRED;
+    ++ured;
+    if (!ab) ab = !warp_wait_smem(P, S, &S.ctrl()[C_RED_FIN + rb], use, i, opc);
+    float *red = S.red(rb) + warp * VT;
+    ring += npg;
+
+    if constexpr (EXACT) {
+        constexpr int NPGMAX = RMAX / RPP;
+        typename X::Acc acc[RMAX][MAXB];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+            for (int b = 0; b < MAXB; ++b) acc[r][b] = 0;
+#pragma unroll
+        for (int pg = 0; pg < NPGMAX; ++pg) {
+            if (pg < npg) {
+                if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
+                const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
+#pragma unroll
+                for (int r = 0; r < RPP; ++r) row_dot<MAXB, NCH>(page + (size_t)r * row_bytes, ct, nchunk, x, acc[pg * RPP + r]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
+                rq.next(P.num_pages);
+            }
+        }
+        float v[VT];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+            for (int b = 0; b < MAXB; ++b) v[r * MAXB + b] = X::value(acc[r][b]);
+        Bfly<VT, 16>::run(v, lane);
+        if constexpr (VT >= 32) {
+#pragma unroll
+            for (int j = 0; j < VT / 32; ++j) red[lane * (VT / 32) + j] = v[j];
+        } else {
+            if ((lane & (32 / VT - 1)) == 0) red[lane / (32 / VT)] = v[0];
+        }
+    } else {
+        constexpr int VP = RPP * MAXB;
+        for (int pg = 0; pg < npg; ++pg) {
+            const int seg = pg >= npg0;
+            const int r0 = (pg - seg * npg0) * rpp;  // first row of the page within its segment
+            const int cnt = min(rpp, nrows - r0);
+            if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
+            const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
+            typename X::Acc acc[RPP][MAXB];
+#pragma unroll
+            for (int r = 0; r < RPP; ++r) {
+#pragma unroll
+                for (int b = 0; b < MAXB; ++b) acc[r][b] = 0;
+                if (r < cnt) row_dot<MAXB, NCH>(page + (size_t)r * row_bytes, ct, nchunk, x, acc[r]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
+            rq.next(P.num_pages);
+            float v[VP];
+#pragma unroll
+            for (int r = 0; r < RPP; ++r)
+#pragma unroll
+                for (int b = 0; b < MAXB; ++b) v[r * MAXB + b] = X::value(acc[r][b]);
+            Bfly<VP, 16>::run(v, lane);
+            const int base = (seg * nrows + r0) * MAXB;
+            if constexpr (VP >= 32) {
+#pragma unroll
+                for (int j = 0; j < VP / 32; ++j) {
+                    const int k = lane * (VP / 32) + j;
+                    if (k / MAXB < cnt) red[base + k] = v[j];
+                }
+            } else {
+                const int k = lane / (32 / VP);
+                if ((lane & (32 / VP - 1)) == 0 && k / MAXB < cnt) red[base + k] = v[0];
+            }
+        }
+    }
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atom_add_acqrel_cta(&S.ctrl()[C_RED_ARR + rb], 1) == (int)(CONSUMER_WARPS * use + CONSUMER_WARPS - 1);
+    if (!__shfl_sync(FULL, last, 0)) return;
+    __syncwarp();
+
+    // epilogue (the last warp): lane handles v = lane + 32 j, i.e. row v / MAXB of sequence v % MAXB
+    const float *rall = S.red(rb);
+    const int out0 = F(I, P_OUT0);
     const uint64_t ptr_a = PTR(I, opc == MK_OP_QKV ? S_QKV_OUT : opc == MK_OP_O ? S_O_HRES
                                 : opc == MK_OP_UP ? S_UP_OUT : opc == MK_OP_DOWN ? S_DN_HRES : S_LM_LOGITS);
     const uint64_t ptr_b = PTR(I, opc == MK_OP_O ? S_O_HMID : S_LM_KEYS);
-    const float *xs = S.abuf();
-    float x[KG > 0 ? KG : 1][8];
-    if constexpr (KG > 0) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
 #pragma unroll
-        for (int k = 0; k < KG; ++k) {
-            const int g = lane + 32 * k;
-            if (g < ngrp) {
-                const float4 a = *reinterpret_cast<const float4 *>(xs + g * 8);
-                const float4 b = *reinterpret_cast<const float4 *>(xs + g * 8 + 4);
-                x[k][0] = a.x; x[k][1] = a.y; x[k][2] = a.z; x[k][3] = a.w;
-                x[k][4] = b.x; x[k][5] = b.y; x[k][6] = b.z; x[k][7] = b.w;
-            } else {
+    for (int j = 0; j < VL; ++j) {
+        const int v = lane + 32 * j, r = v / MAXB, b = v % MAXB;
+        if (v >= VT || b >= B || r >= nrows || ab) continue;
+        float y = 0.f, u = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[k][e] = 0.f;
+        for (int w = 0; w < CONSUMER_WARPS; ++w) y += rall[w * VT + v];
+        if (opc == MK_OP_UP) {
+#pragma unroll
+            for (int w = 0; w < CONSUMER_WARPS; ++w) u += rall[w * VT + nrows * MAXB + v];
+        }
+        if (opc == MK_OP_QKV) {
+            const int G = P.Hq / P.Hkv;
+            reinterpret_cast<float *>(ptr_a)[(size_t)b * P.Hkv * (G + 2) * P.D + out0 + r] = y;
+        } else if (opc == MK_OP_O) {
+            const size_t k = (size_t)b * P.H + out0 + r;
+            reinterpret_cast<float *>(ptr_a)[k] = resid_v[j] + y;
+            reinterpret_cast<float *>(ptr_b)[k] = resid_v[j] + y;
+        } else if (opc == MK_OP_UP) {
+            reinterpret_cast<float *>(ptr_a)[(size_t)b * P.F + out0 + r] = y / (1.0f + __expf(-y)) * u;
+        } else if (opc == MK_OP_DOWN) {
+            atomicAdd(reinterpret_cast<float *>(ptr_a) + (size_t)b * P.H + out0 + r, y);
+        } else if (opc == MK_OP_LM) {
+            reinterpret_cast<float *>(ptr_a)[(size_t)b * P.V + out0 + r] = y;
+            if (y > bv || (y == bv && r < bi)) { bv = y; bi = r; }
+        }
+    }
+    if (opc == MK_OP_LM) {
+        // argmax over the tile's rows of each sequence (lowest index on ties);
+        // lanes with equal lane % MAXB hold the same sequence
+#pragma unroll
+        for (int o = 16; o >= MAXB; o >>= 1) {
+            const float ov = __shfl_xor_sync(FULL, bv, o);
+            const int oi = __shfl_xor_sync(FULL, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (lane < B && !ab && bi != 0x7fffffff) {
+            const unsigned long long key = argmax_key(bv, out0 + bi);
+            if (key > lm_best) {  // lane b keeps sequence b's best key of this step
+                lm_best = key;
+                red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)P.step * B + lane, key);
             }
         }
     }
-    float acc[2][NRW];
-#pragma unroll
-    for (int s = 0; s < 2; ++s)
-#pragma unroll
-        for (int j = 0; j < NRW; ++j) acc[s][j] = 0.f;
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-        if (s < nseg) {
-            for (int pg = 0; pg < npg; ++pg) {
-                const uint32_t p = ring % P.num_pages;
-                if (P.trace && ct == 0 && !mbar_test(&S.full()[p], (ring / P.num_pages) & 1))
-                    P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 8] += 1;   // page not ready on arrival
-                if (!ab) ab = !warp_wait_bar(P, S, &S.full()[p], (ring / P.num_pages) & 1, 2, i, opc);
-                if (P.trace && ct == 0)
-                    P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + ((s == 0 && pg == 0) ? 6 : 7)] = gtimer();
-                const int prow0 = pg * rpp, pnr = min(rpp, nrows - prow0);
-                const uint8_t *page = S.pages() + (size_t)p * P.page_bytes;
-#pragma unroll
-                for (int j = 0; j < NRW; ++j) {
-                    const int r = r0 + j;
-                    if (r >= prow0 && r < prow0 + pnr) {  // warp-uniform
-                        const uint8_t *wr = page + (size_t)(r - prow0) * row_bytes;
-                        float a0 = 0.f, a1 = 0.f;
-                        if constexpr (KG > 0) {
-#pragma unroll
-                            for (int k = 0; k < KG; ++k) {
-                                const int g = lane + 32 * k;
-                                if (g < ngrp) {
-                                    float w8[8];
-                                    bf16x8(*reinterpret_cast<const uint4 *>(wr + g * 16), w8);
-                                    a0 = fmaf(w8[0], x[k][0], a0); a1 = fmaf(w8[1], x[k][1], a1);
-                                    a0 = fmaf(w8[2], x[k][2], a0); a1 = fmaf(w8[3], x[k][3], a1);
-                                    a0 = fmaf(w8[4], x[k][4], a0); a1 = fmaf(w8[5], x[k][5], a1);
-                                    a0 = fmaf(w8[6], x[k][6], a0); a1 = fmaf(w8[7], x[k][7], a1);
-                                }
-                            }
-                        } else {
-#pragma unroll 4
-                            for (int g = lane; g < ngrp; g += 32) {
-                                float w8[8];
-                                bf16x8(*reinterpret_cast<const uint4 *>(wr + g * 16), w8);
-                                const float4 xa = *reinterpret_cast<const float4 *>(xs + g * 8);
-                                const float4 xb = *reinterpret_cast<const float4 *>(xs + g * 8 + 4);
-                                a0 = fmaf(w8[0], xa.x, a0); a1 = fmaf(w8[1], xa.y, a1);
-                                a0 = fmaf(w8[2], xa.z, a0); a1 = fmaf(w8[3], xa.w, a1);
-                                a0 = fmaf(w8[4], xb.x, a0); a1 = fmaf(w8[5], xb.y, a1);
-                                a0 = fmaf(w8[6], xb.z, a0); a1 = fmaf(w8[7], xb.w, a1);
-                            }
-                        }
-                        acc[s][j] += a0 + a1;
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.empty()[p]);
-                ++ring;
-            }
-        }
-    }
-    if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 9] = gtimer();
-    float y[2][NRW];
-#pragma unroll
-    for (int s = 0; s < 2; ++s)
-#pragma unroll
-        for (int j = 0; j < NRW; ++j) y[s][j] = s < nseg ? warp_sum(acc[s][j]) : 0.f;
-    if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 10] = gtimer();
-    const float *resid = slot_resid(P, const_cast<float *>(slot));
-    if (lane == 0 && !ab) {
-#pragma unroll
-        for (int j = 0; j < NRW; ++j) {
-            const int r = r0 + j;
-            if (r >= nrows) continue;
-            if (opc == MK_OP_QKV) {
-                reinterpret_cast<float *>(ptr_a)[out0 + r] = y[0][j];
-            } else if (opc == MK_OP_O) {
-                const float v = resid[r] + y[0][j];
-                reinterpret_cast<float *>(ptr_a)[out0 + r] = v;
-                reinterpret_cast<float *>(ptr_b)[out0 + r] = v;
-            } else if (opc == MK_OP_UP) {
-                const float g = y[0][j], u = y[1][j];
-                reinterpret_cast<float *>(ptr_a)[out0 + r] = g / (1.0f + __expf(-g)) * u;
-            } else if (opc == MK_OP_DOWN) {
-                atomicAdd(reinterpret_cast<float *>(ptr_a) + out0 + r, y[0][j]);
-            } else if (opc == MK_OP_LM) {
-                reinterpret_cast<float *>(ptr_a)[out0 + r] = y[0][j];
-                const unsigned long long key = argmax_key(y[0][j], out0 + r);
-                if (key > lm_best) {
-                    lm_best = key;
-                    red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)P.step, key);
-                }
-            }
-        }
-    }
-    if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 11] = gtimer();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.act_empty()[i & 1]);  // activation buffer and slot no longer needed
+    if (lane == 0) st_release_cta(&S.ctrl()[C_RED_FIN + rb], (int)use + 1);
 }
 
 // Split-KV attention of one (sequence, kv group, split): scores from the

@@ -32,14 +32,14 @@ namespace mk {
 DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int lane = threadIdx.x & 31;
     const uint64_t pol = evict_first_policy();
-    uint32_t ring = 0;
+    uint32_t ring = 0, rp = 0, rph = 0;  // pages issued; ring position and its use parity
     const int NP = P.num_pages, PS = P.page_bytes;
     WIns I;
+    fetch_init(I, P, myq);
     for (int i = 0; i < P.lmax; ++i) {
         if (cta_aborting(S)) break;
-        const int32_t *ins = myq + (size_t)i * W_WORDS;
-        if (lane < 4 && i + 4 + lane < P.lmax) prefetch_l2(ins + (size_t)(4 + lane) * W_WORDS);
-        fetch(I, P, ins);
+        if (lane < 4 && i + 4 + lane < P.lmax) prefetch_l2(myq + (size_t)(i + 4 + lane) * W_WORDS);
+        fetch(I, P, myq, i);
         const int opc = F(I, W_OPC);
         if (!ins_valid(P, I)) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
@@ -59,8 +59,8 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
             }
             for (int r = 0; r < sg.rows; r += rpp) {
                 const int nr = min(rpp, sg.rows - r);
-                const uint32_t p = ring % NP, use = ring / NP;
-                if (!warp_wait_bar(P, S, &S.empty()[p], (use & 1) ^ 1, 0, i, opc)) {
+                const uint32_t p = rp;
+                if (!warp_wait_bar(P, S, &S.empty()[p], rph ^ 1, 0, i, opc)) {
                     stop = true;
                     return;
                 }
@@ -79,6 +79,10 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
                 }
                 __syncwarp();
                 ++ring;
+                if (++rp == (uint32_t)NP) {
+                    rp = 0;
+                    rph ^= 1;
+                }
             }
         };
         if (nseg > 0) issue(s0);
@@ -104,14 +108,15 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
 template <int MAXB>
 DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int lane = threadIdx.x & 31;
-    long long prev_key = -1;
+    const bool two_bufs = P.abuf_count > 1;
+    long long key0 = -1, key1 = -1;   // what each activation buffer holds: op row << 32 | first column
     bool ab = false;
     int seen_ev = -1;           // last event seen satisfied, and the target it met
     uint32_t seen_target = 0;
     WIns I;
+    fetch_init(I, P, myq);
     for (int i = 0; i < P.lmax; ++i) {
-        const int32_t *ins = myq + (size_t)i * W_WORDS;
-        fetch(I, P, ins);
+        fetch(I, P, myq, i);
         const int opc = F(I, W_OPC);
         if (opc == MK_OP_NOOP) continue;
         const int sl = i & 1;
@@ -142,20 +147,24 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
             if (P.D == 64) stage_attn<64>(P, I, slot, ab);
             else stage_attn<128>(P, I, slot, ab);
             flags = SLOT_FRESH;
-            prev_key = -1;
+            key0 = key1 = -1;
         } else if (opc >= MK_OP_QKV) {
+            // two buffers: buffer sl was last read by instruction i - 2, whose
+            // slot release was awaited above; one buffer: instruction i - 1
+            // may still read it
+            const int bi = two_bufs ? sl : 0;
             const long long key = ((long long)F(I, W_ROW) << 32) | (uint32_t)F(I, P_K0);
-            if (key != prev_key || F(I, P_SNAP) > 0) {
-                // the previous instruction's consumers may still read the activation buffer
-                if (i > 0 && !ab)
+            if (key != (bi ? key1 : key0) || F(I, P_SNAP) > 0) {
+                if (!two_bufs && i > 0 && !ab)
                     ab = !warp_wait_bar(P, S, &S.act_empty()[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1, 1, i, opc);
-                stage_gemv<MAXB>(P, I, S.abuf(), ab);
+                stage_gemv<MAXB>(P, I, S.abuf(bi), ab);
                 flags = SLOT_FRESH;
             }
             if (opc == MK_OP_O) stage_resid(P, I, slot);
-            prev_key = key;
+            if (bi) key1 = key;
+            else key0 = key;
         } else {
-            prev_key = -1;
+            key0 = key1 = -1;
         }
         __syncwarp();
         if (lane == 0) {
@@ -167,41 +176,63 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
 
 // ---------------------------------------------------------------- consumer warps
 // Publisher warp.  Every consumer warp posts, with a CTA-scope release store,
-// how many queue slots it has finished.  The publisher takes the minimum over
-// the 8 warps: every instruction below it is fully written back.  One
-// GPU-scope fence then covers the whole batch (it is cumulative over what the
-// CTA-scope acquires observed) and the batch's signals are added to the event
-// counters -- so consumers never wait for a fence.
+// how many queue slots it has finished, and rings a doorbell mbarrier.  The
+// publisher sleeps on the doorbell (a bounded try_wait, so a missed ring costs
+// at most the hint), takes the minimum over the 8 warps: every instruction
+// below it is fully written back.  One GPU-scope fence then covers the whole
+// batch (it is cumulative over what the polls observed) and the batch's
+// signals are added to the event counters -- so consumers never wait for a
+// fence, and the waiting publisher issues no instructions.
+DEV int progress_min(const Smem S) {
+    int4 a, b;
+    const uint32_t p = saddr((const void *)(S.ctrl() + 8));
+    asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w) : "r"(p) : "memory");
+    asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w) : "r"(p + 16) : "memory");
+    return min(min(min(a.x, a.y), min(a.z, a.w)), min(min(b.x, b.y), min(b.z, b.w)));
+}
+
 DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
-    if ((threadIdx.x & 31) != 0) return;
-    int next = 0;  // first slot not yet published
-    uint64_t t0 = 0;
-    uint32_t it = 0;
+    const int lane = threadIdx.x & 31;
+    int next = 0;                                              // first slot not yet published
+    int wc = queue_word(P, myq, 0), wn = queue_word(P, myq, 1);  // words of slots next, next + 1
+    uint32_t bell_ph = 0;
     while (next < P.lmax) {
-        if (__ldg(myq + (size_t)next * W_WORDS + W_OPC) == MK_OP_NOOP) break;  // NoOps only pad the tail
-        int done = P.lmax;
-#pragma unroll
-        for (int w = 0; w < CONSUMER_WARPS; ++w) done = min(done, ld_acquire_cta(&S.ctrl()[8 + w]));
-        if (done > next) {
-            const bool ab = S.ctrl()[0] != 0;
-            if (!ab) fence_acq_rel_gpu();
-            for (; next < done; ++next) {
-                const int32_t *ins = myq + (size_t)next * W_WORDS;
-                const int cnt = __ldg(ins + W_CNT), ns = (cnt >> 8) & 0xff;
-                if (ab) continue;
-                for (int k = 0; k < ns; ++k)
-                    red_relaxed_add(P.counters + __ldg(ins + W_SIG + 2 * k), (uint32_t)__ldg(ins + W_SIG + 2 * k + 1));
+        if (__shfl_sync(FULL, wc, W_OPC) == MK_OP_NOOP) break;  // NoOps only pad the tail
+        int done = next, ab = 0, stop = 0;
+        if (lane == 0) {
+            uint64_t t0 = 0;
+            for (uint32_t it = 0;; ++it) {
+                done = progress_min(S);
+                ab = S.ctrl()[0] != 0;
+                if (done > next || ab) break;
+                if (mbar_wait_hint(S.bell(), bell_ph, 500)) bell_ph ^= 1;
+                if ((it & 15) == 15) {
+                    const uint64_t now = gtimer();
+                    if (t0 == 0) t0 = now;
+                    if (aborted(P, S)) { stop = 1; break; }
+                    if (now - t0 > P.timeout_ns) {
+                        raise_error(P, S, MK_ERR_TIMEOUT, next, -1, (uint32_t)done, (uint32_t)next + 1, -1, 4);
+                        stop = 1;
+                        break;
+                    }
+                }
             }
-            t0 = 0;
-            it = 0;
-        } else if ((++it & 63) == 0) {
-            const uint64_t now = gtimer();
-            if (t0 == 0) t0 = now;
-            if (aborted(P, S)) break;
-            if (now - t0 > P.timeout_ns) {
-                raise_error(P, S, MK_ERR_TIMEOUT, next, -1, (uint32_t)done, (uint32_t)next + 1, -1, 4);
-                break;
+            // the fence makes the polls acquires and the counter adds below releases
+            if (!stop && !ab) fence_acq_rel_gpu();
+        }
+        done = __shfl_sync(FULL, done, 0);
+        ab = __shfl_sync(FULL, ab, 0);
+        if (__shfl_sync(FULL, stop, 0)) break;
+        for (; next < done; ++next) {
+            const int cnt = __shfl_sync(FULL, wc, W_CNT), ns = (cnt >> 8) & 0xff;
+            const int e0 = __shfl_sync(FULL, wc, W_SIG), i0 = __shfl_sync(FULL, wc, W_SIG + 1);
+            const int e1 = __shfl_sync(FULL, wc, W_SIG + 2), i1 = __shfl_sync(FULL, wc, W_SIG + 3);
+            if (lane == 0 && !ab) {
+                if (ns > 0) red_relaxed_add(P.counters + e0, (uint32_t)i0);
+                if (ns > 1) red_relaxed_add(P.counters + e1, (uint32_t)i1);
             }
+            wc = wn;
+            wn = queue_word(P, myq, next + 2);
         }
     }
 }
@@ -210,19 +241,51 @@ DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
 DEV void handoff(const Smem S, int i) {
     __syncwarp();
     const int warp = (threadIdx.x >> 5) - 2;
-    if ((threadIdx.x & 31) == 0) st_release_cta(&S.ctrl()[8 + warp], i + 1);
+    if ((threadIdx.x & 31) == 0) {
+        st_release_cta(&S.ctrl()[8 + warp], i + 1);
+        mbar_arrive(S.bell());
+    }
+}
+
+// GEMV variants: K chunks per consumer thread (NCH) x page geometry.  Pages
+// of exactly 1, 2 or 4 rows that tile the tile's rows take the unrolled path.
+template <int MAXB, int NCH>
+DEV void gemv_geom(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+                   RingPos &rq, uint32_t &ured, unsigned long long &lm_best, bool &ab) {
+    constexpr int RMAX = rows_max<MAXB>();
+    const int rpp = F(I, P_RPP), nrows = F(I, P_NROWS);
+    const bool tiled = rpp <= 4 && (nrows & (rpp - 1)) == 0 && (rpp & (rpp - 1)) == 0;
+    if (tiled && rpp == 4) gemv_tile<MAXB, NCH, 4, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+    else if (tiled && rpp == 2) gemv_tile<MAXB, NCH, 2, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+    else if (tiled && rpp == 1) gemv_tile<MAXB, NCH, 1, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+    else gemv_tile<MAXB, NCH, RMAX, false>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+}
+template <int MAXB>
+DEV void gemv_dispatch(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+                       RingPos &rq, uint32_t &ured, unsigned long long &lm_best, bool &ab) {
+    const int nch = ((F(I, P_KC) >> 3) + CONSUMERS - 1) / CONSUMERS;
+    constexpr int NCHMAX = MAXB >= 8 ? 1 : (MAXB >= 4 ? 2 : (MAXB >= 2 ? 4 : 8));
+    if (nch <= 1) gemv_geom<MAXB, 1>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+    else if constexpr (NCHMAX >= 2) {
+        if (nch <= 2) gemv_geom<MAXB, 2>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+        else if constexpr (NCHMAX >= 4) {
+            if (nch <= 4) gemv_geom<MAXB, 4>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+            else if constexpr (NCHMAX >= 8) gemv_geom<MAXB, 8>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+        }
+    }
 }
 
 template <int MAXB>
 DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int ct = threadIdx.x - 64, lane = ct & 31;
-    uint32_t ring = 0, cph = 0;
+    uint32_t ring = 0, cph = 0, ured = 0;
+    RingPos rq;  // ring position of the next page (kept in step with ring)
     bool ab = false;
     unsigned long long lm_best = 0;
     WIns I;
+    fetch_init(I, P, myq);
     for (int i = 0; i < P.lmax; ++i) {
-        const int32_t *ins = myq + (size_t)i * W_WORDS;
-        fetch(I, P, ins);
+        fetch(I, P, myq, i);
         const int opc = F(I, W_OPC);
         if (opc == MK_OP_NOOP) continue;
         uint64_t t_start = 0;
@@ -236,26 +299,12 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         if (opc == MK_OP_ATTN) {
             if (P.D == 64) attn_task<64>(P, S, I, i, slot, ring, cph, ab);
             else attn_task<128>(P, S, I, i, slot, ring, cph, ab);
+            rq.set(ring, P.num_pages);
         } else if (opc == MK_OP_EMBED) {
             consumer_sync(P, S, cph, ab, i);
             embed_task(P, S, I, i, ab);
         } else if (opc >= MK_OP_QKV) {
-            if constexpr (MAXB == 1) {
-                const int two = F(I, P_NROWS) > CONSUMER_WARPS;
-                const int kg = (F(I, P_KC) / 8 + 31) / 32;  // 8-element groups per lane
-                if (kg <= 1) two ? gemv_rows<2, 1>(P, S, I, i, slot, ring, lm_best, ab) : gemv_rows<1, 1>(P, S, I, i, slot, ring, lm_best, ab);
-                else if (kg <= 3) two ? gemv_rows<2, 3>(P, S, I, i, slot, ring, lm_best, ab) : gemv_rows<1, 3>(P, S, I, i, slot, ring, lm_best, ab);
-                else if (kg <= 8) two ? gemv_rows<2, 8>(P, S, I, i, slot, ring, lm_best, ab) : gemv_rows<1, 8>(P, S, I, i, slot, ring, lm_best, ab);
-                else two ? gemv_rows<2, 0>(P, S, I, i, slot, ring, lm_best, ab) : gemv_rows<1, 0>(P, S, I, i, slot, ring, lm_best, ab);
-            } else {
-                const int nch = (F(I, P_KC) / 8 + CONSUMERS - 1) / CONSUMERS;
-                constexpr int NCHMAX = MAXB >= 8 ? 1 : (MAXB >= 4 ? 2 : 4);
-                if (nch <= 1) gemv_tile<MAXB, 1>(P, S, I, i, slot, ring, cph, ab);
-                else if constexpr (NCHMAX >= 2) {
-                    if (nch <= 2) gemv_tile<MAXB, 2>(P, S, I, i, slot, ring, cph, ab);
-                    else if constexpr (NCHMAX >= 4) gemv_tile<MAXB, 4>(P, S, I, i, slot, ring, cph, ab);
-                }
-            }
+            gemv_dispatch<MAXB>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
         } else {  // COUNTER: the slot handshake only
             consumer_sync(P, S, cph, ab, i);
             __syncwarp();
@@ -277,11 +326,12 @@ template <int MAXB>
 __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
     Smem S;
     S.o_abuf = 0;
-    S.o_act0 = P.abuf_bytes;
+    S.abuf_stride = P.abuf_count > 1 ? P.abuf_bytes : 0;
+    S.o_act0 = P.abuf_count * P.abuf_bytes;
     S.act_stride = P.act_bytes;
-    S.o_pages = P.abuf_bytes + 2 * P.act_bytes;
+    S.o_pages = S.o_act0 + 2 * P.act_bytes;
     S.o_aux = S.o_pages + P.num_pages * P.page_bytes;
-    S.o_red0 = S.o_aux + P.aux_bytes - 2 * P.red_bytes;
+    S.o_red0 = S.o_aux + P.aux_bytes - NRED * P.red_bytes;
     S.red_stride = P.red_bytes;
     S.o_bars = S.o_aux + P.aux_bytes;
     S.o_ctrl = S.o_bars + MBAR_BYTES;
@@ -296,7 +346,8 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
             mbar_init(&S.act_empty()[s], CONSUMER_WARPS);
         }
         mbar_init(S.cbar(), CONSUMER_WARPS);
-        for (int k = 0; k < 16; ++k) S.ctrl()[k] = 0;
+        mbar_init(S.bell(), 1);
+        for (int k = 0; k < CTRL_WORDS; ++k) S.ctrl()[k] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -421,6 +472,7 @@ static KParams base_params(const Plan &p, uint8_t *ws) {
     k.page_bytes = p.page_bytes;
     k.act_bytes = p.act_bytes;
     k.abuf_bytes = p.abuf_bytes;
+    k.abuf_count = p.abuf_count;
     k.aux_bytes = p.aux_bytes;
     k.red_bytes = p.red_bytes;
     k.smem_bytes = p.smem_bytes;

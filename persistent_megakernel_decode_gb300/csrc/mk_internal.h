@@ -35,6 +35,8 @@ enum : int {
     P_MAT = W_P + 5,    // QKV: 0 = Wq, 1 = Wk, 2 = Wv
     P_SNAP = W_P + 6,   // 1 + layer whose residual the activation loader snapshots, or 0
     P_KTOT = W_P + 7,   // row length (elements) of the source matrix
+    P_RPP = W_P + 8,    // weight rows per page: page bytes / (2 * K chunk)
+    P_NPG = W_P + 9,    // pages per segment: ceil(rows / P_RPP)
 };
 // ATTN payload
 enum : int {
@@ -78,7 +80,7 @@ struct KParams {
     uint64_t timeout_ns;
     int lmax, num_workers, num_ops, num_events;
     int step, flags;
-    int num_pages, page_bytes, act_bytes, abuf_bytes, aux_bytes, red_bytes, smem_bytes;
+    int num_pages, page_bytes, act_bytes, abuf_bytes, abuf_count, aux_bytes, red_bytes, smem_bytes;
     int B, H, Hq, Hkv, D, F, V, L, Smax, qk_norm, nsplit_max;
     float eps, theta;
 };
@@ -89,6 +91,7 @@ constexpr int THREADS = CONSUMERS + 96;   // + loader, activation-loader and pub
 constexpr int PUBLISHER_WARP = CONSUMER_WARPS + 2;
 constexpr int RESID_ROWS = 16;           // residual slice staged per slot for O tiles
 constexpr int MAX_TILE_ROWS = 16;
+constexpr int NRED = 4;                  // cross-warp reduction buffers, used round robin by GEMV tiles
 
 }  // namespace mk
 
@@ -99,6 +102,6 @@ inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
 inline int red_bytes(int B) { return CONSUMER_WARPS * MAX_TILE_ROWS * B * 4; }
 inline int attn_aux_bytes(int G, int T, int D) { return (G * T + CONSUMER_WARPS * G * D + 8 * G) * 4; }
 constexpr int MBAR_BYTES = 512;    // up to 64 mbarriers
-constexpr int CTRL_BYTES = 128;
+constexpr int CTRL_BYTES = 128;   // 32 flag words
 constexpr int MAX_PAGES = 26;      // 2 * MAX_PAGES + 9 mbarriers must fit MBAR_BYTES
 }  // namespace mk

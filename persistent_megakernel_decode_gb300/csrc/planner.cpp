@@ -575,10 +575,13 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     p.abuf_bytes = round_up(B * kmax * 4, 128);
     p.act_bytes = round_up(attn_slot + B * RESID_ROWS * 4, 128);
     const int maxb = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8;  // kernel batch template
-    // attention scratch, then two reduction buffers (double-buffered across tiles)
+    // attention scratch, then the GEMV cross-warp reduction buffers
     p.red_bytes = round_up(red_bytes(maxb), 128);
-    int aux = round_up(attn_aux_bytes(G, kn_T, D), 128) + 2 * p.red_bytes;
-    int fixed = p.abuf_bytes + 2 * p.act_bytes + aux + MBAR_BYTES + CTRL_BYTES;
+    int aux = round_up(attn_aux_bytes(G, kn_T, D), 128) + NRED * p.red_bytes;
+    // one activation buffer per slot when two fit in 32 KB: the activation
+    // loader then stages instruction i + 1 while the consumers still read i
+    p.abuf_count = 2 * p.abuf_bytes <= 32768 ? 2 : 1;
+    int fixed = p.abuf_count * p.abuf_bytes + 2 * p.act_bytes + aux + MBAR_BYTES + CTRL_BYTES;
     p.aux_bytes = aux;
     p.num_pages = std::min(MAX_PAGES, (smem_per_cta - fixed) / p.page_bytes);
     p.smem_bytes = fixed + p.num_pages * p.page_bytes;
@@ -735,6 +738,11 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
             break;
         default:
             break;
+        }
+        if (op.opcode != MK_OP_ATTN && op.opcode != MK_OP_EMBED) {
+            const int rpp = p.page_bytes / (2 * pl[P_KC - W_P]);
+            pl[P_RPP - W_P] = rpp;
+            pl[P_NPG - W_P] = ceil_div(pl[P_NROWS - W_P], rpp);
         }
         p.tasks.push_back(t);
     }
