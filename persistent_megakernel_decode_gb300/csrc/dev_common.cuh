@@ -38,6 +38,9 @@ DEV void red_relaxed_add(uint32_t *p, uint32_t v) {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+DEV void st_relaxed_cta(volatile int *p, int v) {
+    asm volatile("st.relaxed.cta.shared.u32 [%0], %1;" ::"r"(saddr((const void *)p)), "r"(v) : "memory");
+}
 DEV void st_release_cta(volatile int *p, int v) {
     asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(saddr((const void *)p)), "r"(v) : "memory");
 }
@@ -183,10 +186,10 @@ struct Smem {
     uint32_t o_aux;       // op scratch (attention scores, partial outputs)
     uint32_t o_red0;      // cross-warp reduction buffers, alternating per instruction
     uint32_t red_stride;  // bytes
-    uint32_t o_bars;      // full[NP], empty[NP], act_full[2], act_empty[2], consumer barrier, doorbell
+    uint32_t o_bars;      // full[NP], empty[NP], act_full[2], act_empty[2], consumer barrier
     uint32_t o_ctrl;      // [0] abort, [1..2] slot flags, [3] attention: last split,
                           // [8..15] consumer warp progress (instructions finished + 1),
-                          // [16..19] reduction buffer arrivals, [20..23] reduction buffer epilogues done
+                          // [16..19] reduction buffer arrivals
     int num_pages;
     DEV float *abuf(int s) const { return reinterpret_cast<float *>(mk_smem + o_abuf + s * abuf_stride); }
     DEV uint8_t *act(int s) const { return mk_smem + o_act0 + s * act_stride; }
@@ -198,14 +201,12 @@ struct Smem {
     DEV uint64_t *act_full() const { return full() + 2 * num_pages; }
     DEV uint64_t *act_empty() const { return full() + 2 * num_pages + 2; }
     DEV uint64_t *cbar() const { return full() + 2 * num_pages + 4; }
-    DEV uint64_t *bell() const { return full() + 2 * num_pages + 5; }  // rung by every consumer hand-off
     DEV volatile int *ctrl() const { return reinterpret_cast<volatile int *>(mk_smem + o_ctrl); }
 };
 
 constexpr int SLOT_FRESH = 1;
 constexpr int C_RED_ARR = 16;   // ctrl words: arrivals per reduction buffer (monotone)
-constexpr int C_RED_FIN = 20;   // ctrl words: finished epilogues per reduction buffer (monotone)
-constexpr int CTRL_WORDS = 24;
+constexpr int CTRL_WORDS = 20;
 
 // Error path, kept out of line so that the hot loops stay small.
 static __device__ __noinline__ void raise_error_at(uint32_t *err, Smem S, int code, int slot, int event, uint32_t obs,
@@ -417,10 +418,12 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
         if (nrows <= 0 || (opc == MK_OP_UP ? 2 * nrows : nrows) > rmax) return false;
         if (kc <= 0 || kc % 8 || 2 * kc > P.page_bytes || kc * P.B * 4 > P.abuf_bytes) return false;
         const int rpp = F(I, P_RPP);
-        if (rpp != P.page_bytes / (2 * kc) || F(I, P_NPG) != (nrows + rpp - 1) / rpp) return false;
+        const int rows = (opc == MK_OP_UP ? 2 : 1) * nrows;
+        if (rpp != P.page_bytes / (2 * kc) || F(I, P_NPG) != (rows + rpp - 1) / rpp) return false;
         // x chunks per consumer thread x batch template must fit the kernel's registers
         const int maxb = P.B <= 1 ? 1 : P.B <= 2 ? 2 : P.B <= 4 ? 4 : 8;
-        if ((kc / 8 + CONSUMERS - 1) / CONSUMERS * maxb > 8) return false;
+        const int nch = (kc / 8 + CONSUMERS - 1) / CONSUMERS;
+        if (nch * maxb > 8 || nch > 4) return false;
     }
     if (opc == MK_OP_ATTN) {
         const int T = F(I, P_T);

@@ -20,45 +20,98 @@ namespace mk {
 
 // RMSNorm-fused ops stage x^ = h * rsqrt(mean(h^2) + eps) * w (fp32); O and
 // DOWN stage the attention output / their K chunk of the MLP activation.
+// Every load of a round is issued before any is used (up to SC float4 of the
+// activation and SC norm-weight quads per lane), so a staging costs a few
+// L2 round trips rather than one per loop iteration.
+constexpr int SC = 8;
+
+DEV void stage_copy(const float4 *s4, float4 *d4, int n4) {
+    const int lane = threadIdx.x & 31;
+    for (int base = 0; base < n4; base += 32 * SC) {
+        float4 v[SC];
+#pragma unroll
+        for (int j = 0; j < SC; ++j) {
+            const int k = base + lane + 32 * j;
+            if (k < n4) v[j] = __ldcg(s4 + k);
+        }
+#pragma unroll
+        for (int j = 0; j < SC; ++j) {
+            const int k = base + lane + 32 * j;
+            if (k < n4) d4[k] = v[j];
+        }
+    }
+}
+
 template <int MAXB>
 DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab) {
     const int lane = threadIdx.x & 31;
     const int opc = F(I, W_OPC);
     const int B = P.B;
     if (opc == MK_OP_QKV || opc == MK_OP_UP || opc == MK_OP_LM) {
-        const int H = P.H;
+        const int H = P.H, n4 = H / 4;
         const float *h = reinterpret_cast<const float *>(
             PTR(I, opc == MK_OP_QKV ? S_QKV_H : opc == MK_OP_UP ? S_UP_H : S_LM_H));
-        const uint16_t *w = reinterpret_cast<const uint16_t *>(
+        const uint2 *w4 = reinterpret_cast<const uint2 *>(
             PTR(I, opc == MK_OP_QKV ? S_QKV_NORM : opc == MK_OP_UP ? S_UP_NORM : S_LM_NORM));
         const int snap = F(I, P_SNAP);
         float *hist = nullptr;
         if (snap > 0 && !ab) hist = reinterpret_cast<float *>(PTR(I, opc == MK_OP_QKV ? S_QKV_HIST : S_LM_HIST));
+        const bool one_round = n4 <= 32 * SC;
         for (int b = 0; b < B; ++b) {
             const float4 *src = reinterpret_cast<const float4 *>(h + (size_t)b * H);
             float4 *dst = reinterpret_cast<float4 *>(abuf + (size_t)b * H);
             float4 *hs = hist ? reinterpret_cast<float4 *>(hist + ((size_t)(snap - 1) * B + b) * H) : nullptr;
             float ss = 0.f;
-#pragma unroll 4
-            for (int k = lane; k < H / 4; k += 32) {
-                const float4 v = __ldcg(src + k);
-                dst[k] = v;
-                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-                if (hs) hs[k] = v;
+            float4 v[SC];
+            uint2 ww[SC];
+            for (int base = 0; base < n4; base += 32 * SC) {
+#pragma unroll
+                for (int j = 0; j < SC; ++j) {
+                    const int k = base + lane + 32 * j;
+                    if (k < n4) {
+                        v[j] = __ldcg(src + k);
+                        ww[j] = __ldg(w4 + k);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < SC; ++j) {
+                    const int k = base + lane + 32 * j;
+                    if (k < n4) {
+                        ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+                        if (!one_round) dst[k] = v[j];
+                        if (hs) hs[k] = v[j];
+                    }
+                }
             }
             ss = warp_sum(ss);
             const float scale = rsqrtf(ss / (float)H + P.eps);
-            __syncwarp();
-            const uint2 *w4 = reinterpret_cast<const uint2 *>(w);
-#pragma unroll 4
-            for (int k = lane; k < H / 4; k += 32) {
-                const uint2 ww = __ldg(w4 + k);
-                float4 v = dst[k];
-                v.x *= scale * __uint_as_float(ww.x << 16);
-                v.y *= scale * __uint_as_float(ww.x & 0xffff0000u);
-                v.z *= scale * __uint_as_float(ww.y << 16);
-                v.w *= scale * __uint_as_float(ww.y & 0xffff0000u);
-                dst[k] = v;
+            auto norm = [&](float4 x, uint2 w) {
+                x.x *= scale * __uint_as_float(w.x << 16);
+                x.y *= scale * __uint_as_float(w.x & 0xffff0000u);
+                x.z *= scale * __uint_as_float(w.y << 16);
+                x.w *= scale * __uint_as_float(w.y & 0xffff0000u);
+                return x;
+            };
+            if (one_round) {
+#pragma unroll
+                for (int j = 0; j < SC; ++j) {
+                    const int k = lane + 32 * j;
+                    if (k < n4) dst[k] = norm(v[j], ww[j]);
+                }
+            } else {
+                __syncwarp();
+                for (int base = 0; base < n4; base += 32 * SC) {
+#pragma unroll
+                    for (int j = 0; j < SC; ++j) {
+                        const int k = base + lane + 32 * j;
+                        if (k < n4) ww[j] = __ldg(w4 + k);
+                    }
+#pragma unroll
+                    for (int j = 0; j < SC; ++j) {
+                        const int k = base + lane + 32 * j;
+                        if (k < n4) dst[k] = norm(dst[k], ww[j]);
+                    }
+                }
             }
         }
     } else {
@@ -72,12 +125,9 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab) {
             src = reinterpret_cast<const float *>(PTR(I, S_DN_IN)) + F(I, P_K0);
             ld = (size_t)P.F;
         }
-        for (int b = 0; b < B; ++b) {
-            const float4 *s4 = reinterpret_cast<const float4 *>(src + b * ld);
-            float4 *d4 = reinterpret_cast<float4 *>(abuf + (size_t)b * kc);
-#pragma unroll 4
-            for (int k = lane; k < kc / 4; k += 32) d4[k] = __ldcg(s4 + k);
-        }
+        for (int b = 0; b < B; ++b)
+            stage_copy(reinterpret_cast<const float4 *>(src + b * ld), reinterpret_cast<float4 *>(abuf + (size_t)b * kc),
+                       kc / 4);
     }
 }
 
@@ -100,8 +150,31 @@ DEV void stage_resid(const KParams &P, const WIns &I, float *slot) {
 // theta_i = theta^(-2i/D)), bf16 rounding of the new k/v, and the KV-cache
 // append by the split that owns the new position.  Slot layout: q as
 // [G][4 quarters][D/4 + 4] (padded against bank conflicts), then k, then v.
+// RoPE factors of one position for this lane's dimension pairs, cached by
+// the activation loader across attention tasks of the same position.
 template <int D>
-DEV void stage_attn(const KParams &P, const WIns &I, float *slot, bool ab) {
+struct Rope {
+    int pos = -1;
+    float cs[D / 64], sn[D / 64];
+    DEV void at(const KParams &P, int p) {
+        if (p == pos) return;
+        pos = p;
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int j = 0; j < D / 64; ++j) {
+            // angle of pair i in double, reduced mod 2 pi, then a float sincos
+            const int i = lane + 32 * j;
+            const double inv_freq = exp2(-(2.0 * i / D) * log2((double)P.theta));
+            const double ang = (double)p * inv_freq;
+            const double two_pi = 6.283185307179586476925286766559;
+            const double red = ang - rint(ang / two_pi) * two_pi;
+            sincosf((float)red, &sn[j], &cs[j]);
+        }
+    }
+};
+
+template <int D, int GMAX>  // GMAX: bound on the q heads per kv head
+DEV void stage_attn(const KParams &P, const WIns &I, float *slot, bool ab, Rope<D> &rope) {
     constexpr int PER = D / 32;
     constexpr int QS = D / 4 + 4;
     const int lane = threadIdx.x & 31;
@@ -115,46 +188,41 @@ DEV void stage_attn(const KParams &P, const WIns &I, float *slot, bool ab) {
     float *kn = slot + G * 4 * QS;
     float *vn = kn + D;
     const float qscale = rsqrtf((float)D) * 1.4426950408889634f;
-    // angle of pair i in double, reduced mod 2 pi, then a float sincos
-    float cs[PER / 2], sn[PER / 2];
+    // every head's values in flight at once
+    float x[GMAX + 2][PER];
 #pragma unroll
-    for (int j = 0; j < PER / 2; ++j) {
-        const int i = lane + 32 * j;
-        const double inv_freq = exp2(-(2.0 * i / D) * log2((double)P.theta));
-        const double ang = (double)pos * inv_freq;
-        const double two_pi = 6.283185307179586476925286766559;
-        const double red = ang - rint(ang / two_pi) * two_pi;
-        sincosf((float)red, &sn[j], &cs[j]);
-    }
-    for (int h = 0; h < G + 2; ++h) {
-        float x[PER];
+    for (int h = 0; h < GMAX + 2; ++h)
 #pragma unroll
-        for (int e = 0; e < PER; ++e) x[e] = __ldcg(src + (size_t)h * D + lane + 32 * e);
+        for (int e = 0; e < PER; ++e) x[h][e] = h < G + 2 ? __ldcg(src + (size_t)h * D + lane + 32 * e) : 0.f;
+    rope.at(P, pos);
+#pragma unroll
+    for (int h = 0; h < GMAX + 2; ++h) {
+        if (h >= G + 2) continue;
         const bool is_q = h < G, is_k = h == G;
         if (P.qk_norm && (is_q || is_k)) {
             const uint16_t *w = is_q ? wq : wk;
             float ss = 0.f;
 #pragma unroll
-            for (int e = 0; e < PER; ++e) ss += x[e] * x[e];
+            for (int e = 0; e < PER; ++e) ss += x[h][e] * x[h][e];
             ss = warp_sum(ss);
             const float sc = rsqrtf(ss / (float)D + P.eps);
 #pragma unroll
-            for (int e = 0; e < PER; ++e) x[e] = x[e] * sc * bf16_at(w, lane + 32 * e);
+            for (int e = 0; e < PER; ++e) x[h][e] = x[h][e] * sc * bf16_at(w, lane + 32 * e);
         }
         if (is_q || is_k) {
 #pragma unroll
             for (int e = 0; e < PER / 2; ++e) {   // element lane+32e pairs with lane+32e+D/2
-                const float a = x[e], c = x[e + PER / 2];
-                x[e] = a * cs[e] - c * sn[e];
-                x[e + PER / 2] = a * sn[e] + c * cs[e];
+                const float a = x[h][e], c = x[h][e + PER / 2];
+                x[h][e] = a * rope.cs[e] - c * rope.sn[e];
+                x[h][e + PER / 2] = a * rope.sn[e] + c * rope.cs[e];
             }
         }
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
             const int d = lane + 32 * e;
-            if (is_q) qp[(h * 4 + d / (D / 4)) * QS + d % (D / 4)] = x[e] * qscale;
-            else if (is_k) kn[d] = round_bf16(x[e]);
-            else vn[d] = round_bf16(x[e]);
+            if (is_q) qp[(h * 4 + d / (D / 4)) * QS + d % (D / 4)] = x[h][e] * qscale;
+            else if (is_k) kn[d] = round_bf16(x[h][e]);
+            else vn[d] = round_bf16(x[h][e]);
         }
     }
     if (!ab && pos >= t0 && pos < t0 + T) {
@@ -238,27 +306,54 @@ DEV void row_dot(const uint8_t *wrow, int ct, int nchunk, const XChunks<MAXB, NC
     }
 }
 
+// Branch-free variant: every thread loads a chunk (threads past the row's
+// end re-read chunk 0 and zero it with `mask`), so the rows of a page can all
+// be in flight at once.
+template <int MAXB, int NCH>
+DEV void row_dot_nb(const uint8_t *wrow, const int (&off)[NCH], const uint32_t (&mask)[NCH],
+                    const XChunks<MAXB, NCH> &x, typename XChunks<MAXB, NCH>::Acc (&acc)[MAXB]) {
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+        uint4 w = *reinterpret_cast<const uint4 *>(wrow + off[j]);
+        w.x &= mask[j]; w.y &= mask[j]; w.z &= mask[j]; w.w &= mask[j];
+        if constexpr (XChunks<MAXB, NCH>::PAIRS) {
+            fma2(acc[0], bf16x2_pair(w.x), x.v[j][0]);
+            fma2(acc[0], bf16x2_pair(w.y), x.v[j][1]);
+            fma2(acc[0], bf16x2_pair(w.z), x.v[j][2]);
+            fma2(acc[0], bf16x2_pair(w.w), x.v[j][3]);
+        } else {
+            float w8[8];
+            bf16x8(w, w8);
+#pragma unroll
+            for (int b = 0; b < MAXB; ++b)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[b] = fmaf(w8[e], x.f[j][b][e], acc[b]);
+        }
+    }
+}
+
 // One GEMV tile (QKV, O, MLP-up, MLP-down, LM head) split over K: consumer
 // thread t holds the 8-wide K chunks t, t + 256, ... of x for every sequence
 // in registers (x is read once per tile, 4 bytes per weight column), so each
-// warp reads a contiguous 512-byte slice of every weight row.  Each warp's
-// partial sums are reduced across its lanes with a transposed butterfly and
-// parked in one of NRED shared buffers; the warp that arrives last sums the
-// 8 warps' partials in warp order and runs the epilogue -- no warp waits for
-// another.  EXACT: every page holds RPP rows of the tile (the page loop is
-// unrolled and one butterfly covers the tile); otherwise pages hold up to RPP
-// rows and each page is reduced on its own.
-template <int MAXB, int NCH, int RPP, bool EXACT>
-DEV void gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+// warp reads a contiguous 512-byte slice of every weight row.  The tile's rows
+// (MLP-up: gate rows, then up rows) lie in its pages in order, RPP to a page
+// at most.  Each warp's partial sums are reduced across its lanes with a
+// transposed butterfly and parked in one of NRED shared buffers; the warp that
+// arrives last sums the 8 warps' partials in warp order and runs the epilogue
+// -- no warp waits for another.  ONE_PAGE: the whole tile is on one page
+// (one wait, one release, one butterfly); otherwise each page is reduced on
+// its own.  Returns whether this warp ran the epilogue (wrote global memory).
+template <int MAXB, int NCH, int RPP, bool ONE_PAGE>
+DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
                    RingPos &rq, uint32_t &ured, unsigned long long &lm_best, bool &ab) {
     constexpr int RMAX = rows_max<MAXB>();
     constexpr int VT = RMAX * MAXB;            // partials per warp in a reduction buffer: row * MAXB + b
     constexpr int VL = VT >= 32 ? VT / 32 : 1; // epilogue values per lane: v = lane + 32 j
     const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
     const int opc = F(I, W_OPC);
-    const int kc = F(I, P_KC), nrows = F(I, P_NROWS), npg0 = F(I, P_NPG);
-    const int rpp = EXACT ? RPP : min(F(I, P_RPP), RPP);
-    const int npg = (opc == MK_OP_UP ? 2 : 1) * npg0;
+    const int kc = F(I, P_KC), nrows = F(I, P_NROWS), npg = F(I, P_NPG);
+    const int total = (opc == MK_OP_UP ? 2 : 1) * nrows;
+    const int rpp = min(F(I, P_RPP), RPP);
     const int nchunk = kc >> 3, row_bytes = kc * 2;
     const int B = P.B;
     using X = XChunks<MAXB, NCH>;
@@ -277,36 +372,48 @@ DEV void gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const f
             if (v < VT && b < B && r < nrows) resid_v[j] = rs[b * RESID_ROWS + r];
         }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.act_empty()[i & 1]);  // activation buffer and slot no longer needed
+    if constexpr (!ONE_PAGE) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.act_empty()[i & 1]);  // activation buffer and slot no longer needed
+    }
 
-    // the reduction buffer this tile uses; its previous tile's epilogue must have read it
+    // The reduction buffer this tile uses.  Its previous user, NRED GEMV tiles
+    // back, has finished its epilogue: a warp reaches slot s only after every
+    // warp released the activation slot of s - 2, i.e. finished slot s - 3
+    // (epilogue included), and NRED >= 3 GEMV tiles lie between the two users.
     const int rb = (int)(ured % NRED);
     const uint32_t use = ured / NRED;
     ++ured;
-    if (!ab) ab = !warp_wait_smem(P, S, &S.ctrl()[C_RED_FIN + rb], use, i, opc);
     float *red = S.red(rb) + warp * VT;
     ring += npg;
 
-    if constexpr (EXACT) {
-        constexpr int NPGMAX = RMAX / RPP;
+    if constexpr (ONE_PAGE) {
+        // all RPP rows of the page, unconditionally: the caller guarantees
+        // RPP * row_bytes <= page_bytes, and rows past the tile's end (stale
+        // page bytes) only feed partials that the epilogue never reads
+        int off[NCH];
+        uint32_t mask[NCH];
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+            const int c = ct + CONSUMERS * j;
+            off[j] = (c < nchunk ? c : 0) * 16;
+            mask[j] = c < nchunk ? 0xffffffffu : 0u;
+        }
         typename X::Acc acc[RMAX][MAXB];
 #pragma unroll
         for (int r = 0; r < RMAX; ++r)
 #pragma unroll
             for (int b = 0; b < MAXB; ++b) acc[r][b] = 0;
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
+        const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
 #pragma unroll
-        for (int pg = 0; pg < NPGMAX; ++pg) {
-            if (pg < npg) {
-                if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
-                const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
-#pragma unroll
-                for (int r = 0; r < RPP; ++r) row_dot<MAXB, NCH>(page + (size_t)r * row_bytes, ct, nchunk, x, acc[pg * RPP + r]);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
-                rq.next(P.num_pages);
-            }
+        for (int r = 0; r < RPP; ++r) row_dot_nb<MAXB, NCH>(page + (size_t)r * row_bytes, off, mask, x, acc[r]);
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&S.empty()[rq.p]);
+            mbar_arrive(&S.act_empty()[i & 1]);  // activation buffer and slot no longer needed
         }
+        rq.next(P.num_pages);
         float v[VT];
 #pragma unroll
         for (int r = 0; r < RMAX; ++r)
@@ -322,9 +429,7 @@ DEV void gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const f
     } else {
         constexpr int VP = RPP * MAXB;
         for (int pg = 0; pg < npg; ++pg) {
-            const int seg = pg >= npg0;
-            const int r0 = (pg - seg * npg0) * rpp;  // first row of the page within its segment
-            const int cnt = min(rpp, nrows - r0);
+            const int r0 = pg * rpp, cnt = min(rpp, total - r0);
             if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
             const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
             typename X::Acc acc[RPP][MAXB];
@@ -343,7 +448,7 @@ DEV void gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const f
 #pragma unroll
                 for (int b = 0; b < MAXB; ++b) v[r * MAXB + b] = X::value(acc[r][b]);
             Bfly<VP, 16>::run(v, lane);
-            const int base = (seg * nrows + r0) * MAXB;
+            const int base = r0 * MAXB;
             if constexpr (VP >= 32) {
 #pragma unroll
                 for (int j = 0; j < VP / 32; ++j) {
@@ -359,7 +464,7 @@ DEV void gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const f
     __syncwarp();
     int last = 0;
     if (lane == 0) last = atom_add_acqrel_cta(&S.ctrl()[C_RED_ARR + rb], 1) == (int)(CONSUMER_WARPS * use + CONSUMER_WARPS - 1);
-    if (!__shfl_sync(FULL, last, 0)) return;
+    if (!__shfl_sync(FULL, last, 0)) return false;
     __syncwarp();
 
     // epilogue (the last warp): lane handles v = lane + 32 j, i.e. row v / MAXB of sequence v % MAXB
@@ -414,8 +519,7 @@ DEV void gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const f
             }
         }
     }
-    __syncwarp();
-    if (lane == 0) st_release_cta(&S.ctrl()[C_RED_FIN + rb], (int)use + 1);
+    return true;
 }
 
 // Split-KV attention of one (sequence, kv group, split): scores from the

@@ -47,46 +47,63 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
         }
         Seg s0, s1;
         const int nseg = describe(P, I, s0, s1);
-        bool stop = false;
         if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 4] = gtimer();
-        // one segment: its rows packed into as few pages as the page size allows
-        auto issue = [&](const Seg &sg) {
-            const int rpp = sg.row_bytes > 0 ? PS / sg.row_bytes : 0;
-            if (rpp < 1) {
-                if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
-                stop = true;
-                return;
-            }
-            for (int r = 0; r < sg.rows; r += rpp) {
-                const int nr = min(rpp, sg.rows - r);
-                const uint32_t p = rp;
-                if (!warp_wait_bar(P, S, &S.empty()[p], rph ^ 1, 0, i, opc)) {
-                    stop = true;
-                    return;
-                }
-                if (lane == 0) {
-                    uint8_t *dst = S.pages() + (size_t)p * PS;
-                    const uint32_t bytes = (uint32_t)nr * sg.row_bytes;
-                    mbar_expect_tx(&S.full()[p], bytes);
-                    const uint8_t *src = sg.src + (long long)r * sg.stride;
-                    if (sg.stride == sg.row_bytes) {
-                        bulk_g2s(dst, src, bytes, &S.full()[p], pol);
-                    } else {
-                        for (int j = 0; j < nr; ++j)
-                            bulk_g2s(dst + (size_t)j * sg.row_bytes, src + (long long)j * sg.stride, sg.row_bytes,
-                                     &S.full()[p], pol);
-                    }
-                }
-                __syncwarp();
-                ++ring;
-                if (++rp == (uint32_t)NP) {
-                    rp = 0;
-                    rph ^= 1;
-                }
+        // Rows go to pages in order, as many whole rows per page as fit.  GEMV
+        // segments (MLP-up: gate rows, then up rows) share pages; attention
+        // keeps its K rows and its V rows on separate pages.
+        const int row_bytes = nseg > 0 ? s0.row_bytes : 0;
+        const int rpp = row_bytes > 0 ? PS / row_bytes : 0;
+        if (nseg > 0 && (rpp < 1 || (nseg > 1 && s1.row_bytes != row_bytes))) {
+            if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
+            break;
+        }
+        // lane 0: copy rows [r, r + n) of a segment to dst
+        auto copy_rows = [&](const Seg &sg, int r, int n, uint8_t *dst, uint64_t *bar) {
+            const uint8_t *src = sg.src + (long long)r * sg.stride;
+            if (sg.stride == sg.row_bytes) {
+                bulk_g2s(dst, src, (uint32_t)n * row_bytes, bar, pol);
+            } else {
+                for (int j = 0; j < n; ++j)
+                    bulk_g2s(dst + (size_t)j * row_bytes, src + (long long)j * sg.stride, row_bytes, bar, pol);
             }
         };
-        if (nseg > 0) issue(s0);
-        if (nseg > 1 && !stop) issue(s1);
+        const bool packed = opc != MK_OP_ATTN;
+        const int n0 = nseg > 0 ? s0.rows : 0, n1 = nseg > 1 ? s1.rows : 0;
+        // pages: packed -> over the concatenated rows; else per segment
+        const int total = packed ? n0 + n1 : 0;
+        const int npages = packed ? (total + rpp - 1) / (rpp > 0 ? rpp : 1)
+                                  : (n0 + rpp - 1) / (rpp > 0 ? rpp : 1) + (n1 + rpp - 1) / (rpp > 0 ? rpp : 1);
+        const int npg0 = packed ? 0 : (n0 + rpp - 1) / (rpp > 0 ? rpp : 1);
+        bool stop = false;
+        for (int k = 0; k < npages; ++k) {
+            if (!warp_wait_bar(P, S, &S.empty()[rp], rph ^ 1, 0, i, opc)) {
+                stop = true;
+                break;
+            }
+            if (lane == 0) {
+                uint8_t *dst = S.pages() + (size_t)rp * PS;
+                uint64_t *bar = &S.full()[rp];
+                if (packed) {
+                    const int r = k * rpp, nr = min(rpp, total - r);
+                    mbar_expect_tx(bar, (uint32_t)nr * row_bytes);
+                    const int a0 = min(nr, max(0, n0 - r));       // rows from segment 0
+                    if (a0 > 0) copy_rows(s0, r, a0, dst, bar);
+                    if (nr > a0) copy_rows(s1, r + a0 - n0, nr - a0, dst + (size_t)a0 * row_bytes, bar);
+                } else {
+                    const bool second = k >= npg0;
+                    const Seg &sg = second ? s1 : s0;
+                    const int r = (second ? k - npg0 : k) * rpp, nr = min(rpp, sg.rows - r);
+                    mbar_expect_tx(bar, (uint32_t)nr * row_bytes);
+                    copy_rows(sg, r, nr, dst, bar);
+                }
+            }
+            __syncwarp();
+            ++ring;
+            if (++rp == (uint32_t)NP) {
+                rp = 0;
+                rph ^= 1;
+            }
+        }
         if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 5] = gtimer();
         if (stop) break;
     }
@@ -111,6 +128,8 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
     const bool two_bufs = P.abuf_count > 1;
     long long key0 = -1, key1 = -1;   // what each activation buffer holds: op row << 32 | first column
     bool ab = false;
+    Rope<64> rope64;
+    Rope<128> rope128;
     int seen_ev = -1;           // last event seen satisfied, and the target it met
     uint32_t seen_target = 0;
     WIns I;
@@ -144,8 +163,9 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
         float *slot = reinterpret_cast<float *>(S.act(sl));
         int flags = 0;
         if (opc == MK_OP_ATTN) {
-            if (P.D == 64) stage_attn<64>(P, I, slot, ab);
-            else stage_attn<128>(P, I, slot, ab);
+            const bool g4 = P.Hq <= 4 * P.Hkv;
+            if (P.D == 64) g4 ? stage_attn<64, 4>(P, I, slot, ab, rope64) : stage_attn<64, 8>(P, I, slot, ab, rope64);
+            else g4 ? stage_attn<128, 4>(P, I, slot, ab, rope128) : stage_attn<128, 8>(P, I, slot, ab, rope128);
             flags = SLOT_FRESH;
             key0 = key1 = -1;
         } else if (opc >= MK_OP_QKV) {
@@ -175,14 +195,13 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
 }
 
 // ---------------------------------------------------------------- consumer warps
-// Publisher warp.  Every consumer warp posts, with a CTA-scope release store,
-// how many queue slots it has finished, and rings a doorbell mbarrier.  The
-// publisher sleeps on the doorbell (a bounded try_wait, so a missed ring costs
-// at most the hint), takes the minimum over the 8 warps: every instruction
-// below it is fully written back.  One GPU-scope fence then covers the whole
-// batch (it is cumulative over what the polls observed) and the batch's
-// signals are added to the event counters -- so consumers never wait for a
-// fence, and the waiting publisher issues no instructions.
+// Publisher warp.  Every consumer warp posts how many queue slots it has
+// finished (a CTA-scope release store when it wrote global memory in the
+// slot, else a relaxed one).  Lane 0 of the publisher polls the 8 counters
+// with two vector loads; their minimum says every instruction below it is
+// fully written back.  One GPU-scope fence then covers the whole batch (it is
+// cumulative over what the polls observed) and the batch's signals are added
+// to the event counters -- so consumers never wait for a fence.
 DEV int progress_min(const Smem S) {
     int4 a, b;
     const uint32_t p = saddr((const void *)(S.ctrl() + 8));
@@ -195,7 +214,6 @@ DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int lane = threadIdx.x & 31;
     int next = 0;                                              // first slot not yet published
     int wc = queue_word(P, myq, 0), wn = queue_word(P, myq, 1);  // words of slots next, next + 1
-    uint32_t bell_ph = 0;
     while (next < P.lmax) {
         if (__shfl_sync(FULL, wc, W_OPC) == MK_OP_NOOP) break;  // NoOps only pad the tail
         int done = next, ab = 0, stop = 0;
@@ -205,8 +223,7 @@ DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
                 done = progress_min(S);
                 ab = S.ctrl()[0] != 0;
                 if (done > next || ab) break;
-                if (mbar_wait_hint(S.bell(), bell_ph, 500)) bell_ph ^= 1;
-                if ((it & 15) == 15) {
+                if ((it & 63) == 63) {
                     const uint64_t now = gtimer();
                     if (t0 == 0) t0 = now;
                     if (aborted(P, S)) { stop = 1; break; }
@@ -237,42 +254,48 @@ DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
     }
 }
 
-// A consumer warp records that queue slot i is written back.
-DEV void handoff(const Smem S, int i) {
+// A consumer warp records that queue slot i is finished.
+DEV void handoff(const Smem S, int i, bool wrote_global) {
     __syncwarp();
     const int warp = (threadIdx.x >> 5) - 2;
     if ((threadIdx.x & 31) == 0) {
-        st_release_cta(&S.ctrl()[8 + warp], i + 1);
-        mbar_arrive(S.bell());
+        if (wrote_global) st_release_cta(&S.ctrl()[8 + warp], i + 1);
+        else st_relaxed_cta(&S.ctrl()[8 + warp], i + 1);
     }
 }
 
-// GEMV variants: K chunks per consumer thread (NCH) x page geometry.  Pages
-// of exactly 1, 2 or 4 rows that tile the tile's rows take the unrolled path.
+// GEMV variants: K chunks per consumer thread (NCH) x one page or several.
+// One-page tiles compute RPP rows unconditionally, RPP the power of two at or
+// above the tile's rows, as long as RPP rows fit the page.
 template <int MAXB, int NCH>
-DEV void gemv_geom(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+DEV bool gemv_geom(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
                    RingPos &rq, uint32_t &ured, unsigned long long &lm_best, bool &ab) {
     constexpr int RMAX = rows_max<MAXB>();
-    const int rpp = F(I, P_RPP), nrows = F(I, P_NROWS);
-    const bool tiled = rpp <= 4 && (nrows & (rpp - 1)) == 0 && (rpp & (rpp - 1)) == 0;
-    if (tiled && rpp == 4) gemv_tile<MAXB, NCH, 4, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
-    else if (tiled && rpp == 2) gemv_tile<MAXB, NCH, 2, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
-    else if (tiled && rpp == 1) gemv_tile<MAXB, NCH, 1, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
-    else gemv_tile<MAXB, NCH, RMAX, false>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+    const int total = (F(I, W_OPC) == MK_OP_UP ? 2 : 1) * F(I, P_NROWS), row_bytes = 2 * F(I, P_KC);
+    if (F(I, P_NPG) == 1) {
+        if (total > 8 && RMAX * row_bytes <= P.page_bytes)
+            return gemv_tile<MAXB, NCH, RMAX, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+        if (total > 4 && total <= 8 && 8 * row_bytes <= P.page_bytes)
+            return gemv_tile<MAXB, NCH, 8, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+        if (total <= 4 && 4 * row_bytes <= P.page_bytes)
+            return gemv_tile<MAXB, NCH, 4, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+    }
+    return gemv_tile<MAXB, NCH, RMAX, false>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
 }
 template <int MAXB>
-DEV void gemv_dispatch(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+DEV bool gemv_dispatch(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
                        RingPos &rq, uint32_t &ured, unsigned long long &lm_best, bool &ab) {
     const int nch = ((F(I, P_KC) >> 3) + CONSUMERS - 1) / CONSUMERS;
-    constexpr int NCHMAX = MAXB >= 8 ? 1 : (MAXB >= 4 ? 2 : (MAXB >= 2 ? 4 : 8));
-    if (nch <= 1) gemv_geom<MAXB, 1>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
-    else if constexpr (NCHMAX >= 2) {
-        if (nch <= 2) gemv_geom<MAXB, 2>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
-        else if constexpr (NCHMAX >= 4) {
-            if (nch <= 4) gemv_geom<MAXB, 4>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
-            else if constexpr (NCHMAX >= 8) gemv_geom<MAXB, 8>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+    constexpr int NCHMAX = MAXB >= 8 ? 1 : (MAXB >= 4 ? 2 : 4);
+    if (nch <= 1) return gemv_geom<MAXB, 1>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+    if constexpr (NCHMAX >= 2) {
+        if (nch <= 2) return gemv_geom<MAXB, 2>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+        if constexpr (NCHMAX >= 4) {
+            if (nch <= 4) return gemv_geom<MAXB, 4>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+            if constexpr (NCHMAX >= 8) return gemv_geom<MAXB, 8>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
         }
     }
+    return false;
 }
 
 template <int MAXB>
@@ -291,8 +314,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         uint64_t t_start = 0;
         if (ct == 0 && P.trace) t_start = gtimer();
         const int sl = i & 1;
-        if (P.trace && ct == 0 && !mbar_test(&S.act_full()[sl], (uint32_t)(i >> 1) & 1))
-            P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 12] = 1;   // activation not ready on arrival
+        bool wrote = true;  // the warp wrote global memory in this slot
         if (!ab) ab = !warp_wait_bar(P, S, &S.act_full()[sl], (uint32_t)(i >> 1) & 1, 2, i, opc);
         if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 13] = gtimer();
         const float *slot = reinterpret_cast<const float *>(S.act(sl));
@@ -304,13 +326,14 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
             consumer_sync(P, S, cph, ab, i);
             embed_task(P, S, I, i, ab);
         } else if (opc >= MK_OP_QKV) {
-            gemv_dispatch<MAXB>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+            wrote = gemv_dispatch<MAXB>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
         } else {  // COUNTER: the slot handshake only
             consumer_sync(P, S, cph, ab, i);
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.act_empty()[sl]);
+            wrote = false;
         }
-        handoff(S, i);
+        handoff(S, i, wrote);
         const int task = F(I, W_TASK);
         if (ct == 0 && P.trace) {
             uint64_t *tr = P.trace + ((size_t)blockIdx.x * P.lmax + i) * 16;
@@ -346,7 +369,6 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
             mbar_init(&S.act_empty()[s], CONSUMER_WARPS);
         }
         mbar_init(S.cbar(), CONSUMER_WARPS);
-        mbar_init(S.bell(), 1);
         for (int k = 0; k < CTRL_WORDS; ++k) S.ctrl()[k] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -36,7 +36,7 @@ enum : int {
     P_SNAP = W_P + 6,   // 1 + layer whose residual the activation loader snapshots, or 0
     P_KTOT = W_P + 7,   // row length (elements) of the source matrix
     P_RPP = W_P + 8,    // weight rows per page: page bytes / (2 * K chunk)
-    P_NPG = W_P + 9,    // pages per segment: ceil(rows / P_RPP)
+    P_NPG = W_P + 9,    // pages of the tile: ceil(rows of all segments / P_RPP)
 };
 // ATTN payload
 enum : int {

@@ -538,8 +538,7 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     auto clampi = [](int v, int lo, int hi) { return std::max(lo, std::min(hi, v)); };
     auto pow2_floor = [](int v) { int r = 1; while (r * 2 <= v) r *= 2; return r; };
     const int tile = 65536;
-    p.page_bytes = tgt->page_bytes > 0 ? tgt->page_bytes : 16384;
-    if (p.page_bytes % 128) return set_error(MK_ERR_INVALID, "page_bytes must be a multiple of 128");
+    if (tgt->page_bytes < 0 || tgt->page_bytes % 128) return set_error(MK_ERR_INVALID, "page_bytes must be a multiple of 128");
     const int rcap = B > 4 ? 8 : 16;
     int kn_qkv = tgt->rows_qkv > 0 ? tgt->rows_qkv : pow2_floor(clampi(tile / (2 * H), 1, rcap));
     int kn_o = tgt->rows_o > 0 ? tgt->rows_o : pow2_floor(clampi(tile / (2 * Hq * D), 1, rcap));
@@ -562,11 +561,9 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     if (D % kn_qkv) return set_error(MK_ERR_UNSUPPORTED, "rows_qkv must divide head_dim");
     if (F % kn_up || F % kn_kc || kn_kc % 8) return set_error(MK_ERR_UNSUPPORTED, "rows_up / kchunk_down must divide ffn");
     if (kn_T > 256 || kn_T < 1) return set_error(MK_ERR_UNSUPPORTED, "attn_split must be 1..256");
-    for (int K : {H, Hq * D, kn_kc}) {
-        if (2 * K > p.page_bytes) return set_error(MK_ERR_UNSUPPORTED, "a weight row does not fit one page");
-        if (B * ceil_div(K, 2048) > 8) return set_error(MK_ERR_UNSUPPORTED, "batch x K too large for register-held activations");
-    }
-    if (kn_T * D * 2 > p.page_bytes * 8) return set_error(MK_ERR_UNSUPPORTED, "attention split too long");
+    for (int K : {H, Hq * D, kn_kc})
+        if (B * ceil_div(K, 2048) > 8 || K > 8192)
+            return set_error(MK_ERR_UNSUPPORTED, "batch x K too large for register-held activations");
     // shared memory budget
     int kmax = std::max(std::max(H, Hq * D), kn_kc);
     int attn_slot = (G * (D + 16) + 2 * D) * 4;
@@ -583,6 +580,21 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     p.abuf_count = 2 * p.abuf_bytes <= 32768 ? 2 : 1;
     int fixed = p.abuf_count * p.abuf_bytes + 2 * p.act_bytes + aux + MBAR_BYTES + CTRL_BYTES;
     p.aux_bytes = aux;
+    // page size: a 64 KB tile per page when three of them fit (one wait and one
+    // release per tile, three tiles in flight), else 32 KB, else 16 KB
+    if (tgt->page_bytes > 0) {
+        p.page_bytes = tgt->page_bytes;
+    } else {
+        p.page_bytes = 16384;
+        for (int pb : {65536, 32768})
+            if ((smem_per_cta - fixed) / pb >= 3) {
+                p.page_bytes = pb;
+                break;
+            }
+    }
+    for (int K : {H, Hq * D, kn_kc})
+        if (2 * K > p.page_bytes) return set_error(MK_ERR_UNSUPPORTED, "a weight row does not fit one page");
+    if (kn_T * D * 2 > p.page_bytes * 8) return set_error(MK_ERR_UNSUPPORTED, "attention split too long");
     p.num_pages = std::min(MAX_PAGES, (smem_per_cta - fixed) / p.page_bytes);
     p.smem_bytes = fixed + p.num_pages * p.page_bytes;
     // pages used by the largest instruction
@@ -591,7 +603,7 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
         int rpp = p.page_bytes / row_bytes;
         return ceil_div(rows, rpp);
     };
-    int need = std::max({pages_for(kn_qkv, 2 * H), pages_for(kn_o, 2 * Hq * D), 2 * pages_for(kn_up, 2 * H),
+    int need = std::max({pages_for(kn_qkv, 2 * H), pages_for(kn_o, 2 * Hq * D), pages_for(2 * kn_up, 2 * H),
                          pages_for(kn_dn, 2 * kn_kc), pages_for(kn_lm, 2 * H), 2 * pages_for(kn_T, 2 * D)});
     if (p.num_pages < std::max(2, need))
         return set_error(MK_ERR_UNSUPPORTED, "shared memory too small for the page pool");
@@ -740,9 +752,10 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
             break;
         }
         if (op.opcode != MK_OP_ATTN && op.opcode != MK_OP_EMBED) {
+            // the tile's rows (MLP-up: gate rows, then up rows) packed into pages
             const int rpp = p.page_bytes / (2 * pl[P_KC - W_P]);
             pl[P_RPP - W_P] = rpp;
-            pl[P_NPG - W_P] = ceil_div(pl[P_NROWS - W_P], rpp);
+            pl[P_NPG - W_P] = ceil_div((op.opcode == MK_OP_UP ? 2 : 1) * pl[P_NROWS - W_P], rpp);
         }
         p.tasks.push_back(t);
     }
