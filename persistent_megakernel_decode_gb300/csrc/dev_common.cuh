@@ -54,11 +54,9 @@ DEV int ld_relaxed_cta(volatile int *p) {
     asm volatile("ld.relaxed.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr((const void *)p)) : "memory");
     return v;
 }
-DEV int atom_add_acqrel_cta(volatile int *p, int v) {
-    int old;
-    asm volatile("atom.acq_rel.cta.shared.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(saddr((const void *)p)), "r"(v) : "memory");
-    return old;
-}
+// Named hardware barrier 1 over the 8 consumer warps (barrier 0 is the
+// block-wide __syncthreads); it also orders their shared-memory accesses.
+DEV void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS) : "memory"); }
 DEV void red_release_add(uint32_t *p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -188,8 +186,7 @@ struct Smem {
     uint32_t red_stride;  // bytes
     uint32_t o_bars;      // full[NP], empty[NP], act_full[2], act_empty[2], consumer barrier
     uint32_t o_ctrl;      // [0] abort, [1..2] slot flags, [3] attention: last split,
-                          // [8..15] consumer warp progress (instructions finished + 1),
-                          // [16..19] reduction buffer arrivals
+                          // [8..15] consumer warp progress (instructions finished + 1)
     int num_pages;
     DEV float *abuf(int s) const { return reinterpret_cast<float *>(mk_smem + o_abuf + s * abuf_stride); }
     DEV uint8_t *act(int s) const { return mk_smem + o_act0 + s * act_stride; }
@@ -205,8 +202,7 @@ struct Smem {
 };
 
 constexpr int SLOT_FRESH = 1;
-constexpr int C_RED_ARR = 16;   // ctrl words: arrivals per reduction buffer (monotone)
-constexpr int CTRL_WORDS = 20;
+constexpr int CTRL_WORDS = 16;
 
 // Error path, kept out of line so that the hot loops stay small.
 static __device__ __noinline__ void raise_error_at(uint32_t *err, Smem S, int code, int slot, int event, uint32_t obs,

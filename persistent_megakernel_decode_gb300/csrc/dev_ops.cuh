@@ -338,9 +338,10 @@ DEV void row_dot_nb(const uint8_t *wrow, const int (&off)[NCH], const uint32_t (
 // warp reads a contiguous 512-byte slice of every weight row.  The tile's rows
 // (MLP-up: gate rows, then up rows) lie in its pages in order, RPP to a page
 // at most.  Each warp's partial sums are reduced across its lanes with a
-// transposed butterfly and parked in one of NRED shared buffers; the warp that
-// arrives last sums the 8 warps' partials in warp order and runs the epilogue
-// -- no warp waits for another.  ONE_PAGE: the whole tile is on one page
+// transposed butterfly and parked in one of NRED shared buffers; after a
+// hardware barrier of the 8 consumer warps, one warp (rotating) sums the
+// partials in warp order and runs the epilogue while the others move on to
+// the next instruction.  ONE_PAGE: the whole tile is on one page
 // (one wait, one release, one butterfly); otherwise each page is reduced on
 // its own.  Returns whether this warp ran the epilogue (wrote global memory).
 template <int MAXB, int NCH, int RPP, bool ONE_PAGE>
@@ -378,9 +379,9 @@ DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const f
     }
 
     // The reduction buffer this tile uses.  Its previous user, NRED GEMV tiles
-    // back, has finished its epilogue: a warp reaches slot s only after every
-    // warp released the activation slot of s - 2, i.e. finished slot s - 3
-    // (epilogue included), and NRED >= 3 GEMV tiles lie between the two users.
+    // back, has finished its epilogue: the epilogue warp of a tile passes the
+    // next GEMV tile's barrier only after it, and every writer of this tile
+    // has passed that barrier too.
     const int rb = (int)(ured % NRED);
     const uint32_t use = ured / NRED;
     ++ured;
@@ -461,11 +462,10 @@ DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const f
             }
         }
     }
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) last = atom_add_acqrel_cta(&S.ctrl()[C_RED_ARR + rb], 1) == (int)(CONSUMER_WARPS * use + CONSUMER_WARPS - 1);
-    if (!__shfl_sync(FULL, last, 0)) return false;
-    __syncwarp();
+    // the 8 consumer warps meet on a hardware barrier (it orders their shared
+    // writes before the epilogue's reads); warp `use % 8` runs the epilogue
+    consumer_bar();
+    if (warp != (int)(use % CONSUMER_WARPS)) return false;
 
     // epilogue (the last warp): lane handles v = lane + 32 j, i.e. row v / MAXB of sequence v % MAXB
     const float *rall = S.red(rb);
