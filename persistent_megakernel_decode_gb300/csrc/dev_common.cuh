@@ -361,6 +361,29 @@ DEV uint64_t PTR(const WIns &I, int k) {
     return ((uint64_t)hi << 32) | lo;
 }
 
+// The fields the consumers need of a slot, read with independent shuffles
+// issued back to back (one round of shuffle latency instead of a chain).
+struct Dec {
+    int opc, row, cnt, task, k0, kc, nrows, out0, snap, npg;
+    uint64_t out, out2;  // GEMV outputs
+};
+DEV Dec decode(const WIns &I) {
+    Dec d;
+    d.opc = F(I, W_OPC);
+    d.row = F(I, W_ROW);
+    d.cnt = F(I, W_CNT);
+    d.task = F(I, W_TASK);
+    d.k0 = F(I, P_K0);
+    d.kc = F(I, P_KC);
+    d.nrows = F(I, P_NROWS);
+    d.out0 = F(I, P_OUT0);
+    d.snap = F(I, P_SNAP);
+    d.npg = F(I, P_NPG);
+    d.out = PTR(I, S_G_OUT);
+    d.out2 = PTR(I, S_G_OUT2);
+    return d;
+}
+
 // Lane k's word of queue slot i (all zero, i.e. a NoOp, past the queue's end).
 DEV int queue_word(const KParams &P, const int32_t *q, int i) {
     return i < P.lmax ? __ldg(q + (size_t)i * W_WORDS + (threadIdx.x & 31)) : 0;

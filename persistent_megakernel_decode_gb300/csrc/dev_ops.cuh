@@ -345,7 +345,7 @@ DEV void row_dot_nb(const uint8_t *wrow, const int (&off)[NCH], const uint32_t (
 // (one wait, one release, one butterfly); otherwise each page is reduced on
 // its own.  Returns whether this warp ran the epilogue (wrote global memory).
 template <int MAXB, int NCH, int RPP, bool ONE_PAGE>
-DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
                    RingPos &rq, uint32_t &ured, unsigned long long &lm_best, bool &ab) {
     constexpr int RMAX = rows_max<MAXB>();
     constexpr int VT = RMAX * MAXB;            // partials per warp in a reduction buffer: row * MAXB + b
@@ -359,7 +359,7 @@ DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const f
     const int B = P.B;
     using X = XChunks<MAXB, NCH>;
     X x;
-    x.load(S.abuf(i & 1), ct, nchunk, kc, B);
+    x.load(S.abuf(sl), ct, nchunk, kc, B);
     // O tiles: the residual values this lane would need in the epilogue, read
     // before the slot is released (any warp may turn out to run the epilogue)
     float resid_v[VL];
@@ -375,7 +375,7 @@ DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const f
     }
     if constexpr (!ONE_PAGE) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.act_empty()[i & 1]);  // activation buffer and slot no longer needed
+        if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // activation buffer and slot no longer needed
     }
 
     // The reduction buffer this tile uses.  Its previous user, NRED GEMV tiles
@@ -412,7 +412,7 @@ DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const f
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(&S.empty()[rq.p]);
-            mbar_arrive(&S.act_empty()[i & 1]);  // activation buffer and slot no longer needed
+            mbar_arrive(&S.act_empty()[sl]);  // activation buffer and slot no longer needed
         }
         rq.next(P.num_pages);
         float v[VT];
@@ -522,12 +522,149 @@ DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, const f
     return true;
 }
 
+// ---------------------------------------------------------------- batch 1, rows per warp
+// Batch-1 GEMV tiles whose rows fit one page and whose K is a multiple of 256
+// up to 2048 take the row-per-warp path: warp w computes rows w and w + 8 of
+// the tile over the whole K, holding x (its lane's 8-wide chunks l, l + 32,
+// ...) in registers across tiles -- no cross-warp reduction and no barrier.
+DEV bool rpw_tile(const KParams &P, const Dec &d) {
+    if (P.B != 1 || d.opc < MK_OP_QKV || d.opc == MK_OP_ATTN) return false;
+    if (d.kc % 256 || d.kc > 2048 || d.npg != 1) return false;
+    return d.opc == MK_OP_UP ? d.nrows == 8 : d.nrows <= 16;
+}
+
+// The activation hand-off (activation loader stages, consumers wait) is due
+// for every slot except a row-per-warp tile that repeats the previous slot's
+// op, K chunk and waits: its input is the one already staged and waited for,
+// and x is still in the consumers' registers.  O tiles (their residual rows)
+// and snapshotting tiles always take it.  Both sides evaluate this on the same
+// instruction stream, so they agree slot by slot.
+struct HandoffChain {
+    int prev = 0;  // this lane's word of the previous slot
+    bool valid = false;
+};
+DEV bool needs_handoff(const KParams &P, const WIns &I, const Dec &d, HandoffChain &c) {
+    const int lane = threadIdx.x & 31;
+    const bool rpw = rpw_tile(P, d);
+    const bool input_word = lane == W_OPC || lane == W_ROW || lane == W_CNT ||
+                            (lane >= W_WAIT && lane < W_SIG) || lane == P_K0 || lane == P_KC;
+    const bool same = c.valid && !__any_sync(FULL, input_word && I.w != c.prev);
+    const bool skip = rpw && same && d.opc != MK_OP_O && d.snap == 0;
+    c.prev = I.w;
+    c.valid = rpw;
+    return !skip;
+}
+
+// x of a consumer lane for the row-per-warp path: chunk k covers columns
+// (lane + 32 k) * 8 .. + 8, as fp32 pairs.
+struct XRow {
+    uint64_t v[8][4];
+    long long key = -1;  // op row << 32 | first column of what v holds
+};
+
+template <int KG>
+DEV void rpw_row(const uint8_t *wrow, int lane, const XRow &x, uint64_t &acc) {
+#pragma unroll
+    for (int k = 0; k < KG; ++k) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(wrow + (lane + 32 * k) * 16);
+        fma2(acc, bf16x2_pair(w.x), x.v[k][0]);
+        fma2(acc, bf16x2_pair(w.y), x.v[k][1]);
+        fma2(acc, bf16x2_pair(w.z), x.v[k][2]);
+        fma2(acc, bf16x2_pair(w.w), x.v[k][3]);
+    }
+}
+
+// KG = K / 256 chunks per lane.  `handoff`: this slot took the activation
+// hand-off (the caller waited for activation slot sl); x is reloaded from the
+// slot's buffer when its input changed.  Returns true (the warp wrote global
+// memory).
+template <int KG>
+DEV bool gemv_rpw(const KParams &P, const Smem S, const Dec &d, int i, bool handoff, int sl, const float *slot,
+                  XRow &x, uint32_t &ring, RingPos &rq, unsigned long long &lm_best, bool &ab) {
+    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int opc = d.opc, nrows = d.nrows, row_bytes = d.kc * 2, out0 = d.out0;
+    const uint64_t ptr_a = d.out, ptr_b = d.out2;
+    const int r0 = warp, r1 = warp + 8;  // this warp's rows (MLP-up: gate row w, up row w)
+    float res0 = 0.f, res1 = 0.f;
+    if (handoff) {
+        const long long key = ((long long)d.row << 32) | (uint32_t)d.k0;
+        if (key != x.key) {
+            const float *xs = S.abuf(sl);
+#pragma unroll
+            for (int k = 0; k < KG; ++k) {
+                const float4 a = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8);
+                const float4 c = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8 + 4);
+                x.v[k][0] = pack2(a.x, a.y); x.v[k][1] = pack2(a.z, a.w);
+                x.v[k][2] = pack2(c.x, c.y); x.v[k][3] = pack2(c.z, c.w);
+            }
+            x.key = key;
+        }
+        if (opc == MK_OP_O) {
+            const float *rs = slot_resid(P, const_cast<float *>(slot));
+            res0 = rs[r0];
+            res1 = rs[r1];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // x and the residual rows are in registers
+    }
+    // this warp's two rows of the tile's page (rows past the tile's end hold
+    // stale page bytes; their results are not stored)
+    if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
+    const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
+    uint64_t acc0 = 0, acc1 = 0;
+    rpw_row<KG>(page + (size_t)r0 * row_bytes, lane, x, acc0);
+    rpw_row<KG>(page + (size_t)r1 * row_bytes, lane, x, acc1);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
+    rq.next(P.num_pages);
+    ++ring;
+    // lanes 0-15 end with row r0's sum, lanes 16-31 with row r1's
+    float v[2] = {sum2(acc0), sum2(acc1)};
+    Bfly<2, 16>::run(v, lane);
+    const float y1 = __shfl_sync(FULL, v[0], 16);
+    if (lane != 0 || ab) return true;
+    const float y0 = v[0];
+    if (opc == MK_OP_UP) {
+        if (r0 < nrows) reinterpret_cast<float *>(ptr_a)[out0 + r0] = y0 / (1.0f + __expf(-y0)) * y1;
+        return true;
+    }
+    const float yr[2] = {y0, y1};
+    const float rr[2] = {res0, res1};
+    float best = -INFINITY;
+    int bi = -1;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int r = j ? r1 : r0;
+        if (r >= nrows) continue;
+        const float y = yr[j];
+        if (opc == MK_OP_QKV) {
+            reinterpret_cast<float *>(ptr_a)[out0 + r] = y;
+        } else if (opc == MK_OP_O) {
+            reinterpret_cast<float *>(ptr_a)[out0 + r] = rr[j] + y;
+            reinterpret_cast<float *>(ptr_b)[out0 + r] = rr[j] + y;
+        } else if (opc == MK_OP_DOWN) {
+            atomicAdd(reinterpret_cast<float *>(ptr_a) + out0 + r, y);
+        } else if (opc == MK_OP_LM) {
+            reinterpret_cast<float *>(ptr_a)[out0 + r] = y;
+            if (y > best) { best = y; bi = r; }  // r0 < r1: ties keep the lower index
+        }
+    }
+    if (opc == MK_OP_LM && bi >= 0) {
+        const unsigned long long key = argmax_key(best, out0 + bi);
+        if (key > lm_best) {  // this warp's best key of the step so far
+            lm_best = key;
+            red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)P.step, key);
+        }
+    }
+    return true;
+}
+
 // Split-KV attention of one (sequence, kv group, split): scores from the
 // cached K rows in the page ring plus the new token, softmax partial in log2
 // units (max, sum), P.V, partial written out; the last split of the
 // (sequence, group) to arrive merges every split (log-sum-exp combine).
 template <int D>
-DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
                    uint32_t &cph, bool &ab) {
     constexpr int PER = D / 32;
     constexpr int QS = D / 4 + 4;
@@ -667,7 +804,7 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, const f
     __syncwarp();
     if (lane == 0) {
         for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(vring + k) % P.num_pages]);
-        mbar_arrive(&S.act_empty()[i & 1]);
+        mbar_arrive(&S.act_empty()[sl]);
     }
     consumer_sync(P, S, cph, ab, i);
     float *part = reinterpret_cast<float *>(PTR(I, S_AT_PART));
@@ -740,10 +877,10 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, const f
     }
 }
 
-DEV void embed_task(const KParams &P, const Smem S, const WIns &I, int i, bool ab) {
+DEV void embed_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, bool ab) {
     const int ct = threadIdx.x - 64, lane = ct & 31;
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.act_empty()[i & 1]);
+    if (lane == 0) mbar_arrive(&S.act_empty()[sl]);
     if (ab) return;
     const uint16_t *E = reinterpret_cast<const uint16_t *>(PTR(I, S_EMB_W));
     float *h = reinterpret_cast<float *>(PTR(I, S_EMB_H));

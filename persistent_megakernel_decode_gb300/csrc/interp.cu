@@ -132,14 +132,17 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
     Rope<128> rope128;
     int seen_ev = -1;           // last event seen satisfied, and the target it met
     uint32_t seen_target = 0;
+    uint32_t hs = 0;            // activation hand-offs so far; hand-off h uses activation slot h % 2
+    HandoffChain chain;
     WIns I;
     fetch_init(I, P, myq);
     for (int i = 0; i < P.lmax; ++i) {
         fetch(I, P, myq, i);
         const int opc = F(I, W_OPC);
         if (opc == MK_OP_NOOP) continue;
-        const int sl = i & 1;
-        const uint32_t use = (uint32_t)(i >> 1);
+        if (!needs_handoff(P, I, decode(I), chain)) continue;  // same input as the previous slot: nothing to stage
+        const int sl = hs & 1;
+        const uint32_t use = hs >> 1;
         if (!ab && !ins_valid(P, I)) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 1);
             ab = true;
@@ -175,8 +178,8 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
             const int bi = two_bufs ? sl : 0;
             const long long key = ((long long)F(I, W_ROW) << 32) | (uint32_t)F(I, P_K0);
             if (key != (bi ? key1 : key0) || F(I, P_SNAP) > 0) {
-                if (!two_bufs && i > 0 && !ab)
-                    ab = !warp_wait_bar(P, S, &S.act_empty()[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1, 1, i, opc);
+                if (!two_bufs && hs > 0 && !ab)
+                    ab = !warp_wait_bar(P, S, &S.act_empty()[(hs - 1) & 1], ((hs - 1) >> 1) & 1, 1, i, opc);
                 stage_gemv<MAXB>(P, I, S.abuf(bi), ab);
                 flags = SLOT_FRESH;
             }
@@ -191,6 +194,7 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
             S.ctrl()[1 + sl] = flags;
             mbar_arrive(&S.act_full()[sl]);
         }
+        ++hs;
     }
 }
 
@@ -255,7 +259,7 @@ DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
 }
 
 // A consumer warp records that queue slot i is finished.
-DEV void handoff(const Smem S, int i, bool wrote_global) {
+DEV void handoff_progress(const Smem S, int i, bool wrote_global) {
     __syncwarp();
     const int warp = (threadIdx.x >> 5) - 2;
     if ((threadIdx.x & 31) == 0) {
@@ -268,31 +272,31 @@ DEV void handoff(const Smem S, int i, bool wrote_global) {
 // One-page tiles compute RPP rows unconditionally, RPP the power of two at or
 // above the tile's rows, as long as RPP rows fit the page.
 template <int MAXB, int NCH>
-DEV bool gemv_geom(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+DEV bool gemv_geom(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
                    RingPos &rq, uint32_t &ured, unsigned long long &lm_best, bool &ab) {
     constexpr int RMAX = rows_max<MAXB>();
     const int total = (F(I, W_OPC) == MK_OP_UP ? 2 : 1) * F(I, P_NROWS), row_bytes = 2 * F(I, P_KC);
     if (F(I, P_NPG) == 1) {
         if (total > 8 && RMAX * row_bytes <= P.page_bytes)
-            return gemv_tile<MAXB, NCH, RMAX, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+            return gemv_tile<MAXB, NCH, RMAX, true>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
         if (total > 4 && total <= 8 && 8 * row_bytes <= P.page_bytes)
-            return gemv_tile<MAXB, NCH, 8, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+            return gemv_tile<MAXB, NCH, 8, true>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
         if (total <= 4 && 4 * row_bytes <= P.page_bytes)
-            return gemv_tile<MAXB, NCH, 4, true>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+            return gemv_tile<MAXB, NCH, 4, true>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
     }
-    return gemv_tile<MAXB, NCH, RMAX, false>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+    return gemv_tile<MAXB, NCH, RMAX, false>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
 }
 template <int MAXB>
-DEV bool gemv_dispatch(const KParams &P, const Smem S, const WIns &I, int i, const float *slot, uint32_t &ring,
+DEV bool gemv_dispatch(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
                        RingPos &rq, uint32_t &ured, unsigned long long &lm_best, bool &ab) {
     const int nch = ((F(I, P_KC) >> 3) + CONSUMERS - 1) / CONSUMERS;
     constexpr int NCHMAX = MAXB >= 8 ? 1 : (MAXB >= 4 ? 2 : 4);
-    if (nch <= 1) return gemv_geom<MAXB, 1>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+    if (nch <= 1) return gemv_geom<MAXB, 1>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
     if constexpr (NCHMAX >= 2) {
-        if (nch <= 2) return gemv_geom<MAXB, 2>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+        if (nch <= 2) return gemv_geom<MAXB, 2>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
         if constexpr (NCHMAX >= 4) {
-            if (nch <= 4) return gemv_geom<MAXB, 4>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
-            if constexpr (NCHMAX >= 8) return gemv_geom<MAXB, 8>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+            if (nch <= 4) return gemv_geom<MAXB, 4>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
+            if constexpr (NCHMAX >= 8) return gemv_geom<MAXB, 8>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
         }
     }
     return false;
@@ -302,42 +306,55 @@ template <int MAXB>
 DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int ct = threadIdx.x - 64, lane = ct & 31;
     uint32_t ring = 0, cph = 0, ured = 0;
-    RingPos rq;  // ring position of the next page (kept in step with ring)
+    uint32_t hs = 0;  // activation hand-offs so far (the activation loader counts the same ones)
+    HandoffChain chain;
+    XRow x;           // batch-1 row-per-warp activation, kept across tiles with the same input
+    RingPos rq;       // ring position of the next page (kept in step with ring)
     bool ab = false;
     unsigned long long lm_best = 0;
     WIns I;
     fetch_init(I, P, myq);
     for (int i = 0; i < P.lmax; ++i) {
         fetch(I, P, myq, i);
-        const int opc = F(I, W_OPC);
+        const Dec d = decode(I);
+        const int opc = d.opc;
         if (opc == MK_OP_NOOP) continue;
         uint64_t t_start = 0;
         if (ct == 0 && P.trace) t_start = gtimer();
-        const int sl = i & 1;
+        const bool handoff = needs_handoff(P, I, d, chain);
+        const int sl = hs & 1;
         bool wrote = true;  // the warp wrote global memory in this slot
-        if (!ab) ab = !warp_wait_bar(P, S, &S.act_full()[sl], (uint32_t)(i >> 1) & 1, 2, i, opc);
+        if (handoff && !ab) ab = !warp_wait_bar(P, S, &S.act_full()[sl], (hs >> 1) & 1, 2, i, opc);
         if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 13] = gtimer();
         const float *slot = reinterpret_cast<const float *>(S.act(sl));
         if (opc == MK_OP_ATTN) {
-            if (P.D == 64) attn_task<64>(P, S, I, i, slot, ring, cph, ab);
-            else attn_task<128>(P, S, I, i, slot, ring, cph, ab);
+            if (P.D == 64) attn_task<64>(P, S, I, i, sl, slot, ring, cph, ab);
+            else attn_task<128>(P, S, I, i, sl, slot, ring, cph, ab);
             rq.set(ring, P.num_pages);
         } else if (opc == MK_OP_EMBED) {
             consumer_sync(P, S, cph, ab, i);
-            embed_task(P, S, I, i, ab);
+            embed_task(P, S, I, i, sl, ab);
         } else if (opc >= MK_OP_QKV) {
-            wrote = gemv_dispatch<MAXB>(P, S, I, i, slot, ring, rq, ured, lm_best, ab);
+            if (MAXB == 1 && rpw_tile(P, d)) {  // (a constant condition for larger batches)
+                const int kg = d.kc >> 8;
+                if (kg <= 1) gemv_rpw<1>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+                else if (kg <= 2) gemv_rpw<2>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+                else if (kg <= 4) gemv_rpw<4>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+                else gemv_rpw<8>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+            } else {
+                wrote = gemv_dispatch<MAXB>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
+            }
         } else {  // COUNTER: the slot handshake only
             consumer_sync(P, S, cph, ab, i);
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.act_empty()[sl]);
             wrote = false;
         }
-        handoff(S, i, wrote);
-        const int task = F(I, W_TASK);
+        if (handoff) ++hs;
+        handoff_progress(S, i, wrote);
         if (ct == 0 && P.trace) {
             uint64_t *tr = P.trace + ((size_t)blockIdx.x * P.lmax + i) * 16;
-            tr[0] = (uint64_t)opc | ((uint64_t)(uint32_t)task << 32);
+            tr[0] = (uint64_t)opc | ((uint64_t)(uint32_t)d.task << 32);
             tr[1] = t_start;
             tr[3] = gtimer();
         }
@@ -478,6 +495,14 @@ static int build_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab) {
             break;
         default:
             break;
+        }
+        switch (p.op_kind[o]) {
+        case MK_OP_QKV: r[S_G_OUT] = r[S_QKV_OUT]; break;
+        case MK_OP_O: r[S_G_OUT] = r[S_O_HRES]; r[S_G_OUT2] = r[S_O_HMID]; break;
+        case MK_OP_UP: r[S_G_OUT] = r[S_UP_OUT]; break;
+        case MK_OP_DOWN: r[S_G_OUT] = r[S_DN_HRES]; break;
+        case MK_OP_LM: r[S_G_OUT] = r[S_LM_LOGITS]; r[S_G_OUT2] = r[S_LM_KEYS]; break;
+        default: break;
         }
     }
     return MK_OK;

@@ -61,6 +61,9 @@ enum : int {
     S_DN_W = 0, S_DN_IN = 1, S_DN_HRES = 2,
     // LM
     S_LM_W = 0, S_LM_NORM = 1, S_LM_H = 2, S_LM_LOGITS = 3, S_LM_KEYS = 4, S_LM_HIST = 5,
+    // every GEMV op: its output (QKV: qkv, O: residual, UP: activation, DOWN:
+    // residual, LM: logits) and second output (O: mid residual, LM: argmax keys)
+    S_G_OUT = 14, S_G_OUT2 = 15,
     N_SLOTS = 16,
 };
 
