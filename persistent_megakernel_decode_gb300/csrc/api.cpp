@@ -26,7 +26,7 @@ void layout_workspace(Plan &p) {
     for (auto &s : p.segments) total_slots += (size_t)s.workers * s.lmax;
     p.ws.err = take(E_WORDS * 4);
     p.ws.counters = take(p.thresholds.size() * 4);
-    p.ws.arrive = take(p.kind == PLAN_LLAMA ? (uint64_t)L * B * Hkv * 4 : 4);
+    p.ws.arrive = take(p.kind == PLAN_LLAMA ? (uint64_t)L * B * Hq * 4 : 4);
     p.ws.queue = take(p.words.size() * 4);
     p.ws.optab = take((uint64_t)p.num_ops * N_SLOTS * 8);
     p.ws.seq0 = take((uint64_t)B * 4);
@@ -34,7 +34,8 @@ void layout_workspace(Plan &p) {
         p.ws.hres = take((uint64_t)B * H * 4);
         p.ws.hmid = take((uint64_t)B * H * 4);
         p.ws.qkv = take((uint64_t)B * Hkv * (G + 2) * D * 4);
-        p.ws.part = take((uint64_t)B * Hq * p.nsplit_max * (D + 2) * 4);
+        // attention partials: per query head, split and token part (8 / G parts)
+        p.ws.part = take((uint64_t)B * Hq * p.nsplit_max * (CONSUMER_WARPS / G) * (D + 2) * 4);
         p.ws.attn_out = take((uint64_t)B * Hq * D * 4);
         p.ws.act = take((uint64_t)B * F * 4);
     } else {

@@ -659,222 +659,213 @@ DEV bool gemv_rpw(const KParams &P, const Smem S, const Dec &d, int i, bool hand
     return true;
 }
 
-// Split-KV attention of one (sequence, kv group, split): scores from the
-// cached K rows in the page ring plus the new token, softmax partial in log2
-// units (max, sum), P.V, partial written out; the last split of the
-// (sequence, group) to arrive merges every split (log-sum-exp combine).
+// Split-KV attention of one (sequence, kv group, split).  Each of the 8
+// consumer warps is an independent piece of the split: query head w / parts
+// of the group over token part w % parts of the split's tokens (parts = 8 /
+// group size).  A warp computes its scores (4 lanes per token, log2 units),
+// the softmax statistics (max, sum of 2^(s - max)) and P.V for its head,
+// writes that partial, and arrives on its head's counter; the warp that
+// arrives last for a head merges all of the head's partials (log-sum-exp
+// combine).  No barrier inside the task.
 template <int D>
 DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
-                   uint32_t &cph, bool &ab) {
+                   bool &ab) {
     constexpr int PER = D / 32;
     constexpr int QS = D / 4 + 4;
     constexpr int DQ = D / 4;
     const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
-    const int G = P.Hq / P.Hkv, b = F(I, P_B), g = F(I, P_G);
+    const int G = P.Hq / P.Hkv, parts = CONSUMER_WARPS / G;
+    const int hh = warp / parts, part = warp % parts;  // head within the kv group, token part
+    const int b = F(I, P_B), g = F(I, P_G);
     const int split = F(I, P_SPLIT), nsplit = F(I, P_NSPLIT), layer = F(I, P_LAYER);
     const int pos = attn_pos(P, I);
     const int t0 = F(I, P_T0), T = F(I, P_T);
     const int ncache = attn_cached_rows(I, pos);
     const bool has_new = pos >= t0 && pos < t0 + T;
     const int ntot = ncache + (has_new ? 1 : 0);
+    const int tp = (T + parts - 1) / parts;
+    const int tb = part * tp, te = min(ntot, tb + tp);  // this warp's tokens [tb, te) of the split
     const float *qp = slot, *kn = slot + G * 4 * QS, *vn = kn + D;
-    float *sc = S.aux();                        // [G][T] scores, then probabilities
-    float *ow = sc + G * T;                   // [warp][G][D]
-    float *ml = ow + CONSUMER_WARPS * G * D;  // [G] max, [G] sum
+    float *sw = S.aux() + warp * tp;  // this warp's scores, then probabilities
+    float *part_base = reinterpret_cast<float *>(PTR(I, S_AT_PART));
+    float *out = reinterpret_cast<float *>(PTR(I, S_AT_OUT));
+    uint32_t *arrive = reinterpret_cast<uint32_t *>(PTR(I, S_AT_ARRIVE));
     const int rpp = P.page_bytes / (D * 2);
-    const int npg = (ncache + rpp - 1) / rpp;
+    const int npg = attn_pages(T, D, P.page_bytes);  // K pages, then as many V pages
     const uint32_t kring = ring, vring = ring + npg;
-    for (int k = 0; k < npg; ++k) {
-        const uint32_t p = (kring + k) % P.num_pages;
-        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[p], ((kring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
-    }
-    // scores: a warp takes 8 tokens at a time, 4 lanes per token, D/4 dims per lane
+    ring = vring + npg;
+    // the split's K (V) rows are consecutive rows of its K (V) page(s); the
+    // planner keeps a split within one page when it fits, else rows are
+    // looked up page by page
+    const uint8_t *kpage = S.pages() + (size_t)(kring % P.num_pages) * P.page_bytes;
+    const uint8_t *vpage = S.pages() + (size_t)(vring % P.num_pages) * P.page_bytes;
+    auto row_at = [&](uint32_t base, const uint8_t *first, int tk) -> const uint8_t * {
+        if (npg == 1) return first + (size_t)tk * (D * 2);
+        return S.pages() + (size_t)((base + tk / rpp) % P.num_pages) * P.page_bytes + (size_t)(tk % rpp) * (D * 2);
+    };
+    for (int k = 0; k < npg; ++k)
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(kring + k) % P.num_pages], ((kring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
+    // scores: 8 tokens per round, 4 lanes per token, DQ dims per lane
     const int qtr = lane & 3;
-    for (int tb = warp * 8; tb < ntot; tb += CONSUMER_WARPS * 8) {
-        const int tk = tb + (lane >> 2);
-        float s[8];
+    float q[DQ];
 #pragma unroll
-        for (int h = 0; h < 8; ++h) s[h] = 0.f;
-        if (tk < ntot) {
-            const uint8_t *row = nullptr;
-            if (tk < ncache)
-                row = S.pages() + (size_t)((kring + tk / rpp) % P.num_pages) * P.page_bytes + (size_t)(tk % rpp) * D * 2;
+    for (int d = 0; d < DQ; d += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(qp + (hh * 4 + qtr) * QS + d);
+        q[d] = v.x; q[d + 1] = v.y; q[d + 2] = v.z; q[d + 3] = v.w;
+    }
+    const int tc = min(te, ncache);  // cached tokens of this warp: [tb, tc); the new token, if ours, is ncache
+    float m = -INFINITY;
+    for (int t = tb; t < te; t += 8) {
+        const int tk = t + (lane >> 2);
+        float s0 = 0.f, s1 = 0.f;
+        if (tk < tc) {
+            const uint8_t *row = row_at(kring, kpage, tk) + qtr * DQ * 2;
+            uint4 kw[DQ / 8];
 #pragma unroll
-            for (int dd = 0; dd < DQ; dd += 8) {
+            for (int d = 0; d < DQ / 8; ++d) kw[d] = *reinterpret_cast<const uint4 *>(row + d * 16);
+#pragma unroll
+            for (int d = 0; d < DQ / 8; ++d) {
                 float k8[8];
-                if (row) {
-                    bf16x8(*reinterpret_cast<const uint4 *>(row + (qtr * DQ + dd) * 2), k8);
-                } else {
-                    const float4 a = *reinterpret_cast<const float4 *>(kn + qtr * DQ + dd);
-                    const float4 c = *reinterpret_cast<const float4 *>(kn + qtr * DQ + dd + 4);
-                    k8[0] = a.x; k8[1] = a.y; k8[2] = a.z; k8[3] = a.w; k8[4] = c.x; k8[5] = c.y; k8[6] = c.z; k8[7] = c.w;
-                }
+                bf16x8(kw[d], k8);
 #pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    if (h < G) {
-                        const float4 qa = *reinterpret_cast<const float4 *>(qp + (h * 4 + qtr) * QS + dd);
-                        const float4 qb = *reinterpret_cast<const float4 *>(qp + (h * 4 + qtr) * QS + dd + 4);
-                        s[h] = fmaf(qa.x, k8[0], s[h]); s[h] = fmaf(qa.y, k8[1], s[h]);
-                        s[h] = fmaf(qa.z, k8[2], s[h]); s[h] = fmaf(qa.w, k8[3], s[h]);
-                        s[h] = fmaf(qb.x, k8[4], s[h]); s[h] = fmaf(qb.y, k8[5], s[h]);
-                        s[h] = fmaf(qb.z, k8[6], s[h]); s[h] = fmaf(qb.w, k8[7], s[h]);
-                    }
+                for (int e = 0; e < 8; e += 2) {
+                    s0 = fmaf(q[d * 8 + e], k8[e], s0);
+                    s1 = fmaf(q[d * 8 + e + 1], k8[e + 1], s1);
                 }
             }
-        }
+        } else if (tk < te) {
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
-            s[h] += __shfl_xor_sync(FULL, s[h], 1);
-            s[h] += __shfl_xor_sync(FULL, s[h], 2);
+            for (int d = 0; d < DQ; ++d) s0 = fmaf(q[d], kn[qtr * DQ + d], s0);
         }
-        if (qtr == 0 && tk < ntot) {
-#pragma unroll
-            for (int h = 0; h < 8; ++h)
-                if (h < G) sc[h * T + tk] = s[h];
+        float s = s0 + s1;
+        s += __shfl_xor_sync(FULL, s, 1);
+        s += __shfl_xor_sync(FULL, s, 2);
+        if (tk < te) {
+            if (qtr == 0) sw[tk - tb] = s;
+            m = fmaxf(m, s);
         }
     }
+    m = warp_max(m);
     __syncwarp();
     if (lane == 0)
         for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(kring + k) % P.num_pages]);
-    consumer_sync(P, S, cph, ab, i);
-    // softmax statistics, one warp per head
-    if (warp < G) {
-        float m = -INFINITY;
-        for (int tk = lane; tk < ntot; tk += 32) m = fmaxf(m, sc[warp * T + tk]);
-        m = warp_max(m);
-        float l = 0.f;
-        for (int tk = lane; tk < ntot; tk += 32) {
-            const float e = exp2f(sc[warp * T + tk] - m);
-            sc[warp * T + tk] = e;
-            l += e;
+    float l = 0.f;
+    for (int t = tb + lane; t < te; t += 32) {
+        const float e = exp2f(sw[t - tb] - m);
+        sw[t - tb] = e;
+        l += e;
+    }
+    l = warp_sum(l);
+    __syncwarp();
+    // P.V: lane owns dims lane * PER .. + PER; four accumulator sets so that
+    // consecutive tokens' loads and multiply-adds overlap
+    for (int k = 0; k < npg; ++k)
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(vring + k) % P.num_pages], ((vring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
+    float acc[4][PER];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[u][e] = 0.f;
+    auto pv = [&](float (&a)[PER], float p, const uint8_t *row) {
+        if constexpr (PER == 2) {
+            const uint32_t u = *reinterpret_cast<const uint32_t *>(row);
+            a[0] = fmaf(p, __uint_as_float(u << 16), a[0]);
+            a[1] = fmaf(p, __uint_as_float(u & 0xffff0000u), a[1]);
+        } else {
+            const uint2 u = *reinterpret_cast<const uint2 *>(row);
+            a[0] = fmaf(p, __uint_as_float(u.x << 16), a[0]);
+            a[1] = fmaf(p, __uint_as_float(u.x & 0xffff0000u), a[1]);
+            a[2] = fmaf(p, __uint_as_float(u.y << 16), a[2]);
+            a[3] = fmaf(p, __uint_as_float(u.y & 0xffff0000u), a[3]);
         }
-        l = warp_sum(l);
-        if (lane == 0) {
-            ml[warp] = m;
-            ml[G + warp] = l;
+    };
+    int t = tb;
+    if (npg == 1) {
+        const uint8_t *vl = vpage + lane * PER * 2;
+        for (; t + 4 <= tc; t += 4) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pv(acc[u], sw[t + u - tb], vl + (size_t)(t + u) * (D * 2));
         }
     }
-    for (int k = 0; k < npg; ++k) {
-        const uint32_t p = (vring + k) % P.num_pages;
-        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[p], ((vring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
+    for (; t < tc; ++t) pv(acc[0], sw[t - tb], row_at(vring, vpage, t) + lane * PER * 2);
+    if (has_new && ncache >= tb && ncache < te) {  // the new token is this warp's
+        const float p = sw[ncache - tb];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[1][e] = fmaf(p, vn[lane * PER + e], acc[1][e]);
     }
-    ring = vring + npg;
-    consumer_sync(P, S, cph, ab, i);
-    // P.V: warp w takes tokens w, w+8, ...; lane holds D/32 consecutive dims
-    {
-        float acc[8][PER];
 #pragma unroll
-        for (int h = 0; h < 8; ++h)
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc[h][e] = 0.f;
-        for (int tk = warp; tk < ntot; tk += CONSUMER_WARPS) {
-            float v[PER];
-            if (tk < ncache) {
-                const uint8_t *row =
-                    S.pages() + (size_t)((vring + tk / rpp) % P.num_pages) * P.page_bytes + (size_t)(tk % rpp) * D * 2;
-                if constexpr (PER == 2) {
-                    const uint32_t u = *reinterpret_cast<const uint32_t *>(row + lane * 4);
-                    v[0] = __uint_as_float(u << 16);
-                    v[1] = __uint_as_float(u & 0xffff0000u);
-                } else {
-                    const uint2 u = *reinterpret_cast<const uint2 *>(row + lane * 8);
-                    v[0] = __uint_as_float(u.x << 16);
-                    v[1] = __uint_as_float(u.x & 0xffff0000u);
-                    v[2] = __uint_as_float(u.y << 16);
-                    v[3] = __uint_as_float(u.y & 0xffff0000u);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < PER; ++e) v[e] = vn[lane * PER + e];
-            }
-#pragma unroll
-            for (int h = 0; h < 8; ++h)
-                if (h < G) {
-                    const float pr = sc[h * T + tk];
-#pragma unroll
-                    for (int e = 0; e < PER; ++e) acc[h][e] = fmaf(pr, v[e], acc[h][e]);
-                }
-        }
-#pragma unroll
-        for (int h = 0; h < 8; ++h)
-            if (h < G)
-#pragma unroll
-                for (int e = 0; e < PER; ++e) ow[(warp * G + h) * D + lane * PER + e] = acc[h][e];
-    }
+    for (int e = 0; e < PER; ++e) acc[0][e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
     __syncwarp();
     if (lane == 0) {
         for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(vring + k) % P.num_pages]);
-        mbar_arrive(&S.act_empty()[sl]);
+        mbar_arrive(&S.act_empty()[sl]);  // q, k, v of the slot no longer needed by this warp
     }
-    consumer_sync(P, S, cph, ab, i);
-    float *part = reinterpret_cast<float *>(PTR(I, S_AT_PART));
-    auto part_at = [&](int h, int s) {
-        return part + (((size_t)b * P.Hq + g * G + h) * P.nsplit_max + s) * (D + 2);
-    };
-    for (int k = ct; k < G * D && !ab; k += CONSUMERS) {
-        const int h = k / D, d = k % D;
-        float o = 0.f;
+    // this warp's partial: (o[D], max, sum) of head (b, g * G + hh), piece split * parts + part
+    const int head = g * G + hh, npieces = P.nsplit_max * parts;
+    float *pp = part_base + ((size_t)(b * P.Hq + head) * npieces + split * parts + part) * (D + 2);
+    if (!ab) {
 #pragma unroll
-        for (int w = 0; w < CONSUMER_WARPS; ++w) o += ow[(w * G + h) * D + d];
-        part_at(h, split)[d] = o;
-    }
-    if (ct < G && !ab) {
-        part_at(ct, split)[D] = ml[ct];
-        part_at(ct, split)[D + 1] = ml[G + ct];
-    }
-    // the acq_rel add below is cumulative over every partial this CTA wrote
-    // before the barrier, and acquires the other splits' partials
-    consumer_sync(P, S, cph, ab, i);
-    uint32_t *arrive = reinterpret_cast<uint32_t *>(PTR(I, S_AT_ARRIVE)) + ((size_t)layer * P.B + b) * P.Hkv + g;
-    if (ct == 0) {
-        int last = 0;
-        if (!ab) {
-            const uint32_t old = atom_acqrel_add(arrive, 1u);
-            last = old == (uint32_t)(P.step + 1) * (uint32_t)nsplit - 1u;
+        for (int e = 0; e < PER; ++e) pp[lane * PER + e] = acc[0][e];
+        if (lane == 0) {
+            pp[D] = m;
+            pp[D + 1] = l;
         }
-        S.ctrl()[3] = last;
     }
-    consumer_sync(P, S, cph, ab, i);
-    if (S.ctrl()[3] && !ab) {
-        float *out = reinterpret_cast<float *>(PTR(I, S_AT_OUT));
-        // log-sum-exp combine; partials are loaded 8 splits at a time so their
-        // L2 round trips overlap instead of queueing one behind another
-        for (int k = ct; k < G * D; k += CONSUMERS) {
-            const int h = k / D, d = k % D;
-            float M = -INFINITY, L = 0.f, o = 0.f;
-            for (int s0 = 0; s0 < nsplit; s0 += 8) {
-                float mv[8], lv[8], ov[8];
+    // the acq_rel add is cumulative over this warp's partial (ordered by the
+    // warp barrier) and acquires the other pieces' partials
+    __syncwarp();
+    int last = 0;
+    if (lane == 0 && !ab) {
+        const uint32_t old = atom_acqrel_add(arrive + ((size_t)layer * P.B + b) * P.Hq + head, 1u);
+        last = old == (uint32_t)(P.step + 1) * (uint32_t)(nsplit * parts) - 1u;
+    }
+    if (!__shfl_sync(FULL, last, 0)) return;
+    __syncwarp();
+    // merge: log-sum-exp over the head's pieces, MB at a time so that their
+    // L2 round trips overlap
+    const float *hb = part_base + (size_t)(b * P.Hq + head) * npieces * (D + 2);
+    const int n = nsplit * parts;
+    float M = -INFINITY, L = 0.f, o[PER];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int s = s0 + u;
-                    if (s < nsplit) {
-                        const float *ps = part_at(h, s);
-                        mv[u] = __ldcg(ps + D);
-                        lv[u] = __ldcg(ps + D + 1);
-                        ov[u] = __ldcg(ps + d);
-                    } else {
-                        mv[u] = -INFINITY;
-                        lv[u] = 0.f;
-                        ov[u] = 0.f;
-                    }
-                }
-                float Mn = M;
+    for (int e = 0; e < PER; ++e) o[e] = 0.f;
+    constexpr int MB = PER <= 2 ? 16 : 8;
+    for (int s0 = 0; s0 < n; s0 += MB) {
+        float mv[MB], lv[MB], ov[MB][PER];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) Mn = fmaxf(Mn, mv[u]);
-                const float r = exp2f(M - Mn);  // rescale what was accumulated so far
-                L *= r;
-                o *= r;
+        for (int u = 0; u < MB; ++u) {
+            const int sp = s0 + u;
+            if (sp < n) {
+                const float *ps = hb + (size_t)sp * (D + 2);
+                mv[u] = __ldcg(ps + D);
+                lv[u] = __ldcg(ps + D + 1);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float f = exp2f(mv[u] - Mn);
-                    L += f * lv[u];
-                    o += f * ov[u];
-                }
-                M = Mn;
+                for (int e = 0; e < PER; ++e) ov[u][e] = __ldcg(ps + lane * PER + e);
+            } else {
+                mv[u] = -INFINITY;
+                lv[u] = 0.f;
+#pragma unroll
+                for (int e = 0; e < PER; ++e) ov[u][e] = 0.f;
             }
-            out[(size_t)b * P.Hq * D + (size_t)(g * G + h) * D + d] = o / L;
         }
+        float Mn = M;
+#pragma unroll
+        for (int u = 0; u < MB; ++u) Mn = fmaxf(Mn, mv[u]);
+        if (Mn == -INFINITY) continue;  // nothing yet
+        const float r = exp2f(M - Mn);  // rescale what was accumulated so far
+        L *= r;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) o[e] *= r;
+#pragma unroll
+        for (int u = 0; u < MB; ++u) {
+            const float f = exp2f(mv[u] - Mn);  // 0 for empty pieces
+            L += f * lv[u];
+#pragma unroll
+            for (int e = 0; e < PER; ++e) o[e] += f * ov[u][e];
+        }
+        M = Mn;
     }
+#pragma unroll
+    for (int e = 0; e < PER; ++e) out[((size_t)b * P.Hq + head) * D + lane * PER + e] = o[e] / L;
 }
 
 DEV void embed_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, bool ab) {

@@ -69,11 +69,12 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
         };
         const bool packed = opc != MK_OP_ATTN;
         const int n0 = nseg > 0 ? s0.rows : 0, n1 = nseg > 1 ? s1.rows : 0;
-        // pages: packed -> over the concatenated rows; else per segment
+        // pages: packed -> over the concatenated rows; attention -> a fixed
+        // number per segment (sized for the split's T rows, filled with the
+        // rows cached so far)
         const int total = packed ? n0 + n1 : 0;
-        const int npages = packed ? (total + rpp - 1) / (rpp > 0 ? rpp : 1)
-                                  : (n0 + rpp - 1) / (rpp > 0 ? rpp : 1) + (n1 + rpp - 1) / (rpp > 0 ? rpp : 1);
-        const int npg0 = packed ? 0 : (n0 + rpp - 1) / (rpp > 0 ? rpp : 1);
+        const int npg0 = packed ? 0 : attn_pages(F(I, P_T), P.D, PS);
+        const int npages = packed ? (total + rpp - 1) / (rpp > 0 ? rpp : 1) : 2 * npg0;
         bool stop = false;
         for (int k = 0; k < npages; ++k) {
             if (!warp_wait_bar(P, S, &S.empty()[rp], rph ^ 1, 0, i, opc)) {
@@ -92,9 +93,9 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
                 } else {
                     const bool second = k >= npg0;
                     const Seg &sg = second ? s1 : s0;
-                    const int r = (second ? k - npg0 : k) * rpp, nr = min(rpp, sg.rows - r);
-                    mbar_expect_tx(bar, (uint32_t)nr * row_bytes);
-                    copy_rows(sg, r, nr, dst, bar);
+                    const int r = (second ? k - npg0 : k) * rpp, nr = max(0, min(rpp, sg.rows - r));
+                    mbar_expect_tx(bar, (uint32_t)nr * row_bytes);  // an empty page just completes
+                    if (nr > 0) copy_rows(sg, r, nr, dst, bar);
                 }
             }
             __syncwarp();
@@ -328,8 +329,8 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 13] = gtimer();
         const float *slot = reinterpret_cast<const float *>(S.act(sl));
         if (opc == MK_OP_ATTN) {
-            if (P.D == 64) attn_task<64>(P, S, I, i, sl, slot, ring, cph, ab);
-            else attn_task<128>(P, S, I, i, sl, slot, ring, cph, ab);
+            if (P.D == 64) attn_task<64>(P, S, I, i, sl, slot, ring, ab);
+            else attn_task<128>(P, S, I, i, sl, slot, ring, ab);
             rq.set(ring, P.num_pages);
         } else if (opc == MK_OP_EMBED) {
             consumer_sync(P, S, cph, ab, i);

@@ -96,6 +96,18 @@ constexpr int RESID_ROWS = 16;           // residual slice staged per slot for O
 constexpr int MAX_TILE_ROWS = 16;
 constexpr int NRED = 4;                  // cross-warp reduction buffers, used round robin by GEMV tiles
 
+#ifdef __CUDACC__
+#define MK_HD __host__ __device__
+#else
+#define MK_HD
+#endif
+// Pages of the ring an attention instruction takes: ceil(T / rows per page)
+// pages of K rows, then as many of V rows, however many rows are cached yet
+// (the others stay empty), so that the count is fixed by the plan.
+MK_HD inline int attn_pages(int T, int D, int page_bytes) {
+    return (T + page_bytes / (2 * D) - 1) / (page_bytes / (2 * D));
+}
+
 }  // namespace mk
 
 namespace mk {
@@ -103,7 +115,8 @@ namespace mk {
 // two activation slots, the page pool, an op scratch area, mbarriers, flags.
 inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
 inline int red_bytes(int B) { return CONSUMER_WARPS * MAX_TILE_ROWS * B * 4; }
-inline int attn_aux_bytes(int G, int T, int D) { return (G * T + CONSUMER_WARPS * G * D + 8 * G) * 4; }
+// attention scratch: each consumer warp's scores over its part of a split
+inline int attn_aux_bytes(int G, int T, int D) { return (CONSUMER_WARPS * ((T + CONSUMER_WARPS / G - 1) / (CONSUMER_WARPS / G)) + 32 + 0 * D) * 4; }
 constexpr int MBAR_BYTES = 512;    // up to 64 mbarriers
 constexpr int CTRL_BYTES = 128;   // 32 flag words
 constexpr int MAX_PAGES = 26;      // 2 * MAX_PAGES + 9 mbarriers must fit MBAR_BYTES

@@ -523,7 +523,7 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     const int G = Hq / Hkv;
     if (B > 8) return set_error(MK_ERR_UNSUPPORTED, "batch above 8");
     if (D != 64 && D != 128) return set_error(MK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
-    if (G > 8) return set_error(MK_ERR_UNSUPPORTED, "more than 8 q heads per kv head");
+    if (G > 8 || 8 % G) return set_error(MK_ERR_UNSUPPORTED, "q heads per kv head must be 1, 2, 4 or 8");
     if (H % 8 || F % 8) return set_error(MK_ERR_UNSUPPORTED, "hidden and ffn must be multiples of 8");
     p.B = B;
     p.max_steps = s->max_steps;
