@@ -434,7 +434,13 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
     if (opc >= MK_OP_QKV && opc != MK_OP_ATTN) {
         const int nrows = F(I, P_NROWS), kc = F(I, P_KC);
         const int rmax = P.B > 4 ? 8 : MAX_TILE_ROWS;
-        if (nrows <= 0 || (opc == MK_OP_UP ? 2 * nrows : nrows) > rmax) return false;
+        const int total = opc == MK_OP_UP ? 2 * nrows : nrows;
+        // more rows only as 2 or 4 pages of 16 rows on the batch-1 row-per-warp path
+        const bool pages16 = P.B == 1 && kc % 256 == 0 && kc <= 2048 && P.page_bytes == 32 * kc;
+        if (nrows <= 0) return false;
+        if (total > rmax && !(pages16 && opc != MK_OP_O && (total == 32 || total == 64) &&
+                              (opc != MK_OP_UP || nrows % 8 == 0)))
+            return false;
         if (kc <= 0 || kc % 8 || 2 * kc > P.page_bytes || kc * P.B * 4 > P.abuf_bytes) return false;
         const int rpp = F(I, P_RPP);
         const int rows = (opc == MK_OP_UP ? 2 : 1) * nrows;

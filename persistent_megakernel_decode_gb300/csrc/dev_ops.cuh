@@ -523,14 +523,21 @@ DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, int sl,
 }
 
 // ---------------------------------------------------------------- batch 1, rows per warp
-// Batch-1 GEMV tiles whose rows fit one page and whose K is a multiple of 256
-// up to 2048 take the row-per-warp path: warp w computes rows w and w + 8 of
-// the tile over the whole K, holding x (its lane's 8-wide chunks l, l + 32,
-// ...) in registers across tiles -- no cross-warp reduction and no barrier.
+// Batch-1 GEMV tiles with K a multiple of 256 up to 2048 take the
+// row-per-warp path: a tile is NPG pages of 16 rows (or one page of at most
+// 16), warp w computes rows w, w + 8, w + 16, ... (rows w and w + 8 of every
+// page) over the whole K, holding x (its lane's 8-wide chunks l, l + 32, ...)
+// in registers across tiles -- no cross-warp reduction and no barrier.
+// MLP-up tiles hold gate rows then up rows; with a multiple of 8 gate rows a
+// gate row and its up row fall to the same warp.
+constexpr int RPW_MAX_PAGES = 4;
 DEV bool rpw_tile(const KParams &P, const Dec &d) {
     if (P.B != 1 || d.opc < MK_OP_QKV || d.opc == MK_OP_ATTN) return false;
-    if (d.kc % 256 || d.kc > 2048 || d.npg != 1) return false;
-    return d.opc == MK_OP_UP ? d.nrows == 8 : d.nrows <= 16;
+    if (d.kc % 256 || d.kc > 2048) return false;
+    const bool up = d.opc == MK_OP_UP;
+    if (d.npg == 1) return up ? d.nrows == 8 : d.nrows <= 16;
+    return (d.npg == 2 || d.npg == RPW_MAX_PAGES) && d.opc != MK_OP_O && P.page_bytes == 32 * d.kc &&
+           (!up || d.nrows % 8 == 0);
 }
 
 // The activation hand-off (activation loader stages, consumers wait) is due
@@ -574,18 +581,20 @@ DEV void rpw_row(const uint8_t *wrow, int lane, const XRow &x, uint64_t &acc) {
     }
 }
 
-// KG = K / 256 chunks per lane.  `handoff`: this slot took the activation
-// hand-off (the caller waited for activation slot sl); x is reloaded from the
-// slot's buffer when its input changed.  Returns true (the warp wrote global
-// memory).
-template <int KG>
+// KG = K / 256 chunks per lane, NPG = pages of the tile.  `handoff`: this
+// slot took the activation hand-off (the caller waited for activation slot
+// sl); x is reloaded from the slot's buffer when its input changed.  Returns
+// true (the warp wrote global memory).
+template <int KG, int NPG>
 DEV bool gemv_rpw(const KParams &P, const Smem S, const Dec &d, int i, bool handoff, int sl, const float *slot,
                   XRow &x, uint32_t &ring, RingPos &rq, unsigned long long &lm_best, bool &ab) {
+    constexpr int V = 2 * NPG;  // rows of this warp: w + 8 v
     const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
     const int opc = d.opc, nrows = d.nrows, row_bytes = d.kc * 2, out0 = d.out0;
     const uint64_t ptr_a = d.out, ptr_b = d.out2;
-    const int r0 = warp, r1 = warp + 8;  // this warp's rows (MLP-up: gate row w, up row w)
-    float res0 = 0.f, res1 = 0.f;
+    float res[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) res[v] = 0.f;
     if (handoff) {
         const long long key = ((long long)d.row << 32) | (uint32_t)d.k0;
         if (key != x.key) {
@@ -599,59 +608,68 @@ DEV bool gemv_rpw(const KParams &P, const Smem S, const Dec &d, int i, bool hand
             }
             x.key = key;
         }
-        if (opc == MK_OP_O) {
+        if (opc == MK_OP_O) {  // O tiles have at most RESID_ROWS rows
             const float *rs = slot_resid(P, const_cast<float *>(slot));
-            res0 = rs[r0];
-            res1 = rs[r1];
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                if (warp + 8 * v < RESID_ROWS) res[v] = rs[warp + 8 * v];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // x and the residual rows are in registers
     }
-    // this warp's two rows of the tile's page (rows past the tile's end hold
-    // stale page bytes; their results are not stored)
-    if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
-    const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
-    uint64_t acc0 = 0, acc1 = 0;
-    rpw_row<KG>(page + (size_t)r0 * row_bytes, lane, x, acc0);
-    rpw_row<KG>(page + (size_t)r1 * row_bytes, lane, x, acc1);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
-    rq.next(P.num_pages);
-    ++ring;
-    // lanes 0-15 end with row r0's sum, lanes 16-31 with row r1's
-    float v[2] = {sum2(acc0), sum2(acc1)};
-    Bfly<2, 16>::run(v, lane);
-    const float y1 = __shfl_sync(FULL, v[0], 16);
-    if (lane != 0 || ab) return true;
-    const float y0 = v[0];
+    // rows w and w + 8 of every page of the tile (rows past the tile's end
+    // hold stale page bytes; their results are not stored)
+    uint64_t acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = 0;
+#pragma unroll
+    for (int pg = 0; pg < NPG; ++pg) {
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
+        const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
+        rpw_row<KG>(page + (size_t)warp * row_bytes, lane, x, acc[2 * pg]);
+        rpw_row<KG>(page + (size_t)(warp + 8) * row_bytes, lane, x, acc[2 * pg + 1]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
+        rq.next(P.num_pages);
+    }
+    ring += NPG;
+    // after the butterfly, lanes L with L % (32 / V) == 0 hold row w + 8 (L / (32 / V))
+    float y[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) y[v] = sum2(acc[v]);
+    Bfly<V, 16>::run(y, lane);
+    constexpr int LPV = 32 / V;
+    const int v = lane / LPV, r = warp + 8 * v;
+    const bool holder = (lane % LPV) == 0;
+    float val = y[0];
     if (opc == MK_OP_UP) {
-        if (r0 < nrows) reinterpret_cast<float *>(ptr_a)[out0 + r0] = y0 / (1.0f + __expf(-y0)) * y1;
+        // the up row of gate row r is r + nrows: value index v + nrows / 8
+        const float u = __shfl_sync(FULL, val, min(31, (v + nrows / 8) * LPV));
+        if (holder && !ab && r < nrows) reinterpret_cast<float *>(ptr_a)[out0 + r] = val / (1.0f + __expf(-val)) * u;
         return true;
     }
-    const float yr[2] = {y0, y1};
-    const float rr[2] = {res0, res1};
-    float best = -INFINITY;
-    int bi = -1;
+    float resid = 0.f;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int r = j ? r1 : r0;
-        if (r >= nrows) continue;
-        const float y = yr[j];
-        if (opc == MK_OP_QKV) {
-            reinterpret_cast<float *>(ptr_a)[out0 + r] = y;
-        } else if (opc == MK_OP_O) {
-            reinterpret_cast<float *>(ptr_a)[out0 + r] = rr[j] + y;
-            reinterpret_cast<float *>(ptr_b)[out0 + r] = rr[j] + y;
-        } else if (opc == MK_OP_DOWN) {
-            atomicAdd(reinterpret_cast<float *>(ptr_a) + out0 + r, y);
-        } else if (opc == MK_OP_LM) {
-            reinterpret_cast<float *>(ptr_a)[out0 + r] = y;
-            if (y > best) { best = y; bi = r; }  // r0 < r1: ties keep the lower index
+    for (int k = 0; k < V; ++k)
+        if (k == v) resid = res[k];
+    const bool mine = holder && !ab && r < nrows;
+    if (opc == MK_OP_QKV) {
+        if (mine) reinterpret_cast<float *>(ptr_a)[out0 + r] = val;
+    } else if (opc == MK_OP_O) {
+        if (mine) {
+            reinterpret_cast<float *>(ptr_a)[out0 + r] = resid + val;
+            reinterpret_cast<float *>(ptr_b)[out0 + r] = resid + val;
         }
-    }
-    if (opc == MK_OP_LM && bi >= 0) {
-        const unsigned long long key = argmax_key(best, out0 + bi);
-        if (key > lm_best) {  // this warp's best key of the step so far
+    } else if (opc == MK_OP_DOWN) {
+        if (mine) atomicAdd(reinterpret_cast<float *>(ptr_a) + out0 + r, val);
+    } else if (opc == MK_OP_LM) {
+        if (mine) reinterpret_cast<float *>(ptr_a)[out0 + r] = val;
+        // this warp's best row of the tile (lowest index on ties), then the
+        // step's running best per warp
+        unsigned long long key = mine ? argmax_key(val, out0 + r) : 0ull;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) key = max(key, __shfl_xor_sync(FULL, key, o));
+        if (lane == 0 && key > lm_best && !ab) {
             lm_best = key;
             red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)P.step, key);
         }

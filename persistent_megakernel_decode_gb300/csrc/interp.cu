@@ -269,6 +269,15 @@ DEV void handoff_progress(const Smem S, int i, bool wrote_global) {
     }
 }
 
+// Row-per-warp variants by pages per tile.
+template <int KG>
+DEV void gemv_rpw_pages(const KParams &P, const Smem S, const Dec &d, int i, bool handoff, int sl, const float *slot,
+                        XRow &x, uint32_t &ring, RingPos &rq, unsigned long long &lm_best, bool &ab) {
+    if (d.npg <= 1) gemv_rpw<KG, 1>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+    else if (d.npg <= 2) gemv_rpw<KG, 2>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+    else gemv_rpw<KG, 4>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+}
+
 // GEMV variants: K chunks per consumer thread (NCH) x one page or several.
 // One-page tiles compute RPP rows unconditionally, RPP the power of two at or
 // above the tile's rows, as long as RPP rows fit the page.
@@ -338,10 +347,10 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         } else if (opc >= MK_OP_QKV) {
             if (MAXB == 1 && rpw_tile(P, d)) {  // (a constant condition for larger batches)
                 const int kg = d.kc >> 8;
-                if (kg <= 1) gemv_rpw<1>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
-                else if (kg <= 2) gemv_rpw<2>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
-                else if (kg <= 4) gemv_rpw<4>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
-                else gemv_rpw<8>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+                if (kg <= 1) gemv_rpw_pages<1>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+                else if (kg <= 2) gemv_rpw_pages<2>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+                else if (kg <= 4) gemv_rpw_pages<4>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+                else gemv_rpw_pages<8>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
             } else {
                 wrote = gemv_dispatch<MAXB>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
             }

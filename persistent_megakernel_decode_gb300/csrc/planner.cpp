@@ -555,9 +555,6 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     p.rows_qkv = kn_qkv; p.rows_o = kn_o; p.rows_up = kn_up; p.rows_down = kn_dn; p.kchunk_down = kn_kc;
     p.rows_lm = kn_lm; p.attn_split = kn_T;
     const int rows_group = (G + 2) * D;
-    const int rmax = B > 4 ? 8 : MAX_TILE_ROWS;  // the batch-8 kernel keeps 8 rows x 8 sequences in registers
-    if (kn_qkv > rmax || kn_o > rmax || kn_dn > rmax || kn_lm > rmax || 2 * kn_up > rmax)
-        return set_error(MK_ERR_UNSUPPORTED, "tile rows above 16 (8 for batch > 4; mlp-up: half of that)");
     if (D % kn_qkv) return set_error(MK_ERR_UNSUPPORTED, "rows_qkv must divide head_dim");
     if (F % kn_up || F % kn_kc || kn_kc % 8) return set_error(MK_ERR_UNSUPPORTED, "rows_up / kchunk_down must divide ffn");
     if (kn_T > 256 || kn_T < 1) return set_error(MK_ERR_UNSUPPORTED, "attn_split must be 1..256");
@@ -594,6 +591,25 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     }
     for (int K : {H, Hq * D, kn_kc})
         if (2 * K > p.page_bytes) return set_error(MK_ERR_UNSUPPORTED, "a weight row does not fit one page");
+    // Batch 1 with pages of exactly 16 rows (K = page_bytes / 32, a multiple of
+    // 256 up to 2048): the row-per-warp path takes tiles of 2 or 4 pages.  The
+    // large ops get them (LM head 64 rows, MLP-up 16 + 16, MLP-down 32) to
+    // spread each tile's fixed costs over more bytes; QKV and O keep one page.
+    auto multi_page = [&](int K) { return B == 1 && K % 256 == 0 && K <= 2048 && p.page_bytes == 32 * K; };
+    if (multi_page(H) && tgt->rows_lm <= 0) kn_lm = 64;
+    if (multi_page(H) && tgt->rows_up <= 0 && F % 16 == 0) kn_up = 16;
+    if (multi_page(kn_kc) && tgt->rows_down <= 0) kn_dn = 32;
+    p.rows_up = kn_up; p.rows_down = kn_dn; p.rows_lm = kn_lm;
+    const int rmax = B > 4 ? 8 : MAX_TILE_ROWS;  // the batch-8 kernel keeps 8 rows x 8 sequences in registers
+    auto rows_ok = [&](int rows, int K, bool up, bool o) {
+        if (rows <= rmax) return true;
+        return !o && multi_page(K) && (rows == 32 || rows == 64) && (!up || rows % 16 == 0);
+    };
+    if (!rows_ok(kn_qkv, H, false, false) || !rows_ok(kn_o, Hq * D, false, true) || !rows_ok(kn_dn, kn_kc, false, false) ||
+        !rows_ok(kn_lm, H, false, false) || !rows_ok(2 * kn_up, H, true, false))
+        return set_error(MK_ERR_UNSUPPORTED, "tile rows above 16 (8 for batch > 4; mlp-up: half of that), except "
+                                             "32 or 64 row tiles of 16-row pages at batch 1");
+    if (F % kn_up) return set_error(MK_ERR_UNSUPPORTED, "rows_up must divide ffn");
     if (kn_T * D * 2 > p.page_bytes * 8) return set_error(MK_ERR_UNSUPPORTED, "attention split too long");
     p.num_pages = std::min(MAX_PAGES, (smem_per_cta - fixed) / p.page_bytes);
     p.smem_bytes = fixed + p.num_pages * p.page_bytes;
@@ -603,8 +619,10 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
         int rpp = p.page_bytes / row_bytes;
         return ceil_div(rows, rpp);
     };
-    int need = std::max({pages_for(kn_qkv, 2 * H), pages_for(kn_o, 2 * Hq * D), pages_for(2 * kn_up, 2 * H),
-                         pages_for(kn_dn, 2 * kn_kc), pages_for(kn_lm, 2 * H), 2 * pages_for(kn_T, 2 * D)});
+    // GEMV tiles release each page before waiting for the next, so any number
+    // of pages streams through the ring; an attention task holds all its K
+    // pages, then all its V pages
+    int need = 2 * pages_for(kn_T, 2 * D);
     if (p.num_pages < std::max(2, need))
         return set_error(MK_ERR_UNSUPPORTED, "shared memory too small for the page pool");
 
