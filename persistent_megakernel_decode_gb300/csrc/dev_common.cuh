@@ -38,6 +38,7 @@ DEV void red_relaxed_add(uint32_t *p, uint32_t v) {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+DEV void fence_acq_rel_cta() { asm volatile("fence.acq_rel.cta;" ::: "memory"); }
 DEV void st_relaxed_cta(volatile int *p, int v) {
     asm volatile("st.relaxed.cta.shared.u32 [%0], %1;" ::"r"(saddr((const void *)p)), "r"(v) : "memory");
 }
@@ -294,7 +295,7 @@ DEV bool warp_wait_smem(const KParams &P, const Smem S, volatile int *flag, uint
 
 // Event counter >= target.  Polls are relaxed loads (an acquire load per
 // poll would also drop the SM's L1 each time); once the target is seen, one
-// fence.acq_rel turns the last poll into the acquire.
+// acquire load of the counter synchronises with the publisher's release.
 static __device__ __noinline__ bool wait_counter_slow(uint32_t *err, uint64_t timeout_ns, Smem S, const uint32_t *c,
                                                int ev, uint32_t target, int slot, int opc) {
     const int lane = threadIdx.x & 31;
@@ -321,7 +322,7 @@ DEV bool warp_wait_counter(const KParams &P, const Smem S, int ev, uint32_t targ
     const uint32_t *c = P.counters + ev;
     bool ok = __all_sync(FULL, ld_relaxed(c) >= target);
     if (!ok) ok = wait_counter_slow(P.err, P.timeout_ns, S, c, ev, target, slot, opc);
-    if (ok) fence_acq_rel_gpu();
+    if (ok) (void)ld_acquire(c);  // an acquire read of the value the polls saw (or a later one)
     return ok;
 }
 

@@ -204,9 +204,10 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
 // finished (a CTA-scope release store when it wrote global memory in the
 // slot, else a relaxed one).  Lane 0 of the publisher polls the 8 counters
 // with two vector loads; their minimum says every instruction below it is
-// fully written back.  One GPU-scope fence then covers the whole batch (it is
-// cumulative over what the polls observed) and the batch's signals are added
-// to the event counters -- so consumers never wait for a fence.
+// fully written back.  A CTA-scope fence turns the polls into acquires, and
+// the batch's signals are added to the event counters with release adds
+// (cumulative over what the publisher acquired) -- so consumers never wait
+// for a GPU-scope fence.
 DEV int progress_min(const Smem S) {
     int4 a, b;
     const uint32_t p = saddr((const void *)(S.ctrl() + 8));
@@ -222,6 +223,7 @@ DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
     while (next < P.lmax) {
         if (__shfl_sync(FULL, wc, W_OPC) == MK_OP_NOOP) break;  // NoOps only pad the tail
         int done = next, ab = 0, stop = 0;
+        uint64_t seen_at = 0;
         if (lane == 0) {
             uint64_t t0 = 0;
             for (uint32_t it = 0;; ++it) {
@@ -239,8 +241,11 @@ DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
                     }
                 }
             }
-            // the fence makes the polls acquires and the counter adds below releases
-            if (!stop && !ab) fence_acq_rel_gpu();
+            // the CTA-scope fence makes the polls acquires of the consumers'
+            // releases; the release adds below then carry their writes to GPU
+            // scope (release is cumulative)
+            if (!stop && !ab) fence_acq_rel_cta();
+            seen_at = P.trace ? gtimer() : 0;
         }
         done = __shfl_sync(FULL, done, 0);
         ab = __shfl_sync(FULL, ab, 0);
@@ -250,8 +255,12 @@ DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
             const int e0 = __shfl_sync(FULL, wc, W_SIG), i0 = __shfl_sync(FULL, wc, W_SIG + 1);
             const int e1 = __shfl_sync(FULL, wc, W_SIG + 2), i1 = __shfl_sync(FULL, wc, W_SIG + 3);
             if (lane == 0 && !ab) {
-                if (ns > 0) red_relaxed_add(P.counters + e0, (uint32_t)i0);
-                if (ns > 1) red_relaxed_add(P.counters + e1, (uint32_t)i1);
+                if (ns > 0) red_release_add(P.counters + e0, (uint32_t)i0);
+                if (ns > 1) red_release_add(P.counters + e1, (uint32_t)i1);
+                if (P.trace) {
+                    P.trace[((size_t)blockIdx.x * P.lmax + next) * 16 + 15] = seen_at;   // seen finished
+                    P.trace[((size_t)blockIdx.x * P.lmax + next) * 16 + 14] = gtimer();  // published
+                }
             }
             wc = wn;
             wn = queue_word(P, myq, next + 2);
