@@ -92,7 +92,18 @@ typedef struct {
     /* tile knobs, 0 = default */
     int rows_qkv, rows_o, rows_up, rows_down, kchunk_down, rows_lm, attn_split;
     int page_bytes;        /* shared-memory page size; 0 = 16384 */
+    int schedule;          /* MK_SCHED_*: how tasks are dealt to workers */
 } mk_target_desc;
+
+/* Queue assignment.  Either way tasks go to workers in one topological order,
+ * so every queue is deadlock-free. */
+enum {
+    MK_SCHED_DEFAULT = 0,  /* MK_SCHED_TIMED */
+    MK_SCHED_BYTES = 1,    /* least-loaded worker by bytes streamed so far (longest-first per range) */
+    MK_SCHED_TIMED = 2     /* earliest finish under a time model of one step: a task is ready a hop
+                              after the counters it waits on are met, and holds its worker for a fixed
+                              cost plus its bytes at the worker's share of HBM bandwidth */
+};
 
 typedef struct {
     int num_workers, lmax, num_tasks, num_events, num_ops, num_launches;

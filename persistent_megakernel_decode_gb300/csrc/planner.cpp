@@ -309,6 +309,58 @@ std::vector<std::vector<int>> greedy(const std::vector<int> &order, const std::v
     return q;
 }
 
+// List scheduling against a time model of one step.  A task is ready HOP
+// after every counter it waits on (this epoch) has met its threshold, and it
+// holds a worker for a fixed cost plus its bytes at the worker's share of HBM
+// bandwidth; it goes to the worker on which it finishes first (ties: lowest
+// index).  Tasks are taken in `order`, a topological order, so every queue is
+// a subsequence of it.  The model balances each dependency phase on its own,
+// where the byte greedy balances whole-step totals.
+std::vector<std::vector<int>> timed(const std::vector<int> &order, const std::vector<TaskRec> &tasks, int workers,
+                                    int n_events) {
+    constexpr double HOP_US = 3.0, TILE_US = 1.0, ATTN_US = 4.0, HBM_BYTES_PER_US = 6.8e6;
+    const double bw = HBM_BYTES_PER_US / std::max(1, workers);
+    std::vector<std::vector<std::pair<double, int>>> sig(n_events);  // (finish, increment) of each signal
+    std::vector<std::vector<std::pair<int64_t, double>>> met(n_events);  // cached (threshold, time met)
+    auto time_met = [&](int e, int64_t thr) {
+        for (auto &c : met[e])
+            if (c.first == thr) return c.second;
+        auto v = sig[e];
+        std::sort(v.begin(), v.end());
+        int64_t acc = 0;
+        double t = 0.0;
+        for (auto &f : v) {
+            acc += f.second;
+            t = f.first;
+            if (acc >= thr) break;
+        }
+        met[e].push_back({thr, t});
+        return t;
+    };
+    std::vector<double> free_at(workers, 0.0);
+    std::vector<std::vector<int>> q(workers);
+    for (int id : order) {
+        const TaskRec &t = tasks[id];
+        double ready = 0.0;
+        for (int i = 0; i < t.nw; ++i)
+            if (t.w_off[i] >= 0 && t.w_thr[i] > 0) ready = std::max(ready, time_met(t.w_ev[i], t.w_thr[i]) + HOP_US);
+        const double dur = (t.opcode == MK_OP_ATTN ? ATTN_US : TILE_US) + (double)t.cost / bw;
+        int best = 0;
+        double best_end = 0.0;
+        for (int w = 0; w < workers; ++w) {
+            const double end = std::max(free_at[w], ready) + dur;
+            if (w == 0 || end < best_end) {
+                best = w;
+                best_end = end;
+            }
+        }
+        free_at[best] = best_end;
+        q[best].push_back(id);
+        for (int i = 0; i < t.ns; ++i) sig[t.s_ev[i]].push_back({best_end, t.s_inc[i]});
+    }
+    return q;
+}
+
 }  // namespace
 
 // ---- encode and finish a plan --------------------------------------------
@@ -332,7 +384,7 @@ void encode_task(const TaskRec &t, int task_id, int32_t *w) {
 
 // Build the launch segments (one for the megakernel, one per op otherwise),
 // simulate them and encode the instruction words.
-int finish_queues(Plan &p, bool round_robin) {
+int finish_queues(Plan &p, bool round_robin, bool timed_model) {
     std::vector<Segment> segs;
     std::vector<std::vector<int>> all_q;
     int n = (int)p.tasks.size();
@@ -341,6 +393,8 @@ int finish_queues(Plan &p, bool round_robin) {
         if (round_robin) {
             q.assign(workers, {});
             for (size_t i = 0; i < order.size(); ++i) q[i % workers].push_back(order[i]);
+        } else if (timed_model) {
+            q = timed(order, p.tasks, workers, (int)p.thresholds.size());
         } else {
             q = greedy(order, p.tasks, workers);
         }
@@ -501,7 +555,7 @@ int plan_graph(const mk_graph_desc *g, const mk_target_desc *tgt, int num_worker
     }
     p.op_kind.assign(g->num_ops, MK_OP_COUNTER);
     p.op_layer.assign(g->num_ops, -1);
-    return finish_queues(p, g->round_robin != 0);
+    return finish_queues(p, g->round_robin != 0, false);
 }
 
 // ---- Llama-style decode step --------------------------------------------
@@ -539,6 +593,9 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     auto pow2_floor = [](int v) { int r = 1; while (r * 2 <= v) r *= 2; return r; };
     const int tile = 65536;
     if (tgt->page_bytes < 0 || tgt->page_bytes % 128) return set_error(MK_ERR_INVALID, "page_bytes must be a multiple of 128");
+    if (tgt->schedule < MK_SCHED_DEFAULT || tgt->schedule > MK_SCHED_TIMED)
+        return set_error(MK_ERR_INVALID, "schedule must be one of MK_SCHED_*");
+    p.schedule = tgt->schedule == MK_SCHED_BYTES ? MK_SCHED_BYTES : MK_SCHED_TIMED;
     const int rcap = B > 4 ? 8 : 16;
     int kn_qkv = tgt->rows_qkv > 0 ? tgt->rows_qkv : pow2_floor(clampi(tile / (2 * H), 1, rcap));
     int kn_o = tgt->rows_o > 0 ? tgt->rows_o : pow2_floor(clampi(tile / (2 * Hq * D), 1, rcap));
@@ -791,7 +848,7 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     int64_t kv_write = (int64_t)2 * B * Hkv * D * 2 * L;
     int64_t norms = (int64_t)(2 * L + 1) * H * 2 + (m->qk_norm ? (int64_t)2 * L * D * 2 : 0);
     p.alg_bytes = weights + kv_read + kv_write + norms;
-    return finish_queues(p, false);
+    return finish_queues(p, false, p.schedule == MK_SCHED_TIMED);
 }
 
 }  // namespace mk

@@ -23,6 +23,7 @@ MK_ERR_RESIDENCY, MK_ERR_TIMEOUT, MK_ERR_DEVICE_CHECK, MK_ERR_UNBOUND = 5, 6, 7,
 OP_NAMES = {0: "noop", 1: "counter", 2: "embed", 3: "qkv", 4: "attn", 5: "o", 6: "up", 7: "down", 8: "lm"}
 OPCODE = {v: k for k, v in OP_NAMES.items()}
 MODE_MEGAKERNEL, MODE_PER_OP = 0, 1
+SCHED_DEFAULT, SCHED_BYTES, SCHED_TIMED = 0, 1, 2
 RUN_HOST_TOKENS, RUN_TRACE = 1, 2
 PAIR_WHOLE, PAIR_TILE, PAIR_TILE_COVER, PAIR_TILE_REDUCE = 0, 1, 2, 3
 TASK_FIELDS = 24
@@ -57,7 +58,8 @@ class StepDesc(C.Structure):
 class TargetDesc(C.Structure):
     _fields_ = [("num_sms", C.c_int), ("smem_per_cta", C.c_int), ("mode", C.c_int), ("rows_qkv", C.c_int),
                 ("rows_o", C.c_int), ("rows_up", C.c_int), ("rows_down", C.c_int), ("kchunk_down", C.c_int),
-                ("rows_lm", C.c_int), ("attn_split", C.c_int), ("page_bytes", C.c_int)]
+                ("rows_lm", C.c_int), ("attn_split", C.c_int), ("page_bytes", C.c_int),
+                ("schedule", C.c_int)]
 
 
 class PlanInfo(C.Structure):

@@ -37,7 +37,10 @@ def _oracle_knobs(info):
 
 
 def _compare(shape, B, seq0, steps, workers=152, **kn):
-    p = rt.Plan.llama(shape, B, seq0, steps, max(seq0) + steps + 3, num_sms=workers, smem_per_cta=232448, **kn)
+    # the oracle deals tasks by bytes, the pages' rule (the default time-model
+    # schedule is checked for validity below)
+    p = rt.Plan.llama(shape, B, seq0, steps, max(seq0) + steps + 3, num_sms=workers, smem_per_cta=232448,
+                      schedule=rt.SCHED_BYTES, **kn)
     info = p.info()
     q, ids, th, tasks = p.export()
     osh = plans.LlamaShape(shape.L, shape.H, shape.Hq, shape.Hkv, shape.D, shape.F, shape.V)
@@ -92,6 +95,39 @@ def test_planner_queue_simulates_over_steps():
     sigs = {i: [(r[17 + 2 * k], r[18 + 2 * k]) for k in range(r[16])] for i, r in enumerate(tasks)}
     res = sim.deadlock_check(ids.tolist(), waits, sigs, len(th), steps=5)
     assert res.ok and res.counters == rules.expected_counters(th.tolist(), 5)
+
+
+@pytest.mark.parametrize("shape,B,seq0,workers", [
+    (synth.TINY, 3, [5, 64, 130], 7),
+    (synth.LLAMA_1B, 1, [1024], 152),
+    (synth.LLAMA_1B, 8, [512, 4096, 700, 2300, 1500, 3999, 600, 2048], 152),
+])
+def test_timed_schedule_is_a_valid_deal_of_the_same_tasks(shape, B, seq0, workers):
+    """The time-model schedule deals exactly the byte schedule's tasks, with the
+    same waits and signals, each queue in one topological order, deadlock-free
+    over several steps; for one worker the two coincide."""
+    steps = 3
+    kw = dict(num_sms=workers, smem_per_cta=232448)
+    pt = rt.Plan.llama(shape, B, seq0, steps, max(seq0) + steps + 3, schedule=rt.SCHED_TIMED, **kw)
+    pb = rt.Plan.llama(shape, B, seq0, steps, max(seq0) + steps + 3, schedule=rt.SCHED_BYTES, **kw)
+    qt, idt, tht, tt = pt.export()
+    qb, idb, thb, tb = pb.export()
+    assert (tt == tb).all() and (tht == thb).all()
+    ids = idt.tolist()
+    flat = sorted(t for row in ids for t in row if t >= 0)
+    assert flat == list(range(len(tt)))
+    for row in ids:
+        real = [t for t in row if t >= 0]
+        assert real == sorted(real)                      # task ids are a topological order
+        assert all(t < 0 for t in row[len(real):])       # NoOps only pad the tail
+    waits = {i: [(r[7 + 3 * k], r[8 + 3 * k], r[9 + 3 * k]) for k in range(r[6])] for i, r in enumerate(tt)}
+    sigs = {i: [(r[17 + 2 * k], r[18 + 2 * k]) for k in range(r[16])] for i, r in enumerate(tt)}
+    res = sim.deadlock_check(ids, waits, sigs, len(tht), steps=steps)
+    assert res.ok and res.counters == rules.expected_counters(tht.tolist(), steps)
+    one_t = rt.Plan.llama(shape, B, seq0, 1, max(seq0) + 4, num_sms=1, smem_per_cta=232448, schedule=rt.SCHED_TIMED)
+    one_b = rt.Plan.llama(shape, B, seq0, 1, max(seq0) + 4, num_sms=1, smem_per_cta=232448, schedule=rt.SCHED_BYTES)
+    if shape is synth.TINY:
+        assert one_t.export()[1].tolist() == one_b.export()[1].tolist()
 
 
 def test_graph_plan_fork_join_example():
