@@ -56,7 +56,10 @@ extern "C" {
 #define MK_OP_UP       6   /* RMSNorm + gate/up rows + SiLU(g) * u */
 #define MK_OP_DOWN     7   /* K chunk of Wd rows, added into the residual */
 #define MK_OP_LM       8   /* final RMSNorm + LM-head rows + argmax */
-#define MK_NUM_OPCODES 9
+#define MK_OP_GLM_A0   9   /* GLM block: Add + RMSNorm + per-128 FP8 quantisation of one token row */
+#define MK_OP_GLM_GEMM 10  /* GLM block: rows of an FP8 weight x FP8 activations, block scales, bf16 out (+RoPE) */
+#define MK_OP_GLM_FIN  11  /* GLM block: one token's q-lora re-quantisation, RoPE and cache writes */
+#define MK_NUM_OPCODES 12
 
 /* ---- plan modes ---- */
 #define MK_MODE_MEGAKERNEL 0   /* one persistent launch per step */
@@ -137,7 +140,34 @@ typedef struct {
 #define MK_BIND_LOGITS     17   /* fp32 [B, V]: logits of the last step run */
 #define MK_BIND_ARGMAX     18   /* uint64 [max_steps, B]: packed argmax of each step */
 #define MK_BIND_HIDDEN     19   /* fp32 [L, B, H]: residual after each layer (capture_hidden) */
-#define MK_BIND_COUNT      20
+/* GLM pre-attention block (mk_plan_glm; M = requests * tokens rows, e4m3 = FP8 "fn"
+ * bytes, weight scales fp32 [ceil(N/128), K/128] per 128 x 128 block) */
+#define MK_BIND_GLM_X       20   /* bf16 [M, hidden]: block input */
+#define MK_BIND_GLM_RES     21   /* bf16 [M, hidden]: residual in */
+#define MK_BIND_GLM_NORM    22   /* bf16 [hidden]: RMSNorm weight */
+#define MK_BIND_GLM_RES_OUT 23   /* bf16 [M, hidden]: out, x + residual */
+#define MK_BIND_GLM_QA      24   /* e4m3 [M, hidden]: out, quantised RMSNorm rows */
+#define MK_BIND_GLM_SA      25   /* fp32 [M, hidden/128]: out, their scales */
+#define MK_BIND_GLM_W_QKVA  26   /* e4m3 [q_lora + kv_lora + rope, hidden] */
+#define MK_BIND_GLM_S_QKVA  27
+#define MK_BIND_GLM_W_GATE  28   /* e4m3 [gate_heads, hidden] */
+#define MK_BIND_GLM_S_GATE  29
+#define MK_BIND_GLM_W_IK    30   /* e4m3 [idx_dim, hidden] */
+#define MK_BIND_GLM_S_IK    31
+#define MK_BIND_GLM_W_QB    32   /* e4m3 [q_heads * q_head_dim, q_lora] */
+#define MK_BIND_GLM_S_QB    33
+#define MK_BIND_GLM_W_IQ    34   /* e4m3 [idx_heads * idx_dim, q_lora] */
+#define MK_BIND_GLM_S_IQ    35
+#define MK_BIND_GLM_QKVA    36   /* bf16 [M, q_lora + kv_lora + rope]: out, QKV-A */
+#define MK_BIND_GLM_IK      37   /* bf16 [M, idx_dim]: out, Indexer-K before RoPE */
+#define MK_BIND_GLM_QB      38   /* e4m3 [M, q_lora]: out, re-quantised q-lora */
+#define MK_BIND_GLM_SB      39   /* fp32 [M, q_lora/128]: out, its scales */
+#define MK_BIND_GLM_GATE    40   /* bf16 [M, gate_heads]: out, Head-Gate */
+#define MK_BIND_GLM_Q       41   /* bf16 [M, q_heads, q_head_dim]: out, Q-B, last `rope` of each head roped */
+#define MK_BIND_GLM_IQ      42   /* bf16 [M, idx_heads, idx_dim]: out, Indexer-Q, last `rope` roped */
+#define MK_BIND_GLM_LATENT  43   /* bf16 [requests, cache_slots, kv_lora + rope]: latent cache */
+#define MK_BIND_GLM_INDEX   44   /* bf16 [requests, cache_slots, idx_dim]: index cache */
+#define MK_BIND_COUNT       45
 
 /* Packed argmax key: (order-preserving bits of the fp32 logit << 32) |
  * (0xFFFFFFFF - index); the largest key is the largest logit, lowest index on
@@ -211,6 +241,41 @@ typedef struct {
 } mk_graph_desc;
 
 int mk_plan_graph(const mk_graph_desc *graph, const mk_target_desc *target, mk_plan_t *out);
+
+/* Plan the GLM FP8 pre-attention block ("MegaRTP megakernel article": the
+ * computation of GLM-5.2-FP8 decode before sparse FlashMLA; sections 1-2 list
+ * its kernels and branches).  Per step, for M = requests x tokens rows:
+ *   A0   new residual = x + res (bf16); RMSNorm (weight bound, eps); per
+ *        (row, 128 columns) e4m3 with scale amax / 448        (M tasks)
+ *   B    QKV-A, Head-Gate, Indexer-K: FP8 GEMMs of A0's rows, 16 weight rows
+ *        per task, K split over the 8 consumer warps
+ *   FIN  per row: q-lora (QKV-A columns 0 .. q_lora-1) re-quantised per 128;
+ *        kv-lora || RoPE(k_pe) -> latent cache, Indexer-K with RoPE on its
+ *        last `rope` columns -> index cache, at slot pos0 + token  (M tasks)
+ *   C    Q-B and Indexer-Q: FP8 GEMMs of the re-quantised q-lora, 64 weight
+ *        rows per task, RoPE on the last `rope` columns of each head
+ * Every GEMM output is sum over 128-wide K blocks of a_scale * w_scale *
+ * (a . w), rounded to bf16; RoPE is rotate-half with angle
+ * pos * rope_theta^(-2i/rope) on those bf16 values.  Events: A0 -> B (whole),
+ * QKV-A + Indexer-K -> FIN (whole), FIN -> C (whole); the next step's A0
+ * waits for the previous step's last tasks.  Constraints (MK_ERR_UNSUPPORTED
+ * otherwise): M <= 16; hidden, q_lora, kv_lora multiples of 128; rope = 64;
+ * q_head_dim and idx_dim multiples of 64 with the roped part the last 64;
+ * q_lora + kv_lora + rope, gate_heads, idx_dim multiples of 16. */
+typedef struct {
+    int requests, tokens;        /* M = requests * tokens rows, token j of request r is row r * tokens + j */
+    int hidden;
+    int q_lora, kv_lora, rope;
+    int q_heads, q_head_dim;
+    int gate_heads;
+    int idx_heads, idx_dim;
+    int cache_slots;             /* slots per request of both caches */
+    int pos0;                    /* position and cache slot of each request's first new token */
+    int max_steps;
+    float eps, rope_theta;
+} mk_glm_desc;
+
+int mk_plan_glm(const mk_glm_desc *glm, const mk_target_desc *target, mk_plan_t *out);
 
 int mk_plan_info_get(mk_plan_t plan, mk_plan_info *info);
 

@@ -30,6 +30,7 @@ void layout_workspace(Plan &p) {
     p.ws.queue = take(p.words.size() * 4);
     p.ws.optab = take((uint64_t)p.num_ops * N_SLOTS * 8);
     p.ws.seq0 = take((uint64_t)B * 4);
+    p.ws.rope = take(p.rope_tab.size() * 4);
     if (p.kind == PLAN_LLAMA) {
         p.ws.hres = take((uint64_t)B * H * 4);
         p.ws.hmid = take((uint64_t)B * H * 4);
@@ -115,6 +116,24 @@ int mk_plan_graph(const mk_graph_desc *graph, const mk_target_desc *target, mk_p
     p.red_bytes = 128;
     p.aux_bytes = 256;
     p.smem_bytes = p.abuf_bytes + 2 * p.act_bytes + p.num_pages * p.page_bytes + p.aux_bytes + MBAR_BYTES + CTRL_BYTES;
+    return finish_new_plan(p, out);
+}
+
+int mk_plan_glm(const mk_glm_desc *glm, const mk_target_desc *target, mk_plan_t *out) {
+    if (!out) return set_error(MK_ERR_INVALID, "out is null");
+    *out = nullptr;
+    mk_target_desc def{};
+    if (!target) target = &def;
+    int workers, smem;
+    int rc = resolve_target(target, workers, smem);
+    if (rc) return rc;
+    Plan p;
+    try {
+        rc = plan_glm(glm, target, workers, smem, p);
+    } catch (const std::bad_alloc &) {
+        return set_error(MK_ERR_INVALID, "out of host memory while planning");
+    }
+    if (rc) return rc;
     return finish_new_plan(p, out);
 }
 

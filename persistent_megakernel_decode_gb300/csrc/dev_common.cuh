@@ -108,6 +108,12 @@ DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uin
         "l"(src), "r"(bytes), "r"(saddr(bar)), "l"(pol)
         : "memory");
 }
+DEV void bulk_g2s_plain(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     saddr(dst)),
+                 "l"(src), "r"(bytes), "r"(saddr(bar))
+                 : "memory");
+}
 DEV void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p)); }
 
 // Two fp32 fused multiply-adds in one instruction: acc.{lo,hi} += a.{lo,hi} * b.{lo,hi}, each rounded
@@ -419,6 +425,9 @@ DEV void fetch(WIns &I, const KParams &P, const int32_t *q, int i) {
 }
 
 // Warp-uniform sanity checks of one instruction against the launch.
+// GLM = the kernel instance of GLM-block plans: only it accepts (and
+// contains the code of) the GLM opcodes.
+template <bool GLM>
 DEV bool ins_valid(const KParams &P, const WIns &I) {
     const int opc = F(I, W_OPC);
     if (opc < 0 || opc >= MK_NUM_OPCODES) return false;
@@ -432,7 +441,27 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
         if ((int)((uint32_t)F(I, W_WAIT + 2 * i) & ~WAIT_PREV_EPOCH) >= P.num_events) return false;
     for (int i = 0; i < ns; ++i)
         if ((uint32_t)F(I, W_SIG + 2 * i) >= (uint32_t)P.num_events) return false;
-    if (opc >= MK_OP_QKV && opc != MK_OP_ATTN) {
+    if (opc >= MK_OP_GLM_A0) {
+        if constexpr (!GLM) return false;
+        const int M = F(I, P_GL_M), T = F(I, P_GL_T);
+        if (M <= 0 || M > GLM_MAX_M || T <= 0 || T > GLM_MAX_M || F(I, P_GL_POS0) < 0) return false;
+        if (opc == MK_OP_GLM_A0) return F(I, P_ROW0) >= 0 && F(I, P_ROW0) < M && P.H % 128 == 0 && P.H <= 8192;
+        if (opc == MK_OP_GLM_FIN) {
+            const int ql = F(I, P_GF_QLORA), kl = F(I, P_GF_KVLORA), id = F(I, P_GF_IDX), m = F(I, P_ROW0);
+            return m >= 0 && m < M && ql > 0 && ql % 128 == 0 && ql <= 16 * 128 && kl >= 0 && kl % 2 == 0 &&
+                   id >= GLM_ROPE && id % 2 == 0 && F(I, P_GL_POS0) + T <= F(I, P_GF_SLOTS) &&
+                   F(I, P_GF_QKVA_LD) >= ql + kl + GLM_ROPE;
+        }
+        const int nr = F(I, P_NROWS), kc = F(I, P_KC), rpp = F(I, P_RPP);
+        if (nr != 16 && nr != 64) return false;
+        if (kc <= 0 || kc % 128 || F(I, P_K0) != 0 || F(I, P_KTOT) != kc || rpp != P.page_bytes / kc || rpp < 1 ||
+            F(I, P_NPG) != (nr + rpp - 1) / rpp || F(I, P_NPG) > P.num_pages)
+            return false;
+        if (GLM_MAX_M * (kc + 16) + GLM_MAX_M * (kc / 128) * 4 > P.abuf_bytes || GLM_MAX_M * 64 * 4 > P.red_bytes)
+            return false;
+        return F(I, P_GL_LD) >= F(I, P_OUT0) + nr && F(I, P_OUT0) >= 0 && (F(I, P_GL_ROPE) == 0 || nr == 64);
+    }
+    if (opc >= MK_OP_QKV && opc <= MK_OP_LM && opc != MK_OP_ATTN) {
         const int nrows = F(I, P_NROWS), kc = F(I, P_KC);
         const int rmax = P.B > 4 ? 8 : MAX_TILE_ROWS;
         const int total = opc == MK_OP_UP ? 2 * nrows : nrows;
@@ -488,6 +517,7 @@ DEV int attn_cached_rows(const WIns &I, int pos) { return max(0, min(F(I, P_T), 
 
 // Weight / cache rows streamed by the loader for one instruction.  Loader and
 // consumers derive the same segments and walk the same page ring.
+template <bool GLM>
 DEV int describe(const KParams &P, const WIns &I, Seg &s0, Seg &s1) {
     const int opc = F(I, W_OPC);
     if (opc == MK_OP_QKV || opc == MK_OP_O || opc == MK_OP_DOWN || opc == MK_OP_LM || opc == MK_OP_UP) {
@@ -506,6 +536,14 @@ DEV int describe(const KParams &P, const WIns &I, Seg &s0, Seg &s1) {
         s1 = s0;
         s1.src = reinterpret_cast<const uint8_t *>(PTR(I, S_UP_WU)) + off;
         return 2;
+    }
+    if (GLM && opc == MK_OP_GLM_GEMM) {
+        const long long ktot = F(I, P_KTOT);
+        s0.src = reinterpret_cast<const uint8_t *>(PTR(I, S_GG_W)) + (long long)F(I, P_ROW0) * ktot;
+        s0.rows = F(I, P_NROWS);
+        s0.row_bytes = F(I, P_KC);
+        s0.stride = ktot;
+        return 1;
     }
     if (opc == MK_OP_ATTN) {
         const int pos = attn_pos(P, I);

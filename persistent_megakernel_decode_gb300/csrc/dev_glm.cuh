@@ -1,0 +1,281 @@
+// GLM FP8 pre-attention block: the three instruction bodies run by the
+// consumer warps, and the activation staging of the GEMM tiles.
+//
+// "MegaRTP megakernel article", section 1: the block is Add+RMSNorm+Quant,
+// FP8 GEMMs with 128-wide block scales, RoPE and the cache write-back;
+// section 2: after the first kernel, QKV-A, Head-Gate and Indexer-K are
+// independent; QKV-A feeds the Q-B (main) and Indexer-Q paths.
+//
+// FP8 is e4m3 ("fn": bias 7, no infinities, largest finite 448).  At 16 token
+// rows the GEMMs are HBM-bound (about 31 flop per weight byte), so they use
+// warp-level m16n8k32 e4m3 tensor-core MMAs with the 16 tokens as the M side
+// and 8 weight rows as the N side, accumulating each 128-wide K block in the
+// MMA and applying its two scales in fp32 registers.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "dev_common.cuh"
+
+namespace mk {
+
+// e4m3 codes of (lo, hi), lo in the low byte (round to nearest even,
+// saturating at +-448)
+DEV uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+DEV float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+DEV float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+DEV uint32_t pack_bf16(float lo, float hi) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
+// D += A * B for A 16 x 32 (rows = tokens), B 32 x 8 (columns = weight rows),
+// e4m3 operands, fp32 accumulators
+DEV void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Quantise 4 values of a 128-column block whose other 124 values sit in the
+// warp's other lanes: scale = amax / 448 (1 for an all-zero block), codes of
+// value / scale.  Returns the 4 codes (first value in the low byte).
+DEV uint32_t quant4(const float (&v)[4], float &scale) {
+    float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    a = warp_max(a);
+    scale = a > 0.f ? a / 448.f : 1.f;
+    return e4m3x2(v[0] / scale, v[1] / scale) | (e4m3x2(v[2] / scale, v[3] / scale) << 16);
+}
+
+// ---------------------------------------------------------------- A0
+// One token row m: h = x + res (the new residual, bf16), RMSNorm of those
+// bf16 values, then per 128 columns e4m3 codes and a scale.  Warp w takes the
+// 128-column blocks w, w + 8, ...; lane l columns 4l .. 4l + 3 of each.
+__device__ __noinline__ void glm_a0_task(const KParams &P, const Smem S, const WIns &I, uint32_t &ured, bool ab) {
+    constexpr int BPW = 8;  // blocks per warp: hidden <= 8192
+    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int m = F(I, P_ROW0), H = P.H, nb = H >> 7;
+    const uint8_t *x = reinterpret_cast<const uint8_t *>(PTR(I, S_GA_X)) + (size_t)m * H * 2;
+    const uint8_t *res = reinterpret_cast<const uint8_t *>(PTR(I, S_GA_RES)) + (size_t)m * H * 2;
+    const uint8_t *nw = reinterpret_cast<const uint8_t *>(PTR(I, S_GA_NORM));
+    uint8_t *rout = reinterpret_cast<uint8_t *>(PTR(I, S_GA_RES_OUT)) + (size_t)m * H * 2;
+    uint8_t *qa = reinterpret_cast<uint8_t *>(PTR(I, S_GA_QA)) + (size_t)m * H;
+    float *sa = reinterpret_cast<float *>(PTR(I, S_GA_SA)) + (size_t)m * nb;
+    float h[BPW][4];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < BPW; ++j) {
+        const int blk = warp + CONSUMER_WARPS * j, col = blk * 128 + lane * 4;
+        if (blk < nb) {
+            const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(x + col * 2));
+            const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(res + col * 2));
+            h[j][0] = round_bf16(bf16_lo(xv.x) + bf16_lo(rv.x));
+            h[j][1] = round_bf16(bf16_hi(xv.x) + bf16_hi(rv.x));
+            h[j][2] = round_bf16(bf16_lo(xv.y) + bf16_lo(rv.y));
+            h[j][3] = round_bf16(bf16_hi(xv.y) + bf16_hi(rv.y));
+            if (!ab)
+                *reinterpret_cast<uint2 *>(rout + col * 2) =
+                    make_uint2(pack_bf16(h[j][0], h[j][1]), pack_bf16(h[j][2], h[j][3]));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ss = fmaf(h[j][e], h[j][e], ss);
+        }
+    }
+    ss = warp_sum(ss);
+    float *red = S.red((int)(ured % NRED));
+    ++ured;
+    if (lane == 0) red[warp] = ss;
+    consumer_bar();
+    float tot = 0.f;
+#pragma unroll
+    for (int k = 0; k < CONSUMER_WARPS; ++k) tot += red[k];
+    const float r = rsqrtf(tot / (float)H + P.eps);
+#pragma unroll
+    for (int j = 0; j < BPW; ++j) {
+        const int blk = warp + CONSUMER_WARPS * j, col = blk * 128 + lane * 4;
+        if (blk < nb) {  // warp-uniform
+            const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(nw + col * 2));
+            const float y[4] = {h[j][0] * r * bf16_lo(wv.x), h[j][1] * r * bf16_hi(wv.x),
+                                h[j][2] * r * bf16_lo(wv.y), h[j][3] * r * bf16_hi(wv.y)};
+            float scale;
+            const uint32_t codes = quant4(y, scale);
+            if (!ab) {
+                *reinterpret_cast<uint32_t *>(qa + col) = codes;
+                if (lane == 0) sa[blk] = scale;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- GEMM tile
+// out[m, out0 + c] for the M token rows and the tile's NR weight rows n0 + c:
+// sum over 128-wide K blocks kb of sa[m, kb] * sw[n / 128, kb] * (a_kb . w_kb),
+// rounded to bf16; a RoPE tile (64 columns, the last 64 of a head) then
+// rotates pairs (c, c + 32) with the position's table entry and rounds again.
+//
+// Warp w takes the 8 weight rows (w mod NR/8) * 8 .. + 7 over K split
+// KS = 64 / NR ways (part w / (NR/8)).  Within each 64-byte K chunk lane
+// (g, t) = (lane / 4, lane % 4) loads 16 contiguous bytes of token rows g and
+// g + 8 and of weight row g at offset 16 t, and feeds them to two MMAs: the K
+// order inside the chunk is permuted the same way for A and B, which leaves
+// the dot products unchanged.  The activation rows are staged in shared
+// memory by the activation loader ([16][K + 16] codes, then [16][K / 128]
+// scales); weight rows come from the tile's pages, whole rows per page.
+template <int NR>
+__device__ __noinline__ void glm_gemm_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, uint32_t &ring, uint32_t &ured,
+                       bool &ab) {
+    constexpr int NG = NR / 8, KS = CONSUMER_WARPS / NG;
+    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int g = lane >> 2, t = lane & 3, gi = warp % NG, ks = warp / NG;
+    const int K = F(I, P_KC), KB = K >> 7, n0 = F(I, P_ROW0), rpp = F(I, P_RPP), npg = F(I, P_NPG);
+    const int M = F(I, P_GL_M), ld = F(I, P_GL_LD), out0 = F(I, P_OUT0), rope = F(I, P_GL_ROPE), T = F(I, P_GL_T);
+    const float *sw = reinterpret_cast<const float *>(PTR(I, S_GG_SW));
+    __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(PTR(I, S_GG_OUT));
+    const float2 *rtab = reinterpret_cast<const float2 *>(PTR(I, S_GG_ROPE));
+    const int NP = P.num_pages;
+    const uint32_t base = ring;
+    ring += npg;
+    const uint8_t *abuf = reinterpret_cast<const uint8_t *>(S.abuf(sl));
+    const int astride = K + 16;
+    const float *sa = reinterpret_cast<const float *>(abuf + GLM_MAX_M * astride);
+    for (int k = 0; k < npg; ++k)
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(base + k) % NP], ((base + k) / NP) & 1, 2, i, MK_OP_GLM_GEMM);
+    const int r = gi * 8 + g;
+    const uint8_t *wrow = S.pages() + (size_t)((base + r / rpp) % NP) * P.page_bytes + (size_t)(r % rpp) * K;
+    const bool lo_ok = g < M, hi_ok = g + 8 < M;
+    const uint8_t *alo = abuf + g * astride, *ahi = abuf + (g + 8) * astride;
+    const int kb0 = ks * KB / KS, kb1 = (ks + 1) * KB / KS;
+    const float *swr = sw + (size_t)((n0 + gi * 8) >> 7) * KB;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int kb = kb0; kb < kb1; ++kb) {
+        float cb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int off = kb * 128 + c * 64 + t * 16;
+            const uint4 w = *reinterpret_cast<const uint4 *>(wrow + off);
+            const uint4 a = lo_ok ? *reinterpret_cast<const uint4 *>(alo + off) : zero;
+            const uint4 b = hi_ok ? *reinterpret_cast<const uint4 *>(ahi + off) : zero;
+            mma_e4m3(cb, a.x, b.x, a.y, b.y, w.x, w.y);
+            mma_e4m3(cb, a.z, b.z, a.w, b.w, w.z, w.w);
+        }
+        const float swv = __ldg(swr + kb);
+        const float s0 = lo_ok ? sa[g * KB + kb] * swv : 0.f;
+        const float s1 = hi_ok ? sa[(g + 8) * KB + kb] * swv : 0.f;
+        acc[0] = fmaf(s0, cb[0], acc[0]);
+        acc[1] = fmaf(s0, cb[1], acc[1]);
+        acc[2] = fmaf(s1, cb[2], acc[2]);
+        acc[3] = fmaf(s1, cb[3], acc[3]);
+    }
+    __syncwarp();
+    if (lane == 0) {
+        for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(base + k) % NP]);
+        mbar_arrive(&S.act_empty()[sl]);  // staged rows no longer needed by this warp
+    }
+    // partials [KS][16][NR] in a reduction buffer (its previous user, NRED
+    // buffer uses back, finished before every warp passed a later barrier)
+    float *red = S.red((int)(ured % NRED));
+    ++ured;
+    float *pr = red + ks * GLM_MAX_M * NR;
+    const int n = gi * 8 + 2 * t;
+    pr[g * NR + n] = acc[0];
+    pr[g * NR + n + 1] = acc[1];
+    pr[(g + 8) * NR + n] = acc[2];
+    pr[(g + 8) * NR + n + 1] = acc[3];
+    consumer_bar();
+    if (ab) return;
+    for (int e = ct; e < M * NR; e += CONSUMERS) {
+        const int m = e / NR, c = e % NR;
+        float v = 0.f, o = 0.f;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) v += red[k * GLM_MAX_M * NR + m * NR + c];
+        v = round_bf16(v);
+        if (NR == 64 && rope) {
+#pragma unroll
+            for (int k = 0; k < KS; ++k) o += red[k * GLM_MAX_M * NR + m * NR + (c ^ 32)];
+            o = round_bf16(o);
+            const float2 cs = rtab[(m % T) * 32 + (c & 31)];
+            v = c < 32 ? v * cs.x - o * cs.y : v * cs.x + o * cs.y;
+        }
+        out[(size_t)m * ld + out0 + c] = __float2bfloat16_rn(v);
+    }
+}
+
+// ---------------------------------------------------------------- FIN
+// One token row m of request m / T at slot pos0 + m % T: q-lora (QKV-A
+// columns 0 .. QL-1) re-quantised per 128 columns, one warp per block; the
+// latent cache row = kv-lora || RoPE(k_pe); the index cache row = Indexer-K
+// with RoPE on its last 64 columns.
+__device__ __noinline__ void glm_fin_task(const KParams &P, const WIns &I, bool ab) {
+    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int m = F(I, P_ROW0), QL = F(I, P_GF_QLORA), KL = F(I, P_GF_KVLORA), ID = F(I, P_GF_IDX);
+    const int slots = F(I, P_GF_SLOTS), LDQ = F(I, P_GF_QKVA_LD), T = F(I, P_GL_T), pos0 = F(I, P_GL_POS0);
+    const __nv_bfloat16 *qkva = reinterpret_cast<const __nv_bfloat16 *>(PTR(I, S_GF_QKVA)) + (size_t)m * LDQ;
+    const __nv_bfloat16 *ik = reinterpret_cast<const __nv_bfloat16 *>(PTR(I, S_GF_IK)) + (size_t)m * ID;
+    uint8_t *qb = reinterpret_cast<uint8_t *>(PTR(I, S_GF_QB)) + (size_t)m * QL;
+    float *sb = reinterpret_cast<float *>(PTR(I, S_GF_SB)) + (size_t)m * (QL >> 7);
+    __nv_bfloat16 *lat = reinterpret_cast<__nv_bfloat16 *>(PTR(I, S_GF_LAT));
+    __nv_bfloat16 *idx = reinterpret_cast<__nv_bfloat16 *>(PTR(I, S_GF_IDX));
+    const float2 *rtab = reinterpret_cast<const float2 *>(PTR(I, S_GF_ROPE));
+    const int req = m / T, j = m % T, slot = pos0 + j;
+    for (int blk = warp; blk < (QL >> 7); blk += CONSUMER_WARPS) {
+        const int col = blk * 128 + lane * 4;
+        const uint2 u = __ldcg(reinterpret_cast<const uint2 *>(qkva + col));
+        const float v[4] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y)};
+        float scale;
+        const uint32_t codes = quant4(v, scale);
+        if (!ab) {
+            *reinterpret_cast<uint32_t *>(qb + col) = codes;
+            if (lane == 0) sb[blk] = scale;
+        }
+    }
+    if (ab) return;
+    __nv_bfloat16 *lrow = lat + ((size_t)req * slots + slot) * (KL + GLM_ROPE);
+    for (int e = ct * 2; e < KL; e += 2 * CONSUMERS)
+        *reinterpret_cast<uint32_t *>(lrow + e) = __ldcg(reinterpret_cast<const uint32_t *>(qkva + QL + e));
+    __nv_bfloat16 *irow = idx + ((size_t)req * slots + slot) * ID;
+    for (int e = ct * 2; e < ID - GLM_ROPE; e += 2 * CONSUMERS)
+        *reinterpret_cast<uint32_t *>(irow + e) = __ldcg(reinterpret_cast<const uint32_t *>(ik + e));
+    // RoPE pairs: threads 0-31 the k_pe slice, 32-63 Indexer-K's last 64
+    if (ct < 64) {
+        const int p = ct & 31;
+        const __nv_bfloat16 *src = ct < 32 ? qkva + QL + KL : ik + ID - GLM_ROPE;
+        __nv_bfloat16 *dst = ct < 32 ? lrow + KL : irow + ID - GLM_ROPE;
+        const unsigned short *s16 = reinterpret_cast<const unsigned short *>(src);
+        const float lo = __uint_as_float((uint32_t)__ldcg(s16 + p) << 16);
+        const float hi = __uint_as_float((uint32_t)__ldcg(s16 + p + 32) << 16);
+        const float2 cs = rtab[j * 32 + p];
+        dst[p] = __float2bfloat16_rn(lo * cs.x - hi * cs.y);
+        dst[p + 32] = __float2bfloat16_rn(hi * cs.x + lo * cs.y);
+    }
+}
+
+// ---------------------------------------------------------------- staging
+// Activation loader, GEMM tiles: after the tile's events were acquired, bulk
+// copies of the M activation rows (into rows of K + 16 bytes) and of their
+// scales into the activation buffer, completing on the slot's full barrier.
+// Returns the bytes in flight (0 if the buffer already holds this input).
+__device__ __noinline__ uint32_t stage_glm(const KParams &P, const WIns &I, uint8_t *abuf, uint64_t *full) {
+    const int lane = threadIdx.x & 31;
+    const int K = F(I, P_KC), M = F(I, P_GL_M);
+    const uint8_t *xq = reinterpret_cast<const uint8_t *>(PTR(I, S_GG_XQ));
+    const uint8_t *xs = reinterpret_cast<const uint8_t *>(PTR(I, S_GG_XS));
+    const uint32_t sbytes = (uint32_t)M * (uint32_t)(K >> 7) * 4u;
+    const uint32_t bytes = (uint32_t)M * (uint32_t)K + sbytes;
+    if (lane == 0) {
+        // the acquire of the tile's events (generic proxy) before the bulk reads (async proxy)
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        mbar_expect_tx(full, bytes);
+        for (int m = 0; m < M; ++m) bulk_g2s_plain(abuf + (size_t)m * (K + 16), xq + (size_t)m * K, (uint32_t)K, full);
+        bulk_g2s_plain(abuf + (size_t)GLM_MAX_M * (K + 16), xs, sbytes, full);
+    }
+    __syncwarp();
+    return bytes;
+}
+
+}  // namespace mk

@@ -532,7 +532,7 @@ DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, int sl,
 // gate row and its up row fall to the same warp.
 constexpr int RPW_MAX_PAGES = 4;
 DEV bool rpw_tile(const KParams &P, const Dec &d) {
-    if (P.B != 1 || d.opc < MK_OP_QKV || d.opc == MK_OP_ATTN) return false;
+    if (P.B != 1 || d.opc < MK_OP_QKV || d.opc > MK_OP_LM || d.opc == MK_OP_ATTN) return false;
     if (d.kc % 256 || d.kc > 2048) return false;
     const bool up = d.opc == MK_OP_UP;
     if (d.npg == 1) return up ? d.nrows == 8 : d.nrows <= 16;

@@ -23,12 +23,14 @@
 #include <mutex>
 #include <vector>
 
+#include "dev_glm.cuh"
 #include "dev_ops.cuh"
 #include "planner.h"
 
 namespace mk {
 
 // ---------------------------------------------------------------- loader warp
+template <bool GLM>
 DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int lane = threadIdx.x & 31;
     const uint64_t pol = evict_first_policy();
@@ -41,12 +43,12 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
         if (lane < 4 && i + 4 + lane < P.lmax) prefetch_l2(myq + (size_t)(i + 4 + lane) * W_WORDS);
         fetch(I, P, myq, i);
         const int opc = F(I, W_OPC);
-        if (!ins_valid(P, I)) {
+        if (!ins_valid<GLM>(P, I)) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
             break;
         }
         Seg s0, s1;
-        const int nseg = describe(P, I, s0, s1);
+        const int nseg = describe<GLM>(P, I, s0, s1);
         if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 4] = gtimer();
         // Rows go to pages in order, as many whole rows per page as fit.  GEMV
         // segments (MLP-up: gate rows, then up rows) share pages; attention
@@ -123,7 +125,7 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
 }
 
 // ---------------------------------------------------------------- activation-loader warp
-template <int MAXB>
+template <int MAXB, bool GLM>
 DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int lane = threadIdx.x & 31;
     const bool two_bufs = P.abuf_count > 1;
@@ -144,7 +146,7 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
         if (!needs_handoff(P, I, decode(I), chain)) continue;  // same input as the previous slot: nothing to stage
         const int sl = hs & 1;
         const uint32_t use = hs >> 1;
-        if (!ab && !ins_valid(P, I)) {
+        if (!ab && !ins_valid<GLM>(P, I)) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 1);
             ab = true;
         }
@@ -166,13 +168,25 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
         if (!ab && lane == 0 && P.trace) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 2] = gtimer();
         float *slot = reinterpret_cast<float *>(S.act(sl));
         int flags = 0;
+        uint32_t tx = 0;  // bytes of bulk copies completing on the slot's full barrier
         if (opc == MK_OP_ATTN) {
             const bool g4 = P.Hq <= 4 * P.Hkv;
             if (P.D == 64) g4 ? stage_attn<64, 4>(P, I, slot, ab, rope64) : stage_attn<64, 8>(P, I, slot, ab, rope64);
             else g4 ? stage_attn<128, 4>(P, I, slot, ab, rope128) : stage_attn<128, 8>(P, I, slot, ab, rope128);
             flags = SLOT_FRESH;
             key0 = key1 = -1;
-        } else if (opc >= MK_OP_QKV) {
+        } else if (GLM && opc == MK_OP_GLM_GEMM) {
+            // the tile's activation rows by bulk copies, unless the buffer
+            // already holds them (key: the input's device address)
+            const long long key = (long long)PTR(I, S_GG_XQ);
+            if (key != key0) {
+                if (hs > 0 && !ab)
+                    ab = !warp_wait_bar(P, S, &S.act_empty()[(hs - 1) & 1], ((hs - 1) >> 1) & 1, 1, i, opc);
+                if (!ab) tx = stage_glm(P, I, reinterpret_cast<uint8_t *>(S.abuf(0)), &S.act_full()[sl]);
+                key0 = ab ? -1 : key;
+            }
+            key1 = -1;
+        } else if (opc >= MK_OP_QKV && opc <= MK_OP_LM) {
             // two buffers: buffer sl was last read by instruction i - 2, whose
             // slot release was awaited above; one buffer: instruction i - 1
             // may still read it
@@ -193,7 +207,7 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
         __syncwarp();
         if (lane == 0) {
             S.ctrl()[1 + sl] = flags;
-            mbar_arrive(&S.act_full()[sl]);
+            if (tx == 0) mbar_arrive(&S.act_full()[sl]);  // (else stage_glm's arrive.expect_tx was the arrival)
         }
         ++hs;
     }
@@ -321,7 +335,7 @@ DEV bool gemv_dispatch(const KParams &P, const Smem S, const WIns &I, int i, int
     return false;
 }
 
-template <int MAXB>
+template <int MAXB, bool GLM>
 DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int ct = threadIdx.x - 64, lane = ct & 31;
     uint32_t ring = 0, cph = 0, ured = 0;
@@ -353,6 +367,15 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         } else if (opc == MK_OP_EMBED) {
             consumer_sync(P, S, cph, ab, i);
             embed_task(P, S, I, i, sl, ab);
+        } else if (GLM && opc == MK_OP_GLM_GEMM) {
+            if (d.nrows == 64) glm_gemm_task<64>(P, S, I, i, sl, ring, ured, ab);
+            else glm_gemm_task<16>(P, S, I, i, sl, ring, ured, ab);
+            rq.set(ring, P.num_pages);
+        } else if (GLM && (opc == MK_OP_GLM_A0 || opc == MK_OP_GLM_FIN)) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // the slot holds nothing for these
+            if (opc == MK_OP_GLM_A0) glm_a0_task(P, S, I, ured, ab);
+            else glm_fin_task(P, I, ab);
         } else if (opc >= MK_OP_QKV) {
             if (MAXB == 1 && rpw_tile(P, d)) {  // (a constant condition for larger batches)
                 const int kg = d.kc >> 8;
@@ -381,8 +404,8 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
 }
 
 // ---------------------------------------------------------------- kernel
-template <int MAXB>
-__global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
+template <int MAXB, bool GLM>
+__global__ void __launch_bounds__(THREADS, 1) mk_interp(__grid_constant__ const KParams P) {
     Smem S;
     S.o_abuf = 0;
     S.abuf_stride = P.abuf_count > 1 ? P.abuf_bytes : 0;
@@ -412,10 +435,10 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
     __syncthreads();
     const int32_t *myq = P.queue + (size_t)blockIdx.x * P.lmax * W_WORDS;
     const int warp = threadIdx.x >> 5;
-    if (warp == 0) loader_role(P, S, myq);
-    else if (warp == 1) aloader_role<MAXB>(P, S, myq);
+    if (warp == 0) loader_role<GLM>(P, S, myq);
+    else if (warp == 1) aloader_role<MAXB, GLM>(P, S, myq);
     else if (warp == PUBLISHER_WARP) publisher_role(P, S, myq);
-    else consumer_role<MAXB>(P, S, myq);
+    else consumer_role<MAXB, GLM>(P, S, myq);
     __syncthreads();
 }
 
@@ -439,15 +462,50 @@ int query_device(int *num_sms, int *smem_optin) {
 
 using KernelFn = void (*)(const KParams);
 
-static KernelFn pick_kernel(int B) {
-    if (B <= 1) return mk_interp<1>;
-    if (B <= 2) return mk_interp<2>;
-    if (B <= 4) return mk_interp<4>;
-    return mk_interp<8>;
+static KernelFn pick_kernel(const Plan &p) {
+    if (p.kind == PLAN_GLM) return mk_interp<1, true>;
+    const int B = p.B;
+    if (B <= 1) return mk_interp<1, false>;
+    if (B <= 2) return mk_interp<2, false>;
+    if (B <= 4) return mk_interp<4, false>;
+    return mk_interp<8, false>;
+}
+
+// Operand rows of the GLM block plan, in the planner's op order: A0,
+// QKV-A, Head-Gate, Indexer-K, FIN, Q-B, Indexer-Q.
+static int build_glm_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab) {
+    for (int b = MK_BIND_GLM_X; b <= MK_BIND_GLM_INDEX; ++b)
+        if (!p.bind[b][0]) {
+            char buf[96];
+            std::snprintf(buf, sizeof buf, "binding %d (GLM block) is not set", b);
+            return set_error(MK_ERR_UNBOUND, buf);
+        }
+    auto B = [&](int b) { return p.bind[b][0]; };
+    auto row = [&](int o) { return &tab[(size_t)o * N_SLOTS]; };
+    uint64_t *r = row(0);
+    r[S_GA_X] = B(MK_BIND_GLM_X); r[S_GA_RES] = B(MK_BIND_GLM_RES); r[S_GA_NORM] = B(MK_BIND_GLM_NORM);
+    r[S_GA_RES_OUT] = B(MK_BIND_GLM_RES_OUT); r[S_GA_QA] = B(MK_BIND_GLM_QA); r[S_GA_SA] = B(MK_BIND_GLM_SA);
+    auto gemm = [&](int o, int w, int sw, int xq, int xs, int out) {
+        uint64_t *g = row(o);
+        g[S_GG_W] = B(w); g[S_GG_SW] = B(sw); g[S_GG_XQ] = B(xq); g[S_GG_XS] = B(xs); g[S_GG_OUT] = B(out);
+    };
+    gemm(1, MK_BIND_GLM_W_QKVA, MK_BIND_GLM_S_QKVA, MK_BIND_GLM_QA, MK_BIND_GLM_SA, MK_BIND_GLM_QKVA);
+    gemm(2, MK_BIND_GLM_W_GATE, MK_BIND_GLM_S_GATE, MK_BIND_GLM_QA, MK_BIND_GLM_SA, MK_BIND_GLM_GATE);
+    gemm(3, MK_BIND_GLM_W_IK, MK_BIND_GLM_S_IK, MK_BIND_GLM_QA, MK_BIND_GLM_SA, MK_BIND_GLM_IK);
+    r = row(4);
+    r[S_GF_QKVA] = B(MK_BIND_GLM_QKVA); r[S_GF_IK] = B(MK_BIND_GLM_IK); r[S_GF_QB] = B(MK_BIND_GLM_QB);
+    r[S_GF_SB] = B(MK_BIND_GLM_SB); r[S_GF_LAT] = B(MK_BIND_GLM_LATENT); r[S_GF_IDX] = B(MK_BIND_GLM_INDEX);
+    gemm(5, MK_BIND_GLM_W_QB, MK_BIND_GLM_S_QB, MK_BIND_GLM_QB, MK_BIND_GLM_SB, MK_BIND_GLM_Q);
+    gemm(6, MK_BIND_GLM_W_IQ, MK_BIND_GLM_S_IQ, MK_BIND_GLM_QB, MK_BIND_GLM_SB, MK_BIND_GLM_IQ);
+    const uint64_t rope = (uint64_t)(uintptr_t)ws + p.ws.rope;
+    for (int o : {1, 2, 3, 5, 6}) row(o)[S_GG_ROPE] = rope;
+    row(4)[S_GF_ROPE] = rope;
+    return MK_OK;
 }
 
 static int build_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab) {
     tab.assign((size_t)p.num_ops * N_SLOTS, 0);
+    if (p.kind == PLAN_GLM) return build_glm_table(p, ws, tab);
     if (p.kind != PLAN_LLAMA) return MK_OK;
     const mk_model_desc &m = p.model;
     const int L = m.layers, B = p.B, Hkv = m.kv_heads, D = m.head_dim;
@@ -548,6 +606,11 @@ static KParams base_params(const Plan &p, uint8_t *ws) {
     k.V = m.vocab; k.L = m.layers; k.Smax = p.smax; k.qk_norm = m.qk_norm; k.nsplit_max = p.nsplit_max;
     k.eps = m.eps;
     k.theta = m.rope_theta;
+    if (p.kind == PLAN_GLM) {
+        k.H = p.glm.hidden;
+        k.eps = p.glm.eps;
+        k.theta = p.glm.rope_theta;
+    }
     return k;
 }
 
@@ -580,6 +643,11 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
                 e = cudaMemcpyAsync(ws + p.ws.seq0, p.seq0.data(), p.seq0.size() * 4, cudaMemcpyHostToDevice, stream);
                 if (e != cudaSuccess) return cuda_fail(e, "upload lengths");
             }
+            if (!p.rope_tab.empty()) {
+                e = cudaMemcpyAsync(ws + p.ws.rope, p.rope_tab.data(), p.rope_tab.size() * 4, cudaMemcpyHostToDevice,
+                                    stream);
+                if (e != cudaSuccess) return cuda_fail(e, "upload RoPE table");
+            }
         }
         // the host images must stay valid until the copies ran
         e = cudaStreamSynchronize(stream);
@@ -596,10 +664,11 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
             if (e != cudaSuccess) return cuda_fail(e, "clear argmax");
         }
     }
-    KernelFn fn = pick_kernel(p.B);
+    KernelFn fn = pick_kernel(p);
     static thread_local int configured_smem = -1;
     if (configured_smem < p.smem_bytes) {
-        for (KernelFn f : {mk_interp<1>, mk_interp<2>, mk_interp<4>, mk_interp<8>}) {
+        for (KernelFn f : {mk_interp<1, false>, mk_interp<2, false>, mk_interp<4, false>, mk_interp<8, false>,
+                           mk_interp<1, true>}) {
             e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         }

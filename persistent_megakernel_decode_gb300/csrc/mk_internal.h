@@ -44,6 +44,21 @@ enum : int {
     P_NSPLIT = W_P + 5, P_LAYER = W_P + 6,
 };
 
+// GLM block payload.  GEMM tiles use the GEMV fields P_ROW0 (first weight
+// row), P_NROWS (16 or 64), P_K0 (0), P_KC = P_KTOT (K, bytes = elements of
+// e4m3), P_OUT0 (first output column), P_RPP, P_NPG, plus:
+enum : int {
+    P_GL_LD = W_P + 10,    // output row stride (elements)
+    P_GL_ROPE = W_P + 11,  // GEMM: 1 if the tile's 64 columns are a RoPE slice
+    P_GL_M = W_P + 12,     // token rows
+    P_GL_T = W_P + 13,     // tokens per request
+    P_GL_POS0 = W_P + 14,  // position of each request's first new token
+    // A0 / FIN: P_ROW0 is the token row; FIN also:
+    P_GF_QLORA = W_P + 1, P_GF_KVLORA = W_P + 2, P_GF_IDX = W_P + 3, P_GF_SLOTS = W_P + 4, P_GF_QKVA_LD = W_P + 5,
+};
+constexpr int GLM_MAX_M = 16;     // token rows of the GLM block (A fragments of m16n8k32)
+constexpr int GLM_ROPE = 64;      // width of a RoPE slice
+
 // ---- operand table slots (16 x uint64 per op row) ------------------------
 enum : int {
     // EMBED
@@ -61,6 +76,10 @@ enum : int {
     S_DN_W = 0, S_DN_IN = 1, S_DN_HRES = 2,
     // LM
     S_LM_W = 0, S_LM_NORM = 1, S_LM_H = 2, S_LM_LOGITS = 3, S_LM_KEYS = 4, S_LM_HIST = 5,
+    // GLM A0 / GEMM / FIN
+    S_GA_X = 0, S_GA_RES = 1, S_GA_NORM = 2, S_GA_RES_OUT = 3, S_GA_QA = 4, S_GA_SA = 5,
+    S_GG_W = 0, S_GG_SW = 1, S_GG_XQ = 2, S_GG_XS = 3, S_GG_OUT = 4, S_GG_ROPE = 5,
+    S_GF_QKVA = 0, S_GF_IK = 1, S_GF_QB = 2, S_GF_SB = 3, S_GF_LAT = 4, S_GF_IDX = 5, S_GF_ROPE = 6,
     // every GEMV op: its output (QKV: qkv, O: residual, UP: activation, DOWN:
     // residual, LM: logits) and second output (O: mid residual, LM: argmax keys)
     S_G_OUT = 14, S_G_OUT2 = 15,

@@ -11,6 +11,7 @@
 // megakernel article", section 4 (TaskGraph).  Queues: section 4
 // (KernelPlan) and "CMU 15-779 Lecture 7 notes", sections 6.3-6.4.
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -848,6 +849,134 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     int64_t kv_write = (int64_t)2 * B * Hkv * D * 2 * L;
     int64_t norms = (int64_t)(2 * L + 1) * H * 2 + (m->qk_norm ? (int64_t)2 * L * D * 2 : 0);
     p.alg_bytes = weights + kv_read + kv_write + norms;
+    return finish_queues(p, false, p.schedule == MK_SCHED_TIMED);
+}
+
+// ---- GLM FP8 pre-attention block ------------------------------------------
+
+int plan_glm(const mk_glm_desc *g, const mk_target_desc *tgt, int num_workers, int smem_per_cta, Plan &p) {
+    if (!g || !tgt) return set_error(MK_ERR_INVALID, "null descriptor");
+    p = Plan{};
+    p.kind = PLAN_GLM;
+    p.glm = *g;
+    p.mode = MK_MODE_MEGAKERNEL;
+    p.num_workers = num_workers;
+    const int M = g->requests * g->tokens, H = g->hidden, QL = g->q_lora, KL = g->kv_lora, R = g->rope;
+    const int NQKVA = QL + KL + R, NQ = g->q_heads * g->q_head_dim, NI = g->idx_heads * g->idx_dim;
+    if (g->requests <= 0 || g->tokens <= 0 || H <= 0 || QL <= 0 || KL <= 0 || g->q_heads <= 0 ||
+        g->q_head_dim <= 0 || g->gate_heads <= 0 || g->idx_heads <= 0 || g->idx_dim <= 0 || g->max_steps <= 0 ||
+        g->pos0 < 0 || g->cache_slots <= 0 || !(g->eps > 0))
+        return set_error(MK_ERR_INVALID, "non-positive GLM block size");
+    if (g->pos0 + g->tokens > g->cache_slots) return set_error(MK_ERR_INVALID, "new tokens past the cache end");
+    if (M > GLM_MAX_M || R != GLM_ROPE || H % 128 || QL % 128 || KL % 128 || H / 128 > 64 || QL / 128 > 16 ||
+        g->q_head_dim % 64 || g->q_head_dim < 64 || g->idx_dim % 64 || g->idx_dim < 64 || NQKVA % 16 ||
+        g->gate_heads % 16 || g->idx_dim % 16 || H > 8192 || QL > 8192)
+        return set_error(MK_ERR_UNSUPPORTED, "GLM block sizes outside the kernels' tiling");
+    if (tgt->schedule < MK_SCHED_DEFAULT || tgt->schedule > MK_SCHED_TIMED)
+        return set_error(MK_ERR_INVALID, "schedule must be one of MK_SCHED_*");
+    p.schedule = tgt->schedule == MK_SCHED_BYTES ? MK_SCHED_BYTES : MK_SCHED_TIMED;
+    p.B = 1;  // the batch-1 kernel instance; the GLM ops take M from their payload
+    p.max_steps = g->max_steps;
+    // shared memory: the staged A operand (M <= 16 padded rows of K bytes, then
+    // the scales), a 4 KB tile reduction area per buffer, pages of whole weight rows
+    const int KMAX = std::max(H, QL);
+    p.abuf_bytes = round_up(GLM_MAX_M * (KMAX + 16) + GLM_MAX_M * (KMAX / 128) * 4, 128);
+    p.abuf_count = 1;
+    p.act_bytes = 128;
+    p.red_bytes = 4096;
+    p.aux_bytes = NRED * p.red_bytes + 256;
+    p.page_bytes = 48 * 1024;  // 8 rows of K = 6144 or 32 rows of K = 1536
+    for (int K : {H, QL})
+        if (p.page_bytes % K) return set_error(MK_ERR_UNSUPPORTED, "a page must hold whole weight rows");
+    const int fixed = p.abuf_bytes + 2 * p.act_bytes + p.aux_bytes + MBAR_BYTES + CTRL_BYTES;
+    p.num_pages = std::min(MAX_PAGES, (smem_per_cta - fixed) / p.page_bytes);
+    if (p.num_pages < 2) return set_error(MK_ERR_UNSUPPORTED, "shared memory holds fewer than two pages");
+    p.smem_bytes = fixed + p.num_pages * p.page_bytes;
+    // ops (operand rows): A0, QKV-A, Head-Gate, Indexer-K, FIN, Q-B, Indexer-Q
+    enum { OA0, OQKVA, OGATE, OIK, OFIN, OQB, OIQ, NOPS };
+    const int kinds[NOPS] = {MK_OP_GLM_A0, MK_OP_GLM_GEMM, MK_OP_GLM_GEMM, MK_OP_GLM_GEMM, MK_OP_GLM_FIN,
+                             MK_OP_GLM_GEMM, MK_OP_GLM_GEMM};
+    p.num_ops = NOPS;
+    for (int o = 0; o < NOPS; ++o) {
+        p.op_kind.push_back(kinds[o]);
+        p.op_layer.push_back(0);
+    }
+    // events: 0 A0 done, 1 QKV-A + Indexer-K done, 2 FIN done, 3 step done
+    enum { EV_A0, EV_B, EV_FIN, EV_DONE, NEV };
+    p.thresholds.assign(NEV, 0);
+    auto add = [&](int op, int opcode, int64_t cost, int wait_ev, int sig_ev) -> TaskRec & {
+        TaskRec t;
+        t.opcode = opcode;
+        t.op_row = op;
+        t.layer = 0;
+        t.cost = cost;
+        if (wait_ev >= 0) { t.w_ev[t.nw] = wait_ev; t.w_off[t.nw++] = 0; }
+        if (sig_ev >= 0) { t.s_ev[t.ns] = sig_ev; t.s_inc[t.ns++] = 1; p.thresholds[sig_ev]++; }
+        t.payload[P_GL_M - W_P] = M;
+        t.payload[P_GL_T - W_P] = g->tokens;
+        t.payload[P_GL_POS0 - W_P] = g->pos0;
+        p.tasks.push_back(t);
+        return p.tasks.back();
+    };
+    for (int m = 0; m < M; ++m) {
+        TaskRec &t = add(OA0, MK_OP_GLM_A0, (int64_t)H * 2 * 3, -1, EV_A0);
+        t.bid[0] = m;
+        t.payload[P_ROW0 - W_P] = m;
+    }
+    const int rpp_h = p.page_bytes / H, rpp_q = p.page_bytes / QL;
+    auto gemm = [&](int op, int N, int K, int nr, int rpp, int wait_ev, int sig_ev, int ld, int head) {
+        for (int n0 = 0; n0 < N; n0 += nr) {
+            TaskRec &t = add(op, MK_OP_GLM_GEMM, (int64_t)nr * K, wait_ev, sig_ev);
+            t.bid[0] = n0 / nr;
+            int32_t *pl = t.payload;
+            pl[P_ROW0 - W_P] = n0; pl[P_NROWS - W_P] = nr; pl[P_K0 - W_P] = 0; pl[P_KC - W_P] = K;
+            pl[P_KTOT - W_P] = K; pl[P_OUT0 - W_P] = n0; pl[P_RPP - W_P] = rpp; pl[P_NPG - W_P] = ceil_div(nr, rpp);
+            pl[P_GL_LD - W_P] = ld;
+            pl[P_GL_ROPE - W_P] = head > 0 && n0 % head == head - GLM_ROPE ? 1 : 0;
+        }
+    };
+    gemm(OQKVA, NQKVA, H, 16, rpp_h, EV_A0, EV_B, NQKVA, 0);
+    gemm(OIK, g->idx_dim, H, 16, rpp_h, EV_A0, EV_B, g->idx_dim, 0);
+    gemm(OGATE, g->gate_heads, H, 16, rpp_h, EV_A0, EV_DONE, g->gate_heads, 0);
+    for (int m = 0; m < M; ++m) {
+        TaskRec &t = add(OFIN, MK_OP_GLM_FIN, (int64_t)(NQKVA + g->idx_dim) * 2, EV_B, EV_FIN);
+        t.bid[0] = m;
+        int32_t *pl = t.payload;
+        pl[P_ROW0 - W_P] = m; pl[P_GF_QLORA - W_P] = QL; pl[P_GF_KVLORA - W_P] = KL; pl[P_GF_IDX - W_P] = g->idx_dim;
+        pl[P_GF_SLOTS - W_P] = g->cache_slots; pl[P_GF_QKVA_LD - W_P] = NQKVA;
+    }
+    // the last tasks of a step (Head-Gate above, FIN's cache writes, Q-B,
+    // Indexer-Q) count into the step-done event
+    for (auto &t : p.tasks)
+        if (t.opcode == MK_OP_GLM_FIN) { t.s_ev[t.ns] = EV_DONE; t.s_inc[t.ns++] = 1; p.thresholds[EV_DONE]++; }
+    gemm(OQB, NQ, QL, 64, rpp_q, EV_FIN, EV_DONE, NQ, g->q_head_dim);
+    gemm(OIQ, NI, QL, 64, rpp_q, EV_FIN, EV_DONE, NI, g->idx_dim);
+    if (NQ % 64 || NI % 64) return set_error(MK_ERR_UNSUPPORTED, "Q-B / Indexer-Q widths must be multiples of 64");
+    for (auto &t : p.tasks) {
+        for (int i = 0; i < t.nw; ++i) t.w_thr[i] = p.thresholds[t.w_ev[i]];
+        if (t.opcode == MK_OP_GLM_A0) {  // the previous step's last tasks
+            t.w_ev[t.nw] = EV_DONE; t.w_thr[t.nw] = p.thresholds[EV_DONE]; t.w_off[t.nw++] = -1;
+        }
+    }
+    // RoPE table: angle (pos0 + j) * theta^(-i/32) of token j and pair i, in double
+    for (int j = 0; j < g->tokens; ++j)
+        for (int i = 0; i < GLM_ROPE / 2; ++i) {
+            const double a = (double)(g->pos0 + j) * std::pow((double)g->rope_theta, -(double)i / (GLM_ROPE / 2));
+            p.rope_tab.push_back((float)std::cos(a));
+            p.rope_tab.push_back((float)std::sin(a));
+        }
+    p.events.assign(NEV, {0, 0, 0});
+    for (int e = 0; e < NEV; ++e) p.events[e].ntrig = p.thresholds[e];
+    // algorithmic bytes: FP8 weights and their scales once; the block's inputs,
+    // outputs and cache rows; each intermediate written and read once
+    const int64_t KBH = H / 128, KBQ = QL / 128;
+    const int64_t wbytes = (int64_t)(NQKVA + g->gate_heads + g->idx_dim) * H + (int64_t)(NQ + NI) * QL;
+    const int64_t sbytes = 4 * (ceil_div(NQKVA, 128) + ceil_div(g->gate_heads, 128) + ceil_div(g->idx_dim, 128)) * KBH +
+                           4 * (ceil_div(NQ, 128) + ceil_div(NI, 128)) * KBQ;
+    const int64_t io = (int64_t)M * H * 2 * 3 + H * 2 + (int64_t)M * (g->gate_heads + NQ + NI) * 2 +
+                       (int64_t)M * (KL + R + g->idx_dim) * 2;
+    const int64_t inter = (int64_t)M * (H + KBH * 4 + (NQKVA + g->idx_dim) * 2 + QL + KBQ * 4);
+    p.alg_bytes = wbytes + sbytes + io + inter;
     return finish_queues(p, false, p.schedule == MK_SCHED_TIMED);
 }
 

@@ -9,7 +9,7 @@
 
 namespace mk {
 
-enum { PLAN_LLAMA = 0, PLAN_GRAPH = 1 };
+enum { PLAN_LLAMA = 0, PLAN_GRAPH = 1, PLAN_GLM = 2 };
 
 struct TaskRec {
     int opcode = MK_OP_COUNTER;
@@ -36,6 +36,8 @@ struct Plan {
     int kind = PLAN_GRAPH;
     int mode = MK_MODE_MEGAKERNEL;
     mk_model_desc model{};
+    mk_glm_desc glm{};           // PLAN_GLM
+    std::vector<float> rope_tab;  // PLAN_GLM: (cos, sin) [tokens][32] of each new position
     int num_workers = 0, B = 1, max_steps = 1, smax = 0;
     bool capture = false;
     std::vector<int> seq0;
@@ -57,7 +59,7 @@ struct Plan {
     std::vector<std::vector<uint64_t>> bind;
     // workspace layout (byte offsets) and upload state
     struct {
-        uint64_t err, counters, arrive, queue, optab, seq0, hres, hmid, qkv, part, attn_out, act, trace, total;
+        uint64_t err, counters, arrive, queue, optab, seq0, rope, hres, hmid, qkv, part, attn_out, act, trace, total;
     } ws{};
     void *uploaded_ws = nullptr;
     bool table_dirty = true;
@@ -69,6 +71,7 @@ extern thread_local std::string g_last_error;
 int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_desc *tgt, int num_workers,
                int smem_per_cta, Plan &p);
 int plan_graph(const mk_graph_desc *g, const mk_target_desc *tgt, int num_workers, Plan &p);
+int plan_glm(const mk_glm_desc *g, const mk_target_desc *tgt, int num_workers, int smem_per_cta, Plan &p);
 void layout_workspace(Plan &p);
 
 }  // namespace mk

@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmk.so")
 # ---- constants mirrored from include/mk.h ----
 MK_OK, MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_DEADLOCK, MK_ERR_CUDA = 0, 1, 2, 3, 4
 MK_ERR_RESIDENCY, MK_ERR_TIMEOUT, MK_ERR_DEVICE_CHECK, MK_ERR_UNBOUND = 5, 6, 7, 8
-OP_NAMES = {0: "noop", 1: "counter", 2: "embed", 3: "qkv", 4: "attn", 5: "o", 6: "up", 7: "down", 8: "lm"}
+OP_NAMES = {0: "noop", 1: "counter", 2: "embed", 3: "qkv", 4: "attn", 5: "o", 6: "up", 7: "down", 8: "lm",
+            9: "glm_a0", 10: "glm_gemm", 11: "glm_fin"}
 OPCODE = {v: k for k, v in OP_NAMES.items()}
 MODE_MEGAKERNEL, MODE_PER_OP = 0, 1
 SCHED_DEFAULT, SCHED_BYTES, SCHED_TIMED = 0, 1, 2
@@ -29,12 +30,16 @@ PAIR_WHOLE, PAIR_TILE, PAIR_TILE_COVER, PAIR_TILE_REDUCE = 0, 1, 2, 3
 TASK_FIELDS = 24
 BIND = {n: i for i, n in enumerate([
     "embed", "lm_head", "norm_final", "wq", "wk", "wv", "wo", "wg", "wu", "wd", "norm_attn", "norm_mlp",
-    "qnorm", "knorm", "kcache", "vcache", "tokens", "logits", "argmax", "hidden"])}
+    "qnorm", "knorm", "kcache", "vcache", "tokens", "logits", "argmax", "hidden",
+    # GLM pre-attention block
+    "glm_x", "glm_res", "glm_norm", "glm_res_out", "glm_qa", "glm_sa", "glm_w_qkva", "glm_s_qkva", "glm_w_gate",
+    "glm_s_gate", "glm_w_ik", "glm_s_ik", "glm_w_qb", "glm_s_qb", "glm_w_iq", "glm_s_iq", "glm_qkva", "glm_ik",
+    "glm_qb", "glm_sb", "glm_gate", "glm_q", "glm_iq", "glm_latent", "glm_index"])}
 PER_LAYER = ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "norm_attn", "norm_mlp", "qnorm", "knorm")
 
 EXPORTED = ["mk_plan", "mk_plan_graph", "mk_plan_info_get", "mk_plan_export", "mk_bind", "mk_run",
             "mk_sync_status", "mk_read_counters", "mk_read_trace", "mk_free", "mk_last_error", "mk_argmax_index",
-            "mk_run_static"]
+            "mk_run_static", "mk_plan_glm"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 
@@ -60,6 +65,12 @@ class TargetDesc(C.Structure):
                 ("rows_o", C.c_int), ("rows_up", C.c_int), ("rows_down", C.c_int), ("kchunk_down", C.c_int),
                 ("rows_lm", C.c_int), ("attn_split", C.c_int), ("page_bytes", C.c_int),
                 ("schedule", C.c_int)]
+
+
+class GlmDesc(C.Structure):
+    _fields_ = [(n, C.c_int) for n in (
+        "requests", "tokens", "hidden", "q_lora", "kv_lora", "rope", "q_heads", "q_head_dim", "gate_heads",
+        "idx_heads", "idx_dim", "cache_slots", "pos0", "max_steps")] + [("eps", C.c_float), ("rope_theta", C.c_float)]
 
 
 class PlanInfo(C.Structure):
@@ -109,6 +120,7 @@ def load():
     P = C.c_void_p
     lib.mk_plan.argtypes = [C.POINTER(ModelDesc), C.POINTER(StepDesc), C.POINTER(TargetDesc), C.POINTER(P)]
     lib.mk_plan_graph.argtypes = [C.POINTER(GraphDesc), C.POINTER(TargetDesc), C.POINTER(P)]
+    lib.mk_plan_glm.argtypes = [C.POINTER(GlmDesc), C.POINTER(TargetDesc), C.POINTER(P)]
     lib.mk_plan_info_get.argtypes = [P, C.POINTER(PlanInfo)]
     lib.mk_plan_export.argtypes = [P, P, P, P, P]
     lib.mk_bind.argtypes = [P, C.c_int, C.c_int, C.c_uint64]
@@ -179,6 +191,18 @@ class Plan:
         t = _target(**target)
         out = C.c_void_p()
         _check(lib.mk_plan_graph(C.byref(g), C.byref(t), C.byref(out)))
+        return cls(out.value)
+
+    @classmethod
+    def glm(cls, dims, max_steps: int = 1, **target):
+        """Plan the GLM pre-attention block; ``dims`` has the fields of ``mk_glm_desc``."""
+        lib = load()
+        d = GlmDesc(dims.R, dims.T, dims.H, dims.qlora, dims.kvlora, dims.rope, dims.q_heads, dims.q_head_dim,
+                    dims.gate_heads, dims.idx_heads, dims.idx_dim, dims.slots, dims.pos0, max_steps, dims.eps,
+                    dims.theta)
+        t = _target(**target)
+        out = C.c_void_p()
+        _check(lib.mk_plan_glm(C.byref(d), C.byref(t), C.byref(out)))
         return cls(out.value)
 
     def info(self) -> dict:
@@ -294,6 +318,66 @@ class Session:
         """Argmax token of every sequence at ``step`` (after sync)."""
         keys = self.argmax[step].cpu().numpy().view(np.uint64)
         return argmax_index(keys)
+
+    def counters(self) -> np.ndarray:
+        out = np.zeros(self.plan.info()["num_events"], np.uint32)
+        _check(load().mk_read_counters(self.plan.h, C.c_void_p(self.ws_ptr), out.ctypes.data))
+        return out
+
+    def trace(self) -> np.ndarray:
+        i = self.plan.info()
+        out = np.zeros((i["num_workers"], i["lmax"], 16), np.uint64)
+        _check(load().mk_read_trace(self.plan.h, C.c_void_p(self.ws_ptr), out.ctypes.data))
+        return out
+
+
+class GlmSession:
+    """Device state of the GLM pre-attention block: inputs and FP8 weights from
+    ``synth.make_glm_inputs`` (torch CUDA tensors), every output and
+    intermediate, and the workspace."""
+
+    OUTPUTS = ("res_out", "qa", "sa", "qkva", "ik", "qb", "sb", "gate", "q", "iq")
+
+    def __init__(self, dims, inputs: Dict[str, object], max_steps: int = 1, stream=None, **target):
+        import torch
+        self.dims = dims
+        dev = inputs["x"].device
+        self.plan = Plan.glm(dims, max_steps, **target)
+        info = self.plan.info()
+        M, H, QL = dims.M, dims.H, dims.qlora
+        NQKVA = dims.qlora + dims.kvlora + dims.rope
+        bf, u8, f32 = torch.bfloat16, torch.uint8, torch.float32
+        z = lambda shape, dt: torch.zeros(shape, dtype=dt, device=dev)
+        self.out = dict(res_out=z((M, H), bf), qa=z((M, H), u8), sa=z((M, H // 128), f32), qkva=z((M, NQKVA), bf),
+                        ik=z((M, dims.idx_dim), bf), qb=z((M, QL), u8), sb=z((M, QL // 128), f32),
+                        gate=z((M, dims.gate_heads), bf), q=z((M, dims.q_heads, dims.q_head_dim), bf),
+                        iq=z((M, dims.idx_heads, dims.idx_dim), bf))
+        self.inputs = inputs
+        self.latent = inputs["latent"]
+        self.index = inputs["index"]
+        self.workspace = torch.zeros(info["workspace_bytes"] + 256, dtype=torch.uint8, device=dev)
+        self.ws_ptr = self.workspace.data_ptr() + (-self.workspace.data_ptr()) % 256
+        self.ws_bytes = info["workspace_bytes"]
+        p = self.plan
+        for n in ("x", "res", "norm", "w_qkva", "s_qkva", "w_gate", "s_gate", "w_ik", "s_ik", "w_qb", "s_qb",
+                  "w_iq", "s_iq", "latent", "index"):
+            p.bind("glm_" + n, inputs[n].data_ptr())
+        for n, t in self.out.items():
+            p.bind("glm_" + n, t.data_ptr())
+        self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
+
+    def run(self, first_step: int = 0, num_steps: int = 1, trace: bool = False, timeout_ns: int = 0):
+        flags = RUN_TRACE if trace else 0
+        _check(load().mk_run(self.plan.h, C.c_void_p(self.ws_ptr), self.ws_bytes, first_step, num_steps, flags,
+                             timeout_ns, C.c_void_p(self.stream.cuda_stream)))
+
+    def sync(self) -> ErrorRecord:
+        rec = ErrorRecord()
+        rc = load().mk_sync_status(self.plan.h, C.c_void_p(self.ws_ptr), C.c_void_p(self.stream.cuda_stream),
+                                   C.byref(rec))
+        if rc != MK_OK:
+            raise MkError(rc, load().mk_last_error().decode())
+        return rec
 
     def counters(self) -> np.ndarray:
         out = np.zeros(self.plan.info()["num_events"], np.uint32)

@@ -9,6 +9,13 @@ Recipe: weights bf16 N(0, 0.02) (norm weights 1), KV caches bf16 N(0, 1),
 tokens uniform over the vocabulary, batch-8 cache lengths uniform in
 [512, 4096]; seeds 1234 + workload index for weights, +100 for caches,
 +200 for tokens and lengths.  There are no trained weights and no dataset.
+
+GLM pre-attention block (workload index 3): activations and residual bf16
+N(0, 1); weights fp32 N(0, 0.02), stored as e4m3 bytes with one fp32 scale
+per 128 x 128 block (scale = block amax / 448, bytes from torch's own
+float8_e4m3fn conversion of weight / scale) -- the block's weights arrive
+quantised, so this is input preparation, not a step of the block; caches
+bf16 N(0, 1).
 """
 from __future__ import annotations
 
@@ -126,6 +133,69 @@ def make_cache(shape: ModelShape, batch: int, smax: int, seed: int, device="cpu"
     g = torch.Generator(device=device).manual_seed(seed)
     dims = (shape.L, batch, shape.Hkv, smax, shape.D)
     return _randn(dims, g, device), _randn(dims, g, device)
+
+
+@dataclass(frozen=True)
+class GlmDims:
+    """GLM-5.2-FP8 decode before sparse attention: 2 requests x 8 new tokens,
+    hidden 6144, QKV-A 1536 + 512 + 64, Head-Gate 64, Indexer-K 128, Q-B
+    64 x 192, Indexer-Q 32 x 128, caches of 8192 slots."""
+    R: int = 2
+    T: int = 8
+    H: int = 6144
+    qlora: int = 1536
+    kvlora: int = 512
+    rope: int = 64
+    q_heads: int = 64
+    q_head_dim: int = 192
+    gate_heads: int = 64
+    idx_heads: int = 32
+    idx_dim: int = 128
+    slots: int = 8192
+    eps: float = 1e-6
+    theta: float = 1e4
+
+    @property
+    def M(self):
+        return self.R * self.T
+
+    @property
+    def pos0(self):
+        return self.slots - self.T
+
+
+GLM = GlmDims()
+GLM_INDEX = 3
+GLM_MATS = ("qkva", "gate", "ik", "qb", "iq")
+
+
+def glm_mat_shapes(d: GlmDims) -> Dict[str, tuple]:
+    return {"qkva": (d.qlora + d.kvlora + d.rope, d.H), "gate": (d.gate_heads, d.H), "ik": (d.idx_dim, d.H),
+            "qb": (d.q_heads * d.q_head_dim, d.qlora), "iq": (d.idx_heads * d.idx_dim, d.qlora)}
+
+
+def make_glm_inputs(d: GlmDims, device="cpu", index: int = GLM_INDEX) -> Dict[str, torch.Tensor]:
+    """x, res, norm, w_<mat> (uint8 e4m3 [N, K]), s_<mat> (fp32 [ceil(N/128), K/128]), latent, index caches."""
+    gw = torch.Generator(device="cpu").manual_seed(1234 + index)
+    ga = torch.Generator(device="cpu").manual_seed(1234 + index + 200)
+    gc = torch.Generator(device="cpu").manual_seed(1234 + index + 100)
+    out: Dict[str, torch.Tensor] = {}
+    out["x"] = torch.randn((d.M, d.H), generator=ga).to(torch.bfloat16)
+    out["res"] = torch.randn((d.M, d.H), generator=ga).to(torch.bfloat16)
+    out["norm"] = torch.ones(d.H, dtype=torch.bfloat16)
+    for name, (n, k) in glm_mat_shapes(d).items():
+        w = torch.randn((n, k), generator=gw) * 0.02
+        nb = (n + 127) // 128
+        wp = torch.zeros((nb * 128, k))
+        wp[:n] = w
+        amax = wp.view(nb, 128, k // 128, 128).abs().amax(dim=(1, 3))
+        scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).float()
+        q = (wp.view(nb, 128, k // 128, 128) / scale[:, None, :, None]).view(nb * 128, k)[:n]
+        out["w_" + name] = q.to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+        out["s_" + name] = scale.contiguous()
+    out["latent"] = torch.randn((d.R, d.slots, d.kvlora + d.rope), generator=gc).to(torch.bfloat16)
+    out["index"] = torch.randn((d.R, d.slots, d.idx_dim), generator=gc).to(torch.bfloat16)
+    return {k: v.to(device) for k, v in out.items()}
 
 
 def to_host_u16(t: torch.Tensor):
