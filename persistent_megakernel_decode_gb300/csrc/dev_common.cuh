@@ -459,6 +459,9 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
             return false;
         if (GLM_MAX_M * (kc + 16) + GLM_MAX_M * (kc / 128) * 4 > P.abuf_bytes || GLM_MAX_M * 64 * 4 > P.red_bytes)
             return false;
+        // each warp's K blocks: at most 32 (their weight scales sit one per lane)
+        const int ks = CONSUMER_WARPS / (nr / 8);
+        if ((kc / 128 + ks - 1) / ks > 32) return false;
         return F(I, P_GL_LD) >= F(I, P_OUT0) + nr && F(I, P_OUT0) >= 0 && (F(I, P_GL_ROPE) == 0 || nr == 64);
     }
     if (opc >= MK_OP_QKV && opc <= MK_OP_LM && opc != MK_OP_ATTN) {

@@ -53,11 +53,17 @@ DEV uint32_t quant4(const float (&v)[4], float &scale) {
     return e4m3x2(v[0] / scale, v[1] / scale) | (e4m3x2(v[2] / scale, v[3] / scale) << 16);
 }
 
+// trace stamp k of slot i (traced runs only; consumer thread 0)
+DEV void glm_stamp(const KParams &P, int i, int k) {
+    if (P.trace && threadIdx.x == 64) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + k] = gtimer();
+}
+
 // ---------------------------------------------------------------- A0
 // One token row m: h = x + res (the new residual, bf16), RMSNorm of those
 // bf16 values, then per 128 columns e4m3 codes and a scale.  Warp w takes the
 // 128-column blocks w, w + 8, ...; lane l columns 4l .. 4l + 3 of each.
-__device__ __noinline__ void glm_a0_task(const KParams &P, const Smem S, const WIns &I, uint32_t &ured, bool ab) {
+DEV void glm_a0_task(const KParams &P, const Smem S, const WIns &I, int i, uint32_t &ured,
+                                         bool ab) {
     constexpr int BPW = 8;  // blocks per warp: hidden <= 8192
     const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
     const int m = F(I, P_ROW0), H = P.H, nb = H >> 7;
@@ -67,26 +73,33 @@ __device__ __noinline__ void glm_a0_task(const KParams &P, const Smem S, const W
     uint8_t *rout = reinterpret_cast<uint8_t *>(PTR(I, S_GA_RES_OUT)) + (size_t)m * H * 2;
     uint8_t *qa = reinterpret_cast<uint8_t *>(PTR(I, S_GA_QA)) + (size_t)m * H;
     float *sa = reinterpret_cast<float *>(PTR(I, S_GA_SA)) + (size_t)m * nb;
+    // every load first (one round trip), then the arithmetic
+    uint2 xv[BPW], rv[BPW], wv[BPW];
+#pragma unroll
+    for (int j = 0; j < BPW; ++j) {
+        const int blk = warp + CONSUMER_WARPS * j, col = blk * 128 + lane * 4;
+        const bool in = blk < nb;
+        xv[j] = in ? __ldg(reinterpret_cast<const uint2 *>(x + col * 2)) : make_uint2(0u, 0u);
+        rv[j] = in ? __ldg(reinterpret_cast<const uint2 *>(res + col * 2)) : make_uint2(0u, 0u);
+        wv[j] = in ? __ldg(reinterpret_cast<const uint2 *>(nw + col * 2)) : make_uint2(0u, 0u);
+    }
     float h[BPW][4];
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < BPW; ++j) {
         const int blk = warp + CONSUMER_WARPS * j, col = blk * 128 + lane * 4;
-        if (blk < nb) {
-            const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(x + col * 2));
-            const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(res + col * 2));
-            h[j][0] = round_bf16(bf16_lo(xv.x) + bf16_lo(rv.x));
-            h[j][1] = round_bf16(bf16_hi(xv.x) + bf16_hi(rv.x));
-            h[j][2] = round_bf16(bf16_lo(xv.y) + bf16_lo(rv.y));
-            h[j][3] = round_bf16(bf16_hi(xv.y) + bf16_hi(rv.y));
-            if (!ab)
-                *reinterpret_cast<uint2 *>(rout + col * 2) =
-                    make_uint2(pack_bf16(h[j][0], h[j][1]), pack_bf16(h[j][2], h[j][3]));
+        h[j][0] = round_bf16(bf16_lo(xv[j].x) + bf16_lo(rv[j].x));
+        h[j][1] = round_bf16(bf16_hi(xv[j].x) + bf16_hi(rv[j].x));
+        h[j][2] = round_bf16(bf16_lo(xv[j].y) + bf16_lo(rv[j].y));
+        h[j][3] = round_bf16(bf16_hi(xv[j].y) + bf16_hi(rv[j].y));
+        if (blk < nb && !ab)
+            *reinterpret_cast<uint2 *>(rout + col * 2) =
+                make_uint2(pack_bf16(h[j][0], h[j][1]), pack_bf16(h[j][2], h[j][3]));
 #pragma unroll
-            for (int e = 0; e < 4; ++e) ss = fmaf(h[j][e], h[j][e], ss);
-        }
+        for (int e = 0; e < 4; ++e) ss = fmaf(h[j][e], h[j][e], ss);  // zero past the row's end
     }
     ss = warp_sum(ss);
+    glm_stamp(P, i, 9);
     float *red = S.red((int)(ured % NRED));
     ++ured;
     if (lane == 0) red[warp] = ss;
@@ -95,13 +108,13 @@ __device__ __noinline__ void glm_a0_task(const KParams &P, const Smem S, const W
 #pragma unroll
     for (int k = 0; k < CONSUMER_WARPS; ++k) tot += red[k];
     const float r = rsqrtf(tot / (float)H + P.eps);
+    glm_stamp(P, i, 10);
 #pragma unroll
     for (int j = 0; j < BPW; ++j) {
         const int blk = warp + CONSUMER_WARPS * j, col = blk * 128 + lane * 4;
         if (blk < nb) {  // warp-uniform
-            const uint2 wv = __ldg(reinterpret_cast<const uint2 *>(nw + col * 2));
-            const float y[4] = {h[j][0] * r * bf16_lo(wv.x), h[j][1] * r * bf16_hi(wv.x),
-                                h[j][2] * r * bf16_lo(wv.y), h[j][3] * r * bf16_hi(wv.y)};
+            const float y[4] = {h[j][0] * r * bf16_lo(wv[j].x), h[j][1] * r * bf16_hi(wv[j].x),
+                                h[j][2] * r * bf16_lo(wv[j].y), h[j][3] * r * bf16_hi(wv[j].y)};
             float scale;
             const uint32_t codes = quant4(y, scale);
             if (!ab) {
@@ -127,7 +140,7 @@ __device__ __noinline__ void glm_a0_task(const KParams &P, const Smem S, const W
 // memory by the activation loader ([16][K + 16] codes, then [16][K / 128]
 // scales); weight rows come from the tile's pages, whole rows per page.
 template <int NR>
-__device__ __noinline__ void glm_gemm_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, uint32_t &ring, uint32_t &ured,
+DEV void glm_gemm_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, uint32_t &ring, uint32_t &ured,
                        bool &ab) {
     constexpr int NG = NR / 8, KS = CONSUMER_WARPS / NG;
     const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
@@ -145,12 +158,14 @@ __device__ __noinline__ void glm_gemm_task(const KParams &P, const Smem S, const
     const float *sa = reinterpret_cast<const float *>(abuf + GLM_MAX_M * astride);
     for (int k = 0; k < npg; ++k)
         if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(base + k) % NP], ((base + k) / NP) & 1, 2, i, MK_OP_GLM_GEMM);
+    glm_stamp(P, i, 7);
     const int r = gi * 8 + g;
     const uint8_t *wrow = S.pages() + (size_t)((base + r / rpp) % NP) * P.page_bytes + (size_t)(r % rpp) * K;
     const bool lo_ok = g < M, hi_ok = g + 8 < M;
     const uint8_t *alo = abuf + g * astride, *ahi = abuf + (g + 8) * astride;
     const int kb0 = ks * KB / KS, kb1 = (ks + 1) * KB / KS;
-    const float *swr = sw + (size_t)((n0 + gi * 8) >> 7) * KB;
+    // the weight scales of this warp's K blocks (at most 32), one per lane
+    const float swl = lane < kb1 - kb0 ? __ldg(sw + (size_t)((n0 + gi * 8) >> 7) * KB + kb0 + lane) : 0.f;
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int kb = kb0; kb < kb1; ++kb) {
@@ -164,7 +179,7 @@ __device__ __noinline__ void glm_gemm_task(const KParams &P, const Smem S, const
             mma_e4m3(cb, a.x, b.x, a.y, b.y, w.x, w.y);
             mma_e4m3(cb, a.z, b.z, a.w, b.w, w.z, w.w);
         }
-        const float swv = __ldg(swr + kb);
+        const float swv = __shfl_sync(FULL, swl, kb - kb0);
         const float s0 = lo_ok ? sa[g * KB + kb] * swv : 0.f;
         const float s1 = hi_ok ? sa[(g + 8) * KB + kb] * swv : 0.f;
         acc[0] = fmaf(s0, cb[0], acc[0]);
@@ -173,6 +188,7 @@ __device__ __noinline__ void glm_gemm_task(const KParams &P, const Smem S, const
         acc[3] = fmaf(s1, cb[3], acc[3]);
     }
     __syncwarp();
+    glm_stamp(P, i, 9);
     if (lane == 0) {
         for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(base + k) % NP]);
         mbar_arrive(&S.act_empty()[sl]);  // staged rows no longer needed by this warp
@@ -188,6 +204,7 @@ __device__ __noinline__ void glm_gemm_task(const KParams &P, const Smem S, const
     pr[(g + 8) * NR + n] = acc[2];
     pr[(g + 8) * NR + n + 1] = acc[3];
     consumer_bar();
+    glm_stamp(P, i, 10);
     if (ab) return;
     for (int e = ct; e < M * NR; e += CONSUMERS) {
         const int m = e / NR, c = e % NR;
@@ -211,7 +228,7 @@ __device__ __noinline__ void glm_gemm_task(const KParams &P, const Smem S, const
 // columns 0 .. QL-1) re-quantised per 128 columns, one warp per block; the
 // latent cache row = kv-lora || RoPE(k_pe); the index cache row = Indexer-K
 // with RoPE on its last 64 columns.
-__device__ __noinline__ void glm_fin_task(const KParams &P, const WIns &I, bool ab) {
+DEV void glm_fin_task(const KParams &P, const WIns &I, bool ab) {
     const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
     const int m = F(I, P_ROW0), QL = F(I, P_GF_QLORA), KL = F(I, P_GF_KVLORA), ID = F(I, P_GF_IDX);
     const int slots = F(I, P_GF_SLOTS), LDQ = F(I, P_GF_QKVA_LD), T = F(I, P_GL_T), pos0 = F(I, P_GL_POS0);
@@ -223,6 +240,15 @@ __device__ __noinline__ void glm_fin_task(const KParams &P, const WIns &I, bool 
     __nv_bfloat16 *idx = reinterpret_cast<__nv_bfloat16 *>(PTR(I, S_GF_IDX));
     const float2 *rtab = reinterpret_cast<const float2 *>(PTR(I, S_GF_ROPE));
     const int req = m / T, j = m % T, slot = pos0 + j;
+    // RoPE pairs: threads 0-31 the k_pe slice, 32-63 Indexer-K's last 64 (loaded first)
+    const int p = ct & 31;
+    float lo = 0.f, hi = 0.f;
+    if (ct < 64) {
+        const __nv_bfloat16 *src = ct < 32 ? qkva + QL + KL : ik + ID - GLM_ROPE;
+        const unsigned short *s16 = reinterpret_cast<const unsigned short *>(src);
+        lo = __uint_as_float((uint32_t)__ldcg(s16 + p) << 16);
+        hi = __uint_as_float((uint32_t)__ldcg(s16 + p + 32) << 16);
+    }
     for (int blk = warp; blk < (QL >> 7); blk += CONSUMER_WARPS) {
         const int col = blk * 128 + lane * 4;
         const uint2 u = __ldcg(reinterpret_cast<const uint2 *>(qkva + col));
@@ -241,14 +267,8 @@ __device__ __noinline__ void glm_fin_task(const KParams &P, const WIns &I, bool 
     __nv_bfloat16 *irow = idx + ((size_t)req * slots + slot) * ID;
     for (int e = ct * 2; e < ID - GLM_ROPE; e += 2 * CONSUMERS)
         *reinterpret_cast<uint32_t *>(irow + e) = __ldcg(reinterpret_cast<const uint32_t *>(ik + e));
-    // RoPE pairs: threads 0-31 the k_pe slice, 32-63 Indexer-K's last 64
     if (ct < 64) {
-        const int p = ct & 31;
-        const __nv_bfloat16 *src = ct < 32 ? qkva + QL + KL : ik + ID - GLM_ROPE;
         __nv_bfloat16 *dst = ct < 32 ? lrow + KL : irow + ID - GLM_ROPE;
-        const unsigned short *s16 = reinterpret_cast<const unsigned short *>(src);
-        const float lo = __uint_as_float((uint32_t)__ldcg(s16 + p) << 16);
-        const float hi = __uint_as_float((uint32_t)__ldcg(s16 + p + 32) << 16);
         const float2 cs = rtab[j * 32 + p];
         dst[p] = __float2bfloat16_rn(lo * cs.x - hi * cs.y);
         dst[p + 32] = __float2bfloat16_rn(hi * cs.x + lo * cs.y);
@@ -260,7 +280,7 @@ __device__ __noinline__ void glm_fin_task(const KParams &P, const WIns &I, bool 
 // copies of the M activation rows (into rows of K + 16 bytes) and of their
 // scales into the activation buffer, completing on the slot's full barrier.
 // Returns the bytes in flight (0 if the buffer already holds this input).
-__device__ __noinline__ uint32_t stage_glm(const KParams &P, const WIns &I, uint8_t *abuf, uint64_t *full) {
+DEV uint32_t stage_glm(const KParams &P, const WIns &I, uint8_t *abuf, uint64_t *full) {
     const int lane = threadIdx.x & 31;
     const int K = F(I, P_KC), M = F(I, P_GL_M);
     const uint8_t *xq = reinterpret_cast<const uint8_t *>(PTR(I, S_GG_XQ));

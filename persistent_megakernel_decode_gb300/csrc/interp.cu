@@ -374,7 +374,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         } else if (GLM && (opc == MK_OP_GLM_A0 || opc == MK_OP_GLM_FIN)) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // the slot holds nothing for these
-            if (opc == MK_OP_GLM_A0) glm_a0_task(P, S, I, ured, ab);
+            if (opc == MK_OP_GLM_A0) glm_a0_task(P, S, I, i, ured, ab);
             else glm_fin_task(P, I, ab);
         } else if (opc >= MK_OP_QKV) {
             if (MAXB == 1 && rpw_tile(P, d)) {  // (a constant condition for larger batches)
@@ -405,7 +405,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
 
 // ---------------------------------------------------------------- kernel
 template <int MAXB, bool GLM>
-__global__ void __launch_bounds__(THREADS, 1) mk_interp(__grid_constant__ const KParams P) {
+__global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
     Smem S;
     S.o_abuf = 0;
     S.abuf_stride = P.abuf_count > 1 ? P.abuf_bytes : 0;
