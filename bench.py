@@ -42,7 +42,7 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("interp.cu", "dev_common.cuh", "dev_ops.cuh", "mk_internal.h", "planner.cpp"):
+    for f in ("interp.cu", "dev_common.cuh", "dev_ops.cuh", "dev_glm.cuh", "mk_internal.h", "planner.cpp"):
         with open(os.path.join(ROOT, "persistent_megakernel_decode_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -275,6 +275,155 @@ def run_mk(args, w, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def run_glm(args, rank, world, dist):
+    """The GLM FP8 pre-attention block (M = 16 = 2 requests x 8 tokens,
+    hidden 6144, 39.3 MB of e4m3 weights).  The weights fit in L2, so every
+    timed step runs cold: an L2-sized buffer is overwritten before it, outside
+    its events.  Warm figures are reported beside."""
+    import torch
+    from persistent_megakernel_decode_gb300 import build, runtime as rt, synth
+    build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = synth.GLM
+    steps_total = args.warmup + 2 * args.steps + 40
+    inp = {k: v.to(dev) for k, v in synth.make_glm_inputs(d).items()}
+    stream = torch.cuda.Stream(dev)
+    target = {}
+    for kv in args.knob:
+        k, v = kv.split("=")
+        target[k] = int(v)
+    sess = rt.GlmSession(d, inp, max_steps=steps_total, stream=stream, **target)
+    info = sess.plan.info()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for st in range(args.warmup):
+            sess.run(st, 1)
+    sess.sync()
+    step = args.warmup
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.fill_(i & 0xff)
+                ev[i][0].record(stream)
+                sess.run(step, 1)
+                ev[i][1].record(stream)
+                step += 1
+        stream.synchronize()
+    cold_ms = np.array([a.elapsed_time(b) for a, b in ev])
+    # warm: back to back, weights L2-resident
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        sess.run(step, args.steps)
+        e1.record(stream)
+    stream.synchronize()
+    step += args.steps
+    warm_ms = e0.elapsed_time(e1) / args.steps
+    rec = sess.sync()
+    total_ms = float(cold_ms.sum())
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = d.M * args.steps * world / (total_ms / 1e3)
+    # end to end: x and residual from pinned host memory in, Q-B / Indexer-Q / Head-Gate out
+    hx = inp["x"].cpu().pin_memory()
+    hres = inp["res"].cpu().pin_memory()
+    outs = [sess.out[k] for k in ("q", "iq", "gate")]
+    hout = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    e2e_steps = 20
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            inp["x"].copy_(hx, non_blocking=True)
+            inp["res"].copy_(hres, non_blocking=True)
+            sess.run(step, 1)
+            step += 1
+            for o, h in zip(outs, hout):
+                h.copy_(o, non_blocking=True)
+            stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": d.M * e2e_steps / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": 2 * hx.numel() * 2, "d2h_bytes_per_step": sum(h.numel() * 2 for h in hout),
+           "steps": e2e_steps}
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    alg = info["algorithmic_bytes_step"]
+    achieved = alg / (float(np.mean(cold_ms)) / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profiled_traffic("glm52_preattn_m16"), "peak_kind": peak_kind,
+                "algorithmic_bytes_per_launch": alg, "kernel": "mk_interp (GLM instance)",
+                "nominal_8tbs_frac": achieved / 8000.0}
+    cpu = None
+    if not args.no_cpu_baseline:
+        from oracle import glm
+        sh = glm.GlmShape(R=d.R, T=d.T, H=d.H, qlora=d.qlora, kvlora=d.kvlora, rope=d.rope, q_heads=d.q_heads,
+                          q_head_dim=d.q_head_dim, gate_heads=d.gate_heads, idx_heads=d.idx_heads,
+                          idx_dim=d.idx_dim, slots=d.slots, eps=d.eps, theta=d.theta)
+        f = lambda t: t.detach().cpu().to(torch.float64).numpy()
+        wts = {}
+        for n in synth.GLM_MATS:
+            wts[n] = inp["w_" + n].cpu().numpy()
+            wts[n + "_s"] = inp["s_" + n].cpu().numpy()
+        t0 = time.perf_counter()
+        glm.forward(sh, f(inp["x"]), f(inp["res"]), f(inp["norm"]), wts)
+        cpu_s = time.perf_counter() - t0
+        cpu = {"value": d.M / cpu_s, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": "one forward of the block (numpy fp64 oracle)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
+        "config": {"workload": "glm52_preattn_m16", "requests": d.R, "tokens": d.T, "hidden": d.H,
+                   "cache_slots": d.slots, "l2": "weights (39.3 MB) fit in L2: a 256 MB buffer is overwritten "
+                   "before every timed step, outside its events", "parallelism": f"replicas{world}"},
+        "step_us": {"median": float(np.median(cold_ms)) * 1e3, "p10": float(np.percentile(cold_ms, 10)) * 1e3,
+                    "p90": float(np.percentile(cold_ms, 90)) * 1e3, "warm_mean": warm_ms * 1e3},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(),
+        "gpu_launches": args.steps * info["num_launches"],
+        "plan": {k: info[k] for k in ("num_workers", "lmax", "num_tasks", "num_events", "num_pages", "smem_bytes")},
+        "device_error": int(rec.code),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_glm_reference(args):
+    """The numpy fp64 oracle of the GLM block on the host cores, a bounded sample of steps."""
+    import torch
+    from oracle import glm
+    from persistent_megakernel_decode_gb300 import synth
+    d = synth.GLM
+    inp = synth.make_glm_inputs(d)
+    sh = glm.GlmShape(R=d.R, T=d.T, H=d.H, qlora=d.qlora, kvlora=d.kvlora, rope=d.rope, q_heads=d.q_heads,
+                      q_head_dim=d.q_head_dim, gate_heads=d.gate_heads, idx_heads=d.idx_heads, idx_dim=d.idx_dim,
+                      slots=d.slots, eps=d.eps, theta=d.theta)
+    f = lambda t: t.to(torch.float64).numpy()
+    wts = {}
+    for n in synth.GLM_MATS:
+        wts[n] = inp["w_" + n].numpy()
+        wts[n + "_s"] = inp["s_" + n].numpy()
+    steps = max(1, min(args.steps, 3))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        glm.forward(sh, f(inp["x"]), f(inp["res"]), f(inp["norm"]), wts)
+    total = time.perf_counter() - t0
+    v = d.M * steps / total
+    print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+                      "steps": steps, "warmup": 0, "ms_per_step": total / steps * 1e3, "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": {"workload": "glm52_preattn_m16"},
+                      "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                       "sample": f"{steps} forwards of the block (numpy fp64 oracle)"},
+                      "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -290,6 +439,16 @@ def main():
     args = ap.parse_args()
     from dataclasses import replace
     from persistent_megakernel_decode_gb300 import synth
+    if args.workload == "glm52_preattn_m16":
+        if args.impl == "reference":
+            if int(os.environ.get("RANK", "0")) == 0:
+                run_glm_reference(args)
+            return
+        rank, world, dist = dist_setup(args.gpus)
+        run_glm(args, rank, world, dist)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     w = synth.WORKLOADS[args.workload]
     if args.layers:
         w = replace(w, name=f"{w.name}_L{args.layers}", shape=replace(w.shape, L=args.layers))
