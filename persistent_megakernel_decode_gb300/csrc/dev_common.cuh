@@ -441,8 +441,8 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
         if ((int)((uint32_t)F(I, W_WAIT + 2 * i) & ~WAIT_PREV_EPOCH) >= P.num_events) return false;
     for (int i = 0; i < ns; ++i)
         if ((uint32_t)F(I, W_SIG + 2 * i) >= (uint32_t)P.num_events) return false;
+    if (GLM != (opc >= MK_OP_GLM_A0) && opc != MK_OP_COUNTER) return false;  // each instance runs its own ops
     if (opc >= MK_OP_GLM_A0) {
-        if constexpr (!GLM) return false;
         const int M = F(I, P_GL_M), T = F(I, P_GL_T);
         if (M <= 0 || M > GLM_MAX_M || T <= 0 || T > GLM_MAX_M || F(I, P_GL_POS0) < 0) return false;
         if (opc == MK_OP_GLM_A0) return F(I, P_ROW0) >= 0 && F(I, P_ROW0) < M && P.H % 128 == 0 && P.H <= 8192;

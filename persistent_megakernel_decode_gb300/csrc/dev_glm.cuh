@@ -167,25 +167,44 @@ DEV void glm_gemm_task(const KParams &P, const Smem S, const WIns &I, int i, int
     // the weight scales of this warp's K blocks (at most 32), one per lane
     const float swl = lane < kb1 - kb0 ? __ldg(sw + (size_t)((n0 + gi * 8) >> 7) * KB + kb0 + lane) : 0.f;
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    // Two K blocks per iteration and one accumulator set per MMA: eight
+    // independent MMAs in flight instead of a chain of four.
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int kb = kb0; kb < kb1; ++kb) {
-        float cb[4] = {0.f, 0.f, 0.f, 0.f};
+    auto block = [&](int kb, float (&c)[4][4]) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int off = kb * 128 + c * 64 + t * 16;
+        for (int h = 0; h < 2; ++h) {
+            const int off = kb * 128 + h * 64 + t * 16;
             const uint4 w = *reinterpret_cast<const uint4 *>(wrow + off);
             const uint4 a = lo_ok ? *reinterpret_cast<const uint4 *>(alo + off) : zero;
             const uint4 b = hi_ok ? *reinterpret_cast<const uint4 *>(ahi + off) : zero;
-            mma_e4m3(cb, a.x, b.x, a.y, b.y, w.x, w.y);
-            mma_e4m3(cb, a.z, b.z, a.w, b.w, w.z, w.w);
+            mma_e4m3(c[2 * h], a.x, b.x, a.y, b.y, w.x, w.y);
+            mma_e4m3(c[2 * h + 1], a.z, b.z, a.w, b.w, w.z, w.w);
         }
+    };
+    auto scale_add = [&](int kb, const float (&c)[4][4]) {
         const float swv = __shfl_sync(FULL, swl, kb - kb0);
         const float s0 = lo_ok ? sa[g * KB + kb] * swv : 0.f;
         const float s1 = hi_ok ? sa[(g + 8) * KB + kb] * swv : 0.f;
-        acc[0] = fmaf(s0, cb[0], acc[0]);
-        acc[1] = fmaf(s0, cb[1], acc[1]);
-        acc[2] = fmaf(s1, cb[2], acc[2]);
-        acc[3] = fmaf(s1, cb[3], acc[3]);
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = (c[0][e] + c[1][e]) + (c[2][e] + c[3][e]);
+        acc[0] = fmaf(s0, v[0], acc[0]);
+        acc[1] = fmaf(s0, v[1], acc[1]);
+        acc[2] = fmaf(s1, v[2], acc[2]);
+        acc[3] = fmaf(s1, v[3], acc[3]);
+    };
+    int kb = kb0;
+    for (; kb + 2 <= kb1; kb += 2) {
+        float c0[4][4] = {}, c1[4][4] = {};
+        block(kb, c0);
+        block(kb + 1, c1);
+        scale_add(kb, c0);
+        scale_add(kb + 1, c1);
+    }
+    if (kb < kb1) {
+        float c0[4][4] = {};
+        block(kb, c0);
+        scale_add(kb, c0);
     }
     __syncwarp();
     glm_stamp(P, i, 9);

@@ -169,23 +169,24 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
         float *slot = reinterpret_cast<float *>(S.act(sl));
         int flags = 0;
         uint32_t tx = 0;  // bytes of bulk copies completing on the slot's full barrier
-        if (opc == MK_OP_ATTN) {
+        if (GLM) {
+            if (opc == MK_OP_GLM_GEMM) {
+                // the tile's activation rows by bulk copies, unless the buffer
+                // already holds them (key: the input's device address)
+                const long long key = (long long)PTR(I, S_GG_XQ);
+                if (key != key0) {
+                    if (hs > 0 && !ab)
+                        ab = !warp_wait_bar(P, S, &S.act_empty()[(hs - 1) & 1], ((hs - 1) >> 1) & 1, 1, i, opc);
+                    if (!ab) tx = stage_glm(P, I, reinterpret_cast<uint8_t *>(S.abuf(0)), &S.act_full()[sl]);
+                    key0 = ab ? -1 : key;
+                }
+            }
+        } else if (opc == MK_OP_ATTN) {
             const bool g4 = P.Hq <= 4 * P.Hkv;
             if (P.D == 64) g4 ? stage_attn<64, 4>(P, I, slot, ab, rope64) : stage_attn<64, 8>(P, I, slot, ab, rope64);
             else g4 ? stage_attn<128, 4>(P, I, slot, ab, rope128) : stage_attn<128, 8>(P, I, slot, ab, rope128);
             flags = SLOT_FRESH;
             key0 = key1 = -1;
-        } else if (GLM && opc == MK_OP_GLM_GEMM) {
-            // the tile's activation rows by bulk copies, unless the buffer
-            // already holds them (key: the input's device address)
-            const long long key = (long long)PTR(I, S_GG_XQ);
-            if (key != key0) {
-                if (hs > 0 && !ab)
-                    ab = !warp_wait_bar(P, S, &S.act_empty()[(hs - 1) & 1], ((hs - 1) >> 1) & 1, 1, i, opc);
-                if (!ab) tx = stage_glm(P, I, reinterpret_cast<uint8_t *>(S.abuf(0)), &S.act_full()[sl]);
-                key0 = ab ? -1 : key;
-            }
-            key1 = -1;
         } else if (opc >= MK_OP_QKV && opc <= MK_OP_LM) {
             // two buffers: buffer sl was last read by instruction i - 2, whose
             // slot release was awaited above; one buffer: instruction i - 1
@@ -360,22 +361,29 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         if (handoff && !ab) ab = !warp_wait_bar(P, S, &S.act_full()[sl], (hs >> 1) & 1, 2, i, opc);
         if (P.trace && ct == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 13] = gtimer();
         const float *slot = reinterpret_cast<const float *>(S.act(sl));
-        if (opc == MK_OP_ATTN) {
+        if constexpr (GLM) {  // GLM-block plans hold only GLM ops and counters
+            if (opc == MK_OP_GLM_GEMM) {
+                if (d.nrows == 64) glm_gemm_task<64>(P, S, I, i, sl, ring, ured, ab);
+                else glm_gemm_task<16>(P, S, I, i, sl, ring, ured, ab);
+                rq.set(ring, P.num_pages);
+            } else if (opc == MK_OP_GLM_A0 || opc == MK_OP_GLM_FIN) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // the slot holds nothing for these
+                if (opc == MK_OP_GLM_A0) glm_a0_task(P, S, I, i, ured, ab);
+                else glm_fin_task(P, I, ab);
+            } else {  // COUNTER: the slot handshake only
+                consumer_sync(P, S, cph, ab, i);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.act_empty()[sl]);
+                wrote = false;
+            }
+        } else if (opc == MK_OP_ATTN) {
             if (P.D == 64) attn_task<64>(P, S, I, i, sl, slot, ring, ab);
             else attn_task<128>(P, S, I, i, sl, slot, ring, ab);
             rq.set(ring, P.num_pages);
         } else if (opc == MK_OP_EMBED) {
             consumer_sync(P, S, cph, ab, i);
             embed_task(P, S, I, i, sl, ab);
-        } else if (GLM && opc == MK_OP_GLM_GEMM) {
-            if (d.nrows == 64) glm_gemm_task<64>(P, S, I, i, sl, ring, ured, ab);
-            else glm_gemm_task<16>(P, S, I, i, sl, ring, ured, ab);
-            rq.set(ring, P.num_pages);
-        } else if (GLM && (opc == MK_OP_GLM_A0 || opc == MK_OP_GLM_FIN)) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // the slot holds nothing for these
-            if (opc == MK_OP_GLM_A0) glm_a0_task(P, S, I, i, ured, ab);
-            else glm_fin_task(P, I, ab);
         } else if (opc >= MK_OP_QKV) {
             if (MAXB == 1 && rpw_tile(P, d)) {  // (a constant condition for larger batches)
                 const int kg = d.kc >> 8;

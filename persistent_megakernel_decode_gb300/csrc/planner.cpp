@@ -18,6 +18,7 @@
 #include <functional>
 #include <numeric>
 #include <queue>
+#include <tuple>
 #include <string>
 #include <vector>
 
@@ -313,19 +314,36 @@ std::vector<std::vector<int>> greedy(const std::vector<int> &order, const std::v
 // List scheduling against a time model of one step.  A task is ready HOP
 // after every counter it waits on (this epoch) has met its threshold, and it
 // holds a worker for a fixed cost plus its bytes at the worker's share of HBM
-// bandwidth; it goes to the worker on which it finishes first (ties: lowest
-// index).  Tasks are taken in `order`, a topological order, so every queue is
-// a subsequence of it.  The model balances each dependency phase on its own,
-// where the byte greedy balances whole-step totals.
+// bandwidth.  Among the tasks whose producers are all placed, the one ready
+// first (ties: earlier in `order`) goes next, to the worker on which it
+// finishes first (ties: lowest index).  The placement order is thus a
+// topological order and every queue a subsequence of it; it lets a consumer
+// that becomes ready early (an MLP-down K chunk) run between the producer
+// tiles still to come instead of behind all of them.  The model balances each
+// dependency phase on its own, where the byte greedy balances whole-step
+// totals.
 std::vector<std::vector<int>> timed(const std::vector<int> &order, const std::vector<TaskRec> &tasks, int workers,
                                     int n_events) {
     constexpr double HOP_US = 3.0, TILE_US = 1.0, ATTN_US = 4.0, HBM_BYTES_PER_US = 6.8e6;
     const double bw = HBM_BYTES_PER_US / std::max(1, workers);
-    std::vector<std::vector<std::pair<double, int>>> sig(n_events);  // (finish, increment) of each signal
-    std::vector<std::vector<std::pair<int64_t, double>>> met(n_events);  // cached (threshold, time met)
+    const int n = (int)tasks.size();
+    std::vector<std::vector<std::pair<double, int>>> sig(n_events);  // (finish, increment) of each placed signal
+    std::vector<std::vector<int>> prod(n_events), cons(n_events);
+    std::vector<int> pending(n, 0), rank(n, 0);
+    for (int i = 0; i < (int)order.size(); ++i) rank[order[i]] = i;
+    for (int id : order) {
+        const TaskRec &t = tasks[id];
+        for (int i = 0; i < t.ns; ++i) prod[t.s_ev[i]].push_back(id);
+    }
+    for (int id : order) {
+        const TaskRec &t = tasks[id];
+        for (int i = 0; i < t.nw; ++i)
+            if (t.w_off[i] >= 0 && t.w_thr[i] > 0) {
+                cons[t.w_ev[i]].push_back(id);
+                pending[id] += (int)prod[t.w_ev[i]].size();
+            }
+    }
     auto time_met = [&](int e, int64_t thr) {
-        for (auto &c : met[e])
-            if (c.first == thr) return c.second;
         auto v = sig[e];
         std::sort(v.begin(), v.end());
         int64_t acc = 0;
@@ -335,16 +353,27 @@ std::vector<std::vector<int>> timed(const std::vector<int> &order, const std::ve
             t = f.first;
             if (acc >= thr) break;
         }
-        met[e].push_back({thr, t});
         return t;
     };
-    std::vector<double> free_at(workers, 0.0);
-    std::vector<std::vector<int>> q(workers);
-    for (int id : order) {
+    auto ready_time = [&](int id) {
         const TaskRec &t = tasks[id];
         double ready = 0.0;
         for (int i = 0; i < t.nw; ++i)
             if (t.w_off[i] >= 0 && t.w_thr[i] > 0) ready = std::max(ready, time_met(t.w_ev[i], t.w_thr[i]) + HOP_US);
+        return ready;
+    };
+    using Cand = std::tuple<double, int, int>;  // ready time, rank, task
+    std::priority_queue<Cand, std::vector<Cand>, std::greater<Cand>> heap;
+    for (int id : order)
+        if (pending[id] == 0) heap.push({ready_time(id), rank[id], id});
+    std::vector<double> free_at(workers, 0.0);
+    std::vector<std::vector<int>> q(workers);
+    int placed = 0;
+    while (!heap.empty()) {
+        const auto [ready, rk, id] = heap.top();
+        (void)rk;
+        heap.pop();
+        const TaskRec &t = tasks[id];
         const double dur = (t.opcode == MK_OP_ATTN ? ATTN_US : TILE_US) + (double)t.cost / bw;
         int best = 0;
         double best_end = 0.0;
@@ -357,8 +386,15 @@ std::vector<std::vector<int>> timed(const std::vector<int> &order, const std::ve
         }
         free_at[best] = best_end;
         q[best].push_back(id);
-        for (int i = 0; i < t.ns; ++i) sig[t.s_ev[i]].push_back({best_end, t.s_inc[i]});
+        ++placed;
+        for (int i = 0; i < t.ns; ++i) {
+            const int e = t.s_ev[i];
+            sig[e].push_back({best_end, t.s_inc[i]});
+            for (int c : cons[e])
+                if (--pending[c] == 0) heap.push({ready_time(c), rank[c], c});
+        }
     }
+    if (placed != (int)order.size()) return greedy(order, tasks, workers);  // not a DAG of this epoch: keep order
     return q;
 }
 

@@ -104,8 +104,9 @@ def test_planner_queue_simulates_over_steps():
 ])
 def test_timed_schedule_is_a_valid_deal_of_the_same_tasks(shape, B, seq0, workers):
     """The time-model schedule deals exactly the byte schedule's tasks, with the
-    same waits and signals, each queue in one topological order, deadlock-free
-    over several steps; for one worker the two coincide."""
+    same waits and signals; the queues are subsequences of one topological
+    order (queue order plus producer -> event -> consumer edges form no cycle)
+    and deadlock-free over several steps."""
     steps = 3
     kw = dict(num_sms=workers, smem_per_cta=232448)
     pt = rt.Plan.llama(shape, B, seq0, steps, max(seq0) + steps + 3, schedule=rt.SCHED_TIMED, **kw)
@@ -116,18 +117,37 @@ def test_timed_schedule_is_a_valid_deal_of_the_same_tasks(shape, B, seq0, worker
     ids = idt.tolist()
     flat = sorted(t for row in ids for t in row if t >= 0)
     assert flat == list(range(len(tt)))
-    for row in ids:
-        real = [t for t in row if t >= 0]
-        assert real == sorted(real)                      # task ids are a topological order
-        assert all(t < 0 for t in row[len(real):])       # NoOps only pad the tail
     waits = {i: [(r[7 + 3 * k], r[8 + 3 * k], r[9 + 3 * k]) for k in range(r[6])] for i, r in enumerate(tt)}
     sigs = {i: [(r[17 + 2 * k], r[18 + 2 * k]) for k in range(r[16])] for i, r in enumerate(tt)}
+    n, ne = len(tt), len(tht)
+    succ = [[] for _ in range(n + ne)]                   # task nodes 0..n-1, event nodes n..n+ne-1
+    for row in ids:
+        real = [t for t in row if t >= 0]
+        assert all(t < 0 for t in row[len(real):])       # NoOps only pad the tail
+        for a, b in zip(real, real[1:]):
+            succ[a].append(b)
+    for i in range(n):
+        for e, _ in sigs[i]:
+            succ[i].append(n + e)
+        for e, _, off in waits[i]:
+            if off >= 0:
+                succ[n + e].append(i)
+    indeg = [0] * (n + ne)
+    for v in succ:
+        for w in v:
+            indeg[w] += 1
+    stack = [v for v in range(n + ne) if indeg[v] == 0]
+    seen = 0
+    while stack:
+        v = stack.pop()
+        seen += 1
+        for w in succ[v]:
+            indeg[w] -= 1
+            if indeg[w] == 0:
+                stack.append(w)
+    assert seen == n + ne                                # acyclic: one topological order holds every queue
     res = sim.deadlock_check(ids, waits, sigs, len(tht), steps=steps)
     assert res.ok and res.counters == rules.expected_counters(tht.tolist(), steps)
-    one_t = rt.Plan.llama(shape, B, seq0, 1, max(seq0) + 4, num_sms=1, smem_per_cta=232448, schedule=rt.SCHED_TIMED)
-    one_b = rt.Plan.llama(shape, B, seq0, 1, max(seq0) + 4, num_sms=1, smem_per_cta=232448, schedule=rt.SCHED_BYTES)
-    if shape is synth.TINY:
-        assert one_t.export()[1].tolist() == one_b.export()[1].tolist()
 
 
 def test_graph_plan_fork_join_example():
