@@ -425,10 +425,16 @@ DEV void fetch(WIns &I, const KParams &P, const int32_t *q, int i) {
 }
 
 // Warp-uniform sanity checks of one instruction against the launch.
-// GLM = the kernel instance of GLM-block plans: only it accepts (and
-// contains the code of) the GLM opcodes.
-template <bool GLM>
+// Kernel instances ("flavours"): FL_GEN runs every Llama-path op; FL_GLM
+// only the GLM-block ops (and holds their code); FL_LEAN is the batch-1
+// instance for plans whose GEMV tiles all take the row-per-warp path and whose
+// head_dim is 64 -- it holds no other GEMV or attention variant, which keeps
+// its registers free of spills.
+constexpr int FL_GEN = 0, FL_GLM = 1, FL_LEAN = 2;
+
+template <int FL>
 DEV bool ins_valid(const KParams &P, const WIns &I) {
+    constexpr bool GLM = FL == FL_GLM;
     const int opc = F(I, W_OPC);
     if (opc < 0 || opc >= MK_NUM_OPCODES) return false;
     if (opc == MK_OP_NOOP) return true;
@@ -520,8 +526,9 @@ DEV int attn_cached_rows(const WIns &I, int pos) { return max(0, min(F(I, P_T), 
 
 // Weight / cache rows streamed by the loader for one instruction.  Loader and
 // consumers derive the same segments and walk the same page ring.
-template <bool GLM>
+template <int FL>
 DEV int describe(const KParams &P, const WIns &I, Seg &s0, Seg &s1) {
+    constexpr bool GLM = FL == FL_GLM;
     const int opc = F(I, W_OPC);
     if (opc == MK_OP_QKV || opc == MK_OP_O || opc == MK_OP_DOWN || opc == MK_OP_LM || opc == MK_OP_UP) {
         const long long ktot = F(I, P_KTOT);

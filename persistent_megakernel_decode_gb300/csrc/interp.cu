@@ -30,7 +30,7 @@
 namespace mk {
 
 // ---------------------------------------------------------------- loader warp
-template <bool GLM>
+template <int FL>
 DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int lane = threadIdx.x & 31;
     const uint64_t pol = evict_first_policy();
@@ -43,12 +43,12 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
         if (lane < 4 && i + 4 + lane < P.lmax) prefetch_l2(myq + (size_t)(i + 4 + lane) * W_WORDS);
         fetch(I, P, myq, i);
         const int opc = F(I, W_OPC);
-        if (!ins_valid<GLM>(P, I)) {
+        if (!ins_valid<FL>(P, I)) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
             break;
         }
         Seg s0, s1;
-        const int nseg = describe<GLM>(P, I, s0, s1);
+        const int nseg = describe<FL>(P, I, s0, s1);
         if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 4] = gtimer();
         // Rows go to pages in order, as many whole rows per page as fit.  GEMV
         // segments (MLP-up: gate rows, then up rows) share pages; attention
@@ -125,8 +125,9 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
 }
 
 // ---------------------------------------------------------------- activation-loader warp
-template <int MAXB, bool GLM>
+template <int MAXB, int FL>
 DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
+    constexpr bool GLM = FL == FL_GLM;
     const int lane = threadIdx.x & 31;
     const bool two_bufs = P.abuf_count > 1;
     long long key0 = -1, key1 = -1;   // what each activation buffer holds: op row << 32 | first column
@@ -146,7 +147,7 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
         if (!needs_handoff(P, I, decode(I), chain)) continue;  // same input as the previous slot: nothing to stage
         const int sl = hs & 1;
         const uint32_t use = hs >> 1;
-        if (!ab && !ins_valid<GLM>(P, I)) {
+        if (!ab && !ins_valid<FL>(P, I)) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 1);
             ab = true;
         }
@@ -183,7 +184,8 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
             }
         } else if (opc == MK_OP_ATTN) {
             const bool g4 = P.Hq <= 4 * P.Hkv;
-            if (P.D == 64) g4 ? stage_attn<64, 4>(P, I, slot, ab, rope64) : stage_attn<64, 8>(P, I, slot, ab, rope64);
+            if (FL == FL_LEAN || P.D == 64)
+                g4 ? stage_attn<64, 4>(P, I, slot, ab, rope64) : stage_attn<64, 8>(P, I, slot, ab, rope64);
             else g4 ? stage_attn<128, 4>(P, I, slot, ab, rope128) : stage_attn<128, 8>(P, I, slot, ab, rope128);
             flags = SLOT_FRESH;
             key0 = key1 = -1;
@@ -336,8 +338,9 @@ DEV bool gemv_dispatch(const KParams &P, const Smem S, const WIns &I, int i, int
     return false;
 }
 
-template <int MAXB, bool GLM>
+template <int MAXB, int FL>
 DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
+    constexpr bool GLM = FL == FL_GLM;
     const int ct = threadIdx.x - 64, lane = ct & 31;
     uint32_t ring = 0, cph = 0, ured = 0;
     uint32_t hs = 0;  // activation hand-offs so far (the activation loader counts the same ones)
@@ -378,7 +381,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
                 wrote = false;
             }
         } else if (opc == MK_OP_ATTN) {
-            if (P.D == 64) attn_task<64>(P, S, I, i, sl, slot, ring, ab);
+            if (FL == FL_LEAN || P.D == 64) attn_task<64>(P, S, I, i, sl, slot, ring, ab);
             else attn_task<128>(P, S, I, i, sl, slot, ring, ab);
             rq.set(ring, P.num_pages);
         } else if (opc == MK_OP_EMBED) {
@@ -391,8 +394,11 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
                 else if (kg <= 2) gemv_rpw_pages<2>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
                 else if (kg <= 4) gemv_rpw_pages<4>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
                 else gemv_rpw_pages<8>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
-            } else {
+            } else if constexpr (FL != FL_LEAN) {
                 wrote = gemv_dispatch<MAXB>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
+            } else {  // the planner picks the lean instance only for plans without such tiles
+                if (lane == 0 && !ab) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 2);
+                ab = true;
             }
         } else {  // COUNTER: the slot handshake only
             consumer_sync(P, S, cph, ab, i);
@@ -412,7 +418,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
 }
 
 // ---------------------------------------------------------------- kernel
-template <int MAXB, bool GLM>
+template <int MAXB, int FL>
 __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
     Smem S;
     S.o_abuf = 0;
@@ -443,10 +449,10 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
     __syncthreads();
     const int32_t *myq = P.queue + (size_t)blockIdx.x * P.lmax * W_WORDS;
     const int warp = threadIdx.x >> 5;
-    if (warp == 0) loader_role<GLM>(P, S, myq);
-    else if (warp == 1) aloader_role<MAXB, GLM>(P, S, myq);
+    if (warp == 0) loader_role<FL>(P, S, myq);
+    else if (warp == 1) aloader_role<MAXB, FL>(P, S, myq);
     else if (warp == PUBLISHER_WARP) publisher_role(P, S, myq);
-    else consumer_role<MAXB, GLM>(P, S, myq);
+    else consumer_role<MAXB, FL>(P, S, myq);
     __syncthreads();
 }
 
@@ -471,12 +477,12 @@ int query_device(int *num_sms, int *smem_optin) {
 using KernelFn = void (*)(const KParams);
 
 static KernelFn pick_kernel(const Plan &p) {
-    if (p.kind == PLAN_GLM) return mk_interp<1, true>;
+    if (p.kind == PLAN_GLM) return mk_interp<1, FL_GLM>;
     const int B = p.B;
-    if (B <= 1) return mk_interp<1, false>;
-    if (B <= 2) return mk_interp<2, false>;
-    if (B <= 4) return mk_interp<4, false>;
-    return mk_interp<8, false>;
+    if (B <= 1) return p.lean ? mk_interp<1, FL_LEAN> : mk_interp<1, FL_GEN>;
+    if (B <= 2) return mk_interp<2, FL_GEN>;
+    if (B <= 4) return mk_interp<4, FL_GEN>;
+    return mk_interp<8, FL_GEN>;
 }
 
 // Operand rows of the GLM block plan, in the planner's op order: A0,
@@ -675,8 +681,8 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
     KernelFn fn = pick_kernel(p);
     static thread_local int configured_smem = -1;
     if (configured_smem < p.smem_bytes) {
-        for (KernelFn f : {mk_interp<1, false>, mk_interp<2, false>, mk_interp<4, false>, mk_interp<8, false>,
-                           mk_interp<1, true>}) {
+        for (KernelFn f : {mk_interp<1, FL_GEN>, mk_interp<2, FL_GEN>, mk_interp<4, FL_GEN>, mk_interp<8, FL_GEN>,
+                           mk_interp<1, FL_GLM>, mk_interp<1, FL_LEAN>}) {
             e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         }

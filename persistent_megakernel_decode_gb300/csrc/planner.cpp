@@ -885,6 +885,20 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     int64_t kv_write = (int64_t)2 * B * Hkv * D * 2 * L;
     int64_t norms = (int64_t)(2 * L + 1) * H * 2 + (m->qk_norm ? (int64_t)2 * L * D * 2 : 0);
     p.alg_bytes = weights + kv_read + kv_write + norms;
+    // the lean batch-1 kernel instance: every GEMV tile must take the
+    // row-per-warp path (the device applies the same rule to each tile)
+    p.lean = B == 1 && D == 64;
+    for (const TaskRec &t : p.tasks) {
+        if (!p.lean) break;
+        if (t.opcode < MK_OP_QKV || t.opcode > MK_OP_LM || t.opcode == MK_OP_ATTN) continue;
+        const int kc = t.payload[P_KC - W_P], nrows = t.payload[P_NROWS - W_P], npg = t.payload[P_NPG - W_P];
+        const bool up = t.opcode == MK_OP_UP;
+        bool ok = kc % 256 == 0 && kc <= 2048;
+        if (ok && npg == 1) ok = up ? nrows == 8 : nrows <= 16;
+        else if (ok) ok = (npg == 2 || npg == 4) && t.opcode != MK_OP_O && p.page_bytes == 32 * kc &&
+                          (!up || nrows % 8 == 0);
+        p.lean = ok;
+    }
     return finish_queues(p, false, p.schedule == MK_SCHED_TIMED);
 }
 

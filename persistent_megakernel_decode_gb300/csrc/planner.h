@@ -43,6 +43,7 @@ struct Plan {
     std::vector<int> seq0;
     int rows_qkv = 0, rows_o = 0, rows_up = 0, rows_down = 0, kchunk_down = 0, rows_lm = 0, attn_split = 0;
     int schedule = MK_SCHED_BYTES;  // MK_SCHED_BYTES or MK_SCHED_TIMED
+    bool lean = false;  // batch 1, head_dim 64, every GEMV tile on the row-per-warp path: the lean kernel instance
     int page_bytes = 16384, act_bytes = 128, abuf_bytes = 128, abuf_count = 1, aux_bytes = 256, red_bytes = 128, num_pages = 2, smem_bytes = 0,
         nsplit_max = 1;
     std::vector<TaskRec> tasks;
