@@ -131,7 +131,71 @@ def barrier(dist):
         dist.barrier()
 
 
-def cpu_oracle_rate(w, steps, warmup=0, device_for_inputs=None):
+def side_measurements(args, w, dev, stream, weights, kc, vc, seq0, max_steps, first_free_step):
+    """The comparison legs measured beside the megakernel in the same run: the
+    same device code launched once per op (stream and CUDA-Graph variants), the
+    megakernel's per-step launches replayed from a CUDA Graph, and an empty
+    kernel's launch time (cooperative and plain, the interpreter's grid)."""
+    import torch
+    from persistent_megakernel_decode_gb300 import runtime as rt
+    out = {}
+    K = 16
+
+    def timed_steps(sess, first, graph):
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for st in range(first, first + K):
+                    sess.run(st, 1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+        else:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for st in range(first, first + K):
+                    sess.run(st, 1)
+                e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    for mode, name in ((rt.MODE_PER_OP, "per_op"), (rt.MODE_MEGAKERNEL, "megakernel")):
+        try:
+            sess = rt.Session(w.shape, weights, kc, vc, seq0, max_steps, stream=stream, mode=mode)
+            sess.tokens[0] = torch.tensor([1] * w.batch, dtype=torch.int32, device=dev)
+            with torch.cuda.stream(stream):
+                for st in range(3):
+                    sess.run(st, 1)
+            sess.sync()
+            launches = sess.plan.info()["num_launches"]
+            ms_stream = timed_steps(sess, 3, False)
+            ms_graph = timed_steps(sess, 3 + K, True)
+            err = int(sess.sync().code)
+            out[name] = {"launches_per_step": launches, "ms_per_step_stream": ms_stream,
+                         "ms_per_step_cuda_graph": ms_graph, "device_error": err, "steps": K}
+            del sess
+        except Exception as e:  # a leg that cannot run is reported, not fatal
+            out[name] = {"unavailable": str(e)[:200]}
+    info = rt.Plan.llama(w.shape, w.batch, seq0, 1, kc.shape[3]).info()
+    for coop in (True, False):
+        n = 200
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(10):
+                rt.launch_probe(info["num_workers"], coop, stream)
+            e0.record(stream)
+            for _ in range(n):
+                rt.launch_probe(info["num_workers"], coop, stream)
+            e1.record(stream)
+        stream.synchronize()
+        out["empty_launch_us_" + ("cooperative" if coop else "plain")] = e0.elapsed_time(e1) / n * 1e3
+    return out
+
+
+def cpu_oracle_rate(w, steps, warmup=0, device_for_inputs=None, nthreads=None):
     """Time the oracle's fp32 twin on the host cores over `steps` decode steps."""
     import torch
     from oracle import forward as orc
@@ -148,7 +212,7 @@ def cpu_oracle_rate(w, steps, warmup=0, device_for_inputs=None):
     kc = rng.integers(0x3000, 0x3F80, size=dims, dtype=np.uint16)   # finite bf16 bit patterns
     vc = rng.integers(0x3000, 0x3F80, size=dims, dtype=np.uint16)
     shape = orc.Shape(s.L, s.H, s.Hq, s.Hkv, s.D, s.F, s.V, s.qk_norm, s.eps, s.theta)
-    cores = os.cpu_count() or 1
+    cores = nthreads or os.cpu_count() or 1
     toks = synth.first_tokens(w)
     times = []
     for i in range(warmup + steps):
@@ -256,6 +320,12 @@ def run_mk(args, w, rank, world, dist):
         total, cores = cpu_oracle_rate(w, cpu_steps, 0, device_for_inputs=dev)
         cpu = {"value": w.batch * cpu_steps / total, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{cpu_steps} decode steps of {w.name} (fp32 oracle, all layers, batch {w.batch})"}
+        total1, _ = cpu_oracle_rate(w, 1, 0, device_for_inputs=dev, nthreads=1)
+        cpu["single_core"] = {"value": w.batch / total1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"1 decode step of {w.name} (fp32 oracle, one thread)"}
+    side = None
+    if not args.no_extras and world == 1:
+        side = side_measurements(args, w, dev, stream, weights, kc, vc, seq0, max_steps, args.warmup + args.steps)
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -268,7 +338,7 @@ def run_mk(args, w, rank, world, dist):
         "step_us": {"median": float(np.median(step_ms)) * 1e3, "p10": float(np.percentile(step_ms, 10)) * 1e3,
                     "p90": float(np.percentile(step_ms, 90)) * 1e3},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": args.steps * info["num_launches"],
+        "gpu_launches": args.steps * info["num_launches"], "side": side,
         "plan": {k: info[k] for k in ("num_workers", "lmax", "num_tasks", "num_events", "num_pages", "smem_bytes")},
         "device_error": int(rec.code),
     }
@@ -433,6 +503,8 @@ def main():
     ap.add_argument("--workload", default="llama1b_b1")
     ap.add_argument("--mode", default="megakernel", choices=["megakernel", "per_op"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the side legs (per-op and CUDA-Graph launches, empty-kernel probe)")
     ap.add_argument("--knob", action="append", default=[], help="planner knob, e.g. attn_split=512")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N decoder layers (a small case for profiling, not a bench line)")

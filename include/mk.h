@@ -353,6 +353,14 @@ int mk_read_trace(mk_plan_t plan, void *workspace, uint64_t *out);
 int mk_run_static(mk_plan_t plan, int first_step, int num_steps, uint32_t flags, uint64_t timeout_ns, void *stream,
                   uint64_t *workspace_out);
 
+/* Launch probe (no counterpart call on the pages; they quote a fixed launch
+ * cost beside their megakernel timings): launches an empty kernel of
+ * num_workers CTAs of the interpreter's block size on `stream`, as a
+ * cooperative launch when `cooperative` is non-zero (like mk_run) or a plain
+ * one otherwise.  Asynchronous; the caller times it with events.  Returns
+ * MK_ERR_CUDA if the launch fails. */
+int mk_launch_probe(int num_workers, int cooperative, void *stream);
+
 /* Free the plan's host memory.  NULL-safe.  Never touches device memory. */
 void mk_free(mk_plan_t plan);
 

@@ -716,6 +716,24 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
     return MK_OK;
 }
 
+// ---------------------------------------------------------------- launch probe
+__global__ void __launch_bounds__(THREADS, 1) mk_empty() {}
+
+int mk_launch_probe(int num_workers, int cooperative, void *stream) {
+    if (num_workers <= 0) return set_error(MK_ERR_INVALID, "num_workers must be positive");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (cooperative) {
+        void *args[] = {nullptr};
+        e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(mk_empty), dim3(num_workers), dim3(THREADS),
+                                        args, 0, st);
+    } else {
+        mk_empty<<<num_workers, THREADS, 0, st>>>();
+        e = cudaGetLastError();
+    }
+    return e == cudaSuccess ? MK_OK : cuda_fail(e, "probe launch");
+}
+
 // ---------------------------------------------------------------- allocation-free entry point
 // The workspace of mk_run_static(): a fixed device array owned by this
 // library.  Host code only ever sees the array's host-side stand-in; the

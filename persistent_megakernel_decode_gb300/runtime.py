@@ -39,7 +39,7 @@ PER_LAYER = ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "norm_attn", "norm_mlp", 
 
 EXPORTED = ["mk_plan", "mk_plan_graph", "mk_plan_info_get", "mk_plan_export", "mk_bind", "mk_run",
             "mk_sync_status", "mk_read_counters", "mk_read_trace", "mk_free", "mk_last_error", "mk_argmax_index",
-            "mk_run_static", "mk_plan_glm"]
+            "mk_run_static", "mk_plan_glm", "mk_launch_probe"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 
@@ -129,6 +129,7 @@ def load():
     lib.mk_sync_status.argtypes = [P, P, P, C.POINTER(ErrorRecord)]
     lib.mk_read_counters.argtypes = [P, P, P]
     lib.mk_read_trace.argtypes = [P, P, P]
+    lib.mk_launch_probe.argtypes = [C.c_int, C.c_int, P]
     lib.mk_free.argtypes = [P]
     lib.mk_free.restype = None
     lib.mk_last_error.restype = C.c_char_p
@@ -155,6 +156,11 @@ def _target(num_sms=0, smem_per_cta=0, mode=MODE_MEGAKERNEL, **knobs) -> TargetD
     for k, v in knobs.items():
         setattr(t, k, int(v))
     return t
+
+
+def launch_probe(num_workers: int, cooperative: bool, stream) -> None:
+    """Launch the empty probe kernel (see ``mk_launch_probe``) on a torch stream."""
+    _check(load().mk_launch_probe(int(num_workers), int(cooperative), C.c_void_p(stream.cuda_stream)))
 
 
 class Plan:
