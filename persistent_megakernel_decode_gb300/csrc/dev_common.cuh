@@ -343,6 +343,12 @@ DEV void consumer_sync(const KParams &P, const Smem S, uint32_t &phase, bool &ab
     ++phase;
 }
 
+// Trace stamp k of slot i: traced runs only, written by consumer thread 0
+// (inside ops, for a breakdown of where an instruction's time goes).
+DEV void trace_stamp(const KParams &P, int i, int k) {
+    if (P.trace && threadIdx.x == 64) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + k] = gtimer();
+}
+
 DEV bool cta_aborting(const Smem S) { return __shfl_sync(FULL, (int)S.ctrl()[0], 0) != 0; }
 
 // ---------------------------------------------------------------- instruction decoding

@@ -53,11 +53,6 @@ DEV uint32_t quant4(const float (&v)[4], float &scale) {
     return e4m3x2(v[0] / scale, v[1] / scale) | (e4m3x2(v[2] / scale, v[3] / scale) << 16);
 }
 
-// trace stamp k of slot i (traced runs only; consumer thread 0)
-DEV void glm_stamp(const KParams &P, int i, int k) {
-    if (P.trace && threadIdx.x == 64) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + k] = gtimer();
-}
-
 // ---------------------------------------------------------------- A0
 // One token row m: h = x + res (the new residual, bf16), RMSNorm of those
 // bf16 values, then per 128 columns e4m3 codes and a scale.  Warp w takes the
@@ -99,7 +94,7 @@ DEV void glm_a0_task(const KParams &P, const Smem S, const WIns &I, int i, uint3
         for (int e = 0; e < 4; ++e) ss = fmaf(h[j][e], h[j][e], ss);  // zero past the row's end
     }
     ss = warp_sum(ss);
-    glm_stamp(P, i, 9);
+    trace_stamp(P, i, 9);
     float *red = S.red((int)(ured % NRED));
     ++ured;
     if (lane == 0) red[warp] = ss;
@@ -108,7 +103,7 @@ DEV void glm_a0_task(const KParams &P, const Smem S, const WIns &I, int i, uint3
 #pragma unroll
     for (int k = 0; k < CONSUMER_WARPS; ++k) tot += red[k];
     const float r = rsqrtf(tot / (float)H + P.eps);
-    glm_stamp(P, i, 10);
+    trace_stamp(P, i, 10);
 #pragma unroll
     for (int j = 0; j < BPW; ++j) {
         const int blk = warp + CONSUMER_WARPS * j, col = blk * 128 + lane * 4;
@@ -158,7 +153,7 @@ DEV void glm_gemm_task(const KParams &P, const Smem S, const WIns &I, int i, int
     const float *sa = reinterpret_cast<const float *>(abuf + GLM_MAX_M * astride);
     for (int k = 0; k < npg; ++k)
         if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(base + k) % NP], ((base + k) / NP) & 1, 2, i, MK_OP_GLM_GEMM);
-    glm_stamp(P, i, 7);
+    trace_stamp(P, i, 7);
     const int r = gi * 8 + g;
     const uint8_t *wrow = S.pages() + (size_t)((base + r / rpp) % NP) * P.page_bytes + (size_t)(r % rpp) * K;
     const bool lo_ok = g < M, hi_ok = g + 8 < M;
@@ -207,7 +202,7 @@ DEV void glm_gemm_task(const KParams &P, const Smem S, const WIns &I, int i, int
         scale_add(kb, c0);
     }
     __syncwarp();
-    glm_stamp(P, i, 9);
+    trace_stamp(P, i, 9);
     if (lane == 0) {
         for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(base + k) % NP]);
         mbar_arrive(&S.act_empty()[sl]);  // staged rows no longer needed by this warp
@@ -223,7 +218,7 @@ DEV void glm_gemm_task(const KParams &P, const Smem S, const WIns &I, int i, int
     pr[(g + 8) * NR + n] = acc[2];
     pr[(g + 8) * NR + n + 1] = acc[3];
     consumer_bar();
-    glm_stamp(P, i, 10);
+    trace_stamp(P, i, 10);
     if (ab) return;
     for (int e = ct; e < M * NR; e += CONSUMERS) {
         const int m = e / NR, c = e % NR;

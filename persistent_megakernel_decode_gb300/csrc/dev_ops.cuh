@@ -723,6 +723,7 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
     };
     for (int k = 0; k < npg; ++k)
         if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(kring + k) % P.num_pages], ((kring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
+    trace_stamp(P, i, 6);
     // scores: 8 tokens per round, 4 lanes per token, DQ dims per lane
     const int qtr = lane & 3;
     float q[DQ];
@@ -764,6 +765,7 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
         }
     }
     m = warp_max(m);
+    trace_stamp(P, i, 7);
     __syncwarp();
     if (lane == 0)
         for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(kring + k) % P.num_pages]);
@@ -779,6 +781,7 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
     // consecutive tokens' loads and multiply-adds overlap
     for (int k = 0; k < npg; ++k)
         if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(vring + k) % P.num_pages], ((vring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
+    trace_stamp(P, i, 8);
     float acc[4][PER];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
@@ -818,6 +821,7 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
         for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(vring + k) % P.num_pages]);
         mbar_arrive(&S.act_empty()[sl]);  // q, k, v of the slot no longer needed by this warp
     }
+    trace_stamp(P, i, 9);
     // this warp's partial: (o[D], max, sum) of head (b, g * G + hh), piece split * parts + part
     const int head = g * G + hh, npieces = P.nsplit_max * parts;
     float *pp = part_base + ((size_t)(b * P.Hq + head) * npieces + split * parts + part) * (D + 2);
@@ -837,6 +841,7 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
         const uint32_t old = atom_acqrel_add(arrive + ((size_t)layer * P.B + b) * P.Hq + head, 1u);
         last = old == (uint32_t)(P.step + 1) * (uint32_t)(nsplit * parts) - 1u;
     }
+    trace_stamp(P, i, 10);
     if (!__shfl_sync(FULL, last, 0)) return;
     __syncwarp();
     // merge: log-sum-exp over the head's pieces, MB at a time so that their
