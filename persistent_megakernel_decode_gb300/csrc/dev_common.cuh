@@ -478,7 +478,10 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
     }
     if (opc >= MK_OP_QKV && opc <= MK_OP_LM && opc != MK_OP_ATTN) {
         const int nrows = F(I, P_NROWS), kc = F(I, P_KC);
-        const int rmax = P.B > 4 ? 8 : MAX_TILE_ROWS;
+        // batch > 4 holds 8 rows x 8 sequences in registers, except on the
+        // tensor-core path (K slices of 64 per warp, tile rows in two pages of 8+)
+        const bool mma = kc % (64 * CONSUMER_WARPS) == 0 && F(I, P_NPG) <= 2 && F(I, P_RPP) >= 8;
+        const int rmax = P.B > 4 && !mma ? 8 : MAX_TILE_ROWS;
         const int total = opc == MK_OP_UP ? 2 * nrows : nrows;
         // more rows only as 2 or 4 pages of 16 rows on the batch-1 row-per-warp path
         const bool pages16 = P.B == 1 && kc % 256 == 0 && kc <= 2048 && P.page_bytes == 32 * kc;

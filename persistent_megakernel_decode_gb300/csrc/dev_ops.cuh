@@ -522,6 +522,175 @@ DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, int sl,
     return true;
 }
 
+// ---------------------------------------------------------------- tensor-core tiles (batch 2-8, or batch 1 off the row-per-warp path)
+// A tile of up to 16 weight rows (MLP-up: 8 gate + 8 up) for every sequence
+// as m16n8k16 bf16 MMAs: the weight rows are the MMA's M side, the (up to 8)
+// sequences its N side.  Warp w takes K slice [w K/8, (w + 1) K/8) in 64-wide
+// chunks; lane (g, t) = (lane / 4, lane % 4) loads 16 contiguous K elements of
+// weight rows g and g + 8 and of sequence g's activation at offset 16 t and
+// feeds them to four k16 steps (the K order inside a chunk is permuted alike
+// for both operands).  The fp32 activation is split into bf16 high and low
+// parts (x = hi + lo to 2^-16 relative) and both are multiplied, so the
+// products keep fp32-level accuracy.  Partials go to the same reduction
+// buffer layout as the split-K path and the same epilogue runs.
+DEV uint32_t bf16_pair_rn(float lo, float hi) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+DEV void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Whether a tile off the batch-1 row-per-warp path takes the tensor-core path.
+DEV bool mma_tile(const KParams &P, const WIns &I) {
+    const int opc = F(I, W_OPC), kc = F(I, P_KC), rpp = F(I, P_RPP), npg = F(I, P_NPG);
+    const int total = (opc == MK_OP_UP ? 2 : 1) * F(I, P_NROWS);
+    return kc % (64 * CONSUMER_WARPS) == 0 && total <= 16 && npg <= 2 && rpp >= 8;
+}
+
+template <int MAXB>
+DEV bool gemv_mma_tile(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
+                       RingPos &rq, uint32_t &ured, unsigned long long &lm_best, bool &ab) {
+    constexpr int RT = 16;                   // rows of the MMA's M side
+    constexpr int VT = RT * MAXB;            // partials per warp in a reduction buffer: row * MAXB + b
+    constexpr int VL = (VT + 31) / 32;
+    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int opc = F(I, W_OPC);
+    const int kc = F(I, P_KC), nrows = F(I, P_NROWS), npg = F(I, P_NPG), rpp = F(I, P_RPP);
+    const int B = P.B, NP = P.num_pages, row_bytes = 2 * kc;
+    const int out0 = F(I, P_OUT0);
+    const uint64_t ptr_a = PTR(I, opc == MK_OP_QKV ? S_QKV_OUT : opc == MK_OP_O ? S_O_HRES
+                                : opc == MK_OP_UP ? S_UP_OUT : opc == MK_OP_DOWN ? S_DN_HRES : S_LM_LOGITS);
+    const uint64_t ptr_b = PTR(I, opc == MK_OP_O ? S_O_HMID : S_LM_KEYS);
+    // O tiles: the residual values of this lane's epilogue entries, read
+    // before the slot is released (any warp may turn out to run the epilogue)
+    float resid_v[VL];
+#pragma unroll
+    for (int j = 0; j < VL; ++j) resid_v[j] = 0.f;
+    if (opc == MK_OP_O) {
+        const float *rs = slot_resid(P, const_cast<float *>(slot));
+#pragma unroll
+        for (int j = 0; j < VL; ++j) {
+            const int v = lane + 32 * j, r = v / MAXB, b = v % MAXB;
+            if (v < VT && b < B && r < nrows) resid_v[j] = rs[b * RESID_ROWS + r];
+        }
+    }
+    const uint32_t base = ring;
+    ring += npg;
+    for (int k = 0; k < npg; ++k)
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(base + k) % NP], ((base + k) / NP) & 1, 2, i, opc);
+    // rows past the tile's end read stale bytes of its own pages; their
+    // results are never stored
+    auto row_ptr = [&](int r) -> const uint8_t * {
+        const int pg = min(r / rpp, npg - 1);
+        return S.pages() + (size_t)((base + pg) % NP) * P.page_bytes + (size_t)(r % rpp) * row_bytes;
+    };
+    const uint8_t *w0 = row_ptr(g), *w1 = row_ptr(g + 8);
+    const bool bok = g < B;
+    const float *xb = S.abuf(sl) + (size_t)(bok ? g : 0) * kc;
+    const int kw = kc / CONSUMER_WARPS;
+    float ch[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = warp * kw; k0 < (warp + 1) * kw; k0 += 64) {
+        const int off = k0 + 16 * t;
+        const uint4 a00 = *reinterpret_cast<const uint4 *>(w0 + off * 2);
+        const uint4 a01 = *reinterpret_cast<const uint4 *>(w0 + off * 2 + 16);
+        const uint4 a10 = *reinterpret_cast<const uint4 *>(w1 + off * 2);
+        const uint4 a11 = *reinterpret_cast<const uint4 *>(w1 + off * 2 + 16);
+        float x[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 v = bok ? *reinterpret_cast<const float4 *>(xb + off + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+        }
+        uint32_t bh[8], bl[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float h0 = round_bf16(x[2 * e]), h1 = round_bf16(x[2 * e + 1]);
+            bh[e] = bf16_pair_rn(h0, h1);
+            bl[e] = bf16_pair_rn(x[2 * e] - h0, x[2 * e + 1] - h1);
+        }
+        const uint32_t ag[8] = {a00.x, a00.y, a00.z, a00.w, a01.x, a01.y, a01.z, a01.w};
+        const uint32_t ag8[8] = {a10.x, a10.y, a10.z, a10.w, a11.x, a11.y, a11.z, a11.w};
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            mma_bf16(ch, ag[2 * s], ag8[2 * s], ag[2 * s + 1], ag8[2 * s + 1], bh[2 * s], bh[2 * s + 1]);
+            mma_bf16(cl, ag[2 * s], ag8[2 * s], ag[2 * s + 1], ag8[2 * s + 1], bl[2 * s], bl[2 * s + 1]);
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(base + k) % NP]);
+        mbar_arrive(&S.act_empty()[sl]);  // activation buffer and slot no longer needed
+    }
+    rq.set(ring, NP);
+    // the reduction buffer (see gemv_tile for why its previous user is done)
+    const int rb = (int)(ured % NRED);
+    const uint32_t use = ured / NRED;
+    ++ured;
+    float *red = S.red(rb) + warp * VT;
+    if (2 * t < MAXB) {
+        red[g * MAXB + 2 * t] = ch[0] + cl[0];
+        red[(g + 8) * MAXB + 2 * t] = ch[2] + cl[2];
+    }
+    if (2 * t + 1 < MAXB) {
+        red[g * MAXB + 2 * t + 1] = ch[1] + cl[1];
+        red[(g + 8) * MAXB + 2 * t + 1] = ch[3] + cl[3];
+    }
+    consumer_bar();
+    if (warp != (int)(use % CONSUMER_WARPS)) return false;
+    const float *rall = S.red(rb);
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < VL; ++j) {
+        const int v = lane + 32 * j, r = v / MAXB, b = v % MAXB;
+        if (v >= VT || b >= B || r >= nrows || ab) continue;
+        float y = 0.f, u = 0.f;
+#pragma unroll
+        for (int w = 0; w < CONSUMER_WARPS; ++w) y += rall[w * VT + v];
+        if (opc == MK_OP_UP) {
+#pragma unroll
+            for (int w = 0; w < CONSUMER_WARPS; ++w) u += rall[w * VT + nrows * MAXB + v];
+        }
+        if (opc == MK_OP_QKV) {
+            const int G = P.Hq / P.Hkv;
+            reinterpret_cast<float *>(ptr_a)[(size_t)b * P.Hkv * (G + 2) * P.D + out0 + r] = y;
+        } else if (opc == MK_OP_O) {
+            const size_t k = (size_t)b * P.H + out0 + r;
+            reinterpret_cast<float *>(ptr_a)[k] = resid_v[j] + y;
+            reinterpret_cast<float *>(ptr_b)[k] = resid_v[j] + y;
+        } else if (opc == MK_OP_UP) {
+            reinterpret_cast<float *>(ptr_a)[(size_t)b * P.F + out0 + r] = y / (1.0f + __expf(-y)) * u;
+        } else if (opc == MK_OP_DOWN) {
+            atomicAdd(reinterpret_cast<float *>(ptr_a) + (size_t)b * P.H + out0 + r, y);
+        } else if (opc == MK_OP_LM) {
+            reinterpret_cast<float *>(ptr_a)[(size_t)b * P.V + out0 + r] = y;
+            if (y > bv || (y == bv && r < bi)) { bv = y; bi = r; }
+        }
+    }
+    if (opc == MK_OP_LM) {
+#pragma unroll
+        for (int o = 16; o >= MAXB; o >>= 1) {
+            const float ov = __shfl_xor_sync(FULL, bv, o);
+            const int oi = __shfl_xor_sync(FULL, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if (lane < B && !ab && bi != 0x7fffffff) {
+            const unsigned long long key = argmax_key(bv, out0 + bi);
+            if (key > lm_best) {
+                lm_best = key;
+                red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)P.step * B + lane, key);
+            }
+        }
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------- batch 1, rows per warp
 // Batch-1 GEMV tiles with K a multiple of 256 up to 2048 take the
 // row-per-warp path: a tile is NPG pages of 16 rows (or one page of at most

@@ -325,6 +325,7 @@ DEV bool gemv_geom(const KParams &P, const Smem S, const WIns &I, int i, int sl,
 template <int MAXB>
 DEV bool gemv_dispatch(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
                        RingPos &rq, uint32_t &ured, unsigned long long &lm_best, bool &ab) {
+    if (mma_tile(P, I)) return gemv_mma_tile<MAXB>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
     const int nch = ((F(I, P_KC) >> 3) + CONSUMERS - 1) / CONSUMERS;
     constexpr int NCHMAX = MAXB >= 8 ? 1 : (MAXB >= 4 ? 2 : 4);
     if (nch <= 1) return gemv_geom<MAXB, 1>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);

@@ -633,19 +633,35 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     if (tgt->schedule < MK_SCHED_DEFAULT || tgt->schedule > MK_SCHED_TIMED)
         return set_error(MK_ERR_INVALID, "schedule must be one of MK_SCHED_*");
     p.schedule = tgt->schedule == MK_SCHED_BYTES ? MK_SCHED_BYTES : MK_SCHED_TIMED;
-    const int rcap = B > 4 ? 8 : 16;
-    int kn_qkv = tgt->rows_qkv > 0 ? tgt->rows_qkv : pow2_floor(clampi(tile / (2 * H), 1, rcap));
-    int kn_o = tgt->rows_o > 0 ? tgt->rows_o : pow2_floor(clampi(tile / (2 * Hq * D), 1, rcap));
-    int kn_up = tgt->rows_up > 0 ? tgt->rows_up : pow2_floor(clampi(tile / (4 * H), 1, rcap / 2));
+    // batch > 1 with every K a multiple of 512: tensor-core tiles of 16 rows
+    // (K slices of 64 per consumer warp); else batch > 4 keeps 8 rows x 8
+    // sequences in registers
+    const bool mma = H % 512 == 0 && (Hq * D) % 512 == 0 && std::min(F, 2048) % 512 == 0;
+    const int rcap = B > 4 && !mma ? 8 : 16;
+    // tensor-core tiles take 16 rows of any K (two pages of 8 rows at most)
+    const int tile_g = mma ? 2 * tile : tile;
+    int kn_qkv = tgt->rows_qkv > 0 ? tgt->rows_qkv : pow2_floor(clampi(tile_g / (2 * H), 1, rcap));
+    int kn_o = tgt->rows_o > 0 ? tgt->rows_o : pow2_floor(clampi(tile_g / (2 * Hq * D), 1, rcap));
+    int kn_up = tgt->rows_up > 0 ? tgt->rows_up : pow2_floor(clampi(tile_g / (4 * H), 1, rcap / 2));
     int kn_kc = tgt->kchunk_down;
     if (kn_kc <= 0) {
         kn_kc = 8;
         for (int c = 8; c <= std::min(F, 2048); c += 8)
             if (F % c == 0) kn_kc = c;
     }
-    int kn_dn = tgt->rows_down > 0 ? tgt->rows_down : pow2_floor(clampi(tile / (2 * kn_kc), 1, rcap));
-    int kn_lm = tgt->rows_lm > 0 ? tgt->rows_lm : pow2_floor(clampi(tile / (2 * H), 1, rcap));
+    int kn_dn = tgt->rows_down > 0 ? tgt->rows_down : pow2_floor(clampi(tile_g / (2 * kn_kc), 1, rcap));
+    int kn_lm = tgt->rows_lm > 0 ? tgt->rows_lm : pow2_floor(clampi(tile_g / (2 * H), 1, rcap));
     int kn_T = tgt->attn_split > 0 ? tgt->attn_split : clampi(16384 / (2 * D), 16, 256);
+    if (tgt->attn_split <= 0) {
+        // long caches: twice the split length once the attention tasks would
+        // outnumber the workers twice over (per-task costs then dominate)
+        auto attn_tasks = [&](int T) {
+            int64_t n = 0;
+            for (int b = 0; b < B; ++b) n += ceil_div(s->seq_len0[b] + s->max_steps, T);
+            return n * Hkv;
+        };
+        if (2 * kn_T <= 256 && attn_tasks(kn_T) > 2 * (int64_t)num_workers) kn_T *= 2;
+    }
     p.rows_qkv = kn_qkv; p.rows_o = kn_o; p.rows_up = kn_up; p.rows_down = kn_dn; p.kchunk_down = kn_kc;
     p.rows_lm = kn_lm; p.attn_split = kn_T;
     const int rows_group = (G + 2) * D;
@@ -694,7 +710,19 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     if (multi_page(H) && tgt->rows_up <= 0 && F % 16 == 0) kn_up = 16;
     if (multi_page(kn_kc) && tgt->rows_down <= 0) kn_dn = 32;
     p.rows_up = kn_up; p.rows_down = kn_dn; p.rows_lm = kn_lm;
-    const int rmax = B > 4 ? 8 : MAX_TILE_ROWS;  // the batch-8 kernel keeps 8 rows x 8 sequences in registers
+    // the tensor-core tiles need whole rows in at most two pages of 8 or more
+    bool mma_pages = mma;
+    for (int K : {H, Hq * D, kn_kc})
+        if (p.page_bytes / (2 * K) < 8 || K % 512) mma_pages = false;
+    if (B > 4 && !mma_pages) {  // back to 8 rows x 8 sequences in registers
+        if (tgt->rows_qkv <= 0) kn_qkv = std::min(kn_qkv, 8);
+        if (tgt->rows_o <= 0) kn_o = std::min(kn_o, 8);
+        if (tgt->rows_down <= 0) kn_dn = std::min(kn_dn, 8);
+        if (tgt->rows_lm <= 0) kn_lm = std::min(kn_lm, 8);
+        if (tgt->rows_up <= 0) kn_up = std::min(kn_up, 4);
+        p.rows_qkv = kn_qkv; p.rows_o = kn_o; p.rows_up = kn_up; p.rows_down = kn_dn; p.rows_lm = kn_lm;
+    }
+    const int rmax = B > 4 && !mma_pages ? 8 : MAX_TILE_ROWS;
     auto rows_ok = [&](int rows, int K, bool up, bool o) {
         if (rows <= rmax) return true;
         return !o && multi_page(K) && (rows == 32 || rows == 64) && (!up || rows % 16 == 0);

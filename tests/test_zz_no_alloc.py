@@ -55,7 +55,7 @@ def test_static_workspace_rejects_oversized_plans():
     from persistent_megakernel_decode_gb300 import build
     build.build()
     # a plan whose workspace exceeds the static array is refused before any GPU work
-    p = rt.Plan.llama(synth.QWEN3_8B, 4, [2048] * 4, 32, 2081, num_sms=152, smem_per_cta=232448)
+    p = rt.Plan.llama(synth.QWEN3_8B, 4, [2048] * 4, 32, 2081, num_sms=152, smem_per_cta=232448, attn_split=16)
     assert p.info()["workspace_bytes"] > rt.STATIC_WORKSPACE_BYTES
     addr = rt.C.c_uint64(0)
     rc = rt.load().mk_run_static(p.h, 0, 1, 0, 0, None, rt.C.byref(addr))
