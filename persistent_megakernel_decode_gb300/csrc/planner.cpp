@@ -699,6 +699,15 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
                 break;
             }
     }
+    // tensor-core tiles want 8 rows per page: for K = 4096 that is 64 KB, which
+    // three pages of need one activation buffer instead of two
+    const int kmax_rows = std::max(std::max(H, Hq * D), kn_kc);
+    if (tgt->page_bytes <= 0 && mma && p.page_bytes < 16 * kmax_rows && p.abuf_count == 2 && 16 * kmax_rows <= 65536 &&
+        (smem_per_cta - (fixed - p.abuf_bytes)) / (16 * kmax_rows) >= 3) {
+        p.abuf_count = 1;
+        fixed -= p.abuf_bytes;
+        p.page_bytes = 16 * kmax_rows;
+    }
     for (int K : {H, Hq * D, kn_kc})
         if (2 * K > p.page_bytes) return set_error(MK_ERR_UNSUPPORTED, "a weight row does not fit one page");
     // Batch 1 with pages of exactly 16 rows (K = page_bytes / 32, a multiple of
