@@ -584,6 +584,7 @@ DEV bool gemv_mma_tile(const KParams &P, const Smem S, const WIns &I, int i, int
     ring += npg;
     for (int k = 0; k < npg; ++k)
         if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(base + k) % NP], ((base + k) / NP) & 1, 2, i, opc);
+    trace_stamp(P, i, 7);
     // rows past the tile's end read stale bytes of its own pages; their
     // results are never stored
     auto row_ptr = [&](int r) -> const uint8_t * {
@@ -594,7 +595,13 @@ DEV bool gemv_mma_tile(const KParams &P, const Smem S, const WIns &I, int i, int
     const bool bok = g < B;
     const float *xb = S.abuf(sl) + (size_t)(bok ? g : 0) * kc;
     const int kw = kc / CONSUMER_WARPS;
-    float ch[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
+    // eight independent accumulator sets (k16 step x high / low part) so that
+    // the MMAs of a chunk do not wait on each other
+    float acc[8][4];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[q][e] = 0.f;
     for (int k0 = warp * kw; k0 < (warp + 1) * kw; k0 += 64) {
         const int off = k0 + 16 * t;
         const uint4 a00 = *reinterpret_cast<const uint4 *>(w0 + off * 2);
@@ -618,11 +625,18 @@ DEV bool gemv_mma_tile(const KParams &P, const Smem S, const WIns &I, int i, int
         const uint32_t ag8[8] = {a10.x, a10.y, a10.z, a10.w, a11.x, a11.y, a11.z, a11.w};
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-            mma_bf16(ch, ag[2 * s], ag8[2 * s], ag[2 * s + 1], ag8[2 * s + 1], bh[2 * s], bh[2 * s + 1]);
-            mma_bf16(cl, ag[2 * s], ag8[2 * s], ag[2 * s + 1], ag8[2 * s + 1], bl[2 * s], bl[2 * s + 1]);
+            mma_bf16(acc[s], ag[2 * s], ag8[2 * s], ag[2 * s + 1], ag8[2 * s + 1], bh[2 * s], bh[2 * s + 1]);
+            mma_bf16(acc[4 + s], ag[2 * s], ag8[2 * s], ag[2 * s + 1], ag8[2 * s + 1], bl[2 * s], bl[2 * s + 1]);
         }
     }
+    float ch[4], cl[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        ch[e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
+        cl[e] = (acc[4][e] + acc[5][e]) + (acc[6][e] + acc[7][e]);
+    }
     __syncwarp();
+    trace_stamp(P, i, 9);
     if (lane == 0) {
         for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(base + k) % NP]);
         mbar_arrive(&S.act_empty()[sl]);  // activation buffer and slot no longer needed
@@ -642,6 +656,7 @@ DEV bool gemv_mma_tile(const KParams &P, const Smem S, const WIns &I, int i, int
         red[(g + 8) * MAXB + 2 * t + 1] = ch[3] + cl[3];
     }
     consumer_bar();
+    trace_stamp(P, i, 10);
     if (warp != (int)(use % CONSUMER_WARPS)) return false;
     const float *rall = S.red(rb);
     float bv = -INFINITY;
