@@ -5,9 +5,12 @@ oracle (on the host cores) at the model shapes of the workloads.
   (every SM a worker, default tiles: 64 KB pages, the row-per-warp GEMV,
   9 attention splits);
 * the same model at batch 8 with sequence lengths drawn from 512..4096 (the
-  batch-8 kernel: split-K GEMV tiles, 32 KB pages);
+  batch-8 kernel: 16-row tensor-core GEMV tiles in 32 KB pages, 256-position
+  attention splits);
+* two layers of the same model at batches 2, 3 and 4 (the tensor-core tiles
+  of the batch-2 and batch-4 kernels, a partly filled MMA N side);
 * Qwen3-8B shape, batch 1, 2048 cached tokens (head_dim 128, q/k RMSNorm,
-  K = 4096: the split-K path at batch 1).
+  K = 4096: tensor-core tiles at batch 1, row-per-warp MLP-down).
 
 Bars: per-layer residual stream, logits and appended K/V within 1e-2
 normwise; an argmax may differ only where the oracle's top-2 logit gap is
@@ -47,6 +50,15 @@ def test_llama1b_batch8_variable_lengths():
     from harness import run_parity
     w = synth.WORKLOADS["llama1b_b8"]
     run = run_parity(w.shape, synth.seq_lengths(w), 2, [1], seed=w.weight_seed)
+    _check(run)
+
+
+@pytest.mark.parametrize("lengths", [[700, 1300], [5, 900, 2048], [64, 128, 1024, 33]])
+def test_llama1b_two_layers_small_batches(lengths):
+    from dataclasses import replace
+    from harness import run_parity
+    shape = replace(synth.LLAMA_1B, L=2)
+    run = run_parity(shape, lengths, 2, [0, 1], seed=1235)
     _check(run)
 
 
