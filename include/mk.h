@@ -193,8 +193,12 @@ typedef struct {
  * embedding task first) is expanded into tile tasks, events are derived with
  * the gcd/lcm rule, tasks are linearised so each event's successors are
  * contiguous ("MPK code walkthrough", building the SM-level DAG), placed
- * longest-first within each successor range and dealt to workers by bytes.
- * The plan is checked by simulating its queues.  *out receives a plan the
+ * longest-first within each successor range, and dealt to workers by the
+ * target's schedule (MK_SCHED_*: by default the time-model list scheduler;
+ * MK_SCHED_BYTES deals by bytes).  Tile sizes follow the kernel paths: the
+ * batch-1 row-per-warp GEMV (K <= 2048), 16-row tensor-core tiles when every
+ * K is a multiple of 512, else split-K tiles.  The plan is checked by
+ * simulating its queues.  *out receives a plan the
  * caller frees with mk_free().  Returns MK_ERR_INVALID / MK_ERR_UNSUPPORTED
  * / MK_ERR_DEADLOCK on failure (nothing allocated). */
 int mk_plan(const mk_model_desc *model, const mk_step_desc *step, const mk_target_desc *target,
