@@ -322,12 +322,16 @@ int mk_sync_status(mk_plan_t plan, void *workspace, void *stream, mk_error_recor
 /* Copy the event counters (uint32 [num_events]) from the workspace to host. */
 int mk_read_counters(mk_plan_t plan, void *workspace, uint32_t *out);
 
-/* Copy the per-instruction trace to host: uint64 [total_slots, 16] =
- * (opcode | task << 32, consumer start, activation ready, consumer done,
- * loader issue start, loader issue end, first page ready, last page ready,
- * pages not ready on arrival, page loop end, reduction end, epilogue end,
- * activation not ready on arrival, activation handed over, 2 reserved),
- * globaltimer ns for times.  Only filled by runs with MK_RUN_TRACE. */
+/* Copy the per-instruction trace to host: uint64 [total_slots, 16]:
+ *   [0] opcode | task << 32      [1] consumer start      [2] activation loader: events met
+ *   [3] consumer done            [4] loader issue start  [5] loader issue end
+ *   [6..10] stamps of consumer thread 0 inside the op (attention: K pages ready, scores,
+ *           V pages ready, P.V, partial written and arrived; tensor-core and GLM GEMM tiles:
+ *           [7] pages ready, [9] K loop end, [10] reduction barrier passed; GLM A0: [9] loads
+ *           and sum of squares, [10] reduction)
+ *   [13] activation handed to the consumers   [14] published   [15] publisher saw the slot done
+ * globaltimer ns (the GPU's globaltimer advances in 256 ns steps on GB300); 0 = not stamped.
+ * Only filled by runs with MK_RUN_TRACE. */
 int mk_read_trace(mk_plan_t plan, void *workspace, uint64_t *out);
 
 /* Allocation-free variant of mk_run (no counterpart on the source pages).
