@@ -141,3 +141,13 @@ def test_poisoned_activation_buffers_are_overwritten_before_use():
         sess.sync()
         lref, href, _ = orc.decode_step(oracle_shape(shape), hw, kh, vh, [64 + s], [17 + s])
         assert normwise(sess.logits.cpu().numpy().astype(np.float64), lref) < 1e-2
+
+
+def test_launch_probe_runs_on_the_interpreter_grid():
+    """The empty-kernel probe the bench times: cooperative and plain launches
+    of the interpreter's grid complete without error."""
+    s = torch.cuda.Stream()
+    n = torch.cuda.get_device_properties(0).multi_processor_count
+    for coop in (True, False):
+        rt.launch_probe(n, coop, s)
+    s.synchronize()

@@ -231,3 +231,8 @@ def test_planner_rejects(bad, code):
 def test_argmax_key_decoding():
     assert rt.load().mk_argmax_index(0xFFFFFFFF) == 0
     assert rt.load().mk_argmax_index((123 << 32) | (0xFFFFFFFF - 77)) == 77
+
+
+def test_launch_probe_rejects_an_empty_grid():
+    rc = rt.load().mk_launch_probe(0, 1, None)
+    assert rc == rt.MK_ERR_INVALID and b"num_workers" in rt.load().mk_last_error()
