@@ -343,6 +343,28 @@ def run_mk(args, w, rank, world, dist):
         "device_error": int(rec.code),
     }
     print(json.dumps(line), flush=True)
+    if args.trace_out:
+        write_trace(args.trace_out, sess, stream, step_ms)
+
+
+def write_trace(path, sess, stream, step_ms):
+    """One traced step (step 1 after a fresh step 0, host tokens) and its
+    summaries: per-opcode shares, the (layer, op) timeline and per-layer means.
+    The stamps are global stores of their own, so the traced step runs a
+    little slower than the timed ones; both spans are written."""
+    import torch
+    from persistent_megakernel_decode_gb300 import trace as tr
+    with torch.cuda.stream(stream):
+        sess.run(0, 1, host_tokens=True)
+        sess.run(1, 1, host_tokens=True, trace=True)
+    rec = sess.sync()
+    t = sess.trace()
+    tasks = sess.plan.export()[3]
+    rows = tr.timeline(t, tasks)
+    out = {"device_error": int(rec.code), "timed_step_us_median": float(np.median(step_ms)) * 1e3,
+           "summary": tr.summarize(t), "layer_profile": tr.layer_profile(rows), "timeline": rows}
+    with open(path, "w") as f:
+        json.dump(out, f, indent=1)
 
 
 def run_glm(args, rank, world, dist):
@@ -506,6 +528,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the side legs (per-op and CUDA-Graph launches, empty-kernel probe)")
     ap.add_argument("--knob", action="append", default=[], help="planner knob, e.g. attn_split=512")
+    ap.add_argument("--trace-out", default="",
+                    help="after the bench line, run one traced step and write its timeline (JSON) here")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N decoder layers (a small case for profiling, not a bench line)")
     args = ap.parse_args()

@@ -8,7 +8,8 @@ oracle (on the host cores) at the model shapes of the workloads.
   batch-8 kernel: 16-row tensor-core GEMV tiles in 32 KB pages, 256-position
   attention splits);
 * two layers of the same model at batches 2, 3 and 4 (the tensor-core tiles
-  of the batch-2 and batch-4 kernels, a partly filled MMA N side);
+  of the batch-2 and batch-4 kernels, a partly filled MMA N side), and at
+  batch 8 over 32 teacher-forced steps (256 argmax samples);
 * Qwen3-8B shape, batch 1, 2048 cached tokens (head_dim 128, q/k RMSNorm,
   K = 4096: tensor-core tiles at batch 1, row-per-warp MLP-down).
 
@@ -60,6 +61,20 @@ def test_llama1b_two_layers_small_batches(lengths):
     shape = replace(synth.LLAMA_1B, L=2)
     run = run_parity(shape, lengths, 2, [0, 1], seed=1235)
     _check(run)
+
+
+def test_llama1b_two_layers_batch8_argmax_over_32_steps():
+    """The greedy-argmax bar at the Llama-1B width: 32 teacher-forced steps of
+    8 sequences (lengths from 512..4096) = 256 (step, sequence) samples,
+    at least 99 % identical to the oracle's."""
+    from dataclasses import replace
+    from harness import run_parity
+    w = synth.WORKLOADS["llama1b_b8"]
+    shape = replace(synth.LLAMA_1B, L=2)
+    run = run_parity(shape, synth.seq_lengths(w), 32, range(32), seed=1236)
+    _check(run)
+    m, t = run.matches()
+    assert t == 256 and m >= 0.99 * t, (m, t)
 
 
 def test_qwen3_8b_batch1():
