@@ -9,6 +9,9 @@ lmax, 16], see ``mk_read_trace``):
 [2]   the activation loader has seen every wait of the slot met
 [3]   consumer warp 0 is done with the slot
 [4]   loader starts issuing the slot's weight pages, [5] has issued them
+[6..10] stamps inside the op (attention: K pages ready, scores, V pages
+      ready, P.V, partial written; tensor-core tiles: [7] pages ready, [9] K
+      loop done, [10] reduction barrier passed)
 [13]  the activation is handed to the consumers (0 when the slot skipped it)
 [14]  the publisher has added the slot's signals, [15] it saw the slot done
 ====  ======================================================================
@@ -28,6 +31,7 @@ import numpy as np
 from .runtime import OP_NAMES
 
 T_OPC, T_START, T_MET, T_DONE, T_LSTART, T_LEND, T_HANDED, T_PUB, T_SEEN = 0, 1, 2, 3, 4, 5, 13, 14, 15
+T_INNER = (6, 7, 8, 9, 10)  # stamps inside an op (attention: K pages, scores, V pages, P.V, partial out)
 
 
 def _valid(trace: np.ndarray) -> np.ndarray:
@@ -37,8 +41,9 @@ def _valid(trace: np.ndarray) -> np.ndarray:
 
 def summarize(trace: np.ndarray) -> dict:
     """Per-opcode busy time (consumer start to done), its share, the mean wait
-    for the activation hand-off, the publish latency (done to published) and
-    the loader's lead (issue start before the consumers reach the slot);
+    for the activation hand-off, the publish latency (done to published), the
+    loader's lead (issue start before the consumers reach the slot) and the
+    mean time of each stamp inside the op from the hand-off (``inner_us``);
     the SM-active fraction is the busy time over workers x span."""
     op = (trace[..., T_OPC] & 0xFFFFFFFF).astype(np.int64)
     t = trace.astype(np.float64)
@@ -62,6 +67,11 @@ def summarize(trace: np.ndarray) -> dict:
         if r[T_LSTART] > 0:
             d["loader_lead"] += r[T_START] - r[T_LSTART]
             d["n_lead"] += 1
+        base = max(r[T_START], r[T_HANDED])
+        for k in T_INNER:
+            if r[k] > 0:
+                d[f"in{k}"] += r[k] - base
+                d[f"n_in{k}"] += 1
     busy = sum(d["busy"] for d in per.values())
     out = {"span_us": span / 1e3, "workers": int(trace.shape[0]),
            "sm_active_frac": busy / (span * trace.shape[0]) if span > 0 else 0.0, "ops": {}}
@@ -74,6 +84,9 @@ def summarize(trace: np.ndarray) -> dict:
             e["publish_us"] = d["publish"] / d["n_pub"] / 1e3
         if d["n_lead"]:
             e["loader_lead_us"] = d["loader_lead"] / d["n_lead"] / 1e3
+        inner = {str(j): d[f"in{j}"] / d[f"n_in{j}"] / 1e3 for j in T_INNER if d[f"n_in{j}"]}
+        if inner:
+            e["inner_us"] = inner
         out["ops"][k] = e
     return out
 

@@ -46,6 +46,16 @@ def test_summarize_shares_and_active_fraction(fake):
     assert s["ops"]["qkv"]["publish_us"] == pytest.approx((0.4 + 0.2) / 2)
     assert s["ops"]["qkv"]["loader_lead_us"] == pytest.approx((1.0 + 0.0) / 2)
     assert s["ops"]["o"]["act_wait_us"] == pytest.approx(8.5)
+    assert "inner_us" not in s["ops"]["qkv"]
+
+
+def test_summarize_inner_stamps(fake):
+    t, _ = fake
+    b = 1_000_000
+    t[1, 1, 6] = b + 8500     # attention: K pages 1 us after its hand-off at 7.5
+    t[1, 1, 10] = b + 11500
+    s = tr.summarize(t)
+    assert s["ops"]["attn"]["inner_us"] == pytest.approx({"6": 1.0, "10": 4.0})
 
 
 def test_timeline_rows(fake):
