@@ -765,58 +765,17 @@ DEV void rpw_row(const uint8_t *wrow, int lane, const XRow &x, uint64_t &acc) {
     }
 }
 
-// KG = K / 256 chunks per lane, NPG = pages of the tile.  `handoff`: this
-// slot took the activation hand-off (the caller waited for activation slot
-// sl); x is reloaded from the slot's buffer when its input changed.  Returns
-// true (the warp wrote global memory).
-template <int KG, int NPG>
-DEV bool gemv_rpw(const KParams &P, const Smem S, const Dec &d, int i, bool handoff, int sl, const float *slot,
-                  XRow &x, uint32_t &ring, RingPos &rq, unsigned long long &lm_best, bool &ab) {
-    constexpr int V = 2 * NPG;  // rows of this warp: w + 8 v
+// Epilogue of the row-per-warp tiles: V row sums per warp (rows w + 8 v),
+// reduced across the warp, then stored by op: QKV rows, O rows plus their
+// residual (both residual copies), SiLU(gate) x up for MLP-up (the up row of
+// gate row r is r + nrows), atomic adds for MLP-down K chunks, logits and the
+// running argmax for the LM head.
+template <int V>
+DEV bool rpw_finish(const KParams &P, const Dec &d, const uint64_t (&acc)[V], const float (&res)[V],
+                    unsigned long long &lm_best, bool ab) {
     const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
-    const int opc = d.opc, nrows = d.nrows, row_bytes = d.kc * 2, out0 = d.out0;
+    const int opc = d.opc, nrows = d.nrows, out0 = d.out0;
     const uint64_t ptr_a = d.out, ptr_b = d.out2;
-    float res[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) res[v] = 0.f;
-    if (handoff) {
-        const long long key = ((long long)d.row << 32) | (uint32_t)d.k0;
-        if (key != x.key) {
-            const float *xs = S.abuf(sl);
-#pragma unroll
-            for (int k = 0; k < KG; ++k) {
-                const float4 a = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8);
-                const float4 c = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8 + 4);
-                x.v[k][0] = pack2(a.x, a.y); x.v[k][1] = pack2(a.z, a.w);
-                x.v[k][2] = pack2(c.x, c.y); x.v[k][3] = pack2(c.z, c.w);
-            }
-            x.key = key;
-        }
-        if (opc == MK_OP_O) {  // O tiles have at most RESID_ROWS rows
-            const float *rs = slot_resid(P, const_cast<float *>(slot));
-#pragma unroll
-            for (int v = 0; v < V; ++v)
-                if (warp + 8 * v < RESID_ROWS) res[v] = rs[warp + 8 * v];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // x and the residual rows are in registers
-    }
-    // rows w and w + 8 of every page of the tile (rows past the tile's end
-    // hold stale page bytes; their results are not stored)
-    uint64_t acc[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] = 0;
-#pragma unroll
-    for (int pg = 0; pg < NPG; ++pg) {
-        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
-        const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
-        rpw_row<KG>(page + (size_t)warp * row_bytes, lane, x, acc[2 * pg]);
-        rpw_row<KG>(page + (size_t)(warp + 8) * row_bytes, lane, x, acc[2 * pg + 1]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
-        rq.next(P.num_pages);
-    }
-    ring += NPG;
     // after the butterfly, lanes L with L % (32 / V) == 0 hold row w + 8 (L / (32 / V))
     float y[V];
 #pragma unroll
@@ -859,6 +818,117 @@ DEV bool gemv_rpw(const KParams &P, const Smem S, const Dec &d, int i, bool hand
         }
     }
     return true;
+}
+
+// KG = K / 256 chunks per lane, NPG = pages of the tile.  `handoff`: this
+// slot took the activation hand-off (the caller waited for activation slot
+// sl); x is reloaded from the slot's buffer when its input changed.  Returns
+// true (the warp wrote global memory).
+template <int KG, int NPG>
+DEV bool gemv_rpw(const KParams &P, const Smem S, const Dec &d, int i, bool handoff, int sl, const float *slot,
+                  XRow &x, uint32_t &ring, RingPos &rq, unsigned long long &lm_best, bool &ab) {
+    constexpr int V = 2 * NPG;  // rows of this warp: w + 8 v
+    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int opc = d.opc, row_bytes = d.kc * 2;
+    float res[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) res[v] = 0.f;
+    if (handoff) {
+        const long long key = ((long long)d.row << 32) | (uint32_t)d.k0;
+        if (key != x.key) {
+            const float *xs = S.abuf(sl);
+#pragma unroll
+            for (int k = 0; k < KG; ++k) {
+                const float4 a = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8);
+                const float4 c = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8 + 4);
+                x.v[k][0] = pack2(a.x, a.y); x.v[k][1] = pack2(a.z, a.w);
+                x.v[k][2] = pack2(c.x, c.y); x.v[k][3] = pack2(c.z, c.w);
+            }
+            x.key = key;
+        }
+        if (opc == MK_OP_O) {  // O tiles have at most RESID_ROWS rows
+            const float *rs = slot_resid(P, const_cast<float *>(slot));
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+                if (warp + 8 * v < RESID_ROWS) res[v] = rs[warp + 8 * v];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // x and the residual rows are in registers
+    }
+    // rows w and w + 8 of every page of the tile (rows past the tile's end
+    // hold stale page bytes; their results are not stored)
+    uint64_t acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = 0;
+#pragma unroll
+    for (int pg = 0; pg < NPG; ++pg) {
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
+        const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
+        rpw_row<KG>(page + (size_t)warp * row_bytes, lane, x, acc[2 * pg]);
+        rpw_row<KG>(page + (size_t)(warp + 8) * row_bytes, lane, x, acc[2 * pg + 1]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
+        rq.next(P.num_pages);
+    }
+    ring += NPG;
+    return rpw_finish<V>(P, d, acc, res, lm_best, ab);
+}
+
+// Batch-1 tiles whose K is too long for x in registers (a multiple of 256
+// above 2048, up to 4096) in pages of 8 rows: warp w computes row w of every
+// page over the whole K, reading its lane's 8-wide chunks of x (l, l + 32,
+// ...) from the activation slot in shared memory; two accumulators per row.
+// The slot is released after the last page, so these tiles always take the
+// hand-off.  MLP-up tiles are 8 gate rows (page 0) and their 8 up rows (page 1).
+constexpr int RPW_WIDE_KMAX = 4096;
+DEV bool rpw_wide_tile(const KParams &P, const Dec &d) {
+    if (P.B != 1 || d.opc < MK_OP_QKV || d.opc > MK_OP_LM || d.opc == MK_OP_ATTN) return false;
+    if (d.kc % 256 || d.kc <= 2048 || d.kc > RPW_WIDE_KMAX || P.page_bytes != 16 * d.kc) return false;
+    if (d.opc == MK_OP_UP) return d.npg == 2 && d.nrows == 8;
+    return d.npg == 1 ? d.nrows <= 8 : d.npg == 2 && d.nrows <= 16;
+}
+
+template <int NPG, int KG = RPW_WIDE_KMAX / 256>
+DEV bool gemv_rpw_wide(const KParams &P, const Smem S, const Dec &d, int i, int sl, const float *slot,
+                       uint32_t &ring, RingPos &rq, unsigned long long &lm_best, bool &ab) {
+    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int opc = d.opc, row_bytes = d.kc * 2, kg = d.kc >> 8;
+    float res[NPG];
+#pragma unroll
+    for (int v = 0; v < NPG; ++v) res[v] = 0.f;
+    if (opc == MK_OP_O) {
+        const float *rs = slot_resid(P, const_cast<float *>(slot));
+#pragma unroll
+        for (int v = 0; v < NPG; ++v)
+            if (warp + 8 * v < RESID_ROWS) res[v] = rs[warp + 8 * v];
+    }
+    const float *xs = S.abuf(sl);
+    uint64_t acc[NPG];
+#pragma unroll
+    for (int pg = 0; pg < NPG; ++pg) {
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
+        const uint8_t *wrow = S.pages() + (size_t)rq.p * P.page_bytes + (size_t)warp * row_bytes;
+        uint64_t a0 = 0, a1 = 0;
+#pragma unroll
+        for (int k = 0; k < KG; ++k) {
+            if (k >= kg) break;
+            const uint4 w = *reinterpret_cast<const uint4 *>(wrow + (lane + 32 * k) * 16);
+            const float4 xa = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8);
+            const float4 xb = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8 + 4);
+            fma2(a0, bf16x2_pair(w.x), pack2(xa.x, xa.y));
+            fma2(a1, bf16x2_pair(w.y), pack2(xa.z, xa.w));
+            fma2(a0, bf16x2_pair(w.z), pack2(xb.x, xb.y));
+            fma2(a1, bf16x2_pair(w.w), pack2(xb.z, xb.w));
+        }
+        acc[pg] = pack2(sum2(a0), sum2(a1));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
+        rq.next(P.num_pages);
+    }
+    ring += NPG;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // x and the residual rows are no longer read
+    return rpw_finish<NPG>(P, d, acc, res, lm_best, ab);
 }
 
 // Split-KV attention of one (sequence, kv group, split).  Each of the 8

@@ -396,7 +396,13 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
                 else if (kg <= 4) gemv_rpw_pages<4>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
                 else gemv_rpw_pages<8>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
             } else if constexpr (FL != FL_LEAN) {
-                wrote = gemv_dispatch<MAXB>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
+                bool wide = false;
+                if constexpr (MAXB == 1) {
+                    wide = rpw_wide_tile(P, d);
+                    if (wide && d.npg <= 1) gemv_rpw_wide<1>(P, S, d, i, sl, slot, ring, rq, lm_best, ab);
+                    else if (wide) gemv_rpw_wide<2>(P, S, d, i, sl, slot, ring, rq, lm_best, ab);
+                }
+                if (!wide) wrote = gemv_dispatch<MAXB>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
             } else {  // the planner picks the lean instance only for plans without such tiles
                 if (lane == 0 && !ab) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 2);
                 ab = true;
