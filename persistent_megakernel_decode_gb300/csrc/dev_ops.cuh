@@ -874,25 +874,27 @@ DEV bool gemv_rpw(const KParams &P, const Smem S, const Dec &d, int i, bool hand
     return rpw_finish<V>(P, d, acc, res, lm_best, ab);
 }
 
-// Batch-1 tiles whose K is too long for x in registers (a multiple of 256
-// above 2048, up to 4096) in pages of 8 rows: warp w computes row w of every
-// page over the whole K, reading its lane's 8-wide chunks of x (l, l + 32,
-// ...) from the activation slot in shared memory; two accumulators per row.
-// The slot is released after the last page, so these tiles always take the
-// hand-off.  MLP-up tiles are 8 gate rows (page 0) and their 8 up rows (page 1).
-constexpr int RPW_WIDE_KMAX = 4096;
+// Batch-1 tiles whose K (4096) is too long for x in registers, in pages of 8
+// rows: warp w computes row w of every page over the whole K, reading its
+// lane's 8-wide chunks of x (l, l + 32, ...) from the activation slot in
+// shared memory once for all pages of the tile (it waits for both pages
+// first; the ring holds three).  The slot is released after the last page, so
+// these tiles always take the hand-off.  MLP-up tiles are 8 gate rows (page 0)
+// and their 8 up rows (page 1).
+constexpr int RPW_WIDE_K = 4096;
 DEV bool rpw_wide_tile(const KParams &P, const Dec &d) {
     if (P.B != 1 || d.opc < MK_OP_QKV || d.opc > MK_OP_LM || d.opc == MK_OP_ATTN) return false;
-    if (d.kc % 256 || d.kc <= 2048 || d.kc > RPW_WIDE_KMAX || P.page_bytes != 16 * d.kc) return false;
+    if (d.kc != RPW_WIDE_K || P.page_bytes != 16 * d.kc || P.num_pages < 2) return false;
     if (d.opc == MK_OP_UP) return d.npg == 2 && d.nrows == 8;
     return d.npg == 1 ? d.nrows <= 8 : d.npg == 2 && d.nrows <= 16;
 }
 
-template <int NPG, int KG = RPW_WIDE_KMAX / 256>
+template <int NPG>
 DEV bool gemv_rpw_wide(const KParams &P, const Smem S, const Dec &d, int i, int sl, const float *slot,
                        uint32_t &ring, RingPos &rq, unsigned long long &lm_best, bool &ab) {
+    constexpr int KG = RPW_WIDE_K / 256;
     const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
-    const int opc = d.opc, row_bytes = d.kc * 2, kg = d.kc >> 8;
+    const int opc = d.opc, row_bytes = d.kc * 2;
     float res[NPG];
 #pragma unroll
     for (int v = 0; v < NPG; ++v) res[v] = 0.f;
@@ -902,32 +904,43 @@ DEV bool gemv_rpw_wide(const KParams &P, const Smem S, const Dec &d, int i, int 
         for (int v = 0; v < NPG; ++v)
             if (warp + 8 * v < RESID_ROWS) res[v] = rs[warp + 8 * v];
     }
-    const float *xs = S.abuf(sl);
-    uint64_t acc[NPG];
+    const uint8_t *wrow[NPG];
+    int pid[NPG];
 #pragma unroll
     for (int pg = 0; pg < NPG; ++pg) {
         if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
-        const uint8_t *wrow = S.pages() + (size_t)rq.p * P.page_bytes + (size_t)warp * row_bytes;
-        uint64_t a0 = 0, a1 = 0;
-#pragma unroll
-        for (int k = 0; k < KG; ++k) {
-            if (k >= kg) break;
-            const uint4 w = *reinterpret_cast<const uint4 *>(wrow + (lane + 32 * k) * 16);
-            const float4 xa = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8);
-            const float4 xb = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8 + 4);
-            fma2(a0, bf16x2_pair(w.x), pack2(xa.x, xa.y));
-            fma2(a1, bf16x2_pair(w.y), pack2(xa.z, xa.w));
-            fma2(a0, bf16x2_pair(w.z), pack2(xb.x, xb.y));
-            fma2(a1, bf16x2_pair(w.w), pack2(xb.z, xb.w));
-        }
-        acc[pg] = pack2(sum2(a0), sum2(a1));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
+        pid[pg] = rq.p;
+        wrow[pg] = S.pages() + (size_t)rq.p * P.page_bytes + (size_t)warp * row_bytes;
         rq.next(P.num_pages);
     }
-    ring += NPG;
+    const float *xs = S.abuf(sl);
+    uint64_t a0[NPG], a1[NPG];
+#pragma unroll
+    for (int pg = 0; pg < NPG; ++pg) a0[pg] = a1[pg] = 0;
+#pragma unroll
+    for (int k = 0; k < KG; ++k) {
+        const float4 xa = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8);
+        const float4 xb = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8 + 4);
+        const uint64_t x0 = pack2(xa.x, xa.y), x1 = pack2(xa.z, xa.w), x2 = pack2(xb.x, xb.y), x3 = pack2(xb.z, xb.w);
+#pragma unroll
+        for (int pg = 0; pg < NPG; ++pg) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(wrow[pg] + (lane + 32 * k) * 16);
+            fma2(a0[pg], bf16x2_pair(w.x), x0);
+            fma2(a1[pg], bf16x2_pair(w.y), x1);
+            fma2(a0[pg], bf16x2_pair(w.z), x2);
+            fma2(a1[pg], bf16x2_pair(w.w), x3);
+        }
+    }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // x and the residual rows are no longer read
+    if (lane == 0) {
+#pragma unroll
+        for (int pg = 0; pg < NPG; ++pg) mbar_arrive(&S.empty()[pid[pg]]);
+        mbar_arrive(&S.act_empty()[sl]);  // x and the residual rows are no longer read
+    }
+    ring += NPG;
+    uint64_t acc[NPG];
+#pragma unroll
+    for (int pg = 0; pg < NPG; ++pg) acc[pg] = pack2(sum2(a0[pg]), sum2(a1[pg]));
     return rpw_finish<NPG>(P, d, acc, res, lm_best, ab);
 }
 
