@@ -653,14 +653,15 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     int kn_lm = tgt->rows_lm > 0 ? tgt->rows_lm : pow2_floor(clampi(tile_g / (2 * H), 1, rcap));
     int kn_T = tgt->attn_split > 0 ? tgt->attn_split : clampi(16384 / (2 * D), 16, 256);
     if (tgt->attn_split <= 0) {
-        // long caches: twice the split length once the attention tasks would
-        // outnumber the workers twice over (per-task costs then dominate)
+        // long caches: double the split length (up to 256 positions) while the
+        // attention tasks outnumber the workers -- a second round of tasks costs
+        // a whole per-task latency, a longer split only its extra positions
         auto attn_tasks = [&](int T) {
             int64_t n = 0;
             for (int b = 0; b < B; ++b) n += ceil_div(s->seq_len0[b] + s->max_steps, T);
             return n * Hkv;
         };
-        if (2 * kn_T <= 256 && attn_tasks(kn_T) > 2 * (int64_t)num_workers) kn_T *= 2;
+        while (2 * kn_T <= 256 && attn_tasks(kn_T) > (int64_t)num_workers) kn_T *= 2;
     }
     p.rows_qkv = kn_qkv; p.rows_o = kn_o; p.rows_up = kn_up; p.rows_down = kn_dn; p.kchunk_down = kn_kc;
     p.rows_lm = kn_lm; p.attn_split = kn_T;
