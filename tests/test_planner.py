@@ -88,6 +88,23 @@ def test_planner_matches_oracle_qwen3_8b_b1():
     _compare(synth.QWEN3_8B, 1, [2048], 32, workers=148)
 
 
+@pytest.mark.parametrize("name,shape,B,steps,want", [
+    ("llama1b_b1", synth.LLAMA_1B, 1, 128, 128),   # 1152 positions / 128 = 9 splits x 8 kv heads = 72 tasks
+    ("qwen3_8b_b1", synth.QWEN3_8B, 1, 32, 128),   # 2080 / 64 = 33 x 8 = 264 > 152; / 128 = 17 x 8 = 136
+    ("llama1b_b8", synth.LLAMA_1B, 8, 64, 256),    # thousands of tasks: capped at 256 positions
+    ("tiny", synth.TINY, 1, 8, 128),               # 72 positions: one split per kv head
+])
+def test_attention_split_doubles_while_tasks_outnumber_workers(name, shape, B, steps, want):
+    seq0 = synth.seq_lengths(synth.WORKLOADS[name])
+    p = rt.Plan.llama(shape, B, seq0, steps, max(seq0) + steps + 1, **GB300)
+    T = p.info()["attn_split"]
+    assert T == want
+    tasks = sum(-(-(s + steps) // T) for s in seq0) * shape.Hkv
+    assert T == 256 or tasks <= GB300["num_sms"]
+    if T > 16384 // (2 * shape.D):  # doubled: the half split gave more tasks than workers
+        assert sum(-(-(s + steps) // (T // 2)) for s in seq0) * shape.Hkv > GB300["num_sms"]
+
+
 def test_planner_queue_simulates_over_steps():
     p = rt.Plan.llama(synth.TINY, 2, [3, 70], 5, 80, **GB300)
     q, ids, th, tasks = p.export()
