@@ -134,6 +134,34 @@ def test_rope_half_invariants():
     assert math.isclose(d1, d2, rel_tol=1e-9, abs_tol=1e-9)          # depends on m - n only
 
 
+def _rope_angles_ok(rope_fn, theta=1e4):
+    """Each pair (i, i + 32) of a 64-wide slice is rotated by +pos * theta^(-i/32),
+    read back with atan2 (direction and frequency, not just norms)."""
+    rng = np.random.default_rng(11)
+    x = rng.normal(0, 1, 64)
+    for pos in (1, 9, 8191):
+        y = rope_fn(x, pos, theta)
+        for i in range(32):
+            a, b, c, d = x[i], x[i + 32], y[i], y[i + 32]
+            ang = math.atan2(a * d - b * c, a * c + b * d)
+            want = math.remainder(pos * theta ** (-i / 32), 2 * math.pi)
+            if abs(math.remainder(ang - want, 2 * math.pi)) > 1e-9:
+                return False
+    return True
+
+
+def test_rope_half_rotation_direction_and_frequency():
+    assert _rope_angles_ok(glm.rope_half)
+
+
+def test_rope_angle_pin_catches_a_planted_sign_error():
+    """The invariants above (pair norms, identity at 0, relative position) all
+    hold for a rotation the wrong way; the angle pin does not."""
+    def wrong_way(x, pos, theta):
+        return glm.rope_half(x, -np.asarray(pos, dtype=np.float64), theta)
+    assert not _rope_angles_ok(wrong_way)
+
+
 def test_rmsnorm_unit_weight_invariant():
     rng = np.random.default_rng(10)
     h = rng.normal(0, 3, (4, 6144))
@@ -177,3 +205,12 @@ def test_forward_small_block_consistency(seed):
     a = out["qkva"][:, kv_end:]
     b = out["latent"][0, :, sh.kvlora:]
     assert np.allclose(a[:, :32] ** 2 + a[:, 32:] ** 2, b[:, :32] ** 2 + b[:, 32:] ** 2, rtol=2e-2, atol=1e-6)
+    # Q-B and Indexer-Q: the GEMM of the re-quantised q-lora, RoPE on the last 64 of each head only
+    for name, mat, heads, hd in (("q", "qb", sh.q_heads, sh.q_head_dim), ("iq", "iq", sh.idx_heads, sh.idx_dim)):
+        g = glm.fp8_gemm(out["qb"], out["qb_s"], wts[mat], wts[mat + "_s"]).reshape(sh.M, heads, hd)
+        r = hd - sh.rope
+        assert np.array_equal(out[name][:, :, :r], g[:, :, :r])
+        got, ref = out[name][:, :, r:], g[:, :, r:]
+        assert not np.array_equal(got, ref)                     # the slice was rotated
+        assert np.allclose(got[..., :32] ** 2 + got[..., 32:] ** 2, ref[..., :32] ** 2 + ref[..., 32:] ** 2,
+                           rtol=2e-2, atol=1e-9)
