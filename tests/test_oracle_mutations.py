@@ -1,0 +1,69 @@
+"""Planted mistakes in the C oracle (no GPU): each test compiles a copy of the
+oracle with one plausible error -- a sign, an index, a scale, a missing term --
+and checks that one of the oracle's pins fails on it.  This is what makes the
+pins a check of the oracle rather than of themselves."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import test_oracle_forward as pins
+from oracle import forward as orc
+
+HERE = os.path.dirname(os.path.abspath(orc.__file__))
+
+MUTATIONS = {
+    # RoPE rotating the wrong way
+    "rope_sign": ("        v[i] = a * c - b * s;\n        v[i + half] = a * s + b * c;",
+                  "        v[i] = a * c + b * s;\n        v[i + half] = -a * s + b * c;",
+                  pins.test_rope_angles_and_invariants),
+    # RoPE frequencies theta^(-i/D) instead of theta^(-2i/D)
+    "rope_freq": ("pow(theta, -2.0 * i / D)", "pow(theta, -1.0 * i / D)", pins.test_rope_angles_and_invariants),
+    # scores scaled by 1/D instead of 1/sqrt(D)
+    "softmax_scale": ("REAL inv = (REAL)(1.0 / sqrt((double)D));", "REAL inv = (REAL)(1.0 / (double)D);",
+                      pins.test_attention_special_cases),
+    # eps added outside the square root
+    "rms_eps": ("sqrt((double)ss / n + eps)", "(sqrt((double)ss / n) + eps)", pins.test_rmsnorm_closed_form),
+    # query head j reading kv head j mod Hkv instead of j / (Hq / Hkv)
+    "gqa_map": ("int g = j / G;", "int g = j % Hkv;", pins.test_step_attention_block_through_identity_output),
+    # attention over the cached tokens only, without the appended one
+    "attn_len": ("FN(attend)(q + j * D, kcache + base, vcache + base, p + 1, D, o + j * D, scr);",
+                 "FN(attend)(q + j * D, kcache + base, vcache + base, p, D, o + j * D, scr);",
+                 pins.test_step_attention_block_through_identity_output),
+    # SwiGLU without the SiLU
+    "silu": ("gt[i] = g / (1 + (REAL)exp(-(double)g)) * ut[i];", "gt[i] = g * ut[i];", pins.test_step_mlp_block),
+    # the attention output replacing the residual instead of adding to it
+    "residual": ("            FN(matvec)(w->wo[l], H, Hq * D, o, t1, nthreads);\n"
+                 "            for (int i = 0; i < H; i++) h[i] += t1[i];",
+                 "            FN(matvec)(w->wo[l], H, Hq * D, o, t1, nthreads);\n"
+                 "            for (int i = 0; i < H; i++) h[i] = t1[i];",
+                 pins.test_step_attention_block_through_identity_output),
+    # the final RMSNorm skipped before the LM head
+    "final_norm": ("        FN(rmsnorm)(h, H, w->norm_final, sh->eps, x);\n        FN(matvec)(w->lm_head, V, H, x,",
+                   "        memcpy(x, h, sizeof(REAL) * H);\n        FN(matvec)(w->lm_head, V, H, x,",
+                   pins.test_step_with_zeroed_output_projections),
+}
+
+
+def _build_mutant(tmp_path, old, new):
+    src = open(os.path.join(HERE, "forward_impl.h")).read()
+    assert src.count(old) == 1, old
+    d = tmp_path / "src"
+    d.mkdir()
+    shutil.copy(os.path.join(HERE, "forward.c"), d / "forward.c")
+    (d / "forward_impl.h").write_text(src.replace(old, new))
+    so = tmp_path / "liboracle_mutant.so"
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", str(so), str(d / "forward.c"), "-lm"])
+    return str(so)
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pin_catches_planted_mistake(name, tmp_path, monkeypatch):
+    old, new, pin = MUTATIONS[name]
+    pin()  # the pin holds on the real oracle
+    so = _build_mutant(tmp_path, old, new)
+    monkeypatch.setattr(orc, "_lib", None)
+    monkeypatch.setattr(orc, "build", lambda force=False: so)
+    with pytest.raises(AssertionError):
+        pin()
