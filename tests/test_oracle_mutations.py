@@ -67,3 +67,49 @@ def test_pin_catches_planted_mistake(name, tmp_path, monkeypatch):
     monkeypatch.setattr(orc, "build", lambda force=False: so)
     with pytest.raises(AssertionError):
         pin()
+
+
+# ---------------------------------------------------------------- planner rules
+import importlib.util  # noqa: E402
+import sys  # noqa: E402
+
+import test_oracle_rules as rule_pins  # noqa: E402
+from oracle import rules  # noqa: E402
+
+RULE_MUTATIONS = {
+    # the per-edge event partition by min instead of gcd
+    "gcd_as_min": ("[math.gcd(a, b) for a, b in zip(pp, cp)]", "[min(a, b) for a, b in zip(pp, cp)]",
+                   rule_pins.test_gcd_examples),
+    # the fork/join normalisation by max instead of lcm (the F/A/B/G example
+    # cannot tell them apart: its groups are 1 and 2; coprime groups can)
+    "lcm_as_max": ("    return a * b // math.gcd(a, b)", "    return max(a, b)",
+                   rule_pins.test_fork_with_coprime_consumer_groups_merges_to_one_event),
+    # grid axes multiplying into the wrong tensor dimension
+    "partition_axis": ("            part[d] *= grid[axis]", "            part[axis] *= grid[axis]",
+                       rule_pins.test_build_partition_example),
+    # counters reset every step instead of growing by epochs
+    "counter_epochs": ("    return [steps * t for t in thresholds]", "    return list(thresholds)",
+                       rule_pins.test_expected_counters),
+}
+
+
+def _load_rules_mutant(old, new):
+    src = open(rules.__file__).read()
+    assert src.count(old) == 1, old
+    spec = importlib.util.spec_from_loader("oracle_rules_mutant", loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules["oracle_rules_mutant"] = mod  # dataclasses resolve their module by name
+    try:
+        exec(compile(src.replace(old, new), rules.__file__, "exec"), mod.__dict__)
+    finally:
+        del sys.modules["oracle_rules_mutant"]
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(RULE_MUTATIONS))
+def test_rule_pin_catches_planted_mistake(name, monkeypatch):
+    old, new, pin = RULE_MUTATIONS[name]
+    pin()
+    monkeypatch.setattr(rule_pins, "rules", _load_rules_mutant(old, new))
+    with pytest.raises(AssertionError):
+        pin()
