@@ -165,9 +165,10 @@ def test_rope_angle_pin_catches_a_planted_sign_error():
 def test_rmsnorm_unit_weight_invariant():
     rng = np.random.default_rng(10)
     h = rng.normal(0, 3, (4, 6144))
-    y = glm.rmsnorm(h, np.ones(6144), 1e-6)
     ms = np.mean(h * h, axis=1)
-    assert np.allclose(np.mean(y * y, axis=1), 1 - 1e-6 / (ms + 1e-6))
+    for eps in (1e-6, 0.5, 30.0):   # large eps values tell where eps sits in the formula
+        y = glm.rmsnorm(h, np.ones(6144), eps)
+        assert np.allclose(np.mean(y * y, axis=1), ms / (ms + eps), rtol=1e-12, atol=0)
 
 
 def test_block_shapes_and_positions():

@@ -113,3 +113,58 @@ def test_rule_pin_catches_planted_mistake(name, monkeypatch):
     monkeypatch.setattr(rule_pins, "rules", _load_rules_mutant(old, new))
     with pytest.raises(AssertionError):
         pin()
+
+
+# ---------------------------------------------------------------- GLM block
+import test_oracle_glm as glm_pins  # noqa: E402
+from oracle import glm  # noqa: E402
+
+GLM_MUTATIONS = {
+    # e4m3 rounding half up instead of to even
+    "e4m3_ties": ("    v = np.round(a / q) * q                  # np.round: ties to even",
+                  "    v = np.floor(a / q + 0.5) * q", glm_pins.test_e4m3_ties_to_even_and_saturation),
+    # activation scale against the wrong format maximum
+    "quant_max": ("scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0))",
+                  "scale = np.where(amax > 0, amax / np.float32(240.0), np.float32(1.0))",
+                  glm_pins.test_quant_blocks_scale_and_zero_block),
+    # the activation's block scale left out of the GEMM
+    "gemm_scale": ("        out += part * sa[:, kb][:, None] * np.repeat(sw[:, kb], BLOCK)[:N][None, :]",
+                   "        out += part * np.repeat(sw[:, kb], BLOCK)[:N][None, :]",
+                   glm_pins.test_fp8_gemm_matches_brute_force),
+    # RoPE rotating the wrong way
+    "rope_sign": ("    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)",
+                  "    return np.concatenate([lo * c + hi * s, hi * c - lo * s], axis=-1)",
+                  glm_pins.test_rope_half_rotation_direction_and_frequency),
+    # bf16 by truncation
+    "bf16_trunc": ("    return np.ldexp(np.round(m * 256.0) / 256.0, e)", "    return np.ldexp(np.trunc(m * 256.0) / 256.0, e)",
+                   glm_pins.test_bf16_round_matches_torch),
+    # eps outside the square root
+    "rms_eps": ("    return h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps) * np.asarray(w, dtype=np.float64)",
+                "    return h / (np.sqrt(np.mean(h * h, axis=-1, keepdims=True)) + eps) * np.asarray(w, dtype=np.float64)",
+                glm_pins.test_rmsnorm_unit_weight_invariant),
+    # every token of both requests at its own position (request index ignored)
+    "positions": ("    return sh.pos0 + (np.arange(sh.M) % sh.T)", "    return sh.pos0 + np.arange(sh.M)",
+                  glm_pins.test_block_shapes_and_positions),
+}
+
+
+def _load_glm_mutant(old, new):
+    src = open(glm.__file__).read()
+    assert src.count(old) == 1, old
+    spec = importlib.util.spec_from_loader("oracle_glm_mutant", loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules["oracle_glm_mutant"] = mod
+    try:
+        exec(compile(src.replace(old, new), glm.__file__, "exec"), mod.__dict__)
+    finally:
+        del sys.modules["oracle_glm_mutant"]
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(GLM_MUTATIONS))
+def test_glm_pin_catches_planted_mistake(name, monkeypatch):
+    old, new, pin = GLM_MUTATIONS[name]
+    pin()
+    monkeypatch.setattr(glm_pins, "glm", _load_glm_mutant(old, new))
+    with pytest.raises(AssertionError):
+        pin()
