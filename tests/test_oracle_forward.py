@@ -219,3 +219,12 @@ def test_qk_norm_path():
     k = f64(host["wk"][0]) @ x
     kn = _rms(k, s.eps) * f64(host["knorm"][0])
     assert np.array_equal(kc[0, 0, 0, pos], bf(orc.rope(kn, pos, s.theta)))
+    # q: per-head RMSNorm with its own weights, then RoPE; read back through Wo = I
+    from scipy.special import softmax
+    q = f64(host["wq"][0]) @ x
+    o = hidden[0, 0] - f64(host["embed"][1])
+    K, V = f64(kc[0, 0, 0, :pos + 1]), f64(vc[0, 0, 0, :pos + 1])
+    for j in range(s.Hq):
+        qj = orc.rope(_rms(q[j * s.D:(j + 1) * s.D], s.eps) * f64(host["qnorm"][0]), pos, s.theta)
+        ref = softmax(K @ qj / math.sqrt(s.D)) @ V
+        assert np.allclose(o[j * s.D:(j + 1) * s.D], ref, rtol=1e-9, atol=1e-12)

@@ -13,6 +13,15 @@ from oracle import forward as orc
 
 HERE = os.path.dirname(os.path.abspath(orc.__file__))
 
+_NORM_Q = "                for (int j = 0; j < Hq; j++) { FN(rmsnorm)(q + j * D, D, w->qnorm[l], sh->eps, tmp); " \
+          "memcpy(q + j * D, tmp, sizeof(REAL) * D); }\n"
+_NORM_K = "                for (int g = 0; g < Hkv; g++) { FN(rmsnorm)(k + g * D, D, w->knorm[l], sh->eps, tmp); " \
+          "memcpy(k + g * D, tmp, sizeof(REAL) * D); }\n"
+_ROPE = ("            for (int j = 0; j < Hq; j++) FN(rope)(q + j * D, D, p, sh->theta);\n"
+         "            for (int g = 0; g < Hkv; g++) FN(rope)(k + g * D, D, p, sh->theta);\n")
+_QK_BLOCK = "            if (sh->qk_norm) {\n" + _NORM_Q + _NORM_K + "            }\n" + _ROPE
+_QK_SWAPPED = _ROPE + "            if (sh->qk_norm) {\n" + _NORM_Q + _NORM_K + "            }\n"
+
 MUTATIONS = {
     # RoPE rotating the wrong way
     "rope_sign": ("        v[i] = a * c - b * s;\n        v[i + half] = a * s + b * c;",
@@ -39,6 +48,11 @@ MUTATIONS = {
                  "            FN(matvec)(w->wo[l], H, Hq * D, o, t1, nthreads);\n"
                  "            for (int i = 0; i < H; i++) h[i] = t1[i];",
                  pins.test_step_attention_block_through_identity_output),
+    # q normalised with the k-norm weights
+    "qnorm_weights": ("FN(rmsnorm)(q + j * D, D, w->qnorm[l], sh->eps, tmp)", "FN(rmsnorm)(q + j * D, D, w->knorm[l], sh->eps, tmp)",
+                      pins.test_qk_norm_path),
+    # RoPE before the per-head RMSNorm instead of after
+    "qk_norm_order": (_QK_BLOCK, _QK_SWAPPED, pins.test_qk_norm_path),
     # the final RMSNorm skipped before the LM head
     "final_norm": ("        FN(rmsnorm)(h, H, w->norm_final, sh->eps, x);\n        FN(matvec)(w->lm_head, V, H, x,",
                    "        memcpy(x, h, sizeof(REAL) * H);\n        FN(matvec)(w->lm_head, V, H, x,",
