@@ -131,6 +131,23 @@ def barrier(dist):
         dist.barrier()
 
 
+def slowest_replica_ms(total_ms, dist, dev=None):
+    """The timed region's length over all ranks: the maximum (the job is done
+    when its slowest replica is).  NCCL reduces a device tensor, gloo a host one."""
+    if dist is None:
+        return total_ms
+    import torch
+    t = torch.tensor([total_ms], dtype=torch.float64,
+                     device=dev if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, total_ms):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / (total_ms / 1e3)
+
+
 def side_measurements(args, w, dev, stream, weights, kc, vc, seq0, max_steps, first_free_step):
     """The comparison legs measured beside the megakernel in the same run: the
     same device code launched once per op (stream and CUDA-Graph variants), the
@@ -281,13 +298,8 @@ def run_mk(args, w, rank, world, dist):
     rec = sess.sync()
     barrier(dist)
     step_ms = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)])
-    total_ms = float(ev[0].elapsed_time(ev[-1]))
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    tokens_all = w.batch * args.steps * world
-    value = tokens_all / (total_ms / 1e3)
+    total_ms = slowest_replica_ms(float(ev[0].elapsed_time(ev[-1])), dist, dev)
+    value = job_rate(w.batch * args.steps, world, total_ms)
     # end to end through the public API with host buffers: token in, argmax out
     e2e_steps = min(args.steps, 32)
     pinned_tok = torch.tensor(synth.first_tokens(w), dtype=torch.int32).pin_memory()
@@ -416,12 +428,8 @@ def run_glm(args, rank, world, dist):
     step += args.steps
     warm_ms = e0.elapsed_time(e1) / args.steps
     rec = sess.sync()
-    total_ms = float(cold_ms.sum())
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = d.M * args.steps * world / (total_ms / 1e3)
+    total_ms = slowest_replica_ms(float(cold_ms.sum()), dist, dev)
+    value = job_rate(d.M * args.steps, world, total_ms)
     # end to end: x and residual from pinned host memory in, Q-B / Indexer-Q / Head-Gate out
     hx = inp["x"].cpu().pin_memory()
     hres = inp["res"].cpu().pin_memory()
