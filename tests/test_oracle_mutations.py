@@ -182,3 +182,44 @@ def test_glm_pin_catches_planted_mistake(name, monkeypatch):
     monkeypatch.setattr(glm_pins, "glm", _load_glm_mutant(old, new))
     with pytest.raises(AssertionError):
         pin()
+
+
+# ---------------------------------------------------------------- queue simulator
+import test_oracle_sim as sim_pins  # noqa: E402
+from oracle import sim  # noqa: E402
+
+SIM_MUTATIONS = {
+    # counters compared with the bare threshold (as if reset every step)
+    "no_epochs": ("                if counters[ev] < thr * (s + 1 + off):", "                if counters[ev] < thr:",
+                  sim_pins.test_waits_target_the_current_epoch),
+    # the epoch offset applied the wrong way
+    "offset_sign": ("                if counters[ev] < thr * (s + 1 + off):",
+                    "                if counters[ev] < thr * (s + 1 - off):", sim_pins.test_wait_one_epoch_back),
+    # a stuck worker not reported
+    "no_blocked": ("        if blocked:\n            return SimResult(False, counters, blocked, order)",
+                   "        if False:\n            return SimResult(False, counters, blocked, order)",
+                   sim_pins.test_deadlock_detected),
+}
+
+
+def _load_sim_mutant(old, new):
+    src = open(sim.__file__).read()
+    assert src.count(old) == 1, old
+    spec = importlib.util.spec_from_loader("oracle.sim_mutant", loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    mod.__package__ = "oracle"  # its relative imports resolve against the real package
+    sys.modules["oracle.sim_mutant"] = mod
+    try:
+        exec(compile(src.replace(old, new), sim.__file__, "exec"), mod.__dict__)
+    finally:
+        del sys.modules["oracle.sim_mutant"]
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(SIM_MUTATIONS))
+def test_sim_pin_catches_planted_mistake(name, monkeypatch):
+    old, new, pin = SIM_MUTATIONS[name]
+    pin()
+    monkeypatch.setattr(sim_pins, "sim", _load_sim_mutant(old, new))
+    with pytest.raises(AssertionError):
+        pin()

@@ -81,3 +81,22 @@ def test_deadlock_detected():
     # a queue that is not a subsequence of a topological order can deadlock on one worker
     r = sim.deadlock_check([[2, 1]], {2: [(0, 1)], 1: []}, {1: [(0, 1)], 2: []}, 1)
     assert not r.ok
+
+
+def test_waits_target_the_current_epoch():
+    """Counters are never reset: at step s a wait of threshold t needs t x (s + 1).
+    Worker 0's consumer must wait for worker 1's producer in every step, not
+    only the first."""
+    waits = {0: [(0, 1)], 1: []}
+    sigs = {0: [], 1: [(0, 1)]}
+    r = sim.deadlock_check([[0], [1]], waits, sigs, 1, steps=3)
+    assert r.ok and r.order == [1, 0, 1, 0, 1, 0] and r.counters == [3]
+
+
+def test_wait_one_epoch_back():
+    """A wait with epoch offset -1 at step s needs t x s: nothing at the first
+    step, the previous step's signals after that."""
+    waits = {0: [(0, 1, -1)], 1: []}
+    sigs = {0: [], 1: [(0, 1)]}
+    r = sim.deadlock_check([[0], [1]], waits, sigs, 1, steps=2)
+    assert r.ok and r.order == [0, 1, 0, 1]
