@@ -253,3 +253,29 @@ def test_argmax_key_decoding():
 def test_launch_probe_rejects_an_empty_grid():
     rc = rt.load().mk_launch_probe(0, 1, None)
     assert rc == rt.MK_ERR_INVALID and b"num_workers" in rt.load().mk_last_error()
+
+
+def test_qwen3_8b_batch1_gemv_tiles_fit_the_wide_row_per_warp_path():
+    """Every K = 4096 GEMV instruction of the Qwen3-8B batch-1 plan has the
+    shape the wide row-per-warp tile takes (64 KB pages of 8 rows, two pages:
+    16 rows, or 8 gate + 8 up rows); MLP-down K chunks of 2048 take the
+    row-per-warp path with x in registers (16-row pages)."""
+    W_P = 14
+    P_NROWS, P_KC, P_RPP, P_NPG = W_P + 1, W_P + 3, W_P + 8, W_P + 9
+    w = synth.WORKLOADS["qwen3_8b_b1"]
+    p = rt.Plan.llama(w.shape, 1, [2048], 32, 2048 + 33, **GB300)
+    assert p.info()["page_bytes"] == 65536
+    q, ids, _, _ = p.export()
+    words = q[ids >= 0]
+    seen = set()
+    for op in ("qkv", "o", "up", "lm", "down"):
+        sel = words[words[:, 0] == rt.OPCODE[op]]
+        assert len(sel)
+        kc, rows, rpp, npg = sel[:, P_KC], sel[:, P_NROWS], sel[:, P_RPP], sel[:, P_NPG]
+        if op == "down":
+            assert (kc == 2048).all() and (rpp == 16).all()
+        else:
+            assert (kc == 4096).all() and (rpp == 8).all() and (npg == 2).all()
+            assert ((rows == 8) if op == "up" else (rows == 16)).all()
+        seen.add(op)
+    assert seen == {"qkv", "o", "up", "lm", "down"}
