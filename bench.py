@@ -544,6 +544,8 @@ def main():
     from dataclasses import replace
     from persistent_megakernel_decode_gb300 import synth
     if args.workload == "glm52_preattn_m16":
+        if args.trace_out:
+            ap.error("--trace-out covers the decoder workloads only")
         if args.impl == "reference":
             if int(os.environ.get("RANK", "0")) == 0:
                 run_glm_reference(args)
