@@ -82,3 +82,21 @@ def test_empty_trace():
     t = np.zeros((3, 5, 16), np.uint64)
     assert tr.summarize(t) == {}
     assert tr.timeline(t, np.zeros((1, 24), np.int32)) == []
+
+
+def test_layer_profile_across_layers():
+    """Two layers of qkv -> down: the second layer's qkv gap runs from the
+    first layer's last down instruction done; means are over layers."""
+    t = np.zeros((1, 4, 16), np.uint64)
+    b = 1_000_000
+    _slot(t, 0, 0, OPCODE["qkv"], 0, b, b + 1000, b + 3000)
+    _slot(t, 0, 1, OPCODE["down"], 1, b + 3000, b + 4000, b + 8000)
+    _slot(t, 0, 2, OPCODE["qkv"], 2, b + 8000, b + 10000, b + 13000)
+    _slot(t, 0, 3, OPCODE["down"], 3, b + 13000, b + 14000, b + 20000)
+    tasks = np.zeros((4, 24), np.int32)
+    tasks[:, 1] = [0, 0, 1, 1]
+    prof = tr.layer_profile(tr.timeline(t, tasks))
+    assert prof["qkv"]["gap_us"] == pytest.approx(2.0)     # 10 - 8: only layer 1 has a previous op
+    assert prof["down"]["gap_us"] == pytest.approx(1.0)    # (4 - 3 + 14 - 13) / 2
+    assert prof["qkv"]["span_us"] == pytest.approx(2.5)    # (3 - 1 + 13 - 10) / 2
+    assert prof["down"]["span_us"] == pytest.approx(5.0)   # (8 - 4 + 20 - 14) / 2
