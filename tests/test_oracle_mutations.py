@@ -223,3 +223,42 @@ def test_sim_pin_catches_planted_mistake(name, monkeypatch):
     monkeypatch.setattr(sim_pins, "sim", _load_sim_mutant(old, new))
     with pytest.raises(AssertionError):
         pin()
+
+
+# ---------------------------------------------------------------- plan builder
+import test_oracle_rules as plan_pins  # noqa: E402  (its plan pins call plans.*)
+from oracle import plans  # noqa: E402
+
+PLAN_MUTATIONS = {
+    # attention splits rounded down: the last partial split dropped
+    "nsplit_floor": ("    nsplit = [_ceil(seq0[b] + max_steps, k.attn_split) for b in range(B)]",
+                     "    nsplit = [(seq0[b] + max_steps) // k.attn_split for b in range(B)]",
+                     plan_pins.test_attention_splits_cover_every_position),
+    # MLP-down without its K chunks (one chunk of the whole F)
+    "down_chunks": ("        ops.append(Op(down, (_ceil(shape.H, k.rows_down), shape.F // k.kchunk_down, 1),",
+                    "        ops.append(Op(down, (_ceil(shape.H, k.rows_down), 1, 1),",
+                    plan_pins.test_llama1b_layer_counts),
+}
+
+
+def _load_plans_mutant(old, new):
+    src = open(plans.__file__).read()
+    assert src.count(old) == 1, old
+    spec = importlib.util.spec_from_loader("oracle.plans_mutant", loader=None)
+    mod = importlib.util.module_from_spec(spec)
+    mod.__package__ = "oracle"
+    sys.modules["oracle.plans_mutant"] = mod
+    try:
+        exec(compile(src.replace(old, new), plans.__file__, "exec"), mod.__dict__)
+    finally:
+        del sys.modules["oracle.plans_mutant"]
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(PLAN_MUTATIONS))
+def test_plan_pin_catches_planted_mistake(name, monkeypatch):
+    old, new, pin = PLAN_MUTATIONS[name]
+    pin()
+    monkeypatch.setattr(plan_pins, "plans", _load_plans_mutant(old, new))
+    with pytest.raises(AssertionError):
+        pin()

@@ -187,3 +187,20 @@ def test_tail_model():
 
 def test_expected_counters():
     assert rules.expected_counters([16, 2, 1], 3) == [48, 6, 3]
+
+
+def test_attention_splits_cover_every_position():
+    """Split-KV: a sequence's splits are 0..n-1 of T positions each and cover
+    every position up to the last step's new token, with no split left empty
+    (checked on ragged lengths, where rounding matters)."""
+    shape = plans.LlamaShape(L=1, H=256, Hq=4, Hkv=2, D=64, F=688, V=1024)
+    for seq0, steps, T in (([1000], 1, 64), ([5, 64, 130], 4, 32)):
+        kn = plans.Knobs(rows_qkv=16, rows_o=16, rows_up=8, rows_down=16, kchunk_down=688, rows_lm=16,
+                         attn_split=T)
+        ops, edges, kinds = plans.llama_step_ops(shape, kn, len(seq0), seq0, steps)
+        g = rules.build_task_graph(ops, edges)
+        for b, s0 in enumerate(seq0):
+            splits = sorted({t.bid[2] for t in g.tasks if kinds[t.op][0] == "attn" and t.bid[1] == b})
+            assert splits == list(range(len(splits)))
+            assert len(splits) * T >= s0 + steps
+            assert (len(splits) - 1) * T < s0 + steps
