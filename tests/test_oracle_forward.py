@@ -214,7 +214,11 @@ def test_qk_norm_path():
     kc, vc = synth.to_host_u16(kc).copy(), synth.to_host_u16(vc).copy()
     shape = orc.Shape(s.L, s.H, s.Hq, s.Hkv, s.D, s.F, s.V, True, s.eps, s.theta)
     pos = 3
-    _, hidden, _ = orc.decode_step(shape, host, kc, vc, [pos], [1])
+    host["norm_final"] = bf(np.linspace(0.8, 1.2, 256))
+    logits, hidden, _ = orc.decode_step(shape, host, kc, vc, [pos], [1])
+    # untied head: logits = W_lm (RMSNorm(h_L) * w_final), not the embedding
+    ref = f64(host["lm_head"]) @ (_rms(hidden[-1, 0], s.eps) * f64(host["norm_final"]))
+    assert np.allclose(logits[0], ref, rtol=1e-11, atol=1e-13)
     x = _rms(f64(host["embed"][1]), s.eps)
     k = f64(host["wk"][0]) @ x
     kn = _rms(k, s.eps) * f64(host["knorm"][0])

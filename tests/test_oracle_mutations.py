@@ -53,6 +53,13 @@ MUTATIONS = {
                       pins.test_qk_norm_path),
     # RoPE before the per-head RMSNorm instead of after
     "qk_norm_order": (_QK_BLOCK, _QK_SWAPPED, pins.test_qk_norm_path),
+    # the embedding used as the LM head of an untied model
+    "untied_head": ("        FN(matvec)(w->lm_head, V, H, x, logits + (size_t)b * V, nthreads);",
+                    "        FN(matvec)(w->embed, V, H, x, logits + (size_t)b * V, nthreads);",
+                    pins.test_qk_norm_path),
+    # the final norm's weights ignored
+    "final_norm_weights": ("        FN(rmsnorm)(h, H, w->norm_final, sh->eps, x);", "        FN(rmsnorm)(h, H, w->norm_mlp[0], sh->eps, x);",
+                           pins.test_qk_norm_path),
     # the final RMSNorm skipped before the LM head
     "final_norm": ("        FN(rmsnorm)(h, H, w->norm_final, sh->eps, x);\n        FN(matvec)(w->lm_head, V, H, x,",
                    "        memcpy(x, h, sizeof(REAL) * H);\n        FN(matvec)(w->lm_head, V, H, x,",
