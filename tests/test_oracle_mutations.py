@@ -53,6 +53,16 @@ MUTATIONS = {
                       pins.test_qk_norm_path),
     # RoPE before the per-head RMSNorm instead of after
     "qk_norm_order": (_QK_BLOCK, _QK_SWAPPED, pins.test_qk_norm_path),
+    # SwiGLU with gate and up exchanged
+    "gate_up_swap": ("                REAL g = gt[i];\n                gt[i] = g / (1 + (REAL)exp(-(double)g)) * ut[i];",
+                     "                REAL g = ut[i];\n                gt[i] = g / (1 + (REAL)exp(-(double)g)) * gt[i];",
+                     pins.test_step_mlp_block),
+    # new k and v appended into each other's cache
+    "kv_swap": ("                    kcache[base + d] = double_to_bf16((double)k[g * D + d]);\n"
+                "                    vcache[base + d] = double_to_bf16((double)v[g * D + d]);",
+                "                    kcache[base + d] = double_to_bf16((double)v[g * D + d]);\n"
+                "                    vcache[base + d] = double_to_bf16((double)k[g * D + d]);",
+                pins.test_step_attention_block_through_identity_output),
     # the embedding used as the LM head of an untied model
     "untied_head": ("        FN(matvec)(w->lm_head, V, H, x, logits + (size_t)b * V, nthreads);",
                     "        FN(matvec)(w->embed, V, H, x, logits + (size_t)b * V, nthreads);",
@@ -163,6 +173,10 @@ GLM_MUTATIONS = {
     "rms_eps": ("    return h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps) * np.asarray(w, dtype=np.float64)",
                 "    return h / (np.sqrt(np.mean(h * h, axis=-1, keepdims=True)) + eps) * np.asarray(w, dtype=np.float64)",
                 glm_pins.test_rmsnorm_unit_weight_invariant),
+    # latent cache rows as k_pe || kv-lora instead of kv-lora || k_pe
+    "latent_order": ("    latent = np.concatenate([kv, kpe], axis=1).reshape(sh.R, sh.T, sh.kvlora + sh.rope)",
+                     "    latent = np.concatenate([kpe, kv], axis=1).reshape(sh.R, sh.T, sh.kvlora + sh.rope)",
+                     lambda: glm_pins.test_forward_small_block_consistency(0)),
     # every token of both requests at its own position (request index ignored)
     "positions": ("    return sh.pos0 + (np.arange(sh.M) % sh.T)", "    return sh.pos0 + np.arange(sh.M)",
                   glm_pins.test_block_shapes_and_positions),
