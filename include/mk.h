@@ -196,9 +196,12 @@ typedef struct {
  * longest-first within each successor range, and dealt to workers by the
  * target's schedule (MK_SCHED_*: by default the time-model list scheduler;
  * MK_SCHED_BYTES deals by bytes).  Tile sizes follow the kernel paths: the
- * batch-1 row-per-warp GEMV (K <= 2048), 16-row tensor-core tiles when every
- * K is a multiple of 512, else split-K tiles.  The plan is checked by
- * simulating its queues.  *out receives a plan the
+ * batch-1 row-per-warp GEMV (K <= 2048 with x in registers; K = 4096 in
+ * pages of 8 rows with x in shared memory), 16-row tensor-core tiles when
+ * every K is a multiple of 512, else split-K tiles.  Unless the target fixes
+ * it, the attention split (16384 / (2 D) positions) doubles, up to 256, while
+ * its tasks outnumber the workers.  The plan is checked by simulating its
+ * queues.  *out receives a plan the
  * caller frees with mk_free().  Returns MK_ERR_INVALID / MK_ERR_UNSUPPORTED
  * / MK_ERR_DEADLOCK on failure (nothing allocated). */
 int mk_plan(const mk_model_desc *model, const mk_step_desc *step, const mk_target_desc *target,

@@ -11,7 +11,8 @@ oracle (on the host cores) at the model shapes of the workloads.
   of the batch-2 and batch-4 kernels, a partly filled MMA N side), and at
   batch 8 over 32 teacher-forced steps (256 argmax samples);
 * Qwen3-8B shape, batch 1, 2048 cached tokens (head_dim 128, q/k RMSNorm,
-  K = 4096: tensor-core tiles at batch 1, row-per-warp MLP-down).
+  K = 4096: row-per-warp tiles reading x from shared memory, row-per-warp
+  MLP-down with x in registers, 128-position attention splits).
 
 Bars: per-layer residual stream, logits and appended K/V within 1e-2
 normwise; an argmax may differ only where the oracle's top-2 logit gap is
