@@ -201,6 +201,9 @@ def test_forward_small_block_consistency(seed):
     assert np.allclose(glm.e4m3_decode(out["qa"]) * np.repeat(out["sa"], 128, axis=1), y, rtol=2 ** -4, atol=1e-3)
     kv_end = sh.qlora + sh.kvlora
     assert np.array_equal(out["latent"][0, :, :sh.kvlora], out["qkva"][:, sh.qlora:kv_end])
+    # Q-B and Indexer-Q read the q-lora columns (the first qlora of QKV-A), re-quantised per 128
+    dq = glm.e4m3_decode(out["qb"]) * np.repeat(out["qb_s"], 128, axis=1)
+    assert np.allclose(dq, out["qkva"][:, :sh.qlora], rtol=2 ** -4, atol=np.max(out["qb_s"]) * 2.0 ** -9)
     assert np.array_equal(out["index"][0, :, :64], out["ik"][:, :64])
     # the roped slice keeps pair norms up to bf16 rounding
     a = out["qkva"][:, kv_end:]

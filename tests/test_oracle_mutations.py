@@ -173,6 +173,10 @@ GLM_MUTATIONS = {
     "rms_eps": ("    return h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps) * np.asarray(w, dtype=np.float64)",
                 "    return h / (np.sqrt(np.mean(h * h, axis=-1, keepdims=True)) + eps) * np.asarray(w, dtype=np.float64)",
                 glm_pins.test_rmsnorm_unit_weight_invariant),
+    # the re-quantised q-lora taken from the wrong columns of QKV-A
+    "qlora_cols": ("    qb_q, qb_s = quant_blocks(qkva[:, :sh.qlora])",
+                   "    qb_q, qb_s = quant_blocks(qkva[:, sh.kvlora:sh.kvlora + sh.qlora])",
+                   lambda: glm_pins.test_forward_small_block_consistency(0)),
     # latent cache rows as k_pe || kv-lora instead of kv-lora || k_pe
     "latent_order": ("    latent = np.concatenate([kv, kpe], axis=1).reshape(sh.R, sh.T, sh.kvlora + sh.rope)",
                      "    latent = np.concatenate([kpe, kv], axis=1).reshape(sh.R, sh.T, sh.kvlora + sh.rope)",
