@@ -14,8 +14,13 @@ Where the article is silent the plainest reading is taken:
   bits, no infinities, largest finite value 448).  Activations are quantised
   per (row, 128-column block): scale = amax / 448 (amax = 0 gives scale 1),
   code = round-to-nearest-even of value / scale, saturating at +-448.  The
-  division and the rounding decision are taken in fp32, the precision of the
-  device kernel (a code is an integer decided by floating point).
+  block scales are stored as fp32 (the workload states "fp32 block scales"),
+  so the scale is amax / 448 rounded to fp32.  Neither the article nor the
+  workload fixes the precision of the division and of the rounding decision;
+  they are taken in fp64 here, like the rest of this oracle, on the fp64
+  values and the fp32-stored scale.  A device that decides in fp32 may land
+  one e4m3 step the other way where value / scale sits within an fp32
+  rounding of a midpoint; the tests count such codes.
 * Weights are e4m3 with one fp32 scale per 128 x 128 block (inputs).
 * A GEMM output is sum over 128-wide K blocks of
   a_scale[m, kb] * w_scale[n // 128, kb] * sum_k a[m, k] * w[n, k], rounded to
@@ -119,13 +124,13 @@ def e4m3_encode(x) -> np.ndarray:
 
 def quant_blocks(y) -> tuple:
     """Per (row, 128-column block) e4m3 quantisation of y [M, K]: (codes, fp32 scales [M, K/128])."""
-    y32 = np.asarray(y, dtype=np.float32)
-    M, K = y32.shape
-    yb = y32.reshape(M, K // BLOCK, BLOCK)
+    y64 = np.asarray(y, dtype=np.float64)
+    M, K = y64.shape
+    yb = y64.reshape(M, K // BLOCK, BLOCK)
     amax = np.abs(yb).max(axis=2)
-    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    v = (yb / scale[:, :, None]).astype(np.float32)
-    return e4m3_encode(v.astype(np.float64)).reshape(M, K), scale
+    scale = np.where(amax > 0, amax / E4M3_MAX, 1.0).astype(np.float32)   # stored as fp32
+    v = yb / scale.astype(np.float64)[:, :, None]
+    return e4m3_encode(v).reshape(M, K), scale
 
 
 # ---------------------------------------------------------------------------

@@ -155,8 +155,8 @@ GLM_MUTATIONS = {
     "e4m3_ties": ("    v = np.round(a / q) * q                  # np.round: ties to even",
                   "    v = np.floor(a / q + 0.5) * q", glm_pins.test_e4m3_ties_to_even_and_saturation),
     # activation scale against the wrong format maximum
-    "quant_max": ("scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0))",
-                  "scale = np.where(amax > 0, amax / np.float32(240.0), np.float32(1.0))",
+    "quant_max": ("scale = np.where(amax > 0, amax / E4M3_MAX, 1.0).astype(np.float32)",
+                  "scale = np.where(amax > 0, amax / 240.0, 1.0).astype(np.float32)",
                   glm_pins.test_quant_blocks_scale_and_zero_block),
     # the activation's block scale left out of the GEMM
     "gemm_scale": ("        out += part * sa[:, kb][:, None] * np.repeat(sw[:, kb], BLOCK)[:N][None, :]",
