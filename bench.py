@@ -42,9 +42,12 @@ def measured_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("interp.cu", "dev_common.cuh", "dev_ops.cuh", "dev_glm.cuh", "mk_internal.h", "planner.cpp"):
+    from persistent_megakernel_decode_gb300 import build as _b
+    for f in _b.SOURCES + _b.HEADERS:
         with open(os.path.join(ROOT, "persistent_megakernel_decode_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
+    with open(os.path.join(ROOT, "include", "mk.h"), "rb") as fh:
+        h.update(fh.read())
     return h.hexdigest()[:16]
 
 

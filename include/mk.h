@@ -172,6 +172,9 @@ typedef struct {
 /* Packed argmax key: (order-preserving bits of the fp32 logit << 32) |
  * (0xFFFFFFFF - index); the largest key is the largest logit, lowest index on
  * ties.  mk_argmax_index() recovers the index. */
+/* (The pages print no argmax layout; greedy decoding takes the usual argmax,
+ * lowest index on ties, and the packed key lets every LM-head tile fold its
+ * best row into one 64-bit max on the device.) */
 int32_t mk_argmax_index(uint64_t key);
 
 /* Device-side failure record, read back by mk_sync_status(). */
@@ -284,10 +287,19 @@ typedef struct {
 
 int mk_plan_glm(const mk_glm_desc *glm, const mk_target_desc *target, mk_plan_t *out);
 
+/* Sizes of a plan: workers, queue length, events, ops, pages, the workspace
+ * and the algorithmic bytes of one step -- the shapes of what the plan
+ * expands into: an instruction tensor, event counters and an operand pointer
+ * table ("MegaRTP megakernel article", section 4, the chain OpGraph ->
+ * TaskGraph -> KernelPlan).  Host only.  MK_ERR_INVALID on a null argument. */
 int mk_plan_info_get(mk_plan_t plan, mk_plan_info *info);
 
 /* Copies of the plan for inspection and bit-exact tests (caller-owned host
- * buffers, sized from mk_plan_info):
+ * buffers, sized from mk_plan_info).  The queue is the KernelPlan's fixed
+ * instruction tensor, every worker's row padded with NoOp to one length
+ * ("MegaRTP megakernel article", section 4, KernelPlan: [148, 5, 32] for its
+ * GLM plan); the task table is its TaskGraph.  Host only; MK_ERR_INVALID on a
+ * null plan.
  *  queue      int32 [total_slots, 32]   raw instruction words; the megakernel
  *             plan's single launch is [num_workers, lmax, 32]; per-op plans
  *             concatenate one [workers_k, lmax_k, 32] block per launch
@@ -300,14 +312,29 @@ int mk_plan_info_get(mk_plan_t plan, mk_plan_info *info);
  * threshold, epoch_offset), n_signals, 2 x (event, increment), 4 reserved */
 int mk_plan_export(mk_plan_t plan, int32_t *queue, int32_t *task_ids, int32_t *thresholds, int32_t *tasks);
 
-/* Bind a caller-owned device buffer (MK_BIND_*).  `layer` selects the layer
- * of per-layer bindings and is ignored otherwise.  Host-only; the table is
- * uploaded by the next mk_run.  Pointers must be 16-byte aligned. */
+/* Bind a caller-owned device buffer (MK_BIND_*) into the plan's operand
+ * pointer table: one [num_ops, 16] uint64 row per op, shared by all of that
+ * op's tile instructions, which carry only the row index ("MegaRTP megakernel
+ * article", section 4, OperandPtrTable).  New buffers of the same shapes are
+ * rebound without replanning; only a change of shape (batch, lengths, model)
+ * needs a new plan (same section: when M or the KV length change, only the
+ * host plan is regenerated).  `layer` selects the layer of per-layer bindings
+ * and is ignored otherwise.  Host-only; the table is uploaded by the next
+ * mk_run.  Pointers must be 16-byte aligned.  MK_ERR_INVALID on an unknown
+ * binding or layer.  The library never frees a bound buffer. */
 int mk_bind(mk_plan_t plan, int binding, int layer, uint64_t device_ptr);
 
-/* Run steps first_step .. first_step+num_steps-1 asynchronously on `stream`.
+/* Run steps first_step .. first_step+num_steps-1 asynchronously on `stream`:
+ * a fixed grid of persistent worker CTAs, one per SM, each looping over its
+ * own queue row ("MegaRTP megakernel article", section 4, Device).  Before
+ * the launch the whole grid is checked for co-residency with its real block
+ * and shared-memory size, and event counters are monotone epochs that are
+ * not reset between steps ("GEMM + AllToAll fusion post", section 2).
+ * A workspace belongs to one plan: the queue is uploaded on a plan's first
+ * call with a given workspace and not checked again, so two plans must not
+ * take turns on one workspace (mk_run_static handles that case for its array).
  * `workspace` is caller-allocated device memory of at least
- * info.workspace_bytes (16-byte aligned); it holds the queue, operand table,
+ * info.workspace_bytes (256-byte aligned, else MK_ERR_INVALID); it holds the queue, operand table,
  * event counters, activations and the error record.  When first_step == 0
  * the counters, the error record and the ARGMAX binding are cleared.
  * One cooperative launch per step (MK_MODE_MEGAKERNEL) or per op
@@ -319,13 +346,21 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
 
 /* Synchronise `stream`, read the device error record into *rec (may be
  * NULL) and return its code (MK_OK, MK_ERR_TIMEOUT, MK_ERR_DEVICE_CHECK) or
- * MK_ERR_CUDA. */
+ * MK_ERR_CUDA.  (No counterpart on the pages, which name debugging tens of
+ * thousands of tasks inside one kernel as an open challenge: "CMU 15-779
+ * Lecture 7 notes", section 4.3.  Every device wait here is bounded; a wait
+ * that runs out records where it was and the kernel drains and returns.) */
 int mk_sync_status(mk_plan_t plan, void *workspace, void *stream, mk_error_record *rec);
 
-/* Copy the event counters (uint32 [num_events]) from the workspace to host. */
+/* Copy the event counters (uint32 [num_events]) from the workspace to host.
+ * After steps 0 .. n-1 each holds n x its per-step increments (monotone
+ * epochs, "GEMM + AllToAll fusion post", section 2).  Synchronous;
+ * MK_ERR_CUDA on a failed copy. */
 int mk_read_counters(mk_plan_t plan, void *workspace, uint32_t *out);
 
-/* Copy the per-instruction trace to host: uint64 [total_slots, 16]:
+/* Copy the per-instruction trace to host (a per-task timeline, like the
+ * profiler MPK ships: "CMU 15-779 Lecture 7 notes", section 8, item 4):
+ * uint64 [total_slots, 16]:
  *   [0] opcode | task << 32      [1] consumer start      [2] activation loader: events met
  *   [3] consumer done            [4] loader issue start  [5] loader issue end
  *   [6..10] stamps of consumer thread 0 inside the op (attention: K pages ready, scores,
@@ -351,11 +386,15 @@ int mk_read_trace(mk_plan_t plan, void *workspace, uint64_t *out);
  * (64 MiB); every GPU that loads the library holds it until the process exits.
  * Plans whose mk_plan_info.workspace_bytes exceed it are rejected with
  * MK_ERR_INVALID.  The first call on each device (with that device current)
- * looks up the array's device address; make that first call before any
- * stream capture.  All calls share the one array and it keeps the previous
- * call's contents: counters and the error record are cleared when first_step
- * is 0, exactly as in mk_run, and a call made with a different plan than the
- * previous one uploads its queue again.  Calls whose work overlaps on the GPU
+ * looks up the array's device address.  Any call that uploads a queue --
+ * a plan's first call, and the first call after another plan used the array
+ * -- synchronises `stream` (as mk_run does for its first call on a
+ * workspace), so make such calls outside any stream capture.  All calls
+ * share the one array and it keeps the previous call's contents: counters
+ * and the error record are cleared when first_step is 0, exactly as in
+ * mk_run.  After another plan has used the array, this plan's counters are
+ * gone: a call with first_step != 0 is then rejected with MK_ERR_INVALID,
+ * and the plan starts again at first_step 0.  Calls whose work overlaps on the GPU
  * (other streams, other threads) race on the array -- serialise them.
  * This entry point calls no cudaMalloc, cudaFree or allocating library
  * routine.  *workspace_out (may be NULL) receives the array's device address,
@@ -372,10 +411,14 @@ int mk_run_static(mk_plan_t plan, int first_step, int num_steps, uint32_t flags,
  * MK_ERR_CUDA if the launch fails. */
 int mk_launch_probe(int num_workers, int cooperative, void *stream);
 
-/* Free the plan's host memory.  NULL-safe.  Never touches device memory. */
+/* Free the plan's host memory.  NULL-safe.  Never touches device memory.
+ * A plan is built once per shape and reused for every step ("CMU 15-779
+ * Lecture 7 notes", section 5.1: the schedule is prepared ahead of time and
+ * reused for hundreds of forward passes). */
 void mk_free(mk_plan_t plan);
 
-/* Thread-local description of the last non-zero status. */
+/* Thread-local description of the last non-zero status (no counterpart on
+ * the pages: the error string of this C ABI). */
 const char *mk_last_error(void);
 
 #ifdef __cplusplus

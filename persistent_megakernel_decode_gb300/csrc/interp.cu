@@ -466,6 +466,8 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
 // ---------------------------------------------------------------- host side
 
 
+constexpr int kMaxDevices = 64;
+
 static int cuda_fail(cudaError_t e, const char *what) {
     return set_error(MK_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
@@ -686,14 +688,19 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
         }
     }
     KernelFn fn = pick_kernel(p);
-    static thread_local int configured_smem = -1;
-    if (configured_smem < p.smem_bytes) {
+    // the attribute is per device: remember what each device was given
+    static thread_local int configured_smem[kMaxDevices] = {};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return set_error(MK_ERR_INVALID, "device ordinal out of range");
+    if (configured_smem[dev] < p.smem_bytes) {
         for (KernelFn f : {mk_interp<1, FL_GEN>, mk_interp<2, FL_GEN>, mk_interp<4, FL_GEN>, mk_interp<8, FL_GEN>,
                            mk_interp<1, FL_GLM>, mk_interp<1, FL_LEAN>}) {
             e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         }
-        configured_smem = p.smem_bytes;
+        configured_smem[dev] = p.smem_bytes;
     }
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, THREADS, p.smem_bytes);
@@ -748,7 +755,6 @@ int mk_launch_probe(int num_workers, int cooperative, void *stream) {
 static __device__ __align__(256) uint8_t g_static_workspace[MK_STATIC_WORKSPACE_BYTES];
 
 namespace {
-constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
 void *g_static_addr[kMaxDevices] = {};      // device address of the array, per device
 const void *g_static_owner[kMaxDevices] = {};  // plan whose queue the array holds
@@ -777,8 +783,17 @@ int mk_run_static(mk_plan_t plan, int first_step, int num_steps, uint32_t flags,
             g_static_addr[dev] = addr;
         }
         ws = g_static_addr[dev];
-        // another plan may have uploaded its queue into the shared array since
-        if (g_static_owner[dev] != plan) plan->p.uploaded_ws = nullptr;
+        // Another plan may have used the array since this plan's last call:
+        // its queue must be uploaded again, and the counters there are the
+        // other plan's, so this plan can only start over at step 0 (its wait
+        // targets are cumulative over steps).
+        if (g_static_owner[dev] != plan) {
+            if (first_step != 0)
+                return set_error(MK_ERR_INVALID,
+                                 "the static workspace was used by another plan since this plan's last call: "
+                                 "start again at first_step 0");
+            plan->p.uploaded_ws = nullptr;
+        }
         g_static_owner[dev] = plan;
     }
     if (workspace_out) *workspace_out = (uint64_t)(uintptr_t)ws;

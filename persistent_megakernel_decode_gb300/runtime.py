@@ -145,9 +145,11 @@ def _check(rc: int):
 
 
 def argmax_index(keys: np.ndarray) -> np.ndarray:
-    """Decode packed argmax keys (see ``mk_argmax_index``)."""
+    """Token index of each packed argmax key, decoded by the library's
+    ``mk_argmax_index``."""
     k = np.asarray(keys, dtype=np.uint64)
-    return (np.uint64(0xFFFFFFFF) - (k & np.uint64(0xFFFFFFFF))).astype(np.int64)
+    f = load().mk_argmax_index
+    return np.array([f(int(v)) for v in k.reshape(-1)], dtype=np.int64).reshape(k.shape)
 
 
 def _target(num_sms=0, smem_per_cta=0, mode=MODE_MEGAKERNEL, **knobs) -> TargetDesc:

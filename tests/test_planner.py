@@ -30,6 +30,45 @@ def test_library_exports_every_declared_function():
         assert hasattr(lib, n), n
 
 
+PAGE_TITLES = ("MegaRTP megakernel article", "GEMM + AllToAll fusion post", "CMU 15-779 Lecture 7 notes",
+               "MPK code walkthrough")
+
+
+def test_every_declaration_cites_its_passage():
+    """Each exported function's comment names the page (and section) that
+    defines the operation, or says that the pages have no counterpart."""
+    hdr = open(os.path.join(ROOT, "include", "mk.h")).read()
+    decl = re.compile(r"^(?:int|void|int32_t|const char \*)\s*\*?\s*(mk_[a-z_]+)\s*\(", re.M)
+    prev_end = 0
+    for m in decl.finditer(hdr):
+        # the comment text between the previous declaration and this one
+        between = hdr[prev_end:m.start()]
+        comments = " ".join(re.findall(r"/\*(.*?)\*/", between, flags=re.S))
+        text = re.sub(r"\s*\*\s*", " ", comments)
+        text = re.sub(r"\s+", " ", text)
+        assert any(t in text for t in PAGE_TITLES) or "no counterpart" in text, m.group(1)
+        prev_end = m.end()
+
+
+def test_binding_decodes_argmax_keys_with_the_export():
+    import inspect
+    src = inspect.getsource(rt.argmax_index)
+    assert "mk_argmax_index" in src and "0xFFFFFFFF" not in src
+    rng = np.random.default_rng(0)
+    idx = rng.integers(0, 151936, 64)
+    keys = (rng.integers(0, 2 ** 31, 64).astype(np.uint64) << np.uint64(32)) | (np.uint64(0xFFFFFFFF) - idx.astype(np.uint64))
+    assert (rt.argmax_index(keys) == idx).all()
+
+
+def test_build_and_bench_hash_cover_every_source():
+    import bench
+    from persistent_megakernel_decode_gb300 import build as b
+    csrc = sorted(os.listdir(b.CSRC))
+    assert sorted(b.SOURCES + b.HEADERS) == csrc
+    h0 = bench.kernel_source_hash()
+    assert isinstance(h0, str) and len(h0) == 16
+
+
 def _oracle_knobs(info):
     return plans.Knobs(rows_qkv=info["rows_qkv"], rows_o=info["rows_o"], rows_up=info["rows_up"],
                        rows_down=info["rows_down"], kchunk_down=info["kchunk_down"], rows_lm=info["rows_lm"],

@@ -60,3 +60,62 @@ def test_static_workspace_rejects_oversized_plans():
     addr = rt.C.c_uint64(0)
     rc = rt.load().mk_run_static(p.h, 0, 1, 0, 0, None, rt.C.byref(addr))
     assert rc == rt.MK_ERR_INVALID and b"static workspace" in rt.load().mk_last_error()
+
+
+def test_static_workspace_alternating_plans():
+    """Two plans take turns on the one static array: each call after a switch
+    uploads that plan's queue again and must start at step 0 (the counters
+    in the array are the other plan's); resuming at a later step after a
+    switch is refused, and the same plan may go on once it owns the array."""
+    from persistent_megakernel_decode_gb300 import build
+    build.build()
+    shape = synth.TINY
+    dev = torch.device("cuda:0")
+    w = synth.make_weights(shape, 12, device=dev)
+    kc, vc = synth.make_cache(shape, 2, 80, 112, device=dev)
+    k1, v1 = synth.make_cache(shape, 1, 80, 113, device=dev)
+    cases = {"A": ([64, 20], kc, vc, [7, 300]), "B": ([33], k1, v1, [512])}
+    ref, nal = {}, {}
+    for n, (seq0, k, v, toks) in cases.items():
+        ref[n] = rt.Session(shape, w, k.clone(), v.clone(), seq0, 2, capture_hidden=True)
+        nal[n] = rt.Session(shape, w, k.clone(), v.clone(), seq0, 2, capture_hidden=True)
+        for s in (ref[n], nal[n]):
+            s.tokens[0] = torch.tensor(toks, dtype=torch.int32, device=dev)
+            s.tokens[1] = torch.tensor(toks, dtype=torch.int32, device=dev) + 1
+    snap = {}  # (plan, step) -> what mk_run left after that step
+    for n in cases:
+        for step in range(2):
+            ref[n].run(step, 1, host_tokens=True)
+            ref[n].sync()
+            snap[n, step] = (ref[n].hidden.cpu().numpy(), ref[n].logits.cpu().numpy(), list(ref[n].step_tokens(step)))
+
+    def check(n, step):
+        h, lg, tok = snap[n, step]
+        b = nal[n]
+        assert _normwise(b.hidden.cpu().numpy(), h) <= 1e-2, (n, step)
+        assert _normwise(b.logits.cpu().numpy(), lg) <= 1e-2, (n, step)
+        assert list(b.step_tokens(step)) == tok, (n, step)
+
+    lib = rt.load()
+    for n in ("A", "B", "A"):
+        # re-running step 0 rewrites the same cache slot with the same values
+        addr = nal[n].run_static(0, 1, host_tokens=True)
+        assert nal[n].sync_static(addr).code == 0
+    check("A", 0)
+    # B runs step 0, then A may not resume at step 1 on B's counters
+    addr = nal["B"].run_static(0, 1, host_tokens=True)
+    assert nal["B"].sync_static(addr).code == 0
+    check("B", 0)
+    out = rt.C.c_uint64(0)
+    rc = lib.mk_run_static(nal["A"].plan.h, 1, 1, rt.RUN_HOST_TOKENS, 0,
+                           rt.C.c_void_p(nal["A"].stream.cuda_stream), rt.C.byref(out))
+    assert rc == rt.MK_ERR_INVALID and b"first_step 0" in lib.mk_last_error()
+    # B still owns the array and goes on to step 1
+    addr = nal["B"].run_static(1, 1, host_tokens=True)
+    assert nal["B"].sync_static(addr).code == 0
+    check("B", 1)
+    # A starts over at step 0 and then continues
+    for s in range(2):
+        addr = nal["A"].run_static(s, 1, host_tokens=True)
+        assert nal["A"].sync_static(addr).code == 0
+    check("A", 1)
