@@ -59,7 +59,8 @@ extern "C" {
 #define MK_OP_GLM_A0   9   /* GLM block: Add + RMSNorm + per-128 FP8 quantisation of one token row */
 #define MK_OP_GLM_GEMM 10  /* GLM block: rows of an FP8 weight x FP8 activations, block scales, bf16 out (+RoPE) */
 #define MK_OP_GLM_FIN  11  /* GLM block: one token's q-lora re-quantisation, RoPE and cache writes */
-#define MK_NUM_OPCODES 12
+#define MK_OP_NORM     12  /* tensor-core plans: RMSNorm of one sequence's residual into bf16 high/low rows */
+#define MK_NUM_OPCODES 13
 
 /* ---- plan modes ---- */
 #define MK_MODE_MEGAKERNEL 0   /* one persistent launch per step */
@@ -81,7 +82,7 @@ typedef struct {
 } mk_model_desc;
 
 typedef struct {
-    int batch;             /* sequences decoded together, 1..8 */
+    int batch;             /* sequences decoded together, 1..16 (above 8: tensor-core tiles) */
     const int *seq_len0;   /* host [batch]: cached tokens per sequence before step 0 */
     int max_steps;         /* the plan serves steps 0 .. max_steps-1 */
     int cache_slots;       /* S_max of the KV cache tensors; >= seq_len0[b] + max_steps */
@@ -96,6 +97,9 @@ typedef struct {
     int rows_qkv, rows_o, rows_up, rows_down, kchunk_down, rows_lm, attn_split;
     int page_bytes;        /* shared-memory page size; 0 = 16384 */
     int schedule;          /* MK_SCHED_*: how tasks are dealt to workers */
+    int tc_tiles;          /* GEMV tiles on tcgen05 tensor cores (128 weight rows x the batch, TMEM
+                              accumulators): 0 = for batch >= 8 where the shape allows, 1 = required
+                              (MK_ERR_UNSUPPORTED if the shape does not allow), -1 = never (batch <= 8) */
 } mk_target_desc;
 
 /* Queue assignment.  Either way tasks go to workers in one topological order,
@@ -117,6 +121,8 @@ typedef struct {
     uint64_t scratch_offset;         /* workspace offset from which every byte is rewritten
                                         within a step before it is read (activations, partials) */
     uint64_t algorithmic_bytes_step; /* weights once + KV read + KV append, at step 0 */
+    int tc_tiles;                    /* 1: the GEMV tiles run on tcgen05 tensor cores */
+    int ksplit_qkv, ksplit_o;        /* tensor-core plans: K splits of the QKV and O tiles */
 } mk_plan_info;
 
 /* ---- bindings: caller-owned device buffers ---- */
@@ -366,7 +372,9 @@ int mk_read_counters(mk_plan_t plan, void *workspace, uint32_t *out);
  *   [6..10] stamps of consumer thread 0 inside the op (attention: K pages ready, scores,
  *           V pages ready, P.V, partial written and arrived; tensor-core and GLM GEMM tiles:
  *           [7] pages ready, [9] K loop end, [10] reduction barrier passed; GLM A0: [9] loads
- *           and sum of squares, [10] reduction)
+ *           and sum of squares, [10] reduction; batch-1 row-per-warp tiles: [6] x in registers,
+ *           [7] first page ready, [8] pages done, [9] epilogue done)
+ *   [11] activation loader: activation staged
  *   [13] activation handed to the consumers   [14] published   [15] publisher saw the slot done
  * globaltimer ns (the GPU's globaltimer advances in 256 ns steps on GB300); 0 = not stamped.
  * Only filled by runs with MK_RUN_TRACE. */

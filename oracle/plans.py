@@ -123,21 +123,116 @@ def llama_step_ops(shape: LlamaShape, k: Knobs, B: int, seq0: Sequence[int], max
     return ops, edges, kinds
 
 
+@dataclass
+class TcKnobs:
+    ksplit_qkv: int   # K splits of the QKV tiles
+    ksplit_o: int     # K splits of the O tiles
+    kchunk_down: int  # K extent of one MLP-down tile
+    attn_split: int   # cache positions per attention task
+
+
+TC_M, TC_SEG, TC_KS = 128, 64, 128   # tile rows, segment rows, K columns per stage
+
+
+def tc_knobs(shape: LlamaShape, B: int, seq0: Sequence[int], max_steps: int, n_workers: int) -> TcKnobs:
+    """Tile knobs of a tensor-core plan, from the stated rules: a K split is
+    the largest power of two up to 8 that keeps the op's tasks within the
+    workers with whole 128-column stages; the MLP-down K chunk is the largest
+    of 2048, 1024, 512, 256 dividing the ffn that gives at least half as many
+    tasks as workers (else the smallest that divides); the attention split is
+    16384 / (2 head_dim) positions, doubled up to 256 while the attention
+    tasks outnumber the workers."""
+    G = shape.Hq // shape.Hkv
+
+    def ksplit(tiles, K):
+        k = 1
+        while k < 8 and tiles * k * 2 <= n_workers and K % (k * 2) == 0 and (K // (k * 2)) % TC_KS == 0:
+            k *= 2
+        return k
+
+    kc = 0
+    for c in (2048, 1024, 512, 256):
+        if shape.F % c == 0:
+            kc = c
+            if (shape.H // TC_M) * (shape.F // c) * 2 >= n_workers:
+                break
+    T = max(16, min(256, 16384 // (2 * shape.D)))
+    while 2 * T <= 256 and sum(_ceil(s + max_steps, T) for s in seq0) * shape.Hkv > n_workers:
+        T *= 2
+    return TcKnobs(ksplit(shape.Hkv * (G + 2) * shape.D // TC_M, shape.H), ksplit(shape.H // TC_M, shape.Hq * shape.D),
+                   kc, T)
+
+
+def llama_tc_step_ops(shape: LlamaShape, k: TcKnobs, B: int, seq0: Sequence[int], max_steps: int):
+    """The decode step on tensor-core tiles of 128 weight rows: per layer an
+    RMSNorm task per sequence, QKV tiles (K split), attention, O tiles (K
+    split, added into the residual), the MLP RMSNorm, MLP-up tiles of 64 gate
+    + 64 up rows, MLP-down tiles per K chunk; then the final RMSNorm and the
+    LM-head tiles.  The same rules (gcd / lcm events) turn it into a plan."""
+    G = shape.Hq // shape.Hkv
+    rows_group = (G + 2) * shape.D
+    nsplit = [_ceil(s + max_steps, k.attn_split) for s in seq0[:B]]
+    ns_max = max(nsplit)
+    H, QD = shape.H, shape.Hq * shape.D
+
+    def attn_rows(bid):
+        g, b, s = bid
+        return max(0, min(k.attn_split, seq0[b] + max_steps - 1 - s * k.attn_split))
+
+    ops: List[Op] = [Op("embed", (1, 1, 1), cost=lambda bid: B * H * 2)]
+    kinds = {"embed": ("embed", -1)}
+    edges: List[Edge] = []
+    whole = lambda a, b: edges.append(Edge(a, b, (-1, -1, -1), (-1, -1, -1)))
+    prev = "embed"
+    for l in range(shape.L):
+        na, qkv, attn, o, nm, up, down = (f"{n}{l}" for n in ("norma", "qkv", "attn", "o", "normm", "up", "down"))
+        ops.append(Op(na, (B, 1, 1), cost=lambda bid: H * 2))
+        ops.append(Op(qkv, (shape.Hkv, rows_group // TC_M, k.ksplit_qkv), cost=lambda bid: TC_M * (H // k.ksplit_qkv) * 2))
+        ops.append(Op(attn, (shape.Hkv, B, ns_max), exists=lambda bid: bid[2] < nsplit[bid[1]],
+                      cost=lambda bid: 2 * shape.D * 2 * attn_rows(bid)))
+        ops.append(Op(o, (H // TC_M, k.ksplit_o, 1), cost=lambda bid: TC_M * (QD // k.ksplit_o) * 2))
+        ops.append(Op(nm, (B, 1, 1), cost=lambda bid: H * 2))
+        ops.append(Op(up, (shape.F // TC_SEG, 1, 1), cost=lambda bid: TC_M * H * 2))
+        ops.append(Op(down, (H // TC_M, shape.F // k.kchunk_down, 1), cost=lambda bid: TC_M * k.kchunk_down * 2))
+        for n, kind in ((na, "norm"), (qkv, "qkv"), (attn, "attn"), (o, "o"), (nm, "norm"), (up, "up"),
+                        (down, "down")):
+            kinds[n] = (kind, l)
+        whole(prev, na)                                   # the residual, read whole
+        whole(na, qkv)                                    # x^, read whole
+        edges.append(Edge(qkv, attn, (1, 2, -1), (1, 0, -1)))   # the K-split axis reduces
+        edges.append(Edge(attn, o, (1, 0, -1), (-1, -1, -1)))
+        whole(o, nm)
+        whole(nm, up)
+        edges.append(Edge(up, down, (1, -1, -1), (-1, 1, -1)))
+        prev = down
+    ops.append(Op("normf", (B, 1, 1), cost=lambda bid: H * 2))
+    ops.append(Op("lm", (_ceil(shape.V, TC_M), 1, 1), cost=lambda bid: min(TC_M, shape.V - bid[0] * TC_M) * H * 2))
+    kinds["normf"] = ("norm", -1)
+    kinds["lm"] = ("lm", -1)
+    whole(prev, "normf")
+    whole("normf", "lm")
+    return ops, edges, kinds
+
+
 def _queue(tasks: List[PlannedTask], graph: rules.TaskGraph, n_workers: int) -> Tuple[List[List[int]], int]:
     q = rules.greedy_balance(range(len(tasks)), [t.cost for t in tasks], n_workers)
     return rules.pad_queues(q)
 
 
-def llama_step_plan(shape: LlamaShape, k: Knobs, B: int, seq0: Sequence[int], max_steps: int,
+def llama_step_plan(shape: LlamaShape, k, B: int, seq0: Sequence[int], max_steps: int,
                     n_workers: int) -> Plan:
     """Plan one decode step; the same plan serves ``max_steps`` consecutive steps.
+    ``k`` is a ``Knobs`` (GEMV tiles) or a ``TcKnobs`` (tensor-core tiles).
 
     Tasks inside each event's successor range are placed longest-first (only
     attention tasks differ in size), then dealt to workers greedily by bytes in
     that order.  The step ends with an extra event that every LM-head task
     triggers; the next step's embedding task waits on it one epoch back.
     """
-    ops, edges, kinds = llama_step_ops(shape, k, B, seq0, max_steps)
+    if isinstance(k, TcKnobs):
+        ops, edges, kinds = llama_tc_step_ops(shape, k, B, seq0, max_steps)
+    else:
+        ops, edges, kinds = llama_step_ops(shape, k, B, seq0, max_steps)
     g = rules.build_task_graph(ops, edges)
     opmap = {o.name: o for o in ops}
     cost = [opmap[t.op].cost(t.bid) for t in g.tasks]

@@ -27,6 +27,17 @@ void layout_workspace(Plan &p) {
     p.ws.err = take(E_WORDS * 4);
     p.ws.counters = take(p.thresholds.size() * 4);
     p.ws.arrive = take(p.kind == PLAN_LLAMA ? (uint64_t)L * B * Hq * 4 : 4);
+    // tensor-core plans: bf16 high/low activation rows [2 np, K] of the
+    // tiles' inputs (RMSNorm output, attention output, MLP activation); they
+    // sit in the region cleared at step 0, so the rows of padding sequences
+    // stay zero
+    if (p.tc) {
+        p.ws.xn = take((uint64_t)2 * p.np * H * 2);
+        p.ws.xo = take((uint64_t)2 * p.np * Hq * D * 2);
+        p.ws.act16 = take((uint64_t)2 * p.np * F * 2);
+    } else {
+        p.ws.xn = p.ws.xo = p.ws.act16 = 0;
+    }
     p.ws.queue = take(p.words.size() * 4);
     p.ws.optab = take((uint64_t)p.num_ops * N_SLOTS * 8);
     p.ws.seq0 = take((uint64_t)B * 4);
@@ -42,6 +53,7 @@ void layout_workspace(Plan &p) {
     } else {
         p.ws.hres = p.ws.hmid = p.ws.qkv = p.ws.part = p.ws.attn_out = p.ws.act = 0;
     }
+    p.ws.tmaps = p.tc ? take((uint64_t)(TC_NTMAPS_FIXED + TC_WMAPS_PER_LAYER * L + 1) * 128) : 0;
     p.ws.trace = take(total_slots * 16 * 8);
     p.ws.total = off;
 }
@@ -162,6 +174,9 @@ int mk_plan_info_get(mk_plan_t plan, mk_plan_info *info) {
     info->workspace_bytes = p.ws.total;
     info->scratch_offset = p.kind == PLAN_LLAMA ? p.ws.hres : p.ws.total;
     info->algorithmic_bytes_step = (uint64_t)p.alg_bytes;
+    info->tc_tiles = p.tc ? 1 : 0;
+    info->ksplit_qkv = p.ksplit_qkv;
+    info->ksplit_o = p.ksplit_o;
     return MK_OK;
 }
 

@@ -206,6 +206,17 @@ struct Smem {
     DEV uint64_t *act_empty() const { return full() + 2 * num_pages + 2; }
     DEV uint64_t *cbar() const { return full() + 2 * num_pages + 4; }
     DEV volatile int *ctrl() const { return reinterpret_cast<volatile int *>(mk_smem + o_ctrl); }
+    // tensor-core plans: the activation ring (in the activation-buffer region),
+    // its barriers, the two accumulators' barriers, the end-of-run drain, the
+    // per-page release counters of attention and the TMEM base address
+    DEV uint8_t *xslot(int s) const { return mk_smem + o_abuf + s * abuf_stride; }
+    DEV uint64_t *xfull() const { return full() + 2 * num_pages + 5; }
+    DEV uint64_t *xempty() const { return xfull() + TC_XSLOTS; }
+    DEV uint64_t *accfull() const { return xempty() + TC_XSLOTS; }
+    DEV uint64_t *accempty() const { return accfull() + 2; }
+    DEV uint64_t *drain() const { return accempty() + 2; }
+    DEV int *page_users() const { return reinterpret_cast<int *>(mk_smem + o_ctrl) + 16; }
+    DEV uint32_t *tmem_slot() const { return reinterpret_cast<uint32_t *>(mk_smem + o_ctrl) + 31; }
 };
 
 constexpr int SLOT_FRESH = 1;
@@ -346,7 +357,7 @@ DEV void consumer_sync(const KParams &P, const Smem S, uint32_t &phase, bool &ab
 // Trace stamp k of slot i: traced runs only, written by consumer thread 0
 // (inside ops, for a breakdown of where an instruction's time goes).
 DEV void trace_stamp(const KParams &P, int i, int k) {
-    if (P.trace && threadIdx.x == 64) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + k] = gtimer();
+    if (P.trace && threadIdx.x == CONSUMER_BASE) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + k] = gtimer();
 }
 
 DEV bool cta_aborting(const Smem S) { return __shfl_sync(FULL, (int)S.ctrl()[0], 0) != 0; }
@@ -436,7 +447,7 @@ DEV void fetch(WIns &I, const KParams &P, const int32_t *q, int i) {
 // instance for plans whose GEMV tiles all take the row-per-warp path and whose
 // head_dim is 64 -- it holds no other GEMV or attention variant, which keeps
 // its registers free of spills.
-constexpr int FL_GEN = 0, FL_GLM = 1, FL_LEAN = 2;
+constexpr int FL_GEN = 0, FL_GLM = 1, FL_LEAN = 2, FL_TC = 3;
 
 template <int FL>
 DEV bool ins_valid(const KParams &P, const WIns &I) {
@@ -453,8 +464,22 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
         if ((int)((uint32_t)F(I, W_WAIT + 2 * i) & ~WAIT_PREV_EPOCH) >= P.num_events) return false;
     for (int i = 0; i < ns; ++i)
         if ((uint32_t)F(I, W_SIG + 2 * i) >= (uint32_t)P.num_events) return false;
-    if (GLM != (opc >= MK_OP_GLM_A0) && opc != MK_OP_COUNTER) return false;  // each instance runs its own ops
-    if (opc >= MK_OP_GLM_A0) {
+    constexpr bool TC = FL == FL_TC;
+    const bool glm_op = opc >= MK_OP_GLM_A0 && opc <= MK_OP_GLM_FIN;
+    if (GLM != glm_op && opc != MK_OP_COUNTER) return false;  // each instance runs its own ops
+    if (opc == MK_OP_NORM && !TC) return false;
+    if (opc == MK_OP_NORM)
+        return F(I, P_NB) >= 0 && F(I, P_NB) < P.B && P.H % 4 == 0 && P.H <= 8192 && P.np >= P.B;
+    if (TC && opc >= MK_OP_QKV && opc <= MK_OP_LM && opc != MK_OP_ATTN) {
+        // tensor-core tile: whole stages, segment matrices among the op's maps, rows within the tile
+        const int kc = F(I, P_KC), k0 = F(I, P_K0), m0 = F(I, P_MAT), m1 = F(I, P_S1_MAT);
+        return kc > 0 && kc % TC_KS == 0 && k0 % TC_BOX == 0 && k0 + kc <= F(I, P_KTOT) &&
+               F(I, P_NPG) == kc / TC_KS && m0 >= 0 && m0 < 3 && m1 >= 0 && m1 < 3 && F(I, P_NROWS) > 0 &&
+               F(I, P_NROWS) <= TC_M && F(I, P_OUT0) >= 0 && F(I, P_ROW0) >= 0 && F(I, P_S1_ROW0) >= 0 &&
+               (P.np == 8 || P.np == 16) && P.B <= P.np && P.page_bytes == TC_STAGE_BYTES &&
+               (opc != MK_OP_UP || F(I, P_NROWS) == TC_SEG);
+    }
+    if (glm_op) {
         const int M = F(I, P_GL_M), T = F(I, P_GL_T);
         if (M <= 0 || M > GLM_MAX_M || T <= 0 || T > GLM_MAX_M || F(I, P_GL_POS0) < 0) return false;
         if (opc == MK_OP_GLM_A0) return F(I, P_ROW0) >= 0 && F(I, P_ROW0) < M && P.H % 128 == 0 && P.H <= 8192;
@@ -486,8 +511,11 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
         // more rows only as 2 or 4 pages of 16 rows on the batch-1 row-per-warp path
         const bool pages16 = P.B == 1 && kc % 256 == 0 && kc <= 2048 && P.page_bytes == 32 * kc;
         if (nrows <= 0) return false;
-        if (total > rmax && !(pages16 && opc != MK_OP_O && (total == 32 || total == 64) &&
-                              (opc != MK_OP_UP || nrows % 8 == 0)))
+        if (opc == MK_OP_UP && nrows > 8 && nrows % 8) return false;  // gate / up rows go to pages in groups of 8
+        // more rows only as whole 16-row pages (MLP-up: 8 gate + 8 up) on the batch-1 row-per-warp path
+        if (total > rmax && !(pages16 && opc != MK_OP_O && F(I, P_NPG) <= 64 &&
+                              (opc == MK_OP_UP ? 2 * nrows == 16 * F(I, P_NPG)
+                                               : nrows > 16 * (F(I, P_NPG) - 1) && nrows <= 16 * F(I, P_NPG))))
             return false;
         if (kc <= 0 || kc % 8 || 2 * kc > P.page_bytes || kc * P.B * 4 > P.abuf_bytes) return false;
         const int rpp = F(I, P_RPP);

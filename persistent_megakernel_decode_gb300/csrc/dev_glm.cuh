@@ -60,7 +60,7 @@ DEV uint32_t quant4(const float (&v)[4], float &scale) {
 DEV void glm_a0_task(const KParams &P, const Smem S, const WIns &I, int i, uint32_t &ured,
                                          bool ab) {
     constexpr int BPW = 8;  // blocks per warp: hidden <= 8192
-    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
     const int m = F(I, P_ROW0), H = P.H, nb = H >> 7;
     const uint8_t *x = reinterpret_cast<const uint8_t *>(PTR(I, S_GA_X)) + (size_t)m * H * 2;
     const uint8_t *res = reinterpret_cast<const uint8_t *>(PTR(I, S_GA_RES)) + (size_t)m * H * 2;
@@ -138,7 +138,7 @@ template <int NR>
 DEV void glm_gemm_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, uint32_t &ring, uint32_t &ured,
                        bool &ab) {
     constexpr int NG = NR / 8, KS = CONSUMER_WARPS / NG;
-    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
     const int g = lane >> 2, t = lane & 3, gi = warp % NG, ks = warp / NG;
     const int K = F(I, P_KC), KB = K >> 7, n0 = F(I, P_ROW0), rpp = F(I, P_RPP), npg = F(I, P_NPG);
     const int M = F(I, P_GL_M), ld = F(I, P_GL_LD), out0 = F(I, P_OUT0), rope = F(I, P_GL_ROPE), T = F(I, P_GL_T);
@@ -243,7 +243,7 @@ DEV void glm_gemm_task(const KParams &P, const Smem S, const WIns &I, int i, int
 // latent cache row = kv-lora || RoPE(k_pe); the index cache row = Indexer-K
 // with RoPE on its last 64 columns.
 DEV void glm_fin_task(const KParams &P, const WIns &I, bool ab) {
-    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
     const int m = F(I, P_ROW0), QL = F(I, P_GF_QLORA), KL = F(I, P_GF_KVLORA), ID = F(I, P_GF_IDX);
     const int slots = F(I, P_GF_SLOTS), LDQ = F(I, P_GF_QKVA_LD), T = F(I, P_GL_T), pos0 = F(I, P_GL_POS0);
     const __nv_bfloat16 *qkva = reinterpret_cast<const __nv_bfloat16 *>(PTR(I, S_GF_QKVA)) + (size_t)m * LDQ;

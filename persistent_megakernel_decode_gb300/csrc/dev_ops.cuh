@@ -25,7 +25,18 @@ namespace mk {
 // L2 round trips rather than one per loop iteration.
 constexpr int SC = 8;
 
-DEV void stage_copy(const float4 *s4, float4 *d4, int n4) {
+// Batch-1 row-per-warp tiles read x as 8-wide chunks c = lane + 32 k, two
+// float4 per chunk.  Staged in natural order, a warp's float4 loads would
+// touch 32-byte-strided addresses (two lanes per bank group); the activation
+// loader stages those tiles' x "lane-interleaved" instead: float4 q of the
+// natural order (chunk q / 2, half q % 2) goes to position
+// ((k * 2 + half) * 32 + lane) -- every warp load is then 512 contiguous bytes.
+DEV int rpw_perm4(int q) {
+    const int c = q >> 1;
+    return (((c >> 5) << 1) + (q & 1)) * 32 + (c & 31);
+}
+
+DEV void stage_copy(const float4 *s4, float4 *d4, int n4, bool perm) {
     const int lane = threadIdx.x & 31;
     for (int base = 0; base < n4; base += 32 * SC) {
         float4 v[SC];
@@ -37,13 +48,13 @@ DEV void stage_copy(const float4 *s4, float4 *d4, int n4) {
 #pragma unroll
         for (int j = 0; j < SC; ++j) {
             const int k = base + lane + 32 * j;
-            if (k < n4) d4[k] = v[j];
+            if (k < n4) d4[perm ? rpw_perm4(k) : k] = v[j];
         }
     }
 }
 
 template <int MAXB>
-DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab) {
+DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab, bool perm) {
     const int lane = threadIdx.x & 31;
     const int opc = F(I, W_OPC);
     const int B = P.B;
@@ -78,7 +89,7 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab) {
                     const int k = base + lane + 32 * j;
                     if (k < n4) {
                         ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
-                        if (!one_round) dst[k] = v[j];
+                        if (!one_round) dst[perm ? rpw_perm4(k) : k] = v[j];
                         if (hs) hs[k] = v[j];
                     }
                 }
@@ -96,7 +107,7 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab) {
 #pragma unroll
                 for (int j = 0; j < SC; ++j) {
                     const int k = lane + 32 * j;
-                    if (k < n4) dst[k] = norm(v[j], ww[j]);
+                    if (k < n4) dst[perm ? rpw_perm4(k) : k] = norm(v[j], ww[j]);
                 }
             } else {
                 __syncwarp();
@@ -109,7 +120,10 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab) {
 #pragma unroll
                     for (int j = 0; j < SC; ++j) {
                         const int k = base + lane + 32 * j;
-                        if (k < n4) dst[k] = norm(dst[k], ww[j]);
+                        if (k < n4) {
+                            const int q = perm ? rpw_perm4(k) : k;
+                            dst[q] = norm(dst[q], ww[j]);
+                        }
                     }
                 }
             }
@@ -127,7 +141,7 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab) {
         }
         for (int b = 0; b < B; ++b)
             stage_copy(reinterpret_cast<const float4 *>(src + b * ld), reinterpret_cast<float4 *>(abuf + (size_t)b * kc),
-                       kc / 4);
+                       kc / 4, perm);
     }
 }
 
@@ -350,7 +364,7 @@ DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, int sl,
     constexpr int RMAX = rows_max<MAXB>();
     constexpr int VT = RMAX * MAXB;            // partials per warp in a reduction buffer: row * MAXB + b
     constexpr int VL = VT >= 32 ? VT / 32 : 1; // epilogue values per lane: v = lane + 32 j
-    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
     const int opc = F(I, W_OPC);
     const int kc = F(I, P_KC), nrows = F(I, P_NROWS), npg = F(I, P_NPG);
     const int total = (opc == MK_OP_UP ? 2 : 1) * nrows;
@@ -558,7 +572,7 @@ DEV bool gemv_mma_tile(const KParams &P, const Smem S, const WIns &I, int i, int
     constexpr int RT = 16;                   // rows of the MMA's M side
     constexpr int VT = RT * MAXB;            // partials per warp in a reduction buffer: row * MAXB + b
     constexpr int VL = (VT + 31) / 32;
-    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
     const int g = lane >> 2, t = lane & 3;
     const int opc = F(I, W_OPC);
     const int kc = F(I, P_KC), nrows = F(I, P_NROWS), npg = F(I, P_NPG), rpp = F(I, P_RPP);
@@ -709,19 +723,21 @@ DEV bool gemv_mma_tile(const KParams &P, const Smem S, const WIns &I, int i, int
 // ---------------------------------------------------------------- batch 1, rows per warp
 // Batch-1 GEMV tiles with K a multiple of 256 up to 2048 take the
 // row-per-warp path: a tile is NPG pages of 16 rows (or one page of at most
-// 16), warp w computes rows w, w + 8, w + 16, ... (rows w and w + 8 of every
-// page) over the whole K, holding x (its lane's 8-wide chunks l, l + 32, ...)
-// in registers across tiles -- no cross-warp reduction and no barrier.
-// MLP-up tiles hold gate rows then up rows; with a multiple of 8 gate rows a
-// gate row and its up row fall to the same warp.
-constexpr int RPW_MAX_PAGES = 4;
+// 16), warp w computes rows w and w + 8 of every page over the whole K,
+// holding x (its lane's 8-wide chunks l, l + 32, ...) in registers across
+// tiles -- no cross-warp reduction and no barrier.  MLP-up pages hold 8 gate
+// rows and their 8 up rows, so a gate row and its up row fall to one warp in
+// one page.  Pages are taken one at a time in a loop (one copy of the code
+// for any page count) and each page's rows are stored as soon as they are
+// summed.
+constexpr int RPW_MAX_PAGES = 64;
 DEV bool rpw_tile(const KParams &P, const Dec &d) {
     if (P.B != 1 || d.opc < MK_OP_QKV || d.opc > MK_OP_LM || d.opc == MK_OP_ATTN) return false;
     if (d.kc % 256 || d.kc > 2048) return false;
     const bool up = d.opc == MK_OP_UP;
     if (d.npg == 1) return up ? d.nrows == 8 : d.nrows <= 16;
-    return (d.npg == 2 || d.npg == RPW_MAX_PAGES) && d.opc != MK_OP_O && P.page_bytes == 32 * d.kc &&
-           (!up || d.nrows % 8 == 0);
+    return d.npg >= 2 && d.npg <= RPW_MAX_PAGES && d.opc != MK_OP_O && P.page_bytes == 32 * d.kc &&
+           (up ? d.nrows == 8 * d.npg : d.nrows > 16 * (d.npg - 1) && d.nrows <= 16 * d.npg);
 }
 
 // The activation hand-off (activation loader stages, consumers wait) is due
@@ -773,7 +789,7 @@ DEV void rpw_row(const uint8_t *wrow, int lane, const XRow &x, uint64_t &acc) {
 template <int V>
 DEV bool rpw_finish(const KParams &P, const Dec &d, const uint64_t (&acc)[V], const float (&res)[V],
                     unsigned long long &lm_best, bool ab) {
-    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
     const int opc = d.opc, nrows = d.nrows, out0 = d.out0;
     const uint64_t ptr_a = d.out, ptr_b = d.out2;
     // after the butterfly, lanes L with L % (32 / V) == 0 hold row w + 8 (L / (32 / V))
@@ -820,58 +836,94 @@ DEV bool rpw_finish(const KParams &P, const Dec &d, const uint64_t (&acc)[V], co
     return true;
 }
 
-// KG = K / 256 chunks per lane, NPG = pages of the tile.  `handoff`: this
-// slot took the activation hand-off (the caller waited for activation slot
-// sl); x is reloaded from the slot's buffer when its input changed.  Returns
-// true (the warp wrote global memory).
-template <int KG, int NPG>
+// KG = K / 256 chunks per lane.  `handoff`: this slot took the activation
+// hand-off (the caller waited for activation slot sl); x is reloaded from the
+// slot's buffer when its input changed.  Each page: rows w and w + 8 of this
+// warp, one butterfly for both (lanes 0 and 16 then hold the two row sums),
+// the stores of the op.  Returns true (the warp wrote global memory).
+template <int KG>
 DEV bool gemv_rpw(const KParams &P, const Smem S, const Dec &d, int i, bool handoff, int sl, const float *slot,
                   XRow &x, uint32_t &ring, RingPos &rq, unsigned long long &lm_best, bool &ab) {
-    constexpr int V = 2 * NPG;  // rows of this warp: w + 8 v
-    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
-    const int opc = d.opc, row_bytes = d.kc * 2;
-    float res[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) res[v] = 0.f;
+    const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
+    const int opc = d.opc, row_bytes = d.kc * 2, npg = d.npg, nrows = d.nrows, out0 = d.out0;
+    float resid = 0.f;  // O tiles (one page): the residual of this lane's row, w (lane 0) or w + 8 (lane 16)
     if (handoff) {
         const long long key = ((long long)d.row << 32) | (uint32_t)d.k0;
         if (key != x.key) {
-            const float *xs = S.abuf(sl);
+            const float4 *xs = reinterpret_cast<const float4 *>(S.abuf(sl));  // lane-interleaved (rpw_perm4)
 #pragma unroll
             for (int k = 0; k < KG; ++k) {
-                const float4 a = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8);
-                const float4 c = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8 + 4);
+                const float4 a = xs[(2 * k) * 32 + lane];
+                const float4 c = xs[(2 * k + 1) * 32 + lane];
                 x.v[k][0] = pack2(a.x, a.y); x.v[k][1] = pack2(a.z, a.w);
                 x.v[k][2] = pack2(c.x, c.y); x.v[k][3] = pack2(c.z, c.w);
             }
             x.key = key;
         }
         if (opc == MK_OP_O) {  // O tiles have at most RESID_ROWS rows
-            const float *rs = slot_resid(P, const_cast<float *>(slot));
-#pragma unroll
-            for (int v = 0; v < V; ++v)
-                if (warp + 8 * v < RESID_ROWS) res[v] = rs[warp + 8 * v];
+            const int r = warp + (lane >> 4) * 8;
+            if (r < RESID_ROWS) resid = slot_resid(P, const_cast<float *>(slot))[r];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // x and the residual rows are in registers
     }
-    // rows w and w + 8 of every page of the tile (rows past the tile's end
-    // hold stale page bytes; their results are not stored)
-    uint64_t acc[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] = 0;
-#pragma unroll
-    for (int pg = 0; pg < NPG; ++pg) {
+    trace_stamp(P, i, 6);
+    float* const out = reinterpret_cast<float *>(d.out);
+    float bv = -INFINITY;  // LM head: this lane's best logit of the tile and its row
+    int bi = 0;
+    for (int pg = 0; pg < npg; ++pg) {
         if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
+        if (pg == 0) trace_stamp(P, i, 7);
         const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
-        rpw_row<KG>(page + (size_t)warp * row_bytes, lane, x, acc[2 * pg]);
-        rpw_row<KG>(page + (size_t)(warp + 8) * row_bytes, lane, x, acc[2 * pg + 1]);
+        uint64_t acc[2] = {0, 0};
+        rpw_row<KG>(page + (size_t)warp * row_bytes, lane, x, acc[0]);
+        rpw_row<KG>(page + (size_t)(warp + 8) * row_bytes, lane, x, acc[1]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
         rq.next(P.num_pages);
+        float y[2] = {sum2(acc[0]), sum2(acc[1])};
+        Bfly<2, 16>::run(y, lane);  // lanes 0-15: row w of the page, lanes 16-31: row w + 8
+        const float val = y[0];
+        if (opc == MK_OP_UP) {
+            // gate row 8 pg + w (page slot w) and its up row (slot w + 8)
+            const float u = __shfl_sync(FULL, val, 16);
+            const int r = 8 * pg + warp;
+            if (lane == 0 && !ab && r < nrows) out[out0 + r] = val / (1.0f + __expf(-val)) * u;
+            continue;
+        }
+        const int r = 16 * pg + warp + (lane >> 4) * 8;
+        const bool mine = (lane & 15) == 0 && !ab && r < nrows;
+        if (opc == MK_OP_QKV) {
+            if (mine) out[out0 + r] = val;
+        } else if (opc == MK_OP_O) {
+            if (mine) {
+                out[out0 + r] = resid + val;
+                reinterpret_cast<float *>(d.out2)[out0 + r] = resid + val;
+            }
+        } else if (opc == MK_OP_DOWN) {
+            if (mine) atomicAdd(out + out0 + r, val);
+        } else {  // LM head
+            if (mine) {
+                out[out0 + r] = val;
+                if (val > bv) { bv = val; bi = r; }  // rows rise with pg: the lowest index wins ties
+            }
+        }
     }
-    ring += NPG;
-    return rpw_finish<V>(P, d, acc, res, lm_best, ab);
+    ring += npg;
+    trace_stamp(P, i, 8);
+    if (opc == MK_OP_LM) {
+        // this warp's best row of the tile (lowest index on ties), then the
+        // step's running best per warp
+        unsigned long long key = bv > -INFINITY ? argmax_key(bv, out0 + bi) : 0ull;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) key = max(key, __shfl_xor_sync(FULL, key, o));
+        if (lane == 0 && key > lm_best && !ab) {
+            lm_best = key;
+            red_max_u64(reinterpret_cast<unsigned long long *>(d.out2) + (size_t)P.step, key);
+        }
+    }
+    trace_stamp(P, i, 9);
+    return true;
 }
 
 // Batch-1 tiles whose K (4096) is too long for x in registers, in pages of 8
@@ -893,7 +945,7 @@ template <int NPG>
 DEV bool gemv_rpw_wide(const KParams &P, const Smem S, const Dec &d, int i, int sl, const float *slot,
                        uint32_t &ring, RingPos &rq, unsigned long long &lm_best, bool &ab) {
     constexpr int KG = RPW_WIDE_K / 256;
-    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
     const int opc = d.opc, row_bytes = d.kc * 2;
     float res[NPG];
 #pragma unroll
@@ -913,14 +965,14 @@ DEV bool gemv_rpw_wide(const KParams &P, const Smem S, const Dec &d, int i, int 
         wrow[pg] = S.pages() + (size_t)rq.p * P.page_bytes + (size_t)warp * row_bytes;
         rq.next(P.num_pages);
     }
-    const float *xs = S.abuf(sl);
+    const float4 *xs = reinterpret_cast<const float4 *>(S.abuf(sl));  // lane-interleaved (rpw_perm4)
     uint64_t a0[NPG], a1[NPG];
 #pragma unroll
     for (int pg = 0; pg < NPG; ++pg) a0[pg] = a1[pg] = 0;
 #pragma unroll
     for (int k = 0; k < KG; ++k) {
-        const float4 xa = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8);
-        const float4 xb = *reinterpret_cast<const float4 *>(xs + (lane + 32 * k) * 8 + 4);
+        const float4 xa = xs[(2 * k) * 32 + lane];
+        const float4 xb = xs[(2 * k + 1) * 32 + lane];
         const uint64_t x0 = pack2(xa.x, xa.y), x1 = pack2(xa.z, xa.w), x2 = pack2(xb.x, xb.y), x3 = pack2(xb.z, xb.w);
 #pragma unroll
         for (int pg = 0; pg < NPG; ++pg) {
@@ -952,13 +1004,28 @@ DEV bool gemv_rpw_wide(const KParams &P, const Smem S, const Dec &d, int i, int 
 // writes that partial, and arrives on its head's counter; the warp that
 // arrives last for a head merges all of the head's partials (log-sum-exp
 // combine).  No barrier inside the task.
-template <int D>
+// Releases page p after the 8 consumer warps read it.  The tensor-core
+// instance's page barriers take one arrival (the MMA commit of a weight
+// stage), so there the last of the 8 warps arrives (a shared counter per page).
+template <int FL>
+DEV void page_release(const Smem S, int p) {
+    if constexpr (FL == FL_TC) {
+        if (atomicAdd(&S.page_users()[p], 1) == CONSUMER_WARPS - 1) {
+            S.page_users()[p] = 0;
+            mbar_arrive(&S.empty()[p]);
+        }
+    } else {
+        mbar_arrive(&S.empty()[p]);
+    }
+}
+
+template <int D, int FL>
 DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
                    bool &ab) {
     constexpr int PER = D / 32;
     constexpr int QS = D / 4 + 4;
     constexpr int DQ = D / 4;
-    const int ct = threadIdx.x - 64, warp = ct >> 5, lane = ct & 31;
+    const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
     const int G = P.Hq / P.Hkv, parts = CONSUMER_WARPS / G;
     const int hh = warp / parts, part = warp % parts;  // head within the kv group, token part
     const int b = F(I, P_B), g = F(I, P_G);
@@ -1035,7 +1102,7 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
     trace_stamp(P, i, 7);
     __syncwarp();
     if (lane == 0)
-        for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(kring + k) % P.num_pages]);
+        for (int k = 0; k < npg; ++k) page_release<FL>(S, (kring + k) % P.num_pages);
     float l = 0.f;
     for (int t = tb + lane; t < te; t += 32) {
         const float e = exp2f(sw[t - tb] - m);
@@ -1085,7 +1152,7 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
     for (int e = 0; e < PER; ++e) acc[0][e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
     __syncwarp();
     if (lane == 0) {
-        for (int k = 0; k < npg; ++k) mbar_arrive(&S.empty()[(vring + k) % P.num_pages]);
+        for (int k = 0; k < npg; ++k) page_release<FL>(S, (vring + k) % P.num_pages);
         mbar_arrive(&S.act_empty()[sl]);  // q, k, v of the slot no longer needed by this warp
     }
     trace_stamp(P, i, 9);
@@ -1154,12 +1221,26 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
         }
         M = Mn;
     }
+    if constexpr (FL == FL_TC) {
+        // the O tiles' input: bf16 high and low rows b and np + b of [2 np, Hq D]
+        uint16_t *o16 = reinterpret_cast<uint16_t *>(out);
+        const size_t ld = (size_t)P.Hq * D;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) out[((size_t)b * P.Hq + head) * D + lane * PER + e] = o[e] / L;
+        for (int e = 0; e < PER; ++e) {
+            const float v = o[e] / L;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+            o16[(size_t)b * ld + (size_t)head * D + lane * PER + e] = __bfloat16_as_ushort(hi);
+            o16[(size_t)(P.np + b) * ld + (size_t)head * D + lane * PER + e] = __bfloat16_as_ushort(lo);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) out[((size_t)b * P.Hq + head) * D + lane * PER + e] = o[e] / L;
+    }
 }
 
 DEV void embed_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, bool ab) {
-    const int ct = threadIdx.x - 64, lane = ct & 31;
+    const int ct = threadIdx.x - CONSUMER_BASE, lane = ct & 31;
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.act_empty()[sl]);
     if (ab) return;

@@ -18,6 +18,9 @@
 // records the failure in the workspace, raises a grid-wide abort flag, and
 // all roles drain the rest of the queue without waiting or writing, so the
 // kernel always returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -25,6 +28,7 @@
 
 #include "dev_glm.cuh"
 #include "dev_ops.cuh"
+#include "dev_tc.cuh"
 #include "planner.h"
 
 namespace mk {
@@ -47,11 +51,36 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
             break;
         }
+        if constexpr (FL == FL_TC) {
+            if (is_gemv_op(opc)) {  // tensor-core tile: one page per stage of 128 K columns
+                const TcTile t = tc_tile_fields(I);
+                if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 4] = gtimer();
+                bool stop = false;
+                for (int s = 0; s < t.nst; ++s) {
+                    if (!warp_wait_bar(P, S, &S.empty()[rp], rph ^ 1, 0, i, opc)) {
+                        stop = true;
+                        break;
+                    }
+                    if (lane == 0) tc_load_stage(t, s, S.pages() + (size_t)rp * PS, &S.full()[rp], pol);
+                    __syncwarp();
+                    ++ring;
+                    if (++rp == (uint32_t)NP) {
+                        rp = 0;
+                        rph ^= 1;
+                    }
+                }
+                if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 5] = gtimer();
+                if (stop) break;
+                continue;
+            }
+        }
         Seg s0, s1;
         const int nseg = describe<FL>(P, I, s0, s1);
         if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 4] = gtimer();
-        // Rows go to pages in order, as many whole rows per page as fit.  GEMV
-        // segments (MLP-up: gate rows, then up rows) share pages; attention
+        // Rows go to pages in order, as many whole rows per page as fit.  The
+        // two segments of an MLP-up tile share pages in groups of up to 8:
+        // gate rows 8g .. 8g + 7, then the same up rows (a tile of n <= 8
+        // gate rows is one group: its gate rows, then its up rows).  Attention
         // keeps its K rows and its V rows on separate pages.
         const int row_bytes = nseg > 0 ? s0.row_bytes : 0;
         const int rpp = row_bytes > 0 ? PS / row_bytes : 0;
@@ -89,9 +118,18 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
                 if (packed) {
                     const int r = k * rpp, nr = min(rpp, total - r);
                     mbar_expect_tx(bar, (uint32_t)nr * row_bytes);
-                    const int a0 = min(nr, max(0, n0 - r));       // rows from segment 0
-                    if (a0 > 0) copy_rows(s0, r, a0, dst, bar);
-                    if (nr > a0) copy_rows(s1, r + a0 - n0, nr - a0, dst + (size_t)a0 * row_bytes, bar);
+                    if (nseg == 1) {
+                        copy_rows(s0, r, nr, dst, bar);
+                    } else {
+                        const int gs = min(8, n0);  // group size; n0 is a multiple of 8 when above 8
+                        for (int j = r; j < r + nr;) {
+                            const int g = j / (2 * gs), w = j % (2 * gs);
+                            const bool up = w >= gs;
+                            const int run = min(r + nr - j, gs - (up ? w - gs : w));
+                            copy_rows(up ? s1 : s0, g * gs + (up ? w - gs : w), run, dst + (size_t)(j - r) * row_bytes, bar);
+                            j += run;
+                        }
+                    }
                 } else {
                     const bool second = k >= npg0;
                     const Seg &sg = second ? s1 : s0;
@@ -138,20 +176,11 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
     uint32_t seen_target = 0;
     uint32_t hs = 0;            // activation hand-offs so far; hand-off h uses activation slot h % 2
     HandoffChain chain;
+    uint32_t xq = 0;            // tensor-core plans: activation stages staged so far
     WIns I;
     fetch_init(I, P, myq);
-    for (int i = 0; i < P.lmax; ++i) {
-        fetch(I, P, myq, i);
-        const int opc = F(I, W_OPC);
-        if (opc == MK_OP_NOOP) continue;
-        if (!needs_handoff(P, I, decode(I), chain)) continue;  // same input as the previous slot: nothing to stage
-        const int sl = hs & 1;
-        const uint32_t use = hs >> 1;
-        if (!ab && !ins_valid<FL>(P, I)) {
-            if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 1);
-            ab = true;
-        }
-        if (!ab) ab = !warp_wait_bar(P, S, &S.act_empty()[sl], (use & 1) ^ 1, 1, i, opc);
+    // the instruction's event waits (acquire), right before its activation is read
+    auto wait_events = [&](int i, int opc) {
         const int cnt = F(I, W_CNT);
         for (int w = 0; w < (cnt & 0xff) && !ab; ++w) {
             const uint32_t ew = (uint32_t)F(I, W_WAIT + 2 * w);
@@ -167,6 +196,32 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
             }
         }
         if (!ab && lane == 0 && P.trace) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 2] = gtimer();
+    };
+    for (int i = 0; i < P.lmax; ++i) {
+        fetch(I, P, myq, i);
+        const int opc = F(I, W_OPC);
+        if (opc == MK_OP_NOOP) continue;
+        if constexpr (FL == FL_TC) {
+            if (is_gemv_op(opc)) {  // tensor-core tile: no slot hand-off, the input streams into the activation ring
+                if (!ab && !ins_valid<FL>(P, I)) {
+                    if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 1);
+                    ab = true;
+                }
+                wait_events(i, opc);
+                tc_stage_x(P, S, I, i, xq, ab);
+                if (lane == 0 && P.trace) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 11] = gtimer();
+                continue;
+            }
+        }
+        if (!needs_handoff(P, I, decode(I), chain)) continue;  // same input as the previous slot: nothing to stage
+        const int sl = hs & 1;
+        const uint32_t use = hs >> 1;
+        if (!ab && !ins_valid<FL>(P, I)) {
+            if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 1);
+            ab = true;
+        }
+        if (!ab) ab = !warp_wait_bar(P, S, &S.act_empty()[sl], (use & 1) ^ 1, 1, i, opc);
+        wait_events(i, opc);
         float *slot = reinterpret_cast<float *>(S.act(sl));
         int flags = 0;
         uint32_t tx = 0;  // bytes of bulk copies completing on the slot's full barrier
@@ -189,16 +244,20 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
             else g4 ? stage_attn<128, 4>(P, I, slot, ab, rope128) : stage_attn<128, 8>(P, I, slot, ab, rope128);
             flags = SLOT_FRESH;
             key0 = key1 = -1;
-        } else if (opc >= MK_OP_QKV && opc <= MK_OP_LM) {
+        } else if (FL != FL_TC && opc >= MK_OP_QKV && opc <= MK_OP_LM) {
             // two buffers: buffer sl was last read by instruction i - 2, whose
             // slot release was awaited above; one buffer: instruction i - 1
             // may still read it
             const int bi = two_bufs ? sl : 0;
-            const long long key = ((long long)F(I, W_ROW) << 32) | (uint32_t)F(I, P_K0);
+            // batch-1 row-per-warp tiles read x lane-interleaved (rpw_perm4);
+            // the layout is part of what a buffer holds
+            const Dec dd = decode(I);
+            const bool perm = MAXB == 1 && (rpw_tile(P, dd) || (FL != FL_LEAN && rpw_wide_tile(P, dd)));
+            const long long key = ((long long)F(I, W_ROW) << 32) | (uint32_t)F(I, P_K0) | ((long long)perm << 62);
             if (key != (bi ? key1 : key0) || F(I, P_SNAP) > 0) {
                 if (!two_bufs && hs > 0 && !ab)
                     ab = !warp_wait_bar(P, S, &S.act_empty()[(hs - 1) & 1], ((hs - 1) >> 1) & 1, 1, i, opc);
-                stage_gemv<MAXB>(P, I, S.abuf(bi), ab);
+                stage_gemv<MAXB>(P, I, S.abuf(bi), ab, perm);
                 flags = SLOT_FRESH;
             }
             if (opc == MK_OP_O) stage_resid(P, I, slot);
@@ -208,6 +267,7 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
             key0 = key1 = -1;
         }
         __syncwarp();
+        if (lane == 0 && P.trace) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 11] = gtimer();
         if (lane == 0) {
             S.ctrl()[1 + sl] = flags;
             if (tx == 0) mbar_arrive(&S.act_full()[sl]);  // (else stage_glm's arrive.expect_tx was the arrival)
@@ -288,20 +348,11 @@ DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
 // A consumer warp records that queue slot i is finished.
 DEV void handoff_progress(const Smem S, int i, bool wrote_global) {
     __syncwarp();
-    const int warp = (threadIdx.x >> 5) - 2;
+    const int warp = (threadIdx.x >> 5) - FIRST_CONSUMER_WARP;
     if ((threadIdx.x & 31) == 0) {
         if (wrote_global) st_release_cta(&S.ctrl()[8 + warp], i + 1);
         else st_relaxed_cta(&S.ctrl()[8 + warp], i + 1);
     }
-}
-
-// Row-per-warp variants by pages per tile.
-template <int KG>
-DEV void gemv_rpw_pages(const KParams &P, const Smem S, const Dec &d, int i, bool handoff, int sl, const float *slot,
-                        XRow &x, uint32_t &ring, RingPos &rq, unsigned long long &lm_best, bool &ab) {
-    if (d.npg <= 1) gemv_rpw<KG, 1>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
-    else if (d.npg <= 2) gemv_rpw<KG, 2>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
-    else gemv_rpw<KG, 4>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
 }
 
 // GEMV variants: K chunks per consumer thread (NCH) x one page or several.
@@ -342,7 +393,7 @@ DEV bool gemv_dispatch(const KParams &P, const Smem S, const WIns &I, int i, int
 template <int MAXB, int FL>
 DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
     constexpr bool GLM = FL == FL_GLM;
-    const int ct = threadIdx.x - 64, lane = ct & 31;
+    const int ct = threadIdx.x - CONSUMER_BASE, lane = ct & 31;
     uint32_t ring = 0, cph = 0, ured = 0;
     uint32_t hs = 0;  // activation hand-offs so far (the activation loader counts the same ones)
     HandoffChain chain;
@@ -350,6 +401,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
     RingPos rq;       // ring position of the next page (kept in step with ring)
     bool ab = false;
     unsigned long long lm_best = 0;
+    TcState tc;       // tensor-core plans: tiles and activation stages so far
     WIns I;
     fetch_init(I, P, myq);
     for (int i = 0; i < P.lmax; ++i) {
@@ -359,7 +411,8 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         if (opc == MK_OP_NOOP) continue;
         uint64_t t_start = 0;
         if (ct == 0 && P.trace) t_start = gtimer();
-        const bool handoff = needs_handoff(P, I, d, chain);
+        // tensor-core tiles take no slot hand-off (their input streams into the activation ring)
+        const bool handoff = FL == FL_TC && is_gemv_op(opc) ? false : needs_handoff(P, I, d, chain);
         const int sl = hs & 1;
         bool wrote = true;  // the warp wrote global memory in this slot
         if (handoff && !ab) ab = !warp_wait_bar(P, S, &S.act_full()[sl], (hs >> 1) & 1, 2, i, opc);
@@ -382,30 +435,39 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
                 wrote = false;
             }
         } else if (opc == MK_OP_ATTN) {
-            if (FL == FL_LEAN || P.D == 64) attn_task<64>(P, S, I, i, sl, slot, ring, ab);
-            else attn_task<128>(P, S, I, i, sl, slot, ring, ab);
+            if (FL == FL_LEAN || P.D == 64) attn_task<64, FL>(P, S, I, i, sl, slot, ring, ab);
+            else attn_task<128, FL>(P, S, I, i, sl, slot, ring, ab);
             rq.set(ring, P.num_pages);
+        } else if (FL == FL_TC && is_gemv_op(opc)) {
+            wrote = tc_tile(P, S, I, d, i, ring, tc, lm_best, ab);
+            rq.set(ring, P.num_pages);
+        } else if (FL == FL_TC && opc == MK_OP_NORM) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // the slot holds nothing for it
+            norm_task(P, S, I, ab);
         } else if (opc == MK_OP_EMBED) {
             consumer_sync(P, S, cph, ab, i);
             embed_task(P, S, I, i, sl, ab);
         } else if (opc >= MK_OP_QKV) {
-            if (MAXB == 1 && rpw_tile(P, d)) {  // (a constant condition for larger batches)
-                const int kg = d.kc >> 8;
-                if (kg <= 1) gemv_rpw_pages<1>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
-                else if (kg <= 2) gemv_rpw_pages<2>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
-                else if (kg <= 4) gemv_rpw_pages<4>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
-                else gemv_rpw_pages<8>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
-            } else if constexpr (FL != FL_LEAN) {
-                bool wide = false;
-                if constexpr (MAXB == 1) {
-                    wide = rpw_wide_tile(P, d);
-                    if (wide && d.npg <= 1) gemv_rpw_wide<1>(P, S, d, i, sl, slot, ring, rq, lm_best, ab);
-                    else if (wide) gemv_rpw_wide<2>(P, S, d, i, sl, slot, ring, rq, lm_best, ab);
+            if constexpr (FL != FL_TC) {  // (the tensor-core instance took its GEMV tiles above)
+                if (MAXB == 1 && rpw_tile(P, d)) {  // (a constant condition for larger batches)
+                    const int kg = d.kc >> 8;
+                    if (kg <= 1) gemv_rpw<1>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+                    else if (kg <= 2) gemv_rpw<2>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+                    else if (kg <= 4) gemv_rpw<4>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+                    else gemv_rpw<8>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
+                } else if constexpr (FL != FL_LEAN) {
+                    bool wide = false;
+                    if constexpr (MAXB == 1) {
+                        wide = rpw_wide_tile(P, d);
+                        if (wide && d.npg <= 1) gemv_rpw_wide<1>(P, S, d, i, sl, slot, ring, rq, lm_best, ab);
+                        else if (wide) gemv_rpw_wide<2>(P, S, d, i, sl, slot, ring, rq, lm_best, ab);
+                    }
+                    if (!wide) wrote = gemv_dispatch<MAXB>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
+                } else {  // the planner picks the lean instance only for plans without such tiles
+                    if (lane == 0 && !ab) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 2);
+                    ab = true;
                 }
-                if (!wide) wrote = gemv_dispatch<MAXB>(P, S, I, i, sl, slot, ring, rq, ured, lm_best, ab);
-            } else {  // the planner picks the lean instance only for plans without such tiles
-                if (lane == 0 && !ab) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 2);
-                ab = true;
             }
         } else {  // COUNTER: the slot handshake only
             consumer_sync(P, S, cph, ab, i);
@@ -439,28 +501,66 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
     S.o_bars = S.o_aux + P.aux_bytes;
     S.o_ctrl = S.o_bars + MBAR_BYTES;
     S.num_pages = P.num_pages;
+    constexpr bool TC = FL == FL_TC;
+    const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int p = 0; p < P.num_pages; ++p) {
             mbar_init(&S.full()[p], 1);
-            mbar_init(&S.empty()[p], CONSUMER_WARPS);
+            // tensor-core instance: one arrival, the MMA commit of a weight
+            // stage or the last of the 8 warps reading an attention page
+            mbar_init(&S.empty()[p], TC ? 1 : CONSUMER_WARPS);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&S.act_full()[s], 1);
             mbar_init(&S.act_empty()[s], CONSUMER_WARPS);
         }
         mbar_init(S.cbar(), CONSUMER_WARPS);
+        if (TC) {
+            for (int s = 0; s < TC_XSLOTS; ++s) {
+                mbar_init(&S.xfull()[s], 1);
+                mbar_init(&S.xempty()[s], 1);
+            }
+            for (int a = 0; a < 2; ++a) {
+                mbar_init(&S.accfull()[a], 1);
+                mbar_init(&S.accempty()[a], TC_EPI_WARPS);
+            }
+            mbar_init(S.drain(), 1);
+        }
         for (int k = 0; k < CTRL_WORDS; ++k) S.ctrl()[k] = 0;
+        if (TC) {
+            for (int p = 0; p < P.num_pages; ++p) S.page_users()[p] = 0;
+            // the swizzled stage buffers need 1024-byte alignment: refuse to run otherwise
+            if ((saddr(mk_smem) & 1023u) != 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, -1, -1, 0, 0, -1, 3);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
+    if (TC && warp == 3) {  // the idle warp owns the TMEM accumulators
+        tmem_alloc(S.tmem_slot(), TC_TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (TC) tc_fence_before();
     __syncthreads();
+    if (TC) tc_fence_after();
     const int32_t *myq = P.queue + (size_t)blockIdx.x * P.lmax * W_WORDS;
-    const int warp = threadIdx.x >> 5;
     if (warp == 0) loader_role<FL>(P, S, myq);
     else if (warp == 1) aloader_role<MAXB, FL>(P, S, myq);
     else if (warp == PUBLISHER_WARP) publisher_role(P, S, myq);
-    else consumer_role<MAXB, FL>(P, S, myq);
+    else if (warp >= FIRST_CONSUMER_WARP) consumer_role<MAXB, FL>(P, S, myq);
+    if (TC && warp == FIRST_CONSUMER_WARP + TC_MMA_WARP) {
+        // every MMA this warp issued has completed before the accumulators are freed
+        if ((threadIdx.x & 31) == 0) tc_commit(S.drain());
+        __syncwarp();
+        const uint64_t t0 = gtimer();
+        while (!mbar_test(S.drain(), 0) && gtimer() - t0 < 2 * P.timeout_ns) {
+        }
+    }
+    if (TC) tc_fence_before();
     __syncthreads();
+    if (TC && warp == 3) {
+        tc_fence_after();
+        tmem_dealloc(*S.tmem_slot(), TC_TMEM_COLS);
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -487,6 +587,7 @@ using KernelFn = void (*)(const KParams);
 
 static KernelFn pick_kernel(const Plan &p) {
     if (p.kind == PLAN_GLM) return mk_interp<1, FL_GLM>;
+    if (p.tc) return mk_interp<TC_MAXB, FL_TC>;
     const int B = p.B;
     if (B <= 1) return p.lean ? mk_interp<1, FL_LEAN> : mk_interp<1, FL_GEN>;
     if (B <= 2) return mk_interp<2, FL_GEN>;
@@ -526,7 +627,71 @@ static int build_glm_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab) {
     return MK_OK;
 }
 
-static int build_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab) {
+// ---- tensor maps of the tensor-core plans --------------------------------
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+static_assert(sizeof(CUtensorMap) == 128, "tensor maps are 128-byte records");
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// A row-major bf16 matrix [rows, cols] read in boxes of 64 columns x
+// box_rows rows, landing 128-byte swizzled (the tiles' K-major layout).
+static int encode_map(CUtensorMap *m, uint64_t base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return set_error(MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)TC_BOX, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, reinterpret_cast<void *>(base), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[120];
+        std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for a %llu x %llu matrix", (int)r,
+                      (unsigned long long)rows, (unsigned long long)cols);
+        return set_error(MK_ERR_CUDA, buf);
+    }
+    return MK_OK;
+}
+
+// Tensor maps, in the workspace's map table order: the three activations
+// (normalised x, attention output, MLP activation; 2 np rows each), then per
+// layer Wq, Wk, Wv, Wo, Wg, Wu, Wd, then the LM head.
+static int build_tc_maps(Plan &p, uint8_t *ws, std::vector<CUtensorMap> &maps) {
+    const mk_model_desc &m = p.model;
+    const int L = m.layers, H = m.hidden, QD = m.q_heads * m.head_dim, KD = m.kv_heads * m.head_dim, F = m.ffn;
+    maps.assign(TC_NTMAPS_FIXED + TC_WMAPS_PER_LAYER * L + 1, CUtensorMap{});
+    const uint64_t W = (uint64_t)(uintptr_t)ws;
+    const uint32_t xr = 2 * p.np;
+    int rc = encode_map(&maps[0], W + p.ws.xn, H, xr, xr);
+    if (!rc) rc = encode_map(&maps[1], W + p.ws.xo, QD, xr, xr);
+    if (!rc) rc = encode_map(&maps[2], W + p.ws.act16, F, xr, xr);
+    for (int l = 0; l < L && !rc; ++l) {
+        CUtensorMap *t = &maps[TC_NTMAPS_FIXED + TC_WMAPS_PER_LAYER * l];
+        rc = encode_map(t + 0, p.bind[MK_BIND_WQ][l], H, QD, TC_SEG);
+        if (!rc) rc = encode_map(t + 1, p.bind[MK_BIND_WK][l], H, KD, TC_SEG);
+        if (!rc) rc = encode_map(t + 2, p.bind[MK_BIND_WV][l], H, KD, TC_SEG);
+        if (!rc) rc = encode_map(t + 3, p.bind[MK_BIND_WO][l], QD, H, TC_SEG);
+        if (!rc) rc = encode_map(t + 4, p.bind[MK_BIND_WG][l], H, F, TC_SEG);
+        if (!rc) rc = encode_map(t + 5, p.bind[MK_BIND_WU][l], H, F, TC_SEG);
+        if (!rc) rc = encode_map(t + 6, p.bind[MK_BIND_WD][l], F, H, TC_SEG);
+    }
+    if (!rc) rc = encode_map(&maps.back(), p.bind[MK_BIND_LM_HEAD][0], H, m.vocab, TC_SEG);
+    return rc;
+}
+
+static int build_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab, std::vector<CUtensorMap> &maps) {
     tab.assign((size_t)p.num_ops * N_SLOTS, 0);
     if (p.kind == PLAN_GLM) return build_glm_table(p, ws, tab);
     if (p.kind != PLAN_LLAMA) return MK_OK;
@@ -605,6 +770,41 @@ static int build_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab) {
         default: break;
         }
     }
+    if (p.tc) {
+        // tensor-core plans: the tiles' tensor maps and bf16 activation rows
+        if (int rc = build_tc_maps(p, ws, maps)) return rc;
+        auto tmap = [&](int idx) { return W + p.ws.tmaps + (uint64_t)idx * sizeof(CUtensorMap); };
+        const uint64_t xn = W + p.ws.xn, xo = W + p.ws.xo, a16 = W + p.ws.act16;
+        for (int o = 0; o < p.num_ops; ++o) {
+            uint64_t *r = &tab[(size_t)o * N_SLOTS];
+            const int l = p.op_layer[o];
+            const int wl = TC_NTMAPS_FIXED + TC_WMAPS_PER_LAYER * std::max(l, 0);
+            switch (p.op_kind[o]) {
+            case MK_OP_NORM: {
+                const int which = p.op_aux[o];
+                r[S_N_H] = hres;
+                r[S_N_W] = which == 0   ? p.bind[MK_BIND_NORM_ATTN][l]
+                           : which == 1 ? p.bind[MK_BIND_NORM_MLP][l]
+                                        : p.bind[MK_BIND_NORM_FINAL][0];
+                r[S_N_XN] = xn; r[S_N_QKV] = qkv; r[S_N_HIST] = hist;
+                break;
+            }
+            case MK_OP_QKV:
+                r[S_T_W0] = tmap(wl + 0); r[S_T_W1] = tmap(wl + 1); r[S_T_W2] = tmap(wl + 2); r[S_T_X] = tmap(0);
+                break;
+            case MK_OP_ATTN: r[S_AT_OUT] = xo; break;
+            case MK_OP_O: r[S_T_W0] = tmap(wl + 3); r[S_T_X] = tmap(1); r[S_G_OUT] = hres; break;
+            case MK_OP_UP:
+                r[S_T_W0] = tmap(wl + 4); r[S_T_W1] = tmap(wl + 5); r[S_T_X] = tmap(0); r[S_G_OUT] = a16;
+                break;
+            case MK_OP_DOWN: r[S_T_W0] = tmap(wl + 6); r[S_T_X] = tmap(2); r[S_G_OUT] = hres; break;
+            case MK_OP_LM:
+                r[S_T_W0] = tmap(TC_NTMAPS_FIXED + TC_WMAPS_PER_LAYER * p.model.layers); r[S_T_X] = tmap(0);
+                break;
+            default: break;
+            }
+        }
+    }
     return MK_OK;
 }
 
@@ -627,6 +827,7 @@ static KParams base_params(const Plan &p, uint8_t *ws) {
     k.B = p.B;
     k.H = m.hidden; k.Hq = m.q_heads; k.Hkv = m.kv_heads > 0 ? m.kv_heads : 1; k.D = m.head_dim; k.F = m.ffn;
     k.V = m.vocab; k.L = m.layers; k.Smax = p.smax; k.qk_norm = m.qk_norm; k.nsplit_max = p.nsplit_max;
+    k.np = p.tc ? p.np : 0;
     k.eps = m.eps;
     k.theta = m.rope_theta;
     if (p.kind == PLAN_GLM) {
@@ -656,9 +857,15 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
     cudaError_t e;
     if (p.table_dirty || p.uploaded_ws != workspace) {
         std::vector<uint64_t> tab;
-        if (int rc = build_table(p, ws, tab)) return rc;
+        std::vector<CUtensorMap> maps;
+        if (int rc = build_table(p, ws, tab, maps)) return rc;
         e = cudaMemcpyAsync(ws + p.ws.optab, tab.data(), tab.size() * 8, cudaMemcpyHostToDevice, stream);
         if (e != cudaSuccess) return cuda_fail(e, "upload operand table");
+        if (!maps.empty()) {
+            e = cudaMemcpyAsync(ws + p.ws.tmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice,
+                                stream);
+            if (e != cudaSuccess) return cuda_fail(e, "upload tensor maps");
+        }
         if (p.uploaded_ws != workspace) {
             e = cudaMemcpyAsync(ws + p.ws.queue, p.words.data(), p.words.size() * 4, cudaMemcpyHostToDevice, stream);
             if (e != cudaSuccess) return cuda_fail(e, "upload queue");
@@ -696,7 +903,7 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
     if (dev < 0 || dev >= kMaxDevices) return set_error(MK_ERR_INVALID, "device ordinal out of range");
     if (configured_smem[dev] < p.smem_bytes) {
         for (KernelFn f : {mk_interp<1, FL_GEN>, mk_interp<2, FL_GEN>, mk_interp<4, FL_GEN>, mk_interp<8, FL_GEN>,
-                           mk_interp<1, FL_GLM>, mk_interp<1, FL_LEAN>}) {
+                           mk_interp<1, FL_GLM>, mk_interp<1, FL_LEAN>, mk_interp<TC_MAXB, FL_TC>}) {
             e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         }

@@ -38,6 +38,22 @@ enum : int {
     P_RPP = W_P + 8,    // weight rows per page: page bytes / (2 * K chunk)
     P_NPG = W_P + 9,    // pages of the tile: ceil(rows of all segments / P_RPP)
 };
+// Tensor-core GEMV tiles (batch 8..16): 128 weight rows in two segments of
+// 64 (P_ROW0 = first row of segment 0 in matrix P_MAT, P_S1_ROW0 / P_S1_MAT
+// of segment 1; matrices index the op's tensor-map slots S_T_W0 + m), K
+// range [P_K0, P_K0 + P_KC) of a row of P_KTOT elements, P_NPG = stages of
+// 128 K columns, P_OUT0 = first output row, P_NROWS = rows stored (< 128 only
+// for a last partial tile).
+enum : int {
+    P_S1_ROW0 = W_P + 10,
+    P_S1_MAT = W_P + 11,
+};
+// NORM payload (tensor-core plans)
+enum : int {
+    P_NB = W_P + 0,      // sequence
+    P_NZERO = W_P + 1,   // 1: also zero that sequence's qkv row (the QKV tiles split K and add)
+    P_NSNAP = W_P + 2,   // 1 + layer whose residual is captured, or 0
+};
 // ATTN payload
 enum : int {
     P_G = W_P + 0, P_B = W_P + 1, P_SPLIT = W_P + 2, P_T0 = W_P + 3, P_T = W_P + 4,
@@ -80,6 +96,12 @@ enum : int {
     S_GA_X = 0, S_GA_RES = 1, S_GA_NORM = 2, S_GA_RES_OUT = 3, S_GA_QA = 4, S_GA_SA = 5,
     S_GG_W = 0, S_GG_SW = 1, S_GG_XQ = 2, S_GG_XS = 3, S_GG_OUT = 4, S_GG_ROPE = 5,
     S_GF_QKVA = 0, S_GF_IK = 1, S_GF_QB = 2, S_GF_SB = 3, S_GF_LAT = 4, S_GF_IDX = 5, S_GF_ROPE = 6,
+    // NORM (tensor-core plans): residual fp32 [B, H], weight, bf16 high/low rows [2 NP, H],
+    // qkv to zero, hidden capture
+    S_N_H = 0, S_N_W = 1, S_N_XN = 2, S_N_QKV = 3, S_N_HIST = 4,
+    // tensor-core GEMV tiles: the weight tensor maps of the op (QKV: Wq, Wk, Wv; UP: Wg, Wu;
+    // else the op's matrix) and the input activation's tensor map (bf16 high/low rows)
+    S_T_W0 = 7, S_T_W1 = 8, S_T_W2 = 9, S_T_X = 10,
     // every GEMV op: its output (QKV: qkv, O: residual, UP: activation, DOWN:
     // residual, LM: logits) and second output (O: mid residual, LM: argmax keys)
     S_G_OUT = 14, S_G_OUT2 = 15,
@@ -104,16 +126,38 @@ struct KParams {
     int step, flags;
     int num_pages, page_bytes, act_bytes, abuf_bytes, abuf_count, aux_bytes, red_bytes, smem_bytes;
     int B, H, Hq, Hkv, D, F, V, L, Smax, qk_norm, nsplit_max;
+    int np;                 // tensor-core plans: the batch padded to 8 or 16 (N = 2 np), else 0
     float eps, theta;
 };
 
+// Warp roles: warpgroup 0 holds the loader (warp 0), the activation loader
+// (1), the publisher (2) and one idle warp (3); warpgroups 1 and 2 are the 8
+// consumer warps (warp w of them sits on TMEM lane quarter w % 4).
 constexpr int CONSUMER_WARPS = 8;
 constexpr int CONSUMERS = CONSUMER_WARPS * 32;
-constexpr int THREADS = CONSUMERS + 96;   // + loader, activation-loader and publisher warps
-constexpr int PUBLISHER_WARP = CONSUMER_WARPS + 2;
+constexpr int FIRST_CONSUMER_WARP = 4;
+constexpr int CONSUMER_BASE = FIRST_CONSUMER_WARP * 32;  // thread index of consumer thread 0
+constexpr int THREADS = CONSUMERS + CONSUMER_BASE;
+constexpr int PUBLISHER_WARP = 2;
 constexpr int RESID_ROWS = 16;           // residual slice staged per slot for O tiles
 constexpr int MAX_TILE_ROWS = 16;
 constexpr int NRED = 4;                  // cross-warp reduction buffers, used round robin by GEMV tiles
+
+// Tensor-core GEMV tiles (batch 8..16; see dev_tc.cuh).
+constexpr int TC_M = 128;          // weight rows per tile (two segments of 64)
+constexpr int TC_SEG = 64;         // rows per segment
+constexpr int TC_KS = 128;         // K columns per stage
+constexpr int TC_BOX = 64;         // K columns per TMA box (128 bytes of bf16)
+constexpr int TC_STAGE_BYTES = TC_M * TC_KS * 2;   // 32 KB of weights per stage = one page
+constexpr int TC_KSTEP = 16;       // K of one kind::f16 MMA
+constexpr int TC_ACC_COLS = 32;    // TMEM columns of one accumulator (N <= 32)
+constexpr int TC_TMEM_COLS = 2 * TC_ACC_COLS;
+constexpr int TC_XSLOTS = 4;       // activation ring slots
+constexpr int TC_EPI_WARPS = 4;    // consumer warps 0..3 read the accumulator
+constexpr int TC_MMA_WARP = 4;     // consumer warp whose lane 0 issues the MMAs
+constexpr int TC_MAXB = 16;        // sequences of a tensor-core plan
+constexpr int TC_NTMAPS_FIXED = 3; // tensor maps of the three activations (norm out, attention out, MLP act)
+constexpr int TC_WMAPS_PER_LAYER = 7;  // Wq, Wk, Wv, Wo, Wg, Wu, Wd
 
 #ifdef __CUDACC__
 #define MK_HD __host__ __device__
@@ -126,6 +170,9 @@ constexpr int NRED = 4;                  // cross-warp reduction buffers, used r
 MK_HD inline int attn_pages(int T, int D, int page_bytes) {
     return (T + page_bytes / (2 * D) - 1) / (page_bytes / (2 * D));
 }
+// Bytes of one activation stage of a tensor-core tile: 2 np rows (high
+// parts, then low parts) of TC_KS bf16 values.
+MK_HD inline int tc_xstage_bytes(int np) { return 2 * np * TC_KS * 2; }
 
 }  // namespace mk
 

@@ -595,6 +595,262 @@ int plan_graph(const mk_graph_desc *g, const mk_target_desc *tgt, int num_worker
     return finish_queues(p, g->round_robin != 0, false);
 }
 
+// ---- Llama-style decode step on tensor-core tiles (batch 8..16) -------------
+// Per layer: NORM (attention RMSNorm, one task per sequence: bf16 high/low
+// rows of x^ for the tiles; zeroes the qkv rows the K-split QKV tiles add
+// into) -> QKV tiles -> attention -> O tiles (K split, added into the
+// residual) -> NORM (MLP RMSNorm) -> MLP-up tiles (64 gate + 64 up rows,
+// SiLU(g) u as bf16 high/low) -> MLP-down tiles per K chunk (added into the
+// residual); then the final NORM and the LM-head tiles.  Every GEMV tile is
+// 128 weight rows over a K range in stages of 128 columns.
+static int plan_llama_tc(const mk_model_desc *m, const mk_step_desc *s, const mk_target_desc *tgt, int num_workers,
+                         int smem_per_cta, Plan &p) {
+    const int L = m->layers, H = m->hidden, Hq = m->q_heads, Hkv = m->kv_heads, D = m->head_dim, F = m->ffn,
+              V = m->vocab, B = s->batch, G = Hq / Hkv;
+    if (tgt->page_bytes != 0 && tgt->page_bytes != TC_STAGE_BYTES)
+        return set_error(MK_ERR_UNSUPPORTED, "tensor-core plans use 32 KB pages");
+    if (tgt->schedule < MK_SCHED_DEFAULT || tgt->schedule > MK_SCHED_TIMED)
+        return set_error(MK_ERR_INVALID, "schedule must be one of MK_SCHED_*");
+    p.schedule = tgt->schedule == MK_SCHED_BYTES ? MK_SCHED_BYTES : MK_SCHED_TIMED;
+    p.tc = true;
+    p.np = B <= 8 ? 8 : 16;
+    p.page_bytes = TC_STAGE_BYTES;
+    const int rows_group = (G + 2) * D;
+    // K splits: the largest power of two up to 8 that keeps the op's tasks
+    // within the workers (a split K range stays a whole number of stages)
+    auto ksplit = [&](int tiles, int K, int knob) {
+        if (knob > 0) return knob;
+        int k = 1;
+        while (k < 8 && (int64_t)tiles * k * 2 <= num_workers && (K / (k * 2)) % TC_KS == 0 && K % (k * 2) == 0) k *= 2;
+        return k;
+    };
+    const int ks_qkv = ksplit(Hkv * rows_group / TC_M, H, 0), ks_o = ksplit(H / TC_M, Hq * D, 0);
+    if (H % (ks_qkv * TC_KS) || (Hq * D) % (ks_o * TC_KS)) return set_error(MK_ERR_UNSUPPORTED, "bad K split");
+    // MLP-down K chunk: the largest of 2048 .. 256 dividing ffn that still
+    // gives at least half as many tasks as workers
+    int kc = tgt->kchunk_down;
+    if (kc <= 0) {
+        kc = 0;
+        for (int c : {2048, 1024, 512, 256})
+            if (F % c == 0) {
+                if (!kc) kc = c;
+                if ((int64_t)(H / TC_M) * (F / c) * 2 >= num_workers) { kc = c; break; }
+                kc = c;
+            }
+    }
+    if (kc <= 0 || F % kc || kc % TC_KS) return set_error(MK_ERR_UNSUPPORTED, "kchunk_down must divide ffn in 128s");
+    p.ksplit_qkv = ks_qkv;
+    p.ksplit_o = ks_o;
+    p.rows_qkv = p.rows_o = p.rows_down = p.rows_lm = TC_M;
+    p.rows_up = TC_SEG;
+    p.kchunk_down = kc;
+    int kn_T = tgt->attn_split > 0 ? tgt->attn_split : std::max(16, std::min(256, 16384 / (2 * D)));
+    if (tgt->attn_split <= 0) {
+        auto attn_tasks = [&](int T) {
+            int64_t n = 0;
+            for (int b = 0; b < B; ++b) n += ceil_div(s->seq_len0[b] + s->max_steps, T);
+            return n * Hkv;
+        };
+        while (2 * kn_T <= 256 && attn_tasks(kn_T) > (int64_t)num_workers) kn_T *= 2;
+    }
+    if (kn_T > 256 || kn_T < 1) return set_error(MK_ERR_UNSUPPORTED, "attn_split must be 1..256");
+    p.attn_split = kn_T;
+    // shared memory: activation ring | two attention slots | pages | op scratch | barriers | flags,
+    // the ring and the pages 1024-byte aligned (swizzled TMA boxes)
+    p.abuf_count = TC_XSLOTS;
+    p.abuf_bytes = tc_xstage_bytes(p.np);
+    const int attn_slot = (G * (D + 16) + 2 * D) * 4;
+    p.act_bytes = round_up(attn_slot, 512);
+    p.red_bytes = 128;
+    p.aux_bytes = round_up(attn_aux_bytes(G, kn_T, D), 128) + 2 * TC_SEG * TC_MAXB * 4 + NRED * p.red_bytes;
+    const int fixed = p.abuf_count * p.abuf_bytes + 2 * p.act_bytes + p.aux_bytes + MBAR_BYTES + CTRL_BYTES;
+    p.num_pages = std::min(8, (smem_per_cta - fixed) / p.page_bytes);
+    const int attn_need = 2 * attn_pages(kn_T, D, p.page_bytes);
+    if (p.num_pages < std::max(3, attn_need))
+        return set_error(MK_ERR_UNSUPPORTED, "shared memory too small for the page pool");
+    p.smem_bytes = fixed + p.num_pages * p.page_bytes;
+
+    std::vector<int> nsplit(B);
+    for (int b = 0; b < B; ++b) nsplit[b] = ceil_div(p.seq0[b] + s->max_steps, kn_T);
+    p.nsplit_max = *std::max_element(nsplit.begin(), nsplit.end());
+    std::vector<int> seq0 = p.seq0;
+    const int max_steps = s->max_steps;
+    std::vector<OpDef> ops;
+    std::vector<EdgeDef> edges;
+    std::vector<int> aux;
+    auto add_op = [&](int opcode, int layer, int gx, int gy, int gz, int a = 0) {
+        OpDef o;
+        o.opcode = opcode;
+        o.layer = layer;
+        o.grid[0] = gx; o.grid[1] = gy; o.grid[2] = gz;
+        ops.push_back(o);
+        aux.push_back(a);
+        return (int)ops.size() - 1;
+    };
+    const int64_t norm_cost = (int64_t)H * 2;
+    int emb = add_op(MK_OP_EMBED, -1, 1, 1, 1);
+    ops[emb].cost = [=](const int *) { return (int64_t)B * H * 2; };
+    int prev = emb;
+    const int none[3] = {-1, -1, -1};
+    auto whole = [&](int a, int b) { edges.push_back({a, b, {none[0], none[1], none[2]}, {-1, -1, -1}}); };
+    for (int l = 0; l < L; ++l) {
+        int na = add_op(MK_OP_NORM, l, B, 1, 1, 0);
+        ops[na].cost = [=](const int *) { return norm_cost; };
+        int q = add_op(MK_OP_QKV, l, Hkv, rows_group / TC_M, ks_qkv);
+        ops[q].cost = [=](const int *) { return (int64_t)TC_M * (H / ks_qkv) * 2; };
+        int a = add_op(MK_OP_ATTN, l, Hkv, B, p.nsplit_max);
+        ops[a].exists = [nsplit](const int *b) { return b[2] < nsplit[b[1]]; };
+        ops[a].cost = [=](const int *b) {
+            int last = seq0[b[1]] + max_steps - 1;
+            int rows = std::max(0, std::min(kn_T, last - b[2] * kn_T));
+            return (int64_t)2 * D * 2 * rows;
+        };
+        int o = add_op(MK_OP_O, l, H / TC_M, ks_o, 1);
+        ops[o].cost = [=](const int *) { return (int64_t)TC_M * (Hq * D / ks_o) * 2; };
+        int nm = add_op(MK_OP_NORM, l, B, 1, 1, 1);
+        ops[nm].cost = [=](const int *) { return norm_cost; };
+        int u = add_op(MK_OP_UP, l, F / TC_SEG, 1, 1);
+        ops[u].cost = [=](const int *) { return (int64_t)TC_M * H * 2; };
+        int d = add_op(MK_OP_DOWN, l, H / TC_M, F / kc, 1);
+        ops[d].cost = [=](const int *) { return (int64_t)TC_M * kc * 2; };
+        whole(prev, na);                                   // residual h read whole
+        whole(na, q);                                      // x^ read whole
+        edges.push_back({q, a, {1, 2, -1}, {1, 0, -1}});   // qkv [B, Hkv, rows]: group & row cuts (K split reduces)
+        edges.push_back({a, o, {1, 0, -1}, {-1, -1, -1}}); // attention output read whole; the split axis reduces
+        whole(o, nm);                                      // h after O read whole
+        whole(nm, u);                                      // x^ read whole
+        edges.push_back({u, d, {1, -1, -1}, {-1, 1, -1}}); // act [B, F]: tiles vs K chunks
+        prev = d;
+    }
+    int nf = add_op(MK_OP_NORM, -1, B, 1, 1, 2);
+    ops[nf].cost = [=](const int *) { return norm_cost; };
+    int lm = add_op(MK_OP_LM, -1, ceil_div(V, TC_M), 1, 1);
+    ops[lm].cost = [=](const int *b) { return (int64_t)std::min(TC_M, V - b[0] * TC_M) * H * 2; };
+    whole(prev, nf);
+    whole(nf, lm);
+
+    std::vector<RawTask> raw;
+    std::vector<RawEvent> evs;
+    int n_first;
+    int rc = build_tasks(ops, edges, raw, evs, n_first);
+    if (rc) return rc;
+    std::vector<int64_t> cost(raw.size());
+    for (size_t i = 0; i < raw.size(); ++i) cost[i] = ops[raw[i].op].cost(raw[i].bid);
+    std::vector<std::pair<int, int>> ranges{{0, n_first}};
+    for (auto &e : evs) ranges.push_back({e.first, e.last});
+    std::sort(ranges.begin(), ranges.end());
+    std::vector<int> order;
+    for (auto &r : ranges) {
+        std::vector<int> ids(r.second - r.first);
+        std::iota(ids.begin(), ids.end(), r.first);
+        std::stable_sort(ids.begin(), ids.end(), [&](int x, int y) { return cost[x] > cost[y]; });
+        order.insert(order.end(), ids.begin(), ids.end());
+    }
+    if ((int)order.size() != (int)raw.size()) return set_error(MK_ERR_INVALID, "task ranges do not cover the graph");
+    const int step_done = (int)evs.size();
+    for (auto &e : evs) p.thresholds.push_back(e.ntrig);
+    p.thresholds.push_back(0);
+    for (auto &e : evs) p.events.push_back({e.ntrig, e.first, e.last});
+    p.events.push_back({0, 0, n_first});
+    p.num_ops = (int)ops.size();
+    for (size_t o = 0; o < ops.size(); ++o) {
+        p.op_kind.push_back(ops[o].opcode);
+        p.op_layer.push_back(ops[o].layer);
+        p.op_aux.push_back(aux[o]);
+    }
+    // QKV rows of a head group: q heads, then k, then v (kv-group-major); a
+    // 64-row segment lies in one of them
+    auto qkv_row = [&](int g, int lr, int &mat) {
+        if (lr < G * D) { mat = 0; return g * G * D + lr; }
+        if (lr < (G + 1) * D) { mat = 1; return g * D + lr - G * D; }
+        mat = 2;
+        return g * D + lr - (G + 1) * D;
+    };
+    p.tasks.reserve(order.size());
+    for (int old : order) {
+        const RawTask &r = raw[old];
+        const OpDef &op = ops[r.op];
+        TaskRec t;
+        t.opcode = op.opcode;
+        t.op_row = r.op;
+        t.layer = op.layer;
+        std::memcpy(t.bid, r.bid, sizeof(t.bid));
+        t.cost = cost[old];
+        if (r.dep >= 0) {
+            t.w_ev[t.nw] = r.dep; t.w_thr[t.nw] = evs[r.dep].ntrig; t.w_off[t.nw++] = 0;
+        }
+        if (r.trig >= 0) { t.s_ev[t.ns] = r.trig; t.s_inc[t.ns++] = 1; }
+        if (op.opcode == MK_OP_LM) {
+            t.s_ev[t.ns] = step_done; t.s_inc[t.ns++] = 1;
+            p.thresholds[step_done]++;
+        }
+        int32_t *pl = t.payload;
+        auto tile = [&](int row0, int mat0, int row1, int mat1, int nrows, int k0, int kcn, int ktot, int out0) {
+            pl[P_ROW0 - W_P] = row0; pl[P_MAT - W_P] = mat0;
+            pl[P_S1_ROW0 - W_P] = row1; pl[P_S1_MAT - W_P] = mat1;
+            pl[P_NROWS - W_P] = nrows; pl[P_K0 - W_P] = k0; pl[P_KC - W_P] = kcn; pl[P_KTOT - W_P] = ktot;
+            pl[P_OUT0 - W_P] = out0; pl[P_NPG - W_P] = kcn / TC_KS; pl[P_RPP - W_P] = TC_M;
+        };
+        switch (op.opcode) {
+        case MK_OP_NORM: {
+            const int which = aux[r.op];
+            pl[P_NB - W_P] = r.bid[0];
+            pl[P_NZERO - W_P] = which == 0 && ks_qkv > 1 ? 1 : 0;
+            int snap = 0;
+            if (p.capture && which == 0 && op.layer > 0) snap = op.layer;  // residual after layer l - 1
+            if (p.capture && which == 2) snap = L;
+            pl[P_NSNAP - W_P] = snap;
+            break;
+        }
+        case MK_OP_QKV: {
+            const int g = r.bid[0], lr = r.bid[1] * TC_M, kq = H / ks_qkv;
+            int m0, m1;
+            const int r0 = qkv_row(g, lr, m0), r1 = qkv_row(g, lr + TC_SEG, m1);
+            tile(r0, m0, r1, m1, TC_M, r.bid[2] * kq, kq, H, g * rows_group + lr);
+            break;
+        }
+        case MK_OP_ATTN:
+            pl[P_G - W_P] = r.bid[0]; pl[P_B - W_P] = r.bid[1]; pl[P_SPLIT - W_P] = r.bid[2];
+            pl[P_T0 - W_P] = r.bid[2] * kn_T; pl[P_T - W_P] = kn_T; pl[P_NSPLIT - W_P] = nsplit[r.bid[1]];
+            pl[P_LAYER - W_P] = op.layer;
+            break;
+        case MK_OP_O: {
+            const int ko = Hq * D / ks_o;
+            tile(r.bid[0] * TC_M, 0, r.bid[0] * TC_M + TC_SEG, 0, TC_M, r.bid[1] * ko, ko, Hq * D, r.bid[0] * TC_M);
+            break;
+        }
+        case MK_OP_UP:
+            tile(r.bid[0] * TC_SEG, 0, r.bid[0] * TC_SEG, 1, TC_SEG, 0, H, H, r.bid[0] * TC_SEG);
+            break;
+        case MK_OP_DOWN:
+            tile(r.bid[0] * TC_M, 0, r.bid[0] * TC_M + TC_SEG, 0, TC_M, r.bid[1] * kc, kc, F, r.bid[0] * TC_M);
+            break;
+        case MK_OP_LM:
+            tile(r.bid[0] * TC_M, 0, r.bid[0] * TC_M + TC_SEG, 0, std::min(TC_M, V - r.bid[0] * TC_M), 0, H, H,
+                 r.bid[0] * TC_M);
+            break;
+        default:
+            break;
+        }
+        p.tasks.push_back(t);
+    }
+    for (auto &t : p.tasks)
+        if (t.opcode == MK_OP_EMBED) {
+            t.w_ev[t.nw] = step_done; t.w_thr[t.nw] = p.thresholds[step_done]; t.w_off[t.nw++] = -1;
+        }
+    // algorithmic bytes at step 0: weights once, KV read, KV append, norm vectors
+    int64_t weights = 0;
+    for (auto &t : p.tasks)
+        if (t.opcode >= MK_OP_QKV && t.opcode <= MK_OP_LM && t.opcode != MK_OP_ATTN) weights += t.cost;
+    weights += (int64_t)B * H * 2;
+    int64_t kv_read = 0;
+    for (int b = 0; b < B; ++b) kv_read += (int64_t)2 * p.seq0[b] * Hkv * D * 2 * L;
+    const int64_t kv_write = (int64_t)2 * B * Hkv * D * 2 * L;
+    const int64_t norms = (int64_t)(2 * L + 1) * H * 2 + (m->qk_norm ? (int64_t)2 * L * D * 2 : 0);
+    p.alg_bytes = weights + kv_read + kv_write + norms;
+    return finish_queues(p, false, p.schedule == MK_SCHED_TIMED);
+}
+
 // ---- Llama-style decode step --------------------------------------------
 
 int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_desc *tgt, int num_workers,
@@ -612,7 +868,7 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
         return set_error(MK_ERR_INVALID, "non-positive model or step size");
     if (Hq % Hkv) return set_error(MK_ERR_INVALID, "q_heads must be a multiple of kv_heads");
     const int G = Hq / Hkv;
-    if (B > 8) return set_error(MK_ERR_UNSUPPORTED, "batch above 8");
+    if (B > TC_MAXB) return set_error(MK_ERR_UNSUPPORTED, "batch above 16");
     if (D != 64 && D != 128) return set_error(MK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
     if (G > 8 || 8 % G) return set_error(MK_ERR_UNSUPPORTED, "q heads per kv head must be 1, 2, 4 or 8");
     if (H % 8 || F % 8) return set_error(MK_ERR_UNSUPPORTED, "hidden and ffn must be multiples of 8");
@@ -626,6 +882,17 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
         if ((int64_t)p.seq0[b] + s->max_steps > s->cache_slots)
             return set_error(MK_ERR_INVALID, "cache_slots smaller than seq_len0 + max_steps");
     }
+    // tensor-core tiles (128 weight rows x the batch): every K and row count a
+    // multiple of 128, each head group's q/k/v rows whole 64-row segments
+    const bool tc_shape = H % TC_M == 0 && (Hq * D) % TC_M == 0 && F % TC_M == 0 && ((G + 2) * D) % TC_M == 0 &&
+                          D % TC_SEG == 0 && H <= 8192;
+    if (tgt->tc_tiles > 0 && !tc_shape)
+        return set_error(MK_ERR_UNSUPPORTED, "tensor-core tiles need hidden, q_heads*head_dim, ffn and a head "
+                                             "group's q/k/v rows in multiples of 128 (hidden <= 8192)");
+    if (B > 8 && (tgt->tc_tiles < 0 || !tc_shape))
+        return set_error(MK_ERR_UNSUPPORTED, "batch above 8 needs tensor-core tiles");
+    if (tgt->tc_tiles > 0 || (tgt->tc_tiles == 0 && B >= 8 && tc_shape))
+        return plan_llama_tc(m, s, tgt, num_workers, smem_per_cta, p);
     auto clampi = [](int v, int lo, int hi) { return std::max(lo, std::min(hi, v)); };
     auto pow2_floor = [](int v) { int r = 1; while (r * 2 <= v) r *= 2; return r; };
     const int tile = 65536;
@@ -712,14 +979,22 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     for (int K : {H, Hq * D, kn_kc})
         if (2 * K > p.page_bytes) return set_error(MK_ERR_UNSUPPORTED, "a weight row does not fit one page");
     // Batch 1 with pages of exactly 16 rows (K = page_bytes / 32, a multiple of
-    // 256 up to 2048): the row-per-warp path takes tiles of 2 or 4 pages.  The
-    // large ops get them (LM head 64 rows, MLP-up 16 + 16, MLP-down 32) to
-    // spread each tile's fixed costs over more bytes; QKV and O keep one page.
+    // 256 up to 2048): the row-per-warp path takes tiles of any number of
+    // whole pages (MLP-up pages: 8 gate + 8 up rows), which spreads each
+    // instruction's fixed costs over more bytes.  Defaults: QKV 32 rows (two
+    // pages, a tile stays within one head), MLP-up 64 gate rows and MLP-down 64
+    // rows (8 and 4 pages; each op then has 128 tiles, a multiple of the
+    // down K chunks), the LM head one tile per worker; O keeps one page (its
+    // residual rows are staged with the activation).
     auto multi_page = [&](int K) { return B == 1 && K % 256 == 0 && K <= 2048 && p.page_bytes == 32 * K; };
-    if (multi_page(H) && tgt->rows_lm <= 0) kn_lm = 64;
-    if (multi_page(H) && tgt->rows_up <= 0 && F % 16 == 0) kn_up = 16;
-    if (multi_page(kn_kc) && tgt->rows_down <= 0) kn_dn = 32;
-    p.rows_up = kn_up; p.rows_down = kn_dn; p.rows_lm = kn_lm;
+    if (multi_page(H) && tgt->rows_lm <= 0) {
+        const int pages = ceil_div(V, 16);
+        kn_lm = 16 * std::min(64, ceil_div(pages, num_workers));
+    }
+    if (multi_page(H) && tgt->rows_up <= 0 && F % 64 == 0) kn_up = 64;
+    if (multi_page(kn_kc) && tgt->rows_down <= 0 && H % 64 == 0) kn_dn = 64;
+    if (multi_page(H) && tgt->rows_qkv <= 0 && D % 32 == 0) kn_qkv = 32;
+    p.rows_qkv = kn_qkv; p.rows_up = kn_up; p.rows_down = kn_dn; p.rows_lm = kn_lm;
     // the tensor-core tiles need whole rows in at most two pages of 8 or more
     bool mma_pages = mma;
     for (int K : {H, Hq * D, kn_kc})
@@ -734,13 +1009,15 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     }
     const int rmax = B > 4 && !mma_pages ? 8 : MAX_TILE_ROWS;
     auto rows_ok = [&](int rows, int K, bool up, bool o) {
-        if (rows <= rmax) return true;
-        return !o && multi_page(K) && (rows == 32 || rows == 64) && (!up || rows % 16 == 0);
+        if (rows <= rmax) return up ? rows / 2 <= 8 || (rows / 2) % 8 == 0 : true;
+        // whole 16-row pages on the batch-1 row-per-warp path, at most 64 of them
+        return !o && multi_page(K) && rows <= 16 * 64 && rows % 16 == 0;
     };
     if (!rows_ok(kn_qkv, H, false, false) || !rows_ok(kn_o, Hq * D, false, true) || !rows_ok(kn_dn, kn_kc, false, false) ||
         !rows_ok(kn_lm, H, false, false) || !rows_ok(2 * kn_up, H, true, false))
         return set_error(MK_ERR_UNSUPPORTED, "tile rows above 16 (8 for batch > 4; mlp-up: half of that), except "
-                                             "32 or 64 row tiles of 16-row pages at batch 1");
+                                             "tiles of up to 64 whole 16-row pages at batch 1 (not O; mlp-up gate "
+                                             "rows a multiple of 8)");
     if (F % kn_up) return set_error(MK_ERR_UNSUPPORTED, "rows_up must divide ffn");
     if (kn_T * D * 2 > p.page_bytes * 8) return set_error(MK_ERR_UNSUPPORTED, "attention split too long");
     p.num_pages = std::min(MAX_PAGES, (smem_per_cta - fixed) / p.page_bytes);
@@ -933,8 +1210,8 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
         const bool up = t.opcode == MK_OP_UP;
         bool ok = kc % 256 == 0 && kc <= 2048;
         if (ok && npg == 1) ok = up ? nrows == 8 : nrows <= 16;
-        else if (ok) ok = (npg == 2 || npg == 4) && t.opcode != MK_OP_O && p.page_bytes == 32 * kc &&
-                          (!up || nrows % 8 == 0);
+        else if (ok) ok = npg <= 64 && t.opcode != MK_OP_O && p.page_bytes == 32 * kc &&
+                          (up ? nrows == 8 * npg : nrows > 16 * (npg - 1) && nrows <= 16 * npg);
         p.lean = ok;
     }
     return finish_queues(p, false, p.schedule == MK_SCHED_TIMED);

@@ -44,6 +44,9 @@ struct Plan {
     int rows_qkv = 0, rows_o = 0, rows_up = 0, rows_down = 0, kchunk_down = 0, rows_lm = 0, attn_split = 0;
     int schedule = MK_SCHED_BYTES;  // MK_SCHED_BYTES or MK_SCHED_TIMED
     bool lean = false;  // batch 1, head_dim 64, every GEMV tile on the row-per-warp path: the lean kernel instance
+    bool tc = false;    // GEMV tiles on tcgen05 tensor cores (the tensor-core kernel instance)
+    int np = 0;         // tensor-core plans: batch padded to 8 or 16
+    int ksplit_qkv = 1, ksplit_o = 1;
     int page_bytes = 16384, act_bytes = 128, abuf_bytes = 128, abuf_count = 1, aux_bytes = 256, red_bytes = 128, num_pages = 2, smem_bytes = 0,
         nsplit_max = 1;
     std::vector<TaskRec> tasks;
@@ -51,6 +54,7 @@ struct Plan {
     std::vector<EventRec> events;
     int num_ops = 0;
     std::vector<int> op_kind, op_layer;
+    std::vector<int> op_aux;  // NORM ops: 0 attention norm, 1 MLP norm, 2 final norm
     std::vector<Segment> segments;
     std::vector<int32_t> words;      // all segments' instruction words
     std::vector<int32_t> slot_task;  // task id per slot, -1 = NoOp
@@ -61,6 +65,7 @@ struct Plan {
     // workspace layout (byte offsets) and upload state
     struct {
         uint64_t err, counters, arrive, queue, optab, seq0, rope, hres, hmid, qkv, part, attn_out, act, trace, total;
+        uint64_t xn, xo, act16, tmaps;  // tensor-core plans: bf16 high/low activations, tensor maps
     } ws{};
     void *uploaded_ws = nullptr;
     bool table_dirty = true;

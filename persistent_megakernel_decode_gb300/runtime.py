@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmk.so")
 MK_OK, MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_DEADLOCK, MK_ERR_CUDA = 0, 1, 2, 3, 4
 MK_ERR_RESIDENCY, MK_ERR_TIMEOUT, MK_ERR_DEVICE_CHECK, MK_ERR_UNBOUND = 5, 6, 7, 8
 OP_NAMES = {0: "noop", 1: "counter", 2: "embed", 3: "qkv", 4: "attn", 5: "o", 6: "up", 7: "down", 8: "lm",
-            9: "glm_a0", 10: "glm_gemm", 11: "glm_fin"}
+            9: "glm_a0", 10: "glm_gemm", 11: "glm_fin", 12: "norm"}
 OPCODE = {v: k for k, v in OP_NAMES.items()}
 MODE_MEGAKERNEL, MODE_PER_OP = 0, 1
 SCHED_DEFAULT, SCHED_BYTES, SCHED_TIMED = 0, 1, 2
@@ -64,7 +64,7 @@ class TargetDesc(C.Structure):
     _fields_ = [("num_sms", C.c_int), ("smem_per_cta", C.c_int), ("mode", C.c_int), ("rows_qkv", C.c_int),
                 ("rows_o", C.c_int), ("rows_up", C.c_int), ("rows_down", C.c_int), ("kchunk_down", C.c_int),
                 ("rows_lm", C.c_int), ("attn_split", C.c_int), ("page_bytes", C.c_int),
-                ("schedule", C.c_int)]
+                ("schedule", C.c_int), ("tc_tiles", C.c_int)]
 
 
 class GlmDesc(C.Structure):
@@ -78,7 +78,8 @@ class PlanInfo(C.Structure):
         "num_workers", "lmax", "num_tasks", "num_events", "num_ops", "num_launches", "num_pages", "page_bytes",
         "smem_bytes", "act_bytes", "rows_qkv", "rows_o", "rows_up", "rows_down", "kchunk_down", "rows_lm",
         "attn_split", "total_slots")] + [("workspace_bytes", C.c_uint64), ("scratch_offset", C.c_uint64),
-                                          ("algorithmic_bytes_step", C.c_uint64)]
+                                          ("algorithmic_bytes_step", C.c_uint64)] + [
+        (n, C.c_int) for n in ("tc_tiles", "ksplit_qkv", "ksplit_o")]
 
 
 class GraphOp(C.Structure):

@@ -67,6 +67,11 @@ TINY = ModelShape(L=2, H=256, Hq=4, Hkv=2, D=64, F=688, V=1024, eps=1e-5, theta=
 LLAMA_1B = ModelShape(L=16, H=2048, Hq=32, Hkv=8, D=64, F=8192, V=128256, eps=1e-5, theta=5e5)
 QWEN3_8B = ModelShape(L=36, H=4096, Hq=32, Hkv=8, D=128, F=12288, V=151936, eps=1e-6, theta=1e6,
                       qk_norm=True, tied=False)
+# Small shapes for the tensor-core tiles' checks (every K and row count a
+# multiple of 128): the tiny decoder with an ffn of 512, and a two-layer
+# Qwen3-style decoder (head_dim 128, q/k norm, untied head).
+TINY_TC = ModelShape(L=2, H=256, Hq=4, Hkv=2, D=64, F=512, V=1024, eps=1e-5, theta=1e4)
+SMALL_QK = ModelShape(L=2, H=512, Hq=4, Hkv=2, D=128, F=512, V=2048, eps=1e-6, theta=1e6, qk_norm=True, tied=False)
 
 WORKLOADS: Dict[str, Workload] = {
     "tiny": Workload("tiny", 0, TINY, 1, 64, 8),

@@ -4,9 +4,12 @@ oracle (on the host cores) at the model shapes of the workloads.
 * Llama-3.2-1B shape, batch 1, 1024 cached tokens: the benchmarked plan
   (every SM a worker, default tiles: 64 KB pages, the row-per-warp GEMV,
   9 attention splits);
-* the same model at batch 8 with sequence lengths drawn from 512..4096 (the
-  batch-8 kernel: 16-row tensor-core GEMV tiles in 32 KB pages, 256-position
-  attention splits);
+* the same model at batch 8 with sequence lengths drawn from 512..4096, on
+  the tcgen05 tiles (128 weight rows x 8 sequences, TMEM accumulators; the
+  default at batch 8) and on the warp-level MMA tiles (16-row m16n8k16 tiles in
+  32 KB pages), both with 256-position attention splits;
+* Qwen3-8B shape at batch 16, 2048 cached tokens (tcgen05 tiles, K-split QKV
+  and O tiles, 2048-column MLP-down chunks);
 * two layers of the same model at batches 2, 3 and 4 (the tensor-core tiles
   of the batch-2 and batch-4 kernels, a partly filled MMA N side), and at
   batch 8 over 32 teacher-forced steps (256 argmax samples);
@@ -52,6 +55,20 @@ def test_llama1b_batch8_variable_lengths():
     from harness import run_parity
     w = synth.WORKLOADS["llama1b_b8"]
     run = run_parity(w.shape, synth.seq_lengths(w), 2, [1], seed=w.weight_seed)
+    _check(run)
+
+
+def test_llama1b_batch8_warp_mma_tiles():
+    from harness import run_parity
+    w = synth.WORKLOADS["llama1b_b8"]
+    run = run_parity(w.shape, synth.seq_lengths(w), 1, [0], seed=w.weight_seed, tc_tiles=-1)
+    _check(run)
+
+
+def test_qwen3_8b_batch16():
+    from harness import run_parity
+    w = synth.WORKLOADS["qwen3_8b_b16"]
+    run = run_parity(w.shape, synth.seq_lengths(w), 1, [0], seed=w.weight_seed)
     _check(run)
 
 

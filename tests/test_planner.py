@@ -105,6 +105,62 @@ def _compare(shape, B, seq0, steps, workers=152, **kn):
     return p, op
 
 
+def _compare_tc(shape, B, seq0, steps, workers=152):
+    """Tensor-core plans against the oracle's statement, which derives its own
+    tile knobs (K splits, MLP-down K chunk, attention split) from the rules."""
+    p = rt.Plan.llama(shape, B, seq0, steps, max(seq0) + steps + 3, num_sms=workers, smem_per_cta=232448,
+                      schedule=rt.SCHED_BYTES)
+    info = p.info()
+    assert info["tc_tiles"] == 1
+    q, ids, th, tasks = p.export()
+    osh = plans.LlamaShape(shape.L, shape.H, shape.Hq, shape.Hkv, shape.D, shape.F, shape.V)
+    kn = plans.tc_knobs(osh, B, seq0, steps, workers)
+    assert (info["ksplit_qkv"], info["ksplit_o"], info["kchunk_down"], info["attn_split"]) == \
+        (kn.ksplit_qkv, kn.ksplit_o, kn.kchunk_down, kn.attn_split)
+    op = plans.llama_step_plan(osh, kn, B, seq0, steps, workers)
+    assert info["num_tasks"] == len(op.tasks)
+    assert list(th) == op.thresholds
+    for i, t in enumerate(op.tasks):
+        r = tasks[i]
+        assert rt.OP_NAMES[r[0]] == t.kind, i
+        assert (r[1], r[2], r[3], r[4], r[5]) == (t.layer, *t.bid, t.cost), i
+        assert [(r[7 + 3 * k], r[8 + 3 * k], r[9 + 3 * k]) for k in range(r[6])] == list(t.waits), i
+        assert [(r[17 + 2 * k], r[18 + 2 * k]) for k in range(r[16])] == list(t.signals), i
+    assert info["lmax"] == op.lmax
+    assert ids.tolist() == op.queues
+    return p, op
+
+
+def test_tc_planner_matches_oracle_small_shapes():
+    _compare_tc(synth.TINY_TC, 16, [64 + 3 * b for b in range(16)], 4)
+    _compare_tc(synth.SMALL_QK, 11, [40 + 17 * b for b in range(11)], 3, workers=37)
+
+
+def test_tc_planner_matches_oracle_qwen3_8b_b16():
+    w = synth.WORKLOADS["qwen3_8b_b16"]
+    p, op = _compare_tc(synth.QWEN3_8B, 16, synth.seq_lengths(w), w.steps)
+    info = p.info()
+    assert (info["ksplit_qkv"], info["ksplit_o"], info["kchunk_down"]) == (2, 4, 2048)
+
+
+def test_tc_planner_matches_oracle_llama1b_b8():
+    w = synth.WORKLOADS["llama1b_b8"]
+    p, op = _compare_tc(synth.LLAMA_1B, 8, synth.seq_lengths(w), w.steps)
+    assert p.info()["kchunk_down"] == 1024
+
+
+def test_tc_plan_needs_shapes_in_128s():
+    # batch above 8 needs the tensor-core tiles; the tiny decoder's ffn of 688 does not allow them
+    with pytest.raises(rt.MkError) as e:
+        rt.Plan.llama(synth.TINY, 12, [10] * 12, 2, 20, **GB300)
+    assert e.value.code == rt.MK_ERR_UNSUPPORTED
+    with pytest.raises(rt.MkError):
+        rt.Plan.llama(synth.TINY, 4, [10] * 4, 2, 20, tc_tiles=1, **GB300)
+    # and batch 8 can still opt out of them
+    p = rt.Plan.llama(synth.LLAMA_1B, 8, [100] * 8, 2, 120, tc_tiles=-1, **GB300)
+    assert p.info()["tc_tiles"] == 0
+
+
 def test_planner_matches_oracle_tiny():
     _compare(synth.TINY, 1, [64], 8)
 
@@ -119,8 +175,9 @@ def test_planner_matches_oracle_llama1b_b1():
 
 
 def test_planner_matches_oracle_llama1b_b8_variable_lengths():
+    # the warp-level tensor-core tiles (batch 8 takes tcgen05 tiles by default)
     w = synth.WORKLOADS["llama1b_b8"]
-    _compare(synth.LLAMA_1B, 8, synth.seq_lengths(w), 64)
+    _compare(synth.LLAMA_1B, 8, synth.seq_lengths(w), 64, tc_tiles=-1)
 
 
 def test_planner_matches_oracle_qwen3_8b_b1():
