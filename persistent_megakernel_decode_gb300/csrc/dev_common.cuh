@@ -310,9 +310,11 @@ DEV bool warp_wait_smem(const KParams &P, const Smem S, volatile int *flag, uint
     return wait_smem_slow(P.err, P.timeout_ns, S, flag, target, slot, opc);
 }
 
-// Event counter >= target.  Polls are relaxed loads (an acquire load per
-// poll would also drop the SM's L1 each time); once the target is seen, one
-// acquire load of the counter synchronises with the publisher's release.
+// Event counter >= target.  Polls are relaxed loads: an acquire load also
+// invalidates the SM's L1, which costs the other roles their cached queue
+// words (measured: a batch-1 step whose waits were all met went from 0.53 to
+// 0.85 ms with acquire polls).  Once the target is seen, one acquire load of
+// the counter synchronises with the publisher's release.
 static __device__ __noinline__ bool wait_counter_slow(uint32_t *err, uint64_t timeout_ns, Smem S, const uint32_t *c,
                                                int ev, uint32_t target, int slot, int opc) {
     const int lane = threadIdx.x & 31;
@@ -529,6 +531,7 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
     if (opc == MK_OP_ATTN) {
         const int T = F(I, P_T);
         if (T <= 0 || T > 256 || F(I, P_B) >= P.B || F(I, P_G) >= P.Hkv || F(I, P_SPLIT) >= P.nsplit_max) return false;
+        if (attn_pages(T, P.D, P.page_bytes) > 4) return false;  // a split spans at most 4 pages of K (and of V)
     }
     return true;
 }

@@ -1046,25 +1046,37 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
     const int npg = attn_pages(T, D, P.page_bytes);  // K pages, then as many V pages
     const uint32_t kring = ring, vring = ring + npg;
     ring = vring + npg;
-    // the split's K (V) rows are consecutive rows of its K (V) page(s); the
-    // planner keeps a split within one page when it fits, else rows are
-    // looked up page by page
-    const uint8_t *kpage = S.pages() + (size_t)(kring % P.num_pages) * P.page_bytes;
-    const uint8_t *vpage = S.pages() + (size_t)(vring % P.num_pages) * P.page_bytes;
-    auto row_at = [&](uint32_t base, const uint8_t *first, int tk) -> const uint8_t * {
-        if (npg == 1) return first + (size_t)tk * (D * 2);
-        return S.pages() + (size_t)((base + tk / rpp) % P.num_pages) * P.page_bytes + (size_t)(tk % rpp) * (D * 2);
+    // the split's K (V) rows are consecutive rows of its K (V) page(s), rpp
+    // (a power of two) to a page; a split spans at most 4 pages of each
+    auto page_ptr = [&](uint32_t r) { return S.pages() + (size_t)(r % P.num_pages) * P.page_bytes; };
+    const uint8_t *kpage = page_ptr(kring), *vpage = page_ptr(vring);
+    const uint8_t *kp1 = page_ptr(kring + 1), *kp2 = page_ptr(kring + 2), *kp3 = page_ptr(kring + 3);
+    const uint8_t *vp1 = page_ptr(vring + 1), *vp2 = page_ptr(vring + 2), *vp3 = page_ptr(vring + 3);
+    const int rsh = 31 - __clz(rpp);
+    auto row_at = [&](bool v, int tk) -> const uint8_t * {
+        const int j = tk >> rsh;
+        const uint8_t *pg = j == 0 ? (v ? vpage : kpage) : j == 1 ? (v ? vp1 : kp1) : j == 2 ? (v ? vp2 : kp2)
+                                                                                        : (v ? vp3 : kp3);
+        return pg + (size_t)(tk & (rpp - 1)) * (D * 2);
     };
     for (int k = 0; k < npg; ++k)
         if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(kring + k) % P.num_pages], ((kring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
     trace_stamp(P, i, 6);
-    // scores: 8 tokens per round, 4 lanes per token, DQ dims per lane
+    // scores: 8 tokens per round, 4 lanes per token, DQ dims per lane in NC
+    // chunks of 8.  Rows are a multiple of 128 bytes apart, so every row
+    // starts on bank 0: each lane walks its chunks in a rotated order (by its
+    // quarter when D = 128, and by the token's parity) so that the 8 lanes of
+    // a quarter-warp phase read 8 different 16-byte bank groups.
+    constexpr int NC = DQ / 8;
     const int qtr = lane & 3;
+    const int rot = ((NC == 4 ? qtr : 0) + ((lane >> 2) & 1)) % NC;
     float q[DQ];
 #pragma unroll
-    for (int d = 0; d < DQ; d += 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(qp + (hh * 4 + qtr) * QS + d);
-        q[d] = v.x; q[d + 1] = v.y; q[d + 2] = v.z; q[d + 3] = v.w;
+    for (int c = 0; c < NC; ++c) {
+        const float *qs = qp + (hh * 4 + qtr) * QS + ((c + rot) % NC) * 8;
+        const float4 v0 = *reinterpret_cast<const float4 *>(qs), v1 = *reinterpret_cast<const float4 *>(qs + 4);
+        q[c * 8] = v0.x; q[c * 8 + 1] = v0.y; q[c * 8 + 2] = v0.z; q[c * 8 + 3] = v0.w;
+        q[c * 8 + 4] = v1.x; q[c * 8 + 5] = v1.y; q[c * 8 + 6] = v1.z; q[c * 8 + 7] = v1.w;
     }
     const int tc = min(te, ncache);  // cached tokens of this warp: [tb, tc); the new token, if ours, is ncache
     float m = -INFINITY;
@@ -1072,10 +1084,10 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
         const int tk = t + (lane >> 2);
         float s0 = 0.f, s1 = 0.f;
         if (tk < tc) {
-            const uint8_t *row = row_at(kring, kpage, tk) + qtr * DQ * 2;
+            const uint8_t *row = row_at(false, tk) + qtr * DQ * 2;
             uint4 kw[DQ / 8];
 #pragma unroll
-            for (int d = 0; d < DQ / 8; ++d) kw[d] = *reinterpret_cast<const uint4 *>(row + d * 16);
+            for (int d = 0; d < DQ / 8; ++d) kw[d] = *reinterpret_cast<const uint4 *>(row + ((d + rot) % NC) * 16);
 #pragma unroll
             for (int d = 0; d < DQ / 8; ++d) {
                 float k8[8];
@@ -1088,7 +1100,7 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
             }
         } else if (tk < te) {
 #pragma unroll
-            for (int d = 0; d < DQ; ++d) s0 = fmaf(q[d], kn[qtr * DQ + d], s0);
+            for (int d = 0; d < DQ; ++d) s0 = fmaf(q[d], kn[qtr * DQ + (((d >> 3) + rot) % NC) * 8 + (d & 7)], s0);
         }
         float s = s0 + s1;
         s += __shfl_xor_sync(FULL, s, 1);
@@ -1141,8 +1153,13 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
 #pragma unroll
             for (int u = 0; u < 4; ++u) pv(acc[u], sw[t + u - tb], vl + (size_t)(t + u) * (D * 2));
         }
+    } else {
+        for (; t + 4 <= tc; t += 4) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) pv(acc[u], sw[t + u - tb], row_at(true, t + u) + lane * PER * 2);
+        }
     }
-    for (; t < tc; ++t) pv(acc[0], sw[t - tb], row_at(vring, vpage, t) + lane * PER * 2);
+    for (; t < tc; ++t) pv(acc[0], sw[t - tb], row_at(true, t) + lane * PER * 2);
     if (has_new && ncache >= tb && ncache < te) {  // the new token is this warp's
         const float p = sw[ncache - tb];
 #pragma unroll
