@@ -199,6 +199,33 @@ def side_measurements(args, w, dev, stream, weights, kc, vc, seq0, max_steps, fi
             del sess
         except Exception as e:  # a leg that cannot run is reported, not fatal
             out[name] = {"unavailable": str(e)[:200]}
+    # several steps in one cooperative launch (MK_RUN_ONE_LAUNCH): ms per step
+    # for 1, 4 and 16 steps per launch, beside the empty-launch probe below
+    try:
+        need = 3 + 1 + 4 + 16
+        if max_steps < need:
+            raise RuntimeError(f"needs a session of {need} steps")
+        sess = rt.Session(w.shape, weights, kc, vc, seq0, max_steps, stream=stream)
+        sess.tokens[0] = torch.tensor([1] * w.batch, dtype=torch.int32, device=dev)
+        with torch.cuda.stream(stream):
+            for st in range(3):
+                sess.run(st, 1)
+        sess.sync()
+        first, per = 3, {}
+        for k in (1, 4, 16):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                sess.run(first, k, one_launch=True)
+                e1.record(stream)
+            stream.synchronize()
+            per[str(k)] = e0.elapsed_time(e1) / k
+            first += k
+        out["megakernel_one_launch"] = {"ms_per_step_by_steps_per_launch": per,
+                                        "device_error": int(sess.sync().code)}
+        del sess
+    except Exception as e:
+        out["megakernel_one_launch"] = {"unavailable": str(e)[:200]}
     info = rt.Plan.llama(w.shape, w.batch, seq0, 1, kc.shape[3]).info()
     for coop in (True, False):
         n = 200

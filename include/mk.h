@@ -69,6 +69,10 @@ extern "C" {
 /* ---- mk_run flags ---- */
 #define MK_RUN_HOST_TOKENS 1u  /* every step reads tokens[s] (teacher forcing) */
 #define MK_RUN_TRACE       2u  /* record per-instruction globaltimer stamps */
+#define MK_RUN_ONE_LAUNCH  4u  /* run all num_steps steps in one cooperative launch: every worker walks its
+                                  queue once per step, the monotone event epochs order the steps (no launch,
+                                  ramp-up or drain between steps); megakernel plans only.  With TRACE, the
+                                  stamps of a slot are those of its last step */
 
 typedef struct mk_plan_s *mk_plan_t;
 
@@ -330,7 +334,10 @@ int mk_plan_export(mk_plan_t plan, int32_t *queue, int32_t *task_ids, int32_t *t
  * binding or layer.  The library never frees a bound buffer. */
 int mk_bind(mk_plan_t plan, int binding, int layer, uint64_t device_ptr);
 
-/* Run steps first_step .. first_step+num_steps-1 asynchronously on `stream`:
+/* Run steps first_step .. first_step+num_steps-1 asynchronously on `stream`
+ * (with MK_RUN_ONE_LAUNCH in one launch: "MegaRTP megakernel article",
+ * sections 4-5, and "CMU 15-779 Lecture 7 notes", section 3.1, count the
+ * fixed cost a launch adds to every step):
  * a fixed grid of persistent worker CTAs, one per SM, each looping over its
  * own queue row ("MegaRTP megakernel article", section 4, Device).  Before
  * the launch the whole grid is checked for co-residency with its real block
@@ -349,6 +356,7 @@ int mk_bind(mk_plan_t plan, int binding, int layer, uint64_t device_ptr);
  * a launch failure.  timeout_ns bounds every device wait (0 = 200 ms). */
 int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_step, int num_steps,
            uint32_t flags, uint64_t timeout_ns, void *stream);
+/* (MK_RUN_ONE_LAUNCH: MK_ERR_INVALID for per-op plans.) */
 
 /* Synchronise `stream`, read the device error record into *rec (may be
  * NULL) and return its code (MK_OK, MK_ERR_TIMEOUT, MK_ERR_DEVICE_CHECK) or

@@ -372,6 +372,7 @@ DEV bool cta_aborting(const Smem S) { return __shfl_sync(FULL, (int)S.ctrl()[0],
 // operand row of slot i + 1 are in flight, so no role waits on a round trip to
 // L2 when it moves to its next instruction.
 struct WIns {
+    int step = 0;           // decode step of the current slot (a launch may run several)
     int w = 0;              // words of the current slot
     uint64_t orow = 0;      // operand row of the current slot
     int row = -1;
@@ -390,7 +391,7 @@ DEV uint64_t PTR(const WIns &I, int k) {
 // The fields the consumers need of a slot, read with independent shuffles
 // issued back to back (one round of shuffle latency instead of a chain).
 struct Dec {
-    int opc, row, cnt, task, k0, kc, nrows, out0, snap, npg;
+    int opc, row, cnt, task, k0, kc, nrows, out0, snap, npg, step;
     uint64_t out, out2;  // GEMV outputs
 };
 DEV Dec decode(const WIns &I) {
@@ -405,14 +406,17 @@ DEV Dec decode(const WIns &I) {
     d.out0 = F(I, P_OUT0);
     d.snap = F(I, P_SNAP);
     d.npg = F(I, P_NPG);
+    d.step = I.step;
     d.out = PTR(I, S_G_OUT);
     d.out2 = PTR(I, S_G_OUT2);
     return d;
 }
 
 // Lane k's word of queue slot i (all zero, i.e. a NoOp, past the queue's end).
-DEV int queue_word(const KParams &P, const int32_t *q, int i) {
-    return i < P.lmax ? __ldg(q + (size_t)i * W_WORDS + (threadIdx.x & 31)) : 0;
+// Slots are numbered through the launch: slot v is queue slot v % lmax of
+// step v / lmax.
+DEV int queue_word(const KParams &P, const int32_t *q, int v) {
+    return v < P.lmax * P.nsteps ? __ldg(q + (size_t)(v % P.lmax) * W_WORDS + (threadIdx.x & 31)) : 0;
 }
 
 // Starts loading the operand row of the instruction held in `w` unless `row`
@@ -560,7 +564,7 @@ struct Seg {
 
 DEV int attn_pos(const KParams &P, const WIns &I) {
     const int32_t *seq0 = reinterpret_cast<const int32_t *>(PTR(I, S_AT_SEQ0));
-    return __ldg(seq0 + F(I, P_B)) + P.step;
+    return __ldg(seq0 + F(I, P_B)) + I.step;
 }
 DEV int attn_cached_rows(const WIns &I, int pos) { return max(0, min(F(I, P_T), pos - F(I, P_T0))); }
 

@@ -529,7 +529,7 @@ DEV bool gemv_tile(const KParams &P, const Smem S, const WIns &I, int i, int sl,
             const unsigned long long key = argmax_key(bv, out0 + bi);
             if (key > lm_best) {  // lane b keeps sequence b's best key of this step
                 lm_best = key;
-                red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)P.step * B + lane, key);
+                red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)I.step * B + lane, key);
             }
         }
     }
@@ -713,7 +713,7 @@ DEV bool gemv_mma_tile(const KParams &P, const Smem S, const WIns &I, int i, int
             const unsigned long long key = argmax_key(bv, out0 + bi);
             if (key > lm_best) {
                 lm_best = key;
-                red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)P.step * B + lane, key);
+                red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)I.step * B + lane, key);
             }
         }
     }
@@ -830,7 +830,7 @@ DEV bool rpw_finish(const KParams &P, const Dec &d, const uint64_t (&acc)[V], co
         for (int o = 16; o; o >>= 1) key = max(key, __shfl_xor_sync(FULL, key, o));
         if (lane == 0 && key > lm_best && !ab) {
             lm_best = key;
-            red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)P.step, key);
+            red_max_u64(reinterpret_cast<unsigned long long *>(ptr_b) + (size_t)d.step, key);
         }
     }
     return true;
@@ -919,7 +919,7 @@ DEV bool gemv_rpw(const KParams &P, const Smem S, const Dec &d, int i, bool hand
         for (int o = 16; o; o >>= 1) key = max(key, __shfl_xor_sync(FULL, key, o));
         if (lane == 0 && key > lm_best && !ab) {
             lm_best = key;
-            red_max_u64(reinterpret_cast<unsigned long long *>(d.out2) + (size_t)P.step, key);
+            red_max_u64(reinterpret_cast<unsigned long long *>(d.out2) + (size_t)d.step, key);
         }
     }
     trace_stamp(P, i, 9);
@@ -1190,7 +1190,7 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
     int last = 0;
     if (lane == 0 && !ab) {
         const uint32_t old = atom_acqrel_add(arrive + ((size_t)layer * P.B + b) * P.Hq + head, 1u);
-        last = old == (uint32_t)(P.step + 1) * (uint32_t)(nsplit * parts) - 1u;
+        last = old == (uint32_t)(I.step + 1) * (uint32_t)(nsplit * parts) - 1u;
     }
     trace_stamp(P, i, 10);
     if (!__shfl_sync(FULL, last, 0)) return;
@@ -1265,13 +1265,14 @@ DEV void embed_task(const KParams &P, const Smem S, const WIns &I, int i, int sl
     float *h = reinterpret_cast<float *>(PTR(I, S_EMB_H));
     int32_t *tokens = reinterpret_cast<int32_t *>(PTR(I, S_EMB_TOK));
     const unsigned long long *keys = reinterpret_cast<const unsigned long long *>(PTR(I, S_EMB_KEYS));
-    const bool host_tokens = (P.flags & MK_RUN_HOST_TOKENS) || P.step == 0;
+    const int step = I.step;
+    const bool host_tokens = (P.flags & MK_RUN_HOST_TOKENS) || step == 0;
     for (int b = 0; b < P.B; ++b) {
         int tok;
-        if (host_tokens) tok = __ldcg(tokens + (size_t)P.step * P.B + b);
-        else tok = (int)(0xFFFFFFFFu - (uint32_t)(__ldcg(keys + (size_t)(P.step - 1) * P.B + b) & 0xFFFFFFFFull));
+        if (host_tokens) tok = __ldcg(tokens + (size_t)step * P.B + b);
+        else tok = (int)(0xFFFFFFFFu - (uint32_t)(__ldcg(keys + (size_t)(step - 1) * P.B + b) & 0xFFFFFFFFull));
         if (tok < 0 || tok >= P.V) tok = 0;  // out-of-range ids read row 0 instead of faulting
-        if (!host_tokens && ct == 0) tokens[(size_t)P.step * P.B + b] = tok;
+        if (!host_tokens && ct == 0) tokens[(size_t)step * P.B + b] = tok;
         for (int k = ct; k < P.H; k += CONSUMERS) h[(size_t)b * P.H + k] = bf16_at(E, (size_t)tok * P.H + k);
     }
 }

@@ -239,7 +239,7 @@ DEV bool tc_epilogue(const KParams &P, const Smem S, const WIns &I, const Dec &d
         }
         if (lane < B && !ab && mine > lm_best) {
             lm_best = mine;
-            red_max_u64(reinterpret_cast<unsigned long long *>(d.out2) + (size_t)P.step * B + lane, mine);
+            red_max_u64(reinterpret_cast<unsigned long long *>(d.out2) + (size_t)d.step * B + lane, mine);
         }
     }
     return true;

@@ -42,10 +42,12 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int NP = P.num_pages, PS = P.page_bytes;
     WIns I;
     fetch_init(I, P, myq);
-    for (int i = 0; i < P.lmax; ++i) {
+    for (int v = 0; v < P.lmax * P.nsteps; ++v) {
+        const int i = v % P.lmax;
+        if (i == 0) I.step = P.step + v / P.lmax;  // the step of slot v
         if (cta_aborting(S)) break;
         if (lane < 4 && i + 4 + lane < P.lmax) prefetch_l2(myq + (size_t)(i + 4 + lane) * W_WORDS);
-        fetch(I, P, myq, i);
+        fetch(I, P, myq, v);
         const int opc = F(I, W_OPC);
         if (!ins_valid<FL>(P, I)) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
@@ -72,6 +74,18 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
                 if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 5] = gtimer();
                 if (stop) break;
                 continue;
+            }
+        }
+        if (opc == MK_OP_ATTN && I.step > P.step) {
+            // K/V rows appended by an earlier step of this launch: their writer
+            // published them with the layer's attention event of that step --
+            // acquire it (long since met) before the bulk copies read the rows
+            const int pos0 = attn_pos(P, I) - (I.step - P.step);  // first position appended in this launch
+            if (F(I, P_T0) + attn_cached_rows(I, attn_pos(P, I)) > pos0) {
+                const int ev = F(I, W_SIG);
+                const uint32_t target = (uint32_t)F(I, P_ATHR) * (uint32_t)I.step;
+                if (!warp_wait_counter(P, S, ev, target, i, opc)) break;
+                fence_proxy_async_global();
             }
         }
         Seg s0, s1;
@@ -186,7 +200,7 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
             const uint32_t ew = (uint32_t)F(I, W_WAIT + 2 * w);
             const uint32_t thr = (uint32_t)F(I, W_WAIT + 2 * w + 1);
             const int ev = (int)(ew & ~WAIT_PREV_EPOCH);
-            const int epoch = P.step + 1 - ((ew & WAIT_PREV_EPOCH) ? 1 : 0);
+            const int epoch = I.step + 1 - ((ew & WAIT_PREV_EPOCH) ? 1 : 0);
             const uint32_t target = thr * (uint32_t)epoch;
             // counters only grow within a launch: a target already met needs no new round trip
             if (target > 0 && !(ev == seen_ev && target <= seen_target)) {
@@ -197,8 +211,14 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
         }
         if (!ab && lane == 0 && P.trace) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 2] = gtimer();
     };
-    for (int i = 0; i < P.lmax; ++i) {
-        fetch(I, P, myq, i);
+    for (int v = 0; v < P.lmax * P.nsteps; ++v) {
+        const int i = v % P.lmax;
+        if (i == 0) {  // a new step: nothing staged so far holds this step's activations
+            I.step = P.step + v / P.lmax;
+            key0 = key1 = -1;
+            chain.valid = false;
+        }
+        fetch(I, P, myq, v);
         const int opc = F(I, W_OPC);
         if (opc == MK_OP_NOOP) continue;
         if constexpr (FL == FL_TC) {
@@ -295,10 +315,17 @@ DEV int progress_min(const Smem S) {
 
 DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int lane = threadIdx.x & 31;
-    int next = 0;                                              // first slot not yet published
+    const int total = P.lmax * P.nsteps;
+    int next = 0;                                              // first slot not yet published (launch-wide)
     int wc = queue_word(P, myq, 0), wn = queue_word(P, myq, 1);  // words of slots next, next + 1
-    while (next < P.lmax) {
-        if (__shfl_sync(FULL, wc, W_OPC) == MK_OP_NOOP) break;  // NoOps only pad the tail
+    while (next < total) {
+        if (__shfl_sync(FULL, wc, W_OPC) == MK_OP_NOOP) {
+            // NoOps only pad the tail of a step's queue: go on at the next step's first slot
+            next = (next / P.lmax + 1) * P.lmax;
+            wc = queue_word(P, myq, next);
+            wn = queue_word(P, myq, next + 1);
+            continue;
+        }
         int done = next, ab = 0, stop = 0;
         uint64_t seen_at = 0;
         if (lane == 0) {
@@ -334,9 +361,10 @@ DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
             if (lane == 0 && !ab) {
                 if (ns > 0) red_release_add(P.counters + e0, (uint32_t)i0);
                 if (ns > 1) red_release_add(P.counters + e1, (uint32_t)i1);
-                if (P.trace) {
-                    P.trace[((size_t)blockIdx.x * P.lmax + next) * 16 + 15] = seen_at;   // seen finished
-                    P.trace[((size_t)blockIdx.x * P.lmax + next) * 16 + 14] = gtimer();  // published
+                if (P.trace) {  // (a slot's stamps: its last step's)
+                    const size_t e = ((size_t)blockIdx.x * P.lmax + next % P.lmax) * 16;
+                    P.trace[e + 15] = seen_at;   // seen finished
+                    P.trace[e + 14] = gtimer();  // published
                 }
             }
             wc = wn;
@@ -404,8 +432,15 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
     TcState tc;       // tensor-core plans: tiles and activation stages so far
     WIns I;
     fetch_init(I, P, myq);
-    for (int i = 0; i < P.lmax; ++i) {
-        fetch(I, P, myq, i);
+    for (int v = 0; v < P.lmax * P.nsteps; ++v) {
+        const int i = v % P.lmax;
+        if (i == 0) {  // a new step: its own argmax, activations and hand-off chain
+            I.step = P.step + v / P.lmax;
+            lm_best = 0;
+            x.key = -1;
+            chain.valid = false;
+        }
+        fetch(I, P, myq, v);
         const Dec d = decode(I);
         const int opc = d.opc;
         if (opc == MK_OP_NOOP) continue;
@@ -476,7 +511,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
             wrote = false;
         }
         if (handoff) ++hs;
-        handoff_progress(S, i, wrote);
+        handoff_progress(S, v, wrote);
         if (ct == 0 && P.trace) {
             uint64_t *tr = P.trace + ((size_t)blockIdx.x * P.lmax + i) * 16;
             tr[0] = (uint64_t)opc | ((uint64_t)(uint32_t)d.task << 32);
@@ -853,6 +888,9 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
     if ((uintptr_t)workspace % 256) return set_error(MK_ERR_INVALID, "workspace must be 256-byte aligned");
     if (first_step < 0 || num_steps < 0 || (p.kind == PLAN_LLAMA && first_step + num_steps > p.max_steps))
         return set_error(MK_ERR_INVALID, "steps outside the planned range");
+    const bool one_launch = (flags & MK_RUN_ONE_LAUNCH) != 0;
+    if (one_launch && p.segments.size() != 1)
+        return set_error(MK_ERR_INVALID, "MK_RUN_ONE_LAUNCH needs a megakernel plan");
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     cudaError_t e;
     if (p.table_dirty || p.uploaded_ws != workspace) {
@@ -917,7 +955,10 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
     KParams k = base_params(p, ws);
     k.timeout_ns = timeout_ns ? timeout_ns : 200000000ull;
     k.flags = (int)flags;
-    for (int s = first_step; s < first_step + num_steps; ++s) {
+    // one launch per step, or one launch for all of them
+    const int launches = one_launch ? (num_steps > 0 ? 1 : 0) : num_steps;
+    k.nsteps = one_launch ? num_steps : 1;
+    for (int s = first_step; s < first_step + launches; ++s) {
         k.step = s;
         for (const Segment &seg : p.segments) {
             if (per_sm < 1 || seg.workers > per_sm * sms)

@@ -58,6 +58,7 @@ enum : int {
 enum : int {
     P_G = W_P + 0, P_B = W_P + 1, P_SPLIT = W_P + 2, P_T0 = W_P + 3, P_T = W_P + 4,
     P_NSPLIT = W_P + 5, P_LAYER = W_P + 6,
+    P_ATHR = W_P + 7,   // threshold of the event the layer's attention tasks signal
 };
 
 // GLM block payload.  GEMM tiles use the GEMV fields P_ROW0 (first weight
@@ -123,7 +124,8 @@ struct KParams {
     uint64_t *trace;        // [num_workers, lmax, 4] or null
     uint64_t timeout_ns;
     int lmax, num_workers, num_ops, num_events;
-    int step, flags;
+    int step, flags;        // first step of this launch, MK_RUN_* flags
+    int nsteps;             // steps this launch runs (the queue is walked once per step)
     int num_pages, page_bytes, act_bytes, abuf_bytes, abuf_count, aux_bytes, red_bytes, smem_bytes;
     int B, H, Hq, Hkv, D, F, V, L, Smax, qk_norm, nsplit_max;
     int np;                 // tensor-core plans: the batch padded to 8 or 16 (N = 2 np), else 0

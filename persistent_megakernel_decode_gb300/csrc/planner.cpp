@@ -813,6 +813,7 @@ static int plan_llama_tc(const mk_model_desc *m, const mk_step_desc *s, const mk
             pl[P_G - W_P] = r.bid[0]; pl[P_B - W_P] = r.bid[1]; pl[P_SPLIT - W_P] = r.bid[2];
             pl[P_T0 - W_P] = r.bid[2] * kn_T; pl[P_T - W_P] = kn_T; pl[P_NSPLIT - W_P] = nsplit[r.bid[1]];
             pl[P_LAYER - W_P] = op.layer;
+            pl[P_ATHR - W_P] = r.trig >= 0 ? evs[r.trig].ntrig : 0;
             break;
         case MK_OP_O: {
             const int ko = Hq * D / ks_o;
@@ -1156,6 +1157,7 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
             pl[P_G - W_P] = r.bid[0]; pl[P_B - W_P] = r.bid[1]; pl[P_SPLIT - W_P] = r.bid[2];
             pl[P_T0 - W_P] = r.bid[2] * kn_T; pl[P_T - W_P] = kn_T; pl[P_NSPLIT - W_P] = nsplit[r.bid[1]];
             pl[P_LAYER - W_P] = op.layer;
+            pl[P_ATHR - W_P] = r.trig >= 0 ? evs[r.trig].ntrig : 0;
             break;
         case MK_OP_O:
             pl[P_ROW0 - W_P] = r.bid[0] * kn_o; pl[P_NROWS - W_P] = std::min(kn_o, H - r.bid[0] * kn_o);

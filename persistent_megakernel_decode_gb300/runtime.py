@@ -25,7 +25,7 @@ OP_NAMES = {0: "noop", 1: "counter", 2: "embed", 3: "qkv", 4: "attn", 5: "o", 6:
 OPCODE = {v: k for k, v in OP_NAMES.items()}
 MODE_MEGAKERNEL, MODE_PER_OP = 0, 1
 SCHED_DEFAULT, SCHED_BYTES, SCHED_TIMED = 0, 1, 2
-RUN_HOST_TOKENS, RUN_TRACE = 1, 2
+RUN_HOST_TOKENS, RUN_TRACE, RUN_ONE_LAUNCH = 1, 2, 4
 PAIR_WHOLE, PAIR_TILE, PAIR_TILE_COVER, PAIR_TILE_REDUCE = 0, 1, 2, 3
 TASK_FIELDS = 24
 BIND = {n: i for i, n in enumerate([
@@ -294,8 +294,9 @@ class Session:
         self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
 
     def run(self, first_step: int, num_steps: int = 1, host_tokens: bool = False, trace: bool = False,
-            timeout_ns: int = 0):
-        flags = (RUN_HOST_TOKENS if host_tokens else 0) | (RUN_TRACE if trace else 0)
+            timeout_ns: int = 0, one_launch: bool = False):
+        flags = (RUN_HOST_TOKENS if host_tokens else 0) | (RUN_TRACE if trace else 0) | \
+            (RUN_ONE_LAUNCH if one_launch else 0)
         _check(load().mk_run(self.plan.h, C.c_void_p(self.ws_ptr), self.ws_bytes, first_step, num_steps, flags,
                              timeout_ns, C.c_void_p(self.stream.cuda_stream)))
 
@@ -375,8 +376,9 @@ class GlmSession:
             p.bind("glm_" + n, t.data_ptr())
         self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
 
-    def run(self, first_step: int = 0, num_steps: int = 1, trace: bool = False, timeout_ns: int = 0):
-        flags = RUN_TRACE if trace else 0
+    def run(self, first_step: int = 0, num_steps: int = 1, trace: bool = False, timeout_ns: int = 0,
+            one_launch: bool = False):
+        flags = (RUN_TRACE if trace else 0) | (RUN_ONE_LAUNCH if one_launch else 0)
         _check(load().mk_run(self.plan.h, C.c_void_p(self.ws_ptr), self.ws_bytes, first_step, num_steps, flags,
                              timeout_ns, C.c_void_p(self.stream.cuda_stream)))
 
