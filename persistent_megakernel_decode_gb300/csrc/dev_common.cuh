@@ -414,9 +414,16 @@ DEV Dec decode(const WIns &I) {
 
 // Lane k's word of queue slot i (all zero, i.e. a NoOp, past the queue's end).
 // Slots are numbered through the launch: slot v is queue slot v % lmax of
-// step v / lmax.
-DEV int queue_word(const KParams &P, const int32_t *q, int v) {
-    return v < P.lmax * P.nsteps ? __ldg(q + (size_t)(v % P.lmax) * W_WORDS + (threadIdx.x & 31)) : 0;
+// step v / lmax.  Lane k's word of queue slot i (in-step index), or 0 (a
+// NoOp) where the launch has no such slot.
+DEV int queue_word(const int32_t *q, int i, bool exists) {
+    return exists ? __ldg(q + (size_t)i * W_WORDS + (threadIdx.x & 31)) : 0;
+}
+// In-step index of the slot `ahead` slots after in-step index i.
+DEV int slot_ahead(const KParams &P, int i, int ahead) {
+    int j = i + ahead;
+    while (j >= P.lmax) j -= P.lmax;
+    return j;
 }
 
 // Starts loading the operand row of the instruction held in `w` unless `row`
@@ -432,20 +439,25 @@ DEV void load_orow(const KParams &P, int w, int &row, uint64_t &orow) {
 }
 
 DEV void fetch_init(WIns &I, const KParams &P, const int32_t *q) {
-    I.w1 = queue_word(P, q, 0);
+    const int total = P.lmax * P.nsteps;
+    I.w1 = queue_word(q, 0, total > 0);
     load_orow(P, I.w1, I.row1, I.orow1);
-    I.w2 = queue_word(P, q, 1);
+    I.w2 = queue_word(q, slot_ahead(P, 0, 1), total > 1);
 }
 
-// Moves the warp to slot i; slots must be visited in order 0, 1, 2, ...
+// Moves the warp to slot i of step I.step; slots must be visited in order
+// (step by step, slot by slot).
 DEV void fetch(WIns &I, const KParams &P, const int32_t *q, int i) {
     I.w = I.w1;
     I.orow = I.orow1;
     I.row = I.row1;
     I.w1 = I.w2;
-    I.w2 = queue_word(P, q, i + 2);
+    const int j = i + 2, steps_on = j >= P.lmax ? (j >= 2 * P.lmax ? 2 : 1) : 0;
+    I.w2 = queue_word(q, slot_ahead(P, i, 2), I.step + steps_on < P.step + P.nsteps);
     load_orow(P, I.w1, I.row1, I.orow1);
 }
+// The launch-wide number of slot i of step I.step (progress words count these).
+DEV int launch_slot(const KParams &P, const WIns &I, int i) { return (I.step - P.step) * P.lmax + i; }
 
 // Warp-uniform sanity checks of one instruction against the launch.
 // Kernel instances ("flavours"): FL_GEN runs every Llama-path op; FL_GLM

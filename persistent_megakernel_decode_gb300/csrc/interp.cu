@@ -42,16 +42,15 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int NP = P.num_pages, PS = P.page_bytes;
     WIns I;
     fetch_init(I, P, myq);
-    for (int v = 0; v < P.lmax * P.nsteps; ++v) {
-        const int i = v % P.lmax;
-        if (i == 0) I.step = P.step + v / P.lmax;  // the step of slot v
-        if (cta_aborting(S)) break;
+    for (I.step = P.step; I.step < P.step + P.nsteps; ++I.step)
+    for (int i = 0; i < P.lmax; ++i) {
+        if (cta_aborting(S)) goto drain;
         if (lane < 4 && i + 4 + lane < P.lmax) prefetch_l2(myq + (size_t)(i + 4 + lane) * W_WORDS);
-        fetch(I, P, myq, v);
+        fetch(I, P, myq, i);
         const int opc = F(I, W_OPC);
         if (!ins_valid<FL>(P, I)) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
-            break;
+            goto drain;
         }
         if constexpr (FL == FL_TC) {
             if (is_gemv_op(opc)) {  // tensor-core tile: one page per stage of 128 K columns
@@ -72,7 +71,7 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
                     }
                 }
                 if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 5] = gtimer();
-                if (stop) break;
+                if (stop) goto drain;
                 continue;
             }
         }
@@ -84,7 +83,7 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
             if (F(I, P_T0) + attn_cached_rows(I, attn_pos(P, I)) > pos0) {
                 const int ev = F(I, W_SIG);
                 const uint32_t target = (uint32_t)F(I, P_ATHR) * (uint32_t)I.step;
-                if (!warp_wait_counter(P, S, ev, target, i, opc)) break;
+                if (!warp_wait_counter(P, S, ev, target, i, opc)) goto drain;
                 fence_proxy_async_global();
             }
         }
@@ -100,7 +99,7 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
         const int rpp = row_bytes > 0 ? PS / row_bytes : 0;
         if (nseg > 0 && (rpp < 1 || (nseg > 1 && s1.row_bytes != row_bytes))) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
-            break;
+            goto drain;
         }
         // lane 0: copy rows [r, r + n) of a segment to dst
         auto copy_rows = [&](const Seg &sg, int r, int n, uint8_t *dst, uint64_t *bar) {
@@ -160,8 +159,9 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
             }
         }
         if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 5] = gtimer();
-        if (stop) break;
+        if (stop) goto drain;
     }
+drain:
     // no bulk copy may still target this CTA's shared memory when it exits
     if (lane == 0) {
         const uint32_t first = ring > (uint32_t)NP ? ring - NP : 0;
@@ -211,14 +211,13 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
         }
         if (!ab && lane == 0 && P.trace) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 2] = gtimer();
     };
-    for (int v = 0; v < P.lmax * P.nsteps; ++v) {
-        const int i = v % P.lmax;
+    for (I.step = P.step; I.step < P.step + P.nsteps; ++I.step)
+    for (int i = 0; i < P.lmax; ++i) {
         if (i == 0) {  // a new step: nothing staged so far holds this step's activations
-            I.step = P.step + v / P.lmax;
             key0 = key1 = -1;
             chain.valid = false;
         }
-        fetch(I, P, myq, v);
+        fetch(I, P, myq, i);
         const int opc = F(I, W_OPC);
         if (opc == MK_OP_NOOP) continue;
         if constexpr (FL == FL_TC) {
@@ -316,14 +315,15 @@ DEV int progress_min(const Smem S) {
 DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
     const int lane = threadIdx.x & 31;
     const int total = P.lmax * P.nsteps;
-    int next = 0;                                              // first slot not yet published (launch-wide)
-    int wc = queue_word(P, myq, 0), wn = queue_word(P, myq, 1);  // words of slots next, next + 1
+    int next = 0, ni = 0;  // first slot not yet published (launch-wide) and its in-step index
+    int wc = queue_word(myq, 0, total > 0), wn = queue_word(myq, slot_ahead(P, 0, 1), total > 1);  // slots next, next + 1
     while (next < total) {
         if (__shfl_sync(FULL, wc, W_OPC) == MK_OP_NOOP) {
             // NoOps only pad the tail of a step's queue: go on at the next step's first slot
-            next = (next / P.lmax + 1) * P.lmax;
-            wc = queue_word(P, myq, next);
-            wn = queue_word(P, myq, next + 1);
+            next += P.lmax - ni;
+            ni = 0;
+            wc = queue_word(myq, 0, next < total);
+            wn = queue_word(myq, slot_ahead(P, 0, 1), next + 1 < total);
             continue;
         }
         int done = next, ab = 0, stop = 0;
@@ -362,13 +362,14 @@ DEV void publisher_role(const KParams &P, const Smem S, const int32_t *myq) {
                 if (ns > 0) red_release_add(P.counters + e0, (uint32_t)i0);
                 if (ns > 1) red_release_add(P.counters + e1, (uint32_t)i1);
                 if (P.trace) {  // (a slot's stamps: its last step's)
-                    const size_t e = ((size_t)blockIdx.x * P.lmax + next % P.lmax) * 16;
+                    const size_t e = ((size_t)blockIdx.x * P.lmax + ni) * 16;
                     P.trace[e + 15] = seen_at;   // seen finished
                     P.trace[e + 14] = gtimer();  // published
                 }
             }
             wc = wn;
-            wn = queue_word(P, myq, next + 2);
+            wn = queue_word(myq, slot_ahead(P, ni, 2), next + 2 < total);
+            ni = ni + 1 == P.lmax ? 0 : ni + 1;
         }
     }
 }
@@ -432,15 +433,14 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
     TcState tc;       // tensor-core plans: tiles and activation stages so far
     WIns I;
     fetch_init(I, P, myq);
-    for (int v = 0; v < P.lmax * P.nsteps; ++v) {
-        const int i = v % P.lmax;
+    for (I.step = P.step; I.step < P.step + P.nsteps; ++I.step)
+    for (int i = 0; i < P.lmax; ++i) {
         if (i == 0) {  // a new step: its own argmax, activations and hand-off chain
-            I.step = P.step + v / P.lmax;
             lm_best = 0;
             x.key = -1;
             chain.valid = false;
         }
-        fetch(I, P, myq, v);
+        fetch(I, P, myq, i);
         const Dec d = decode(I);
         const int opc = d.opc;
         if (opc == MK_OP_NOOP) continue;
@@ -511,7 +511,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
             wrote = false;
         }
         if (handoff) ++hs;
-        handoff_progress(S, v, wrote);
+        handoff_progress(S, launch_slot(P, I, i), wrote);
         if (ct == 0 && P.trace) {
             uint64_t *tr = P.trace + ((size_t)blockIdx.x * P.lmax + i) * 16;
             tr[0] = (uint64_t)opc | ((uint64_t)(uint32_t)d.task << 32);
