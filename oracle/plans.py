@@ -123,6 +123,89 @@ def llama_step_ops(shape: LlamaShape, k: Knobs, B: int, seq0: Sequence[int], max
     return ops, edges, kinds
 
 
+def _round_up(x, a):
+    return -(-x // a) * a
+
+
+def llama_knobs(shape: LlamaShape, B: int, seq0: Sequence[int], max_steps: int, n_workers: int,
+                smem_per_cta: int) -> Knobs:
+    """Tile knobs of a plan of GEMV tiles (batch 1..8), from the stated rules.
+
+    * Rows per tile: the most rows (a power of two) of K bf16 values that fit a
+      64 KB tile (128 KB when every K is a multiple of 512 at batch above 1:
+      the warp-level tensor-core tiles take two pages), at most 16 (8 at batch
+      above 4 without those tiles), MLP-up half of that; MLP-down's K chunk is
+      the largest multiple of 8 up to 2048 that divides the ffn.
+    * The page: 64 KB when three fit beside the fixed buffers (two activation
+      buffers of batch x the longest K in fp32 when both fit in 32 KB, else
+      one; two slots for the attention staging and the O residual rows; the
+      attention scores and 4 reduction buffers; barriers and flags), else
+      32 KB, else 16 KB; the tensor-core tiles at K = 4096 take 64 KB pages of
+      8 rows with a single activation buffer.
+    * Batch 1 with pages of exactly 16 rows: QKV 32 rows, MLP-up 64 gate rows,
+      MLP-down 64 rows, LM head one tile per worker (whole pages).
+    * Batch above 4 without the tensor-core tiles' pages: at most 8 rows (MLP-up 4).
+    * Attention: 16384 / (2 head_dim) positions, doubled up to 256 while the
+      attention tasks outnumber the workers.
+    """
+    H, Hq, Hkv, D, F, V = shape.H, shape.Hq, shape.Hkv, shape.D, shape.F, shape.V
+    G = Hq // Hkv
+    WARPS, TILE_ROWS, RESID, NRED, MBAR, CTRL = 8, 16, 16, 4, 512, 128
+
+    def pow2_floor(v):
+        r = 1
+        while r * 2 <= v:
+            r *= 2
+        return r
+
+    clamp = lambda v, lo, hi: max(lo, min(hi, v))
+    mma = H % 512 == 0 and (Hq * D) % 512 == 0 and min(F, 2048) % 512 == 0
+    rcap = 8 if B > 4 and not mma else 16
+    tile = 2 * 65536 if mma else 65536
+    qkv = pow2_floor(clamp(tile // (2 * H), 1, rcap))
+    o = pow2_floor(clamp(tile // (2 * Hq * D), 1, rcap))
+    up = pow2_floor(clamp(tile // (4 * H), 1, rcap // 2))
+    kc = 8
+    for c in range(8, min(F, 2048) + 1, 8):
+        if F % c == 0:
+            kc = c
+    down = pow2_floor(clamp(tile // (2 * kc), 1, rcap))
+    lm = pow2_floor(clamp(tile // (2 * H), 1, rcap))
+    T = clamp(16384 // (2 * D), 16, 256)
+    while 2 * T <= 256 and sum(_ceil(s + max_steps, T) for s in seq0) * Hkv > n_workers:
+        T *= 2
+    # shared memory beside the pages
+    kmax = max(H, Hq * D, kc)
+    abuf = _round_up(B * kmax * 4, 128)
+    act = _round_up((G * (D + 16) + 2 * D) * 4 + B * RESID * 4, 128)
+    maxb = 1 if B <= 1 else 2 if B <= 2 else 4 if B <= 4 else 8
+    red = _round_up(WARPS * TILE_ROWS * maxb * 4, 128)
+    aux = _round_up((WARPS * _ceil(T, WARPS // G) + 32) * 4, 128) + NRED * red
+    nbuf = 2 if 2 * abuf <= 32768 else 1
+    fixed = nbuf * abuf + 2 * act + aux + MBAR + CTRL
+    page = 16384
+    for pb in (65536, 32768):
+        if (smem_per_cta - fixed) // pb >= 3:
+            page = pb
+            break
+    if mma and page < 16 * kmax and nbuf == 2 and 16 * kmax <= 65536 and \
+            (smem_per_cta - (fixed - abuf)) // (16 * kmax) >= 3:
+        page = 16 * kmax
+    multi = lambda K: B == 1 and K % 256 == 0 and K <= 2048 and page == 32 * K
+    if multi(H):
+        lm = 16 * min(64, _ceil(_ceil(V, 16), n_workers))
+        if F % 64 == 0:
+            up = 64
+        if D % 32 == 0:
+            qkv = 32
+    if multi(kc) and H % 64 == 0:
+        down = 64
+    mma_pages = mma and all(page // (2 * K) >= 8 and K % 512 == 0 for K in (H, Hq * D, kc))
+    if B > 4 and not mma_pages:
+        qkv, o, down, lm, up = min(qkv, 8), min(o, 8), min(down, 8), min(lm, 8), min(up, 4)
+    return Knobs(qkv, o, up, down, kc, lm, T)
+
+
 @dataclass
 class TcKnobs:
     ksplit_qkv: int   # K splits of the QKV tiles

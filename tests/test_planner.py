@@ -83,7 +83,13 @@ def _compare(shape, B, seq0, steps, workers=152, **kn):
     info = p.info()
     q, ids, th, tasks = p.export()
     osh = plans.LlamaShape(shape.L, shape.H, shape.Hq, shape.Hkv, shape.D, shape.F, shape.V)
-    op = plans.llama_step_plan(osh, _oracle_knobs(info), B, seq0, steps, workers)
+    tile_knobs = {k: v for k, v in kn.items() if k != "tc_tiles"}
+    if tile_knobs:  # a test that sets tile knobs itself: the oracle takes the same
+        okn = _oracle_knobs(info)
+    else:           # defaults: the oracle derives them from its own statement of the rules
+        okn = plans.llama_knobs(osh, B, seq0, steps, workers, 232448)
+        assert okn == _oracle_knobs(info), (okn, _oracle_knobs(info))
+    op = plans.llama_step_plan(osh, okn, B, seq0, steps, workers)
     assert info["num_tasks"] == len(op.tasks)
     assert list(th) == op.thresholds
     for i, t in enumerate(op.tasks):
