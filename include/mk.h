@@ -103,7 +103,9 @@ typedef struct {
     int schedule;          /* MK_SCHED_*: how tasks are dealt to workers */
     int tc_tiles;          /* GEMV tiles on tcgen05 tensor cores (128 weight rows x the batch, TMEM
                               accumulators): 0 = for batch >= 8 where the shape allows, 1 = required
-                              (MK_ERR_UNSUPPORTED if the shape does not allow), -1 = never (batch <= 8) */
+                              (MK_ERR_UNSUPPORTED if the shape does not allow), -1 = never (batch <= 8).
+                              GLM block plans: 0 = the FP8 GEMMs on tcgen05 tiles where M = 16, 1 =
+                              required, -1 = warp-level MMA tiles */
 } mk_target_desc;
 
 /* Queue assignment.  Either way tasks go to workers in one topological order,
@@ -125,7 +127,7 @@ typedef struct {
     uint64_t scratch_offset;         /* workspace offset from which every byte is rewritten
                                         within a step before it is read (activations, partials) */
     uint64_t algorithmic_bytes_step; /* weights once + KV read + KV append, at step 0 */
-    int tc_tiles;                    /* 1: the GEMV tiles run on tcgen05 tensor cores */
+    int tc_tiles;                    /* 1: the GEMV (GLM: FP8 GEMM) tiles run on tcgen05 tensor cores */
     int ksplit_qkv, ksplit_o;        /* tensor-core plans: K splits of the QKV and O tiles */
 } mk_plan_info;
 
@@ -267,13 +269,16 @@ int mk_plan_graph(const mk_graph_desc *graph, const mk_target_desc *target, mk_p
  * its kernels and branches).  Per step, for M = requests x tokens rows:
  *   A0   new residual = x + res (bf16); RMSNorm (weight bound, eps); per
  *        (row, 128 columns) e4m3 with scale amax / 448        (M tasks)
- *   B    QKV-A, Head-Gate, Indexer-K: FP8 GEMMs of A0's rows, 16 weight rows
- *        per task, K split over the 8 consumer warps
+ *   B    QKV-A, Head-Gate, Indexer-K: FP8 GEMMs of A0's rows -- warp-level
+ *        tiles: 16 weight rows per task, K split over the 8 consumer warps;
+ *        tcgen05 tiles (M = 16): 128 weight rows per task, K split over
+ *        tasks (fp32 sums; the last part of a row tile rounds them to bf16)
  *   FIN  per row: q-lora (QKV-A columns 0 .. q_lora-1) re-quantised per 128;
  *        kv-lora || RoPE(k_pe) -> latent cache, Indexer-K with RoPE on its
  *        last `rope` columns -> index cache, at slot pos0 + token  (M tasks)
  *   C    Q-B and Indexer-Q: FP8 GEMMs of the re-quantised q-lora, 64 weight
- *        rows per task, RoPE on the last `rope` columns of each head
+ *        rows per task (tcgen05 tiles: 128), RoPE on the last `rope` columns
+ *        of each head
  * Every GEMM output is sum over 128-wide K blocks of a_scale * w_scale *
  * (a . w), rounded to bf16; RoPE is rotate-half with angle
  * pos * rope_theta^(-2i/rope) on those bf16 values.  Events: A0 -> B (whole),
@@ -281,7 +286,9 @@ int mk_plan_graph(const mk_graph_desc *graph, const mk_target_desc *target, mk_p
  * waits for the previous step's last tasks.  Constraints (MK_ERR_UNSUPPORTED
  * otherwise): M <= 16; hidden, q_lora, kv_lora multiples of 128; rope = 64;
  * q_head_dim and idx_dim multiples of 64 with the roped part the last 64;
- * q_lora + kv_lora + rope, gate_heads, idx_dim multiples of 16. */
+ * q_lora + kv_lora + rope, gate_heads, idx_dim multiples of 16; kv_lora
+ * and idx_dim - rope at most 512, gate_heads at most 256; tcgen05 tiles
+ * also M = 16 and q_lora <= 1536. */
 typedef struct {
     int requests, tokens;        /* M = requests * tokens rows, token j of request r is row r * tokens + j */
     int hidden;

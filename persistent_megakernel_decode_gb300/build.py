@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIB_DIR, "libmk.so")
 SOURCES = ["interp.cu", "api.cpp", "planner.cpp"]
-HEADERS = ["mk_internal.h", "planner.h", "dev_common.cuh", "dev_ops.cuh", "dev_glm.cuh", "dev_tc.cuh"]
+HEADERS = ["mk_internal.h", "planner.h", "dev_common.cuh", "dev_ops.cuh", "dev_glm.cuh", "dev_tc.cuh", "dev_glm_tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -38,6 +38,15 @@ void layout_workspace(Plan &p) {
     } else {
         p.ws.xn = p.ws.xo = p.ws.act16 = 0;
     }
+    // GLM tensor-core plans: the fp32 sums of the K-split GEMMs, zero at step
+    // 0 (FIN zeroes them again for the next step)
+    p.ws.gsum[0] = p.ws.gsum[1] = p.ws.gsum[2] = 0;
+    if (p.kind == PLAN_GLM && p.tc) {
+        const int M = GT_N;
+        p.ws.gsum[0] = take((uint64_t)M * (p.glm.q_lora + p.glm.kv_lora + p.glm.rope) * 4);
+        p.ws.gsum[1] = take((uint64_t)M * p.glm.gate_heads * 4);
+        p.ws.gsum[2] = take((uint64_t)M * p.glm.idx_dim * 4);
+    }
     p.ws.queue = take(p.words.size() * 4);
     p.ws.optab = take((uint64_t)p.num_ops * N_SLOTS * 8);
     p.ws.seq0 = take((uint64_t)B * 4);
@@ -53,7 +62,9 @@ void layout_workspace(Plan &p) {
     } else {
         p.ws.hres = p.ws.hmid = p.ws.qkv = p.ws.part = p.ws.attn_out = p.ws.act = 0;
     }
-    p.ws.tmaps = p.tc ? take((uint64_t)(TC_NTMAPS_FIXED + TC_WMAPS_PER_LAYER * L + 1) * 128) : 0;
+    p.ws.tmaps = !p.tc                   ? 0
+                 : p.kind == PLAN_GLM    ? take((uint64_t)GT_NTMAPS * 128)
+                                         : take((uint64_t)(TC_NTMAPS_FIXED + TC_WMAPS_PER_LAYER * L + 1) * 128);
     p.ws.trace = take(total_slots * 16 * 8);
     p.ws.total = off;
 }

@@ -213,8 +213,8 @@ struct Smem {
     DEV uint64_t *xfull() const { return full() + 2 * num_pages + 5; }
     DEV uint64_t *xempty() const { return xfull() + TC_XSLOTS; }
     DEV uint64_t *accfull() const { return xempty() + TC_XSLOTS; }
-    DEV uint64_t *accempty() const { return accfull() + 2; }
-    DEV uint64_t *drain() const { return accempty() + 2; }
+    DEV uint64_t *accempty() const { return accfull() + GT_NACC; }
+    DEV uint64_t *drain() const { return accempty() + GT_NACC; }
     DEV int *page_users() const { return reinterpret_cast<int *>(mk_smem + o_ctrl) + 16; }
     DEV uint32_t *tmem_slot() const { return reinterpret_cast<uint32_t *>(mk_smem + o_ctrl) + 31; }
 };
@@ -461,15 +461,18 @@ DEV int launch_slot(const KParams &P, const WIns &I, int i) { return (I.step - P
 
 // Warp-uniform sanity checks of one instruction against the launch.
 // Kernel instances ("flavours"): FL_GEN runs every Llama-path op; FL_GLM
-// only the GLM-block ops (and holds their code); FL_LEAN is the batch-1
-// instance for plans whose GEMV tiles all take the row-per-warp path and whose
-// head_dim is 64 -- it holds no other GEMV or attention variant, which keeps
-// its registers free of spills.
-constexpr int FL_GEN = 0, FL_GLM = 1, FL_LEAN = 2, FL_TC = 3;
+// only the GLM-block ops (and holds their code), with warp-level MMA tiles,
+// FL_GLMTC the same with tcgen05 tiles -- two instances, so that each holds
+// only one GEMM path; FL_LEAN is the batch-1 instance for plans whose GEMV
+// tiles all take the row-per-warp path and whose head_dim is 64 -- it holds
+// no other GEMV or attention variant, which keeps its registers free of
+// spills; FL_TC the batched decoder's tcgen05 instance.
+constexpr int FL_GEN = 0, FL_GLM = 1, FL_LEAN = 2, FL_TC = 3, FL_GLMTC = 4;
+MK_HD constexpr bool fl_glm(int fl) { return fl == FL_GLM || fl == FL_GLMTC; }
 
 template <int FL>
 DEV bool ins_valid(const KParams &P, const WIns &I) {
-    constexpr bool GLM = FL == FL_GLM;
+    constexpr bool GLM = fl_glm(FL);
     const int opc = F(I, W_OPC);
     if (opc < 0 || opc >= MK_NUM_OPCODES) return false;
     if (opc == MK_OP_NOOP) return true;
@@ -504,10 +507,23 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
         if (opc == MK_OP_GLM_FIN) {
             const int ql = F(I, P_GF_QLORA), kl = F(I, P_GF_KVLORA), id = F(I, P_GF_IDX), m = F(I, P_ROW0);
             return m >= 0 && m < M && ql > 0 && ql % 128 == 0 && ql <= 16 * 128 && kl >= 0 && kl % 2 == 0 &&
+                   kl <= 2 * CONSUMERS && id - GLM_ROPE <= 2 * CONSUMERS && F(I, P_GF_GATE) <= CONSUMERS &&
                    id >= GLM_ROPE && id % 2 == 0 && F(I, P_GL_POS0) + T <= F(I, P_GF_SLOTS) &&
-                   F(I, P_GF_QKVA_LD) >= ql + kl + GLM_ROPE;
+                   F(I, P_GF_QKVA_LD) >= ql + kl + GLM_ROPE && F(I, P_GF_QKVA_LD) % 4 == 0 && id % 4 == 0 &&
+                   F(I, P_GF_SUMS) == (FL == FL_GLMTC ? 1 : 0) && (FL != FL_GLMTC || (P.np == GT_N && F(I, P_GF_GATE) > 0));
         }
         const int nr = F(I, P_NROWS), kc = F(I, P_KC), rpp = F(I, P_RPP);
+        if ((F(I, P_GL_TCT) != 0) != (FL == FL_GLMTC)) return false;  // each instance runs its own tiles
+        if (FL == FL_GLMTC) {
+            // tensor-core tile: whole stages of one scale block, 128-row tiles, the plan's slot and page sizes
+            const int k0 = F(I, P_K0), K = F(I, P_KTOT), nst = F(I, P_NPG), sum = F(I, P_GL_SUM);
+            return P.np == GT_N && M == GT_N && P.page_bytes == GT_STAGE_BYTES && P.abuf_count >= GT_XSLOTS &&
+                   P.abuf_bytes >= GT_XSLOT_BYTES && P.aux_bytes >= GT_EX_BYTES + NRED * P.red_bytes && kc > 0 &&
+                   kc % GT_KS == 0 && k0 % GT_KS == 0 && K % GT_KS == 0 && k0 + kc <= K && nst == kc / GT_KS &&
+                   nst <= GT_MAX_STAGES && K / GT_KS <= GT_MAX_KB && nr > 0 && nr <= GT_M && F(I, P_ROW0) >= 0 && F(I, P_ROW0) % GT_M == 0 &&
+                   F(I, P_OUT0) >= 0 && F(I, P_GL_LD) >= F(I, P_OUT0) + nr && (sum == 0 || sum == 1) &&
+                   (F(I, P_GL_ROPE) & ~3) == 0 && (sum == 0 || F(I, P_GL_ROPE) == 0);
+        }
         if (nr != 16 && nr != 64) return false;
         if (kc <= 0 || kc % 128 || F(I, P_K0) != 0 || F(I, P_KTOT) != kc || rpp != P.page_bytes / kc || rpp < 1 ||
             F(I, P_NPG) != (nr + rpp - 1) / rpp || F(I, P_NPG) > P.num_pages)
@@ -584,7 +600,7 @@ DEV int attn_cached_rows(const WIns &I, int pos) { return max(0, min(F(I, P_T), 
 // consumers derive the same segments and walk the same page ring.
 template <int FL>
 DEV int describe(const KParams &P, const WIns &I, Seg &s0, Seg &s1) {
-    constexpr bool GLM = FL == FL_GLM;
+    constexpr bool GLM = fl_glm(FL);
     const int opc = F(I, W_OPC);
     if (opc == MK_OP_QKV || opc == MK_OP_O || opc == MK_OP_DOWN || opc == MK_OP_LM || opc == MK_OP_UP) {
         const long long ktot = F(I, P_KTOT);

@@ -44,13 +44,18 @@ DEV void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t
 }
 
 // Quantise 4 values of a 128-column block whose other 124 values sit in the
-// warp's other lanes: scale = amax / 448 (1 for an all-zero block), codes of
-// value / scale.  Returns the 4 codes (first value in the low byte).
+// warp's other lanes: scale = amax / 448 (1 for an all-zero block; an IEEE
+// division, so the fp32 scale is the correctly rounded one), codes of value
+// / scale -- taken as value times the correctly rounded reciprocal, within
+// 2^-23 of the quotient, so a code can only differ from the exact quotient's
+// rounding where that quotient sits that close to a midpoint between two
+// codes.  Returns the 4 codes (first value in the low byte).
 DEV uint32_t quant4(const float (&v)[4], float &scale) {
     float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
     a = warp_max(a);
     scale = a > 0.f ? a / 448.f : 1.f;
-    return e4m3x2(v[0] / scale, v[1] / scale) | (e4m3x2(v[2] / scale, v[3] / scale) << 16);
+    const float inv = __frcp_rn(scale);
+    return e4m3x2(v[0] * inv, v[1] * inv) | (e4m3x2(v[2] * inv, v[3] * inv) << 16);
 }
 
 // ---------------------------------------------------------------- A0
@@ -118,6 +123,7 @@ DEV void glm_a0_task(const KParams &P, const Smem S, const WIns &I, int i, uint3
             }
         }
     }
+    trace_stamp(P, i, 12);
 }
 
 // ---------------------------------------------------------------- GEMM tile
@@ -241,51 +247,138 @@ DEV void glm_gemm_task(const KParams &P, const Smem S, const WIns &I, int i, int
 // One token row m of request m / T at slot pos0 + m % T: q-lora (QKV-A
 // columns 0 .. QL-1) re-quantised per 128 columns, one warp per block; the
 // latent cache row = kv-lora || RoPE(k_pe); the index cache row = Indexer-K
-// with RoPE on its last 64 columns.
+// with RoPE on its last 64 columns.  With the tensor-core tiles (SUMS) the
+// first GEMMs left fp32 sums: FIN reads each value of its row once from
+// them, rounds it to bf16 (the GEMM output), stores that and zeroes the sum
+// -- the Head-Gate row too.  Every thread loads all its values before any
+// store (one round trip); the plan keeps each part within one pass of the
+// 256 consumer threads (q-lora <= 16 blocks, kv-lora <= 512, Indexer-K's
+// unroped part <= 512, Head-Gate <= 256).
+template <bool SUMS>  // the tensor-core instance: the first GEMMs left fp32 sums
 DEV void glm_fin_task(const KParams &P, const WIns &I, bool ab) {
     const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
     const int m = F(I, P_ROW0), QL = F(I, P_GF_QLORA), KL = F(I, P_GF_KVLORA), ID = F(I, P_GF_IDX);
     const int slots = F(I, P_GF_SLOTS), LDQ = F(I, P_GF_QKVA_LD), T = F(I, P_GL_T), pos0 = F(I, P_GL_POS0);
-    const __nv_bfloat16 *qkva = reinterpret_cast<const __nv_bfloat16 *>(PTR(I, S_GF_QKVA)) + (size_t)m * LDQ;
-    const __nv_bfloat16 *ik = reinterpret_cast<const __nv_bfloat16 *>(PTR(I, S_GF_IK)) + (size_t)m * ID;
+    const int G = F(I, P_GF_GATE);
+    __nv_bfloat16 *qkva = reinterpret_cast<__nv_bfloat16 *>(PTR(I, S_GF_QKVA)) + (size_t)m * LDQ;
+    __nv_bfloat16 *ik = reinterpret_cast<__nv_bfloat16 *>(PTR(I, S_GF_IK)) + (size_t)m * ID;
     uint8_t *qb = reinterpret_cast<uint8_t *>(PTR(I, S_GF_QB)) + (size_t)m * QL;
     float *sb = reinterpret_cast<float *>(PTR(I, S_GF_SB)) + (size_t)m * (QL >> 7);
     __nv_bfloat16 *lat = reinterpret_cast<__nv_bfloat16 *>(PTR(I, S_GF_LAT));
     __nv_bfloat16 *idx = reinterpret_cast<__nv_bfloat16 *>(PTR(I, S_GF_IDX));
     const float2 *rtab = reinterpret_cast<const float2 *>(PTR(I, S_GF_ROPE));
-    const int req = m / T, j = m % T, slot = pos0 + j;
-    // RoPE pairs: threads 0-31 the k_pe slice, 32-63 Indexer-K's last 64 (loaded first)
-    const int p = ct & 31;
-    float lo = 0.f, hi = 0.f;
-    if (ct < 64) {
-        const __nv_bfloat16 *src = ct < 32 ? qkva + QL + KL : ik + ID - GLM_ROPE;
-        const unsigned short *s16 = reinterpret_cast<const unsigned short *>(src);
-        lo = __uint_as_float((uint32_t)__ldcg(s16 + p) << 16);
-        hi = __uint_as_float((uint32_t)__ldcg(s16 + p + 32) << 16);
+    float *fq = SUMS ? reinterpret_cast<float *>(PTR(I, S_GF_FQKVA)) + (size_t)m * LDQ : nullptr;
+    float *fi = SUMS ? reinterpret_cast<float *>(PTR(I, S_GF_FIK)) + (size_t)m * ID : nullptr;
+    float *fg = SUMS ? reinterpret_cast<float *>(PTR(I, S_GF_FGATE)) + (size_t)m * G : nullptr;
+    __nv_bfloat16 *gate = SUMS ? reinterpret_cast<__nv_bfloat16 *>(PTR(I, S_GF_GATE)) + (size_t)m * G : nullptr;
+    if (ab) return;
+    const int req = m / T, j = m % T, slot = pos0 + j, p = ct & 31, nqb = QL >> 7;
+    // what this thread handles: a RoPE pair (threads 0-31 the k_pe slice,
+    // 32-63 Indexer-K's last 64), up to two q-lora blocks' 4 values, a
+    // kv-lora pair, an unroped Indexer-K pair, a Head-Gate value
+    const bool has_rp = ct < 64, has_l = ct * 2 < KL, has_i = ct * 2 < ID - GLM_ROPE, has_g = SUMS && ct < G;
+    const int c_rp = ct < 32 ? QL + KL + p : ID - GLM_ROPE + p;  // column in QKV-A (ct < 32) or Indexer-K
+    float rp[2] = {0.f, 0.f}, qv[2][4] = {}, lv[2] = {0.f, 0.f}, iv[2] = {0.f, 0.f}, gv = 0.f;
+    if constexpr (SUMS) {
+        float *fr = ct < 32 ? fq : fi;
+        if (has_rp) {
+            rp[0] = __ldcg(fr + c_rp);
+            rp[1] = __ldcg(fr + c_rp + 32);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int blk = warp + CONSUMER_WARPS * k;
+            if (blk < nqb) {
+                const float4 x = __ldcg(reinterpret_cast<const float4 *>(fq + blk * 128 + lane * 4));
+                qv[k][0] = x.x; qv[k][1] = x.y; qv[k][2] = x.z; qv[k][3] = x.w;
+            }
+        }
+        if (has_l) {
+            const float2 x = __ldcg(reinterpret_cast<const float2 *>(fq + QL + ct * 2));
+            lv[0] = x.x; lv[1] = x.y;
+        }
+        if (has_i) {
+            const float2 x = __ldcg(reinterpret_cast<const float2 *>(fi + ct * 2));
+            iv[0] = x.x; iv[1] = x.y;
+        }
+        if (has_g) gv = __ldcg(fg + ct);
+        // the GEMM outputs: every sum rounded to bf16, stored, and zeroed for the next step
+        auto r = [](float &v) { v = round_bf16(v); };
+        if (has_rp) {
+            __nv_bfloat16 *o = ct < 32 ? qkva : ik;
+            r(rp[0]); r(rp[1]);
+            o[c_rp] = __float2bfloat16_rn(rp[0]);
+            o[c_rp + 32] = __float2bfloat16_rn(rp[1]);
+            __stcg(fr + c_rp, 0.f);
+            __stcg(fr + c_rp + 32, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int blk = warp + CONSUMER_WARPS * k, col = blk * 128 + lane * 4;
+            if (blk < nqb) {
+                for (int e = 0; e < 4; ++e) r(qv[k][e]);
+                *reinterpret_cast<uint2 *>(qkva + col) =
+                    make_uint2(pack_bf16(qv[k][0], qv[k][1]), pack_bf16(qv[k][2], qv[k][3]));
+                __stcg(reinterpret_cast<float4 *>(fq + col), make_float4(0.f, 0.f, 0.f, 0.f));
+            }
+        }
+        if (has_l) {
+            r(lv[0]); r(lv[1]);
+            *reinterpret_cast<uint32_t *>(qkva + QL + ct * 2) = pack_bf16(lv[0], lv[1]);
+            __stcg(reinterpret_cast<float2 *>(fq + QL + ct * 2), make_float2(0.f, 0.f));
+        }
+        if (has_i) {
+            r(iv[0]); r(iv[1]);
+            *reinterpret_cast<uint32_t *>(ik + ct * 2) = pack_bf16(iv[0], iv[1]);
+            __stcg(reinterpret_cast<float2 *>(fi + ct * 2), make_float2(0.f, 0.f));
+        }
+        if (has_g) {
+            r(gv);
+            gate[ct] = __float2bfloat16_rn(gv);
+            __stcg(fg + ct, 0.f);
+        }
+    } else {
+        const unsigned short *br = reinterpret_cast<const unsigned short *>(ct < 32 ? qkva : ik);
+        if (has_rp) {
+            rp[0] = __uint_as_float((uint32_t)__ldcg(br + c_rp) << 16);
+            rp[1] = __uint_as_float((uint32_t)__ldcg(br + c_rp + 32) << 16);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int blk = warp + CONSUMER_WARPS * k;
+            if (blk < nqb) {
+                const uint2 u = __ldcg(reinterpret_cast<const uint2 *>(qkva + blk * 128 + lane * 4));
+                qv[k][0] = bf16_lo(u.x); qv[k][1] = bf16_hi(u.x); qv[k][2] = bf16_lo(u.y); qv[k][3] = bf16_hi(u.y);
+            }
+        }
+        if (has_l) {
+            const uint32_t u = __ldcg(reinterpret_cast<const uint32_t *>(qkva + QL + ct * 2));
+            lv[0] = bf16_lo(u); lv[1] = bf16_hi(u);
+        }
+        if (has_i) {
+            const uint32_t u = __ldcg(reinterpret_cast<const uint32_t *>(ik + ct * 2));
+            iv[0] = bf16_lo(u); iv[1] = bf16_hi(u);
+        }
     }
-    for (int blk = warp; blk < (QL >> 7); blk += CONSUMER_WARPS) {
-        const int col = blk * 128 + lane * 4;
-        const uint2 u = __ldcg(reinterpret_cast<const uint2 *>(qkva + col));
-        const float v[4] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y)};
-        float scale;
-        const uint32_t codes = quant4(v, scale);
-        if (!ab) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int blk = warp + CONSUMER_WARPS * k, col = blk * 128 + lane * 4;
+        if (blk < nqb) {  // warp-uniform
+            float scale;
+            const uint32_t codes = quant4(qv[k], scale);
             *reinterpret_cast<uint32_t *>(qb + col) = codes;
             if (lane == 0) sb[blk] = scale;
         }
     }
-    if (ab) return;
     __nv_bfloat16 *lrow = lat + ((size_t)req * slots + slot) * (KL + GLM_ROPE);
-    for (int e = ct * 2; e < KL; e += 2 * CONSUMERS)
-        *reinterpret_cast<uint32_t *>(lrow + e) = __ldcg(reinterpret_cast<const uint32_t *>(qkva + QL + e));
     __nv_bfloat16 *irow = idx + ((size_t)req * slots + slot) * ID;
-    for (int e = ct * 2; e < ID - GLM_ROPE; e += 2 * CONSUMERS)
-        *reinterpret_cast<uint32_t *>(irow + e) = __ldcg(reinterpret_cast<const uint32_t *>(ik + e));
-    if (ct < 64) {
+    if (has_l) *reinterpret_cast<uint32_t *>(lrow + ct * 2) = pack_bf16(lv[0], lv[1]);
+    if (has_i) *reinterpret_cast<uint32_t *>(irow + ct * 2) = pack_bf16(iv[0], iv[1]);
+    if (has_rp) {
         __nv_bfloat16 *dst = ct < 32 ? lrow + KL : irow + ID - GLM_ROPE;
         const float2 cs = rtab[j * 32 + p];
-        dst[p] = __float2bfloat16_rn(lo * cs.x - hi * cs.y);
-        dst[p + 32] = __float2bfloat16_rn(hi * cs.x + lo * cs.y);
+        dst[p] = __float2bfloat16_rn(rp[0] * cs.x - rp[1] * cs.y);
+        dst[p + 32] = __float2bfloat16_rn(rp[1] * cs.x + rp[0] * cs.y);
     }
 }
 

@@ -29,6 +29,7 @@
 #include "dev_glm.cuh"
 #include "dev_ops.cuh"
 #include "dev_tc.cuh"
+#include "dev_glm_tc.cuh"
 #include "planner.h"
 
 namespace mk {
@@ -52,9 +53,15 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
             if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
             goto drain;
         }
-        if constexpr (FL == FL_TC) {
-            if (is_gemv_op(opc)) {  // tensor-core tile: one page per stage of 128 K columns
-                const TcTile t = tc_tile_fields(I);
+        if constexpr (FL == FL_TC || FL == FL_GLMTC) {
+            if (FL == FL_TC ? is_gemv_op(opc) : opc == MK_OP_GLM_GEMM) {  // tensor-core tile: one page per stage
+                TcTile t{};
+                GtTile g{};
+                if (FL == FL_TC) t = tc_tile_fields(I);
+                else {
+                    g = gt_tile_fields(I);
+                    t.nst = g.nst;
+                }
                 if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 4] = gtimer();
                 bool stop = false;
                 for (int s = 0; s < t.nst; ++s) {
@@ -62,7 +69,10 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
                         stop = true;
                         break;
                     }
-                    if (lane == 0) tc_load_stage(t, s, S.pages() + (size_t)rp * PS, &S.full()[rp], pol);
+                    if (lane == 0) {
+                        if (FL == FL_TC) tc_load_stage(t, s, S.pages() + (size_t)rp * PS, &S.full()[rp], pol);
+                        else gt_load_stage(g, s, S.pages() + (size_t)rp * PS, &S.full()[rp], pol);
+                    }
                     __syncwarp();
                     ++ring;
                     if (++rp == (uint32_t)NP) {
@@ -179,7 +189,7 @@ drain:
 // ---------------------------------------------------------------- activation-loader warp
 template <int MAXB, int FL>
 DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
-    constexpr bool GLM = FL == FL_GLM;
+    constexpr bool GLM = fl_glm(FL);
     const int lane = threadIdx.x & 31;
     const bool two_bufs = P.abuf_count > 1;
     long long key0 = -1, key1 = -1;   // what each activation buffer holds: op row << 32 | first column
@@ -190,7 +200,7 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
     uint32_t seen_target = 0;
     uint32_t hs = 0;            // activation hand-offs so far; hand-off h uses activation slot h % 2
     HandoffChain chain;
-    uint32_t xq = 0;            // tensor-core plans: activation stages staged so far
+    uint32_t xq = 0;            // tensor-core plans: activation stages (GLM: tiles) staged so far
     WIns I;
     fetch_init(I, P, myq);
     // the instruction's event waits (acquire), right before its activation is read
@@ -232,6 +242,18 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
                 continue;
             }
         }
+        if constexpr (FL == FL_GLMTC) {
+            if (opc == MK_OP_GLM_GEMM) {  // tensor-core tile: no slot hand-off, its input goes to an activation slot
+                if (!ab && !ins_valid<FL>(P, I)) {
+                    if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 1);
+                    ab = true;
+                }
+                wait_events(i, opc);
+                gt_stage_x(P, S, I, i, xq, ab);
+                if (lane == 0 && P.trace) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 11] = gtimer();
+                continue;
+            }
+        }
         if (!needs_handoff(P, I, decode(I), chain)) continue;  // same input as the previous slot: nothing to stage
         const int sl = hs & 1;
         const uint32_t use = hs >> 1;
@@ -245,7 +267,7 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
         int flags = 0;
         uint32_t tx = 0;  // bytes of bulk copies completing on the slot's full barrier
         if (GLM) {
-            if (opc == MK_OP_GLM_GEMM) {
+            if (FL == FL_GLM && opc == MK_OP_GLM_GEMM) {
                 // the tile's activation rows by bulk copies, unless the buffer
                 // already holds them (key: the input's device address)
                 const long long key = (long long)PTR(I, S_GG_XQ);
@@ -421,7 +443,7 @@ DEV bool gemv_dispatch(const KParams &P, const Smem S, const WIns &I, int i, int
 
 template <int MAXB, int FL>
 DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
-    constexpr bool GLM = FL == FL_GLM;
+    constexpr bool GLM = fl_glm(FL);
     const int ct = threadIdx.x - CONSUMER_BASE, lane = ct & 31;
     uint32_t ring = 0, cph = 0, ured = 0;
     uint32_t hs = 0;  // activation hand-offs so far (the activation loader counts the same ones)
@@ -447,7 +469,9 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         uint64_t t_start = 0;
         if (ct == 0 && P.trace) t_start = gtimer();
         // tensor-core tiles take no slot hand-off (their input streams into the activation ring)
-        const bool handoff = FL == FL_TC && is_gemv_op(opc) ? false : needs_handoff(P, I, d, chain);
+        const bool handoff =
+            (FL == FL_TC && is_gemv_op(opc)) || (FL == FL_GLMTC && opc == MK_OP_GLM_GEMM) ? false
+                                                                                         : needs_handoff(P, I, d, chain);
         const int sl = hs & 1;
         bool wrote = true;  // the warp wrote global memory in this slot
         if (handoff && !ab) ab = !warp_wait_bar(P, S, &S.act_full()[sl], (hs >> 1) & 1, 2, i, opc);
@@ -455,14 +479,18 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         const float *slot = reinterpret_cast<const float *>(S.act(sl));
         if constexpr (GLM) {  // GLM-block plans hold only GLM ops and counters
             if (opc == MK_OP_GLM_GEMM) {
-                if (d.nrows == 64) glm_gemm_task<64>(P, S, I, i, sl, ring, ured, ab);
-                else glm_gemm_task<16>(P, S, I, i, sl, ring, ured, ab);
+                if constexpr (FL == FL_GLMTC) {
+                    wrote = glm_tc_tile(P, S, I, i, ring, tc, ab);
+                } else {
+                    if (d.nrows == 64) glm_gemm_task<64>(P, S, I, i, sl, ring, ured, ab);
+                    else glm_gemm_task<16>(P, S, I, i, sl, ring, ured, ab);
+                }
                 rq.set(ring, P.num_pages);
             } else if (opc == MK_OP_GLM_A0 || opc == MK_OP_GLM_FIN) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // the slot holds nothing for these
                 if (opc == MK_OP_GLM_A0) glm_a0_task(P, S, I, i, ured, ab);
-                else glm_fin_task(P, I, ab);
+                else glm_fin_task<FL == FL_GLMTC>(P, I, ab);
             } else {  // COUNTER: the slot handshake only
                 consumer_sync(P, S, cph, ab, i);
                 __syncwarp();
@@ -536,12 +564,13 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
     S.o_bars = S.o_aux + P.aux_bytes;
     S.o_ctrl = S.o_bars + MBAR_BYTES;
     S.num_pages = P.num_pages;
-    constexpr bool TC = FL == FL_TC;
+    // tensor-core instances: the batched decoder's, the GLM block's with tcgen05 GEMM tiles
+    constexpr bool TC = FL == FL_TC || FL == FL_GLMTC;
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int p = 0; p < P.num_pages; ++p) {
             mbar_init(&S.full()[p], 1);
-            // tensor-core instance: one arrival, the MMA commit of a weight
+            // tensor-core plans: one arrival, the MMA commit of a weight
             // stage or the last of the 8 warps reading an attention page
             mbar_init(&S.empty()[p], TC ? 1 : CONSUMER_WARPS);
         }
@@ -553,9 +582,10 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
         if (TC) {
             for (int s = 0; s < TC_XSLOTS; ++s) {
                 mbar_init(&S.xfull()[s], 1);
-                mbar_init(&S.xempty()[s], 1);
+                // GLM tiles: the MMA commit and the four epilogue warps (done with the slot's scales)
+                mbar_init(&S.xempty()[s], FL == FL_GLMTC ? 1 + TC_EPI_WARPS : 1);
             }
-            for (int a = 0; a < 2; ++a) {
+            for (int a = 0; a < GT_NACC; ++a) {
                 mbar_init(&S.accfull()[a], 1);
                 mbar_init(&S.accempty()[a], TC_EPI_WARPS);
             }
@@ -570,6 +600,7 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
+    static_assert(GT_TMEM_COLS == TC_TMEM_COLS, "one TMEM allocation serves both tensor-core paths");
     if (TC && warp == 3) {  // the idle warp owns the TMEM accumulators
         tmem_alloc(S.tmem_slot(), TC_TMEM_COLS);
         tmem_relinquish();
@@ -621,7 +652,7 @@ int query_device(int *num_sms, int *smem_optin) {
 using KernelFn = void (*)(const KParams);
 
 static KernelFn pick_kernel(const Plan &p) {
-    if (p.kind == PLAN_GLM) return mk_interp<1, FL_GLM>;
+    if (p.kind == PLAN_GLM) return p.tc ? mk_interp<1, FL_GLMTC> : mk_interp<1, FL_GLM>;
     if (p.tc) return mk_interp<TC_MAXB, FL_TC>;
     const int B = p.B;
     if (B <= 1) return p.lean ? mk_interp<1, FL_LEAN> : mk_interp<1, FL_GEN>;
@@ -630,9 +661,14 @@ static KernelFn pick_kernel(const Plan &p) {
     return mk_interp<8, FL_GEN>;
 }
 
+static int encode_map(CUtensorMap *m, uint64_t base, uint64_t cols, uint64_t rows, uint32_t box_rows,
+                      bool bytes1);
+
 // Operand rows of the GLM block plan, in the planner's op order: A0,
-// QKV-A, Head-Gate, Indexer-K, FIN, Q-B, Indexer-Q.
-static int build_glm_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab) {
+// QKV-A, Head-Gate, Indexer-K, FIN, Q-B, Indexer-Q.  Tensor-core plans also
+// get the tensor maps: the five e4m3 weight matrices (boxes of 128 rows),
+// then A0's and FIN's activation codes (boxes of the 16 token rows).
+static int build_glm_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab, std::vector<CUtensorMap> &maps) {
     for (int b = MK_BIND_GLM_X; b <= MK_BIND_GLM_INDEX; ++b)
         if (!p.bind[b][0]) {
             char buf[96];
@@ -656,9 +692,35 @@ static int build_glm_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab) {
     r[S_GF_SB] = B(MK_BIND_GLM_SB); r[S_GF_LAT] = B(MK_BIND_GLM_LATENT); r[S_GF_IDX] = B(MK_BIND_GLM_INDEX);
     gemm(5, MK_BIND_GLM_W_QB, MK_BIND_GLM_S_QB, MK_BIND_GLM_QB, MK_BIND_GLM_SB, MK_BIND_GLM_Q);
     gemm(6, MK_BIND_GLM_W_IQ, MK_BIND_GLM_S_IQ, MK_BIND_GLM_QB, MK_BIND_GLM_SB, MK_BIND_GLM_IQ);
-    const uint64_t rope = (uint64_t)(uintptr_t)ws + p.ws.rope;
+    const uint64_t W = (uint64_t)(uintptr_t)ws;
+    const uint64_t rope = W + p.ws.rope;
     for (int o : {1, 2, 3, 5, 6}) row(o)[S_GG_ROPE] = rope;
     row(4)[S_GF_ROPE] = rope;
+    if (!p.tc) return MK_OK;
+    const mk_glm_desc &g = p.glm;
+    const int H = g.hidden, QL = g.q_lora, NQKVA = g.q_lora + g.kv_lora + g.rope;
+    const struct { int op, bind; uint64_t rows, cols; } mats[5] = {
+        {1, MK_BIND_GLM_W_QKVA, (uint64_t)NQKVA, (uint64_t)H},
+        {2, MK_BIND_GLM_W_GATE, (uint64_t)g.gate_heads, (uint64_t)H},
+        {3, MK_BIND_GLM_W_IK, (uint64_t)g.idx_dim, (uint64_t)H},
+        {5, MK_BIND_GLM_W_QB, (uint64_t)g.q_heads * g.q_head_dim, (uint64_t)QL},
+        {6, MK_BIND_GLM_W_IQ, (uint64_t)g.idx_heads * g.idx_dim, (uint64_t)QL},
+    };
+    maps.assign(GT_NTMAPS, CUtensorMap{});
+    auto tmap = [&](int idx) { return W + p.ws.tmaps + (uint64_t)idx * sizeof(CUtensorMap); };
+    for (int k = 0; k < 5; ++k) {
+        if (int rc = encode_map(&maps[k], B(mats[k].bind), mats[k].cols, mats[k].rows, GT_M, true)) return rc;
+        row(mats[k].op)[S_GG_TW] = tmap(k);
+        row(mats[k].op)[S_GG_TX] = tmap(mats[k].op <= 3 ? 5 : 6);
+    }
+    if (int rc = encode_map(&maps[5], B(MK_BIND_GLM_QA), H, GT_N, GT_N, true)) return rc;
+    if (int rc = encode_map(&maps[6], B(MK_BIND_GLM_QB), QL, GT_N, GT_N, true)) return rc;
+    for (int k = 0; k < 3; ++k) row(1 + k)[S_GG_FSUM] = W + p.ws.gsum[k];
+    // FIN rounds the sums: QKV-A (op 1) and Indexer-K (op 3) into their bf16
+    // outputs, Head-Gate (op 2) into its own
+    r = row(4);
+    r[S_GF_FQKVA] = W + p.ws.gsum[0]; r[S_GF_FGATE] = W + p.ws.gsum[1]; r[S_GF_FIK] = W + p.ws.gsum[2];
+    r[S_GF_GATE] = B(MK_BIND_GLM_GATE);
     return MK_OK;
 }
 
@@ -679,16 +741,20 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// A row-major bf16 matrix [rows, cols] read in boxes of 64 columns x
+// A row-major matrix [rows, cols] of bf16 (or, `bytes1`, of 1-byte e4m3
+// codes) read in boxes of 128 bytes of a row (64 bf16 / 128 codes) x
 // box_rows rows, landing 128-byte swizzled (the tiles' K-major layout).
-static int encode_map(CUtensorMap *m, uint64_t base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+// Rows past the end read as zeros.
+static int encode_map(CUtensorMap *m, uint64_t base, uint64_t cols, uint64_t rows, uint32_t box_rows,
+                      bool bytes1 = false) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return set_error(MK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)TC_BOX, box_rows};
+    const cuuint64_t strides[1] = {cols * (bytes1 ? 1 : 2)};
+    const cuuint32_t box[2] = {(cuuint32_t)(bytes1 ? GT_KS : TC_BOX), box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, reinterpret_cast<void *>(base), dims, strides, box,
+    const CUresult r = enc(m, bytes1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                           reinterpret_cast<void *>(base), dims, strides, box,
                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -728,7 +794,7 @@ static int build_tc_maps(Plan &p, uint8_t *ws, std::vector<CUtensorMap> &maps) {
 
 static int build_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab, std::vector<CUtensorMap> &maps) {
     tab.assign((size_t)p.num_ops * N_SLOTS, 0);
-    if (p.kind == PLAN_GLM) return build_glm_table(p, ws, tab);
+    if (p.kind == PLAN_GLM) return build_glm_table(p, ws, tab, maps);
     if (p.kind != PLAN_LLAMA) return MK_OK;
     const mk_model_desc &m = p.model;
     const int L = m.layers, B = p.B, Hkv = m.kv_heads, D = m.head_dim;
@@ -941,7 +1007,8 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
     if (dev < 0 || dev >= kMaxDevices) return set_error(MK_ERR_INVALID, "device ordinal out of range");
     if (configured_smem[dev] < p.smem_bytes) {
         for (KernelFn f : {mk_interp<1, FL_GEN>, mk_interp<2, FL_GEN>, mk_interp<4, FL_GEN>, mk_interp<8, FL_GEN>,
-                           mk_interp<1, FL_GLM>, mk_interp<1, FL_LEAN>, mk_interp<TC_MAXB, FL_TC>}) {
+                           mk_interp<1, FL_GLM>, mk_interp<1, FL_GLMTC>, mk_interp<1, FL_LEAN>,
+                           mk_interp<TC_MAXB, FL_TC>}) {
             e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         }

@@ -72,9 +72,39 @@ enum : int {
     P_GL_POS0 = W_P + 14,  // position of each request's first new token
     // A0 / FIN: P_ROW0 is the token row; FIN also:
     P_GF_QLORA = W_P + 1, P_GF_KVLORA = W_P + 2, P_GF_IDX = W_P + 3, P_GF_SLOTS = W_P + 4, P_GF_QKVA_LD = W_P + 5,
+    P_GF_SUMS = W_P + 6,   // FIN, tensor-core plans: 1 = the first GEMMs left fp32 sums; FIN rounds them
+                           // to bf16 (QKV-A, Indexer-K, Head-Gate outputs) and zeroes them
+    P_GF_GATE = W_P + 7,   // FIN: Head-Gate width
+    // tensor-core GEMM tiles (128 weight rows x the 16 token rows, see
+    // dev_glm_tc.cuh): P_ROW0 first weight row, P_NROWS rows stored (<= 128),
+    // P_K0 / P_KC the K range (multiples of 128), P_KTOT = K, P_NPG stages
+    // of 128 K, P_GL_ROPE bit j = rows 64 j .. 64 j + 63 are a RoPE slice,
+    // and:
+    P_GL_TCT = W_P + 15,     // 1: a tensor-core tile
+    P_GL_SUM = W_P + 16,     // 1: add the tile's fp32 part into the GEMM's sums (K split over tiles;
+                             // FIN rounds them), 0: store the bf16 outputs (with RoPE)
 };
 constexpr int GLM_MAX_M = 16;     // token rows of the GLM block (A fragments of m16n8k32)
 constexpr int GLM_ROPE = 64;      // width of a RoPE slice
+// GLM tensor-core tiles: tcgen05.mma kind::f8f6f4 (e4m3 x e4m3, fp32
+// accumulators in TMEM), M = 128 weight rows, N = 16 token rows, one stage =
+// one 128-wide K block of the block scales.
+constexpr int GT_M = 128;                        // weight rows per tile
+constexpr int GT_N = 16;                         // token rows (the MMA's N)
+constexpr int GT_KS = 128;                       // K per stage (e4m3 bytes of a row)
+constexpr int GT_STAGE_BYTES = GT_M * GT_KS;     // 16 KB of weights per stage = one page
+constexpr int GT_XSTAGE_BYTES = GT_N * GT_KS;    // 2 KB of activation codes per stage
+constexpr int GT_KSTEP = 32;                     // K of one kind::f8f6f4 MMA
+constexpr int GT_MAX_STAGES = 12;                // stages of one tile (its activation is staged whole)
+constexpr int GT_NACC = 4;                       // accumulators in flight (one per stage)
+constexpr int GT_ACC_COLS = 16;                  // TMEM columns of one accumulator
+constexpr int GT_TMEM_COLS = GT_NACC * GT_ACC_COLS;
+constexpr int GT_XSLOTS = 1;                     // activation slots: a worker's tiles are one per GEMM level,
+                                                 // and the levels are an event apart
+constexpr int GT_MAX_KB = 64;                    // K blocks of a GEMM's activation (hidden <= 8192)
+constexpr int GT_XSLOT_BYTES = GT_MAX_STAGES * GT_XSTAGE_BYTES + GT_N * GT_MAX_KB * 4;  // codes, then all scales
+constexpr int GT_EX_BYTES = GT_M * GT_N * 4;     // RoPE exchange of the epilogue warps
+constexpr int GT_NTMAPS = 7;                     // 5 weight matrices, 2 activations (A0 codes, FIN codes)
 
 // ---- operand table slots (16 x uint64 per op row) ------------------------
 enum : int {
@@ -96,7 +126,10 @@ enum : int {
     // GLM A0 / GEMM / FIN
     S_GA_X = 0, S_GA_RES = 1, S_GA_NORM = 2, S_GA_RES_OUT = 3, S_GA_QA = 4, S_GA_SA = 5,
     S_GG_W = 0, S_GG_SW = 1, S_GG_XQ = 2, S_GG_XS = 3, S_GG_OUT = 4, S_GG_ROPE = 5,
+    // tensor-core GEMM tiles: weight and activation tensor maps, fp32 sums [16][N] of K-split tiles
+    S_GG_TW = 6, S_GG_TX = 7, S_GG_FSUM = 8,
     S_GF_QKVA = 0, S_GF_IK = 1, S_GF_QB = 2, S_GF_SB = 3, S_GF_LAT = 4, S_GF_IDX = 5, S_GF_ROPE = 6,
+    S_GF_FQKVA = 7, S_GF_FIK = 8, S_GF_FGATE = 9, S_GF_GATE = 10,  // tensor-core plans: the sums, the gate output
     // NORM (tensor-core plans): residual fp32 [B, H], weight, bf16 high/low rows [2 NP, H],
     // qkv to zero, hidden capture
     S_N_H = 0, S_N_W = 1, S_N_XN = 2, S_N_QKV = 3, S_N_HIST = 4,
@@ -128,7 +161,8 @@ struct KParams {
     int nsteps;             // steps this launch runs (the queue is walked once per step)
     int num_pages, page_bytes, act_bytes, abuf_bytes, abuf_count, aux_bytes, red_bytes, smem_bytes;
     int B, H, Hq, Hkv, D, F, V, L, Smax, qk_norm, nsplit_max;
-    int np;                 // tensor-core plans: the batch padded to 8 or 16 (N = 2 np), else 0
+    int np;                 // tensor-core plans: the batch padded to 8 or 16 (N = 2 np), else 0;
+                            // GLM plans: 16 with tensor-core GEMM tiles, else 0
     float eps, theta;
 };
 
@@ -187,5 +221,6 @@ inline int red_bytes(int B) { return CONSUMER_WARPS * MAX_TILE_ROWS * B * 4; }
 inline int attn_aux_bytes(int G, int T, int D) { return (CONSUMER_WARPS * ((T + CONSUMER_WARPS / G - 1) / (CONSUMER_WARPS / G)) + 32 + 0 * D) * 4; }
 constexpr int MBAR_BYTES = 512;    // up to 64 mbarriers
 constexpr int CTRL_BYTES = 128;   // 32 flag words
-constexpr int MAX_PAGES = 26;      // 2 * MAX_PAGES + 9 mbarriers must fit MBAR_BYTES
+constexpr int MAX_PAGES = 26;      // 2 * MAX_PAGES + 5 mbarriers must fit MBAR_BYTES
+constexpr int MAX_PAGES_TC = 16;   // tensor-core plans: 2 * pages + 22 mbarriers
 }  // namespace mk

@@ -1237,26 +1237,47 @@ int plan_glm(const mk_glm_desc *g, const mk_target_desc *tgt, int num_workers, i
     if (g->pos0 + g->tokens > g->cache_slots) return set_error(MK_ERR_INVALID, "new tokens past the cache end");
     if (M > GLM_MAX_M || R != GLM_ROPE || H % 128 || QL % 128 || KL % 128 || H / 128 > 64 || QL / 128 > 16 ||
         g->q_head_dim % 64 || g->q_head_dim < 64 || g->idx_dim % 64 || g->idx_dim < 64 || NQKVA % 16 ||
-        g->gate_heads % 16 || g->idx_dim % 16 || H > 8192 || QL > 8192)
+        g->gate_heads % 16 || g->idx_dim % 16 || H > 8192 || QL > 8192 || KL > 2 * CONSUMERS ||
+        g->idx_dim - R > 2 * CONSUMERS || g->gate_heads > CONSUMERS)
         return set_error(MK_ERR_UNSUPPORTED, "GLM block sizes outside the kernels' tiling");
     if (tgt->schedule < MK_SCHED_DEFAULT || tgt->schedule > MK_SCHED_TIMED)
         return set_error(MK_ERR_INVALID, "schedule must be one of MK_SCHED_*");
     p.schedule = tgt->schedule == MK_SCHED_BYTES ? MK_SCHED_BYTES : MK_SCHED_TIMED;
     p.B = 1;  // the batch-1 kernel instance; the GLM ops take M from their payload
     p.max_steps = g->max_steps;
-    // shared memory: the staged A operand (M <= 16 padded rows of K bytes, then
-    // the scales), a 4 KB tile reduction area per buffer, pages of whole weight rows
-    const int KMAX = std::max(H, QL);
-    p.abuf_bytes = round_up(GLM_MAX_M * (KMAX + 16) + GLM_MAX_M * (KMAX / 128) * 4, 128);
-    p.abuf_count = 1;
-    p.act_bytes = 128;
-    p.red_bytes = 4096;
-    p.aux_bytes = NRED * p.red_bytes + 256;
-    p.page_bytes = 48 * 1024;  // 8 rows of K = 6144 or 32 rows of K = 1536
-    for (int K : {H, QL})
-        if (p.page_bytes % K) return set_error(MK_ERR_UNSUPPORTED, "a page must hold whole weight rows");
-    const int fixed = p.abuf_bytes + 2 * p.act_bytes + p.aux_bytes + MBAR_BYTES + CTRL_BYTES;
-    p.num_pages = std::min(MAX_PAGES, (smem_per_cta - fixed) / p.page_bytes);
+    // tcgen05 tiles: the 16 token rows are the MMA's N side; a second-level
+    // tile stages its whole K range of activation codes
+    const bool tc_shape = M == GT_N && QL / 128 <= GT_MAX_STAGES;
+    if (tgt->tc_tiles > 0 && !tc_shape)
+        return set_error(MK_ERR_UNSUPPORTED, "tensor-core GLM tiles need M = 16 and q_lora <= 1536");
+    p.tc = tgt->tc_tiles >= 0 && tc_shape;
+    p.np = p.tc ? GT_N : 0;
+    if (p.tc) {
+        // shared memory: two activation slots (a tile's codes in 2 KB stages,
+        // 1024-byte aligned for the 128-byte swizzle, then its scales), two
+        // 512-byte hand-off slots (A0 / FIN), the epilogue's RoPE exchange,
+        // 16 KB pages of one weight stage each
+        p.abuf_bytes = round_up(GT_XSLOT_BYTES, 1024);
+        p.abuf_count = GT_XSLOTS;
+        p.act_bytes = 512;
+        p.red_bytes = 256;
+        p.aux_bytes = NRED * p.red_bytes + GT_EX_BYTES + 256;
+        p.page_bytes = GT_STAGE_BYTES;
+    } else {
+        // shared memory: the staged A operand (M <= 16 padded rows of K bytes, then
+        // the scales), a 4 KB tile reduction area per buffer, pages of whole weight rows
+        const int KMAX = std::max(H, QL);
+        p.abuf_bytes = round_up(GLM_MAX_M * (KMAX + 16) + GLM_MAX_M * (KMAX / 128) * 4, 128);
+        p.abuf_count = 1;
+        p.act_bytes = 128;
+        p.red_bytes = 4096;
+        p.aux_bytes = NRED * p.red_bytes + 256;
+        p.page_bytes = 48 * 1024;  // 8 rows of K = 6144 or 32 rows of K = 1536
+        for (int K : {H, QL})
+            if (p.page_bytes % K) return set_error(MK_ERR_UNSUPPORTED, "a page must hold whole weight rows");
+    }
+    const int fixed = p.abuf_count * p.abuf_bytes + 2 * p.act_bytes + p.aux_bytes + MBAR_BYTES + CTRL_BYTES;
+    p.num_pages = std::min(p.tc ? MAX_PAGES_TC : MAX_PAGES, (smem_per_cta - fixed) / p.page_bytes);
     if (p.num_pages < 2) return set_error(MK_ERR_UNSUPPORTED, "shared memory holds fewer than two pages");
     p.smem_bytes = fixed + p.num_pages * p.page_bytes;
     // ops (operand rows): A0, QKV-A, Head-Gate, Indexer-K, FIN, Q-B, Indexer-Q
@@ -1302,22 +1323,72 @@ int plan_glm(const mk_glm_desc *g, const mk_target_desc *tgt, int num_workers, i
             pl[P_GL_ROPE - W_P] = head > 0 && n0 % head == head - GLM_ROPE ? 1 : 0;
         }
     };
-    gemm(OQKVA, NQKVA, H, 16, rpp_h, EV_A0, EV_B, NQKVA, 0);
-    gemm(OIK, g->idx_dim, H, 16, rpp_h, EV_A0, EV_B, g->idx_dim, 0);
-    gemm(OGATE, g->gate_heads, H, 16, rpp_h, EV_A0, EV_DONE, g->gate_heads, 0);
+    // tcgen05 tiles: 128 weight rows (the last row tile of a matrix may hold
+    // fewer; the tile reads zeros past the end) over P_NPG stages of 128 K;
+    // the first GEMMs split K into `ks` parts that add into fp32 sums (FIN
+    // rounds them), the second GEMMs store their bf16 outputs with RoPE on
+    // the 64-row halves that are a head's last 64 rows
+    auto gemm_tc = [&](int op, int N, int K, int ks, bool sums, int wait_ev, int sig_ev, int ld, int head) {
+        const int kc = K / ks;
+        for (int n0 = 0; n0 < N; n0 += GT_M) {
+            for (int part = 0; part < ks; ++part) {
+                const int nr = std::min(GT_M, N - n0);
+                TaskRec &t = add(op, MK_OP_GLM_GEMM, (int64_t)nr * kc, wait_ev, sig_ev);
+                t.bid[0] = n0 / GT_M;
+                t.bid[1] = part;
+                int32_t *pl = t.payload;
+                pl[P_ROW0 - W_P] = n0; pl[P_NROWS - W_P] = nr; pl[P_K0 - W_P] = part * kc; pl[P_KC - W_P] = kc;
+                pl[P_KTOT - W_P] = K; pl[P_OUT0 - W_P] = n0; pl[P_RPP - W_P] = 0; pl[P_NPG - W_P] = kc / GT_KS;
+                pl[P_GL_LD - W_P] = ld;
+                int rope = 0;
+                for (int j = 0; j < 2; ++j) {
+                    const int r = n0 + GLM_ROPE * j;
+                    if (head > 0 && r < N && r % head == head - GLM_ROPE) rope |= 1 << j;
+                }
+                pl[P_GL_ROPE - W_P] = rope;
+                pl[P_GL_TCT - W_P] = 1;
+                pl[P_GL_SUM - W_P] = sums ? 1 : 0;
+            }
+        }
+    };
+    if (p.tc) {
+        // K parts of the first GEMMs: the largest divisor of H / 128 that
+        // keeps row tiles x parts within the workers, with at most
+        // GT_MAX_STAGES stages per part
+        const int KB = H / GT_KS;
+        const int rt = ceil_div(NQKVA, GT_M) + ceil_div(g->gate_heads, GT_M) + ceil_div(g->idx_dim, GT_M);
+        int ks = 0;
+        for (int d = 1; d <= KB; ++d)
+            if (KB % d == 0 && KB / d <= GT_MAX_STAGES && (ks == 0 || rt * d <= num_workers)) ks = d;
+        p.glm_ksplit = ks;
+        // (Head-Gate's sums are rounded by FIN too, so its tiles count into FIN's event)
+        gemm_tc(OQKVA, NQKVA, H, ks, true, EV_A0, EV_B, NQKVA, 0);
+        gemm_tc(OIK, g->idx_dim, H, ks, true, EV_A0, EV_B, g->idx_dim, 0);
+        gemm_tc(OGATE, g->gate_heads, H, ks, true, EV_A0, EV_B, g->gate_heads, 0);
+    } else {
+        gemm(OQKVA, NQKVA, H, 16, rpp_h, EV_A0, EV_B, NQKVA, 0);
+        gemm(OIK, g->idx_dim, H, 16, rpp_h, EV_A0, EV_B, g->idx_dim, 0);
+        gemm(OGATE, g->gate_heads, H, 16, rpp_h, EV_A0, EV_DONE, g->gate_heads, 0);
+    }
     for (int m = 0; m < M; ++m) {
         TaskRec &t = add(OFIN, MK_OP_GLM_FIN, (int64_t)(NQKVA + g->idx_dim) * 2, EV_B, EV_FIN);
         t.bid[0] = m;
         int32_t *pl = t.payload;
         pl[P_ROW0 - W_P] = m; pl[P_GF_QLORA - W_P] = QL; pl[P_GF_KVLORA - W_P] = KL; pl[P_GF_IDX - W_P] = g->idx_dim;
         pl[P_GF_SLOTS - W_P] = g->cache_slots; pl[P_GF_QKVA_LD - W_P] = NQKVA;
+        pl[P_GF_SUMS - W_P] = p.tc ? 1 : 0; pl[P_GF_GATE - W_P] = g->gate_heads;
     }
     // the last tasks of a step (Head-Gate above, FIN's cache writes, Q-B,
     // Indexer-Q) count into the step-done event
     for (auto &t : p.tasks)
         if (t.opcode == MK_OP_GLM_FIN) { t.s_ev[t.ns] = EV_DONE; t.s_inc[t.ns++] = 1; p.thresholds[EV_DONE]++; }
-    gemm(OQB, NQ, QL, 64, rpp_q, EV_FIN, EV_DONE, NQ, g->q_head_dim);
-    gemm(OIQ, NI, QL, 64, rpp_q, EV_FIN, EV_DONE, NI, g->idx_dim);
+    if (p.tc) {
+        gemm_tc(OQB, NQ, QL, 1, false, EV_FIN, EV_DONE, NQ, g->q_head_dim);
+        gemm_tc(OIQ, NI, QL, 1, false, EV_FIN, EV_DONE, NI, g->idx_dim);
+    } else {
+        gemm(OQB, NQ, QL, 64, rpp_q, EV_FIN, EV_DONE, NQ, g->q_head_dim);
+        gemm(OIQ, NI, QL, 64, rpp_q, EV_FIN, EV_DONE, NI, g->idx_dim);
+    }
     if (NQ % 64 || NI % 64) return set_error(MK_ERR_UNSUPPORTED, "Q-B / Indexer-Q widths must be multiples of 64");
     for (auto &t : p.tasks) {
         for (int i = 0; i < t.nw; ++i) t.w_thr[i] = p.thresholds[t.w_ev[i]];

@@ -47,6 +47,7 @@ struct Plan {
     bool tc = false;    // GEMV tiles on tcgen05 tensor cores (the tensor-core kernel instance)
     int np = 0;         // tensor-core plans: batch padded to 8 or 16
     int ksplit_qkv = 1, ksplit_o = 1;
+    int glm_ksplit = 1;  // GLM tensor-core plans: K parts of the first GEMMs
     int page_bytes = 16384, act_bytes = 128, abuf_bytes = 128, abuf_count = 1, aux_bytes = 256, red_bytes = 128, num_pages = 2, smem_bytes = 0,
         nsplit_max = 1;
     std::vector<TaskRec> tasks;
@@ -66,6 +67,8 @@ struct Plan {
     struct {
         uint64_t err, counters, arrive, queue, optab, seq0, rope, hres, hmid, qkv, part, attn_out, act, trace, total;
         uint64_t xn, xo, act16, tmaps;  // tensor-core plans: bf16 high/low activations, tensor maps
+        uint64_t gsum[3];               // GLM tensor-core plans: fp32 sums of the K-split GEMMs
+                                        // (QKV-A, Head-Gate, Indexer-K)
     } ws{};
     void *uploaded_ws = nullptr;
     bool table_dirty = true;
