@@ -251,7 +251,7 @@ def cpu_oracle_rate(w, steps, warmup=0, device_for_inputs=None, nthreads=None):
     seq0 = synth.seq_lengths(w)
     dev = device_for_inputs or "cpu"
     wt = synth.make_weights(s, w.weight_seed, device=dev)
-    hw = {k: ([synth.to_host_u16(t) for t in v] if isinstance(v, list) else synth.to_host_u16(v)) for k, v in wt.items()}
+    hw = synth.host_weights(wt)
     del wt
     smax = max(seq0) + warmup + steps + 1
     dims = (s.L, w.batch, s.Hkv, smax, s.D)

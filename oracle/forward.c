@@ -20,7 +20,23 @@ typedef struct {
     const uint16_t *embed, *lm_head, *norm_final;
     const uint16_t *const *wq, *const *wk, *const *wv, *const *wo, *const *wg, *const *wu, *const *wd;
     const uint16_t *const *norm_attn, *const *norm_mlp, *const *qnorm, *const *knorm;
+    /* fp8 != 0: the seven projections are e4m3 codes w8[m][layer] [N][K]
+     * with fp32 scales s8[m][layer] [ceil(N/128)][K/128], m = q, k, v, o,
+     * gate, up, down (the bf16 pointers above are then unused) */
+    int fp8;
+    const uint8_t *const *w8[7];
+    const float *const *s8[7];
 } orc_weights;
+
+/* Value of an e4m3 ("fn") byte: sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; exponent field 0 is subnormal (m / 8 * 2^-6); S.1111.111 is
+ * NaN and there are no infinities (the OCP 8-bit floating point format). */
+double e4m3_to_double(uint8_t c) {
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
 
 double bf16_to_double(uint16_t u) {
     uint32_t bits = (uint32_t)u << 16;
@@ -82,3 +98,6 @@ void orc_attend(const double *q, const uint16_t *K, const uint16_t *V, int n, in
     free(scr);
 }
 void orc_to_bf16(const double *x, uint16_t *y, long n) { for (long i = 0; i < n; i++) y[i] = double_to_bf16(x[i]); }
+void orc_matvec8(const uint8_t *W, const float *S, int N, int K, const double *x, double *y) {
+    matvec8_f64(W, S, N, K, x, y, 1);
+}

@@ -48,7 +48,11 @@ _PP = C.POINTER(C.c_void_p)
 
 class _Weights(C.Structure):
     _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("norm_final", C.c_void_p)] + [
-        (n, _PP) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "norm_attn", "norm_mlp", "qnorm", "knorm")]
+        (n, _PP) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "norm_attn", "norm_mlp", "qnorm", "knorm")] + [
+        ("fp8", C.c_int), ("w8", _PP * 7), ("s8", _PP * 7)]
+
+
+PROJ = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")  # the seven projections, in the C oracle's matrix order
 
 
 def lib():
@@ -62,6 +66,9 @@ def lib():
         _lib.orc_rope.argtypes = [d, C.c_int, C.c_int, C.c_double]
         _lib.orc_attend.argtypes = [d, u16, u16, C.c_int, C.c_int, d]
         _lib.orc_to_bf16.argtypes = [d, u16, C.c_long]
+        _lib.orc_matvec8.argtypes = [C.POINTER(C.c_uint8), C.POINTER(C.c_float), C.c_int, C.c_int, d, d]
+        _lib.e4m3_to_double.argtypes = [C.c_uint8]
+        _lib.e4m3_to_double.restype = C.c_double
         _lib.bf16_to_double.argtypes = [C.c_uint16]
         _lib.bf16_to_double.restype = C.c_double
         for nm in ("orc_decode_step_f64", "orc_decode_step_f32"):
@@ -96,6 +103,24 @@ def matvec(W_bf16: np.ndarray, x: np.ndarray) -> np.ndarray:
     y = np.empty(N)
     lib().orc_matvec(_up(np.ascontiguousarray(W_bf16)), N, K, _dp(x), _dp(y))
     return y
+
+
+def matvec8(codes: np.ndarray, scales: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """y = W x for e4m3 codes [N, K] with fp32 scales [ceil(N/128), K/128] (one per 128 x 128 block)."""
+    N, K = codes.shape
+    assert K % 128 == 0
+    c = np.ascontiguousarray(codes, np.uint8)
+    sc = np.ascontiguousarray(scales, np.float32)
+    assert sc.shape == ((N + 127) // 128, K // 128)
+    x = np.ascontiguousarray(x, np.float64)
+    y = np.empty(N)
+    lib().orc_matvec8(c.ctypes.data_as(C.POINTER(C.c_uint8)), sc.ctypes.data_as(C.POINTER(C.c_float)), N, K,
+                      _dp(x), _dp(y))
+    return y
+
+
+def e4m3_value(code: int) -> float:
+    return lib().e4m3_to_double(code)
 
 
 def rope(v: np.ndarray, pos: int, theta: float) -> np.ndarray:
@@ -149,7 +174,9 @@ def decode_step(shape: Shape, w: Dict[str, object], kcache: np.ndarray, vcache: 
                 nthreads: Optional[int] = None, want_hidden: bool = True):
     """One decode step for all B sequences.  ``w`` maps names to uint16 arrays:
     embed [V,H], lm_head [V,H], norm_final [H], and per-layer lists wq, wk, wv,
-    wo, wg, wu, wd, norm_attn, norm_mlp (+ qnorm, knorm when qk_norm).
+    wo, wg, wu, wd, norm_attn, norm_mlp (+ qnorm, knorm when qk_norm).  With
+    ``w["fp8"]`` true the seven projection lists hold (e4m3 codes uint8 [N, K],
+    fp32 block scales [ceil(N/128), K/128]) pairs instead.
     ``kcache``/``vcache`` are uint16 [L, B, Hkv, Smax, D], appended in place.
     Returns (logits [B,V], hidden [L,B,H] or None, argmax [B])."""
     L, B = shape.L, len(tokens)
@@ -164,15 +191,29 @@ def decode_step(shape: Shape, w: Dict[str, object], kcache: np.ndarray, vcache: 
         a = np.ascontiguousarray(w[n])
         keep.append(a)
         setattr(ws, n, a.ctypes.data)
+    fp8 = bool(w.get("fp8", False))
+    ws.fp8 = int(fp8)
     for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "norm_attn", "norm_mlp", "qnorm", "knorm"):
         lst = w.get(n)
-        if lst is None:
+        if lst is None or (fp8 and n in PROJ):
             lst = [np.zeros(shape.D, np.uint16)] * L
         arrs = [np.ascontiguousarray(a) for a in lst]
         keep.append(arrs)
         p, t = _ptr_array(arrs)
         keep.append(t)
         setattr(ws, n, p)
+    if fp8:
+        for m, n in enumerate(PROJ):
+            codes = [np.ascontiguousarray(c, np.uint8) for c, _ in w[n]]
+            scales = [np.ascontiguousarray(sc, np.float32) for _, sc in w[n]]
+            for c, sc in zip(codes, scales):  # whole 128-wide column blocks, one scale per 128 x 128 block
+                assert c.shape[1] % 128 == 0 and sc.shape == ((c.shape[0] + 127) // 128, c.shape[1] // 128)
+            keep.append((codes, scales))
+            pc, tc = _ptr_array(codes)
+            psc, tsc = _ptr_array(scales)
+            keep.append((tc, tsc))
+            ws.w8[m] = pc
+            ws.s8[m] = psc
     dt = np.float64 if precision == 64 else np.float32
     logits = np.empty((B, shape.V), dt)
     hidden = np.empty((L, B, shape.H), dt) if want_hidden else None

@@ -6,7 +6,8 @@
  * at position pos[b] (0-based, equal to the number of cached tokens):
  *   h = E[token]
  *   per layer:  x = RMSNorm(h; w_attn)
- *               q, k, v = Wq x, Wk x, Wv x
+ *               q, k, v = Wq x, Wk x, Wv x   (projections bf16, or e4m3 with
+ *                                            128 x 128 block scales)
  *               [qk_norm] q_j = RMSNorm_D(q_j; w_q), k_g = RMSNorm_D(k_g; w_k)
  *               RoPE(q, k, pos)
  *               cache[pos] = bf16(k), bf16(v)
@@ -32,6 +33,21 @@ static void FN(matvec)(const uint16_t *W, int N, int K, const REAL *x, REAL *y, 
         const uint16_t *row = W + (size_t)n * K;
         REAL acc = 0;
         for (int k = 0; k < K; k++) acc += (REAL)bf16_to_double(row[k]) * x[k];
+        y[n] = acc;
+    }
+}
+
+/* FP8 weights: w[n][k] = e4m3 code x the fp32 scale of its 128 x 128 block
+ * (row block n / 128, column block k / 128) -- the block-scale convention of
+ * the "MegaRTP megakernel article", section 4 -- then the same dot product. */
+static void FN(matvec8)(const uint8_t *W, const float *S, int N, int K, const REAL *x, REAL *y, int nthreads) {
+    const int KB = K / 128;
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+    for (int n = 0; n < N; n++) {
+        const uint8_t *row = W + (size_t)n * K;
+        const float *srow = S + (size_t)(n / 128) * KB;
+        REAL acc = 0;
+        for (int k = 0; k < K; k++) acc += (REAL)(e4m3_to_double(row[k]) * (double)srow[k / 128]) * x[k];
         y[n] = acc;
     }
 }
@@ -68,6 +84,13 @@ static void FN(attend)(const REAL *q, const uint16_t *K, const uint16_t *V, int 
     }
 }
 
+/* A projection of layer l: matrix m (0 q, 1 k, 2 v, 3 o, 4 gate, 5 up, 6 down) in bf16 or fp8. */
+static void FN(project)(const orc_weights *w, int m, const uint16_t *const *bf, int l, int N, int K, const REAL *x,
+                        REAL *y, int nthreads) {
+    if (w->fp8) FN(matvec8)(w->w8[m][l], w->s8[m][l], N, K, x, y, nthreads);
+    else FN(matvec)(bf[l], N, K, x, y, nthreads);
+}
+
 static int FN(decode_step)(const orc_shape *sh, const orc_weights *w, uint16_t *kcache, uint16_t *vcache,
                            int B, int Smax, const int *pos, const int *tokens, int nthreads,
                            REAL *logits, REAL *hidden) {
@@ -85,9 +108,9 @@ static int FN(decode_step)(const orc_shape *sh, const orc_weights *w, uint16_t *
         for (int i = 0; i < H; i++) h[i] = (REAL)bf16_to_double(w->embed[(size_t)tokens[b] * H + i]);
         for (int l = 0; l < L; l++) {
             FN(rmsnorm)(h, H, w->norm_attn[l], sh->eps, x);
-            FN(matvec)(w->wq[l], Hq * D, H, x, q, nthreads);
-            FN(matvec)(w->wk[l], Hkv * D, H, x, k, nthreads);
-            FN(matvec)(w->wv[l], Hkv * D, H, x, v, nthreads);
+            FN(project)(w, 0, w->wq, l, Hq * D, H, x, q, nthreads);
+            FN(project)(w, 1, w->wk, l, Hkv * D, H, x, k, nthreads);
+            FN(project)(w, 2, w->wv, l, Hkv * D, H, x, v, nthreads);
             if (sh->qk_norm) {
                 for (int j = 0; j < Hq; j++) { FN(rmsnorm)(q + j * D, D, w->qnorm[l], sh->eps, tmp); memcpy(q + j * D, tmp, sizeof(REAL) * D); }
                 for (int g = 0; g < Hkv; g++) { FN(rmsnorm)(k + g * D, D, w->knorm[l], sh->eps, tmp); memcpy(k + g * D, tmp, sizeof(REAL) * D); }
@@ -109,16 +132,16 @@ static int FN(decode_step)(const orc_shape *sh, const orc_weights *w, uint16_t *
                 FN(attend)(q + j * D, kcache + base, vcache + base, p + 1, D, o + j * D, scr);
                 free(scr);
             }
-            FN(matvec)(w->wo[l], H, Hq * D, o, t1, nthreads);
+            FN(project)(w, 3, w->wo, l, H, Hq * D, o, t1, nthreads);
             for (int i = 0; i < H; i++) h[i] += t1[i];
             FN(rmsnorm)(h, H, w->norm_mlp[l], sh->eps, x);
-            FN(matvec)(w->wg[l], F, H, x, gt, nthreads);
-            FN(matvec)(w->wu[l], F, H, x, ut, nthreads);
+            FN(project)(w, 4, w->wg, l, F, H, x, gt, nthreads);
+            FN(project)(w, 5, w->wu, l, F, H, x, ut, nthreads);
             for (int i = 0; i < F; i++) {
                 REAL g = gt[i];
                 gt[i] = g / (1 + (REAL)exp(-(double)g)) * ut[i];
             }
-            FN(matvec)(w->wd[l], H, F, gt, t1, nthreads);
+            FN(project)(w, 6, w->wd, l, H, F, gt, t1, nthreads);
             for (int i = 0; i < H; i++) h[i] += t1[i];
             if (hidden) memcpy(hidden + ((size_t)l * B + b) * H, h, sizeof(REAL) * H);
         }

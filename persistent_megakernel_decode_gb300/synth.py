@@ -103,10 +103,28 @@ def _randn(shape, g, device, std=1.0):
     return t.to(torch.bfloat16)
 
 
-def make_weights(shape: ModelShape, seed: int, device="cpu", std: float = 0.02) -> Dict[str, object]:
+def quant_e4m3_blocks(w: torch.Tensor):
+    """FP8 weights from fp32 ones, the recipe the pages give for FP8 weights:
+    per 128 x 128 block scale = amax / 448 (1 for an all-zero block), codes
+    = e4m3 of w / scale (torch's float8_e4m3fn cast).  Returns (uint8 codes
+    [N, K], fp32 scales [ceil(N/128), K/128])."""
+    n, k = w.shape
+    nb = (n + 127) // 128
+    wp = torch.zeros((nb * 128, k), device=w.device)
+    wp[:n] = w
+    amax = wp.view(nb, 128, k // 128, 128).abs().amax(dim=(1, 3))
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).float()
+    q = (wp.view(nb, 128, k // 128, 128) / scale[:, None, :, None]).view(nb * 128, k)[:n]
+    return q.to(torch.float8_e4m3fn).view(torch.uint8).contiguous(), scale.contiguous()
+
+
+def make_weights(shape: ModelShape, seed: int, device="cpu", std: float = 0.02, fp8: bool = False) -> Dict[str, object]:
     """Weights in the usual [out_features, in_features] row-major layout.
     Per-layer tensors are lists indexed by layer.  With tied embeddings
-    ``lm_head`` is the same tensor as ``embed``."""
+    ``lm_head`` is the same tensor as ``embed``.  ``fp8``: the seven
+    projections are (e4m3 codes, 128 x 128 block scales) pairs drawn from
+    fp32 N(0, std) (``quant_e4m3_blocks``), and ``w["fp8"]`` is True; the
+    embedding, LM head and norm weights stay bf16."""
     g = torch.Generator(device=device).manual_seed(seed)
     s = shape
     w: Dict[str, object] = {"embed": _randn((s.V, s.H), g, device, std)}
@@ -114,20 +132,27 @@ def make_weights(shape: ModelShape, seed: int, device="cpu", std: float = 0.02) 
     if s.qk_norm:
         per["qnorm"], per["knorm"] = [], []
     ones_h = torch.ones(s.H, dtype=torch.bfloat16, device=device)
+
+    def proj(shp):
+        if not fp8:
+            return _randn(shp, g, device, std)
+        return quant_e4m3_blocks(torch.randn(shp, generator=g, device=device, dtype=torch.float32) * std)
+
     for _ in range(s.L):
-        per["wq"].append(_randn((s.Hq * s.D, s.H), g, device, std))
-        per["wk"].append(_randn((s.Hkv * s.D, s.H), g, device, std))
-        per["wv"].append(_randn((s.Hkv * s.D, s.H), g, device, std))
-        per["wo"].append(_randn((s.H, s.Hq * s.D), g, device, std))
-        per["wg"].append(_randn((s.F, s.H), g, device, std))
-        per["wu"].append(_randn((s.F, s.H), g, device, std))
-        per["wd"].append(_randn((s.H, s.F), g, device, std))
+        per["wq"].append(proj((s.Hq * s.D, s.H)))
+        per["wk"].append(proj((s.Hkv * s.D, s.H)))
+        per["wv"].append(proj((s.Hkv * s.D, s.H)))
+        per["wo"].append(proj((s.H, s.Hq * s.D)))
+        per["wg"].append(proj((s.F, s.H)))
+        per["wu"].append(proj((s.F, s.H)))
+        per["wd"].append(proj((s.H, s.F)))
         per["norm_attn"].append(ones_h.clone())
         per["norm_mlp"].append(ones_h.clone())
         if s.qk_norm:
             per["qnorm"].append(torch.ones(s.D, dtype=torch.bfloat16, device=device))
             per["knorm"].append(torch.ones(s.D, dtype=torch.bfloat16, device=device))
     w.update(per)
+    w["fp8"] = fp8
     w["norm_final"] = ones_h.clone()
     w["lm_head"] = w["embed"] if s.tied else _randn((s.V, s.H), g, device, std)
     return w
@@ -189,15 +214,7 @@ def make_glm_inputs(d: GlmDims, device="cpu", index: int = GLM_INDEX) -> Dict[st
     out["res"] = torch.randn((d.M, d.H), generator=ga).to(torch.bfloat16)
     out["norm"] = torch.ones(d.H, dtype=torch.bfloat16)
     for name, (n, k) in glm_mat_shapes(d).items():
-        w = torch.randn((n, k), generator=gw) * 0.02
-        nb = (n + 127) // 128
-        wp = torch.zeros((nb * 128, k))
-        wp[:n] = w
-        amax = wp.view(nb, 128, k // 128, 128).abs().amax(dim=(1, 3))
-        scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).float()
-        q = (wp.view(nb, 128, k // 128, 128) / scale[:, None, :, None]).view(nb * 128, k)[:n]
-        out["w_" + name] = q.to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
-        out["s_" + name] = scale.contiguous()
+        out["w_" + name], out["s_" + name] = quant_e4m3_blocks(torch.randn((n, k), generator=gw) * 0.02)
     out["latent"] = torch.randn((d.R, d.slots, d.kvlora + d.rope), generator=gc).to(torch.bfloat16)
     out["index"] = torch.randn((d.R, d.slots, d.idx_dim), generator=gc).to(torch.bfloat16)
     return {k: v.to(device) for k, v in out.items()}
@@ -206,3 +223,14 @@ def make_glm_inputs(d: GlmDims, device="cpu", index: int = GLM_INDEX) -> Dict[st
 def to_host_u16(t: torch.Tensor):
     """bf16 tensor -> numpy uint16 bit patterns (for the CPU checks)."""
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view("uint16")
+
+
+def host_weights(w: Dict[str, object]) -> Dict[str, object]:
+    """A ``make_weights`` dict on the host: bf16 tensors as uint16 bit
+    patterns, FP8 (codes, scales) pairs as (uint8, float32) arrays."""
+    def one(t):
+        if isinstance(t, tuple):
+            return (t[0].detach().contiguous().cpu().numpy(), t[1].detach().contiguous().cpu().numpy())
+        return to_host_u16(t)
+    return {k: ([one(t) for t in v] if isinstance(v, list) else v if isinstance(v, bool) else one(v))
+            for k, v in w.items()}

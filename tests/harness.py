@@ -29,10 +29,7 @@ HIDDEN_TOL = 1e-2
 
 
 def host_weights(w: Dict[str, object]) -> Dict[str, object]:
-    out = {}
-    for k, v in w.items():
-        out[k] = [synth.to_host_u16(t) for t in v] if isinstance(v, list) else synth.to_host_u16(v)
-    return out
+    return synth.host_weights(w)
 
 
 def oracle_shape(s: synth.ModelShape) -> orc.Shape:

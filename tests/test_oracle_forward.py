@@ -117,11 +117,10 @@ def test_attention_special_cases():
 
 # ---------------------------------------------------------------- whole step
 
-def _setup(B=1, pos=(5,), seed=0):
-    s = synth.TINY
+def _setup(B=1, pos=(5,), seed=0, s=synth.TINY):
     w = synth.make_weights(s, seed)
     kc, vc = synth.make_cache(s, B, 80, seed + 1)
-    host = {k: ([synth.to_host_u16(t) for t in v] if isinstance(v, list) else synth.to_host_u16(v)) for k, v in w.items()}
+    host = synth.host_weights(w)
     shape = orc.Shape(s.L, s.H, s.Hq, s.Hkv, s.D, s.F, s.V, s.qk_norm, s.eps, s.theta)
     return s, shape, host, synth.to_host_u16(kc).copy(), synth.to_host_u16(vc).copy()
 
@@ -205,7 +204,7 @@ def test_step_batch_independence_and_precisions():
 def test_qk_norm_path():
     s = synth.ModelShape(L=1, H=256, Hq=2, Hkv=1, D=128, F=64, V=64, eps=1e-6, theta=1e6, qk_norm=True, tied=False)
     w = synth.make_weights(s, 3)
-    host = {k: ([synth.to_host_u16(t) for t in v] if isinstance(v, list) else synth.to_host_u16(v)) for k, v in w.items()}
+    host = synth.host_weights(w)
     host["wo"] = [bf(np.eye(256))]
     host["wd"] = [np.zeros((256, 64), np.uint16)]
     host["qnorm"] = [bf(np.linspace(0.5, 1.5, 128))]
@@ -232,3 +231,93 @@ def test_qk_norm_path():
         qj = orc.rope(_rms(q[j * s.D:(j + 1) * s.D], s.eps) * f64(host["qnorm"][0]), pos, s.theta)
         ref = softmax(K @ qj / math.sqrt(s.D)) @ V
         assert np.allclose(o[j * s.D:(j + 1) * s.D], ref, rtol=1e-9, atol=1e-12)
+
+
+# ---------------------------------------------------------------- FP8 projections
+
+def _e4m3_codes(r, shape):
+    c = r.integers(0, 256, shape).astype(np.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x7E  # no NaN codes
+    return c
+
+
+def _e4m3_as_bf16(codes):
+    """The codes' values as bf16 bit patterns (torch's own e4m3 cast; every e4m3 value is exact in bf16)."""
+    return synth.to_host_u16(torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.bfloat16))
+
+
+def test_e4m3_decode_matches_torch_exhaustive():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([orc.e4m3_value(int(c)) for c in codes])
+    nan = np.isnan(ref)
+    assert nan.sum() == 2 and np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_matvec8_with_unit_scales_is_the_bf16_matvec():
+    r = np.random.default_rng(5)
+    N, K = 200, 384
+    codes = _e4m3_codes(r, (N, K))
+    x = r.standard_normal(K)
+    ones = np.ones(((N + 127) // 128, K // 128), np.float32)
+    assert np.array_equal(orc.matvec8(codes, ones, x), orc.matvec(_e4m3_as_bf16(codes), x))
+
+
+@pytest.mark.parametrize("rb,kb,sv", [(0, 2, 0.5), (1, 0, 2.0), (1, 2, 0.25)])
+def test_matvec8_block_scale_placement(rb, kb, sv):
+    """One nonzero block scale (power of two, so scaling is exact): rows outside
+    row block rb are zero; rows inside are sv x the bf16 matvec over column
+    block kb alone (a transposed or shifted scale index fails this)."""
+    r = np.random.default_rng(6)
+    N, K = 200, 384
+    codes = _e4m3_codes(r, (N, K))
+    x = r.standard_normal(K)
+    sc = np.zeros(((N + 127) // 128, K // 128), np.float32)
+    sc[rb, kb] = sv
+    y = orc.matvec8(codes, sc, x)
+    xk = np.zeros(K)
+    xk[kb * 128:(kb + 1) * 128] = x[kb * 128:(kb + 1) * 128]
+    rows = np.arange(N) // 128 == rb
+    assert (y[~rows] == 0).all()
+    assert np.array_equal(y[rows], sv * orc.matvec(_e4m3_as_bf16(codes), xk)[rows])
+
+
+def test_step_fp8_equals_the_bf16_step_on_the_same_values():
+    """A whole decode step with e4m3 projections and block scales 2^-6 (a
+    power of two: code x scale is exact in bf16) equals the bf16 step on the
+    dequantised weights, bit for bit (ffn 512: whole 128-wide blocks)."""
+    s, shape, w, kc, vc = _setup(s=synth.TINY_TC)
+    r = np.random.default_rng(7)
+    w8 = dict(w)
+    w8["fp8"] = True
+    for n in orc.PROJ:
+        pairs = []
+        for l in range(s.L):
+            N, K = w[n][l].shape
+            codes = _e4m3_codes(r, (N, K)) & 0xBF  # exponent field <= 7: values within +-1.875
+            pairs.append((codes, np.full(((N + 127) // 128, K // 128), 2.0 ** -6, np.float32)))
+            vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64) * 2.0 ** -6
+            w[n][l] = synth.to_host_u16(vals.to(torch.bfloat16))
+        w8[n] = pairs
+    kc2, vc2 = kc.copy(), vc.copy()
+    lb, hb, ab = orc.decode_step(shape, w, kc, vc, [5], [42])
+    l8, h8, a8 = orc.decode_step(shape, w8, kc2, vc2, [5], [42])
+    assert np.isfinite(lb).all() and np.abs(hb).max() < 1e3
+    assert np.array_equal(lb, l8) and np.array_equal(hb, h8) and np.array_equal(ab, a8)
+    assert np.array_equal(kc, kc2) and np.array_equal(vc, vc2)
+
+
+def test_fp8_weights_recipe():
+    """synth's FP8 projections: every block's largest code is +-448 (scale =
+    amax / 448) and code x scale reproduces N(0, 0.02)-sized weights."""
+    w = synth.make_weights(synth.TINY_TC, 11, fp8=True)
+    assert w["fp8"] is True
+    codes, scales = w["wq"][0]
+    v = torch.from_numpy(codes.numpy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    N, K = codes.shape
+    blocks = np.abs(v).reshape((N + 127) // 128, -1, K // 128, 128).max(axis=(1, 3)) if N % 128 == 0 else None
+    if blocks is not None:
+        assert (blocks == 448.0).all()
+    deq = v * np.repeat(np.repeat(scales.numpy(), 128, axis=0)[:N], 128, axis=1)
+    assert 0.015 < deq.std() < 0.025

@@ -74,6 +74,14 @@ MUTATIONS = {
     "final_norm": ("        FN(rmsnorm)(h, H, w->norm_final, sh->eps, x);\n        FN(matvec)(w->lm_head, V, H, x,",
                    "        memcpy(x, h, sizeof(REAL) * H);\n        FN(matvec)(w->lm_head, V, H, x,",
                    pins.test_step_with_zeroed_output_projections),
+    # FP8 block scales indexed [column block][row block]
+    "fp8_scale_transposed": ("(REAL)(e4m3_to_double(row[k]) * (double)srow[k / 128]) * x[k];",
+                             "(REAL)(e4m3_to_double(row[k]) * (double)S[(size_t)(k / 128) * KB + n / 128]) * x[k];",
+                             lambda: pins.test_matvec8_block_scale_placement(1, 0, 2.0)),
+    # FP8 projections: the up matrix used for the gate
+    "fp8_gate_matrix": ("FN(project)(w, 4, w->wg, l, F, H, x, gt, nthreads);",
+                        "FN(project)(w, 5, w->wg, l, F, H, x, gt, nthreads);",
+                        pins.test_step_fp8_equals_the_bf16_step_on_the_same_values),
 }
 
 
