@@ -43,9 +43,9 @@ MUTATIONS = {
     # SwiGLU without the SiLU
     "silu": ("gt[i] = g / (1 + (REAL)exp(-(double)g)) * ut[i];", "gt[i] = g * ut[i];", pins.test_step_mlp_block),
     # the attention output replacing the residual instead of adding to it
-    "residual": ("            FN(matvec)(w->wo[l], H, Hq * D, o, t1, nthreads);\n"
+    "residual": ("            FN(project)(w, 3, w->wo, l, H, Hq * D, o, t1, nthreads);\n"
                  "            for (int i = 0; i < H; i++) h[i] += t1[i];",
-                 "            FN(matvec)(w->wo[l], H, Hq * D, o, t1, nthreads);\n"
+                 "            FN(project)(w, 3, w->wo, l, H, Hq * D, o, t1, nthreads);\n"
                  "            for (int i = 0; i < H; i++) h[i] = t1[i];",
                  pins.test_step_attention_block_through_identity_output),
     # q normalised with the k-norm weights
