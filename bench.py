@@ -250,7 +250,7 @@ def cpu_oracle_rate(w, steps, warmup=0, device_for_inputs=None, nthreads=None):
     s = w.shape
     seq0 = synth.seq_lengths(w)
     dev = device_for_inputs or "cpu"
-    wt = synth.make_weights(s, w.weight_seed, device=dev)
+    wt = synth.make_weights(s, w.weight_seed, device=dev, fp8=w.fp8)
     hw = synth.host_weights(wt)
     del wt
     smax = max(seq0) + warmup + steps + 1
@@ -297,7 +297,7 @@ def run_mk(args, w, rank, world, dist):
     seq0 = synth.seq_lengths(w)
     steps_total = args.warmup + args.steps
     max_steps = max(w.steps, steps_total)
-    weights = synth.make_weights(s, w.weight_seed, device=dev)
+    weights = synth.make_weights(s, w.weight_seed, device=dev, fp8=w.fp8)
     smax = max(seq0) + max_steps + 1
     kc, vc = synth.make_cache(s, w.batch, smax, w.cache_seed, device=dev)
     stream = torch.cuda.Stream(dev)
@@ -372,9 +372,10 @@ def run_mk(args, w, rank, world, dist):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3 projections, bf16 LM head" if w.fp8 else "bf16", "accumulate": "f32",
+        "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seq_len, "layers": s.L, "hidden": s.H,
-                   "vocab": s.V, "mode": args.mode,
+                   "vocab": s.V, "mode": args.mode, "weights": "fp8 e4m3, 128x128 block scales" if w.fp8 else "bf16",
                    "l2": f"weights ({alg / 1e9:.2f} GB) exceed L2 (129 MB); no flush",
                    "parallelism": f"replicas{world}"},
         "step_us": {"median": float(np.median(step_ms)) * 1e3, "p10": float(np.percentile(step_ms, 10)) * 1e3,

@@ -83,6 +83,12 @@ typedef struct {
     int qk_norm;        /* per-head RMSNorm of q and k before RoPE (Qwen3-style) */
     float eps;          /* RMSNorm epsilon */
     float rope_theta;   /* RoPE base, rotate-half pairing (i, i + head_dim/2) */
+    int weight_fp8;     /* 1: the seven projections (Wq Wk Wv Wo Wg Wu Wd) are e4m3 codes, same
+                           [out, in] layout, with one fp32 scale per 128 x 128 block (MK_BIND_SQ ..
+                           MK_BIND_SD; the block-scale convention of the "MegaRTP megakernel article",
+                           section 4); the embedding, LM head and norms stay bf16.  Batch 1 with
+                           hidden = q_heads x head_dim = 2048, head_dim 64, ffn a multiple of 2048
+                           (MK_ERR_UNSUPPORTED otherwise) */
 } mk_model_desc;
 
 typedef struct {
@@ -129,19 +135,20 @@ typedef struct {
     uint64_t algorithmic_bytes_step; /* weights once + KV read + KV append, at step 0 */
     int tc_tiles;                    /* 1: the GEMV (GLM: FP8 GEMM) tiles run on tcgen05 tensor cores */
     int ksplit_qkv, ksplit_o;        /* tensor-core plans: K splits of the QKV and O tiles */
+    int weight_fp8;                  /* 1: the projections stream e4m3 rows */
 } mk_plan_info;
 
 /* ---- bindings: caller-owned device buffers ---- */
 #define MK_BIND_EMBED       0   /* bf16 [V, H] */
 #define MK_BIND_LM_HEAD     1   /* bf16 [V, H] (may be the embedding) */
 #define MK_BIND_NORM_FINAL  2   /* bf16 [H] */
-#define MK_BIND_WQ          3   /* per layer, bf16 [Hq*D, H] */
-#define MK_BIND_WK          4   /* per layer, bf16 [Hkv*D, H] */
-#define MK_BIND_WV          5   /* per layer, bf16 [Hkv*D, H] */
-#define MK_BIND_WO          6   /* per layer, bf16 [H, Hq*D] */
-#define MK_BIND_WG          7   /* per layer, bf16 [F, H] */
-#define MK_BIND_WU          8   /* per layer, bf16 [F, H] */
-#define MK_BIND_WD          9   /* per layer, bf16 [H, F] */
+#define MK_BIND_WQ          3   /* per layer, bf16 (e4m3 with weight_fp8) [Hq*D, H] */
+#define MK_BIND_WK          4   /* per layer, bf16 (e4m3 with weight_fp8) [Hkv*D, H] */
+#define MK_BIND_WV          5   /* per layer, bf16 (e4m3 with weight_fp8) [Hkv*D, H] */
+#define MK_BIND_WO          6   /* per layer, bf16 (e4m3 with weight_fp8) [H, Hq*D] */
+#define MK_BIND_WG          7   /* per layer, bf16 (e4m3 with weight_fp8) [F, H] */
+#define MK_BIND_WU          8   /* per layer, bf16 (e4m3 with weight_fp8) [F, H] */
+#define MK_BIND_WD          9   /* per layer, bf16 (e4m3 with weight_fp8) [H, F] */
 #define MK_BIND_NORM_ATTN  10   /* per layer, bf16 [H] */
 #define MK_BIND_NORM_MLP   11   /* per layer, bf16 [H] */
 #define MK_BIND_QNORM      12   /* per layer, bf16 [D] (qk_norm only) */
@@ -179,7 +186,16 @@ typedef struct {
 #define MK_BIND_GLM_IQ      42   /* bf16 [M, idx_heads, idx_dim]: out, Indexer-Q, last `rope` roped */
 #define MK_BIND_GLM_LATENT  43   /* bf16 [requests, cache_slots, kv_lora + rope]: latent cache */
 #define MK_BIND_GLM_INDEX   44   /* bf16 [requests, cache_slots, idx_dim]: index cache */
-#define MK_BIND_COUNT       45
+/* FP8 projections (weight_fp8): fp32 block scales [ceil(N/128), K/128] of
+ * the matrix [N, K] bound at MK_BIND_WQ + k, per layer */
+#define MK_BIND_SQ          45
+#define MK_BIND_SK          46
+#define MK_BIND_SV          47
+#define MK_BIND_SO          48
+#define MK_BIND_SG          49
+#define MK_BIND_SU          50
+#define MK_BIND_SD          51
+#define MK_BIND_COUNT       52
 
 /* Packed argmax key: (order-preserving bits of the fp32 logit << 32) |
  * (0xFFFFFFFF - index); the largest key is the largest logit, lowest index on

@@ -44,6 +44,7 @@ class Knobs:
     kchunk_down: int  # K extent of one down-projection tile
     rows_lm: int
     attn_split: int   # cache positions per attention task
+    wbytes: int = 2   # bytes per projection weight: 2 (bf16), 1 (e4m3); the LM head stays bf16
 
 
 def _ceil(a, b):
@@ -82,10 +83,12 @@ def llama_step_ops(shape: LlamaShape, k: Knobs, B: int, seq0: Sequence[int], max
         last_pos = seq0[b] + max_steps - 1          # cached rows at the last step
         return max(0, min(k.attn_split, last_pos - s * k.attn_split))
 
-    def rows_cost(n_rows, rows, kdim, mult=1):
+    wb = k.wbytes
+
+    def rows_cost(n_rows, rows, kdim, mult=1, wbytes=wb):
         def f(bid):
             r0 = bid[0] * rows
-            return mult * min(rows, n_rows - r0) * kdim * 2
+            return mult * min(rows, n_rows - r0) * kdim * wbytes
         return f
 
     ops: List[Op] = [Op("embed", (1, 1, 1), cost=lambda bid: B * shape.H * 2)]
@@ -95,11 +98,11 @@ def llama_step_ops(shape: LlamaShape, k: Knobs, B: int, seq0: Sequence[int], max
     for l in range(shape.L):
         qkv, attn, o, up, down = (f"{n}{l}" for n in ("qkv", "attn", "o", "up", "down"))
         ops.append(Op(qkv, (shape.Hkv, rows_group // k.rows_qkv, 1),
-                      cost=lambda bid: k.rows_qkv * shape.H * 2))
+                      cost=lambda bid: k.rows_qkv * shape.H * wb))
         ops.append(Op(attn, (shape.Hkv, B, ns_max), exists=lambda bid: bid[2] < nsplit[bid[1]],
                       cost=lambda bid: 2 * shape.D * 2 * attn_rows(bid)))
         ops.append(Op(o, (_ceil(shape.H, k.rows_o), 1, 1), cost=rows_cost(shape.H, k.rows_o, shape.Hq * shape.D)))
-        ops.append(Op(up, (shape.F // k.rows_up, 1, 1), cost=lambda bid: 2 * k.rows_up * shape.H * 2))
+        ops.append(Op(up, (shape.F // k.rows_up, 1, 1), cost=lambda bid: 2 * k.rows_up * shape.H * wb))
         ops.append(Op(down, (_ceil(shape.H, k.rows_down), shape.F // k.kchunk_down, 1),
                       cost=rows_cost(shape.H, k.rows_down, k.kchunk_down)))
         for n, kind in ((qkv, "qkv"), (attn, "attn"), (o, "o"), (up, "up"), (down, "down")):
@@ -115,7 +118,7 @@ def llama_step_ops(shape: LlamaShape, k: Knobs, B: int, seq0: Sequence[int], max
         # act [B, F]: up cuts F by tiles, down cuts F by K chunks
         edges.append(Edge(up, down, (1, -1, -1), (-1, 1, -1)))
         prev = down
-    ops.append(Op("lm", (_ceil(shape.V, k.rows_lm), 1, 1), cost=rows_cost(shape.V, k.rows_lm, shape.H)))
+    ops.append(Op("lm", (_ceil(shape.V, k.rows_lm), 1, 1), cost=rows_cost(shape.V, k.rows_lm, shape.H, wbytes=2)))
     kinds["lm"] = ("lm", -1)
     edges.append(Edge(prev, "lm", (1, -1, -1), (-1, -1, -1)))
     # the embed op writes all of h with one task: its out_map cuts nothing
@@ -128,8 +131,12 @@ def _round_up(x, a):
 
 
 def llama_knobs(shape: LlamaShape, B: int, seq0: Sequence[int], max_steps: int, n_workers: int,
-                smem_per_cta: int) -> Knobs:
+                smem_per_cta: int, fp8: bool = False) -> Knobs:
     """Tile knobs of a plan of GEMV tiles (batch 1..8), from the stated rules.
+
+    * FP8 projections (batch 1, every projection K = 2048): the same knobs as
+      bf16 (the row-per-warp tiles then hold 32 e4m3 rows per 64 KB page), one
+      byte per projection weight in the task costs.
 
     * Rows per tile: the most rows (a power of two) of K bf16 values that fit a
       64 KB tile (128 KB when every K is a multiple of 512 at batch above 1:
@@ -203,7 +210,7 @@ def llama_knobs(shape: LlamaShape, B: int, seq0: Sequence[int], max_steps: int, 
     mma_pages = mma and all(page // (2 * K) >= 8 and K % 512 == 0 for K in (H, Hq * D, kc))
     if B > 4 and not mma_pages:
         qkv, o, down, lm, up = min(qkv, 8), min(o, 8), min(down, 8), min(lm, 8), min(up, 4)
-    return Knobs(qkv, o, up, down, kc, lm, T)
+    return Knobs(qkv, o, up, down, kc, lm, T, 1 if fp8 else 2)
 
 
 @dataclass

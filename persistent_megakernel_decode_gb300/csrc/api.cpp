@@ -186,6 +186,7 @@ int mk_plan_info_get(mk_plan_t plan, mk_plan_info *info) {
     info->scratch_offset = p.kind == PLAN_LLAMA ? p.ws.hres : p.ws.total;
     info->algorithmic_bytes_step = (uint64_t)p.alg_bytes;
     info->tc_tiles = p.tc ? 1 : 0;
+    info->weight_fp8 = p.w8 ? 1 : 0;
     info->ksplit_qkv = p.ksplit_qkv;
     info->ksplit_o = p.ksplit_o;
     return MK_OK;
@@ -230,7 +231,7 @@ int mk_bind(mk_plan_t plan, int binding, int layer, uint64_t ptr) {
     Plan &p = plan->p;
     if (binding < 0 || binding >= MK_BIND_COUNT) return set_error(MK_ERR_INVALID, "unknown binding");
     if (ptr % 16) return set_error(MK_ERR_INVALID, "device pointers must be 16-byte aligned");
-    bool per_layer = binding >= MK_BIND_WQ && binding <= MK_BIND_KNORM;
+    bool per_layer = (binding >= MK_BIND_WQ && binding <= MK_BIND_KNORM) || (binding >= MK_BIND_SQ && binding <= MK_BIND_SD);
     if (per_layer && (layer < 0 || layer >= (int)p.bind[binding].size()))
         return set_error(MK_ERR_INVALID, "layer out of range");
     p.bind[binding][per_layer ? layer : 0] = ptr;

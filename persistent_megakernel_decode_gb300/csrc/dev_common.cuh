@@ -467,7 +467,9 @@ DEV int launch_slot(const KParams &P, const WIns &I, int i) { return (I.step - P
 // tiles all take the row-per-warp path and whose head_dim is 64 -- it holds
 // no other GEMV or attention variant, which keeps its registers free of
 // spills; FL_TC the batched decoder's tcgen05 instance.
-constexpr int FL_GEN = 0, FL_GLM = 1, FL_LEAN = 2, FL_TC = 3, FL_GLMTC = 4;
+// FL_W8 is the batch-1 instance of plans with FP8 projections (their e4m3
+// row-per-warp tiles, the bf16 LM head, attention at head_dim 64).
+constexpr int FL_GEN = 0, FL_GLM = 1, FL_LEAN = 2, FL_TC = 3, FL_GLMTC = 4, FL_W8 = 5;
 MK_HD constexpr bool fl_glm(int fl) { return fl == FL_GLM || fl == FL_GLMTC; }
 
 template <int FL>
@@ -534,6 +536,21 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
         const int ks = CONSUMER_WARPS / (nr / 8);
         if ((kc / 128 + ks - 1) / ks > 32) return false;
         return F(I, P_GL_LD) >= F(I, P_OUT0) + nr && F(I, P_OUT0) >= 0 && (F(I, P_GL_ROPE) == 0 || nr == 64);
+    }
+    if (FL != FL_W8 && F(I, P_W8) != 0) return false;  // FP8 tiles run in their instance only
+    if (FL == FL_W8 && opc >= MK_OP_QKV && opc <= MK_OP_LM && opc != MK_OP_ATTN && F(I, P_W8) != 0) {
+        // FP8 tile: pages of 32 rows of K = 2048 (MLP-up 16 gate + 16 up), one page of up to 32 rows
+        // (O 16, MLP-up exactly 16 gate rows) or whole pages, rows in one 128-row block
+        if (P.B != 1 || opc == MK_OP_LM || F(I, P_W8) != 1) return false;
+        const int nrows = F(I, P_NROWS), npg = F(I, P_NPG), row0 = F(I, P_ROW0);
+        const bool up = opc == MK_OP_UP;
+        const int rows = (up ? 2 : 1) * nrows;
+        if (F(I, P_KC) != W8_K || P.page_bytes != W8_ROWS * W8_K || F(I, P_RPP) != W8_ROWS || nrows <= 0 ||
+            npg != (rows + W8_ROWS - 1) / W8_ROWS || npg > 64 || row0 < 0 || row0 / 128 != (row0 + nrows - 1) / 128)
+            return false;
+        if (up) return nrows % 16 == 0;
+        if (opc == MK_OP_O) return npg == 1 && nrows <= RESID_ROWS;
+        return npg == 1 || nrows > W8_ROWS * (npg - 1);
     }
     if (opc >= MK_OP_QKV && opc <= MK_OP_LM && opc != MK_OP_ATTN) {
         const int nrows = F(I, P_NROWS), kc = F(I, P_KC);
@@ -604,7 +621,8 @@ DEV int describe(const KParams &P, const WIns &I, Seg &s0, Seg &s1) {
     const int opc = F(I, W_OPC);
     if (opc == MK_OP_QKV || opc == MK_OP_O || opc == MK_OP_DOWN || opc == MK_OP_LM || opc == MK_OP_UP) {
         const long long ktot = F(I, P_KTOT);
-        const long long off = ((long long)F(I, P_ROW0) * ktot + F(I, P_K0)) * 2;
+        const int eb = FL == FL_W8 && F(I, P_W8) != 0 ? 1 : 2;  // bytes per weight: e4m3 or bf16
+        const long long off = ((long long)F(I, P_ROW0) * ktot + F(I, P_K0)) * eb;
         const int slot = opc == MK_OP_QKV ? S_QKV_WQ + F(I, P_MAT)
                        : opc == MK_OP_O   ? S_O_W
                        : opc == MK_OP_DOWN ? S_DN_W
@@ -612,8 +630,8 @@ DEV int describe(const KParams &P, const WIns &I, Seg &s0, Seg &s1) {
                                           : S_UP_WG;
         s0.src = reinterpret_cast<const uint8_t *>(PTR(I, slot)) + off;
         s0.rows = F(I, P_NROWS);
-        s0.row_bytes = F(I, P_KC) * 2;
-        s0.stride = ktot * 2;
+        s0.row_bytes = F(I, P_KC) * eb;
+        s0.stride = ktot * eb;
         if (opc != MK_OP_UP) return 1;
         s1 = s0;
         s1.src = reinterpret_cast<const uint8_t *>(PTR(I, S_UP_WU)) + off;

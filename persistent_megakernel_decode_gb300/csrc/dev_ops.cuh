@@ -10,6 +10,8 @@
 // attention task's activation stage instead of the QKV epilogue, because a
 // QKV tile holds 16 rows of a head and RoPE pairs dimension i with i + D/2.
 #pragma once
+#include <cuda_fp16.h>
+
 #include <type_traits>
 
 #include "dev_common.cuh"
@@ -35,8 +37,24 @@ DEV int rpw_perm4(int q) {
     const int c = q >> 1;
     return (((c >> 5) << 1) + (q & 1)) * 32 + (c & 31);
 }
+// FP8 row-per-warp tiles read x as 16-wide chunks c = lane + 32 k, four
+// float4 per chunk: float4 q (chunk q / 4, quarter q % 4) goes to position
+// ((k * 4 + quarter) * 32 + lane).
+DEV int rpw_perm8(int q) {
+    const int c = q >> 2;
+    return (((c >> 5) << 2) + (q & 3)) * 32 + (c & 31);
+}
+// Staging position of float4 q: natural order, or one of the two lane-interleaved orders.
+template <bool P8>
+DEV int stage_pos(int q, bool perm, bool perm8) {
+    if constexpr (P8) {
+        if (perm8) return rpw_perm8(q);
+    }
+    return perm ? rpw_perm4(q) : q;
+}
 
-DEV void stage_copy(const float4 *s4, float4 *d4, int n4, bool perm) {
+template <bool P8 = false>
+DEV void stage_copy(const float4 *s4, float4 *d4, int n4, bool perm, bool perm8 = false) {
     const int lane = threadIdx.x & 31;
     for (int base = 0; base < n4; base += 32 * SC) {
         float4 v[SC];
@@ -48,13 +66,14 @@ DEV void stage_copy(const float4 *s4, float4 *d4, int n4, bool perm) {
 #pragma unroll
         for (int j = 0; j < SC; ++j) {
             const int k = base + lane + 32 * j;
-            if (k < n4) d4[perm ? rpw_perm4(k) : k] = v[j];
+            if (k < n4) d4[stage_pos<P8>(k, perm, perm8)] = v[j];
         }
     }
 }
 
-template <int MAXB>
-DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab, bool perm) {
+// P8 (the FP8 instance): `perm8` stages x in the FP8 tiles' order (rpw_perm8).
+template <int MAXB, bool P8 = false>
+DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab, bool perm, bool perm8 = false) {
     const int lane = threadIdx.x & 31;
     const int opc = F(I, W_OPC);
     const int B = P.B;
@@ -89,7 +108,7 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab, bool 
                     const int k = base + lane + 32 * j;
                     if (k < n4) {
                         ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
-                        if (!one_round) dst[perm ? rpw_perm4(k) : k] = v[j];
+                        if (!one_round) dst[stage_pos<P8>(k, perm, perm8)] = v[j];
                         if (hs) hs[k] = v[j];
                     }
                 }
@@ -107,7 +126,7 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab, bool 
 #pragma unroll
                 for (int j = 0; j < SC; ++j) {
                     const int k = lane + 32 * j;
-                    if (k < n4) dst[perm ? rpw_perm4(k) : k] = norm(v[j], ww[j]);
+                    if (k < n4) dst[stage_pos<P8>(k, perm, perm8)] = norm(v[j], ww[j]);
                 }
             } else {
                 __syncwarp();
@@ -121,7 +140,7 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab, bool 
                     for (int j = 0; j < SC; ++j) {
                         const int k = base + lane + 32 * j;
                         if (k < n4) {
-                            const int q = perm ? rpw_perm4(k) : k;
+                            const int q = stage_pos<P8>(k, perm, perm8);
                             dst[q] = norm(dst[q], ww[j]);
                         }
                     }
@@ -140,8 +159,8 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab, bool 
             ld = (size_t)P.F;
         }
         for (int b = 0; b < B; ++b)
-            stage_copy(reinterpret_cast<const float4 *>(src + b * ld), reinterpret_cast<float4 *>(abuf + (size_t)b * kc),
-                       kc / 4, perm);
+            stage_copy<P8>(reinterpret_cast<const float4 *>(src + b * ld),
+                           reinterpret_cast<float4 *>(abuf + (size_t)b * kc), kc / 4, perm, perm8);
     }
 }
 
@@ -750,9 +769,11 @@ struct HandoffChain {
     int prev = 0;  // this lane's word of the previous slot
     bool valid = false;
 };
+template <int FL>
 DEV bool needs_handoff(const KParams &P, const WIns &I, const Dec &d, HandoffChain &c) {
     const int lane = threadIdx.x & 31;
-    const bool rpw = rpw_tile(P, d);
+    // (the FP8 instance: its e4m3 tiles hold x in registers the same way)
+    const bool rpw = (FL == FL_W8 && F(I, P_W8) != 0) || rpw_tile(P, d);
     const bool input_word = lane == W_OPC || lane == W_ROW || lane == W_CNT ||
                             (lane >= W_WAIT && lane < W_SIG) || lane == P_K0 || lane == P_KC;
     const bool same = c.valid && !__any_sync(FULL, input_word && I.w != c.prev);
@@ -922,6 +943,122 @@ DEV bool gemv_rpw(const KParams &P, const Smem S, const Dec &d, int i, bool hand
             red_max_u64(reinterpret_cast<unsigned long long *>(d.out2) + (size_t)d.step, key);
         }
     }
+    trace_stamp(P, i, 9);
+    return true;
+}
+
+// ---------------------------------------------------------------- batch 1, FP8 rows per warp
+// FP8 projections (e4m3 rows of K = 2048, one fp32 scale per 128 x 128
+// block): pages of 32 rows (MLP-up: 16 gate rows, then their 16 up rows),
+// warp w takes rows w, w + 8, w + 16, w + 24 of every page over the whole K.
+// Lane l holds x's 16-wide chunks c = l + 32 k (k < 4; x staged in that
+// order, rpw_perm8) in registers, and the scale of each chunk's 128-column
+// block -- a tile's rows lie in one 128-row block, so four scales per matrix
+// and lane serve the whole tile.  Each chunk: 16 codes to fp32 pairs
+// (cvt.rn.f16x2.e4m3x2, exact), 8 packed multiply-adds into a partial, the
+// partial times its block scale into the row sum.
+DEV uint64_t e4m3x2_pair(uint32_t v) {  // codes in the low 16 bits, the first in the low byte
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)(v & 0xffffu)));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    return pack2(f.x, f.y);
+}
+DEV void rpw8_row(const uint8_t *wrow, int lane, const XRow &x, const float (&sc)[4], uint64_t &acc) {
+#pragma unroll
+    for (int k = 0; k < W8_K / 512; ++k) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(wrow + (lane + 32 * k) * 16);
+        uint64_t part = 0;
+        fma2(part, e4m3x2_pair(w.x), x.v[2 * k][0]);
+        fma2(part, e4m3x2_pair(w.x >> 16), x.v[2 * k][1]);
+        fma2(part, e4m3x2_pair(w.y), x.v[2 * k][2]);
+        fma2(part, e4m3x2_pair(w.y >> 16), x.v[2 * k][3]);
+        fma2(part, e4m3x2_pair(w.z), x.v[2 * k + 1][0]);
+        fma2(part, e4m3x2_pair(w.z >> 16), x.v[2 * k + 1][1]);
+        fma2(part, e4m3x2_pair(w.w), x.v[2 * k + 1][2]);
+        fma2(part, e4m3x2_pair(w.w >> 16), x.v[2 * k + 1][3]);
+        fma2(acc, part, pack2(sc[k], sc[k]));
+    }
+}
+// This lane's four chunk scales of a matrix for the tile (row block row0 / 128).
+DEV void rpw8_scales(const float *s, int row0, int k0, int ktot, int lane, float (&sc)[4]) {
+    const float *srow = s + (size_t)(row0 / 128) * (ktot / 128) + k0 / 128;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sc[k] = __ldg(srow + (lane + 32 * k) / 8);
+}
+
+DEV bool gemv_rpw8(const KParams &P, const Smem S, const WIns &I, const Dec &d, int i, bool handoff, int sl,
+                   const float *slot, XRow &x, uint32_t &ring, RingPos &rq, bool &ab) {
+    const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
+    const int opc = d.opc, npg = d.npg, nrows = d.nrows, out0 = d.out0;
+    const bool up = opc == MK_OP_UP;
+    // block scales: the tile's matrix (QKV: its q, k or v matrix; MLP-up: gate, then up)
+    const int row0 = F(I, P_ROW0), ktot = F(I, P_KTOT), mat = opc == MK_OP_QKV ? F(I, P_MAT) : 0;
+    const float *s0 = reinterpret_cast<const float *>(PTR(I, S_W8_S0 + mat));
+    const float *s1 = reinterpret_cast<const float *>(PTR(I, S_W8_S1));
+    float sa[4], sb[4];
+    rpw8_scales(s0, row0, d.k0, ktot, lane, sa);
+    if (up) rpw8_scales(s1, row0, d.k0, ktot, lane, sb);
+    float resid = 0.f;  // O tiles (one page): the residual of this lane's row w + 8 (lane / 8)
+    if (handoff) {
+        const long long key = ((long long)d.row << 32) | (uint32_t)d.k0 | (1ll << 61);  // (FP8 layout)
+        if (key != x.key) {
+            const float4 *xs = reinterpret_cast<const float4 *>(S.abuf(sl));  // lane-interleaved (rpw_perm8)
+#pragma unroll
+            for (int k = 0; k < W8_K / 512; ++k)
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float4 a = xs[(4 * k + h) * 32 + lane];
+                    x.v[2 * k + (h >> 1)][(h & 1) * 2] = pack2(a.x, a.y);
+                    x.v[2 * k + (h >> 1)][(h & 1) * 2 + 1] = pack2(a.z, a.w);
+                }
+            x.key = key;
+        }
+        if (opc == MK_OP_O) {
+            const int r = warp + 8 * (lane >> 3);
+            if (r < RESID_ROWS) resid = slot_resid(P, const_cast<float *>(slot))[r];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.act_empty()[sl]);  // x and the residual rows are in registers
+    }
+    trace_stamp(P, i, 6);
+    float *const out = reinterpret_cast<float *>(d.out);
+    for (int pg = 0; pg < npg; ++pg) {
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[rq.p], rq.ph, 2, i, opc);
+        if (pg == 0) trace_stamp(P, i, 7);
+        const uint8_t *page = S.pages() + (size_t)rq.p * P.page_bytes;
+        uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)  // MLP-up: rows 0..15 gate (j 0, 1), 16..31 up (j 2, 3)
+            rpw8_row(page + (size_t)(warp + 8 * j) * W8_K, lane, x, up && j >= 2 ? sb : sa, acc[j]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty()[rq.p]);
+        rq.next(P.num_pages);
+        float y[4] = {sum2(acc[0]), sum2(acc[1]), sum2(acc[2]), sum2(acc[3])};
+        Bfly<4, 16>::run(y, lane);  // lanes 8 j .. 8 j + 7: row w + 8 j of the page
+        const float val = y[0];
+        const int j = lane >> 3;
+        const bool holder = (lane & 7) == 0;
+        if (up) {
+            // gate row 16 pg + w + 8 j (j 0, 1) and its up row (page row 16 + w + 8 j: lane 8 j + 16)
+            const float u = __shfl_sync(FULL, val, (lane + 16) & 31);
+            const int r = 16 * pg + warp + 8 * j;
+            if (holder && j < 2 && !ab && r < nrows) out[out0 + r] = val / (1.0f + __expf(-val)) * u;
+            continue;
+        }
+        const int r = W8_ROWS * pg + warp + 8 * j;
+        const bool mine = holder && !ab && r < nrows;
+        if (opc == MK_OP_QKV) {
+            if (mine) out[out0 + r] = val;
+        } else if (opc == MK_OP_O) {
+            if (mine) {
+                out[out0 + r] = resid + val;
+                reinterpret_cast<float *>(d.out2)[out0 + r] = resid + val;
+            }
+        } else {  // MLP-down K chunk
+            if (mine) atomicAdd(out + out0 + r, val);
+        }
+    }
+    ring += npg;
     trace_stamp(P, i, 9);
     return true;
 }

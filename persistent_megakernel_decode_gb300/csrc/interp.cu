@@ -99,6 +99,8 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
         }
         Seg s0, s1;
         const int nseg = describe<FL>(P, I, s0, s1);
+        // MLP-up pages: groups of 8 gate + 8 up rows (bf16), 16 + 16 (FP8 rows, 32 to a page)
+        const int upg = FL == FL_W8 && F(I, P_W8) != 0 ? W8_ROWS / 2 : 8;
         if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 4] = gtimer();
         // Rows go to pages in order, as many whole rows per page as fit.  The
         // two segments of an MLP-up tile share pages in groups of up to 8:
@@ -144,7 +146,7 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
                     if (nseg == 1) {
                         copy_rows(s0, r, nr, dst, bar);
                     } else {
-                        const int gs = min(8, n0);  // group size; n0 is a multiple of 8 when above 8
+                        const int gs = min(upg, n0);  // group size; n0 is a multiple of it when above it
                         for (int j = r; j < r + nr;) {
                             const int g = j / (2 * gs), w = j % (2 * gs);
                             const bool up = w >= gs;
@@ -254,7 +256,7 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
                 continue;
             }
         }
-        if (!needs_handoff(P, I, decode(I), chain)) continue;  // same input as the previous slot: nothing to stage
+        if (!needs_handoff<FL>(P, I, decode(I), chain)) continue;  // same input as the previous slot: nothing to stage
         const int sl = hs & 1;
         const uint32_t use = hs >> 1;
         if (!ab && !ins_valid<FL>(P, I)) {
@@ -280,7 +282,7 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
             }
         } else if (opc == MK_OP_ATTN) {
             const bool g4 = P.Hq <= 4 * P.Hkv;
-            if (FL == FL_LEAN || P.D == 64)
+            if (FL == FL_LEAN || FL == FL_W8 || P.D == 64)
                 g4 ? stage_attn<64, 4>(P, I, slot, ab, rope64) : stage_attn<64, 8>(P, I, slot, ab, rope64);
             else g4 ? stage_attn<128, 4>(P, I, slot, ab, rope128) : stage_attn<128, 8>(P, I, slot, ab, rope128);
             flags = SLOT_FRESH;
@@ -293,12 +295,14 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
             // batch-1 row-per-warp tiles read x lane-interleaved (rpw_perm4);
             // the layout is part of what a buffer holds
             const Dec dd = decode(I);
-            const bool perm = MAXB == 1 && (rpw_tile(P, dd) || (FL != FL_LEAN && rpw_wide_tile(P, dd)));
-            const long long key = ((long long)F(I, W_ROW) << 32) | (uint32_t)F(I, P_K0) | ((long long)perm << 62);
+            const bool perm8 = FL == FL_W8 && F(I, P_W8) != 0;  // FP8 tiles' order (their instance only)
+            const bool perm = !perm8 && MAXB == 1 && (rpw_tile(P, dd) || (FL != FL_LEAN && FL != FL_W8 && rpw_wide_tile(P, dd)));
+            const long long key = ((long long)F(I, W_ROW) << 32) | (uint32_t)F(I, P_K0) | ((long long)perm << 62) |
+                                  ((long long)perm8 << 61);
             if (key != (bi ? key1 : key0) || F(I, P_SNAP) > 0) {
                 if (!two_bufs && hs > 0 && !ab)
                     ab = !warp_wait_bar(P, S, &S.act_empty()[(hs - 1) & 1], ((hs - 1) >> 1) & 1, 1, i, opc);
-                stage_gemv<MAXB>(P, I, S.abuf(bi), ab, perm);
+                stage_gemv<MAXB, FL == FL_W8>(P, I, S.abuf(bi), ab, perm, perm8);
                 flags = SLOT_FRESH;
             }
             if (opc == MK_OP_O) stage_resid(P, I, slot);
@@ -471,7 +475,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         // tensor-core tiles take no slot hand-off (their input streams into the activation ring)
         const bool handoff =
             (FL == FL_TC && is_gemv_op(opc)) || (FL == FL_GLMTC && opc == MK_OP_GLM_GEMM) ? false
-                                                                                         : needs_handoff(P, I, d, chain);
+                                                                                         : needs_handoff<FL>(P, I, d, chain);
         const int sl = hs & 1;
         bool wrote = true;  // the warp wrote global memory in this slot
         if (handoff && !ab) ab = !warp_wait_bar(P, S, &S.act_full()[sl], (hs >> 1) & 1, 2, i, opc);
@@ -498,7 +502,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
                 wrote = false;
             }
         } else if (opc == MK_OP_ATTN) {
-            if (FL == FL_LEAN || P.D == 64) attn_task<64, FL>(P, S, I, i, sl, slot, ring, ab);
+            if (FL == FL_LEAN || FL == FL_W8 || P.D == 64) attn_task<64, FL>(P, S, I, i, sl, slot, ring, ab);
             else attn_task<128, FL>(P, S, I, i, sl, slot, ring, ab);
             rq.set(ring, P.num_pages);
         } else if (FL == FL_TC && is_gemv_op(opc)) {
@@ -511,6 +515,8 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         } else if (opc == MK_OP_EMBED) {
             consumer_sync(P, S, cph, ab, i);
             embed_task(P, S, I, i, sl, ab);
+        } else if (FL == FL_W8 && opc >= MK_OP_QKV && F(I, P_W8) != 0) {
+            if constexpr (FL == FL_W8) wrote = gemv_rpw8(P, S, I, d, i, handoff, sl, slot, x, ring, rq, ab);
         } else if (opc >= MK_OP_QKV) {
             if constexpr (FL != FL_TC) {  // (the tensor-core instance took its GEMV tiles above)
                 if (MAXB == 1 && rpw_tile(P, d)) {  // (a constant condition for larger batches)
@@ -519,7 +525,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
                     else if (kg <= 2) gemv_rpw<2>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
                     else if (kg <= 4) gemv_rpw<4>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
                     else gemv_rpw<8>(P, S, d, i, handoff, sl, slot, x, ring, rq, lm_best, ab);
-                } else if constexpr (FL != FL_LEAN) {
+                } else if constexpr (FL != FL_LEAN && FL != FL_W8) {
                     bool wide = false;
                     if constexpr (MAXB == 1) {
                         wide = rpw_wide_tile(P, d);
@@ -655,6 +661,7 @@ static KernelFn pick_kernel(const Plan &p) {
     if (p.kind == PLAN_GLM) return p.tc ? mk_interp<1, FL_GLMTC> : mk_interp<1, FL_GLM>;
     if (p.tc) return mk_interp<TC_MAXB, FL_TC>;
     const int B = p.B;
+    if (p.w8) return mk_interp<1, FL_W8>;
     if (B <= 1) return p.lean ? mk_interp<1, FL_LEAN> : mk_interp<1, FL_GEN>;
     if (B <= 2) return mk_interp<2, FL_GEN>;
     if (B <= 4) return mk_interp<4, FL_GEN>;
@@ -815,6 +822,9 @@ static int build_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab, std::ve
         for (int b : {MK_BIND_WQ, MK_BIND_WK, MK_BIND_WV, MK_BIND_WO, MK_BIND_WG, MK_BIND_WU, MK_BIND_WD,
                       MK_BIND_NORM_ATTN, MK_BIND_NORM_MLP})
             if (int rc = need(b, l)) return rc;
+        if (p.w8)
+            for (int b = MK_BIND_SQ; b <= MK_BIND_SD; ++b)
+                if (int rc = need(b, l)) return rc;
         if (m.qk_norm)
             for (int b : {MK_BIND_QNORM, MK_BIND_KNORM})
                 if (int rc = need(b, l)) return rc;
@@ -861,6 +871,17 @@ static int build_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab, std::ve
             break;
         default:
             break;
+        }
+        if (p.w8 && l >= 0) {  // FP8 projections: their block scales
+            switch (p.op_kind[o]) {
+            case MK_OP_QKV:
+                r[S_W8_S0] = p.bind[MK_BIND_SQ][l]; r[S_W8_S1] = p.bind[MK_BIND_SK][l]; r[S_W8_S2] = p.bind[MK_BIND_SV][l];
+                break;
+            case MK_OP_O: r[S_W8_S0] = p.bind[MK_BIND_SO][l]; break;
+            case MK_OP_UP: r[S_W8_S0] = p.bind[MK_BIND_SG][l]; r[S_W8_S1] = p.bind[MK_BIND_SU][l]; break;
+            case MK_OP_DOWN: r[S_W8_S0] = p.bind[MK_BIND_SD][l]; break;
+            default: break;
+            }
         }
         switch (p.op_kind[o]) {
         case MK_OP_QKV: r[S_G_OUT] = r[S_QKV_OUT]; break;
@@ -1008,7 +1029,7 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
     if (configured_smem[dev] < p.smem_bytes) {
         for (KernelFn f : {mk_interp<1, FL_GEN>, mk_interp<2, FL_GEN>, mk_interp<4, FL_GEN>, mk_interp<8, FL_GEN>,
                            mk_interp<1, FL_GLM>, mk_interp<1, FL_GLMTC>, mk_interp<1, FL_LEAN>,
-                           mk_interp<TC_MAXB, FL_TC>}) {
+                           mk_interp<1, FL_W8>, mk_interp<TC_MAXB, FL_TC>}) {
             e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
         }

@@ -48,6 +48,13 @@ enum : int {
     P_S1_ROW0 = W_P + 10,
     P_S1_MAT = W_P + 11,
 };
+// Batch-1 GEMV tiles of FP8 projections: e4m3 rows (K bytes) with one fp32
+// scale per 128 x 128 block; the tile's rows lie in one 128-row block
+enum : int {
+    P_W8 = W_P + 12,    // 1: the tile's weights are e4m3
+};
+constexpr int W8_K = 2048;          // K of every FP8 projection tile (row bytes)
+constexpr int W8_ROWS = 32;         // e4m3 rows of K = 2048 per 64 KB page
 // NORM payload (tensor-core plans)
 enum : int {
     P_NB = W_P + 0,      // sequence
@@ -136,6 +143,8 @@ enum : int {
     // tensor-core GEMV tiles: the weight tensor maps of the op (QKV: Wq, Wk, Wv; UP: Wg, Wu;
     // else the op's matrix) and the input activation's tensor map (bf16 high/low rows)
     S_T_W0 = 7, S_T_W1 = 8, S_T_W2 = 9, S_T_X = 10,
+    // FP8 GEMV tiles: block scales of the op's matrices (QKV: q, k, v; UP: gate, up; else the matrix)
+    S_W8_S0 = 11, S_W8_S1 = 12, S_W8_S2 = 13,
     // every GEMV op: its output (QKV: qkv, O: residual, UP: activation, DOWN:
     // residual, LM: logits) and second output (O: mid residual, LM: argmax keys)
     S_G_OUT = 14, S_G_OUT2 = 15,

@@ -883,6 +883,14 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
         if ((int64_t)p.seq0[b] + s->max_steps > s->cache_slots)
             return set_error(MK_ERR_INVALID, "cache_slots smaller than seq_len0 + max_steps");
     }
+    // FP8 projections: the batch-1 row-per-warp tiles over e4m3 rows of K = 2048
+    const bool w8 = m->weight_fp8 != 0;
+    if (w8 && (B != 1 || H != W8_K || Hq * D != W8_K || D != 64 || F % W8_K || tgt->tc_tiles > 0 ||
+               (tgt->kchunk_down > 0 && tgt->kchunk_down != W8_K)))
+        return set_error(MK_ERR_UNSUPPORTED, "FP8 projections need batch 1, hidden = q_heads x head_dim = 2048, "
+                                             "head_dim 64, ffn a multiple of 2048 (MLP-down K chunks of 2048)");
+    p.w8 = w8;
+    const int wb = w8 ? 1 : 2;  // bytes per projection weight (the LM head stays bf16)
     // tensor-core tiles (128 weight rows x the batch): every K and row count a
     // multiple of 128, each head group's q/k/v rows whole 64-row segments
     const bool tc_shape = H % TC_M == 0 && (Hq * D) % TC_M == 0 && F % TC_M == 0 && ((G + 2) * D) % TC_M == 0 &&
@@ -1020,6 +1028,16 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
                                              "tiles of up to 64 whole 16-row pages at batch 1 (not O; mlp-up gate "
                                              "rows a multiple of 8)");
     if (F % kn_up) return set_error(MK_ERR_UNSUPPORTED, "rows_up must divide ffn");
+    if (w8) {
+        // 32 e4m3 rows per page: a tile is one page of at most 32 rows or whole
+        // pages (MLP-up: pages of 16 gate + 16 up rows), and stays in one
+        // 128-row block of the block scales (a power of two of rows up to 128)
+        auto pow2 = [](int v) { return v > 0 && (v & (v - 1)) == 0; };
+        if (kn_kc != W8_K || p.page_bytes != W8_ROWS * W8_K || !pow2(kn_qkv) || kn_qkv > 128 || !pow2(kn_dn) ||
+            kn_dn > 128 || !pow2(kn_o) || kn_o > RESID_ROWS || !pow2(kn_up) || kn_up < 16 || kn_up > 64)
+            return set_error(MK_ERR_UNSUPPORTED, "FP8 tiles: 64 KB pages, MLP-down K chunks of 2048, QKV / MLP-down "
+                                                 "rows a power of two up to 128, O up to 16, MLP-up 16, 32 or 64 gate rows");
+    }
     if (kn_T * D * 2 > p.page_bytes * 8) return set_error(MK_ERR_UNSUPPORTED, "attention split too long");
     p.num_pages = std::min(MAX_PAGES, (smem_per_cta - fixed) / p.page_bytes);
     p.smem_bytes = fixed + p.num_pages * p.page_bytes;
@@ -1053,15 +1071,15 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
         ops.push_back(o);
         return (int)ops.size() - 1;
     };
-    auto rows_cost = [](int n_rows, int rows, int kdim) {
-        return [=](const int *b) { return (int64_t)std::min(rows, n_rows - b[0] * rows) * kdim * 2; };
+    auto rows_cost = [](int n_rows, int rows, int kdim, int bytes) {
+        return [=](const int *b) { return (int64_t)std::min(rows, n_rows - b[0] * rows) * kdim * bytes; };
     };
     int emb = add_op(MK_OP_EMBED, -1, 1, 1, 1);
     ops[emb].cost = [=](const int *) { return (int64_t)B * H * 2; };
     int prev = emb;
     for (int l = 0; l < L; ++l) {
         int q = add_op(MK_OP_QKV, l, Hkv, rows_group / kn_qkv, 1);
-        ops[q].cost = [=](const int *) { return (int64_t)kn_qkv * H * 2; };
+        ops[q].cost = [=](const int *) { return (int64_t)kn_qkv * H * wb; };
         int a = add_op(MK_OP_ATTN, l, Hkv, B, ns_max);
         ops[a].exists = [nsplit](const int *b) { return b[2] < nsplit[b[1]]; };
         ops[a].cost = [=](const int *b) {
@@ -1070,11 +1088,11 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
             return (int64_t)2 * D * 2 * rows;
         };
         int o = add_op(MK_OP_O, l, ceil_div(H, kn_o), 1, 1);
-        ops[o].cost = rows_cost(H, kn_o, Hq * D);
+        ops[o].cost = rows_cost(H, kn_o, Hq * D, wb);
         int u = add_op(MK_OP_UP, l, F / kn_up, 1, 1);
-        ops[u].cost = [=](const int *) { return (int64_t)2 * kn_up * H * 2; };
+        ops[u].cost = [=](const int *) { return (int64_t)2 * kn_up * H * wb; };
         int d = add_op(MK_OP_DOWN, l, ceil_div(H, kn_dn), F / kn_kc, 1);
-        ops[d].cost = rows_cost(H, kn_dn, kn_kc);
+        ops[d].cost = rows_cost(H, kn_dn, kn_kc, wb);
         if (prev == emb) edges.push_back({prev, q, {-1, -1, -1}, {-1, -1, -1}});
         else edges.push_back({prev, q, {1, -1, -1}, {-1, -1, -1}});
         edges.push_back({q, a, {1, 2, -1}, {1, 0, -1}});   // qkv [B, Hkv, rows]: group & row cuts vs batch & group
@@ -1084,7 +1102,7 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
         prev = d;
     }
     int lm = add_op(MK_OP_LM, -1, ceil_div(V, kn_lm), 1, 1);
-    ops[lm].cost = rows_cost(V, kn_lm, H);
+    ops[lm].cost = rows_cost(V, kn_lm, H, 2);
     edges.push_back({prev, lm, {1, -1, -1}, {-1, -1, -1}});
 
     std::vector<RawTask> raw;
@@ -1182,7 +1200,9 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
         }
         if (op.opcode != MK_OP_ATTN && op.opcode != MK_OP_EMBED) {
             // the tile's rows (MLP-up: gate rows, then up rows) packed into pages
-            const int rpp = p.page_bytes / (2 * pl[P_KC - W_P]);
+            const bool e4m3 = w8 && op.opcode != MK_OP_LM;
+            pl[P_W8 - W_P] = e4m3 ? 1 : 0;
+            const int rpp = p.page_bytes / ((e4m3 ? 1 : 2) * pl[P_KC - W_P]);
             pl[P_RPP - W_P] = rpp;
             pl[P_NPG - W_P] = ceil_div((op.opcode == MK_OP_UP ? 2 : 1) * pl[P_NROWS - W_P], rpp);
         }
@@ -1201,10 +1221,17 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     for (int b = 0; b < B; ++b) kv_read += (int64_t)2 * p.seq0[b] * Hkv * D * 2 * L;
     int64_t kv_write = (int64_t)2 * B * Hkv * D * 2 * L;
     int64_t norms = (int64_t)(2 * L + 1) * H * 2 + (m->qk_norm ? (int64_t)2 * L * D * 2 : 0);
-    p.alg_bytes = weights + kv_read + kv_write + norms;
+    int64_t scales = 0;  // FP8: one fp32 per 128 x 128 block of every projection
+    if (w8) {
+        auto blocks = [](int n, int k) { return (int64_t)ceil_div(n, 128) * (k / 128); };
+        scales = (int64_t)L * 4 *
+                 (blocks(Hq * D, H) + 2 * blocks(Hkv * D, H) + blocks(H, Hq * D) + 2 * blocks(F, H) + blocks(H, F));
+    }
+    p.alg_bytes = weights + kv_read + kv_write + norms + scales;
     // the lean batch-1 kernel instance: every GEMV tile must take the
-    // row-per-warp path (the device applies the same rule to each tile)
-    p.lean = B == 1 && D == 64;
+    // row-per-warp path (the device applies the same rule to each tile);
+    // FP8 plans run their own instance
+    p.lean = B == 1 && D == 64 && !w8;
     for (const TaskRec &t : p.tasks) {
         if (!p.lean) break;
         if (t.opcode < MK_OP_QKV || t.opcode > MK_OP_LM || t.opcode == MK_OP_ATTN) continue;

@@ -45,6 +45,7 @@ struct Plan {
     int schedule = MK_SCHED_BYTES;  // MK_SCHED_BYTES or MK_SCHED_TIMED
     bool lean = false;  // batch 1, head_dim 64, every GEMV tile on the row-per-warp path: the lean kernel instance
     bool tc = false;    // GEMV tiles on tcgen05 tensor cores (the tensor-core kernel instance)
+    bool w8 = false;    // FP8 projections (the batch-1 FP8 kernel instance)
     int np = 0;         // tensor-core plans: batch padded to 8 or 16
     int ksplit_qkv = 1, ksplit_o = 1;
     int glm_ksplit = 1;  // GLM tensor-core plans: K parts of the first GEMMs

@@ -34,7 +34,10 @@ BIND = {n: i for i, n in enumerate([
     # GLM pre-attention block
     "glm_x", "glm_res", "glm_norm", "glm_res_out", "glm_qa", "glm_sa", "glm_w_qkva", "glm_s_qkva", "glm_w_gate",
     "glm_s_gate", "glm_w_ik", "glm_s_ik", "glm_w_qb", "glm_s_qb", "glm_w_iq", "glm_s_iq", "glm_qkva", "glm_ik",
-    "glm_qb", "glm_sb", "glm_gate", "glm_q", "glm_iq", "glm_latent", "glm_index"])}
+    "glm_qb", "glm_sb", "glm_gate", "glm_q", "glm_iq", "glm_latent", "glm_index",
+    # FP8 projections: block scales of wq .. wd
+    "sq", "sk", "sv", "so", "sg", "su", "sd"])}
+SCALE_OF = {"wq": "sq", "wk": "sk", "wv": "sv", "wo": "so", "wg": "sg", "wu": "su", "wd": "sd"}
 PER_LAYER = ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "norm_attn", "norm_mlp", "qnorm", "knorm")
 
 EXPORTED = ["mk_plan", "mk_plan_graph", "mk_plan_info_get", "mk_plan_export", "mk_bind", "mk_run",
@@ -52,7 +55,7 @@ class MkError(RuntimeError):
 class ModelDesc(C.Structure):
     _fields_ = [("layers", C.c_int), ("hidden", C.c_int), ("q_heads", C.c_int), ("kv_heads", C.c_int),
                 ("head_dim", C.c_int), ("ffn", C.c_int), ("vocab", C.c_int), ("qk_norm", C.c_int),
-                ("eps", C.c_float), ("rope_theta", C.c_float)]
+                ("eps", C.c_float), ("rope_theta", C.c_float), ("weight_fp8", C.c_int)]
 
 
 class StepDesc(C.Structure):
@@ -79,7 +82,7 @@ class PlanInfo(C.Structure):
         "smem_bytes", "act_bytes", "rows_qkv", "rows_o", "rows_up", "rows_down", "kchunk_down", "rows_lm",
         "attn_split", "total_slots")] + [("workspace_bytes", C.c_uint64), ("scratch_offset", C.c_uint64),
                                           ("algorithmic_bytes_step", C.c_uint64)] + [
-        (n, C.c_int) for n in ("tc_tiles", "ksplit_qkv", "ksplit_o")]
+        (n, C.c_int) for n in ("tc_tiles", "ksplit_qkv", "ksplit_o", "weight_fp8")]
 
 
 class GraphOp(C.Structure):
@@ -175,10 +178,11 @@ class Plan:
 
     @classmethod
     def llama(cls, shape, batch: int, seq_len0: Sequence[int], max_steps: int, cache_slots: int,
-              capture_hidden: bool = False, **target):
+              capture_hidden: bool = False, fp8: bool = False, **target):
+        """``fp8``: the seven projections are e4m3 with 128 x 128 block scales."""
         lib = load()
         m = ModelDesc(shape.L, shape.H, shape.Hq, shape.Hkv, shape.D, shape.F, shape.V, int(shape.qk_norm),
-                      shape.eps, shape.theta)
+                      shape.eps, shape.theta, int(fp8))
         lens = (C.c_int * batch)(*[int(x) for x in seq_len0])
         s = StepDesc(batch, lens, max_steps, cache_slots, int(capture_hidden))
         t = _target(**target)
@@ -253,7 +257,8 @@ class Plan:
 class Session:
     """Device-resident decode state: weights, KV caches, outputs and the workspace.
 
-    ``weights`` follows ``synth.make_weights`` naming (torch bf16 CUDA tensors);
+    ``weights`` follows ``synth.make_weights`` naming (torch bf16 CUDA tensors;
+    with ``weights["fp8"]`` the projections are (e4m3 codes, block scales) pairs);
     ``kcache`` / ``vcache`` are [L, B, Hkv, S_max, D] bf16 CUDA tensors, appended in place.
     """
 
@@ -266,7 +271,8 @@ class Session:
         self.max_steps = max_steps
         self.seq_len0 = list(seq_len0)
         dev = kcache.device
-        self.plan = Plan.llama(shape, self.B, seq_len0, max_steps, kcache.shape[3], capture_hidden, **target)
+        fp8 = bool(weights.get("fp8", False))
+        self.plan = Plan.llama(shape, self.B, seq_len0, max_steps, kcache.shape[3], capture_hidden, fp8=fp8, **target)
         info = self.plan.info()
         self.weights, self.kcache, self.vcache = weights, kcache, vcache
         self.tokens = torch.zeros((max_steps + 1, self.B), dtype=torch.int32, device=dev)
@@ -283,7 +289,11 @@ class Session:
         for n in PER_LAYER:
             if n in weights:
                 for l, t in enumerate(weights[n]):
-                    p.bind(n, t.data_ptr(), l)
+                    if isinstance(t, tuple):  # FP8: codes, then their block scales
+                        p.bind(n, t[0].data_ptr(), l)
+                        p.bind(SCALE_OF[n], t[1].data_ptr(), l)
+                    else:
+                        p.bind(n, t.data_ptr(), l)
         p.bind("kcache", kcache.data_ptr())
         p.bind("vcache", vcache.data_ptr())
         p.bind("tokens", self.tokens.data_ptr())

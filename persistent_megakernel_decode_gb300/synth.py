@@ -49,6 +49,7 @@ class Workload:
     seq_len: int              # cached tokens per sequence before the first step
     steps: int
     len_range: Optional[tuple] = None   # (lo, hi) inclusive: per-sequence lengths drawn from a seed
+    fp8: bool = False                   # projections e4m3 with 128 x 128 block scales (make_weights(fp8=True))
 
     @property
     def weight_seed(self):
@@ -76,6 +77,8 @@ SMALL_QK = ModelShape(L=2, H=512, Hq=4, Hkv=2, D=128, F=512, V=2048, eps=1e-6, t
 WORKLOADS: Dict[str, Workload] = {
     "tiny": Workload("tiny", 0, TINY, 1, 64, 8),
     "llama1b_b1": Workload("llama1b_b1", 1, LLAMA_1B, 1, 1024, 128),
+    # the same model and step with FP8 projections (SURVEY's next row: FP8 weight streaming)
+    "llama1b_b1_fp8": Workload("llama1b_b1_fp8", 1, LLAMA_1B, 1, 1024, 128, fp8=True),
     "llama1b_b8": Workload("llama1b_b8", 2, LLAMA_1B, 8, 4096, 64, len_range=(512, 4096)),
     "qwen3_8b_b1": Workload("qwen3_8b_b1", 4, QWEN3_8B, 1, 2048, 32),
     "qwen3_8b_b16": Workload("qwen3_8b_b16", 4, QWEN3_8B, 16, 2048, 32),

@@ -86,8 +86,9 @@ def bf16_ulp_distance(a_u16: np.ndarray, b_u16: np.ndarray) -> float:
 
 def run_parity(shape: synth.ModelShape, seq0: Sequence[int], steps: int, check_steps: Sequence[int],
                seed: int = 0, teacher_forced: bool = True, nthreads: Optional[int] = None,
-               first_tokens: Optional[Sequence[int]] = None, **target) -> ParityRun:
+               first_tokens: Optional[Sequence[int]] = None, fp8: bool = False, **target) -> ParityRun:
     """Run ``steps`` decode steps on the GPU; check the listed steps against the oracle.
+    ``fp8``: the projections are e4m3 with 128 x 128 block scales (both sides).
 
     teacher_forced: every step's token is the oracle's argmax of the previous
     step (host-provided tokens); otherwise the GPU feeds its own argmax and the
@@ -95,7 +96,7 @@ def run_parity(shape: synth.ModelShape, seq0: Sequence[int], steps: int, check_s
     B = len(seq0)
     smax = max(seq0) + steps + 1
     dev = torch.device("cuda:0")
-    w = synth.make_weights(shape, seed, device=dev)
+    w = synth.make_weights(shape, seed, device=dev, fp8=fp8)
     kc, vc = synth.make_cache(shape, B, smax, seed + 100, device=dev)
     hw = host_weights(w)
     oshape = oracle_shape(shape)

@@ -3,6 +3,8 @@ oracle's independent statement of the same rules -- bit for bit."""
 import os
 import re
 
+from dataclasses import replace
+
 import numpy as np
 import pytest
 
@@ -75,20 +77,21 @@ def _oracle_knobs(info):
                        attn_split=info["attn_split"])
 
 
-def _compare(shape, B, seq0, steps, workers=152, **kn):
+def _compare(shape, B, seq0, steps, workers=152, fp8=False, **kn):
     # the oracle deals tasks by bytes, the pages' rule (the default time-model
     # schedule is checked for validity below)
     p = rt.Plan.llama(shape, B, seq0, steps, max(seq0) + steps + 3, num_sms=workers, smem_per_cta=232448,
-                      schedule=rt.SCHED_BYTES, **kn)
+                      schedule=rt.SCHED_BYTES, fp8=fp8, **kn)
     info = p.info()
+    assert info["weight_fp8"] == int(fp8)
     q, ids, th, tasks = p.export()
     osh = plans.LlamaShape(shape.L, shape.H, shape.Hq, shape.Hkv, shape.D, shape.F, shape.V)
     tile_knobs = {k: v for k, v in kn.items() if k != "tc_tiles"}
     if tile_knobs:  # a test that sets tile knobs itself: the oracle takes the same
         okn = _oracle_knobs(info)
     else:           # defaults: the oracle derives them from its own statement of the rules
-        okn = plans.llama_knobs(osh, B, seq0, steps, workers, 232448)
-        assert okn == _oracle_knobs(info), (okn, _oracle_knobs(info))
+        okn = plans.llama_knobs(osh, B, seq0, steps, workers, 232448, fp8=fp8)
+        assert okn == replace(_oracle_knobs(info), wbytes=okn.wbytes), (okn, _oracle_knobs(info))
     op = plans.llama_step_plan(osh, okn, B, seq0, steps, workers)
     assert info["num_tasks"] == len(op.tasks)
     assert list(th) == op.thresholds
@@ -381,3 +384,32 @@ def test_qwen3_8b_batch1_gemv_tiles_fit_the_wide_row_per_warp_path():
             assert ((rows == 8) if op == "up" else (rows == 16)).all()
         seen.add(op)
     assert seen == {"qkv", "o", "up", "lm", "down"}
+
+
+def test_fp8_plan_matches_the_oracle_and_its_tiles():
+    """FP8 projections (Llama-1B width, 2 layers, batch 1): the plan equals the
+    oracle's (same knobs, one byte per projection weight in the costs), and
+    every projection tile is marked e4m3 with 32 rows to a page, inside one
+    128-row block; the LM head stays bf16; the algorithmic bytes count e4m3
+    weights and their block scales."""
+    from dataclasses import replace as rep
+    sh = rep(synth.LLAMA_1B, L=2)
+    p, op = _compare(sh, 1, [1024], 4, fp8=True)
+    q, ids, th, tasks = p.export()
+    P_W8, P_RPP, P_NPG, P_ROW0, P_NROWS = 26, 22, 23, 14, 15
+    for w in q.reshape(-1, 32):
+        kind = rt.OP_NAMES[w[0]]
+        if kind in ("qkv", "o", "up", "down"):
+            assert w[P_W8] == 1 and w[P_RPP] == 32, kind
+            rows = (2 if kind == "up" else 1) * w[P_NROWS]
+            assert w[P_NPG] == -(-rows // 32)
+            assert w[P_ROW0] // 128 == (w[P_ROW0] + w[P_NROWS] - 1) // 128
+        elif kind == "lm":
+            assert w[P_W8] == 0 and w[P_RPP] == 16
+    H, QD, KD, F, L, V = sh.H, sh.Hq * sh.D, sh.Hkv * sh.D, sh.F, sh.L, sh.V
+    blocks = lambda n, k: -(-n // 128) * (k // 128)
+    weights = L * (QD * H + 2 * KD * H + H * QD + 2 * F * H + H * F) + V * H * 2
+    scales = L * 4 * (blocks(QD, H) + 2 * blocks(KD, H) + blocks(H, QD) + 2 * blocks(F, H) + blocks(H, F))
+    kv = 2 * 1024 * sh.Hkv * sh.D * 2 * L + 2 * sh.Hkv * sh.D * 2 * L
+    norms = (2 * L + 1) * H * 2
+    assert p.info()["algorithmic_bytes_step"] == weights + scales + H * 2 + kv + norms
