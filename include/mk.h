@@ -60,7 +60,9 @@ extern "C" {
 #define MK_OP_GLM_GEMM 10  /* GLM block: rows of an FP8 weight x FP8 activations, block scales, bf16 out (+RoPE) */
 #define MK_OP_GLM_FIN  11  /* GLM block: one token's q-lora re-quantisation, RoPE and cache writes */
 #define MK_OP_NORM     12  /* tensor-core plans: RMSNorm of one sequence's residual into bf16 high/low rows */
-#define MK_NUM_OPCODES 13
+#define MK_OP_ATTN_POOL 13 /* attn_pool plans: one per worker and layer; claims the layer's attention tasks
+                              (longest first) from a device counter until none is left */
+#define MK_NUM_OPCODES 14
 
 /* ---- plan modes ---- */
 #define MK_MODE_MEGAKERNEL 0   /* one persistent launch per step */
@@ -112,6 +114,13 @@ typedef struct {
                               (MK_ERR_UNSUPPORTED if the shape does not allow), -1 = never (batch <= 8).
                               GLM block plans: 0 = the FP8 GEMMs on tcgen05 tiles where M = 16, 1 =
                               required, -1 = warp-level MMA tiles */
+    int attn_pool;         /* 1: device-side dispatch of the attention tasks ("CMU 15-779 Lecture 7
+                              notes", section 6, JIT scheduling; "MPK code walkthrough", the
+                              scheduler): every worker gets one MK_OP_ATTN_POOL instruction per
+                              layer, which claims tasks from the layer's list, longest first, with an
+                              atomic counter until the list is exhausted, so whoever is free takes
+                              the next task; the layer's attention then waits for its whole QKV op
+                              and O for every worker's pool; batch >= 2.  0 = the host deals attention tasks */
 } mk_target_desc;
 
 /* Queue assignment.  Either way tasks go to workers in one topological order,
@@ -136,6 +145,7 @@ typedef struct {
     int tc_tiles;                    /* 1: the GEMV (GLM: FP8 GEMM) tiles run on tcgen05 tensor cores */
     int ksplit_qkv, ksplit_o;        /* tensor-core plans: K splits of the QKV and O tiles */
     int weight_fp8;                  /* 1: the projections stream e4m3 rows */
+    int attn_table_rows;             /* attn_pool plans: rows of the attention task table, else 0 */
 } mk_plan_info;
 
 /* ---- bindings: caller-owned device buffers ---- */
@@ -344,6 +354,13 @@ int mk_plan_info_get(mk_plan_t plan, mk_plan_info *info);
 /* tasks row: kind(opcode), layer, bx, by, bz, cost, n_waits, 3 x (event,
  * threshold, epoch_offset), n_signals, 2 x (event, increment), 4 reserved */
 int mk_plan_export(mk_plan_t plan, int32_t *queue, int32_t *task_ids, int32_t *thresholds, int32_t *tasks);
+
+/* attn_pool plans: the attention task table the pools claim from ("CMU
+ * 15-779 Lecture 7 notes", section 6: the tasks a JIT scheduler hands out),
+ * int32 [mk_plan_info.attn_table_rows, 32] instruction words -- per layer its
+ * tasks, longest first; a pool instruction's P_TBASE / P_PT name its layer's
+ * rows.  Host only; caller-owned buffer; MK_ERR_INVALID on a null argument. */
+int mk_plan_export_attn_table(mk_plan_t plan, int32_t *rows);
 
 /* Bind a caller-owned device buffer (MK_BIND_*) into the plan's operand
  * pointer table: one [num_ops, 16] uint64 row per op, shared by all of that

@@ -157,7 +157,7 @@ def llama_knobs(shape: LlamaShape, B: int, seq0: Sequence[int], max_steps: int, 
     """
     H, Hq, Hkv, D, F, V = shape.H, shape.Hq, shape.Hkv, shape.D, shape.F, shape.V
     G = Hq // Hkv
-    WARPS, TILE_ROWS, RESID, NRED, MBAR, CTRL = 8, 16, 16, 4, 512, 128
+    WARPS, TILE_ROWS, RESID, NRED, MBAR, CTRL = 8, 16, 16, 4, 512, 256
 
     def pow2_floor(v):
         r = 1

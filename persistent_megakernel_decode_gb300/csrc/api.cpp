@@ -47,7 +47,10 @@ void layout_workspace(Plan &p) {
         p.ws.gsum[1] = take((uint64_t)M * p.glm.gate_heads * 4);
         p.ws.gsum[2] = take((uint64_t)M * p.glm.idx_dim * 4);
     }
+    // attn_pool plans: one claim counter per step and layer, zero at step 0
+    p.ws.claims = p.attn_table.empty() ? 0 : take((uint64_t)p.max_steps * std::max(1, L) * 4);
     p.ws.queue = take(p.words.size() * 4);
+    p.ws.atab = p.attn_table.empty() ? 0 : take(p.attn_table.size() * 4);
     p.ws.optab = take((uint64_t)p.num_ops * N_SLOTS * 8);
     p.ws.seq0 = take((uint64_t)B * 4);
     p.ws.rope = take(p.rope_tab.size() * 4);
@@ -187,8 +190,16 @@ int mk_plan_info_get(mk_plan_t plan, mk_plan_info *info) {
     info->algorithmic_bytes_step = (uint64_t)p.alg_bytes;
     info->tc_tiles = p.tc ? 1 : 0;
     info->weight_fp8 = p.w8 ? 1 : 0;
+    info->attn_table_rows = (int)(p.attn_table.size() / W_WORDS);
     info->ksplit_qkv = p.ksplit_qkv;
     info->ksplit_o = p.ksplit_o;
+    return MK_OK;
+}
+
+int mk_plan_export_attn_table(mk_plan_t plan, int32_t *rows) {
+    if (!plan || !rows) return set_error(MK_ERR_INVALID, "null plan or buffer");
+    const Plan &p = plan->p;
+    if (!p.attn_table.empty()) std::memcpy(rows, p.attn_table.data(), p.attn_table.size() * 4);
     return MK_OK;
 }
 

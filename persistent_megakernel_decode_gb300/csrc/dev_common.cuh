@@ -217,10 +217,16 @@ struct Smem {
     DEV uint64_t *drain() const { return accempty() + GT_NACC; }
     DEV int *page_users() const { return reinterpret_cast<int *>(mk_smem + o_ctrl) + 16; }
     DEV uint32_t *tmem_slot() const { return reinterpret_cast<uint32_t *>(mk_smem + o_ctrl) + 31; }
+    // attention pools: the claim ring (the loader posts claimed task indices,
+    // -1 when the pool is empty), how many it posted, and how many each
+    // reader took (activation loader, then the 8 consumer warps)
+    DEV volatile int *claim_ring() const { return reinterpret_cast<volatile int *>(mk_smem + o_ctrl) + 32; }
+    DEV volatile int *claims_posted() const { return reinterpret_cast<volatile int *>(mk_smem + o_ctrl) + 48; }
+    DEV volatile int *claims_taken() const { return reinterpret_cast<volatile int *>(mk_smem + o_ctrl) + 49; }
 };
 
 constexpr int SLOT_FRESH = 1;
-constexpr int CTRL_WORDS = 16;
+constexpr int CTRL_WORDS = 64;
 
 // Error path, kept out of line so that the hot loops stay small.
 static __device__ __noinline__ void raise_error_at(uint32_t *err, Smem S, int code, int slot, int event, uint32_t obs,
@@ -459,6 +465,39 @@ DEV void fetch(WIns &I, const KParams &P, const int32_t *q, int i) {
 // The launch-wide number of slot i of step I.step (progress words count these).
 DEV int launch_slot(const KParams &P, const WIns &I, int i) { return (I.step - P.step) * P.lmax + i; }
 
+// ---------------------------------------------------------------- attention pools
+// The loader claims a pool's tasks and posts each claim (a task index, or -1
+// once the pool is empty) to the worker's other roles through a ring of
+// CLAIM_RING entries; claim `seq` goes to entry seq % CLAIM_RING.  The
+// loader reuses an entry only after all nine readers (the activation loader,
+// reader 0, and the 8 consumer warps, readers 1..8) took the claim before
+// it; every wait is bounded.
+DEV bool post_claim(const KParams &P, const Smem S, int seq, int value, int slot, int opc) {
+    const int lane = threadIdx.x & 31;
+    if (seq >= CLAIM_RING)
+        for (int r = 0; r < 1 + CONSUMER_WARPS; ++r)
+            if (!warp_wait_smem(P, S, S.claims_taken() + r, (uint32_t)(seq - CLAIM_RING + 1), slot, opc)) return false;
+    if (lane == 0) {
+        S.claim_ring()[seq % CLAIM_RING] = value;
+        st_release_cta(S.claims_posted(), seq + 1);
+    }
+    __syncwarp();
+    return true;
+}
+// Reader `reader` takes claim `seq` (the whole warp; false on abort or timeout).
+DEV bool read_claim(const KParams &P, const Smem S, int seq, int reader, int &value, int slot, int opc) {
+    const int lane = threadIdx.x & 31;
+    if (!warp_wait_smem(P, S, S.claims_posted(), (uint32_t)(seq + 1), slot, opc)) return false;
+    value = S.claim_ring()[seq % CLAIM_RING];
+    __syncwarp();
+    if (lane == 0) st_release_cta(S.claims_taken() + reader, seq + 1);  // (after the read: release)
+    return true;
+}
+// Lane k's word of attention-table row `row` (a claimed task's instruction).
+DEV int attn_table_word(const KParams &P, int row) {
+    return __ldg(P.attn_table + (size_t)row * W_WORDS + (threadIdx.x & 31));
+}
+
 // Warp-uniform sanity checks of one instruction against the launch.
 // Kernel instances ("flavours"): FL_GEN runs every Llama-path op; FL_GLM
 // only the GLM-block ops (and holds their code), with warp-level MMA tiles,
@@ -471,6 +510,9 @@ DEV int launch_slot(const KParams &P, const WIns &I, int i) { return (I.step - P
 // row-per-warp tiles, the bf16 LM head, attention at head_dim 64).
 constexpr int FL_GEN = 0, FL_GLM = 1, FL_LEAN = 2, FL_TC = 3, FL_GLMTC = 4, FL_W8 = 5;
 MK_HD constexpr bool fl_glm(int fl) { return fl == FL_GLM || fl == FL_GLMTC; }
+// Instances that hold the attention pools (device-side dispatch of attention
+// tasks, for batches of variable-length sequences): the batched ones.
+MK_HD constexpr bool fl_pools(int fl, int maxb) { return fl == FL_TC || (fl == FL_GEN && maxb > 1); }
 
 template <int FL>
 DEV bool ins_valid(const KParams &P, const WIns &I) {
@@ -490,6 +532,9 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
     constexpr bool TC = FL == FL_TC;
     const bool glm_op = opc >= MK_OP_GLM_A0 && opc <= MK_OP_GLM_FIN;
     if (GLM != glm_op && opc != MK_OP_COUNTER) return false;  // each instance runs its own ops
+    if (opc == MK_OP_ATTN_POOL)
+        return (FL == FL_TC || (FL == FL_GEN && P.B > 1)) && P.claims && P.attn_table && F(I, P_LAYER) >= 0 && F(I, P_LAYER) < P.L &&
+               F(I, P_PT) >= 0 && F(I, P_TBASE) >= 0 && (F(I, W_CNT) & 0xff) <= MAX_WAITS;
     if (opc == MK_OP_NORM && !TC) return false;
     if (opc == MK_OP_NORM)
         return F(I, P_NB) >= 0 && F(I, P_NB) < P.B && P.H % 4 == 0 && P.H <= 8192 && P.np >= P.B;

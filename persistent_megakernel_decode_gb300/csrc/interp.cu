@@ -35,11 +35,13 @@
 namespace mk {
 
 // ---------------------------------------------------------------- loader warp
-template <int FL>
+template <int MAXB, int FL>
 DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
+    constexpr bool POOLS = fl_pools(FL, MAXB);
     const int lane = threadIdx.x & 31;
     const uint64_t pol = evict_first_policy();
     uint32_t ring = 0, rp = 0, rph = 0;  // pages issued; ring position and its use parity
+    int cseq = 0;                        // attention-pool claims posted so far
     const int NP = P.num_pages, PS = P.page_bytes;
     WIns I;
     fetch_init(I, P, myq);
@@ -85,93 +87,118 @@ DEV void loader_role(const KParams &P, const Smem S, const int32_t *myq) {
                 continue;
             }
         }
-        if (opc == MK_OP_ATTN && I.step > P.step) {
-            // K/V rows appended by an earlier step of this launch: their writer
-            // published them with the layer's attention event of that step --
-            // acquire it (long since met) before the bulk copies read the rows
-            const int pos0 = attn_pos(P, I) - (I.step - P.step);  // first position appended in this launch
-            if (F(I, P_T0) + attn_cached_rows(I, attn_pos(P, I)) > pos0) {
-                const int ev = F(I, W_SIG);
-                const uint32_t target = (uint32_t)F(I, P_ATHR) * (uint32_t)I.step;
-                if (!warp_wait_counter(P, S, ev, target, i, opc)) goto drain;
-                fence_proxy_async_global();
-            }
-        }
-        Seg s0, s1;
-        const int nseg = describe<FL>(P, I, s0, s1);
-        // MLP-up pages: groups of 8 gate + 8 up rows (bf16), 16 + 16 (FP8 rows, 32 to a page)
-        const int upg = FL == FL_W8 && F(I, P_W8) != 0 ? W8_ROWS / 2 : 8;
-        if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 4] = gtimer();
-        // Rows go to pages in order, as many whole rows per page as fit.  The
-        // two segments of an MLP-up tile share pages in groups of up to 8:
-        // gate rows 8g .. 8g + 7, then the same up rows (a tile of n <= 8
-        // gate rows is one group: its gate rows, then its up rows).  Attention
-        // keeps its K rows and its V rows on separate pages.
-        const int row_bytes = nseg > 0 ? s0.row_bytes : 0;
-        const int rpp = row_bytes > 0 ? PS / row_bytes : 0;
-        if (nseg > 0 && (rpp < 1 || (nseg > 1 && s1.row_bytes != row_bytes))) {
-            if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
-            goto drain;
-        }
-        // lane 0: copy rows [r, r + n) of a segment to dst
-        auto copy_rows = [&](const Seg &sg, int r, int n, uint8_t *dst, uint64_t *bar) {
-            const uint8_t *src = sg.src + (long long)r * sg.stride;
-            if (sg.stride == sg.row_bytes) {
-                bulk_g2s(dst, src, (uint32_t)n * row_bytes, bar, pol);
-            } else {
-                for (int j = 0; j < n; ++j)
-                    bulk_g2s(dst + (size_t)j * row_bytes, src + (long long)j * sg.stride, row_bytes, bar, pol);
-            }
-        };
-        const bool packed = opc != MK_OP_ATTN;
-        const int n0 = nseg > 0 ? s0.rows : 0, n1 = nseg > 1 ? s1.rows : 0;
-        // pages: packed -> over the concatenated rows; attention -> a fixed
-        // number per segment (sized for the split's T rows, filled with the
-        // rows cached so far)
-        const int total = packed ? n0 + n1 : 0;
-        const int npg0 = packed ? 0 : attn_pages(F(I, P_T), P.D, PS);
-        const int npages = packed ? (total + rpp - 1) / (rpp > 0 ? rpp : 1) : 2 * npg0;
-        bool stop = false;
-        for (int k = 0; k < npages; ++k) {
-            if (!warp_wait_bar(P, S, &S.empty()[rp], rph ^ 1, 0, i, opc)) {
-                stop = true;
-                break;
-            }
-            if (lane == 0) {
-                uint8_t *dst = S.pages() + (size_t)rp * PS;
-                uint64_t *bar = &S.full()[rp];
-                if (packed) {
-                    const int r = k * rpp, nr = min(rpp, total - r);
-                    mbar_expect_tx(bar, (uint32_t)nr * row_bytes);
-                    if (nseg == 1) {
-                        copy_rows(s0, r, nr, dst, bar);
-                    } else {
-                        const int gs = min(upg, n0);  // group size; n0 is a multiple of it when above it
-                        for (int j = r; j < r + nr;) {
-                            const int g = j / (2 * gs), w = j % (2 * gs);
-                            const bool up = w >= gs;
-                            const int run = min(r + nr - j, gs - (up ? w - gs : w));
-                            copy_rows(up ? s1 : s0, g * gs + (up ? w - gs : w), run, dst + (size_t)(j - r) * row_bytes, bar);
-                            j += run;
-                        }
-                    }
-                } else {
-                    const bool second = k >= npg0;
-                    const Seg &sg = second ? s1 : s0;
-                    const int r = (second ? k - npg0 : k) * rpp, nr = max(0, min(rpp, sg.rows - r));
-                    mbar_expect_tx(bar, (uint32_t)nr * row_bytes);  // an empty page just completes
-                    if (nr > 0) copy_rows(sg, r, nr, dst, bar);
+        // the instruction's weight or K/V rows into pages (false: stop)
+        auto stream = [&](int i, int opc) -> bool {
+            if (opc == MK_OP_ATTN && I.step > P.step) {
+                // K/V rows appended by an earlier step of this launch: their writer
+                // published them with the layer's attention event of that step --
+                // acquire it (long since met) before the bulk copies read the rows
+                const int pos0 = attn_pos(P, I) - (I.step - P.step);  // first position appended in this launch
+                if (F(I, P_T0) + attn_cached_rows(I, attn_pos(P, I)) > pos0) {
+                    const int ev = F(I, W_SIG);
+                    const uint32_t target = (uint32_t)F(I, P_ATHR) * (uint32_t)I.step;
+                    if (!warp_wait_counter(P, S, ev, target, i, opc)) return false;
+                    fence_proxy_async_global();
                 }
             }
-            __syncwarp();
-            ++ring;
-            if (++rp == (uint32_t)NP) {
-                rp = 0;
-                rph ^= 1;
+            Seg s0, s1;
+            const int nseg = describe<FL>(P, I, s0, s1);
+            // MLP-up pages: groups of 8 gate + 8 up rows (bf16), 16 + 16 (FP8 rows, 32 to a page)
+            const int upg = FL == FL_W8 && F(I, P_W8) != 0 ? W8_ROWS / 2 : 8;
+            if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 4] = gtimer();
+            // Rows go to pages in order, as many whole rows per page as fit.  The
+            // two segments of an MLP-up tile share pages in groups of up to 8:
+            // gate rows 8g .. 8g + 7, then the same up rows (a tile of n <= 8
+            // gate rows is one group: its gate rows, then its up rows).  Attention
+            // keeps its K rows and its V rows on separate pages.
+            const int row_bytes = nseg > 0 ? s0.row_bytes : 0;
+            const int rpp = row_bytes > 0 ? PS / row_bytes : 0;
+            if (nseg > 0 && (rpp < 1 || (nseg > 1 && s1.row_bytes != row_bytes))) {
+                if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 0);
+                return false;
             }
+            // lane 0: copy rows [r, r + n) of a segment to dst
+            auto copy_rows = [&](const Seg &sg, int r, int n, uint8_t *dst, uint64_t *bar) {
+                const uint8_t *src = sg.src + (long long)r * sg.stride;
+                if (sg.stride == sg.row_bytes) {
+                    bulk_g2s(dst, src, (uint32_t)n * row_bytes, bar, pol);
+                } else {
+                    for (int j = 0; j < n; ++j)
+                        bulk_g2s(dst + (size_t)j * row_bytes, src + (long long)j * sg.stride, row_bytes, bar, pol);
+                }
+            };
+            const bool packed = opc != MK_OP_ATTN;
+            const int n0 = nseg > 0 ? s0.rows : 0, n1 = nseg > 1 ? s1.rows : 0;
+            // pages: packed -> over the concatenated rows; attention -> a fixed
+            // number per segment (sized for the split's T rows, filled with the
+            // rows cached so far)
+            const int total = packed ? n0 + n1 : 0;
+            const int npg0 = packed ? 0 : attn_pages(F(I, P_T), P.D, PS);
+            const int npages = packed ? (total + rpp - 1) / (rpp > 0 ? rpp : 1) : 2 * npg0;
+            bool stop = false;
+            for (int k = 0; k < npages; ++k) {
+                if (!warp_wait_bar(P, S, &S.empty()[rp], rph ^ 1, 0, i, opc)) {
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) {
+                    uint8_t *dst = S.pages() + (size_t)rp * PS;
+                    uint64_t *bar = &S.full()[rp];
+                    if (packed) {
+                        const int r = k * rpp, nr = min(rpp, total - r);
+                        mbar_expect_tx(bar, (uint32_t)nr * row_bytes);
+                        if (nseg == 1) {
+                            copy_rows(s0, r, nr, dst, bar);
+                        } else {
+                            const int gs = min(upg, n0);  // group size; n0 is a multiple of it when above it
+                            for (int j = r; j < r + nr;) {
+                                const int g = j / (2 * gs), w = j % (2 * gs);
+                                const bool up = w >= gs;
+                                const int run = min(r + nr - j, gs - (up ? w - gs : w));
+                                copy_rows(up ? s1 : s0, g * gs + (up ? w - gs : w), run, dst + (size_t)(j - r) * row_bytes, bar);
+                                j += run;
+                            }
+                        }
+                    } else {
+                        const bool second = k >= npg0;
+                        const Seg &sg = second ? s1 : s0;
+                        const int r = (second ? k - npg0 : k) * rpp, nr = max(0, min(rpp, sg.rows - r));
+                        mbar_expect_tx(bar, (uint32_t)nr * row_bytes);  // an empty page just completes
+                        if (nr > 0) copy_rows(sg, r, nr, dst, bar);
+                    }
+                }
+                __syncwarp();
+                ++ring;
+                if (++rp == (uint32_t)NP) {
+                    rp = 0;
+                    rph ^= 1;
+                }
+            }
+
+            if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 5] = gtimer();
+            return !stop;
+        };
+        if (POOLS && opc == MK_OP_ATTN_POOL) {
+            // claim the layer's attention tasks one by one (longest first) until none is left
+            const int layer = F(I, P_LAYER), n = F(I, P_PT), base = F(I, P_TBASE);
+            uint32_t *claim = P.claims + (size_t)I.step * P.L + layer;
+            for (;;) {
+                int idx = 0;
+                if (lane == 0) idx = (int)atomicAdd(claim, 1u);
+                idx = __shfl_sync(FULL, idx, 0);
+                const int v = idx < n ? idx : -1;
+                if (!post_claim(P, S, cseq++, v, i, opc)) goto drain;
+                if (v < 0) break;
+                I.w = attn_table_word(P, base + v);
+                if (!ins_valid<FL>(P, I)) {
+                    if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, MK_OP_ATTN, 0);
+                    goto drain;
+                }
+                if (!stream(i, MK_OP_ATTN)) goto drain;
+            }
+            continue;
         }
-        if (P.trace && lane == 0) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 5] = gtimer();
-        if (stop) goto drain;
+        if (!stream(i, opc)) goto drain;
     }
 drain:
     // no bulk copy may still target this CTA's shared memory when it exits
@@ -203,6 +230,7 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
     uint32_t hs = 0;            // activation hand-offs so far; hand-off h uses activation slot h % 2
     HandoffChain chain;
     uint32_t xq = 0;            // tensor-core plans: activation stages (GLM: tiles) staged so far
+    int cseq = 0;               // attention-pool claims taken so far
     WIns I;
     fetch_init(I, P, myq);
     // the instruction's event waits (acquire), right before its activation is read
@@ -255,6 +283,38 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
                 if (lane == 0 && P.trace) P.trace[((size_t)blockIdx.x * P.lmax + i) * 16 + 11] = gtimer();
                 continue;
             }
+        }
+        if (fl_pools(FL, MAXB) && opc == MK_OP_ATTN_POOL) {
+            // the pool's wait (the layer's QKV), then each claimed task's hand-off, as an attention slot's
+            if (!ab && !ins_valid<FL>(P, I)) {
+                if (lane == 0) raise_error(P, S, MK_ERR_DEVICE_CHECK, i, -1, 0, 0, opc, 1);
+                ab = true;
+            }
+            wait_events(i, opc);
+            const int base = F(I, P_TBASE);
+            for (;;) {
+                int v = -1;
+                if (!ab) ab = !read_claim(P, S, cseq++, 0, v, i, opc);
+                if (ab || v < 0) break;
+                I.w = attn_table_word(P, base + v);
+                const int sl = hs & 1;
+                const uint32_t use = hs >> 1;
+                if (!ab) ab = !warp_wait_bar(P, S, &S.act_empty()[sl], (use & 1) ^ 1, 1, i, MK_OP_ATTN);
+                float *slot = reinterpret_cast<float *>(S.act(sl));
+                const bool g4 = P.Hq <= 4 * P.Hkv;
+                if (FL == FL_LEAN || FL == FL_W8 || P.D == 64)
+                    g4 ? stage_attn<64, 4>(P, I, slot, ab, rope64) : stage_attn<64, 8>(P, I, slot, ab, rope64);
+                else g4 ? stage_attn<128, 4>(P, I, slot, ab, rope128) : stage_attn<128, 8>(P, I, slot, ab, rope128);
+                key0 = key1 = -1;
+                __syncwarp();
+                if (lane == 0) {
+                    S.ctrl()[1 + sl] = SLOT_FRESH;
+                    mbar_arrive(&S.act_full()[sl]);
+                }
+                ++hs;
+            }
+            chain.valid = false;
+            continue;
         }
         if (!needs_handoff<FL>(P, I, decode(I), chain)) continue;  // same input as the previous slot: nothing to stage
         const int sl = hs & 1;
@@ -457,6 +517,7 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
     bool ab = false;
     unsigned long long lm_best = 0;
     TcState tc;       // tensor-core plans: tiles and activation stages so far
+    int cseq = 0;     // attention-pool claims taken so far
     WIns I;
     fetch_init(I, P, myq);
     for (I.step = P.step; I.step < P.step + P.nsteps; ++I.step)
@@ -472,6 +533,38 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
         if (opc == MK_OP_NOOP) continue;
         uint64_t t_start = 0;
         if (ct == 0 && P.trace) t_start = gtimer();
+        if (fl_pools(FL, MAXB) && opc == MK_OP_ATTN_POOL) {
+            // every task the loader claimed for this pool, each with its hand-off, as an attention slot
+            const int base = F(I, P_TBASE), cw = ct >> 5;
+            for (;;) {
+                int v = -1;
+                const int seq = cseq++;
+                if (!ab) ab = !read_claim(P, S, seq, 1 + cw, v, i, opc);
+                if (!ab && v < 0) {
+                    // the pool is done here only once its waits are met: the activation loader takes
+                    // this last claim after them (an empty pool has no hand-off to order it)
+                    ab = !warp_wait_smem(P, S, S.claims_taken(), (uint32_t)(seq + 1), i, opc);
+                }
+                if (ab || v < 0) break;
+                I.w = attn_table_word(P, base + v);
+                const int sl = hs & 1;
+                if (!ab) ab = !warp_wait_bar(P, S, &S.act_full()[sl], (hs >> 1) & 1, 2, i, MK_OP_ATTN);
+                const float *slot = reinterpret_cast<const float *>(S.act(sl));
+                if (FL == FL_LEAN || FL == FL_W8 || P.D == 64) attn_task<64, FL>(P, S, I, i, sl, slot, ring, ab);
+                else attn_task<128, FL>(P, S, I, i, sl, slot, ring, ab);
+                rq.set(ring, P.num_pages);
+                ++hs;
+            }
+            chain.valid = false;
+            handoff_progress(S, launch_slot(P, I, i), true);
+            if (ct == 0 && P.trace) {
+                uint64_t *tr = P.trace + ((size_t)blockIdx.x * P.lmax + i) * 16;
+                tr[0] = (uint64_t)opc | ((uint64_t)(uint32_t)d.task << 32);
+                tr[1] = t_start;
+                tr[3] = gtimer();
+            }
+            continue;
+        }
         // tensor-core tiles take no slot hand-off (their input streams into the activation ring)
         const bool handoff =
             (FL == FL_TC && is_gemv_op(opc)) || (FL == FL_GLMTC && opc == MK_OP_GLM_GEMM) ? false
@@ -597,7 +690,8 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
             }
             mbar_init(S.drain(), 1);
         }
-        for (int k = 0; k < CTRL_WORDS; ++k) S.ctrl()[k] = 0;
+        for (int k = 0; k < CTRL_WORDS; ++k)
+            if (k != 31) S.ctrl()[k] = 0;  // (word 31 is the TMEM address, written by warp 3 meanwhile)
         if (TC) {
             for (int p = 0; p < P.num_pages; ++p) S.page_users()[p] = 0;
             // the swizzled stage buffers need 1024-byte alignment: refuse to run otherwise
@@ -615,7 +709,7 @@ __global__ void __launch_bounds__(THREADS, 1) mk_interp(const KParams P) {
     __syncthreads();
     if (TC) tc_fence_after();
     const int32_t *myq = P.queue + (size_t)blockIdx.x * P.lmax * W_WORDS;
-    if (warp == 0) loader_role<FL>(P, S, myq);
+    if (warp == 0) loader_role<MAXB, FL>(P, S, myq);
     else if (warp == 1) aloader_role<MAXB, FL>(P, S, myq);
     else if (warp == PUBLISHER_WARP) publisher_role(P, S, myq);
     else if (warp >= FIRST_CONSUMER_WARP) consumer_role<MAXB, FL>(P, S, myq);
@@ -847,6 +941,7 @@ static int build_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab, std::ve
             r[S_QKV_NORM] = p.bind[MK_BIND_NORM_ATTN][l]; r[S_QKV_H] = hres; r[S_QKV_OUT] = qkv; r[S_QKV_HIST] = hist;
             break;
         case MK_OP_ATTN:
+        case MK_OP_ATTN_POOL:  // (its claimed tasks are attention instructions of this operand row)
             r[S_AT_K] = p.bind[MK_BIND_KCACHE][0] + (uint64_t)l * layer_cache;
             r[S_AT_V] = p.bind[MK_BIND_VCACHE][0] + (uint64_t)l * layer_cache;
             r[S_AT_QKV] = qkv;
@@ -914,7 +1009,8 @@ static int build_table(Plan &p, uint8_t *ws, std::vector<uint64_t> &tab, std::ve
             case MK_OP_QKV:
                 r[S_T_W0] = tmap(wl + 0); r[S_T_W1] = tmap(wl + 1); r[S_T_W2] = tmap(wl + 2); r[S_T_X] = tmap(0);
                 break;
-            case MK_OP_ATTN: r[S_AT_OUT] = xo; break;
+            case MK_OP_ATTN:
+            case MK_OP_ATTN_POOL: r[S_AT_OUT] = xo; break;
             case MK_OP_O: r[S_T_W0] = tmap(wl + 3); r[S_T_X] = tmap(1); r[S_G_OUT] = hres; break;
             case MK_OP_UP:
                 r[S_T_W0] = tmap(wl + 4); r[S_T_W1] = tmap(wl + 5); r[S_T_X] = tmap(0); r[S_G_OUT] = a16;
@@ -950,6 +1046,8 @@ static KParams base_params(const Plan &p, uint8_t *ws) {
     k.H = m.hidden; k.Hq = m.q_heads; k.Hkv = m.kv_heads > 0 ? m.kv_heads : 1; k.D = m.head_dim; k.F = m.ffn;
     k.V = m.vocab; k.L = m.layers; k.Smax = p.smax; k.qk_norm = m.qk_norm; k.nsplit_max = p.nsplit_max;
     k.np = p.tc ? p.np : 0;
+    k.claims = p.attn_table.empty() ? nullptr : reinterpret_cast<uint32_t *>(ws + p.ws.claims);
+    k.attn_table = p.attn_table.empty() ? nullptr : reinterpret_cast<const int32_t *>(ws + p.ws.atab);
     k.eps = m.eps;
     k.theta = m.rope_theta;
     if (p.kind == PLAN_GLM) {
@@ -997,6 +1095,11 @@ int mk_run(mk_plan_t plan, void *workspace, size_t workspace_bytes, int first_st
             if (!p.seq0.empty()) {
                 e = cudaMemcpyAsync(ws + p.ws.seq0, p.seq0.data(), p.seq0.size() * 4, cudaMemcpyHostToDevice, stream);
                 if (e != cudaSuccess) return cuda_fail(e, "upload lengths");
+            }
+            if (!p.attn_table.empty()) {
+                e = cudaMemcpyAsync(ws + p.ws.atab, p.attn_table.data(), p.attn_table.size() * 4,
+                                    cudaMemcpyHostToDevice, stream);
+                if (e != cudaSuccess) return cuda_fail(e, "upload attention task table");
             }
             if (!p.rope_tab.empty()) {
                 e = cudaMemcpyAsync(ws + p.ws.rope, p.rope_tab.data(), p.rope_tab.size() * 4, cudaMemcpyHostToDevice,

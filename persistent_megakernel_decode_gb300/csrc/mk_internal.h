@@ -67,6 +67,14 @@ enum : int {
     P_NSPLIT = W_P + 5, P_LAYER = W_P + 6,
     P_ATHR = W_P + 7,   // threshold of the event the layer's attention tasks signal
 };
+// ATTN_POOL payload (P_LAYER as above): the layer's attention tasks are rows
+// P_TBASE .. P_TBASE + P_PT - 1 of the attention task table, each an ATTN
+// instruction (no waits or signals of its own: the pool slot carries them)
+enum : int {
+    P_PT = W_P + 8,
+    P_TBASE = W_P + 9,
+};
+constexpr int CLAIM_RING = 16;   // claimed task indices in flight between a worker's roles
 
 // GLM block payload.  GEMM tiles use the GEMV fields P_ROW0 (first weight
 // row), P_NROWS (16 or 64), P_K0 (0), P_KC = P_KTOT (K, bytes = elements of
@@ -170,6 +178,8 @@ struct KParams {
     int nsteps;             // steps this launch runs (the queue is walked once per step)
     int num_pages, page_bytes, act_bytes, abuf_bytes, abuf_count, aux_bytes, red_bytes, smem_bytes;
     int B, H, Hq, Hkv, D, F, V, L, Smax, qk_norm, nsplit_max;
+    uint32_t *claims;       // attn_pool plans: task claim counters [max_steps][L]
+    const int32_t *attn_table;  // attn_pool plans: attention task instructions [tasks][32]
     int np;                 // tensor-core plans: the batch padded to 8 or 16 (N = 2 np), else 0;
                             // GLM plans: 16 with tensor-core GEMM tiles, else 0
     float eps, theta;
@@ -229,7 +239,7 @@ inline int red_bytes(int B) { return CONSUMER_WARPS * MAX_TILE_ROWS * B * 4; }
 // attention scratch: each consumer warp's scores over its part of a split
 inline int attn_aux_bytes(int G, int T, int D) { return (CONSUMER_WARPS * ((T + CONSUMER_WARPS / G - 1) / (CONSUMER_WARPS / G)) + 32 + 0 * D) * 4; }
 constexpr int MBAR_BYTES = 512;    // up to 64 mbarriers
-constexpr int CTRL_BYTES = 128;   // 32 flag words
+constexpr int CTRL_BYTES = 256;   // 64 flag words
 constexpr int MAX_PAGES = 26;      // 2 * MAX_PAGES + 5 mbarriers must fit MBAR_BYTES
 constexpr int MAX_PAGES_TC = 16;   // tensor-core plans: 2 * pages + 22 mbarriers
 }  // namespace mk

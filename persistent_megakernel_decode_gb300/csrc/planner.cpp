@@ -301,9 +301,18 @@ std::vector<std::vector<int>> greedy(const std::vector<int> &order, const std::v
     std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
     for (int w = 0; w < workers; ++w) heap.push({0, w});
     std::vector<std::vector<int>> q(workers);
+    std::vector<int64_t> pinned_load(workers, 0);
     for (int t : order) {
+        if (tasks[t].opcode == MK_OP_ATTN_POOL) {  // one attention pool per worker and layer: its own worker
+            const int w = tasks[t].bid[0] % workers;
+            q[w].push_back(t);
+            pinned_load[w] += tasks[t].cost;
+            continue;
+        }
         Item it = heap.top();
         heap.pop();
+        it.first += pinned_load[it.second];
+        pinned_load[it.second] = 0;
         q[it.second].push_back(t);
         it.first += tasks[t].cost;
         heap.push(it);
@@ -374,7 +383,8 @@ std::vector<std::vector<int>> timed(const std::vector<int> &order, const std::ve
         (void)rk;
         heap.pop();
         const TaskRec &t = tasks[id];
-        const double dur = (t.opcode == MK_OP_ATTN ? ATTN_US : TILE_US) + (double)t.cost / bw;
+        const bool attn = t.opcode == MK_OP_ATTN || t.opcode == MK_OP_ATTN_POOL;
+        const double dur = (attn ? ATTN_US : TILE_US) + (double)t.cost / bw;
         int best = 0;
         double best_end = 0.0;
         for (int w = 0; w < workers; ++w) {
@@ -383,6 +393,10 @@ std::vector<std::vector<int>> timed(const std::vector<int> &order, const std::ve
                 best = w;
                 best_end = end;
             }
+        }
+        if (t.opcode == MK_OP_ATTN_POOL) {  // one attention pool per worker and layer: its own worker
+            best = t.bid[0] % workers;
+            best_end = std::max(free_at[best], ready) + dur;
         }
         free_at[best] = best_end;
         q[best].push_back(id);
@@ -603,6 +617,59 @@ int plan_graph(const mk_graph_desc *g, const mk_target_desc *tgt, int num_worker
 // SiLU(g) u as bf16 high/low) -> MLP-down tiles per K chunk (added into the
 // residual); then the final NORM and the LM-head tiles.  Every GEMV tile is
 // 128 weight rows over a K range in stages of 128 columns.
+// attn_pool plans: the payload of every pool instruction (its layer's task
+// rows) and the attention task table -- per layer, the tasks (kv head g,
+// sequence b, split) as ATTN instructions, longest first (cached rows at the
+// last step of the plan; ties in (g, b, split) order).  A table instruction
+// has no waits or signals: its pool slot waits for the layer's QKV and
+// signals the layer's attention event; W_SIG names that event and P_ATHR its
+// per-step threshold for the loader's wait on K/V rows appended by an earlier
+// step of the same launch.
+static void build_attn_pool(Plan &p, int Hkv, int kn_T, const std::vector<int> &nsplit, int max_steps) {
+    const int L = p.model.layers, B = p.B;
+    int per_layer = 0;
+    for (int b = 0; b < B; ++b) per_layer += nsplit[b];
+    per_layer *= Hkv;
+    p.attn_table.assign((size_t)L * per_layer * W_WORDS, 0);
+    std::vector<int> pool_row(L, -1), pool_ev(L, -1), pool_thr(L, 0);
+    for (TaskRec &t : p.tasks) {
+        if (t.opcode != MK_OP_ATTN_POOL) continue;
+        t.payload[P_LAYER - W_P] = t.layer;
+        t.payload[P_PT - W_P] = per_layer;
+        t.payload[P_TBASE - W_P] = t.layer * per_layer;
+        pool_row[t.layer] = t.op_row;
+        pool_ev[t.layer] = t.ns > 0 ? t.s_ev[0] : -1;
+        pool_thr[t.layer] = t.ns > 0 ? p.thresholds[t.s_ev[0]] : 0;
+        t.payload[P_ATHR - W_P] = pool_thr[t.layer];
+    }
+    for (int l = 0; l < L; ++l) {
+        struct Item { int64_t cost; int g, b, s; };
+        std::vector<Item> items;
+        for (int g = 0; g < Hkv; ++g)
+            for (int b = 0; b < B; ++b)
+                for (int sp = 0; sp < nsplit[b]; ++sp) {
+                    const int last = p.seq0[b] + max_steps - 1;
+                    items.push_back({std::max(0, std::min(kn_T, last - sp * kn_T)), g, b, sp});
+                }
+        std::stable_sort(items.begin(), items.end(), [](const Item &x, const Item &y) { return x.cost > y.cost; });
+        for (int idx = 0; idx < (int)items.size(); ++idx) {
+            const Item &it = items[idx];
+            TaskRec a;
+            a.opcode = MK_OP_ATTN;
+            a.op_row = pool_row[l];
+            a.layer = l;
+            int32_t *pl = a.payload;
+            pl[P_G - W_P] = it.g; pl[P_B - W_P] = it.b; pl[P_SPLIT - W_P] = it.s;
+            pl[P_T0 - W_P] = it.s * kn_T; pl[P_T - W_P] = kn_T; pl[P_NSPLIT - W_P] = nsplit[it.b];
+            pl[P_LAYER - W_P] = l; pl[P_ATHR - W_P] = pool_thr[l];
+            const int row = l * per_layer + idx;
+            int32_t *w = &p.attn_table[(size_t)row * W_WORDS];
+            encode_task(a, row, w);
+            w[W_SIG] = pool_ev[l];  // (no signal is counted: W_CNT says none)
+        }
+    }
+}
+
 static int plan_llama_tc(const mk_model_desc *m, const mk_step_desc *s, const mk_target_desc *tgt, int num_workers,
                          int smem_per_cta, Plan &p) {
     const int L = m->layers, H = m->hidden, Hq = m->q_heads, Hkv = m->kv_heads, D = m->head_dim, F = m->ffn,
@@ -673,6 +740,12 @@ static int plan_llama_tc(const mk_model_desc *m, const mk_step_desc *s, const mk
     std::vector<int> nsplit(B);
     for (int b = 0; b < B; ++b) nsplit[b] = ceil_div(p.seq0[b] + s->max_steps, kn_T);
     p.nsplit_max = *std::max_element(nsplit.begin(), nsplit.end());
+    const bool pool = tgt->attn_pool != 0;  // device-side attention dispatch
+    if (pool && B < 2) return set_error(MK_ERR_UNSUPPORTED, "attention pools are for batches of 2 or more");
+    int64_t attn_layer_bytes = 0;           // (the pools' share of it is their scheduling cost)
+    for (int b = 0; b < B; ++b)
+        for (int sp = 0; sp < nsplit[b]; ++sp)
+            attn_layer_bytes += (int64_t)2 * D * 2 * Hkv * std::max(0, std::min(kn_T, p.seq0[b] + s->max_steps - 1 - sp * kn_T));
     std::vector<int> seq0 = p.seq0;
     const int max_steps = s->max_steps;
     std::vector<OpDef> ops;
@@ -698,13 +771,19 @@ static int plan_llama_tc(const mk_model_desc *m, const mk_step_desc *s, const mk
         ops[na].cost = [=](const int *) { return norm_cost; };
         int q = add_op(MK_OP_QKV, l, Hkv, rows_group / TC_M, ks_qkv);
         ops[q].cost = [=](const int *) { return (int64_t)TC_M * (H / ks_qkv) * 2; };
-        int a = add_op(MK_OP_ATTN, l, Hkv, B, p.nsplit_max);
-        ops[a].exists = [nsplit](const int *b) { return b[2] < nsplit[b[1]]; };
-        ops[a].cost = [=](const int *b) {
-            int last = seq0[b[1]] + max_steps - 1;
-            int rows = std::max(0, std::min(kn_T, last - b[2] * kn_T));
-            return (int64_t)2 * D * 2 * rows;
-        };
+        int a;
+        if (pool) {  // one pool per worker; its cost: the layer's attention bytes over the workers
+            a = add_op(MK_OP_ATTN_POOL, l, num_workers, 1, 1);
+            ops[a].cost = [=](const int *) { return attn_layer_bytes / num_workers; };
+        } else {
+            a = add_op(MK_OP_ATTN, l, Hkv, B, p.nsplit_max);
+            ops[a].exists = [nsplit](const int *b) { return b[2] < nsplit[b[1]]; };
+            ops[a].cost = [=](const int *b) {
+                int last = seq0[b[1]] + max_steps - 1;
+                int rows = std::max(0, std::min(kn_T, last - b[2] * kn_T));
+                return (int64_t)2 * D * 2 * rows;
+            };
+        }
         int o = add_op(MK_OP_O, l, H / TC_M, ks_o, 1);
         ops[o].cost = [=](const int *) { return (int64_t)TC_M * (Hq * D / ks_o) * 2; };
         int nm = add_op(MK_OP_NORM, l, B, 1, 1, 1);
@@ -715,8 +794,13 @@ static int plan_llama_tc(const mk_model_desc *m, const mk_step_desc *s, const mk
         ops[d].cost = [=](const int *) { return (int64_t)TC_M * kc * 2; };
         whole(prev, na);                                   // residual h read whole
         whole(na, q);                                      // x^ read whole
-        edges.push_back({q, a, {1, 2, -1}, {1, 0, -1}});   // qkv [B, Hkv, rows]: group & row cuts (K split reduces)
-        edges.push_back({a, o, {1, 0, -1}, {-1, -1, -1}}); // attention output read whole; the split axis reduces
+        if (pool) {
+            whole(q, a);                                   // a pool may claim any group's task
+            whole(a, o);
+        } else {
+            edges.push_back({q, a, {1, 2, -1}, {1, 0, -1}});   // qkv [B, Hkv, rows]: group & row cuts (K split reduces)
+            edges.push_back({a, o, {1, 0, -1}, {-1, -1, -1}}); // attention output read whole; the split axis reduces
+        }
         whole(o, nm);                                      // h after O read whole
         whole(nm, u);                                      // x^ read whole
         edges.push_back({u, d, {1, -1, -1}, {-1, 1, -1}}); // act [B, F]: tiles vs K chunks
@@ -849,6 +933,7 @@ static int plan_llama_tc(const mk_model_desc *m, const mk_step_desc *s, const mk
     const int64_t kv_write = (int64_t)2 * B * Hkv * D * 2 * L;
     const int64_t norms = (int64_t)(2 * L + 1) * H * 2 + (m->qk_norm ? (int64_t)2 * L * D * 2 : 0);
     p.alg_bytes = weights + kv_read + kv_write + norms;
+    if (pool) build_attn_pool(p, Hkv, kn_T, nsplit, max_steps);
     return finish_queues(p, false, p.schedule == MK_SCHED_TIMED);
 }
 
@@ -1059,6 +1144,12 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     for (int b = 0; b < B; ++b) nsplit[b] = ceil_div(p.seq0[b] + s->max_steps, kn_T);
     int ns_max = *std::max_element(nsplit.begin(), nsplit.end());
     p.nsplit_max = ns_max;
+    const bool pool = tgt->attn_pool != 0;  // device-side attention dispatch
+    if (pool && B < 2) return set_error(MK_ERR_UNSUPPORTED, "attention pools are for batches of 2 or more");
+    int64_t attn_layer_bytes = 0;           // (the pools' share of it is their scheduling cost)
+    for (int b = 0; b < B; ++b)
+        for (int sp = 0; sp < nsplit[b]; ++sp)
+            attn_layer_bytes += (int64_t)2 * D * 2 * Hkv * std::max(0, std::min(kn_T, p.seq0[b] + s->max_steps - 1 - sp * kn_T));
     std::vector<int> seq0 = p.seq0;
     const int max_steps = s->max_steps;
     std::vector<OpDef> ops;
@@ -1080,13 +1171,19 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     for (int l = 0; l < L; ++l) {
         int q = add_op(MK_OP_QKV, l, Hkv, rows_group / kn_qkv, 1);
         ops[q].cost = [=](const int *) { return (int64_t)kn_qkv * H * wb; };
-        int a = add_op(MK_OP_ATTN, l, Hkv, B, ns_max);
-        ops[a].exists = [nsplit](const int *b) { return b[2] < nsplit[b[1]]; };
-        ops[a].cost = [=](const int *b) {
-            int last = seq0[b[1]] + max_steps - 1;
-            int rows = std::max(0, std::min(kn_T, last - b[2] * kn_T));
-            return (int64_t)2 * D * 2 * rows;
-        };
+        int a;
+        if (pool) {  // one pool per worker; its cost: the layer's attention bytes over the workers
+            a = add_op(MK_OP_ATTN_POOL, l, num_workers, 1, 1);
+            ops[a].cost = [=](const int *) { return attn_layer_bytes / num_workers; };
+        } else {
+            a = add_op(MK_OP_ATTN, l, Hkv, B, ns_max);
+            ops[a].exists = [nsplit](const int *b) { return b[2] < nsplit[b[1]]; };
+            ops[a].cost = [=](const int *b) {
+                int last = seq0[b[1]] + max_steps - 1;
+                int rows = std::max(0, std::min(kn_T, last - b[2] * kn_T));
+                return (int64_t)2 * D * 2 * rows;
+            };
+        }
         int o = add_op(MK_OP_O, l, ceil_div(H, kn_o), 1, 1);
         ops[o].cost = rows_cost(H, kn_o, Hq * D, wb);
         int u = add_op(MK_OP_UP, l, F / kn_up, 1, 1);
@@ -1095,8 +1192,13 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
         ops[d].cost = rows_cost(H, kn_dn, kn_kc, wb);
         if (prev == emb) edges.push_back({prev, q, {-1, -1, -1}, {-1, -1, -1}});
         else edges.push_back({prev, q, {1, -1, -1}, {-1, -1, -1}});
-        edges.push_back({q, a, {1, 2, -1}, {1, 0, -1}});   // qkv [B, Hkv, rows]: group & row cuts vs batch & group
-        edges.push_back({a, o, {1, 0, -1}, {-1, -1, -1}});  // attn_out read whole; split axis reduces
+        if (pool) {  // a pool may claim any group's task
+            edges.push_back({q, a, {-1, -1, -1}, {-1, -1, -1}});
+            edges.push_back({a, o, {-1, -1, -1}, {-1, -1, -1}});
+        } else {
+            edges.push_back({q, a, {1, 2, -1}, {1, 0, -1}});   // qkv [B, Hkv, rows]: group & row cuts vs batch & group
+            edges.push_back({a, o, {1, 0, -1}, {-1, -1, -1}});  // attn_out read whole; split axis reduces
+        }
         edges.push_back({o, u, {1, -1, -1}, {-1, -1, -1}}); // h read whole
         edges.push_back({u, d, {1, -1, -1}, {-1, 1, -1}});  // act [B, F]: tiles vs K chunks
         prev = d;
@@ -1198,7 +1300,7 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
         default:
             break;
         }
-        if (op.opcode != MK_OP_ATTN && op.opcode != MK_OP_EMBED) {
+        if (op.opcode != MK_OP_ATTN && op.opcode != MK_OP_EMBED && op.opcode != MK_OP_ATTN_POOL) {
             // the tile's rows (MLP-up: gate rows, then up rows) packed into pages
             const bool e4m3 = w8 && op.opcode != MK_OP_LM;
             pl[P_W8 - W_P] = e4m3 ? 1 : 0;
@@ -1215,7 +1317,7 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     // algorithmic bytes at step 0: weights once, KV read, KV append
     int64_t weights = 0;
     for (auto &t : p.tasks)
-        if (t.opcode != MK_OP_ATTN && t.opcode != MK_OP_EMBED) weights += t.cost;
+        if (t.opcode != MK_OP_ATTN && t.opcode != MK_OP_EMBED && t.opcode != MK_OP_ATTN_POOL) weights += t.cost;
     weights += (int64_t)B * H * 2;  // embedding rows
     int64_t kv_read = 0;
     for (int b = 0; b < B; ++b) kv_read += (int64_t)2 * p.seq0[b] * Hkv * D * 2 * L;
@@ -1243,6 +1345,7 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
                           (up ? nrows == 8 * npg : nrows > 16 * (npg - 1) && nrows <= 16 * npg);
         p.lean = ok;
     }
+    if (pool) build_attn_pool(p, Hkv, kn_T, nsplit, s->max_steps);
     return finish_queues(p, false, p.schedule == MK_SCHED_TIMED);
 }
 

@@ -38,6 +38,7 @@ struct Plan {
     mk_model_desc model{};
     mk_glm_desc glm{};           // PLAN_GLM
     std::vector<float> rope_tab;  // PLAN_GLM: (cos, sin) [tokens][32] of each new position
+    std::vector<int32_t> attn_table;  // attn_pool plans: the attention task instructions [L * tasks][32]
     int num_workers = 0, B = 1, max_steps = 1, smax = 0;
     bool capture = false;
     std::vector<int> seq0;
@@ -68,6 +69,7 @@ struct Plan {
     struct {
         uint64_t err, counters, arrive, queue, optab, seq0, rope, hres, hmid, qkv, part, attn_out, act, trace, total;
         uint64_t xn, xo, act16, tmaps;  // tensor-core plans: bf16 high/low activations, tensor maps
+        uint64_t claims, atab;          // attn_pool plans: claim counters [max_steps][L], the task table
         uint64_t gsum[3];               // GLM tensor-core plans: fp32 sums of the K-split GEMMs
                                         // (QKV-A, Head-Gate, Indexer-K)
     } ws{};

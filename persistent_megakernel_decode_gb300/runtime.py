@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmk.so")
 MK_OK, MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_DEADLOCK, MK_ERR_CUDA = 0, 1, 2, 3, 4
 MK_ERR_RESIDENCY, MK_ERR_TIMEOUT, MK_ERR_DEVICE_CHECK, MK_ERR_UNBOUND = 5, 6, 7, 8
 OP_NAMES = {0: "noop", 1: "counter", 2: "embed", 3: "qkv", 4: "attn", 5: "o", 6: "up", 7: "down", 8: "lm",
-            9: "glm_a0", 10: "glm_gemm", 11: "glm_fin", 12: "norm"}
+            9: "glm_a0", 10: "glm_gemm", 11: "glm_fin", 12: "norm", 13: "attn_pool"}
 OPCODE = {v: k for k, v in OP_NAMES.items()}
 MODE_MEGAKERNEL, MODE_PER_OP = 0, 1
 SCHED_DEFAULT, SCHED_BYTES, SCHED_TIMED = 0, 1, 2
@@ -42,7 +42,7 @@ PER_LAYER = ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "norm_attn", "norm_mlp", 
 
 EXPORTED = ["mk_plan", "mk_plan_graph", "mk_plan_info_get", "mk_plan_export", "mk_bind", "mk_run",
             "mk_sync_status", "mk_read_counters", "mk_read_trace", "mk_free", "mk_last_error", "mk_argmax_index",
-            "mk_run_static", "mk_plan_glm", "mk_launch_probe"]
+            "mk_run_static", "mk_plan_glm", "mk_launch_probe", "mk_plan_export_attn_table"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 
@@ -67,7 +67,7 @@ class TargetDesc(C.Structure):
     _fields_ = [("num_sms", C.c_int), ("smem_per_cta", C.c_int), ("mode", C.c_int), ("rows_qkv", C.c_int),
                 ("rows_o", C.c_int), ("rows_up", C.c_int), ("rows_down", C.c_int), ("kchunk_down", C.c_int),
                 ("rows_lm", C.c_int), ("attn_split", C.c_int), ("page_bytes", C.c_int),
-                ("schedule", C.c_int), ("tc_tiles", C.c_int)]
+                ("schedule", C.c_int), ("tc_tiles", C.c_int), ("attn_pool", C.c_int)]
 
 
 class GlmDesc(C.Structure):
@@ -82,7 +82,7 @@ class PlanInfo(C.Structure):
         "smem_bytes", "act_bytes", "rows_qkv", "rows_o", "rows_up", "rows_down", "kchunk_down", "rows_lm",
         "attn_split", "total_slots")] + [("workspace_bytes", C.c_uint64), ("scratch_offset", C.c_uint64),
                                           ("algorithmic_bytes_step", C.c_uint64)] + [
-        (n, C.c_int) for n in ("tc_tiles", "ksplit_qkv", "ksplit_o", "weight_fp8")]
+        (n, C.c_int) for n in ("tc_tiles", "ksplit_qkv", "ksplit_o", "weight_fp8", "attn_table_rows")]
 
 
 class GraphOp(C.Structure):
@@ -127,6 +127,7 @@ def load():
     lib.mk_plan_glm.argtypes = [C.POINTER(GlmDesc), C.POINTER(TargetDesc), C.POINTER(P)]
     lib.mk_plan_info_get.argtypes = [P, C.POINTER(PlanInfo)]
     lib.mk_plan_export.argtypes = [P, P, P, P, P]
+    lib.mk_plan_export_attn_table.argtypes = [P, P]
     lib.mk_bind.argtypes = [P, C.c_int, C.c_int, C.c_uint64]
     lib.mk_run.argtypes = [P, P, C.c_size_t, C.c_int, C.c_int, C.c_uint32, C.c_uint64, P]
     lib.mk_run_static.argtypes = [P, C.c_int, C.c_int, C.c_uint32, C.c_uint64, P, C.POINTER(C.c_uint64)]
@@ -217,6 +218,13 @@ class Plan:
         out = C.c_void_p()
         _check(lib.mk_plan_glm(C.byref(d), C.byref(t), C.byref(out)))
         return cls(out.value)
+
+    def attn_table(self) -> np.ndarray:
+        """attn_pool plans: the attention task table, int32 [rows, 32]."""
+        n = self.info()["attn_table_rows"]
+        out = np.zeros((max(n, 1), 32), np.int32)
+        _check(load().mk_plan_export_attn_table(self.h, C.c_void_p(out.ctypes.data)))
+        return out[:n]
 
     def info(self) -> dict:
         if self._info is None:

@@ -413,3 +413,70 @@ def test_fp8_plan_matches_the_oracle_and_its_tiles():
     kv = 2 * 1024 * sh.Hkv * sh.D * 2 * L + 2 * sh.Hkv * sh.D * 2 * L
     norms = (2 * L + 1) * H * 2
     assert p.info()["algorithmic_bytes_step"] == weights + scales + H * 2 + kv + norms
+
+
+# ---------------------------------------------------------------- attention pools
+
+def _pool_plan(B=8, steps=3, workers=152, **kn):
+    shape = synth.LLAMA_1B
+    seq0 = synth.seq_lengths(synth.WORKLOADS["llama1b_b8"])
+    p = rt.Plan.llama(shape, B, seq0[:B], steps, max(seq0[:B]) + steps + 3, num_sms=workers, smem_per_cta=232448,
+                      attn_pool=1, **kn)
+    return shape, seq0[:B], p
+
+
+@pytest.mark.parametrize("tc", [0, -1], ids=["tcgen05", "warp_mma"])
+def test_attention_pools_one_per_worker_and_layer(tc):
+    """attn_pool plans: no host-dealt attention task; every worker holds exactly
+    one pool slot per layer; O waits for all of them (threshold = workers); a
+    layer's pool waits for its whole QKV op."""
+    shape, seq0, p = _pool_plan(tc_tiles=tc)
+    info = p.info()
+    q, ids, th, tasks = p.export()
+    W = info["num_workers"]
+    assert not (tasks[:, 0] == rt.OPCODE["attn"]).any()
+    pool = tasks[:, 0] == rt.OPCODE["attn_pool"]
+    assert pool.sum() == W * shape.L
+    for l in range(shape.L):
+        rows = np.where(pool & (tasks[:, 1] == l))[0]
+        assert sorted(tasks[rows, 2].tolist()) == list(range(W))       # bid[0] = the worker
+        ev = set(tasks[rows, 17].tolist())
+        assert len(ev) == 1 and th[ev.pop()] == W                       # one event, W signals a step
+        waits = {tuple(tasks[r, 7:10]) for r in rows}
+        assert len(waits) == 1
+        wev, wthr, woff = waits.pop()
+        qkv = (tasks[:, 0] == rt.OPCODE["qkv"]) & (tasks[:, 1] == l)
+        assert woff == 0 and wthr == qkv.sum() == th[wev]                 # the whole QKV op
+    # each worker's queue holds its own pools (slot words carry the worker in the task table)
+    for w in range(W):
+        mine = [t for t in ids[w] if t >= 0 and tasks[t, 0] == rt.OPCODE["attn_pool"]]
+        assert len(mine) == shape.L and all(tasks[t, 2] == w for t in mine)
+
+
+def test_attention_pool_table_covers_each_task_once_longest_first():
+    shape, seq0, p = _pool_plan()
+    info = p.info()
+    tab = p.attn_table()
+    G, T = shape.Hq // shape.Hkv, info["attn_split"]
+    nsplit = [-(-(s0 + 3) // T) for s0 in seq0]
+    per_layer = shape.Hkv * sum(nsplit)
+    assert tab.shape == (shape.L * per_layer, 32)
+    P_G, P_B, P_SPLIT, P_T0, P_T, P_NSPLIT, P_LAYER, P_ATHR = range(14, 22)
+    q, ids, th, tasks = p.export()
+    for l in range(shape.L):
+        rows = tab[l * per_layer:(l + 1) * per_layer]
+        assert (rows[:, 0] == rt.OPCODE["attn"]).all() and (rows[:, 2] == 0).all()   # no waits, no signals
+        keys = sorted((int(r[P_G]), int(r[P_B]), int(r[P_SPLIT])) for r in rows)
+        assert keys == sorted((g, b, s) for g in range(shape.Hkv) for b in range(len(seq0)) for s in range(nsplit[b]))
+        cached = [max(0, min(T, seq0[r[P_B]] + 3 - 1 - r[P_SPLIT] * T)) for r in rows]
+        assert cached == sorted(cached, reverse=True)                                   # longest first
+        assert (rows[:, P_LAYER] == l).all() and (rows[:, P_T0] == rows[:, P_SPLIT] * T).all()
+        assert all(int(r[P_NSPLIT]) == nsplit[r[P_B]] for r in rows)
+        pool_ev = {int(r[10]) for r in rows}
+        assert len(pool_ev) == 1 and (rows[:, P_ATHR] == th[pool_ev.pop()]).all()
+
+
+def test_attention_pools_need_a_batch():
+    with pytest.raises(rt.MkError) as e:
+        rt.Plan.llama(synth.LLAMA_1B, 1, [100], 3, 110, attn_pool=1, num_sms=152, smem_per_cta=232448)
+    assert e.value.code == rt.MK_ERR_UNSUPPORTED
