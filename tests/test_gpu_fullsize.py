@@ -3,7 +3,9 @@ oracle (on the host cores) at the model shapes of the workloads.
 
 * Llama-3.2-1B shape, batch 1, 1024 cached tokens: the benchmarked plan
   (every SM a worker, default tiles: 64 KB pages, the row-per-warp GEMV,
-  9 attention splits);
+  9 attention splits), over 3 steps, and the greedy-argmax bar at full
+  depth: 256 teacher-forced steps (1024 -> 1280 cached tokens), every one
+  checked, at least 99 % identical to the oracle's argmax;
 * the same model at batch 8 with sequence lengths drawn from 512..4096, on
   the tcgen05 tiles (128 weight rows x 8 sequences, TMEM accumulators; the
   default at batch 8) and on the warp-level MMA tiles (16-row m16n8k16 tiles in
@@ -49,6 +51,15 @@ def test_llama1b_batch1_benchmarked_plan():
     w = synth.WORKLOADS["llama1b_b1"]
     run = run_parity(w.shape, [w.seq_len], 3, [0, 2], seed=w.weight_seed)
     _check(run)
+
+
+def test_llama1b_batch1_argmax_over_256_steps_full_depth():
+    from harness import run_parity
+    w = synth.WORKLOADS["llama1b_b1"]
+    run = run_parity(w.shape, [w.seq_len], 256, range(256), seed=w.weight_seed + 7)
+    _check(run)
+    m, t = run.matches()
+    assert t == 256 and m >= 0.99 * t, (m, t)
 
 
 def test_llama1b_batch8_variable_lengths():
