@@ -53,6 +53,22 @@ DEV int stage_pos(int q, bool perm, bool perm8) {
     return perm ? rpw_perm4(q) : q;
 }
 
+// h * w (w: four bf16) and x * s, elementwise
+DEV float4 wmul(float4 x, uint2 w) {
+    x.x *= __uint_as_float(w.x << 16);
+    x.y *= __uint_as_float(w.x & 0xffff0000u);
+    x.z *= __uint_as_float(w.y << 16);
+    x.w *= __uint_as_float(w.y & 0xffff0000u);
+    return x;
+}
+DEV float4 fscale(float4 x, float s) {
+    x.x *= s;
+    x.y *= s;
+    x.z *= s;
+    x.w *= s;
+    return x;
+}
+
 template <bool P8 = false>
 DEV void stage_copy(const float4 *s4, float4 *d4, int n4, bool perm, bool perm8 = false) {
     const int lane = threadIdx.x & 31;
@@ -108,41 +124,35 @@ DEV void stage_gemv(const KParams &P, const WIns &I, float *abuf, bool ab, bool 
                     const int k = base + lane + 32 * j;
                     if (k < n4) {
                         ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
-                        if (!one_round) dst[stage_pos<P8>(k, perm, perm8)] = v[j];
+                        if (!one_round) dst[stage_pos<P8>(k, perm, perm8)] = wmul(v[j], ww[j]);
                         if (hs) hs[k] = v[j];
                     }
                 }
             }
             ss = warp_sum(ss);
             const float scale = rsqrtf(ss / (float)H + P.eps);
-            auto norm = [&](float4 x, uint2 w) {
-                x.x *= scale * __uint_as_float(w.x << 16);
-                x.y *= scale * __uint_as_float(w.x & 0xffff0000u);
-                x.z *= scale * __uint_as_float(w.y << 16);
-                x.w *= scale * __uint_as_float(w.y & 0xffff0000u);
-                return x;
-            };
             if (one_round) {
 #pragma unroll
                 for (int j = 0; j < SC; ++j) {
                     const int k = lane + 32 * j;
-                    if (k < n4) dst[stage_pos<P8>(k, perm, perm8)] = norm(v[j], ww[j]);
+                    if (k < n4) dst[stage_pos<P8>(k, perm, perm8)] = fscale(wmul(v[j], ww[j]), scale);
                 }
             } else {
-                __syncwarp();
-                for (int base = 0; base < n4; base += 32 * SC) {
+                // h * w went to shared memory as each round arrived (the
+                // weights are not loaded twice): apply the scale in place, each
+                // lane to the positions it wrote, a round's loads issued before
+                // its stores
+                for (int base = 0; base < n4; base += 32 * (SC / 2)) {
+                    float4 y[SC / 2];
 #pragma unroll
-                    for (int j = 0; j < SC; ++j) {
+                    for (int j = 0; j < SC / 2; ++j) {
                         const int k = base + lane + 32 * j;
-                        if (k < n4) ww[j] = __ldg(w4 + k);
+                        if (k < n4) y[j] = dst[stage_pos<P8>(k, perm, perm8)];
                     }
 #pragma unroll
-                    for (int j = 0; j < SC; ++j) {
+                    for (int j = 0; j < SC / 2; ++j) {
                         const int k = base + lane + 32 * j;
-                        if (k < n4) {
-                            const int q = stage_pos<P8>(k, perm, perm8);
-                            dst[q] = norm(dst[q], ww[j]);
-                        }
+                        if (k < n4) dst[stage_pos<P8>(k, perm, perm8)] = fscale(y[j], scale);
                     }
                 }
             }
@@ -177,6 +187,20 @@ DEV void stage_resid(const KParams &P, const WIns &I, float *slot) {
         resid[k] = r < nrows ? __ldcg(hres + (size_t)b * P.H + out0 + r) : 0.f;
     }
 }
+// Batch 1 (RESID_ROWS <= 32 values): the load is issued before the
+// activation's first round and stored after it, so both share a round trip.
+DEV float resid_load1(const WIns &I) {
+    const int lane = threadIdx.x & 31;
+    // (instruction fields are warp shuffles: read them in uniform code)
+    const float *hres = reinterpret_cast<const float *>(PTR(I, S_O_HRES));
+    const int out0 = F(I, P_OUT0), nrows = min(F(I, P_NROWS), RESID_ROWS);
+    return lane < nrows ? __ldcg(hres + out0 + lane) : 0.f;
+}
+DEV void resid_store1(const KParams &P, float *slot, float v) {
+    const int lane = threadIdx.x & 31;
+    if (lane < RESID_ROWS) slot_resid(P, slot)[lane] = v;
+}
+static_assert(RESID_ROWS <= 32, "batch-1 residual staging: one value per lane");
 
 // q (pre-scaled by log2(e)/sqrt(D)), new k and v of one (sequence, kv group):
 // q/k RMSNorm (optional), RoPE at the new position (rotate-half pairs,

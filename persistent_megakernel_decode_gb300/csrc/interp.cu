@@ -362,10 +362,17 @@ DEV void aloader_role(const KParams &P, const Smem S, const int32_t *myq) {
             if (key != (bi ? key1 : key0) || F(I, P_SNAP) > 0) {
                 if (!two_bufs && hs > 0 && !ab)
                     ab = !warp_wait_bar(P, S, &S.act_empty()[(hs - 1) & 1], ((hs - 1) >> 1) & 1, 1, i, opc);
+                // batch 1: the O tile's residual rows load in the same round trip as x
+                const float rv = MAXB == 1 && opc == MK_OP_O ? resid_load1(I) : 0.f;
                 stage_gemv<MAXB, FL == FL_W8>(P, I, S.abuf(bi), ab, perm, perm8);
                 flags = SLOT_FRESH;
+                if (opc == MK_OP_O) {
+                    if (MAXB == 1) resid_store1(P, slot, rv);
+                    else stage_resid(P, I, slot);
+                }
+            } else if (opc == MK_OP_O) {
+                stage_resid(P, I, slot);
             }
-            if (opc == MK_OP_O) stage_resid(P, I, slot);
             if (bi) key1 = key;
             else key0 = key;
         } else {
