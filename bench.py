@@ -3,8 +3,13 @@
 Default workload: Llama-3.2-1B shape, batch 1, KV cache pre-filled to 1024
 tokens, random bf16 weights (synthetic; no trained weights, no dataset).  A
 step is one decode step of the whole model: embedding, 16 layers, LM head and
-argmax, run as one persistent kernel launch.  Weights (2.5 GB) exceed the
-129 MB L2, so no flush is needed between steps.
+argmax, run by the persistent kernel.  The timed region runs the steps in
+cooperative launches of up to --steps-per-launch (default 16) steps each: the
+next step's token is the previous step's greedy argmax, read on the device,
+so no step is skipped or cached; --steps-per-launch 1 times one launch per
+step (the side legs report both).  The end-to-end figure keeps one launch per
+step with the token copied in and the argmax copied out each step.  Weights
+(2.5 GB) exceed the 129 MB L2, so no flush is needed between steps.
 
 Arms:
   --impl mk (default)   the CUDA path through the C ABI (libmk)
@@ -305,29 +310,43 @@ def run_mk(args, w, rank, world, dist):
     for kv in args.knob:
         k, v = kv.split("=")
         target[k] = int(v)
+    if w.batch >= 2 and args.mode != "per_op":
+        # batched workloads: attention tasks claimed on the device, longest
+        # first (measured faster at batch 8 and 16); --knob attn_pool=0 deals them on the host
+        target.setdefault("attn_pool", 1)
     sess = rt.Session(s, weights, kc, vc, seq0, max_steps, stream=stream, **target)
     info = sess.plan.info()
     sess.tokens[0] = torch.tensor(synth.first_tokens(w), dtype=torch.int32, device=dev)
     torch.cuda.synchronize()
-    # warm-up
+    # launches of up to `spl` decode steps each (MK_RUN_ONE_LAUNCH: the next
+    # step's token is the previous step's argmax, on the device); the per-op
+    # baseline mode launches per op and step
+    spl = 1 if args.mode == "per_op" else max(1, args.steps_per_launch)
+
+    def chunks(first, n):
+        return [(first + i, min(spl, n - i)) for i in range(0, n, spl)]
+
+    # warm-up, in the same launch shape as the timed steps
     with torch.cuda.stream(stream):
-        for st in range(args.warmup):
-            sess.run(st, 1)
+        for st, k in chunks(0, args.warmup):
+            sess.run(st, k, one_launch=k > 1)
     sess.sync()
-    # timed: one launch per step, events on the launching stream
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    # timed: events on the launching stream around every launch
+    timed = chunks(args.warmup, args.steps)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(timed) + 1)]
     barrier(dist)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         with torch.cuda.stream(stream):
             ev[0].record(stream)
-            for i in range(args.steps):
-                sess.run(args.warmup + i, 1)
-                ev[i + 1].record(stream)
+            for j, (st, k) in enumerate(timed):
+                sess.run(st, k, one_launch=k > 1)
+                ev[j + 1].record(stream)
         stream.synchronize()
     rec = sess.sync()
     barrier(dist)
-    step_ms = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)])
+    # per step: each launch's time over its steps
+    step_ms = np.concatenate([np.full(k, ev[j].elapsed_time(ev[j + 1]) / k) for j, (st, k) in enumerate(timed)])
     total_ms = slowest_replica_ms(float(ev[0].elapsed_time(ev[-1])), dist, dev)
     value = job_rate(w.batch * args.steps, world, total_ms)
     # end to end through the public API with host buffers: token in, argmax out
@@ -377,11 +396,12 @@ def run_mk(args, w, rank, world, dist):
         "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seq_len, "layers": s.L, "hidden": s.H,
                    "vocab": s.V, "mode": args.mode, "weights": "fp8 e4m3, 128x128 block scales" if w.fp8 else "bf16",
                    "l2": f"weights ({alg / 1e9:.2f} GB) exceed L2 (129 MB); no flush",
+                   "steps_per_launch": spl, "knobs": {k: v for k, v in target.items() if k != "mode"},
                    "parallelism": f"replicas{world}"},
         "step_us": {"median": float(np.median(step_ms)) * 1e3, "p10": float(np.percentile(step_ms, 10)) * 1e3,
                     "p90": float(np.percentile(step_ms, 90)) * 1e3},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": args.steps * info["num_launches"], "side": side,
+        "gpu_launches": len(timed) * info["num_launches"], "side": side,
         "plan": {k: info[k] for k in ("num_workers", "lmax", "num_tasks", "num_events", "num_pages", "smem_bytes")},
         "device_error": int(rec.code),
     }
@@ -569,6 +589,8 @@ def main():
     ap.add_argument("--knob", action="append", default=[], help="planner knob, e.g. attn_split=512")
     ap.add_argument("--trace-out", default="",
                     help="after the bench line, run one traced step and write its timeline (JSON) here")
+    ap.add_argument("--steps-per-launch", type=int, default=16,
+                    help="decode steps per cooperative launch in the timed region (1: one launch per step)")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N decoder layers (a small case for profiling, not a bench line)")
     args = ap.parse_args()

@@ -1,8 +1,9 @@
 """Several decode steps in one cooperative launch (MK_RUN_ONE_LAUNCH) against
 the same steps launched one by one -- which the parity tests check against
 the oracle -- on every kernel instance: the lean batch-1 instance (the tiny
-decoder and two layers of the Llama-1B width), the general instance (batch
-3), the tensor-core instance (batch 16) and the GLM block.
+decoder, two layers of the Llama-1B width, and the full benchmarked plan at
+16 steps per launch), the general instance (batch 3), the tensor-core
+instance (batch 16) and the GLM block.
 
 Within one launch every worker walks its queue once per step; the monotone
 event epochs order the steps, the next step's embedding waits for the
@@ -73,6 +74,35 @@ def test_one_launch_matches_step_launches(name, shape, lengths):
         assert _normwise(y.float().cpu().numpy(), x.float().cpu().numpy()) <= 2.0 ** -8
     th = a.plan.export()[2]
     assert (a.counters() == STEPS * th).all() and (b.counters() == STEPS * th).all()
+
+
+def test_benchmarked_plan_16_steps_in_one_launch():
+    """The launch shape the benchmark times: the full 16-layer Llama-1B plan at
+    batch 1 (1024 cached tokens), 16 steps in one launch against 16 launches."""
+    wl = synth.WORKLOADS["llama1b_b1"]
+    steps = 16
+    dev = torch.device("cuda:0")
+
+    def run(one_launch):
+        w = synth.make_weights(wl.shape, wl.weight_seed, device=dev)
+        kc, vc = synth.make_cache(wl.shape, 1, wl.seq_len + steps + 1, wl.cache_seed, device=dev)
+        sess = rt.Session(wl.shape, w, kc, vc, [wl.seq_len], steps)
+        sess.tokens[0] = torch.tensor(synth.first_tokens(wl), dtype=torch.int32, device=dev)
+        if one_launch:
+            sess.run(0, steps, one_launch=True)
+        else:
+            for s in range(steps):
+                sess.run(s, 1)
+        assert sess.sync().code == 0
+        return sess
+
+    a, b = run(False), run(True)
+    assert np.array_equal(a.tokens.cpu().numpy(), b.tokens.cpu().numpy())
+    assert _normwise(b.logits.cpu().numpy(), a.logits.cpu().numpy()) <= 1e-4
+    for x, y in ((a.kcache, b.kcache), (a.vcache, b.vcache)):
+        assert _normwise(y.float().cpu().numpy(), x.float().cpu().numpy()) <= 2.0 ** -8
+    th = a.plan.export()[2]
+    assert (a.counters() == steps * th).all() and (b.counters() == steps * th).all()
 
 
 @pytest.mark.parametrize("tc_tiles", [0, -1], ids=["tcgen05", "warp_mma"])
