@@ -371,9 +371,13 @@ def run_mk(args, w, rank, world, dist):
     alg = info["algorithmic_bytes_step"]
     avg_launch_s = float(np.mean(step_ms)) / 1e3
     achieved = alg / avg_launch_s / 1e9
+    # per launch of `spl` steps: every step streams the whole model, so the
+    # one-step ncu traffic scales with the steps a launch runs
     traffic = profiled_traffic(w.name)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": alg,
+                "traffic": traffic * spl if traffic is not None else None, "peak_kind": peak_kind,
+                "algorithmic_bytes_per_launch": alg * spl, "steps_per_launch": spl,
+                "algorithmic_bytes_per_step": alg, "traffic_per_step": traffic,
                 "kernel": "mk_interp", "nominal_8tbs_frac": achieved / 8000.0}
     cpu = None
     if not args.no_cpu_baseline:
