@@ -56,6 +56,11 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def launch_chunks(first, n, spl):
+    """Steps first .. first + n - 1 as (first step, steps) launches of at most spl steps."""
+    return [(first + i, min(spl, n - i)) for i in range(0, n, spl)]
+
+
 def profiled_traffic(workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
@@ -324,7 +329,7 @@ def run_mk(args, w, rank, world, dist):
     spl = 1 if args.mode == "per_op" else max(1, args.steps_per_launch)
 
     def chunks(first, n):
-        return [(first + i, min(spl, n - i)) for i in range(0, n, spl)]
+        return launch_chunks(first, n, spl)
 
     # warm-up, in the same launch shape as the timed steps
     with torch.cuda.stream(stream):

@@ -39,3 +39,13 @@ def test_reference_arm_other_ranks_do_no_work():
     r = _run({"RANK": "1"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_launch_chunks_cover_every_step_once():
+    import bench
+    for first, n, spl in [(5, 100, 16), (0, 3, 16), (3, 32, 16), (0, 7, 1), (2, 16, 16), (0, 0, 4)]:
+        ch = bench.launch_chunks(first, n, spl)
+        steps = [s for st, k in ch for s in range(st, st + k)]
+        assert steps == list(range(first, first + n))
+        assert all(1 <= k <= spl for _, k in ch)
+        assert len(ch) == -(-n // spl)
