@@ -1231,13 +1231,15 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
     constexpr int NC = DQ / 8;
     const int qtr = lane & 3;
     const int rot = ((NC == 4 ? qtr : 0) + ((lane >> 2) & 1)) % NC;
-    float q[DQ];
+    uint64_t q2[DQ / 2];  // q as fp32 pairs for packed multiply-adds
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
         const float *qs = qp + (hh * 4 + qtr) * QS + ((c + rot) % NC) * 8;
         const float4 v0 = *reinterpret_cast<const float4 *>(qs), v1 = *reinterpret_cast<const float4 *>(qs + 4);
-        q[c * 8] = v0.x; q[c * 8 + 1] = v0.y; q[c * 8 + 2] = v0.z; q[c * 8 + 3] = v0.w;
-        q[c * 8 + 4] = v1.x; q[c * 8 + 5] = v1.y; q[c * 8 + 6] = v1.z; q[c * 8 + 7] = v1.w;
+        q2[c * 4] = pack2(v0.x, v0.y);
+        q2[c * 4 + 1] = pack2(v0.z, v0.w);
+        q2[c * 4 + 2] = pack2(v1.x, v1.y);
+        q2[c * 4 + 3] = pack2(v1.z, v1.w);
     }
     const int tc = min(te, ncache);  // cached tokens of this warp: [tb, tc); the new token, if ours, is ncache
     float m = -INFINITY;
@@ -1249,19 +1251,23 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
             uint4 kw[DQ / 8];
 #pragma unroll
             for (int d = 0; d < DQ / 8; ++d) kw[d] = *reinterpret_cast<const uint4 *>(row + ((d + rot) % NC) * 16);
+            uint64_t sa = 0, sb = 0;
 #pragma unroll
             for (int d = 0; d < DQ / 8; ++d) {
-                float k8[8];
-                bf16x8(kw[d], k8);
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    s0 = fmaf(q[d * 8 + e], k8[e], s0);
-                    s1 = fmaf(q[d * 8 + e + 1], k8[e + 1], s1);
-                }
+                fma2(sa, bf16x2_pair(kw[d].x), q2[d * 4]);
+                fma2(sb, bf16x2_pair(kw[d].y), q2[d * 4 + 1]);
+                fma2(sa, bf16x2_pair(kw[d].z), q2[d * 4 + 2]);
+                fma2(sb, bf16x2_pair(kw[d].w), q2[d * 4 + 3]);
             }
+            s0 = sum2(sa);
+            s1 = sum2(sb);
         } else if (tk < te) {
 #pragma unroll
-            for (int d = 0; d < DQ; ++d) s0 = fmaf(q[d], kn[qtr * DQ + (((d >> 3) + rot) % NC) * 8 + (d & 7)], s0);
+            for (int d = 0; d < DQ; d += 2) {
+                const float *kk = kn + qtr * DQ + (((d >> 3) + rot) % NC) * 8 + (d & 7);
+                s0 = fmaf(__uint_as_float((uint32_t)q2[d / 2]), kk[0], s0);
+                s1 = fmaf(__uint_as_float((uint32_t)(q2[d / 2] >> 32)), kk[1], s1);
+            }
         }
         float s = s0 + s1;
         s += __shfl_xor_sync(FULL, s, 1);
@@ -1289,45 +1295,59 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
     for (int k = 0; k < npg; ++k)
         if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(vring + k) % P.num_pages], ((vring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
     trace_stamp(P, i, 8);
-    float acc[4][PER];
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc[u][e] = 0.f;
-    auto pv = [&](float (&a)[PER], float p, const uint8_t *row) {
-        if constexpr (PER == 2) {
-            const uint32_t u = *reinterpret_cast<const uint32_t *>(row);
-            a[0] = fmaf(p, __uint_as_float(u << 16), a[0]);
-            a[1] = fmaf(p, __uint_as_float(u & 0xffff0000u), a[1]);
-        } else {
-            const uint2 u = *reinterpret_cast<const uint2 *>(row);
-            a[0] = fmaf(p, __uint_as_float(u.x << 16), a[0]);
-            a[1] = fmaf(p, __uint_as_float(u.x & 0xffff0000u), a[1]);
-            a[2] = fmaf(p, __uint_as_float(u.y << 16), a[2]);
-            a[3] = fmaf(p, __uint_as_float(u.y & 0xffff0000u), a[3]);
-        }
+    // P.V: lane (token lane tg, dim group dg) sums 8 dims (one 16-byte load
+    // of a V row) over tokens tb + tg, tb + tg + TG, ... with packed fp32
+    // multiply-adds, two tokens in flight; the TG token lanes are then summed
+    // with shuffles.  A warp instruction reads TG whole rows (conflict-free).
+    constexpr int NG = D / 8, TG = 32 / NG;
+    const int dg = lane % NG, tg = lane / NG;
+    uint64_t a0[4] = {0, 0, 0, 0}, a1[4] = {0, 0, 0, 0};
+    auto pv8 = [&](uint64_t (&a)[4], float p, const uint8_t *row) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(row + dg * 16);
+        const uint64_t pp = pack2(p, p);
+        fma2(a[0], bf16x2_pair(u.x), pp);
+        fma2(a[1], bf16x2_pair(u.y), pp);
+        fma2(a[2], bf16x2_pair(u.z), pp);
+        fma2(a[3], bf16x2_pair(u.w), pp);
     };
-    int t = tb;
+    int t = tb + tg;
     if (npg == 1) {
-        const uint8_t *vl = vpage + lane * PER * 2;
-        for (; t + 4 <= tc; t += 4) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) pv(acc[u], sw[t + u - tb], vl + (size_t)(t + u) * (D * 2));
+        for (; t + TG < tc; t += 2 * TG) {
+            pv8(a0, sw[t - tb], vpage + (size_t)t * (D * 2));
+            pv8(a1, sw[t + TG - tb], vpage + (size_t)(t + TG) * (D * 2));
         }
     } else {
-        for (; t + 4 <= tc; t += 4) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) pv(acc[u], sw[t + u - tb], row_at(true, t + u) + lane * PER * 2);
+        for (; t + TG < tc; t += 2 * TG) {
+            pv8(a0, sw[t - tb], row_at(true, t));
+            pv8(a1, sw[t + TG - tb], row_at(true, t + TG));
         }
     }
-    for (; t < tc; ++t) pv(acc[0], sw[t - tb], row_at(true, t) + lane * PER * 2);
+    if (t < tc) pv8(a0, sw[t - tb], row_at(true, t));
+    float o8[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        o8[2 * j] = __uint_as_float((uint32_t)a0[j]) + __uint_as_float((uint32_t)a1[j]);
+        o8[2 * j + 1] = __uint_as_float((uint32_t)(a0[j] >> 32)) + __uint_as_float((uint32_t)(a1[j] >> 32));
+    }
+#pragma unroll
+    for (int sft = NG; sft < 32; sft <<= 1)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o8[j] += __shfl_xor_sync(FULL, o8[j], sft);
     if (has_new && ncache >= tb && ncache < te) {  // the new token is this warp's
         const float p = sw[ncache - tb];
 #pragma unroll
-        for (int e = 0; e < PER; ++e) acc[1][e] = fmaf(p, vn[lane * PER + e], acc[1][e]);
+        for (int j = 0; j < 8; ++j) o8[j] = fmaf(p, vn[dg * 8 + j], o8[j]);
     }
+    // every lane of a dim group holds its 8 sums: token lane tg keeps the
+    // 8 / TG of them it stores (dims dg * 8 + tg * PER ..)
+    float acc[PER];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[0][e] = (acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e]);
+    for (int e = 0; e < PER; ++e) {
+        float v = o8[e];
+#pragma unroll
+        for (int k = 1; k < TG; ++k) v = tg == k ? o8[k * PER + e] : v;
+        acc[e] = v;
+    }
     __syncwarp();
     if (lane == 0) {
         for (int k = 0; k < npg; ++k) page_release<FL>(S, (vring + k) % P.num_pages);
@@ -1339,7 +1359,7 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
     float *pp = part_base + ((size_t)(b * P.Hq + head) * npieces + split * parts + part) * (D + 2);
     if (!ab) {
 #pragma unroll
-        for (int e = 0; e < PER; ++e) pp[lane * PER + e] = acc[0][e];
+        for (int e = 0; e < PER; ++e) pp[dg * 8 + tg * PER + e] = acc[e];
         if (lane == 0) {
             pp[D] = m;
             pp[D + 1] = l;
