@@ -58,8 +58,8 @@ void layout_workspace(Plan &p) {
         p.ws.hres = take((uint64_t)B * H * 4);
         p.ws.hmid = take((uint64_t)B * H * 4);
         p.ws.qkv = take((uint64_t)B * Hkv * (G + 2) * D * 4);
-        // attention partials: per query head, split and token part (8 / G parts)
-        p.ws.part = take((uint64_t)B * Hq * p.nsplit_max * (CONSUMER_WARPS / G) * (D + 2) * 4);
+        // attention partials: per query head, split and piece of a split
+        p.ws.part = take((uint64_t)B * Hq * p.nsplit_max * attn_split_pieces(G, D) * (D + 2) * 4);
         p.ws.attn_out = take((uint64_t)B * Hq * D * 4);
         p.ws.act = take((uint64_t)B * F * 4);
     } else {

@@ -1180,8 +1180,10 @@ DEV void page_release(const Smem S, int p) {
     }
 }
 
+// Attention, one warp per (q head, token part): head_dim 64, where the
+// per-instruction latency matters more than the instruction count.
 template <int D, int FL>
-DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
+DEV void attn_task_heads(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
                    bool &ab) {
     constexpr int PER = D / 32;
     constexpr int QS = D / 4 + 4;
@@ -1435,6 +1437,382 @@ DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl,
 #pragma unroll
         for (int e = 0; e < PER; ++e) out[((size_t)b * P.Hq + head) * D + lane * PER + e] = o[e] / L;
     }
+}
+
+// Attention of one (sequence, kv head, split of positions).  Each warp takes
+// every q head of its kv group (up to 4; with 8 heads per kv head, two groups
+// of 4 warps) over its share of the split's tokens, so each K / V row is read
+// and converted once per warp, not once per head:
+//   scores   8 lanes per token, D / 8 dims per lane, the 4 heads' sums
+//            reduce-scattered over the 8 lanes (one head's score per lane);
+//   P.V      lane (token lane, group of 8 dims), one 16-byte V load per token
+//            for the 4 heads, then reduce-scattered over the token lanes;
+//   combine  the warps' pieces (o, max, sum) meet in the split's first V page
+//            (after a barrier, so no warp still reads V) and warp h merges head
+//            h's pieces into the split's partial; the last split to arrive for
+//            a head merges the head's partials (log-sum-exp).
+template <int D, int FL>
+DEV void attn_task_group(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
+                   uint32_t &cph, bool &ab) {
+    constexpr int PER = D / 32;              // dims per lane in the merges
+    constexpr int QS = D / 4 + 4;            // staged q: [head][quarter][QS]
+    constexpr int NCH = D / 64;              // 16-byte K chunks per lane and token in the scores
+    constexpr int NG = D / 8, TG = 32 / NG;  // P.V: groups of 8 dims, token lanes
+    const int ct = threadIdx.x - CONSUMER_BASE, warp = ct >> 5, lane = ct & 31;
+    const int G = P.Hq / P.Hkv;
+    const int hpw = G < 4 ? G : 4, tw = G <= 4 ? CONSUMER_WARPS : CONSUMER_WARPS / 2;
+    const int wh = warp / tw, wt = warp % tw;  // head group (heads wh * hpw ..), token part
+    const int b = F(I, P_B), g = F(I, P_G);
+    const int split = F(I, P_SPLIT), nsplit = F(I, P_NSPLIT), layer = F(I, P_LAYER);
+    const int pos = attn_pos(P, I);
+    const int t0 = F(I, P_T0), T = F(I, P_T);
+    const int ncache = attn_cached_rows(I, pos);
+    const bool has_new = pos >= t0 && pos < t0 + T;
+    const int ntot = ncache + (has_new ? 1 : 0);
+    const int tp = (T + tw - 1) / tw;
+    const int tb = wt * tp, te = min(ntot, tb + tp);  // this warp's tokens [tb, te) of the split
+    const int tc = min(te, ncache);                    // cached ones [tb, tc); the new token, if ours, is ncache
+    const float *qp = slot, *kn = slot + G * 4 * QS, *vn = kn + D;
+    float *sw = S.aux() + warp * hpw * tp;  // this warp's scores, then probabilities: [hpw][tp]
+    float *part_base = reinterpret_cast<float *>(PTR(I, S_AT_PART));
+    float *out = reinterpret_cast<float *>(PTR(I, S_AT_OUT));
+    uint32_t *arrive = reinterpret_cast<uint32_t *>(PTR(I, S_AT_ARRIVE));
+    const int rpp = P.page_bytes / (D * 2);
+    const int npg = attn_pages(T, D, P.page_bytes);  // K pages, then as many V pages
+    const uint32_t kring = ring, vring = ring + npg;
+    ring = vring + npg;
+    // the split's K (V) rows are consecutive rows of its K (V) page(s), rpp
+    // (a power of two) to a page; a split spans at most 4 pages of each
+    auto page_ptr = [&](uint32_t r) { return S.pages() + (size_t)(r % P.num_pages) * P.page_bytes; };
+    uint8_t *vpage = page_ptr(vring);
+    const uint8_t *kpage = page_ptr(kring);
+    const uint8_t *kp1 = page_ptr(kring + 1), *kp2 = page_ptr(kring + 2), *kp3 = page_ptr(kring + 3);
+    const uint8_t *vp1 = page_ptr(vring + 1), *vp2 = page_ptr(vring + 2), *vp3 = page_ptr(vring + 3);
+    const int rsh = 31 - __clz(rpp);
+    auto row_at = [&](bool v, int tk) -> const uint8_t * {
+        const int j = tk >> rsh;
+        const uint8_t *pg = j == 0 ? (v ? vpage : kpage) : j == 1 ? (v ? vp1 : kp1) : j == 2 ? (v ? vp2 : kp2)
+                                                                                        : (v ? vp3 : kp3);
+        return pg + (size_t)(tk & (rpp - 1)) * (D * 2);
+    };
+    for (int k = 0; k < npg; ++k)
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(kring + k) % P.num_pages], ((kring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
+    trace_stamp(P, i, 6);
+    // ---- scores.  Lane (tl, dq): token t + tl of a round of 4, dims
+    // c * 64 + dq * 8 .. + 8 of each chunk c: the 8 lanes of a token read 128
+    // contiguous bytes of its row, a warp 4 rows (conflict-free).
+    const int tl = lane >> 3, dq = lane & 7;
+    uint64_t q2[4][NCH * 4];  // q of the warp's heads (zero past hpw) as fp32 pairs
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int d0 = c * 64 + dq * 8, hh = wh * hpw + (j < hpw ? j : 0);
+            const float *qs = qp + (hh * 4 + d0 / (D / 4)) * QS + d0 % (D / 4);
+            float4 v0 = *reinterpret_cast<const float4 *>(qs), v1 = *reinterpret_cast<const float4 *>(qs + 4);
+            if (j >= hpw) v0 = v1 = make_float4(0.f, 0.f, 0.f, 0.f);
+            q2[j][c * 4] = pack2(v0.x, v0.y);
+            q2[j][c * 4 + 1] = pack2(v0.z, v0.w);
+            q2[j][c * 4 + 2] = pack2(v1.x, v1.y);
+            q2[j][c * 4 + 3] = pack2(v1.z, v1.w);
+        }
+    // after the reduce-scatter lane dq holds the score of head hown
+    const int hown = ((dq >> 2) & 1) * 2 + ((dq >> 1) & 1);
+    float mown = -INFINITY;
+    for (int t = tb; t < te; t += 4) {
+        const int tk = t + tl;
+        uint64_t a[4] = {0, 0, 0, 0};
+        auto dot = [&](int c, uint64_t k0, uint64_t k1, uint64_t k2, uint64_t k3) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                fma2(a[j], k0, q2[j][c * 4]);
+                fma2(a[j], k1, q2[j][c * 4 + 1]);
+                fma2(a[j], k2, q2[j][c * 4 + 2]);
+                fma2(a[j], k3, q2[j][c * 4 + 3]);
+            }
+        };
+        if (tk < tc) {
+            const uint8_t *row = row_at(false, tk) + dq * 16;
+            uint4 kw[NCH];
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) kw[c] = *reinterpret_cast<const uint4 *>(row + c * 128);
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+                dot(c, bf16x2_pair(kw[c].x), bf16x2_pair(kw[c].y), bf16x2_pair(kw[c].z), bf16x2_pair(kw[c].w));
+        } else if (tk < te) {  // the new token: its k staged in fp32 (bf16-rounded)
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                const float *kk = kn + c * 64 + dq * 8;
+                const float4 x0 = *reinterpret_cast<const float4 *>(kk), x1 = *reinterpret_cast<const float4 *>(kk + 4);
+                dot(c, pack2(x0.x, x0.y), pack2(x0.z, x0.w), pack2(x1.x, x1.y), pack2(x1.z, x1.w));
+            }
+        }
+        float s[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[j] = sum2(a[j]);
+        // reduce-scatter over the 8 dim lanes: xor 4 keeps heads {0,1} or
+        // {2,3}, xor 2 one of the pair, xor 1 completes the sum
+        const bool h4 = dq & 4, h2 = dq & 2;
+        const float r0 = __shfl_xor_sync(FULL, h4 ? s[0] : s[2], 4);
+        const float r1 = __shfl_xor_sync(FULL, h4 ? s[1] : s[3], 4);
+        const float u0 = (h4 ? s[2] : s[0]) + r0, u1 = (h4 ? s[3] : s[1]) + r1;
+        float v = (h2 ? u1 : u0) + __shfl_xor_sync(FULL, h2 ? u0 : u1, 2);
+        v += __shfl_xor_sync(FULL, v, 1);
+        if (tk < te && hown < hpw) {
+            if ((dq & 1) == 0) sw[hown * tp + tk - tb] = v;
+            mown = fmaxf(mown, v);
+        }
+    }
+    mown = fmaxf(mown, __shfl_xor_sync(FULL, mown, 8));
+    mown = fmaxf(mown, __shfl_xor_sync(FULL, mown, 16));
+    float M[4];  // head j's maximum sits on lanes 2j, 2j + 1
+#pragma unroll
+    for (int j = 0; j < 4; ++j) M[j] = __shfl_sync(FULL, mown, 2 * j);
+    trace_stamp(P, i, 7);
+    __syncwarp();
+    if (lane == 0)
+        for (int k = 0; k < npg; ++k) page_release<FL>(S, (kring + k) % P.num_pages);
+    float l4[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int t = lane; t < te - tb; t += 32) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (j < hpw) {
+                const float e = exp2f(sw[j * tp + t] - M[j]);
+                sw[j * tp + t] = e;
+                l4[j] += e;
+            }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) l4[j] = warp_sum(l4[j]);
+    __syncwarp();
+    // ---- P.V
+    for (int k = 0; k < npg; ++k)
+        if (!ab) ab = !warp_wait_bar(P, S, &S.full()[(vring + k) % P.num_pages], ((vring + k) / P.num_pages) & 1, 2, i, MK_OP_ATTN);
+    trace_stamp(P, i, 8);
+    const int dg = lane % NG, tg = lane / NG;
+    uint64_t acc[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[j][k] = 0;
+    auto pv = [&](int t, const uint8_t *row) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(row + dg * 16);
+        const uint64_t v0 = bf16x2_pair(u.x), v1 = bf16x2_pair(u.y), v2 = bf16x2_pair(u.z), v3 = bf16x2_pair(u.w);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float p = j < hpw ? sw[j * tp + t - tb] : 0.f;
+            const uint64_t pp = pack2(p, p);
+            fma2(acc[j][0], v0, pp);
+            fma2(acc[j][1], v1, pp);
+            fma2(acc[j][2], v2, pp);
+            fma2(acc[j][3], v3, pp);
+        }
+    };
+    if (npg == 1) {
+        for (int t = tb + tg; t < tc; t += TG) pv(t, vpage + (size_t)t * (D * 2));
+    } else {
+        for (int t = tb + tg; t < tc; t += TG) pv(t, row_at(true, t));
+    }
+    // reduce-scatter over the TG token lanes: each lane keeps 8 dims of
+    // 4 / TG heads, hk[0 .. 4 / TG) (TG = 2: heads 2 tg, 2 tg + 1; TG = 4:
+    // head 2 (tg & 1) + (tg >> 1))
+    constexpr int HK = 4 / TG;
+    float o[HK][8];
+    int hk[HK];
+    {
+        const bool b0 = tg & 1;
+        uint64_t keep[2][4];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t send = b0 ? acc[jj][k] : acc[2 + jj][k];
+                const uint64_t mine = b0 ? acc[2 + jj][k] : acc[jj][k];
+                const uint64_t r = __shfl_xor_sync(FULL, send, NG);
+                keep[jj][k] = pack2(__uint_as_float((uint32_t)mine) + __uint_as_float((uint32_t)r),
+                                    __uint_as_float((uint32_t)(mine >> 32)) + __uint_as_float((uint32_t)(r >> 32)));
+            }
+        if constexpr (TG == 2) {
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                hk[jj] = 2 * (b0 ? 1 : 0) + jj;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    o[jj][2 * k] = __uint_as_float((uint32_t)keep[jj][k]);
+                    o[jj][2 * k + 1] = __uint_as_float((uint32_t)(keep[jj][k] >> 32));
+                }
+            }
+        } else {
+            const bool b1 = tg & 2;
+            hk[0] = 2 * (b0 ? 1 : 0) + (b1 ? 1 : 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t send = b1 ? keep[0][k] : keep[1][k];
+                const uint64_t mine = b1 ? keep[1][k] : keep[0][k];
+                const uint64_t r = __shfl_xor_sync(FULL, send, 2 * NG);
+                o[0][2 * k] = __uint_as_float((uint32_t)mine) + __uint_as_float((uint32_t)r);
+                o[0][2 * k + 1] = __uint_as_float((uint32_t)(mine >> 32)) + __uint_as_float((uint32_t)(r >> 32));
+            }
+        }
+    }
+    if (has_new && ncache >= tb && ncache < te) {  // the new token is this warp's
+#pragma unroll
+        for (int jj = 0; jj < HK; ++jj) {
+            const float p = hk[jj] < hpw ? sw[hk[jj] * tp + ncache - tb] : 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[jj][e] = fmaf(p, vn[dg * 8 + e], o[jj][e]);
+        }
+    }
+    // ---- combine the warps' pieces in the first V page: [warp][head 0..3][D]
+    // fp32 (at most 16 KB, one page); max and sum over the slot's staged q
+    // (dead by now; the slot, like the page, is not refilled before every
+    // warp has released it)
+    consumer_sync(P, S, cph, ab, i);  // no warp reads V, q, k or v any more (a bounded wait)
+    float *cb = reinterpret_cast<float *>(vpage);
+    float *mlb = const_cast<float *>(slot);  // [warp][head 0..3][2]
+#pragma unroll
+    for (int jj = 0; jj < HK; ++jj)
+        if (hk[jj] < hpw) {
+            float4 *dst = reinterpret_cast<float4 *>(cb + (size_t)(warp * 4 + hk[jj]) * D + dg * 8);
+            dst[0] = make_float4(o[jj][0], o[jj][1], o[jj][2], o[jj][3]);
+            dst[1] = make_float4(o[jj][4], o[jj][5], o[jj][6], o[jj][7]);
+        }
+    if (lane < hpw) {
+        float mj = M[0], lj = l4[0];
+#pragma unroll
+        for (int j = 1; j < 4; ++j) {
+            mj = lane == j ? M[j] : mj;
+            lj = lane == j ? l4[j] : lj;
+        }
+        mlb[(warp * 4 + lane) * 2] = mj;
+        mlb[(warp * 4 + lane) * 2 + 1] = lj;
+    }
+    // the page's next contents arrive by bulk copy (async proxy)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    consumer_sync(P, S, cph, ab, i);
+    const bool merger = warp < G;  // warp h merges head h of the kv group
+    if (!merger) {
+        __syncwarp();
+        if (lane == 0) {
+            for (int k = 0; k < npg; ++k) page_release<FL>(S, (vring + k) % P.num_pages);
+            mbar_arrive(&S.act_empty()[sl]);  // q, k, v of the slot no longer needed by this warp
+        }
+        trace_stamp(P, i, 9);
+        trace_stamp(P, i, 10);
+        return;
+    }
+    const int jm = warp % hpw, src0 = (warp / hpw) * tw;  // the head's pieces: warps src0 .. src0 + tw
+    float Mx = -INFINITY;
+    for (int k = 0; k < tw; ++k) Mx = fmaxf(Mx, mlb[((src0 + k) * 4 + jm) * 2]);
+    float L = 0.f, om[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) om[e] = 0.f;
+    if (Mx != -INFINITY) {
+        for (int k = 0; k < tw; ++k) {
+            const float f = exp2f(mlb[((src0 + k) * 4 + jm) * 2] - Mx);  // 0 for a warp with no tokens
+            L += f * mlb[((src0 + k) * 4 + jm) * 2 + 1];
+            const float *ps = cb + (size_t)((src0 + k) * 4 + jm) * D + lane * PER;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) om[e] = fmaf(f, ps[e], om[e]);
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        for (int k = 0; k < npg; ++k) page_release<FL>(S, (vring + k) % P.num_pages);
+        mbar_arrive(&S.act_empty()[sl]);
+    }
+    trace_stamp(P, i, 9);
+    // the split's partial (o[D], max, sum) of head (b, g * G + warp)
+    const int head = g * G + warp;
+    float *pp = part_base + ((size_t)(b * P.Hq + head) * P.nsplit_max + split) * (D + 2);
+    if (!ab) {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) pp[lane * PER + e] = om[e];
+        if (lane == 0) {
+            pp[D] = Mx;
+            pp[D + 1] = L;
+        }
+    }
+    // the acq_rel add is cumulative over this warp's partial (ordered by the
+    // warp barrier) and acquires the other splits' partials
+    __syncwarp();
+    int last = 0;
+    if (lane == 0 && !ab) {
+        const uint32_t old = atom_acqrel_add(arrive + ((size_t)layer * P.B + b) * P.Hq + head, 1u);
+        last = old == (uint32_t)(I.step + 1) * (uint32_t)nsplit - 1u;
+    }
+    trace_stamp(P, i, 10);
+    if (!__shfl_sync(FULL, last, 0)) return;
+    __syncwarp();
+    // merge: log-sum-exp over the head's splits, MB at a time so that their
+    // L2 round trips overlap
+    const float *hb = part_base + (size_t)(b * P.Hq + head) * P.nsplit_max * (D + 2);
+    const int n = nsplit;
+    float MM = -INFINITY, LL = 0.f, ov2[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) ov2[e] = 0.f;
+    constexpr int MB = PER <= 2 ? 16 : 8;
+    for (int s0 = 0; s0 < n; s0 += MB) {
+        float mv[MB], lv[MB], ov[MB][PER];
+#pragma unroll
+        for (int u = 0; u < MB; ++u) {
+            const int sp = s0 + u;
+            if (sp < n) {
+                const float *ps = hb + (size_t)sp * (D + 2);
+                mv[u] = __ldcg(ps + D);
+                lv[u] = __ldcg(ps + D + 1);
+#pragma unroll
+                for (int e = 0; e < PER; ++e) ov[u][e] = __ldcg(ps + lane * PER + e);
+            } else {
+                mv[u] = -INFINITY;
+                lv[u] = 0.f;
+#pragma unroll
+                for (int e = 0; e < PER; ++e) ov[u][e] = 0.f;
+            }
+        }
+        float Mn = MM;
+#pragma unroll
+        for (int u = 0; u < MB; ++u) Mn = fmaxf(Mn, mv[u]);
+        if (Mn == -INFINITY) continue;  // nothing yet
+        const float r = exp2f(MM - Mn);  // rescale what was accumulated so far
+        LL *= r;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) ov2[e] *= r;
+#pragma unroll
+        for (int u = 0; u < MB; ++u) {
+            const float f = exp2f(mv[u] - Mn);  // 0 for empty pieces
+            LL += f * lv[u];
+#pragma unroll
+            for (int e = 0; e < PER; ++e) ov2[e] += f * ov[u][e];
+        }
+        MM = Mn;
+    }
+    if constexpr (FL == FL_TC) {
+        // the O tiles' input: bf16 high and low rows b and np + b of [2 np, Hq D]
+        uint16_t *o16 = reinterpret_cast<uint16_t *>(out);
+        const size_t ld = (size_t)P.Hq * D;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            const float v = ov2[e] / LL;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+            o16[(size_t)b * ld + (size_t)head * D + lane * PER + e] = __bfloat16_as_ushort(hi);
+            o16[(size_t)(P.np + b) * ld + (size_t)head * D + lane * PER + e] = __bfloat16_as_ushort(lo);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) out[((size_t)b * P.Hq + head) * D + lane * PER + e] = ov2[e] / LL;
+    }
+}
+
+// One attention instruction: the per-head form at head_dim 64, the grouped
+// form (fewer loads and conversions per K / V byte) at head_dim 128.  A split
+// leaves attn_split_pieces(G, D) partials per head (the workspace's stride).
+template <int D, int FL>
+DEV void attn_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, const float *slot, uint32_t &ring,
+                   uint32_t &cph, bool &ab) {
+    if constexpr (D == 64) attn_task_heads<D, FL>(P, S, I, i, sl, slot, ring, ab);
+    else attn_task_group<D, FL>(P, S, I, i, sl, slot, ring, cph, ab);
 }
 
 DEV void embed_task(const KParams &P, const Smem S, const WIns &I, int i, int sl, bool ab) {

@@ -557,8 +557,8 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
                 const int sl = hs & 1;
                 if (!ab) ab = !warp_wait_bar(P, S, &S.act_full()[sl], (hs >> 1) & 1, 2, i, MK_OP_ATTN);
                 const float *slot = reinterpret_cast<const float *>(S.act(sl));
-                if (FL == FL_LEAN || FL == FL_W8 || P.D == 64) attn_task<64, FL>(P, S, I, i, sl, slot, ring, ab);
-                else attn_task<128, FL>(P, S, I, i, sl, slot, ring, ab);
+                if (FL == FL_LEAN || FL == FL_W8 || P.D == 64) attn_task<64, FL>(P, S, I, i, sl, slot, ring, cph, ab);
+                else attn_task<128, FL>(P, S, I, i, sl, slot, ring, cph, ab);
                 rq.set(ring, P.num_pages);
                 ++hs;
             }
@@ -602,8 +602,8 @@ DEV void consumer_role(const KParams &P, const Smem S, const int32_t *myq) {
                 wrote = false;
             }
         } else if (opc == MK_OP_ATTN) {
-            if (FL == FL_LEAN || FL == FL_W8 || P.D == 64) attn_task<64, FL>(P, S, I, i, sl, slot, ring, ab);
-            else attn_task<128, FL>(P, S, I, i, sl, slot, ring, ab);
+            if (FL == FL_LEAN || FL == FL_W8 || P.D == 64) attn_task<64, FL>(P, S, I, i, sl, slot, ring, cph, ab);
+            else attn_task<128, FL>(P, S, I, i, sl, slot, ring, cph, ab);
             rq.set(ring, P.num_pages);
         } else if (FL == FL_TC && is_gemv_op(opc)) {
             wrote = tc_tile(P, S, I, d, i, ring, tc, lm_best, ab);

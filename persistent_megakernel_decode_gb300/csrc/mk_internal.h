@@ -222,6 +222,9 @@ constexpr int TC_WMAPS_PER_LAYER = 7;  // Wq, Wk, Wv, Wo, Wg, Wu, Wd
 // Pages of the ring an attention instruction takes: ceil(T / rows per page)
 // pages of K rows, then as many of V rows, however many rows are cached yet
 // (the others stay empty), so that the count is fixed by the plan.
+// Attention partials a split leaves per query head: one per token part of
+// the per-head form (head_dim 64), one of the grouped form (head_dim 128).
+MK_HD inline int attn_split_pieces(int G, int D) { return D == 64 ? CONSUMER_WARPS / G : 1; }
 MK_HD inline int attn_pages(int T, int D, int page_bytes) {
     return (T + page_bytes / (2 * D) - 1) / (page_bytes / (2 * D));
 }
