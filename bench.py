@@ -315,10 +315,9 @@ def run_mk(args, w, rank, world, dist):
     for kv in args.knob:
         k, v = kv.split("=")
         target[k] = int(v)
-    if w.batch >= 2 and args.mode != "per_op":
-        # batched workloads: attention tasks claimed on the device, longest
-        # first (measured faster at batch 8 and 16); --knob attn_pool=0 deals them on the host
-        target.setdefault("attn_pool", 1)
+    # batched workloads: attention tasks dealt on the host by the time-model
+    # scheduler (with 512-position splits measured faster than device-side
+    # claims at batch 8 and 16); --knob attn_pool=1 claims them on the device
     sess = rt.Session(s, weights, kc, vc, seq0, max_steps, stream=stream, **target)
     info = sess.plan.info()
     sess.tokens[0] = torch.tensor(synth.first_tokens(w), dtype=torch.int32, device=dev)

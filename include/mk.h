@@ -240,7 +240,7 @@ typedef struct {
  * batch-1 row-per-warp GEMV (K <= 2048 with x in registers; K = 4096 in
  * pages of 8 rows with x in shared memory), 16-row tensor-core tiles when
  * every K is a multiple of 512, else split-K tiles.  Unless the target fixes
- * it, the attention split (16384 / (2 D) positions) doubles, up to 256, while
+ * it, the attention split (16384 / (2 D) positions) doubles, up to 512, while
  * its tasks outnumber the workers.  The plan is checked by simulating its
  * queues.  *out receives a plan the
  * caller frees with mk_free().  Returns MK_ERR_INVALID / MK_ERR_UNSUPPORTED

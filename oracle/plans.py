@@ -152,7 +152,7 @@ def llama_knobs(shape: LlamaShape, B: int, seq0: Sequence[int], max_steps: int, 
     * Batch 1 with pages of exactly 16 rows: QKV 32 rows, MLP-up 64 gate rows,
       MLP-down 64 rows, LM head one tile per worker (whole pages).
     * Batch above 4 without the tensor-core tiles' pages: at most 8 rows (MLP-up 4).
-    * Attention: 16384 / (2 head_dim) positions, doubled up to 256 while the
+    * Attention: 16384 / (2 head_dim) positions, doubled up to 512 while the
       attention tasks outnumber the workers.
     """
     H, Hq, Hkv, D, F, V = shape.H, shape.Hq, shape.Hkv, shape.D, shape.F, shape.V
@@ -179,7 +179,7 @@ def llama_knobs(shape: LlamaShape, B: int, seq0: Sequence[int], max_steps: int, 
     down = pow2_floor(clamp(tile // (2 * kc), 1, rcap))
     lm = pow2_floor(clamp(tile // (2 * H), 1, rcap))
     T = clamp(16384 // (2 * D), 16, 256)
-    while 2 * T <= 256 and sum(_ceil(s + max_steps, T) for s in seq0) * Hkv > n_workers:
+    while 2 * T <= 512 and sum(_ceil(s + max_steps, T) for s in seq0) * Hkv > n_workers:
         T *= 2
     # shared memory beside the pages
     kmax = max(H, Hq * D, kc)
@@ -230,7 +230,7 @@ def tc_knobs(shape: LlamaShape, B: int, seq0: Sequence[int], max_steps: int, n_w
     workers with whole 128-column stages; the MLP-down K chunk is the largest
     of 2048, 1024, 512, 256 dividing the ffn that gives at least half as many
     tasks as workers (else the smallest that divides); the attention split is
-    16384 / (2 head_dim) positions, doubled up to 256 while the attention
+    16384 / (2 head_dim) positions, doubled up to 512 while the attention
     tasks outnumber the workers."""
     G = shape.Hq // shape.Hkv
 
@@ -247,7 +247,7 @@ def tc_knobs(shape: LlamaShape, B: int, seq0: Sequence[int], max_steps: int, n_w
             if (shape.H // TC_M) * (shape.F // c) * 2 >= n_workers:
                 break
     T = max(16, min(256, 16384 // (2 * shape.D)))
-    while 2 * T <= 256 and sum(_ceil(s + max_steps, T) for s in seq0) * shape.Hkv > n_workers:
+    while 2 * T <= 512 and sum(_ceil(s + max_steps, T) for s in seq0) * shape.Hkv > n_workers:
         T *= 2
     return TcKnobs(ksplit(shape.Hkv * (G + 2) * shape.D // TC_M, shape.H), ksplit(shape.H // TC_M, shape.Hq * shape.D),
                    kc, T)

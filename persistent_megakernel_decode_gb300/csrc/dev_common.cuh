@@ -624,7 +624,7 @@ DEV bool ins_valid(const KParams &P, const WIns &I) {
     }
     if (opc == MK_OP_ATTN) {
         const int T = F(I, P_T);
-        if (T <= 0 || T > 256 || F(I, P_B) >= P.B || F(I, P_G) >= P.Hkv || F(I, P_SPLIT) >= P.nsplit_max) return false;
+        if (T <= 0 || T > 512 || F(I, P_B) >= P.B || F(I, P_G) >= P.Hkv || F(I, P_SPLIT) >= P.nsplit_max) return false;
         if (attn_pages(T, P.D, P.page_bytes) > 4) return false;  // a split spans at most 4 pages of K (and of V)
     }
     return true;

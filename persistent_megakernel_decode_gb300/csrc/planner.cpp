@@ -718,9 +718,9 @@ static int plan_llama_tc(const mk_model_desc *m, const mk_step_desc *s, const mk
             for (int b = 0; b < B; ++b) n += ceil_div(s->seq_len0[b] + s->max_steps, T);
             return n * Hkv;
         };
-        while (2 * kn_T <= 256 && attn_tasks(kn_T) > (int64_t)num_workers) kn_T *= 2;
+        while (2 * kn_T <= 512 && attn_tasks(kn_T) > (int64_t)num_workers) kn_T *= 2;
     }
-    if (kn_T > 256 || kn_T < 1) return set_error(MK_ERR_UNSUPPORTED, "attn_split must be 1..256");
+    if (kn_T > 512 || kn_T < 1) return set_error(MK_ERR_UNSUPPORTED, "attn_split must be 1..512");
     p.attn_split = kn_T;
     // shared memory: activation ring | two attention slots | pages | op scratch | barriers | flags,
     // the ring and the pages 1024-byte aligned (swizzled TMA boxes)
@@ -732,8 +732,9 @@ static int plan_llama_tc(const mk_model_desc *m, const mk_step_desc *s, const mk
     p.aux_bytes = round_up(attn_aux_bytes(G, kn_T, D), 128) + 2 * TC_SEG * TC_MAXB * 4 + NRED * p.red_bytes;
     const int fixed = p.abuf_count * p.abuf_bytes + 2 * p.act_bytes + p.aux_bytes + MBAR_BYTES + CTRL_BYTES;
     p.num_pages = std::min(8, (smem_per_cta - fixed) / p.page_bytes);
-    const int attn_need = 2 * attn_pages(kn_T, D, p.page_bytes);
-    if (p.num_pages < std::max(3, attn_need))
+    // an attention task holds its K pages, releases them, then waits for its V pages
+    const int attn_need = attn_pages(kn_T, D, p.page_bytes);
+    if (attn_need > 4 || p.num_pages < std::max(3, attn_need))
         return set_error(MK_ERR_UNSUPPORTED, "shared memory too small for the page pool");
     p.smem_bytes = fixed + p.num_pages * p.page_bytes;
 
@@ -1014,7 +1015,7 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     int kn_lm = tgt->rows_lm > 0 ? tgt->rows_lm : pow2_floor(clampi(tile_g / (2 * H), 1, rcap));
     int kn_T = tgt->attn_split > 0 ? tgt->attn_split : clampi(16384 / (2 * D), 16, 256);
     if (tgt->attn_split <= 0) {
-        // long caches: double the split length (up to 256 positions) while the
+        // long caches: double the split length (up to 512 positions) while the
         // attention tasks outnumber the workers -- a second round of tasks costs
         // a whole per-task latency, a longer split only its extra positions
         auto attn_tasks = [&](int T) {
@@ -1022,14 +1023,14 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
             for (int b = 0; b < B; ++b) n += ceil_div(s->seq_len0[b] + s->max_steps, T);
             return n * Hkv;
         };
-        while (2 * kn_T <= 256 && attn_tasks(kn_T) > (int64_t)num_workers) kn_T *= 2;
+        while (2 * kn_T <= 512 && attn_tasks(kn_T) > (int64_t)num_workers) kn_T *= 2;
     }
     p.rows_qkv = kn_qkv; p.rows_o = kn_o; p.rows_up = kn_up; p.rows_down = kn_dn; p.kchunk_down = kn_kc;
     p.rows_lm = kn_lm; p.attn_split = kn_T;
     const int rows_group = (G + 2) * D;
     if (D % kn_qkv) return set_error(MK_ERR_UNSUPPORTED, "rows_qkv must divide head_dim");
     if (F % kn_up || F % kn_kc || kn_kc % 8) return set_error(MK_ERR_UNSUPPORTED, "rows_up / kchunk_down must divide ffn");
-    if (kn_T > 256 || kn_T < 1) return set_error(MK_ERR_UNSUPPORTED, "attn_split must be 1..256");
+    if (kn_T > 512 || kn_T < 1) return set_error(MK_ERR_UNSUPPORTED, "attn_split must be 1..512");
     for (int K : {H, Hq * D, kn_kc})
         if (B * ceil_div(K, 2048) > 8 || K > 8192)
             return set_error(MK_ERR_UNSUPPORTED, "batch x K too large for register-held activations");
@@ -1134,9 +1135,9 @@ int plan_llama(const mk_model_desc *m, const mk_step_desc *s, const mk_target_de
     };
     // GEMV tiles release each page before waiting for the next, so any number
     // of pages streams through the ring; an attention task holds all its K
-    // pages, then all its V pages
-    int need = 2 * pages_for(kn_T, 2 * D);
-    if (p.num_pages < std::max(2, need))
+    // pages (at most 4), releases them, then waits for its V pages
+    int need = pages_for(kn_T, 2 * D);
+    if (need > 4 || p.num_pages < std::max(2, need))
         return set_error(MK_ERR_UNSUPPORTED, "shared memory too small for the page pool");
 
     // ---- op list (topological): embed, per layer qkv attn o up down, lm

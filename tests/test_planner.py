@@ -196,7 +196,8 @@ def test_planner_matches_oracle_qwen3_8b_b1():
 @pytest.mark.parametrize("name,shape,B,steps,want", [
     ("llama1b_b1", synth.LLAMA_1B, 1, 128, 128),   # 1152 positions / 128 = 9 splits x 8 kv heads = 72 tasks
     ("qwen3_8b_b1", synth.QWEN3_8B, 1, 32, 128),   # 2080 / 64 = 33 x 8 = 264 > 152; / 128 = 17 x 8 = 136
-    ("llama1b_b8", synth.LLAMA_1B, 8, 64, 256),    # thousands of tasks: capped at 256 positions
+    ("llama1b_b8", synth.LLAMA_1B, 8, 64, 512),    # thousands of tasks: capped at 512 positions
+    ("qwen3_8b_b16", synth.QWEN3_8B, 16, 32, 512), # 16 x 2080 / 256 = 9 x 16 x 8 = 1152 tasks: capped at 512
     ("tiny", synth.TINY, 1, 8, 128),               # 72 positions: one split per kv head
 ])
 def test_attention_split_doubles_while_tasks_outnumber_workers(name, shape, B, steps, want):
@@ -205,7 +206,7 @@ def test_attention_split_doubles_while_tasks_outnumber_workers(name, shape, B, s
     T = p.info()["attn_split"]
     assert T == want
     tasks = sum(-(-(s + steps) // T) for s in seq0) * shape.Hkv
-    assert T == 256 or tasks <= GB300["num_sms"]
+    assert T == 512 or tasks <= GB300["num_sms"]
     if T > 16384 // (2 * shape.D):  # doubled: the half split gave more tasks than workers
         assert sum(-(-(s + steps) // (T // 2)) for s in seq0) * shape.Hkv > GB300["num_sms"]
 
