@@ -375,12 +375,15 @@ def run_mk(args, w, rank, world, dist):
     alg = info["algorithmic_bytes_step"]
     avg_launch_s = float(np.mean(step_ms)) / 1e3
     achieved = alg / avg_launch_s / 1e9
-    # per launch of `spl` steps: every step streams the whole model, so the
-    # one-step ncu traffic scales with the steps a launch runs
+    # per timed launch (its mean number of steps: at most `spl` each): every
+    # step streams the whole model, so the one-step ncu traffic scales with
+    # the steps a launch runs
     traffic = profiled_traffic(w.name)
+    per_launch = args.steps / len(timed)
+    per_launch = int(per_launch) if float(per_launch).is_integer() else per_launch
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic * spl if traffic is not None else None, "peak_kind": peak_kind,
-                "algorithmic_bytes_per_launch": alg * spl, "steps_per_launch": spl,
+                "traffic": traffic * per_launch if traffic is not None else None, "peak_kind": peak_kind,
+                "algorithmic_bytes_per_launch": alg * per_launch, "steps_per_launch": per_launch,
                 "algorithmic_bytes_per_step": alg, "traffic_per_step": traffic,
                 "kernel": "mk_interp", "nominal_8tbs_frac": achieved / 8000.0}
     cpu = None
@@ -597,8 +600,9 @@ def main():
     ap.add_argument("--knob", action="append", default=[], help="planner knob, e.g. attn_split=512")
     ap.add_argument("--trace-out", default="",
                     help="after the bench line, run one traced step and write its timeline (JSON) here")
-    ap.add_argument("--steps-per-launch", type=int, default=16,
-                    help="decode steps per cooperative launch in the timed region (1: one launch per step)")
+    ap.add_argument("--steps-per-launch", type=int, default=128,
+                    help="decode steps per cooperative launch in the timed region, at most (1: one launch per "
+                         "step; the default covers a whole 128-step decode)")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N decoder layers (a small case for profiling, not a bench line)")
     args = ap.parse_args()
