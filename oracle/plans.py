@@ -228,7 +228,7 @@ def tc_knobs(shape: LlamaShape, B: int, seq0: Sequence[int], max_steps: int, n_w
     """Tile knobs of a tensor-core plan, from the stated rules: a K split is
     the largest power of two up to 8 that keeps the op's tasks within the
     workers with whole 128-column stages; the MLP-down K chunk is the largest
-    of 2048, 1024, 512, 256 dividing the ffn that gives at least half as many
+    of 1024, 512, 256 dividing the ffn that gives at least half as many
     tasks as workers (else the smallest that divides); the attention split is
     16384 / (2 head_dim) positions, doubled up to 512 while the attention
     tasks outnumber the workers."""
@@ -241,7 +241,7 @@ def tc_knobs(shape: LlamaShape, B: int, seq0: Sequence[int], max_steps: int, n_w
         return k
 
     kc = 0
-    for c in (2048, 1024, 512, 256):
+    for c in (1024, 512, 256):
         if shape.F % c == 0:
             kc = c
             if (shape.H // TC_M) * (shape.F // c) * 2 >= n_workers:

@@ -693,12 +693,13 @@ static int plan_llama_tc(const mk_model_desc *m, const mk_step_desc *s, const mk
     };
     const int ks_qkv = ksplit(Hkv * rows_group / TC_M, H, 0), ks_o = ksplit(H / TC_M, Hq * D, 0);
     if (H % (ks_qkv * TC_KS) || (Hq * D) % (ks_o * TC_KS)) return set_error(MK_ERR_UNSUPPORTED, "bad K split");
-    // MLP-down K chunk: the largest of 2048 .. 256 dividing ffn that still
-    // gives at least half as many tasks as workers
+    // MLP-down K chunk: the largest of 1024 .. 256 dividing ffn that still
+    // gives at least half as many tasks as workers (a 2048-wide chunk makes
+    // MLP-down wait on larger pieces of MLP-up: slower at batch 16)
     int kc = tgt->kchunk_down;
     if (kc <= 0) {
         kc = 0;
-        for (int c : {2048, 1024, 512, 256})
+        for (int c : {1024, 512, 256})
             if (F % c == 0) {
                 if (!kc) kc = c;
                 if ((int64_t)(H / TC_M) * (F / c) * 2 >= num_workers) { kc = c; break; }

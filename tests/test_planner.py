@@ -149,7 +149,7 @@ def test_tc_planner_matches_oracle_qwen3_8b_b16():
     w = synth.WORKLOADS["qwen3_8b_b16"]
     p, op = _compare_tc(synth.QWEN3_8B, 16, synth.seq_lengths(w), w.steps)
     info = p.info()
-    assert (info["ksplit_qkv"], info["ksplit_o"], info["kchunk_down"]) == (2, 4, 2048)
+    assert (info["ksplit_qkv"], info["ksplit_o"], info["kchunk_down"]) == (2, 4, 1024)
 
 
 def test_tc_planner_matches_oracle_llama1b_b8():
