@@ -61,6 +61,14 @@ def launch_chunks(first, n, spl):
     return [(first + i, min(spl, n - i)) for i in range(0, n, spl)]
 
 
+def steps_per_launch(chunks):
+    """Mean decode steps of the timed launches (an int when they are all equal):
+    the factor between the per-step and the per-launch byte figures."""
+    total = sum(k for _, k in chunks)
+    m = total / len(chunks)
+    return int(m) if float(m).is_integer() else m
+
+
 def profiled_traffic(workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
@@ -379,8 +387,7 @@ def run_mk(args, w, rank, world, dist):
     # step streams the whole model, so the one-step ncu traffic scales with
     # the steps a launch runs
     traffic = profiled_traffic(w.name)
-    per_launch = args.steps / len(timed)
-    per_launch = int(per_launch) if float(per_launch).is_integer() else per_launch
+    per_launch = steps_per_launch(timed)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic * per_launch if traffic is not None else None, "peak_kind": peak_kind,
                 "algorithmic_bytes_per_launch": alg * per_launch, "steps_per_launch": per_launch,

@@ -49,3 +49,14 @@ def test_launch_chunks_cover_every_step_once():
         assert steps == list(range(first, first + n))
         assert all(1 <= k <= spl for _, k in ch)
         assert len(ch) == -(-n // spl)
+
+
+def test_per_launch_bytes_follow_the_steps_each_launch_runs():
+    """The roofline's per-launch figures scale the per-step bytes by the steps a
+    timed launch actually runs, which the launch length only bounds."""
+    import bench
+    assert bench.steps_per_launch(bench.launch_chunks(5, 20, 128)) == 20    # one launch of every timed step
+    assert bench.steps_per_launch(bench.launch_chunks(5, 128, 128)) == 128
+    assert bench.steps_per_launch(bench.launch_chunks(0, 32, 16)) == 16
+    assert bench.steps_per_launch(bench.launch_chunks(0, 100, 16)) == 100 / 7  # six of 16 and one of 4
+    assert bench.steps_per_launch(bench.launch_chunks(0, 7, 1)) == 1
