@@ -338,7 +338,7 @@ def run_mk(args, w, rank, world, dist):
     def chunks(first, n):
         return launch_chunks(first, n, spl)
 
-    # warm-up, in the same launch shape as the timed steps
+    # warm-up: launches of up to `spl` steps, like the timed ones
     with torch.cuda.stream(stream):
         for st, k in chunks(0, args.warmup):
             sess.run(st, k, one_launch=k > 1)
