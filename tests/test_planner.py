@@ -481,3 +481,23 @@ def test_attention_pools_need_a_batch():
     with pytest.raises(rt.MkError) as e:
         rt.Plan.llama(synth.LLAMA_1B, 1, [100], 3, 110, attn_pool=1, num_sms=152, smem_per_cta=232448)
     assert e.value.code == rt.MK_ERR_UNSUPPORTED
+
+
+def test_attention_split_needs_its_k_pages_in_the_ring():
+    """A task holds its K pages (at most 4), releases them, then waits for its
+    V pages: 512 positions of head_dim 128 fit 32 KB pages (4 of K) and 64 KB
+    pages (2), and the planner refuses a split whose K would take more than 4
+    pages even where the pool has room for them."""
+    p = rt.Plan.llama(synth.QWEN3_8B, 16, [2048] * 16, 2, 2060, attn_split=512, **GB300)
+    info = p.info()
+    assert info["attn_split"] == 512 and info["page_bytes"] == 32768 and info["num_pages"] >= 4
+    p = rt.Plan.llama(synth.QWEN3_8B, 1, [2048], 2, 2060, attn_split=512, **GB300)
+    assert p.info()["attn_split"] == 512 and p.info()["page_bytes"] == 65536
+    p = rt.Plan.llama(synth.QWEN3_8B, 1, [2048], 2, 2060, attn_split=256, page_bytes=16384, **GB300)
+    assert p.info()["num_pages"] >= 8  # 4 pages of K at 16 KB
+    with pytest.raises(rt.MkError) as e:  # 8 pages of K
+        rt.Plan.llama(synth.QWEN3_8B, 1, [2048], 2, 2060, attn_split=512, page_bytes=16384, **GB300)
+    assert e.value.code == rt.MK_ERR_UNSUPPORTED and "page pool" in rt.load().mk_last_error().decode()
+    with pytest.raises(rt.MkError) as e:
+        rt.Plan.llama(synth.QWEN3_8B, 16, [2048] * 16, 2, 2060, attn_split=1024, **GB300)
+    assert e.value.code == rt.MK_ERR_UNSUPPORTED
